@@ -1,0 +1,174 @@
+"""CPU oracle for the MoE expert layer (test infrastructure only).
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may
+import this package.  The CUDA library never imports, links or calls it, and it never
+imports the CUDA library.
+
+* ``moe_oracle.cpp`` (built into ``liboracle.so``): the fp64 reference of the layer
+  (routing, permutation, scaled-SwiGLU expert FFN, combine, MXFP8 codec).
+* ``brute.py``: a second, independent numpy brute force (all experts evaluated densely,
+  top-k by a full stable sort, quantiser by nearest-code search) used to pin the C++
+  oracle on tiny inputs.
+
+Functions of this module are thin ctypes marshalling around the C++ oracle.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+DT = {"f32": 0, "bf16": 1, "e4m3": 2, "f64": 3}
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with g++ (OpenMP)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp]
+        subprocess.check_call(cmd)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i64, i32 = ctypes.c_int64, ctypes.c_int
+        lib.oracle_version.restype = i32
+        lib.oracle_e4m3_decode.argtypes = [P, i64, P]
+        lib.oracle_e4m3_encode.argtypes = [P, i64, P]
+        lib.oracle_mx_quantize.argtypes = [P, i32, i64, i64, i64, P, P, i32]
+        lib.oracle_mx_quantize.restype = i32
+        lib.oracle_route_topk.argtypes = [P, i64, i32, i32, P, P]
+        lib.oracle_route_topk.restype = i32
+        lib.oracle_permute.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P]
+        lib.oracle_permute.restype = i32
+        lib.oracle_moe_forward.argtypes = [P, i32, P, i64, i32, i32, i32, i32, i32, i32, i32, P, P, P,
+                                           P, P, P, i32, P, i64, P, i32]
+        lib.oracle_moe_forward.restype = i32
+        lib.oracle_down_proj_mx.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, P, P, i32]
+        lib.oracle_down_proj_mx.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def threads() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+# ----------------------------------------------------------------------------- codec
+def e4m3_decode(codes) -> np.ndarray:
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_e4m3_decode(_p(c), c.size, _p(out))
+    return out
+
+
+def e4m3_encode(v) -> np.ndarray:
+    a = _c(v, np.float64)
+    out = np.empty(a.shape, np.uint8)
+    _load().oracle_e4m3_encode(_p(a), a.size, _p(out))
+    return out
+
+
+def mx_quantize(a, dtype: str, shape3) -> tuple[np.ndarray, np.ndarray]:
+    """MXFP8-quantise ``a`` viewed as [n_outer, K, n_inner] in 32-blocks along K.
+
+    Returns (codes with a's shape, scales [n_outer, K/32, n_inner]) as uint8.
+    """
+    n_outer, K, n_inner = shape3
+    src = _c(a, {"f32": np.float32, "bf16": np.uint16, "f64": np.float64}[dtype])
+    assert src.size == n_outer * K * n_inner
+    codes = np.empty(src.shape, np.uint8)
+    scales = np.empty((n_outer, K // 32, n_inner), np.uint8)
+    st = _load().oracle_mx_quantize(_p(src), DT[dtype], n_outer, K, n_inner, _p(codes), _p(scales), threads())
+    if st != 0:
+        raise ValueError("oracle_mx_quantize: K must be a multiple of 32")
+    return codes, scales
+
+
+# ----------------------------------------------------------------------------- layer
+def route_topk(logits, k: int):
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    ids = np.empty((T, k), np.int32)
+    probs = np.empty((T, k), np.float64)
+    st = _load().oracle_route_topk(_p(lg), T, E, k, _p(ids), _p(probs))
+    if st != 0:
+        raise ValueError(f"oracle_route_topk status {st}")
+    return ids, probs
+
+
+def permute(ids, e0: int, E_loc: int) -> dict:
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    counts = np.empty(E_loc, np.int32)
+    offsets = np.empty(E_loc + 1, np.int32)
+    cap = T * k
+    row_src = np.full(cap, -1, np.int32)
+    row_slot = np.full(cap, -1, np.int32)
+    p2r = np.empty((T, k), np.int32)
+    _load().oracle_permute(_p(ids), T, k, e0, E_loc, _p(counts), _p(offsets), _p(row_src), _p(row_slot), _p(p2r))
+    N = int(offsets[-1])
+    return dict(counts=counts, offsets=offsets, row_src_token=row_src[:N], row_slot=row_slot[:N], pair_to_row=p2r, N=N)
+
+
+def moe_forward(x, x_dtype: str, logits, d: int, f: int, E: int, k: int, e0: int, E_loc: int,
+                W_gate, W_up, W_down, w_dtype: str, w_scales=(None, None, None), mx_act: bool = False,
+                tokens=None, nthreads: int | None = None) -> np.ndarray:
+    """fp64 layer output for ``tokens`` (default: all) -> [n_tokens, d].
+
+    x: [T, d] f32 or bf16 bits; logits [T, E] fp32; weights in user layout
+    (W_gate/W_up [E_loc, d, f], W_down [E_loc, f, d]) as f32, bf16 bits, or E4M3 codes
+    with E8M0 scales ``w_scales`` ([E_loc, d/32, f], [E_loc, d/32, f], [E_loc, f/32, d]).
+    """
+    npdt = {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8}
+    x = _c(x, npdt[x_dtype])
+    lg = _c(logits, np.float32)
+    T = x.shape[0]
+    tok = np.arange(T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
+    wg, wu, wd = (_c(w, npdt[w_dtype]) for w in (W_gate, W_up, W_down))
+    sg, su, sd = ((None if s is None else _c(s, np.uint8)) for s in w_scales)
+    y = np.empty((tok.size, d), np.float64)
+    st = _load().oracle_moe_forward(_p(x), DT[x_dtype], _p(lg), T, d, f, E, k, e0, E_loc, DT[w_dtype],
+                                    _p(wg), _p(wu), _p(wd), _p(sg), _p(su), _p(sd), int(mx_act),
+                                    _p(tok), tok.size, _p(y), nthreads or threads())
+    if st != 0:
+        raise ValueError(f"oracle_moe_forward status {st}")
+    return y
+
+
+def down_proj_mx(h_codes, h_scales, row_expert, d: int, f: int, E_loc: int, W_down, w_dtype: str,
+                 Wd_scale=None) -> np.ndarray:
+    """fp64 h W_down for given MXFP8 h rows (diagnostic)."""
+    npdt = {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8}
+    hc = _c(h_codes, np.uint8)
+    hs = _c(h_scales, np.uint8)
+    re = _c(row_expert, np.int32)
+    wd = _c(W_down, npdt[w_dtype])
+    sd = None if Wd_scale is None else _c(Wd_scale, np.uint8)
+    out = np.empty((re.size, d), np.float64)
+    st = _load().oracle_down_proj_mx(_p(hc), _p(hs), _p(re), re.size, d, f, E_loc, DT[w_dtype], _p(wd), _p(sd),
+                                     _p(out), threads())
+    if st != 0:
+        raise ValueError(f"oracle_down_proj_mx status {st}")
+    return out

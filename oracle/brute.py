@@ -1,0 +1,115 @@
+"""Independent numpy brute force of the MoE expert layer (test infrastructure only).
+
+It pins the C++ oracle on tiny inputs.  It shares no code with it and takes different
+routes to the same definitions:
+
+* top-k by a full stable sort on the key (-logit, id) with ``np.lexsort`` (the C++ side
+  uses a partial sort with a comparator);
+* every local expert's FFN is evaluated densely for every token with matrix products, and
+  the routing probability multiplies the expert output after the down projection (the
+  C++ side applies it to h; the two agree in exact arithmetic, and in fp64 to ~1e-15);
+* the E4M3 quantiser is a nearest-code search over a table decoded from the format's
+  bit fields, ties going to the code with an even mantissa (the C++ side rounds the
+  scaled value arithmetically).  In MXFP8 mode the probability is applied before h is
+  quantised, as the layer's fused epilogue does.
+
+Sources: "Wide-EP ... (NVIDIA)" explainer, section "MoE basics" (router picks experts per
+token, chosen experts' results are summed); "Efficient MoE training for biological
+foundation models", sections "GroupedLinear Optimizes Expert Computation" (ScaledSwiGLU)
+and "MXFP8 Precision Reduces Memory Footprint" (one scale per 32 consecutive values).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _e4m3_table() -> np.ndarray:
+    """Values of the 126 non-negative finite codes 0x00..0x7E from the bit fields."""
+    vals = []
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        vals.append((m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return np.array(vals, np.float64)
+
+
+_TABLE = _e4m3_table()
+
+
+def e4m3_nearest(v: np.ndarray) -> np.ndarray:
+    """Codes of v by nearest search; ties to the even-mantissa code; |v| >= 448 -> 448."""
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), 448.0).reshape(-1)
+    dist = np.abs(a[:, None] - _TABLE[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    # among the (at most two) nearest codes prefer the one with an even code (even mantissa)
+    even = cand & ((np.arange(0x7F) % 2) == 0)[None, :]
+    pick = np.where(even.any(axis=1), even.argmax(axis=1), cand.argmax(axis=1))
+    codes = pick.astype(np.uint8)
+    codes = np.where(np.signbit(v.reshape(-1)), codes | np.uint8(0x80), codes)
+    return codes.reshape(v.shape).astype(np.uint8)
+
+
+def e4m3_value(codes: np.ndarray) -> np.ndarray:
+    c = np.asarray(codes, np.uint8)
+    mag = _TABLE[np.minimum(c & 0x7F, 0x7E)]
+    return np.where(c & 0x80, -mag, mag)
+
+
+def mx_quantize_rows(v: np.ndarray):
+    """Quantise the last axis of v in blocks of 32; returns (codes, scale codes, dequantised)."""
+    v = np.asarray(v, np.float64)
+    *lead, K = v.shape
+    b = v.reshape(*lead, K // 32, 32)
+    amax = np.abs(b).max(axis=-1)
+    _, ex = np.frexp(amax)  # amax = m 2^ex, m in [0.5, 1)
+    X = np.where(amax == 0, 0, np.clip(ex - 1 - 8, -127, 127)).astype(np.int64)
+    scaled = b * np.exp2(-X.astype(np.float64))[..., None]
+    codes = e4m3_nearest(scaled)
+    deq = e4m3_value(codes) * np.exp2(X.astype(np.float64))[..., None]
+    return codes.reshape(v.shape), (X + 127).astype(np.uint8), deq.reshape(v.shape)
+
+
+def topk(logits_row: np.ndarray, k: int):
+    lg = np.asarray(logits_row, np.float64)
+    order = np.lexsort((np.arange(lg.size), -lg))
+    ids = order[:k]
+    sel = lg[ids]
+    w = np.exp(sel - sel.max())
+    return ids, w / w.sum()
+
+
+def silu(a):
+    return a / (1.0 + np.exp(-a))
+
+
+def forward(x, logits, Wg, Wu, Wd, k: int, e0: int, mx: bool = False) -> np.ndarray:
+    """y [T, d] (fp64).  x [T,d], logits [T,E], Wg/Wu [E_loc,d,f], Wd [E_loc,f,d] (fp64 values).
+
+    In ``mx`` mode the weights must already be the dequantised MXFP8 values; x rows and h
+    rows are quantised here.
+    """
+    x = np.asarray(x, np.float64)
+    T, d = x.shape
+    E_loc = Wg.shape[0]
+    if mx:
+        x = mx_quantize_rows(x)[2]
+    y = np.zeros((T, d))
+    for t in range(T):
+        ids, p = topk(logits[t], k)
+        g = np.einsum("c,ecn->en", x[t], Wg)       # all local experts, densely
+        u = np.einsum("c,ecn->en", x[t], Wu)
+        act = silu(g) * u                           # [E_loc, f]
+        if not mx:
+            out = np.einsum("en,enm->em", act, Wd)  # every expert's FFN output
+            for j in range(k):
+                e = ids[j] - e0
+                if 0 <= e < E_loc:
+                    y[t] += p[j] * out[e]
+        else:
+            for j in range(k):
+                e = ids[j] - e0
+                if 0 <= e < E_loc:
+                    h = mx_quantize_rows(p[j] * act[e])[2]
+                    y[t] += h @ Wd[e]
+    return y
