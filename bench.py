@@ -1,0 +1,463 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE expert-layer forward pass on B300.
+
+One step = the whole hot path on one batch of seeded synthetic input already resident in
+HBM: route -> permute -> grouped GEMM1 + scaled SwiGLU -> grouped GEMM2 -> combine, each a
+call through the C ABI (libmoe.so), with CUDA events between the calls so that every
+kernel's duration is measured live inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  ``value`` = tokens/s of the whole job (all ranks).  Under
+torchrun (N > 1) every rank runs an independent replica on its own token batch (the layer
+shards by tokens with no exchange), time = max over ranks.
+
+``--impl reference`` times the CPU oracle (fp64, OpenMP on the host cores) on a bounded
+sample of tokens of the same workload instead; it is a deliberately slow baseline.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synthetic import WORKLOADS, gen_logits, gen_weights, gen_x  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; grouped-GEMM TFLOP/s as % of B300 BF16/MXFP8 peak"
+DEFAULT_WORKLOAD = "bf16_e64"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh), "measured"
+    except OSError:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_inputs(w):
+    import oracle
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    if w.dtype == "mxfp8":
+        cg, sg = oracle.mx_quantize(Wg, "bf16", (w.E_loc, w.d, w.f))
+        cu, su = oracle.mx_quantize(Wu, "bf16", (w.E_loc, w.d, w.f))
+        cd, sd = oracle.mx_quantize(Wd, "bf16", (w.E_loc, w.f, w.d))
+        wts = (cg, cu, cd, "e4m3", (sg, su, sd))
+    else:
+        wts = (Wg, Wu, Wd, w.act_dtype, (None, None, None))
+    return x, lg, wts
+
+
+def oracle_time(w, x, lg, wts, tokens, threads):
+    import oracle
+    Wg, Wu, Wd, wdt, scales = wts
+    t0 = time.perf_counter()
+    oracle.moe_forward(x, w.act_dtype, lg, w.d, w.f, w.E, w.k, w.e0, w.E_loc, Wg, Wu, Wd, wdt, scales,
+                       mx_act=(w.dtype == "mxfp8"), tokens=tokens, nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def calibrate_sample(w, x, lg, wts, threads, budget_s):
+    """Number of tokens whose oracle run takes about budget_s (tokens drawn round-robin)."""
+    n = max(threads, 8)
+    rng = np.random.default_rng(123)
+    order = rng.permutation(w.T)
+    while True:
+        dt = oracle_time(w, x, lg, wts, np.sort(order[:n]), threads)
+        if dt > budget_s / 4 or n >= w.T:
+            break
+        n = min(w.T, n * 4)
+    n = int(min(w.T, max(1, n * budget_s / max(dt, 1e-6))))
+    return np.sort(order[:n])
+
+
+def cpu_baseline(w, budget_s):
+    threads = host_cores()
+    x, lg, wts = oracle_inputs(w)
+    tok = calibrate_sample(w, x, lg, wts, threads, budget_s)
+    dt = oracle_time(w, x, lg, wts, tok, threads)
+    return {"value": tok.size / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{tok.size} of {w.T} tokens of {w.name} (seeded uniform sample), fp64 C++ oracle, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    threads = host_cores()
+    x, lg, wts = oracle_inputs(w)
+    per_step = max(1.0, 150.0 / (args.steps + args.warmup))
+    tok = calibrate_sample(w, x, lg, wts, threads, per_step)
+    for _ in range(args.warmup):
+        oracle_time(w, x, lg, wts, tok, threads)
+    times = [oracle_time(w, x, lg, wts, tok, threads) for _ in range(args.steps)]
+    total = sum(times)
+    value = tok.size * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{tok.size} of {w.T} tokens per step (seeded sample), fp64 C++ oracle"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.perf_counter(), ln.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.perf_counter())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0, t1 = getattr(self, "t_begin", 0.0), getattr(self, "t_end", 1e30) + 0.05
+        for ts, ln in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            try:
+                power.append(float(parts[2]))
+            except ValueError:
+                pass
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- ours
+def workload_config(w):
+    wbytes = 3 * w.d * w.f * w.E_loc * (4 if w.dtype == "f32" else 2 if w.dtype == "bf16" else 1)
+    return {"workload": w.name, "T": w.T, "d": w.d, "f": w.f, "E": w.E, "k": w.k, "e0": w.e0, "E_loc": w.E_loc,
+            "bias": list(w.bias) if w.bias else None, "seed": w.seed,
+            "l2": ("inputs larger than L2 (local expert weights %.0f MB)" % (wbytes / 1e6)) if wbytes > L2_BYTES
+            else "L2 flushed between timed steps (256 MB write)",
+            "parallelism": "token-sharded replicas (no exchange)"}
+
+
+def src_hash(path):
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu capture, if the kernel source is unchanged."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(kernel, {}).get(workload)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "mixture_experts_layer_103_b300", "csrc", ent["source"])
+    if not os.path.exists(src) or src_hash(src) != ent["source_sha"]:
+        return None
+    return ent["dram_bytes_per_launch"]
+
+
+def to_dev(a):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(a).cuda()
+
+
+def layer_bytes_flops(w, N, nonempty, n_tok_local):
+    """Algorithmic FLOPs and bytes of the layer and of each grouped GEMM for one step."""
+    wb = 4 if w.dtype == "f32" else 2 if w.dtype == "bf16" else 1 + 1 / 32
+    ab = 4 if w.dtype == "f32" else 2          # x / y element bytes
+    pb = 4 if w.dtype == "f32" else 2 if w.dtype == "bf16" else 1 + 1 / 32  # permuted x and h
+    out = {
+        "layer_flops": 6.0 * N * w.d * w.f,
+        "layer_bytes": 3.0 * w.d * w.f * wb * nonempty + n_tok_local * w.d * ab + w.T * w.d * ab + w.T * w.E * 4,
+        "gemm1_flops": 4.0 * N * w.d * w.f,
+        "gemm1_bytes": 2.0 * w.d * w.f * wb * nonempty + N * w.d * pb + N * w.f * pb,
+        "gemm2_flops": 2.0 * N * w.d * w.f,
+        "gemm2_bytes": 1.0 * w.d * w.f * wb * nonempty + N * w.f * pb + N * w.d * 2,
+    }
+    return out
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import mixture_experts_layer_103_b300 as moe
+
+    pk, pk_kind = peaks()
+    wr = w.replace(seed=w.seed + rank)  # each rank its own token batch; same expert weights
+    x, lg = gen_x(wr), gen_logits(wr)
+    Wg, Wu, Wd = gen_weights(w)
+    xd, lgd = to_dev(x), to_dev(lg)
+    wg_d, wu_d, wd_d = to_dev(Wg), to_dev(Wu), to_dev(Wd)
+    pw = moe.moe_pack_weights(wg_d, wu_d, wd_d, w.dtype)
+    torch.cuda.synchronize()
+    del wg_d, wu_d, wd_d, Wg, Wu, Wd
+    torch.cuda.empty_cache()
+
+    T, d, k, E_loc, e0 = w.T, w.d, w.k, w.E_loc, w.e0
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    probs = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    P = moe.alloc_permute(T, d, k, E_loc, xd.dtype, w.dtype)
+    ws_perm = moe.workspace(moe.moe_permute_workspace_size(T, k, E_loc))
+    h, hs = moe.alloc_h(moe.n_cap(T, k, E_loc), pw)
+    Y2 = torch.empty(moe.n_cap(T, k, E_loc), d, dtype=moe.torch_dtype(w.dtype), device="cuda")
+    y = torch.empty(T, d, dtype=moe.torch_dtype(w.dtype), device="cuda")
+    ws_g = moe.workspace(256)
+    wbytes = 3 * w.d * w.f * w.E_loc * (4 if w.dtype == "f32" else 2 if w.dtype == "bf16" else 1)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if wbytes <= L2_BYTES else None
+
+    names = ["route_topk", "permute", "gemm1_swiglu", "gemm2", "combine"]
+    n_ev = len(names) + 1
+
+    def step(evs):
+        evs[0].record()
+        moe.moe_route_topk(lgd, k, ids, probs)
+        evs[1].record()
+        moe.moe_permute(xd, ids, probs, e0, E_loc, w.dtype, ws=ws_perm, out=P)
+        evs[2].record()
+        moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, h=h,
+                                    h_scale=hs, ws=ws_g)
+        evs[3].record()
+        moe.moe_expert_gemm2(h, hs, P["offsets"], pw, Y2=Y2, ws=ws_g)
+        evs[4].record()
+        moe.moe_unpermute_combine(Y2, P["pair_to_row"], w.dtype, y=y)
+        evs[5].record()
+
+    warm = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step(warm)
+    torch.cuda.synchronize()
+    err = moe.moe_get_device_error(ws_g)
+    if err != 0:
+        raise RuntimeError(f"device error {err} during warm-up")
+    offs = P["offsets"].cpu().numpy().astype(np.int64)
+    N = int(offs[-1])
+    nonempty = int((np.diff(offs) > 0).sum())
+    p2r = P["pair_to_row"].cpu().numpy()
+    n_tok_local = int((p2r >= 0).any(axis=1).sum())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    region0, region1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if rank == 0:
+        clocks.start()
+    clocks.mark("t_begin")
+    region0.record()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        step(evs[i])
+    region1.record()
+    torch.cuda.synchronize()
+    clocks.mark("t_end")
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    err = moe.moe_get_device_error(ws_g)
+    if err != 0:
+        raise RuntimeError(f"device error {err} in the timed region")
+
+    step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps)]
+    kern_ms = {nm: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+               for j, nm in enumerate(names)}
+    total_ms = sum(step_ms)
+    region_ms = region0.elapsed_time(region1)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = T * world / (ms_per_step / 1e3)
+
+    # ---- roofline of the dominant kernel and of the whole layer
+    bf = layer_bytes_flops(w, N, nonempty, n_tok_local)
+    hbm = pk["hbm_gbs"]
+    tpeak = pk["bf16_tflops"] * (2.0 if w.dtype == "mxfp8" else 1.0)
+    dom = max(("gemm1_swiglu", "gemm2"), key=lambda n: kern_ms[n])
+    key = "gemm1" if dom == "gemm1_swiglu" else "gemm2"
+    fl, by = bf[key + "_flops"], bf[key + "_bytes"]
+    t_s = kern_ms[dom] / 1e3
+    tensor_bound = (fl / (tpeak * 1e12)) >= (by / (hbm * 1e9))
+    if w.dtype == "f32":
+        roof = {"bound": "alu", "achieved": fl / t_s / 1e12, "peak": None, "unit": "TFLOP/s", "frac": None}
+    elif tensor_bound:
+        roof = {"bound": "tensor", "achieved": fl / t_s / 1e12, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": fl / t_s / 1e12 / tpeak}
+    else:
+        roof = {"bound": "hbm", "achieved": by / t_s / 1e9, "peak": hbm, "unit": "GB/s",
+                "frac": by / t_s / 1e9 / hbm}
+    kname = "tc_grouped_gemm_kernel" if w.dtype != "f32" else "simt_grouped_gemm_kernel"
+    roof.update({"kernel": f"{kname} ({dom})", "traffic": recorded_traffic(dom, w.name),
+                 "peak_kind": pk_kind + (" (bf16 x2 nominal fp8 ratio)" if w.dtype == "mxfp8" else "")})
+    t_roof = max(bf["layer_flops"] / (tpeak * 1e12), bf["layer_bytes"] / (hbm * 1e9))
+    gemm_s = (kern_ms["gemm1_swiglu"] + kern_ms["gemm2"]) / 1e3
+    layer = {"roofline_us": t_roof * 1e6, "measured_us": ms_per_step * 1e3, "frac": t_roof / (ms_per_step / 1e3),
+             "algorithmic_bytes": bf["layer_bytes"], "flops": bf["layer_flops"], "N_pairs": N,
+             "nonempty_experts": nonempty, "tokens_with_local_expert": n_tok_local,
+             "grouped_gemm_tflops": bf["layer_flops"] / gemm_s / 1e12,
+             "grouped_gemm_pct_of_peak": 100 * bf["layer_flops"] / gemm_s / 1e12 / tpeak}
+
+    # ---- end to end through moe_layer_forward with host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        x_pin = torch.empty(xd.shape, dtype=xd.dtype).pin_memory()
+        x_pin.copy_(xd.cpu())
+        lg_pin = torch.empty(lgd.shape, dtype=lgd.dtype).pin_memory()
+        lg_pin.copy_(lgd.cpu())
+        y_pin = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        xd2, lgd2, yd2 = torch.empty_like(xd), torch.empty_like(lgd), torch.empty_like(y)
+        ws_layer = moe.workspace(moe.moe_layer_workspace_size(T, d, w.f, w.E, k, E_loc, w.dtype))
+
+        def e2e_step():
+            xd2.copy_(x_pin, non_blocking=True)
+            lgd2.copy_(lg_pin, non_blocking=True)
+            moe.moe_layer_forward(xd2, lgd2, w.E, k, e0, pw, y=yd2, ws=ws_layer)
+            y_pin.copy_(yd2, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n2 = args.e2e_steps or max(3, args.steps // 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n2):
+            if flush is not None:
+                flush.zero_()
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_error(ws_layer) == 0
+        ms = a.elapsed_time(b) / n2
+        e2e = {"value": T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+               "h2d_bytes_per_step": int(x_pin.numel() * x_pin.element_size() + lg_pin.numel() * 4),
+               "d2h_bytes_per_step": int(y_pin.numel() * y_pin.element_size()), "steps": n2,
+               "entry_point": "moe_layer_forward"}
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    launches_per_step = 8
+    cpu = None if args.no_cpu_baseline else cpu_baseline(w, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "mxfp8": "e4m3+e8m0 (mxfp8)"}[w.dtype],
+        "data": "synthetic (seeded; shapes of the pages' workloads)", "config": workload_config(w),
+        "roofline": roof, "layer": layer, "kernels_us": {n: 1e3 * v for n, v in kern_ms.items()},
+        "timed_region_ms": region_ms, "e2e": e2e, "cpu_baseline": cpu,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

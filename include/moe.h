@@ -1,0 +1,223 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) MoE expert-layer library (libmoe.so).
+ *
+ * The library runs the forward pass of a Mixture-of-Experts expert layer on the experts
+ * one GPU holds: top-k routing over router logits, a stable permute of token rows into
+ * expert-contiguous order, a grouped GEMM1 (gate and up projections) with the scaled
+ * SwiGLU fused into its epilogue, a grouped GEMM2 (down projection), and the combine
+ * back to token order.
+ *
+ * Sources for the operations (page titles of the source material):
+ *   [WEP]  "Wide-EP ... MoE ... NVIDIA" explainer, section "MoE basics": a router picks,
+ *          per token, the experts it uses (DeepSeek-R1: 256 experts, 8 chosen); only those
+ *          experts compute and their results are summed.  Section "Wide-EP": under EP8
+ *          one GPU holds 32 experts per layer, under EP64 it holds 4.  Section
+ *          "Prerequisite: fast GPU-to-GPU links": dispatch sends each token to its
+ *          experts, combine brings the results back (on one GPU: permute / unpermute).
+ *   [BIO]  "Efficient MoE training for biological foundation models" (BioNeMo), section
+ *          "GroupedLinear Optimizes Expert Computation": per-expert matrices submitted as
+ *          one grouped operation; GroupedLinear -> ScaledSwiGLU -> GroupedLinear fused
+ *          with no intermediate materialised; ScaledSwiGLU applies the routing
+ *          probabilities ("scales") inside the activation.  Section "MXFP8 Precision
+ *          Reduces Memory Footprint": 8-bit values with one scale per block of 32
+ *          consecutive values, run on Blackwell tensor-core instructions, with
+ *          quantisation, SwiGLU and routing-weight scaling fused in one kernel.
+ *
+ * Common conventions
+ *   - Every pointer argument named *device* below is a CUDA device pointer owned by the
+ *     caller; the library never allocates, never frees and keeps no state between calls
+ *     (scratch lives in the caller's workspace).  Calls are re-entrant.
+ *   - Every call is asynchronous on the given stream and never synchronises the host,
+ *     except moe_get_device_error().  Arguments are validated on the host before any
+ *     launch; the first failed check returns an error and launches nothing.  A failed
+ *     launch returns MOE_ERR_CUDA.
+ *   - Matrices are dense, row-major and contiguous.  "bf16" means IEEE bfloat16 bits.
+ *   - Device-detected errors (a bounded wait in a kernel that gave up) are written to
+ *     the first 4 bytes of the workspace; read them with moe_get_device_error().
+ *   - Only compute capability 10.3 (B300, sm_103a) is supported; there is no CPU path.
+ */
+#ifndef MOE_B300_MOE_H_
+#define MOE_B300_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef int32_t moe_status;
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1 /* null pointer, out-of-range size, k > E, ...            */
+#define MOE_ERR_UNSUPPORTED 2 /* dtype / shape / device the kernels do not handle      */
+#define MOE_ERR_WORKSPACE 3   /* workspace pointer NULL, misaligned or too small        */
+#define MOE_ERR_CUDA 4        /* a CUDA runtime call or a kernel launch failed          */
+#define MOE_ERR_TIMEOUT 5     /* a bounded device-side wait gave up (device error word) */
+
+typedef int32_t moe_dtype;
+#define MOE_F32 0   /* fp32 inputs and outputs; expert GEMMs in fp32 FMA                  */
+#define MOE_BF16 1  /* bf16 inputs/weights/outputs; tcgen05 bf16 MMA, fp32 accumulate   */
+#define MOE_MXFP8 2 /* E4M3 values + E8M0 scale per 32 along K; tcgen05 block-scaled MMA */
+
+/* MXFP8 quantisation rule (both for x, the weights and the intermediate h): blocks of 32
+ * consecutive values along the contraction dimension K; amax = max |v| over the block;
+ * shared exponent X = floor(log2(amax)) - 8, clamped to [-127, 127] (X = 0 for an
+ * all-zero block); scale byte = X + 127 (E8M0); element = E4M3 (OCP "E4M3FN": bias 7,
+ * max 448, no infinities) of v * 2^-X, round to nearest even, saturating to +-448. */
+
+/* Layout of MXFP8 scale factors ("SF tile layout").  A matrix with rows grouped in tiles
+ * of 128 rows and K a multiple of 128 stores its scales in 512-byte atoms, one per
+ * (row tile, 128-wide K group): inside an atom the scale of row i (0..127 within the
+ * tile) and K block kk (0..3 within the group) sits at byte (i % 32) * 16 + (i / 32) * 4
+ * + kk.  Rows of a tile past the end of its segment hold unspecified bytes.
+ *   - activations (perm_x, h): row tiles are the per-expert m-tiles: expert e's segment
+ *     [offsets[e], offsets[e+1]) is cut into ceil(count_e / 128) tiles, numbered
+ *     globally in expert order (tile base of expert e = sum over e' < e of
+ *     ceil(count_e' / 128)); atom (tile, g) is at byte (tile * (K / 128) + g) * 512.
+ *     Capacity: moe_mx_act_scale_bytes().
+ *   - packed weights: row tiles are 128 consecutive packed output rows of one expert;
+ *     atom (e, g, n_tile) is at byte ((e * (K / 128) + g) * (rows / 128) + n_tile) * 512. */
+
+/* Packed weight layout (output of moe_pack_weights, input of the grouped GEMMs).
+ *   Wgu_packed [E_loc, 2f, d]  K-major (row = one output column of GEMM1, contiguous
+ *              over d).  Gate and up columns are interleaved in blocks of G =
+ *              moe_gu_block(f) columns: packed rows [2G*b, 2G*b + G) are gate columns
+ *              [G*b, G*b + G) and packed rows [2G*b + G, 2G*b + 2G) are the up columns
+ *              of the same range.
+ *   Wd_packed  [E_loc, d, f]   K-major (row = one output column of GEMM2, contiguous over f).
+ *   Element type: fp32 (MOE_F32), bf16 (MOE_BF16) or E4M3 bytes (MOE_MXFP8, with the
+ *   scales in Wgu_scale / Wd_scale in the SF tile layout, see above). */
+int moe_gu_block(int f);
+
+/* Route (step 1) [WEP "MoE basics"].
+ * For each token t, the k experts with the largest logits logits[t, :], in descending
+ * order; equal logits go to the lower expert id (+0.0 and -0.0 are equal); then
+ * topk_probs[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k chosen logits.
+ *   logits     device fp32 [T, E]    (NaN logits: unspecified result; +-inf order normally)
+ *   topk_ids   device int32 [T, k]   out
+ *   topk_probs device fp32  [T, k]   out
+ * Requires 1 <= k <= E <= 1024 and k <= 32, T >= 0.  T == 0 launches nothing. */
+moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_probs,
+                          moe_stream_t stream);
+
+/* Permute (step 2) [WEP "Prerequisite ...": dispatch, here as a local permute].
+ * Local experts are the ids [e0, e0 + E_loc); pairs (t, j) whose expert is not local are
+ * skipped.  counts[e] = number of pairs routed to local expert e0+e; offsets = exclusive
+ * prefix sum of counts (offsets[E_loc] = N, the number of local pairs).  Row offsets[e]+r
+ * of the permuted buffers holds the r-th token, in ascending token order, that chose
+ * expert e0+e: row_src_token[row] = t, row_prob[row] = topk_probs[t, j],
+ * pair_to_row[t, j] = row (or -1 if not local), perm_x[row, :] = x[t, :].  The result is
+ * deterministic (no atomics decide a position).
+ *   x            device [T, d]  x_dtype MOE_F32 or MOE_BF16
+ *   perm_dtype   element type of perm_x: MOE_F32 (x fp32), MOE_BF16 (x bf16) or MOE_MXFP8
+ *                (x bf16; rows quantised while copied, scales to perm_x_scale)
+ *   perm_x       device [N_cap, d], N_cap = T * min(k, E_loc); rows >= N untouched
+ *   perm_x_scale device, MOE_MXFP8 only (else NULL): SF tile layout, K = d,
+ *                moe_mx_act_scale_bytes(N_cap, d, E_loc) bytes
+ *   counts [E_loc], offsets [E_loc+1], row_src_token [N_cap], row_prob [N_cap] (fp32),
+ *   pair_to_row [T, k]: device int32 outputs
+ *   workspace    device, >= moe_permute_workspace_size(T, k, E_loc) bytes, 256-aligned
+ * Requires 0 <= e0, 1 <= E_loc, e0 + E_loc <= 65536, 1 <= k <= 32; d % 8 == 0 (bf16),
+ * d % 4 == 0 (fp32), d % 128 == 0 (MXFP8). */
+moe_status moe_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d,
+                       const int32_t* topk_ids, const float* topk_probs, int k, int e0, int E_loc,
+                       void* perm_x, uint8_t* perm_x_scale, int32_t* counts, int32_t* offsets,
+                       int32_t* row_src_token, float* row_prob, int32_t* pair_to_row, void* workspace,
+                       size_t workspace_bytes, moe_stream_t stream);
+size_t moe_permute_workspace_size(int T, int k, int E_loc);
+
+/* Bytes of an activation scale buffer in the SF tile layout for N_cap rows, K columns. */
+size_t moe_mx_act_scale_bytes(int64_t N_cap, int K, int E_loc);
+
+/* Pack weights (one-off, untimed) [BIO "GroupedLinear ..."].
+ * From the user layout W_gate, W_up [E_loc, d, f] and W_down [E_loc, f, d] (src_dtype
+ * MOE_F32 or MOE_BF16) to the packed layout above in dst_dtype: MOE_F32 (src fp32),
+ * MOE_BF16 (src bf16) or MOE_MXFP8 (src bf16 or fp32; quantised per output column in
+ * blocks of 32 along K, scales to Wgu_scale / Wd_scale, sizes moe_mx_weight_scale_bytes).
+ * All pointers device.  MXFP8 requires d % 128 == 0 and f % 128 == 0. */
+moe_status moe_pack_weights(const void* W_gate, const void* W_up, const void* W_down, moe_dtype src_dtype,
+                            moe_dtype dst_dtype, int E_loc, int d, int f, void* Wgu_packed, void* Wd_packed,
+                            uint8_t* Wgu_scale, uint8_t* Wd_scale, moe_stream_t stream);
+size_t moe_mx_weight_scale_bytes(int E_loc, int rows, int K);
+
+/* Grouped expert MLP (steps 3-4) [BIO "GroupedLinear ...", "MXFP8 Precision ..."].
+ * For each local expert e and each row i of its segment [offsets[e], offsets[e+1]):
+ *   g = perm_x[i] W_gate_e,  u = perm_x[i] W_up_e          (grouped GEMM1, fp32 accumulate)
+ *   h = row_prob[i] * silu(g) * u,  silu(a) = a / (1 + e^-a)  (fused GEMM1 epilogue; h is
+ *       stored once, as bf16 (MOE_BF16), fp32 (MOE_F32) or MXFP8 codes + scales
+ *       (MOE_MXFP8, quantised in blocks of 32 along f); the 2f-wide pre-activation is never
+ *       stored)
+ *   Y2[i] = h W_down_e                                      (grouped GEMM2, fp32 accumulate)
+ * N = offsets[E_loc] is read on the device; rows [N, N_cap) of Y2 are not written.
+ *   perm_x, perm_x_scale   as produced by moe_permute (perm_x_scale NULL unless MXFP8)
+ *   offsets [E_loc+1], row_prob [N_cap]   device
+ *   Wgu_packed, Wgu_scale, Wd_packed, Wd_scale   packed weights (scales NULL unless MXFP8)
+ *   Y2      device [N_cap, d]: fp32 for MOE_F32, bf16 otherwise
+ *   workspace device >= moe_grouped_mlp_workspace_size(...) bytes, 256-byte aligned
+ * Requires d % 8 == 0 and f % 32 == 0 (bf16); d % 128 == 0 and f % 128 == 0 (MXFP8). */
+moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
+                           const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
+                           const void* Wgu_packed, const uint8_t* Wgu_scale, const void* Wd_packed,
+                           const uint8_t* Wd_scale, void* Y2, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream);
+size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype);
+
+/* The two halves of moe_grouped_mlp, for callers that keep h themselves (same
+ * preconditions; N = offsets[E_loc] on the device).
+ *   moe_expert_gemm1_swiglu: perm_x (+ scales) -> h [N_cap, f] (fp32 / bf16 / E4M3 bytes)
+ *       and, for MOE_MXFP8, h_scale in the SF tile layout with K = f
+ *       (moe_mx_act_scale_bytes(N_cap, f, E_loc) bytes) [BIO "GroupedLinear ...":
+ *       GroupedLinear + ScaledSwiGLU (+ quantisation) in one kernel].
+ *   moe_expert_gemm2: h (+ h_scale) -> Y2 [N_cap, d] (fp32 for MOE_F32, else bf16)
+ *       [BIO: the second GroupedLinear].
+ *   workspace: >= moe_expert_gemm_workspace_size() bytes, 256-byte aligned (error word). */
+moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
+                                   const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
+                                   const void* Wgu_packed, const uint8_t* Wgu_scale, void* h, uint8_t* h_scale,
+                                   void* workspace, size_t workspace_bytes, moe_stream_t stream);
+moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t* offsets, int64_t N_cap, int E_loc,
+                            int d, int f, moe_dtype dtype, const void* Wd_packed, const uint8_t* Wd_scale, void* Y2,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream);
+size_t moe_expert_gemm_workspace_size(void);
+
+/* Unpermute + combine (step 5) [WEP "MoE basics": results of the chosen experts are
+ * summed; "Prerequisite ...": combine].
+ * y[t] = sum over j = 0..k-1 with pair_to_row[t, j] >= 0 of Y2[pair_to_row[t, j]], summed
+ * in slot order in fp32 and rounded once; tokens with no local expert get a zero row.
+ * (The routing probability was already applied inside the SwiGLU.)
+ *   Y2 device [N_cap, d] (fp32 if dtype == MOE_F32, else bf16); pair_to_row device [T, k];
+ *   y  device [T, d] (fp32 if dtype == MOE_F32, else bf16), fully written.
+ * Requires d % 8 == 0 (bf16) / d % 4 == 0 (fp32). */
+moe_status moe_unpermute_combine(const void* Y2, const int32_t* pair_to_row, int T, int k, int d,
+                                 moe_dtype dtype, void* y, moe_stream_t stream);
+
+/* Whole layer (steps 1-5 in one call) on the local experts [e0, e0 + E_loc).
+ *   x [T, d] (fp32 for MOE_F32, else bf16), logits [T, E] fp32, packed weights as above,
+ *   y [T, d] (fp32 for MOE_F32, else bf16): device pointers.
+ *   workspace device >= moe_layer_workspace_size(...) bytes, 256-byte aligned; it holds
+ *   the routing table, the permutation, the permuted rows, h and Y2. */
+moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0,
+                             int E_loc, moe_dtype dtype, const void* Wgu_packed, const uint8_t* Wgu_scale,
+                             const void* Wd_packed, const uint8_t* Wd_scale, void* y, void* workspace,
+                             size_t workspace_bytes, moe_stream_t stream);
+size_t moe_layer_workspace_size(int T, int d, int f, int E, int k, int E_loc, moe_dtype dtype);
+
+/* Synchronises `stream`, then reads and clears the device error word at the start of
+ * `workspace`.  Writes MOE_OK or the error code a kernel stored (MOE_ERR_TIMEOUT) to
+ * *device_error.  Returns MOE_ERR_CUDA if the synchronisation fails. */
+moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* device_error);
+
+/* 1 if the current CUDA device is compute capability 10.3 (sm_103a), else 0. */
+int moe_supported(void);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_MOE_H_ */

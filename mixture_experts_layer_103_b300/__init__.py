@@ -1,0 +1,277 @@
+"""B300 (sm_103a) MoE expert layer: Python binding of libmoe.so.
+
+Thin ctypes marshalling over the C ABI declared in ``include/moe.h``: every function
+here has the same name as the C entry point it calls, passes raw device pointers and the
+current torch CUDA stream, and raises :class:`MoeError` on a non-zero status.  torch is
+used only to allocate device memory and to name the stream; every step of the layer runs
+in the library's CUDA kernels.  There is no fallback: importing this package fails if
+``libmoe.so`` has not been built (``python -m mixture_experts_layer_103_b300.build``).
+
+The layer (sources: "Wide-EP ... NVIDIA" explainer, section "MoE basics"; "Efficient MoE
+training for biological foundation models", sections "GroupedLinear Optimizes Expert
+Computation" and "MXFP8 Precision Reduces Memory Footprint"): route each token to its
+top-k experts, permute token rows into expert-contiguous order, grouped GEMM1 with the
+scaled SwiGLU fused into its epilogue, grouped GEMM2, and combine back to token order.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_F32, MOE_BF16, MOE_MXFP8 = 0, 1, 2
+DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "mxfp8": MOE_MXFP8}
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+        self.status = status
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m mixture_experts_layer_103_b300.build`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+_SIGS = {
+    "moe_gu_block": (_I, [_I]),
+    "moe_route_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_permute": (_I, [_P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
+    "moe_mx_act_scale_bytes": (_SZ, [_I64, _I, _I]),
+    "moe_pack_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_mx_weight_scale_bytes": (_SZ, [_I, _I, _I]),
+    "moe_grouped_mlp": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_mlp_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
+    "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_gemm_workspace_size": (_SZ, []),
+    "moe_unpermute_combine": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_layer_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_layer_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_get_device_error": (_I, [_P, _P, _P]),
+    "moe_supported": (_I, []),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+def lib():
+    return _lib
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise MoeError(fn, st)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dt(dtype) -> int:
+    return DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+
+
+def torch_dtype(dtype) -> torch.dtype:
+    """Storage dtype of activations/outputs for a layer dtype."""
+    return torch.float32 if _dt(dtype) == MOE_F32 else torch.bfloat16
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A caller-owned device workspace (torch allocations are 256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def n_cap(T: int, k: int, E_loc: int) -> int:
+    return T * min(k, E_loc)
+
+
+# ----------------------------------------------------------------------------- entry points
+def moe_supported() -> bool:
+    return bool(_lib.moe_supported())
+
+
+def moe_route_topk(logits: torch.Tensor, k: int, topk_ids=None, topk_probs=None):
+    T, E = logits.shape
+    ids = topk_ids if topk_ids is not None else torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    probs = topk_probs if topk_probs is not None else torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    _check("moe_route_topk", _lib.moe_route_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(probs), _stream()))
+    return ids, probs
+
+
+def alloc_permute(T: int, d: int, k: int, E_loc: int, x_dtype: torch.dtype, perm_dtype="bf16", device="cuda") -> dict:
+    """Output buffers of moe_permute."""
+    cap = n_cap(T, k, E_loc)
+    if _dt(perm_dtype) == MOE_MXFP8:
+        perm_x = torch.empty(cap, d, dtype=torch.uint8, device=device)
+        perm_sf = torch.empty(max(1, _lib.moe_mx_act_scale_bytes(cap, d, E_loc)), dtype=torch.uint8, device=device)
+    else:
+        perm_x = torch.empty(cap, d, dtype=x_dtype, device=device)
+        perm_sf = None
+    return dict(perm_x=perm_x, perm_x_scale=perm_sf,
+                counts=torch.empty(E_loc, dtype=torch.int32, device=device),
+                offsets=torch.empty(E_loc + 1, dtype=torch.int32, device=device),
+                row_src_token=torch.empty(cap, dtype=torch.int32, device=device),
+                row_prob=torch.empty(cap, dtype=torch.float32, device=device),
+                pair_to_row=torch.empty(T, k, dtype=torch.int32, device=device))
+
+
+def moe_permute(x: torch.Tensor, topk_ids: torch.Tensor, topk_probs: torch.Tensor, e0: int, E_loc: int,
+                perm_dtype="bf16", ws=None, out=None) -> dict:
+    T, d = x.shape
+    k = topk_ids.shape[1]
+    x_dt = MOE_F32 if x.dtype == torch.float32 else MOE_BF16
+    out = out if out is not None else alloc_permute(T, d, k, E_loc, x.dtype, perm_dtype, x.device)
+    nb = _lib.moe_permute_workspace_size(T, k, E_loc)
+    ws = ws if ws is not None else workspace(nb, x.device)
+    _check("moe_permute", _lib.moe_permute(
+        _ptr(x), x_dt, _dt(perm_dtype), T, d, _ptr(topk_ids), _ptr(topk_probs), k, e0, E_loc, _ptr(out["perm_x"]),
+        _ptr(out["perm_x_scale"]), _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["row_src_token"]),
+        _ptr(out["row_prob"]), _ptr(out["pair_to_row"]), _ptr(ws), ws.numel(), _stream()))
+    return out
+
+
+def moe_permute_workspace_size(T: int, k: int, E_loc: int) -> int:
+    return int(_lib.moe_permute_workspace_size(T, k, E_loc))
+
+
+@dataclasses.dataclass
+class PackedWeights:
+    dtype: int
+    E_loc: int
+    d: int
+    f: int
+    Wgu: torch.Tensor
+    Wd: torch.Tensor
+    Wgu_scale: torch.Tensor | None = None
+    Wd_scale: torch.Tensor | None = None
+
+
+def moe_pack_weights(W_gate: torch.Tensor, W_up: torch.Tensor, W_down: torch.Tensor, dtype="bf16") -> PackedWeights:
+    E_loc, d, f = W_gate.shape
+    dev = W_gate.device
+    src = MOE_F32 if W_gate.dtype == torch.float32 else MOE_BF16
+    dst = _dt(dtype)
+    if dst == MOE_MXFP8:
+        Wgu = torch.empty(E_loc, 2 * f, d, dtype=torch.uint8, device=dev)
+        Wd = torch.empty(E_loc, d, f, dtype=torch.uint8, device=dev)
+        sg = torch.empty(_lib.moe_mx_weight_scale_bytes(E_loc, 2 * f, d), dtype=torch.uint8, device=dev)
+        sd = torch.empty(_lib.moe_mx_weight_scale_bytes(E_loc, d, f), dtype=torch.uint8, device=dev)
+    else:
+        tdt = torch.float32 if dst == MOE_F32 else torch.bfloat16
+        Wgu = torch.empty(E_loc, 2 * f, d, dtype=tdt, device=dev)
+        Wd = torch.empty(E_loc, d, f, dtype=tdt, device=dev)
+        sg = sd = None
+    _check("moe_pack_weights", _lib.moe_pack_weights(
+        _ptr(W_gate), _ptr(W_up), _ptr(W_down), src, dst, E_loc, d, f, _ptr(Wgu), _ptr(Wd), _ptr(sg), _ptr(sd),
+        _stream()))
+    return PackedWeights(dst, E_loc, d, f, Wgu, Wd, sg, sd)
+
+
+def moe_grouped_mlp(perm_x, perm_x_scale, offsets, row_prob, pw: PackedWeights, Y2=None, ws=None):
+    cap = perm_x.shape[0]
+    dev = perm_x.device
+    Y2 = Y2 if Y2 is not None else torch.empty(cap, pw.d, dtype=torch_dtype(pw.dtype), device=dev)
+    nb = _lib.moe_grouped_mlp_workspace_size(cap, pw.E_loc, pw.d, pw.f, pw.dtype)
+    ws = ws if ws is not None else workspace(nb, dev)
+    _check("moe_grouped_mlp", _lib.moe_grouped_mlp(
+        _ptr(perm_x), _ptr(perm_x_scale), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f, pw.dtype,
+        _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(pw.Wd), _ptr(pw.Wd_scale), _ptr(Y2), _ptr(ws), ws.numel(), _stream()))
+    return Y2, ws
+
+
+def alloc_h(N_cap: int, pw: PackedWeights, device="cuda"):
+    """h buffer (+ its MXFP8 scales) for moe_expert_gemm1_swiglu."""
+    if pw.dtype == MOE_MXFP8:
+        return (torch.empty(N_cap, pw.f, dtype=torch.uint8, device=device),
+                torch.empty(max(1, _lib.moe_mx_act_scale_bytes(N_cap, pw.f, pw.E_loc)), dtype=torch.uint8,
+                            device=device))
+    return torch.empty(N_cap, pw.f, dtype=torch_dtype(pw.dtype), device=device), None
+
+
+def moe_expert_gemm1_swiglu(perm_x, perm_x_scale, offsets, row_prob, pw: PackedWeights, h=None, h_scale=None,
+                            ws=None):
+    cap = perm_x.shape[0]
+    if h is None:
+        h, h_scale = alloc_h(cap, pw, perm_x.device)
+    ws = ws if ws is not None else workspace(_lib.moe_expert_gemm_workspace_size(), perm_x.device)
+    _check("moe_expert_gemm1_swiglu", _lib.moe_expert_gemm1_swiglu(
+        _ptr(perm_x), _ptr(perm_x_scale), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f, pw.dtype,
+        _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(h), _ptr(h_scale), _ptr(ws), ws.numel(), _stream()))
+    return h, h_scale, ws
+
+
+def moe_expert_gemm2(h, h_scale, offsets, pw: PackedWeights, Y2=None, ws=None):
+    cap = h.shape[0]
+    Y2 = Y2 if Y2 is not None else torch.empty(cap, pw.d, dtype=torch_dtype(pw.dtype), device=h.device)
+    ws = ws if ws is not None else workspace(_lib.moe_expert_gemm_workspace_size(), h.device)
+    _check("moe_expert_gemm2", _lib.moe_expert_gemm2(
+        _ptr(h), _ptr(h_scale), _ptr(offsets), cap, pw.E_loc, pw.d, pw.f, pw.dtype, _ptr(pw.Wd), _ptr(pw.Wd_scale),
+        _ptr(Y2), _ptr(ws), ws.numel(), _stream()))
+    return Y2, ws
+
+
+def moe_unpermute_combine(Y2, pair_to_row, dtype, y=None):
+    T, k = pair_to_row.shape
+    d = Y2.shape[1]
+    y = y if y is not None else torch.empty(T, d, dtype=torch_dtype(dtype), device=Y2.device)
+    _check("moe_unpermute_combine", _lib.moe_unpermute_combine(_ptr(Y2), _ptr(pair_to_row), T, k, d, _dt(dtype),
+                                                               _ptr(y), _stream()))
+    return y
+
+
+def moe_layer_workspace_size(T, d, f, E, k, E_loc, dtype) -> int:
+    return int(_lib.moe_layer_workspace_size(T, d, f, E, k, E_loc, _dt(dtype)))
+
+
+def moe_layer_forward(x, logits, E: int, k: int, e0: int, pw: PackedWeights, y=None, ws=None):
+    T, d = x.shape
+    y = y if y is not None else torch.empty(T, d, dtype=torch_dtype(pw.dtype), device=x.device)
+    nb = moe_layer_workspace_size(T, d, pw.f, E, k, pw.E_loc, pw.dtype)
+    ws = ws if ws is not None else workspace(nb, x.device)
+    _check("moe_layer_forward", _lib.moe_layer_forward(
+        _ptr(x), _ptr(logits), T, d, pw.f, E, k, e0, pw.E_loc, pw.dtype, _ptr(pw.Wgu), _ptr(pw.Wgu_scale),
+        _ptr(pw.Wd), _ptr(pw.Wd_scale), _ptr(y), _ptr(ws), ws.numel(), _stream()))
+    return y, ws
+
+
+def moe_get_device_error(ws: torch.Tensor) -> int:
+    code = ctypes.c_int32(0)
+    _check("moe_get_device_error", _lib.moe_get_device_error(_ptr(ws), _stream(), ctypes.byref(code)))
+    return code.value
+
+
+class MoELayer:
+    """The expert layer on one GPU's experts [e0, e0 + E_loc): packed weights + workspace."""
+
+    def __init__(self, W_gate, W_up, W_down, E: int, k: int, e0: int = 0, dtype="bf16"):
+        self.E, self.k, self.e0 = E, k, e0
+        self.weights = moe_pack_weights(W_gate, W_up, W_down, dtype)
+        self._ws = None
+
+    def __call__(self, x, logits, y=None):
+        T, d = x.shape
+        nb = moe_layer_workspace_size(T, d, self.weights.f, self.E, self.k, self.weights.E_loc, self.weights.dtype)
+        if self._ws is None or self._ws.numel() < nb:
+            self._ws = workspace(nb, x.device)
+        y, _ = moe_layer_forward(x, logits, self.E, self.k, self.e0, self.weights, y=y, ws=self._ws)
+        return y
+
+    def device_error(self) -> int:
+        return 0 if self._ws is None else moe_get_device_error(self._ws)

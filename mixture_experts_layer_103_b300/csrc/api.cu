@@ -1,0 +1,385 @@
+// C ABI of the MoE expert-layer library: argument validation, workspace layout and the
+// launch sequence of each entry point (declared and documented in include/moe.h).
+#include <cstring>
+#include <mutex>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs, cudaStream_t st);
+cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d, const int32_t* ids,
+                           const float* probs, int k, int e0, int E_loc, void* perm_x, uint8_t* perm_sf,
+                           int32_t* counts, int32_t* offsets, int32_t* row_src_token, float* row_prob,
+                           int32_t* pair_to_row, uint8_t* ws, cudaStream_t st);
+size_t permute_ws_bytes(int T, int E_loc);
+cudaError_t launch_combine(const void* Y2, const int32_t* p2r, int T, int k, int d, moe_dtype dtype, void* y,
+                           cudaStream_t st);
+cudaError_t launch_simt_gemm1(const float* perm_x, const int32_t* offsets, const float* row_prob, int64_t N_cap,
+                              int E_loc, int d, int f, const float* Wgu, float* h, cudaStream_t st);
+cudaError_t launch_simt_gemm2(const float* h, const int32_t* offsets, int64_t N_cap, int E_loc, int d, int f,
+                              const float* Wd, float* Y2, cudaStream_t st);
+cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
+                            int64_t N_cap, int E_loc, int d, int f, bool mx, const void* Wgu, const uint8_t* Wgu_sf,
+                            void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
+                            int f, bool mx, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
+                            uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
+                        int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
+constexpr int kMaxDevices = 64;
+
+int num_sms() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+int gather_grid(cudaStream_t) { return num_sms() * 6; }
+
+static int elt_bytes(moe_dtype dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+static size_t mx_act_sf_bytes(int64_t n_cap, int K, int E_loc) {
+  return static_cast<size_t>(mx_tiles_cap(n_cap, E_loc)) * (K / 128) * 512;
+}
+
+// ---- grouped MLP scratch: h (+ its scales) -------------------------------------------
+struct MlpScratch {
+  void* h;
+  uint8_t* h_sf;
+};
+static size_t mlp_scratch_bytes(int64_t n_cap, int E_loc, int f, moe_dtype dt) {
+  size_t b = align_up(static_cast<size_t>(n_cap) * f * elt_bytes(dt), kAlign);
+  if (dt == MOE_MXFP8) b += align_up(mx_act_sf_bytes(n_cap, f, E_loc), kAlign);
+  return b;
+}
+static MlpScratch carve_mlp(uint8_t* p, int64_t n_cap, int f, moe_dtype dt) {
+  MlpScratch s;
+  s.h = p;
+  s.h_sf = dt == MOE_MXFP8 ? p + align_up(static_cast<size_t>(n_cap) * f * elt_bytes(dt), kAlign) : nullptr;
+  return s;
+}
+
+static moe_status check_mlp_shape(int d, int f, int E_loc, moe_dtype dt) {
+  if (d <= 0 || f <= 0 || E_loc < 1 || E_loc > 1024) return MOE_ERR_INVALID_ARG;
+  if (f % 32 != 0) return MOE_ERR_UNSUPPORTED;
+  if (dt == MOE_BF16 && d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (dt == MOE_MXFP8 && (d % 128 != 0 || f % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (dt != MOE_F32 && dt != MOE_BF16 && dt != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static cudaError_t run_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets,
+                             const float* row_prob, int64_t n_cap, int E_loc, int d, int f, moe_dtype dt,
+                             const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
+                             cudaStream_t st) {
+  if (n_cap == 0) return cudaSuccess;
+  if (dt == MOE_F32)
+    return launch_simt_gemm1(static_cast<const float*>(perm_x), offsets, row_prob, n_cap, E_loc, d, f,
+                             static_cast<const float*>(Wgu), static_cast<float*>(h), st);
+  return launch_tc_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt == MOE_MXFP8, Wgu, Wgu_sf, h, h_sf,
+                         err, kTimeoutNs, st);
+}
+
+static cudaError_t run_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t n_cap, int E_loc,
+                             int d, int f, moe_dtype dt, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
+                             cudaStream_t st) {
+  if (n_cap == 0) return cudaSuccess;
+  if (dt == MOE_F32)
+    return launch_simt_gemm2(static_cast<const float*>(h), offsets, n_cap, E_loc, d, f, static_cast<const float*>(Wd),
+                             static_cast<float*>(Y2), st);
+  return launch_tc_gemm2(h, h_sf, offsets, n_cap, E_loc, d, f, dt == MOE_MXFP8, Wd, Wd_sf, Y2, err, kTimeoutNs, st);
+}
+
+static cudaError_t run_mlp(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
+                           int64_t n_cap, int E_loc, int d, int f, moe_dtype dt, const void* Wgu, const uint8_t* Wgu_sf,
+                           const void* Wd, const uint8_t* Wd_sf, void* Y2, uint8_t* scratch, int32_t* err,
+                           cudaStream_t st) {
+  MlpScratch s = carve_mlp(scratch, n_cap, f, dt);
+  cudaError_t e = run_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt, Wgu, Wgu_sf, s.h, s.h_sf, err, st);
+  if (e != cudaSuccess) return e;
+  return run_gemm2(s.h, s.h_sf, offsets, n_cap, E_loc, d, f, dt, Wd, Wd_sf, Y2, err, st);
+}
+
+// ---- whole-layer workspace -------------------------------------------------------------
+struct LayerWs {
+  int32_t* err;
+  int32_t* topk_ids;
+  float* topk_probs;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_src_token;
+  float* row_prob;
+  int32_t* pair_to_row;
+  uint8_t* perm_ws;
+  void* perm_x;
+  uint8_t* perm_sf;
+  uint8_t* mlp;
+  void* Y2;
+  size_t total;
+};
+static LayerWs layer_layout(uint8_t* base, int T, int d, int f, int k, int E_loc, moe_dtype dt) {
+  const int64_t n_cap = n_cap_of(T, k, E_loc);
+  LayerWs w{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? base + o : nullptr;
+    o += align_up(bytes, kAlign);
+    return p;
+  };
+  w.err = reinterpret_cast<int32_t*>(take(sizeof(WsHeader)));
+  w.topk_ids = reinterpret_cast<int32_t*>(take(static_cast<size_t>(T) * k * 4));
+  w.topk_probs = reinterpret_cast<float*>(take(static_cast<size_t>(T) * k * 4));
+  w.counts = reinterpret_cast<int32_t*>(take(static_cast<size_t>(E_loc) * 4));
+  w.offsets = reinterpret_cast<int32_t*>(take(static_cast<size_t>(E_loc + 1) * 4));
+  w.row_src_token = reinterpret_cast<int32_t*>(take(static_cast<size_t>(n_cap) * 4));
+  w.row_prob = reinterpret_cast<float*>(take(static_cast<size_t>(n_cap) * 4));
+  w.pair_to_row = reinterpret_cast<int32_t*>(take(static_cast<size_t>(T) * k * 4));
+  w.perm_ws = take(permute_ws_bytes(T, E_loc));
+  w.perm_x = take(static_cast<size_t>(n_cap) * d * elt_bytes(dt));
+  w.perm_sf = dt == MOE_MXFP8 ? take(mx_act_sf_bytes(n_cap, d, E_loc)) : nullptr;
+  w.mlp = take(mlp_scratch_bytes(n_cap, E_loc, f, dt));
+  w.Y2 = take(static_cast<size_t>(n_cap) * d * (dt == MOE_F32 ? 4 : 2));
+  w.total = o;
+  return w;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_gu_block(int f) { return f > 0 && f % 32 == 0 ? 32 : 0; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+int moe_supported(void) {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return 0;
+  return (major == 10 && minor == 3) ? 1 : 0;
+}
+
+size_t moe_mx_act_scale_bytes(int64_t N_cap, int K, int E_loc) {
+  if (N_cap < 0 || K <= 0 || K % 128 != 0 || E_loc < 1) return 0;
+  return mx_act_sf_bytes(N_cap, K, E_loc);
+}
+
+size_t moe_mx_weight_scale_bytes(int E_loc, int rows, int K) {
+  if (E_loc < 1 || rows <= 0 || rows % 128 != 0 || K <= 0 || K % 128 != 0) return 0;
+  return static_cast<size_t>(E_loc) * (rows / 128) * (K / 128) * 512;
+}
+
+moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_probs,
+                          moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !topk_ids || !topk_probs)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_route_topk(logits, T, E, k, topk_ids, topk_probs, stream));
+}
+
+size_t moe_permute_workspace_size(int T, int k, int E_loc) {
+  (void)k;
+  if (T < 0 || E_loc < 1) return 0;
+  return sizeof(WsHeader) + permute_ws_bytes(T, E_loc);
+}
+
+static moe_status check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d, const void* ids,
+                                const void* probs, int k, int e0, int E_loc, const void* perm_x, const void* perm_sf,
+                                const void* counts, const void* offsets, const void* rst, const void* rp,
+                                const void* p2r) {
+  if (T < 0 || d <= 0 || k < 1 || k > 32 || e0 < 0 || E_loc < 1 || E_loc > 1024 || e0 > (1 << 30))
+    return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !ids || !probs || !perm_x || !rst || !rp || !p2r)) return MOE_ERR_INVALID_ARG;
+  const bool ok_types = (x_dtype == MOE_F32 && perm_dtype == MOE_F32) || (x_dtype == MOE_BF16 && perm_dtype == MOE_BF16) ||
+                        ((x_dtype == MOE_BF16 || x_dtype == MOE_F32) && perm_dtype == MOE_MXFP8);
+  if (!ok_types) return MOE_ERR_UNSUPPORTED;
+  if ((x_dtype == MOE_BF16 && d % 8 != 0) || (x_dtype == MOE_F32 && d % 4 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (perm_dtype == MOE_MXFP8 && (d % 128 != 0 || (T > 0 && !perm_sf))) return perm_sf ? MOE_ERR_UNSUPPORTED
+                                                                                          : MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(x) || !aligned16(perm_x))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status moe_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d, const int32_t* topk_ids,
+                       const float* topk_probs, int k, int e0, int E_loc, void* perm_x, uint8_t* perm_x_scale,
+                       int32_t* counts, int32_t* offsets, int32_t* row_src_token, float* row_prob,
+                       int32_t* pair_to_row, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  moe_status s = check_permute(x, x_dtype, perm_dtype, T, d, topk_ids, topk_probs, k, e0, E_loc, perm_x, perm_x_scale,
+                               counts, offsets, row_src_token, row_prob, pair_to_row);
+  if (s != MOE_OK) return s;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < moe_permute_workspace_size(T, k, E_loc))
+    return MOE_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_permute(x, x_dtype, perm_dtype, T, d, topk_ids, topk_probs, k, e0, E_loc, perm_x,
+                                    perm_x_scale, counts, offsets, row_src_token, row_prob, pair_to_row,
+                                    ws + sizeof(WsHeader), stream));
+}
+
+moe_status moe_pack_weights(const void* W_gate, const void* W_up, const void* W_down, moe_dtype src_dtype,
+                            moe_dtype dst_dtype, int E_loc, int d, int f, void* Wgu_packed, void* Wd_packed,
+                            uint8_t* Wgu_scale, uint8_t* Wd_scale, moe_stream_t stream) {
+  if (!W_gate || !W_up || !W_down || !Wgu_packed || !Wd_packed) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_mlp_shape(d, f, E_loc, dst_dtype);
+  if (s != MOE_OK) return s;
+  const bool ok_types = (src_dtype == MOE_F32 && dst_dtype == MOE_F32) ||
+                        (src_dtype == MOE_BF16 && dst_dtype == MOE_BF16) ||
+                        ((src_dtype == MOE_BF16 || src_dtype == MOE_F32) && dst_dtype == MOE_MXFP8);
+  if (!ok_types) return MOE_ERR_UNSUPPORTED;
+  if (dst_dtype == MOE_MXFP8 && (!Wgu_scale || !Wd_scale)) return MOE_ERR_INVALID_ARG;
+  if (dst_dtype == MOE_MXFP8 && (!aligned16(Wgu_packed) || !aligned16(Wd_packed))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack(W_gate, W_up, W_down, src_dtype, dst_dtype, E_loc, d, f, Wgu_packed, Wd_packed,
+                                 Wgu_scale, Wd_scale, stream));
+}
+
+size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype) {
+  (void)d;
+  if (N_cap < 0 || E_loc < 1 || f <= 0) return 0;
+  return sizeof(WsHeader) + mlp_scratch_bytes(N_cap, E_loc, f, dtype);
+}
+
+moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
+                           const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
+                           const void* Wgu_packed, const uint8_t* Wgu_scale, const void* Wd_packed,
+                           const uint8_t* Wd_scale, void* Y2, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream) {
+  moe_status s = check_mlp_shape(d, f, E_loc, dtype);
+  if (s != MOE_OK) return s;
+  if (N_cap < 0 || N_cap > (int64_t(1) << 31) - 1) return MOE_ERR_INVALID_ARG;
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  if (N_cap > 0 && (!perm_x || !row_prob || !Wgu_packed || !Wd_packed || !Y2)) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_MXFP8 && N_cap > 0 && (!perm_x_scale || !Wgu_scale || !Wd_scale)) return MOE_ERR_INVALID_ARG;
+  if (N_cap > 0 && (!aligned16(perm_x) || !aligned16(Wgu_packed) || !aligned16(Wd_packed) || !aligned16(Y2) ||
+                    (perm_x_scale && !aligned16(perm_x_scale)) || (Wgu_scale && !aligned16(Wgu_scale)) ||
+                    (Wd_scale && !aligned16(Wd_scale))))
+    return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < moe_grouped_mlp_workspace_size(N_cap, E_loc, d, f, dtype))
+    return MOE_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(run_mlp(perm_x, perm_x_scale, offsets, row_prob, N_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale,
+                             Wd_packed, Wd_scale, Y2, ws + sizeof(WsHeader), reinterpret_cast<int32_t*>(ws), stream));
+}
+
+size_t moe_expert_gemm_workspace_size(void) { return sizeof(WsHeader); }
+
+static moe_status check_gemm_common(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype, const void* offsets,
+                                    const void* a, const void* a_sf, const void* w, const void* w_sf, const void* out,
+                                    const void* out_sf) {
+  moe_status s = check_mlp_shape(d, f, E_loc, dtype);
+  if (s != MOE_OK) return s;
+  if (N_cap < 0 || N_cap > (int64_t(1) << 31) - 1 || !offsets) return MOE_ERR_INVALID_ARG;
+  if (N_cap == 0) return MOE_OK;
+  if (!a || !w || !out || !aligned16(a) || !aligned16(w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_MXFP8 && (!a_sf || !w_sf || !aligned16(a_sf) || !aligned16(w_sf))) return MOE_ERR_INVALID_ARG;
+  (void)out_sf;
+  return MOE_OK;
+}
+
+moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
+                                   const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
+                                   const void* Wgu_packed, const uint8_t* Wgu_scale, void* h, uint8_t* h_scale,
+                                   void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  moe_status s = check_gemm_common(N_cap, E_loc, d, f, dtype, offsets, perm_x, perm_x_scale, Wgu_packed, Wgu_scale, h,
+                                   h_scale);
+  if (s != MOE_OK) return s;
+  if (N_cap > 0 && (!row_prob || (dtype == MOE_MXFP8 && !h_scale))) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+  int32_t* err = static_cast<int32_t*>(workspace);
+  if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(run_gemm1(perm_x, perm_x_scale, offsets, row_prob, N_cap, E_loc, d, f, dtype, Wgu_packed,
+                               Wgu_scale, h, h_scale, err, stream));
+}
+
+moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t* offsets, int64_t N_cap, int E_loc,
+                            int d, int f, moe_dtype dtype, const void* Wd_packed, const uint8_t* Wd_scale, void* Y2,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  moe_status s = check_gemm_common(N_cap, E_loc, d, f, dtype, offsets, h, h_scale, Wd_packed, Wd_scale, Y2, nullptr);
+  if (s != MOE_OK) return s;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+  int32_t* err = static_cast<int32_t*>(workspace);
+  if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(run_gemm2(h, h_scale, offsets, N_cap, E_loc, d, f, dtype, Wd_packed, Wd_scale, Y2, err, stream));
+}
+
+moe_status moe_unpermute_combine(const void* Y2, const int32_t* pair_to_row, int T, int k, int d, moe_dtype dtype,
+                                 void* y, moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > 32 || d <= 0) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F32 && dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if ((dtype == MOE_F32 && d % 4 != 0) || (dtype != MOE_F32 && d % 8 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && (!Y2 || !pair_to_row || !y || !aligned16(Y2) || !aligned16(y))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(Y2, pair_to_row, T, k, d, dtype, y, stream));
+}
+
+size_t moe_layer_workspace_size(int T, int d, int f, int E, int k, int E_loc, moe_dtype dtype) {
+  if (T < 0 || d <= 0 || f <= 0 || E < 1 || k < 1 || E_loc < 1) return 0;
+  (void)E;
+  return layer_layout(nullptr, T, d, f, k, E_loc, dtype).total;
+}
+
+moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0, int E_loc,
+                             moe_dtype dtype, const void* Wgu_packed, const uint8_t* Wgu_scale, const void* Wd_packed,
+                             const uint8_t* Wd_scale, void* y, void* workspace, size_t workspace_bytes,
+                             moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
+  if (e0 < 0 || E_loc < 1 || e0 + E_loc > E) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_mlp_shape(d, f, E_loc, dtype);
+  if (s != MOE_OK) return s;
+  if (!Wgu_packed || !Wd_packed) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_MXFP8 && (!Wgu_scale || !Wd_scale)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !logits || !y || !aligned16(x) || !aligned16(y))) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(Wgu_packed) || !aligned16(Wd_packed)) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_F32 && d % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  const size_t need = moe_layer_workspace_size(T, d, f, E, k, E_loc, dtype);
+  if (!workspace || !aligned256(workspace) || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+  LayerWs w = layer_layout(static_cast<uint8_t*>(workspace), T, d, f, k, E_loc, dtype);
+  const int64_t n_cap = n_cap_of(T, k, E_loc);
+  const moe_dtype x_dtype = dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
+  cudaError_t e = cudaMemsetAsync(w.err, 0, 4, stream);
+  if (e == cudaSuccess) e = launch_route_topk(logits, T, E, k, w.topk_ids, w.topk_probs, stream);
+  if (e == cudaSuccess)
+    e = launch_permute(x, x_dtype, dtype, T, d, w.topk_ids, w.topk_probs, k, e0, E_loc, w.perm_x, w.perm_sf, w.counts,
+                       w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
+  if (e == cudaSuccess)
+    e = run_mlp(w.perm_x, w.perm_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale,
+                Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, stream);
+  if (e == cudaSuccess) e = launch_combine(w.Y2, w.pair_to_row, T, k, d, dtype, y, stream);
+  return cuda_status(e);
+}
+
+moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* device_error) {
+  if (!workspace || !device_error) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(workspace, 0, 4) != cudaSuccess) return MOE_ERR_CUDA;
+  *device_error = v;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,430 @@
+// Steps 3-4: grouped GEMMs of the expert MLP on the 5th-generation tensor cores.
+//
+// "Efficient MoE training for biological foundation models" (BioNeMo), section
+// "GroupedLinear Optimizes Expert Computation": every expert keeps its own matrices but
+// all experts run as one grouped operation; GroupedLinear -> ScaledSwiGLU -> GroupedLinear
+// is fused so the gate/up pre-activation is never materialised, and ScaledSwiGLU applies
+// the routing probabilities inside the activation.  Section "MXFP8 Precision Reduces
+// Memory Footprint": 8-bit values with one scale per 32 along K on Blackwell tensor-core
+// instructions, with quantisation fused into the same kernel.
+//
+// One persistent kernel per GEMM, one CTA per SM, 6 warps:
+//   warp 0      TMA producer: per pipeline stage one 128 x 128-byte tile of A (the
+//               expert's token rows) and one BN x 128-byte tile of B (the expert's packed
+//               weights), 128-byte swizzled; MXFP8 adds the two scale-factor atoms (plain
+//               bulk copies; the SF tile layout makes each one contiguous)
+//   warp 1      TMEM allocator + MMA issuer (one thread): tcgen05.mma 128 x BN x 16 (bf16)
+//               or block-scaled 128 x BN x 32 (E4M3 x E4M3 with E8M0 scales copied to TMEM
+//               by tcgen05.cp), fp32 accumulators in TMEM, double-buffered when they fit
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one TMEM lane = one row per
+//               thread), then either bf16 store (GEMM2) or the fused scaled SwiGLU
+//               h = p * silu(gate) * up with bf16 or MXFP8 (32 values = one block per
+//               thread) output (GEMM1)
+// The tile scheduler is static: tile t -> (global m-tile t / n_tiles, n-tile t % n_tiles);
+// m-tiles are 128-row slices of each expert's segment [offsets[e], offsets[e+1]),
+// numbered in expert order, so experts with no tokens cost nothing and their weights are
+// never read.  Rows of a tile past its expert's segment are computed and discarded.
+// Every wait is bounded; on a timeout the kernel records MOE_ERR_TIMEOUT in the device
+// error word, drains its own copies and MMAs and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "moe_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+constexpr int kBM = 128;
+constexpr int kRowBytes = 128;  // bytes of one operand row per pipeline stage
+constexpr int kGemmThreads = 192;
+constexpr int kMaxEloc = 1024;
+
+enum { EPI_STORE_BF16 = 0, EPI_SWIGLU_BF16 = 1, EPI_SWIGLU_MX = 2 };
+
+struct GemmArgs {
+  const int32_t* offsets;  // [E_loc + 1]
+  int E_loc;
+  int n_out;               // output columns (GEMM1: packed 2f; GEMM2: d)
+  int K;                   // contraction length in elements
+  void* out;               // bf16 [rows, ld_out] or E4M3 bytes [rows, ld_out]
+  int64_t ld_out;          // elements per output row
+  uint8_t* out_sf;         // EPI_SWIGLU_MX: scales of h (activation SF tile layout, K = n_out / 2)
+  const float* row_prob;   // GEMM1: routing probability per permuted row
+  const uint8_t* a_sf;     // MXFP8: scales of A (activation SF tile layout)
+  const uint8_t* b_sf;     // MXFP8: scales of B (weight SF tile layout)
+  int32_t* err;            // device error word
+  uint64_t timeout_ns;
+};
+
+template <int BN, int STAGES, bool MX>
+struct GemmCfg {
+  static constexpr int A_BYTES = kBM * kRowBytes;
+  static constexpr int B_BYTES = BN * kRowBytes;
+  static constexpr int SFA_BYTES = MX ? 512 : 0;
+  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
+  static constexpr int BK = MX ? 128 : 64;      // K elements per stage
+  static constexpr int UMMA_K = MX ? 32 : 16;   // K elements per MMA
+  static constexpr int NUM_ACC = MX ? 1 : 2;
+  static constexpr int ACC_COLS = NUM_ACC * BN;
+  static constexpr int SF_REGION = MX ? (BN / 128 + 1) * 4 : 0;  // SFA 4 cols + SFB 4 per 128 rows
+  static constexpr int USED_COLS = ACC_COLS + 2 * SF_REGION;
+  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
+                                   : USED_COLS <= 256 ? 256 : 512;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+  static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_TAB = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = OFF_TAB + 2 * (kMaxEloc + 1) * 4 + 1024;  // + alignment slack
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
+  static_assert(!MX || BN % 128 == 0, "MXFP8 tiles cover whole 128-row scale atoms");
+  static_assert(USED_COLS <= 512, "TMEM has 512 columns");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+struct Tile {
+  int e, mt, row0, rows, n0;
+};
+
+template <int BN>
+__device__ __forceinline__ Tile decode_tile(int t, int n_tiles_n, const int* s_off, const int* s_mtp, int E_loc) {
+  const int gm = t / n_tiles_n;
+  int lo = 0, hi = E_loc - 1;  // last expert whose first m-tile is <= gm (skips empty experts)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_mtp[mid] <= gm) lo = mid;
+    else hi = mid - 1;
+  }
+  Tile r;
+  r.e = lo;
+  r.mt = gm;
+  r.row0 = s_off[lo] + (gm - s_mtp[lo]) * kBM;
+  r.rows = min(kBM, s_off[lo + 1] - r.row0);
+  r.n0 = (t - gm * n_tiles_n) * BN;
+  return r;
+}
+
+__device__ __forceinline__ void gemm_abort(const GemmArgs& g, volatile int* s_abort) {
+  *s_abort = 1;
+  set_device_error(g.err, MOE_ERR_TIMEOUT);
+}
+
+template <int BN, int STAGES, bool MX, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const GemmArgs g) {
+  using C = GemmCfg<BN, STAGES, MX>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* s_off = reinterpret_cast<int*>(smem + C::OFF_TAB);
+  int* s_mtp = s_off + g.E_loc + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull_bar(a), 1);
+      ptx::mbar_init(tempty_bar(a), 4);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 2) build_mtile_prefix(g.offsets, g.E_loc, kBM, s_off, s_mtp);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_tiles_n = (g.n_out + BN - 1) / BN;
+  const int total = s_mtp[g.E_loc] * n_tiles_n;
+  const int num_kb = (g.K + C::BK - 1) / C::BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<BN>(t, n_tiles_n, s_off, s_mtp, g.E_loc);
+        const int sfb_bytes = MX ? min(BN, g.n_out - tl.n0) / 128 * 512 : 0;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (*s_abort) { ok = false; break; }
+          if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
+          const uint32_t fb = full_bar(s);
+          ptx::mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + C::SFA_BYTES + sfb_bytes);
+          ptx::tma_load_3d(sbase + C::OFF_A + s * C::A_BYTES, &tmA, fb, kb * C::BK, tl.row0, 0);
+          ptx::tma_load_3d(sbase + C::OFF_B + s * C::B_BYTES, &tmB, fb, kb * C::BK, tl.n0, tl.e);
+          if constexpr (MX) {
+            const int kg = g.K / 128;
+            ptx::bulk_load(sbase + C::OFF_SFA + s * C::SFA_BYTES,
+                           g.a_sf + (static_cast<int64_t>(tl.mt) * kg + kb) * 512, 512, fb);
+            ptx::bulk_load(sbase + C::OFF_SFB + s * C::SFB_BYTES,
+                           g.b_sf + ((static_cast<int64_t>(tl.e) * kg + kb) * (g.n_out / 128) + tl.n0 / 128) * 512,
+                           sfb_bytes, fb);
+          }
+          ++issued;
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {  // let the copies already issued land before the CTA exits
+        for (int64_t i = issued - 1; i >= 0 && i >= issued - STAGES; --i)
+          ptx::mbar_wait(full_bar(static_cast<int>(i % STAGES)), static_cast<uint32_t>((i / STAGES) & 1),
+                         g.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = MX ? ptx::idesc_mxf8(kBM, BN) : ptx::idesc_bf16(kBM, BN);
+      int s = 0;
+      uint32_t ph = 0, kbg = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        const int acc = C::NUM_ACC == 2 ? (it & 1) : 0;
+        const uint32_t acc_ph = C::NUM_ACC == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
+        if (!ptx::mbar_wait(tempty_bar(acc), acc_ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); break; }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait(full_bar(s), ph, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = sbase + C::OFF_A + s * C::A_BYTES;
+          const uint32_t b_addr = sbase + C::OFF_B + s * C::B_BYTES;
+          if constexpr (MX) {
+            const uint32_t sf_col = tmem_base + C::ACC_COLS + (kbg & 1u) * C::SF_REGION;
+            ptx::tmem_cp_32x128b_x4(sf_col, ptx::sdesc_sf(sbase + C::OFF_SFA + s * C::SFA_BYTES));
+#pragma unroll
+            for (int i = 0; i < BN / 128; ++i)
+              ptx::tmem_cp_32x128b_x4(sf_col + 4 + 4 * i,
+                                      ptx::sdesc_sf(sbase + C::OFF_SFB + s * C::SFB_BYTES + i * 512));
+#pragma unroll
+            for (int k = 0; k < C::BK / C::UMMA_K; ++k)
+              ptx::mma_mxf8(d_tmem, ptx::sdesc_sw128(a_addr + k * 32), ptx::sdesc_sw128(b_addr + k * 32),
+                            ptx::idesc_sf_id(idesc, k), sf_col, sf_col + 4, (kb | k) != 0);
+            ++kbg;
+          } else {
+#pragma unroll
+            for (int k = 0; k < C::BK / C::UMMA_K; ++k)
+              ptx::mma_bf16(d_tmem, ptx::sdesc_sw128(a_addr + k * 32), ptx::sdesc_sw128(b_addr + k * 32), idesc,
+                            (kb | k) != 0);
+          }
+          ptx::mma_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::mma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
+      }
+      ptx::mma_commit(drain_bar);  // every MMA issued by this thread has completed
+      ptx::mbar_wait(drain_bar, 0, g.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      if (*s_abort) break;
+      const Tile tl = decode_tile<BN>(t, n_tiles_n, s_off, s_mtp, g.E_loc);
+      const int acc = C::NUM_ACC == 2 ? (it & 1) : 0;
+      const uint32_t acc_ph = C::NUM_ACC == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
+      int okw = 0;
+      if (lane == 0) okw = ptx::mbar_wait(tfull_bar(acc), acc_ph, g.timeout_ns) ? 1 : 0;
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      if (!okw) { if (lane == 0) gemm_abort(g, s_abort); break; }
+      (void)ptx::mbar_try_wait(tfull_bar(acc), acc_ph);  // completed phase: acquire for every lane
+      ptx::tc_fence_after();
+      const int r = q * 32 + lane;
+      const bool valid = r < tl.rows;
+      const int64_t grow = static_cast<int64_t>(tl.row0) + r;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (EPI == EPI_STORE_BF16) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tbase + c, v);
+          ptx::tmem_ld_wait();
+          const int n = tl.n0 + c;
+          if (valid && n < g.n_out) {
+            uint4* dst = reinterpret_cast<uint4*>(out + grow * g.ld_out + n);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (n + 8 * j < g.n_out)
+                dst[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+                                    pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                                    pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                                    pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+          }
+        }
+      } else {
+        const float p = valid ? __ldg(g.row_prob + grow) : 0.0f;
+        const int fdim = g.n_out / 2;
+#pragma unroll 1
+        for (int sb = 0; sb < BN / 64; ++sb) {
+          uint32_t gv[32], uv[32];
+          ptx::tmem_ld32(tbase + sb * 64, gv);       // 32 gate columns
+          ptx::tmem_ld32(tbase + sb * 64 + 32, uv);  // the matching 32 up columns
+          ptx::tmem_ld_wait();
+          const int fc = tl.n0 / 2 + sb * 32;  // first h column of this block
+          float h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float gg = __uint_as_float(gv[i]);
+            h[i] = p * (gg / (1.0f + __expf(-gg))) * __uint_as_float(uv[i]);
+          }
+          if (valid && fc < fdim) {
+            if constexpr (EPI == EPI_SWIGLU_BF16) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g.out) + grow * g.ld_out + fc);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_uint4(pack_bf16x2(h[8 * j + 0], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
+                                    pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
+            } else {
+              float amax = 0.0f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+              const int X = mx_exponent(amax);
+              const float inv = mx_inv_scale(X);
+              uint32_t w[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                w[j] = static_cast<uint32_t>(e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv)) |
+                       (static_cast<uint32_t>(e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv)) << 16);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(g.out) + grow * g.ld_out + fc);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              g.out_sf[sf_act_offset(tl.mt, r, fc, fdim)] = static_cast<uint8_t>(X + 127);
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D K-major operand [outer, rows, K] (outer = 1 for a plain matrix), box [1, box_rows, 128 bytes].
+static bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, uint64_t rows, uint64_t outer,
+                             uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const uint32_t elt = fp8 ? 1 : 2;
+  const cuuint64_t dims[3] = {K, rows, outer};
+  const cuuint64_t strides[2] = {K * elt, rows * K * elt};
+  const cuuint32_t box[3] = {kRowBytes / elt, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms();
+
+template <int BN, int STAGES, bool MX, int EPI>
+static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
+                                    cudaStream_t st) {
+  using C = GemmCfg<BN, STAGES, MX>;
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, A, MX, g.K, a_rows, 1, kBM)) return cudaErrorInvalidValue;
+  if (!make_operand_map(&tb, B, MX, g.K, g.n_out, g.E_loc, BN)) return cudaErrorInvalidValue;
+  auto kern = tc_grouped_gemm_kernel<BN, STAGES, MX, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms(), kGemmThreads, C::SMEM_BYTES, st>>>(ta, tb, g);
+  return cudaGetLastError();
+}
+
+static GemmArgs base_args(const int32_t* offsets, int E_loc, int32_t* err, uint64_t timeout_ns) {
+  GemmArgs g{};
+  g.offsets = offsets;
+  g.E_loc = E_loc;
+  g.err = err;
+  g.timeout_ns = timeout_ns;
+  return g;
+}
+
+// GEMM1 + fused scaled SwiGLU on the tensor cores.
+//   bf16:  perm_x bf16 [N_cap, d] -> h bf16 [N_cap, f]
+//   mxfp8: perm_x E4M3 [N_cap, d] + SF -> h E4M3 [N_cap, f] + SF
+cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
+                            int64_t N_cap, int E_loc, int d, int f, bool mx, const void* Wgu, const uint8_t* Wgu_sf,
+                            void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
+  GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
+  g.n_out = 2 * f;
+  g.K = d;
+  g.out = h;
+  g.ld_out = f;
+  g.out_sf = h_sf;
+  g.row_prob = row_prob;
+  g.a_sf = perm_sf;
+  g.b_sf = Wgu_sf;
+  if (mx) return launch_gemm_inst<256, 4, true, EPI_SWIGLU_MX>(perm_x, N_cap, Wgu, g, st);
+  return launch_gemm_inst<256, 4, false, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
+}
+
+// GEMM2 on the tensor cores: h [N_cap, f] (bf16, or E4M3 + SF) -> Y2 bf16 [N_cap, d].
+cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
+                            int f, bool mx, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
+                            uint64_t timeout_ns, cudaStream_t st) {
+  GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
+  g.n_out = d;
+  g.K = f;
+  g.out = Y2;
+  g.ld_out = d;
+  g.a_sf = h_sf;
+  g.b_sf = Wd_sf;
+  if (mx) return launch_gemm_inst<256, 4, true, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
+  return launch_gemm_inst<256, 4, false, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
+}
+
+}  // namespace moe

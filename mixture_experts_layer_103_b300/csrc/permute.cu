@@ -1,0 +1,291 @@
+// Step 2: stable permute of token rows into expert-contiguous order (the single-GPU
+// analogue of the dispatch step described in the "Wide-EP ... NVIDIA" explainer, section
+// "Prerequisite: fast GPU-to-GPU links": each token goes to the experts it was routed to).
+//
+// Row offsets[e] + r holds the r-th token (ascending token id) routed to local expert e.
+// Positions are fixed without atomics so the result is deterministic:
+//   count   per 256-token tile, per-expert counts (shared-memory counters; order-free)
+//   scan    one CTA: exclusive scan over (expert, tile) in expert-major order gives each
+//           (expert, tile) its first row; offsets and the MXFP8 m-tile bases fall out
+//   scatter per tile, the rank of token t among the tile's tokens routed to e is the
+//           popcount of a per-expert token bitmask below t
+//   gather  one warp per permuted row copies x[t] with 16-byte vector loads/stores (HBM
+//           bound); in MXFP8 mode it quantises each 32-value block while copying ("MXFP8
+//           Precision Reduces Memory Footprint": one scale per 32 consecutive values).
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr int kPermTile = 256;  // tokens per tile (count / scatter)
+
+__global__ void __launch_bounds__(kPermTile) perm_count_kernel(const int32_t* __restrict__ ids, int T, int k, int e0,
+                                                               int E_loc, int n_tiles, int32_t* __restrict__ tile_counts) {
+  extern __shared__ int s_cnt[];
+  for (int e = threadIdx.x; e < E_loc; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kPermTile + threadIdx.x;
+  if (t < T)
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(ids + t * k + j) - e0;
+      if (static_cast<unsigned>(e) < static_cast<unsigned>(E_loc)) atomicAdd(&s_cnt[e], 1);
+    }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E_loc; e += blockDim.x)
+    tile_counts[static_cast<int64_t>(e) * n_tiles + blockIdx.x] = s_cnt[e];
+}
+
+// Exclusive scan over a 1024-thread block; returns the prefix of v and the block total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int prefix = warp > 0 ? s_warp[warp - 1] : 0;
+  total = s_warp[nwarps - 1];
+  __syncthreads();
+  return prefix + x - v;
+}
+
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ tile_counts, int n_tiles, int E_loc,
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ mtile_base) {
+  __shared__ int s_warp[32];
+  __shared__ int s_off[1025];
+  const int n = E_loc * n_tiles;
+  int carry = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int v = i < n ? tile_counts[i] : 0;
+    int total;
+    const int ex = block_exclusive_scan(v, s_warp, total);
+    if (i < n) {
+      tile_counts[i] = carry + ex;  // first row of (expert i / n_tiles, tile i % n_tiles)
+      if (i % n_tiles == 0) s_off[i / n_tiles] = carry + ex;
+    }
+    carry += total;
+  }
+  if (threadIdx.x == 0) s_off[E_loc] = carry;
+  __syncthreads();
+  const int e = threadIdx.x;
+  int mt = 0;
+  if (e < E_loc) {
+    const int c = s_off[e + 1] - s_off[e];
+    counts[e] = c;
+    offsets[e] = s_off[e];
+    mt = (c + 127) / 128;
+  }
+  if (e == 0) offsets[E_loc] = s_off[E_loc];
+  int total;
+  const int ex = block_exclusive_scan(mt, s_warp, total);
+  if (mtile_base) {
+    if (e < E_loc) mtile_base[e] = ex;
+    if (e == 0) mtile_base[E_loc] = total;
+  }
+}
+
+__global__ void __launch_bounds__(kPermTile) perm_scatter_kernel(const int32_t* __restrict__ ids,
+                                                                 const float* __restrict__ probs, int T, int k, int e0,
+                                                                 int E_loc, int n_tiles,
+                                                                 const int32_t* __restrict__ tile_base,
+                                                                 int32_t* __restrict__ pair_to_row,
+                                                                 int32_t* __restrict__ row_src_token,
+                                                                 float* __restrict__ row_prob) {
+  extern __shared__ uint32_t s_mask[];  // [E_loc][kPermTile / 32] token bitmasks
+  constexpr int W = kPermTile / 32;
+  for (int i = threadIdx.x; i < E_loc * W; i += blockDim.x) s_mask[i] = 0u;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kPermTile + threadIdx.x;
+  if (t < T)
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(ids + t * k + j) - e0;
+      if (static_cast<unsigned>(e) < static_cast<unsigned>(E_loc)) atomicOr(&s_mask[e * W + warp], 1u << lane);
+    }
+  __syncthreads();
+  if (t >= T) return;
+  for (int j = 0; j < k; ++j) {
+    const int e = __ldg(ids + t * k + j) - e0;
+    int32_t row = -1;
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E_loc)) {
+      int rank = __popc(s_mask[e * W + warp] & ((1u << lane) - 1u));
+      for (int w = 0; w < warp; ++w) rank += __popc(s_mask[e * W + w]);
+      row = tile_base[static_cast<int64_t>(e) * n_tiles + blockIdx.x] + rank;
+      row_src_token[row] = static_cast<int32_t>(t);
+      row_prob[row] = __ldg(probs + t * k + j);
+    }
+    pair_to_row[t * k + j] = row;
+  }
+}
+
+// ------------------------------------------------------------------------------ gather
+// Plain copy of rows (fp32 -> fp32 or bf16 -> bf16), 16-byte vectors.
+__global__ void __launch_bounds__(256) perm_gather_copy_kernel(const uint4* __restrict__ x, int64_t row_vecs,
+                                                               const int32_t* __restrict__ offsets, int E_loc,
+                                                               const int32_t* __restrict__ row_src_token,
+                                                               uint4* __restrict__ perm_x) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int N = __ldg(offsets + E_loc);
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < N; r += warps) {
+    const int64_t t = __ldg(row_src_token + r);
+    const uint4* src = x + t * row_vecs;
+    uint4* dst = perm_x + r * row_vecs;
+    int64_t c = lane;
+    for (; c + 96 < row_vecs; c += 128) {
+      const uint4 a = __ldg(src + c), b = __ldg(src + c + 32), cc = __ldg(src + c + 64), d = __ldg(src + c + 96);
+      dst[c] = a;
+      dst[c + 32] = b;
+      dst[c + 64] = cc;
+      dst[c + 96] = d;
+    }
+    for (; c < row_vecs; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
+// Row copy with MXFP8 quantisation (blocks of 32 along d).  IN = 1: bf16 input (8 values
+// per 16-byte vector, 4 lanes per block); IN = 0: fp32 input (4 per vector, 8 lanes).
+template <int IN_BF16>
+__global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __restrict__ x, int d,
+                                                             const int32_t* __restrict__ offsets, int E_loc,
+                                                             const int32_t* __restrict__ mtile_base,
+                                                             const int32_t* __restrict__ row_src_token,
+                                                             uint8_t* __restrict__ perm_x, uint8_t* __restrict__ perm_sf) {
+  constexpr int VPV = IN_BF16 ? 8 : 4;  // values per 16-byte vector
+  constexpr int LPB = 32 / VPV;         // lanes per 32-value block
+  extern __shared__ int32_t s_tab[];    // offsets [E_loc+1], mtile_base [E_loc+1]
+  for (int i = threadIdx.x; i <= E_loc; i += blockDim.x) {
+    s_tab[i] = offsets[i];
+    s_tab[E_loc + 1 + i] = mtile_base[i];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int N = s_tab[E_loc];
+  const int row_vecs = d / VPV;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < N; r += warps) {
+    // expert of row r: the last e with offsets[e] <= r
+    int lo = 0, hi = E_loc - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tab[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    const int il = static_cast<int>(r - s_tab[lo]);
+    const int64_t tile = s_tab[E_loc + 1 + lo] + il / 128;
+    const int i = il % 128;
+    const int64_t t = __ldg(row_src_token + r);
+    const uint4* src = x + t * row_vecs;
+    uint8_t* dst = perm_x + r * d;
+    for (int base = 0; base < row_vecs; base += 32) {
+      const int c = base + lane;
+      const bool act = c < row_vecs;
+      float v[VPV];
+      if (act) {
+        const uint4 q = __ldg(src + c);
+        if (IN_BF16) {
+          v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+          v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
+        } else {
+          v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+          v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < VPV; ++u) v[u] = 0.0f;
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int u = 0; u < VPV; ++u) amax = fmaxf(amax, fabsf(v[u]));
+#pragma unroll
+      for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const int X = mx_exponent(amax);
+      const float inv = mx_inv_scale(X);
+      if (act) {
+        if (IN_BF16) {
+          uint2 o;
+          o.x = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
+                (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
+          o.y = static_cast<uint32_t>(e4m3x2(v[4] * inv, v[5] * inv)) |
+                (static_cast<uint32_t>(e4m3x2(v[6] * inv, v[7] * inv)) << 16);
+          *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(c) * 8) = o;
+        } else {
+          const uint32_t o = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
+                             (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
+          *reinterpret_cast<uint32_t*>(dst + static_cast<int64_t>(c) * 4) = o;
+        }
+        if ((lane % LPB) == 0) perm_sf[sf_act_offset(tile, i, c * VPV, d)] = static_cast<uint8_t>(X + 127);
+      }
+    }
+  }
+}
+
+struct PermuteWs {
+  int32_t* tile_counts;  // [E_loc][n_tiles]
+  int32_t* mtile_base;   // [E_loc + 1]
+};
+
+size_t permute_ws_bytes(int T, int E_loc) {
+  const int64_t n_tiles = ceil_div(T > 0 ? T : 1, kPermTile);
+  return align_up(static_cast<size_t>(n_tiles) * E_loc * 4, kAlign) + align_up((E_loc + 1) * 4, kAlign);
+}
+
+static PermuteWs carve_permute_ws(uint8_t* base, int T, int E_loc) {
+  const int64_t n_tiles = ceil_div(T > 0 ? T : 1, kPermTile);
+  PermuteWs w;
+  w.tile_counts = reinterpret_cast<int32_t*>(base);
+  w.mtile_base = reinterpret_cast<int32_t*>(base + align_up(static_cast<size_t>(n_tiles) * E_loc * 4, kAlign));
+  return w;
+}
+
+int gather_grid(cudaStream_t st);
+
+// perm_dtype: MOE_F32 / MOE_BF16 (copy in x's type) or MOE_MXFP8 (quantise).
+cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d,
+                           const int32_t* ids, const float* probs, int k, int e0, int E_loc, void* perm_x,
+                           uint8_t* perm_sf, int32_t* counts, int32_t* offsets, int32_t* row_src_token,
+                           float* row_prob, int32_t* pair_to_row, uint8_t* ws, cudaStream_t st) {
+  const int n_tiles = static_cast<int>(ceil_div(T > 0 ? T : 1, kPermTile));
+  PermuteWs w = carve_permute_ws(ws, T, E_loc);
+  if (T > 0) {
+    perm_count_kernel<<<n_tiles, kPermTile, E_loc * 4, st>>>(ids, T, k, e0, E_loc, n_tiles, w.tile_counts);
+  } else {
+    cudaMemsetAsync(w.tile_counts, 0, static_cast<size_t>(n_tiles) * E_loc * 4, st);
+  }
+  perm_scan_kernel<<<1, 1024, 0, st>>>(w.tile_counts, n_tiles, E_loc, counts, offsets, w.mtile_base);
+  if (T > 0) {
+    perm_scatter_kernel<<<n_tiles, kPermTile, E_loc * (kPermTile / 32) * 4, st>>>(
+        ids, probs, T, k, e0, E_loc, n_tiles, w.tile_counts, pair_to_row, row_src_token, row_prob);
+    const int grid = gather_grid(st);
+    if (perm_dtype == MOE_MXFP8) {
+      const size_t sm = static_cast<size_t>(2 * (E_loc + 1)) * 4;
+      if (x_dtype == MOE_BF16)
+        perm_gather_mx_kernel<1><<<grid, 256, sm, st>>>(static_cast<const uint4*>(x), d, offsets, E_loc, w.mtile_base,
+                                                        row_src_token, static_cast<uint8_t*>(perm_x), perm_sf);
+      else
+        perm_gather_mx_kernel<0><<<grid, 256, sm, st>>>(static_cast<const uint4*>(x), d, offsets, E_loc, w.mtile_base,
+                                                        row_src_token, static_cast<uint8_t*>(perm_x), perm_sf);
+    } else {
+      const int64_t row_vecs = static_cast<int64_t>(d) * (x_dtype == MOE_F32 ? 4 : 2) / 16;
+      perm_gather_copy_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(x), row_vecs, offsets, E_loc,
+                                                    row_src_token, static_cast<uint4*>(perm_x));
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,88 @@
+// Step 1: top-k routing over fp32 router logits ("Wide-EP ... NVIDIA" explainer, section
+// "MoE basics": the router chooses, per token, the experts it uses; DeepSeek-R1 picks 8 of
+// 256).  One warp per token: each lane holds E/32 logits as 64-bit keys
+// (order-preserving fp32 bits << 32 | ~expert_id), k rounds of a warp max-reduction pick
+// the winners in descending order with ties going to the lower id, then the softmax over
+// the k chosen logits gives the probabilities.  The logits are read once, coalesced.
+#include "moe_common.cuh"
+
+namespace moe {
+
+constexpr int kRouteWarps = 8;
+
+// Order-preserving map of a non-NaN fp32 to uint32 (-0.0 folded onto +0.0).
+__device__ __forceinline__ uint32_t ordered_bits(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0) u = 0;  // +-0.0 -> +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int VPL>  // values per lane = ceil(E / 32)
+__global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const float* __restrict__ logits, int T, int E,
+                                                                       int k, int32_t* __restrict__ ids,
+                                                                       float* __restrict__ probs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* row = logits + t * E;
+  unsigned long long key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = 0ull;  // below every real key (real keys have a non-zero high word or id bits)
+    if (e < E) {
+      const float v = __ldg(row + e);
+      key[i] = (static_cast<unsigned long long>(ordered_bits(v)) << 32) | static_cast<uint32_t>(~e);
+    }
+  }
+  int my_id = 0;
+  float my_val = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = key[0];
+#pragma unroll
+    for (int i = 1; i < VPL; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o > best ? o : best;
+    }
+    const int win = static_cast<int>(~static_cast<uint32_t>(best));
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)  // remove the winner
+      if (lane + 32 * i == win) key[i] = 0ull;
+    if (lane == j) {
+      my_id = win;
+      my_val = __ldg(row + win);
+    }
+  }
+  // softmax over the k chosen logits; lane 0 holds the largest one
+  const float l0 = __shfl_sync(0xffffffffu, my_val, 0);
+  const float w = (lane < k) ? expf(my_val - l0) : 0.0f;
+  float s = w;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane < k) {
+    ids[t * k + lane] = my_id;
+    probs[t * k + lane] = w / s;
+  }
+}
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* probs,
+                              cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(ceil_div(T, kRouteWarps))), block(kRouteWarps * 32);
+  const int vpl = static_cast<int>(ceil_div(E, 32));
+#define MOE_ROUTE_CASE(V) \
+  case V: route_topk_kernel<V><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs); break;
+  switch (vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : vpl <= 16 ? 16 : 32) {
+    MOE_ROUTE_CASE(2)
+    MOE_ROUTE_CASE(4)
+    MOE_ROUTE_CASE(8)
+    MOE_ROUTE_CASE(16)
+    MOE_ROUTE_CASE(32)
+  }
+#undef MOE_ROUTE_CASE
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,103 @@
+"""The C ABI without a GPU: libmoe.so builds for sm_103a, loads, exports every function
+include/moe.h declares, and its host-side logic (sizes, validation) answers correctly.
+No call here reaches a kernel: every validation case fails before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_layer_103_b300 import build
+    build.build()
+    import mixture_experts_layer_103_b300 as m
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    so = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in names if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_the_header(lib):
+    import mixture_experts_layer_103_b300 as m
+    for n in declared_functions():
+        assert n in m._SIGS, n
+
+
+def test_status_strings(lib):
+    L = lib.lib()
+    assert L.moe_status_string(0) == b"MOE_OK"
+    assert L.moe_status_string(5) == b"MOE_ERR_TIMEOUT"
+    assert L.moe_status_string(99) == b"MOE_ERR_UNKNOWN"
+
+
+def test_sizes(lib):
+    L = lib.lib()
+    assert L.moe_gu_block(2048) == 32 and L.moe_gu_block(48) == 0
+    # weight scales: E_loc * (rows/128) * (K/128) atoms of 512 bytes
+    assert L.moe_mx_weight_scale_bytes(32, 4096, 7168) == 32 * 32 * 56 * 512
+    assert L.moe_mx_weight_scale_bytes(1, 100, 128) == 0
+    # activation scales: (ceil(N_cap/128) + E_loc) tiles x (K/128) atoms
+    assert L.moe_mx_act_scale_bytes(1000, 256, 8) == (8 + 8) * 2 * 512
+    assert L.moe_permute_workspace_size(4096, 8, 64) > 256
+    big = L.moe_layer_workspace_size(4096, 2048, 1024, 64, 8, 64, 1)
+    # perm_x + Y2 (bf16) + h dominate: N_cap = 32768
+    assert big >= 32768 * 2048 * 2 * 2 + 32768 * 1024 * 2
+    assert L.moe_expert_gemm_workspace_size() == 256
+
+
+def _null():
+    return ctypes.c_void_p(0)
+
+
+def test_validation_before_any_launch(lib):
+    L = lib.lib()
+    P = ctypes.c_void_p(256)  # never dereferenced: every case below fails validation first
+    s = _null()
+    # route: k > E, k > 32, E > 1024, null pointers
+    assert L.moe_route_topk(P, 4, 8, 9, P, P, s) == 1
+    assert L.moe_route_topk(P, 4, 64, 33, P, P, s) == 1
+    assert L.moe_route_topk(P, 4, 1025, 8, P, P, s) == 1
+    assert L.moe_route_topk(_null(), 4, 8, 2, P, P, s) == 1
+    # pack: f not a multiple of 32 / MXFP8 d not a multiple of 128 / bad dtype pairs
+    assert L.moe_pack_weights(P, P, P, 1, 1, 2, 64, 48, P, P, None, None, s) == 2
+    assert L.moe_pack_weights(P, P, P, 1, 2, 2, 96, 128, P, P, P, P, s) == 2
+    assert L.moe_pack_weights(P, P, P, 0, 1, 2, 64, 64, P, P, None, None, s) == 2
+    assert L.moe_pack_weights(P, P, P, 1, 2, 2, 128, 128, P, P, None, None, s) == 1
+    # permute: workspace too small / misaligned
+    assert L.moe_permute(P, 1, 1, 16, 64, P, P, 2, 0, 8, P, None, P, P, P, P, P, P, 0, s) == 3
+    assert L.moe_permute(P, 1, 1, 16, 64, P, P, 2, 0, 8, P, None, P, P, P, P, P, ctypes.c_void_p(272), 1 << 20,
+                         s) == 3
+    assert L.moe_permute(P, 1, 1, 16, 60, P, P, 2, 0, 8, P, None, P, P, P, P, P, P, 1 << 20, s) == 2
+    assert L.moe_permute(P, 1, 2, 16, 64, P, P, 2, 0, 8, P, None, P, P, P, P, P, P, 1 << 20, s) == 1
+    # grouped MLP: E_loc out of range, unsupported dtype, workspace too small
+    assert L.moe_grouped_mlp(P, None, P, P, 64, 0, 64, 64, 1, P, None, P, None, P, P, 1 << 20, s) == 1
+    assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 64, 64, 7, P, None, P, None, P, P, 1 << 20, s) == 2
+    assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 64, 64, 1, P, None, P, None, P, P, 16, s) == 3
+    # MXFP8 without scales
+    assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 128, 128, 2, P, None, P, None, P, P, 1 << 20, s) == 1
+    # combine: k > 32, bf16 d not a multiple of 8
+    assert L.moe_unpermute_combine(P, P, 4, 33, 64, 1, P, s) == 1
+    assert L.moe_unpermute_combine(P, P, 4, 2, 60, 1, P, s) == 2
+    # layer: e0 + E_loc > E, workspace too small
+    assert L.moe_layer_forward(P, P, 8, 64, 64, 8, 2, 4, 8, 1, P, None, P, None, P, P, 1 << 30, s) == 1
+    assert L.moe_layer_forward(P, P, 8, 64, 64, 8, 2, 0, 8, 1, P, None, P, None, P, P, 64, s) == 3
+    # expert GEMMs: workspace missing
+    assert L.moe_expert_gemm2(P, None, P, 64, 4, 64, 64, 1, P, None, P, _null(), 256, s) == 3
+    # device error read: null output
+    assert L.moe_get_device_error(P, s, None) == 1

@@ -1,0 +1,316 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle, on a B300.
+
+Bit-exact: routing ids, per-expert counts/offsets, the permutation maps, the permuted
+rows (bf16/fp32 copies and MXFP8 codes + scales of x and of the weights).
+Within the layer tolerances (relative L2 vs the fp64 oracle): 1e-5 fp32, 2e-2 bf16,
+5e-2 MXFP8 -- on small workloads that span several 128-row tiles with ragged tails, on
+edge cases (1/127/128/129 rows per expert, one expert holding every token, empty
+experts, no local expert), and at full size on sampled tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import WORKLOADS, Workload, bf16_to_f32, gen_logits, gen_weights, gen_x, sample_tokens
+from moe_testlib import TOL, bf16_bits_np, gate_up_rows, rel_l2, to_dev, to_np, unpack_act_sf, unpack_w_sf
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mixture_experts_layer_103_b300 import build
+    build.build()
+    import mixture_experts_layer_103_b300 as m
+    assert m.moe_supported(), "needs compute capability 10.3 (B300)"
+    return m
+
+
+def _logits(kind, T, E, seed=0):
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        return rng.standard_normal((T, E)).astype(np.float32)
+    if kind == "quarter":  # many exact ties
+        return (rng.integers(-6, 6, size=(T, E)) * 0.25).astype(np.float32)
+    if kind == "equal":
+        return np.full((T, E), 0.5, np.float32)
+    if kind == "signed_zero":
+        lg = (rng.integers(-1, 2, size=(T, E)) * 0.0).astype(np.float32)
+        lg[:, ::3] = -0.0
+        lg[:, 1::5] = 0.0
+        return lg
+    raise ValueError(kind)
+
+
+# ----------------------------------------------------------------------------- route
+@pytest.mark.parametrize("T,E,k,kind", [
+    (512, 256, 8, "normal"), (300, 64, 8, "normal"), (64, 8, 2, "normal"), (100, 1024, 32, "normal"),
+    (77, 37, 5, "normal"), (256, 256, 8, "quarter"), (33, 256, 8, "equal"), (40, 96, 7, "signed_zero"),
+    (5, 1, 1, "normal"), (0, 8, 2, "normal"),
+])
+def test_route_parity(moe, T, E, k, kind):
+    lg = _logits(kind, T, E, seed=T + E)
+    ids, probs = moe.moe_route_topk(to_dev(lg), k)
+    torch.cuda.synchronize()
+    oids, oprobs = oracle.route_topk(lg, k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(probs.cpu().numpy(), oprobs, rtol=2e-6, atol=1e-7)
+
+
+# ----------------------------------------------------------------------------- permute
+PERM_CASES = [
+    # T, E, k, e0, E_loc, d, x dtype
+    (300, 64, 8, 0, 64, 256, "bf16"),
+    (1000, 256, 8, 32, 32, 128, "bf16"),
+    (2048, 256, 8, 0, 4, 512, "bf16"),
+    (64, 8, 2, 0, 8, 128, "f32"),
+    (257, 16, 4, 5, 1, 64, "f32"),
+    (33, 9, 9, 0, 9, 8, "bf16"),
+]
+
+
+@pytest.mark.parametrize("T,E,k,e0,E_loc,d,xdt", PERM_CASES)
+def test_permute_parity(moe, T, E, k, e0, E_loc, d, xdt):
+    w = Workload("perm", T, d, 32, E, k, e0, E_loc, xdt)
+    x = gen_x(w)
+    lg = (np.random.default_rng(T).integers(-4, 4, size=(T, E)) * 0.5).astype(np.float32)  # ties
+    ids_d, probs_d = moe.moe_route_topk(to_dev(lg), k)
+    P = moe.moe_permute(to_dev(x), ids_d, probs_d, e0, E_loc, xdt)
+    torch.cuda.synchronize()
+    ids = ids_d.cpu().numpy()
+    probs = probs_d.cpu().numpy()
+    O = oracle.permute(ids, e0, E_loc)
+    N = O["N"]
+    np.testing.assert_array_equal(P["counts"].cpu().numpy(), O["counts"])
+    np.testing.assert_array_equal(P["offsets"].cpu().numpy(), O["offsets"])
+    np.testing.assert_array_equal(P["pair_to_row"].cpu().numpy(), O["pair_to_row"])
+    rst = P["row_src_token"].cpu().numpy()[:N]
+    np.testing.assert_array_equal(rst, O["row_src_token"])
+    np.testing.assert_array_equal(P["row_prob"].cpu().numpy()[:N], probs[O["row_src_token"], O["row_slot"]])
+    px = P["perm_x"][:N]
+    got = bf16_bits_np(px) if xdt == "bf16" else px.cpu().numpy()
+    np.testing.assert_array_equal(got, x[O["row_src_token"]])
+
+
+@pytest.mark.parametrize("T,E,k,e0,E_loc,d,xdt", [
+    (300, 64, 8, 0, 64, 256, "bf16"), (700, 256, 8, 0, 32, 384, "bf16"), (129, 8, 2, 2, 4, 128, "f32"),
+])
+def test_permute_mx_parity(moe, T, E, k, e0, E_loc, d, xdt):
+    w = Workload("permmx", T, d, 32, E, k, e0, E_loc, xdt)
+    x = gen_x(w)
+    x[5] = 0  # an all-zero row: scale code 127
+    lg = gen_logits(w)
+    ids_d, probs_d = moe.moe_route_topk(to_dev(lg), k)
+    P = moe.moe_permute(to_dev(x), ids_d, probs_d, e0, E_loc, "mxfp8")
+    torch.cuda.synchronize()
+    O = oracle.permute(ids_d.cpu().numpy(), e0, E_loc)
+    N = O["N"]
+    codes, scales = oracle.mx_quantize(x[O["row_src_token"]], xdt, (N, d, 1))
+    np.testing.assert_array_equal(P["perm_x"][:N].cpu().numpy(), codes)
+    sf = unpack_act_sf(P["perm_x_scale"].cpu().numpy(), O["offsets"], d, N)
+    np.testing.assert_array_equal(sf, scales[:, :, 0])
+
+
+# ----------------------------------------------------------------------------- pack
+@pytest.mark.parametrize("dtype,E_loc,d,f", [("bf16", 3, 256, 96), ("f32", 2, 128, 64), ("mxfp8", 3, 256, 384),
+                                             ("mxfp8", 2, 384, 128)])
+def test_pack_parity(moe, dtype, E_loc, d, f):
+    w = Workload("pack", 1, d, f, E_loc, 1, 0, E_loc, "f32" if dtype == "f32" else "bf16")
+    Wg, Wu, Wd = gen_weights(w)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), dtype)
+    torch.cuda.synchronize()
+    gr, ur = gate_up_rows(f)
+    if dtype != "mxfp8":
+        get = bf16_bits_np if dtype == "bf16" else (lambda t: t.cpu().numpy())
+        Wgu = get(pw.Wgu)
+        np.testing.assert_array_equal(Wgu[:, gr, :], np.swapaxes(Wg, 1, 2))
+        np.testing.assert_array_equal(Wgu[:, ur, :], np.swapaxes(Wu, 1, 2))
+        np.testing.assert_array_equal(get(pw.Wd), np.swapaxes(Wd, 1, 2))
+        return
+    cg, sg = oracle.mx_quantize(Wg, "bf16", (E_loc, d, f))
+    cu, su = oracle.mx_quantize(Wu, "bf16", (E_loc, d, f))
+    cd, sd = oracle.mx_quantize(Wd, "bf16", (E_loc, f, d))
+    Wgu = pw.Wgu.cpu().numpy()
+    np.testing.assert_array_equal(Wgu[:, gr, :], np.swapaxes(cg, 1, 2))
+    np.testing.assert_array_equal(Wgu[:, ur, :], np.swapaxes(cu, 1, 2))
+    np.testing.assert_array_equal(pw.Wd.cpu().numpy(), np.swapaxes(cd, 1, 2))
+    S = unpack_w_sf(pw.Wgu_scale.cpu().numpy(), E_loc, 2 * f, d)
+    np.testing.assert_array_equal(S[:, gr, :], np.swapaxes(sg, 1, 2))
+    np.testing.assert_array_equal(S[:, ur, :], np.swapaxes(su, 1, 2))
+    np.testing.assert_array_equal(unpack_w_sf(pw.Wd_scale.cpu().numpy(), E_loc, d, f), np.swapaxes(sd, 1, 2))
+
+
+# ----------------------------------------------------------------------------- layer
+def oracle_layer(w: Workload, x, lg, Wg, Wu, Wd, tokens=None):
+    if w.dtype == "mxfp8":
+        cg, sg = oracle.mx_quantize(Wg, "bf16", (w.E_loc, w.d, w.f))
+        cu, su = oracle.mx_quantize(Wu, "bf16", (w.E_loc, w.d, w.f))
+        cd, sd = oracle.mx_quantize(Wd, "bf16", (w.E_loc, w.f, w.d))
+        return oracle.moe_forward(x, "bf16", lg, w.d, w.f, w.E, w.k, w.e0, w.E_loc, cg, cu, cd, "e4m3",
+                                  (sg, su, sd), mx_act=True, tokens=tokens)
+    return oracle.moe_forward(x, w.act_dtype, lg, w.d, w.f, w.E, w.k, w.e0, w.E_loc, Wg, Wu, Wd, w.act_dtype,
+                              tokens=tokens)
+
+
+def gpu_layer(moe, w: Workload, x, lg, Wg, Wu, Wd):
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), w.dtype)
+    y, ws = moe.moe_layer_forward(to_dev(x), to_dev(lg), w.E, w.k, w.e0, pw)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    return y
+
+
+SMALL = [
+    Workload("f32_tiny", 64, 128, 256, 8, 2, 0, 8, "f32"),
+    Workload("f32_slice", 200, 64, 96, 16, 4, 4, 8, "f32"),
+    Workload("bf16_a", 256, 256, 256, 8, 2, 0, 8, "bf16"),
+    Workload("bf16_ragged", 300, 200, 96, 16, 4, 4, 8, "bf16"),
+    Workload("bf16_e64", 1024, 512, 512, 64, 8, 0, 64, "bf16", ("normal", 0.5)),
+    Workload("bf16_ep64", 4096, 384, 256, 256, 8, 0, 4, "bf16"),
+    Workload("bf16_zipf", 512, 256, 128, 256, 8, 0, 32, "bf16", ("zipf", 1.1)),
+    Workload("mx_a", 256, 256, 256, 8, 2, 0, 8, "mxfp8"),
+    Workload("mx_ragged", 300, 384, 384, 16, 4, 4, 8, "mxfp8"),
+    Workload("mx_zipf", 1024, 512, 256, 256, 8, 0, 32, "mxfp8", ("zipf", 1.1)),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_layer_parity_small(moe, w):
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    y = gpu_layer(moe, w, x, lg, Wg, Wu, Wd)
+    yo = oracle_layer(w, x, lg, Wg, Wu, Wd)
+    err = rel_l2(to_np(y), yo)
+    assert err <= TOL[w.dtype], f"{w.name}: rel L2 {err:.3e}"
+
+
+def _forced_logits(counts, E, seed=0):
+    """k = 1 logits giving exactly counts[e] tokens to expert e (tokens shuffled)."""
+    owner = np.concatenate([np.full(c, e) for e, c in enumerate(counts)]).astype(np.int64)
+    rng = np.random.default_rng(seed)
+    rng.shuffle(owner)
+    lg = rng.standard_normal((owner.size, E)).astype(np.float32)
+    lg[np.arange(owner.size), owner] = 8.0
+    return lg
+
+
+EDGE = [
+    ("rows_1_127_128_129", [1, 127, 128, 129, 0, 255, 0, 2]),
+    ("one_expert_all", [0, 0, 0, 700, 0, 0, 0, 0]),
+    ("tiny_segments", [1, 1, 1, 1, 1, 1, 1, 1]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "mxfp8"])
+@pytest.mark.parametrize("name,counts", EDGE, ids=[e[0] for e in EDGE])
+def test_layer_edge_counts(moe, dtype, name, counts):
+    E = len(counts)
+    lg = _forced_logits(counts, E)
+    T = lg.shape[0]
+    w = Workload(name, T, 256, 128, E, 1, 0, E, dtype)
+    x = gen_x(w)
+    Wg, Wu, Wd = gen_weights(w)
+    y = gpu_layer(moe, w, x, lg, Wg, Wu, Wd)
+    yo = oracle_layer(w, x, lg, Wg, Wu, Wd)
+    assert rel_l2(to_np(y), yo) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
+def test_no_local_expert_gives_zeros(moe, dtype):
+    E, T = 16, 64
+    lg = _forced_logits([T // 4] * 4 + [0] * 12, E)
+    w = Workload("nolocal", T, 128, 128, E, 2, 8, 8, dtype)  # experts 8..15 get nothing
+    x = gen_x(w)
+    Wg, Wu, Wd = gen_weights(w)
+    lg[:, 8:] = -8.0
+    y = gpu_layer(moe, w, x, lg, Wg, Wu, Wd)
+    assert (to_np(y) == 0).all()
+
+
+def test_split_calls_equal_fused_call(moe):
+    """route -> permute -> gemm1 -> gemm2 -> combine through the separate entry points
+    gives exactly the fused moe_layer_forward result (same kernels, same order)."""
+    w = Workload("split", 512, 256, 256, 32, 4, 8, 16, "bf16")
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), "bf16")
+    xd, lgd = to_dev(x), to_dev(lg)
+    y_fused, _ = moe.moe_layer_forward(xd, lgd, w.E, w.k, w.e0, pw)
+    ids, probs = moe.moe_route_topk(lgd, w.k)
+    P = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, "bf16")
+    h, hs, _ = moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw)
+    Y2, _ = moe.moe_expert_gemm2(h, hs, P["offsets"], pw)
+    y = moe.moe_unpermute_combine(Y2, P["pair_to_row"], "bf16")
+    Y2b, _ = moe.moe_grouped_mlp(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_fused)
+    N = int(P["offsets"][-1])
+    assert torch.equal(Y2[:N], Y2b[:N])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
+def test_deterministic(moe, dtype):
+    w = Workload("det", 777, 256, 256, 64, 8, 0, 64, dtype, ("normal", 0.5))
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), dtype)
+    xd, lgd = to_dev(x), to_dev(lg)
+    y1, ws = moe.moe_layer_forward(xd, lgd, w.E, w.k, w.e0, pw)
+    y1 = y1.clone()
+    ws.fill_(0xA5)
+    y2, _ = moe.moe_layer_forward(xd, lgd, w.E, w.k, w.e0, pw, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "mxfp8"])
+def test_canaries_untouched(moe, dtype):
+    """Output and workspace carry guard bands before and after; none may change."""
+    w = Workload("canary", 300, 256, 128, 16, 4, 2, 8, dtype)
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), dtype)
+    pad = 4096
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    ybig = torch.full((w.T * w.d + 2 * pad,), 7.0, dtype=tdt, device="cuda")
+    y = ybig[pad:pad + w.T * w.d].view(w.T, w.d)
+    nb = moe.moe_layer_workspace_size(w.T, w.d, w.f, w.E, w.k, w.E_loc, dtype)
+    wsbig = torch.full((nb + 2 * 256 * 64,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws = wsbig[256 * 64: 256 * 64 + nb]
+    moe.moe_layer_forward(to_dev(x), to_dev(lg), w.E, w.k, w.e0, pw, y=y, ws=ws)
+    torch.cuda.synchronize()
+    assert (ybig[:pad] == 7.0).all() and (ybig[-pad:] == 7.0).all()
+    assert (wsbig[:256 * 64] == 0x5A).all() and (wsbig[256 * 64 + nb:] == 0x5A).all()
+    yo = oracle_layer(w, x, lg, Wg, Wu, Wd)
+    assert rel_l2(to_np(y), yo) <= TOL[dtype]
+
+
+# ----------------------------------------------------------------------------- full size
+FULL = ["tiny_fp32", "bf16_e64", "ep8_zipf_T512", "ep64_T2048", "ep64_T8192", "ep64_T32768",
+        "mxfp8_ep8_zipf_T8192", "mxfp8_ep64_T8192"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(moe, name):
+    """Full workload through moe_layer_forward; routing/permutation checked for every token,
+    the output on a seeded sample of tokens against the oracle."""
+    w = WORKLOADS[name]
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    xd, lgd = to_dev(x), to_dev(lg)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), w.dtype)
+    y, ws = moe.moe_layer_forward(xd, lgd, w.E, w.k, w.e0, pw)
+    ids, _ = moe.moe_route_topk(lgd, w.k)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    oids, _ = oracle.route_topk(lg, w.k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), oids)
+    tok = sample_tokens(w, 48 if w.T > 64 else w.T)
+    # always include tokens with a local expert so the sample is not all zeros
+    local = np.where(((oids >= w.e0) & (oids < w.e0 + w.E_loc)).any(1))[0]
+    tok = np.unique(np.concatenate([tok, local[:: max(1, local.size // 48)][:48]]))
+    yo = oracle_layer(w, x, lg, Wg, Wu, Wd, tokens=tok)
+    err = rel_l2(to_np(y)[tok], yo)
+    assert err <= TOL[w.dtype], f"{name}: rel L2 {err:.3e}"
