@@ -49,6 +49,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     return p.parse_args()
 
 
@@ -395,7 +396,7 @@ def run_ours(args, w):
 
     # ---- end to end through moe_layer_forward with host buffers
     e2e = None
-    if rank == 0 or world > 1:
+    if not args.no_e2e:
         x_pin = torch.empty(xd.shape, dtype=xd.dtype).pin_memory()
         x_pin.copy_(xd.cpu())
         lg_pin = torch.empty(lgd.shape, dtype=lgd.dtype).pin_memory()
