@@ -129,6 +129,30 @@ moe_status moe_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, i
                        size_t workspace_bytes, moe_stream_t stream);
 size_t moe_permute_workspace_size(int T, int k, int E_loc);
 
+/* moe_permute without a workspace argument.  (The source pages have no counterpart; this
+ * entry point exists for callers of the library, not for the layer's definition.)
+ * For callers that cannot call cudaMalloc at the time they permute -- e.g. a serving
+ * engine that has given all free device memory to its KV-cache pool and plans every
+ * buffer up front, or a host that is recording a CUDA graph and must not allocate.  It
+ * computes exactly what moe_permute computes, with the same arguments minus the
+ * workspace; the caller still passes every input and output buffer.  The scratch (error
+ * word, per-tile expert counts, m-tile bases) lives in a 1 MiB file-scope device array
+ * that every device using this library keeps until the process exits; nothing is
+ * allocated or freed.
+ *   Limit: moe_permute_workspace_size(T, k, E_loc) <= 1 MiB, i.e. ceil(T / 256) * E_loc
+ *   <= about 260,000 (T <= 65,024 tokens at E_loc = 1024, T <= 260,864 at E_loc <= 256);
+ *   larger inputs return MOE_ERR_WORKSPACE and launch nothing.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call before any
+ *   stream capture.  Every call shares the one array: calls whose kernels may overlap on
+ *   the GPU (different streams, or different host threads on one device) race on it and
+ *   must be serialised by the caller.  Everything the kernels need zeroed is cleared by
+ *   the call itself. */
+moe_status moe_permute_noalloc(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d,
+                               const int32_t* topk_ids, const float* topk_probs, int k, int e0, int E_loc,
+                               void* perm_x, uint8_t* perm_x_scale, int32_t* counts, int32_t* offsets,
+                               int32_t* row_src_token, float* row_prob, int32_t* pair_to_row, moe_stream_t stream);
+
 /* Bytes of an activation scale buffer in the SF tile layout for N_cap rows, K columns. */
 size_t moe_mx_act_scale_bytes(int64_t N_cap, int K, int E_loc);
 

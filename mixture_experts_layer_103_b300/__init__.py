@@ -4,8 +4,8 @@ Thin ctypes marshalling over the C ABI declared in ``include/moe.h``: every func
 here has the same name as the C entry point it calls, passes raw device pointers and the
 current torch CUDA stream, and raises :class:`MoeError` on a non-zero status.  torch is
 used only to allocate device memory and to name the stream; every step of the layer runs
-in the library's CUDA kernels.  There is no fallback: importing this package fails if
-``libmoe.so`` has not been built (``python -m mixture_experts_layer_103_b300.build``).
+in the library's CUDA kernels.  There is no fallback: importing this package builds ``libmoe.so``
+if it is missing or stale and fails if it cannot be built or loaded.
 
 The layer (sources: "Wide-EP ... NVIDIA" explainer, section "MoE basics"; "Efficient MoE
 training for biological foundation models", sections "GroupedLinear Optimizes Expert
@@ -36,8 +36,13 @@ class MoeError(RuntimeError):
         self.status = status
 
 
-if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m mixture_experts_layer_103_b300.build`")
+from . import build as _build  # noqa: E402  (build.py does not import this package)
+
+try:
+    # compiles libmoe.so when it is missing or older than its sources (nvcc, sm_103a)
+    LIB_PATH = _build.build()
+except Exception as exc:  # no CUDA library, no layer: fail loudly
+    raise ImportError(f"cannot build or find {LIB_PATH}: {exc}") from exc
 _lib = ctypes.CDLL(LIB_PATH)
 
 _P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -46,6 +51,7 @@ _SIGS = {
     "moe_route_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_permute": (_I, [_P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
+    "moe_permute_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_mx_act_scale_bytes": (_SZ, [_I64, _I, _I]),
     "moe_pack_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_mx_weight_scale_bytes": (_SZ, [_I, _I, _I]),
@@ -144,6 +150,20 @@ def moe_permute(x: torch.Tensor, topk_ids: torch.Tensor, topk_probs: torch.Tenso
         _ptr(x), x_dt, _dt(perm_dtype), T, d, _ptr(topk_ids), _ptr(topk_probs), k, e0, E_loc, _ptr(out["perm_x"]),
         _ptr(out["perm_x_scale"]), _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["row_src_token"]),
         _ptr(out["row_prob"]), _ptr(out["pair_to_row"]), _ptr(ws), ws.numel(), _stream()))
+    return out
+
+
+def moe_permute_noalloc(x: torch.Tensor, topk_ids: torch.Tensor, topk_probs: torch.Tensor, e0: int, E_loc: int,
+                        perm_dtype="bf16", out=None) -> dict:
+    """moe_permute with the library's static scratch (no workspace; the library allocates nothing)."""
+    T, d = x.shape
+    k = topk_ids.shape[1]
+    x_dt = MOE_F32 if x.dtype == torch.float32 else MOE_BF16
+    out = out if out is not None else alloc_permute(T, d, k, E_loc, x.dtype, perm_dtype, x.device)
+    _check("moe_permute_noalloc", _lib.moe_permute_noalloc(
+        _ptr(x), x_dt, _dt(perm_dtype), T, d, _ptr(topk_ids), _ptr(topk_probs), k, e0, E_loc, _ptr(out["perm_x"]),
+        _ptr(out["perm_x_scale"]), _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["row_src_token"]),
+        _ptr(out["row_prob"]), _ptr(out["pair_to_row"]), _stream()))
     return out
 
 
