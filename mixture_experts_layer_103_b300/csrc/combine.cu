@@ -8,31 +8,51 @@
 
 namespace moe {
 
+constexpr int kCombineGroup = 8;  // slots whose loads are in flight together
+
 template <bool F32>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ p2r,
                                                       int T, int k, int64_t row_vecs, uint4* __restrict__ y) {
+  constexpr int V = F32 ? 4 : 8;  // values per 16-byte vector
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   const int32_t my_row = lane < k ? __ldg(p2r + t * k + lane) : -1;
-  const uint32_t valid = __ballot_sync(0xffffffffu, my_row >= 0);
+  const uint32_t valid = __ballot_sync(0xffffffffu, my_row >= 0);  // local slots, ascending j
+  const int nv = __popc(valid);
   uint4* dst = y + t * row_vecs;
-  for (int64_t c = lane; c < row_vecs; c += 32) {
-    float acc[F32 ? 4 : 8];
+  for (int64_t base = 0; base < row_vecs; base += 32) {  // warp-uniform trip count
+    const int64_t c = base + lane;
+    const bool act = c < row_vecs;
+    float acc[V];
 #pragma unroll
-    for (int u = 0; u < (F32 ? 4 : 8); ++u) acc[u] = 0.0f;
+    for (int u = 0; u < V; ++u) acc[u] = 0.0f;
     uint32_t m = valid;
-    while (m) {  // slots in ascending order j = 0..k-1
-      const int j = __ffs(m) - 1;
-      m &= m - 1;
-      const int64_t row = __shfl_sync(0xffffffffu, my_row, j);
-      const uint4 q = __ldg(Y2 + row * row_vecs + c);
-      if (F32) {
-        acc[0] += __uint_as_float(q.x); acc[1] += __uint_as_float(q.y);
-        acc[2] += __uint_as_float(q.z); acc[3] += __uint_as_float(q.w);
-      } else {
-        acc[0] += bf16_lo(q.x); acc[1] += bf16_hi(q.x); acc[2] += bf16_lo(q.y); acc[3] += bf16_hi(q.y);
-        acc[4] += bf16_lo(q.z); acc[5] += bf16_hi(q.z); acc[6] += bf16_lo(q.w); acc[7] += bf16_hi(q.w);
+    for (int g = 0; g < nv; g += kCombineGroup) {
+      // issue the loads of up to 8 slots, then add them in slot order
+      uint4 q[kCombineGroup];
+#pragma unroll
+      for (int j = 0; j < kCombineGroup; ++j) {
+        q[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (g + j < nv) {
+          const int src = __ffs(m) - 1;
+          m &= m - 1;
+          const int64_t row = __shfl_sync(0xffffffffu, my_row, src);
+          if (act) q[j] = __ldg(Y2 + row * row_vecs + c);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kCombineGroup; ++j) {
+        if (g + j < nv) {
+          if (F32) {
+            acc[0] += __uint_as_float(q[j].x); acc[1] += __uint_as_float(q[j].y);
+            acc[2] += __uint_as_float(q[j].z); acc[3] += __uint_as_float(q[j].w);
+          } else {
+            acc[0] += bf16_lo(q[j].x); acc[1] += bf16_hi(q[j].x); acc[2] += bf16_lo(q[j].y);
+            acc[3] += bf16_hi(q[j].y); acc[4] += bf16_lo(q[j].z); acc[5] += bf16_hi(q[j].z);
+            acc[6] += bf16_lo(q[j].w); acc[7] += bf16_hi(q[j].w);
+          }
+        }
       }
     }
     uint4 o;
@@ -43,7 +63,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
       o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                      pack_bf16x2(acc[6], acc[7]));
     }
-    dst[c] = o;
+    if (act) dst[c] = o;
   }
 }
 

@@ -57,41 +57,56 @@ struct GemmArgs {
   uint64_t timeout_ns;
 };
 
-template <int BN, int STAGES, bool MX>
-struct GemmCfg {
-  static constexpr int A_BYTES = kBM * kRowBytes;
-  static constexpr int B_BYTES = BN * kRowBytes;
-  static constexpr int SFA_BYTES = MX ? 512 : 0;
-  static constexpr int SFB_BYTES = MX ? (BN / 128) * 512 : 0;
-  static constexpr int BK = MX ? 128 : 64;      // K elements per stage
-  static constexpr int UMMA_K = MX ? 32 : 16;   // K elements per MMA
-  static constexpr int NUM_ACC = MX ? 1 : 2;
-  static constexpr int ACC_COLS = NUM_ACC * BN;
-  static constexpr int SF_REGION = MX ? (BN / 128 + 1) * 4 : 0;  // SFA 4 cols + SFB 4 per 128 rows
-  static constexpr int USED_COLS = ACC_COLS + 2 * SF_REGION;
-  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
-                                   : USED_COLS <= 256 ? 256 : 512;
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-  static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+// Shared-memory plan.  The A/B pipeline is a ring of variable-size stages inside a fixed
+// byte budget: a stage holds one 128-row A tile and one BN-row B tile (128 bytes per
+// row), so the depth is 4 stages at BN = 256, 6 at BN = 128 and 8 at BN = 64.  The MXFP8
+// scale atoms of each stage live in a separate ring.
+template <bool MX>
+struct GemmSmem {
+  static constexpr int MAX_STAGES = 8;
+  static constexpr int A_BYTES = kBM * kRowBytes;           // 16 KB
+  static constexpr int PIPE_BYTES = 192 * 1024;             // A + B ring
+  static constexpr int SF_STAGE_BYTES = MX ? 512 + 1024 : 0; // SFA atom + up to two SFB atoms
+  static constexpr int BK = MX ? 128 : 64;                  // K elements per stage
+  static constexpr int UMMA_K = MX ? 32 : 16;               // K elements per MMA
+  static constexpr int OFF_PIPE = 0;
+  static constexpr int OFF_SF = OFF_PIPE + PIPE_BYTES;
+  static constexpr int OFF_BAR = OFF_SF + MAX_STAGES * SF_STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TAB = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = OFF_TAB + 2 * (kMaxEloc + 1) * 4 + 1024;  // + alignment slack
-  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 128");
-  static_assert(!MX || BN % 128 == 0, "MXFP8 tiles cover whole 128-row scale atoms");
-  static_assert(USED_COLS <= 512, "TMEM has 512 columns");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
+
+// Tile width of a launch, identical in every CTA: the candidate with the fewest
+// "weighted waves", waves(BN) * c(BN), where c is the relative time of one tile (a
+// 128x128 tile costs ~0.6 of a 128x256 one: same A traffic, half the MMA work; a 128x64
+// tile ~0.4: its MMAs are shared-memory bound).  Many tiles -> 256 (best reuse); few
+// tiles (decode-like slices) -> narrower tiles so that more SMs stream the weights.
+__device__ __forceinline__ int choose_bn(int m_tiles, int n_out, int ctas, bool mx) {
+  const int cand[3] = {256, 128, 64};
+  const float cost[3] = {1.0f, 0.6f, 0.4f};
+  int best = 256;
+  float best_cost = 3.0e38f;
+  for (int i = 0; i < (mx ? 2 : 3); ++i) {
+    const long tiles = static_cast<long>(m_tiles) * ((n_out + cand[i] - 1) / cand[i]);
+    const long waves = (tiles + ctas - 1) / ctas;
+    const float c = static_cast<float>(waves) * cost[i];
+    if (c < best_cost) {
+      best_cost = c;
+      best = cand[i];
+    }
+  }
+  return best;
+}
 
 struct Tile {
   int e, mt, row0, rows, n0;
 };
 
-template <int BN>
-__device__ __forceinline__ Tile decode_tile(int t, int n_tiles_n, const int* s_off, const int* s_mtp, int E_loc) {
+__device__ __forceinline__ Tile decode_tile(int t, int n_tiles_n, int bn, const int* s_off, const int* s_mtp,
+                                            int E_loc) {
   const int gm = t / n_tiles_n;
   int lo = 0, hi = E_loc - 1;  // last expert whose first m-tile is <= gm (skips empty experts)
   while (lo < hi) {
@@ -104,7 +119,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles_n, const int* s_o
   r.mt = gm;
   r.row0 = s_off[lo] + (gm - s_mtp[lo]) * kBM;
   r.rows = min(kBM, s_off[lo + 1] - r.row0);
-  r.n0 = (t - gm * n_tiles_n) * BN;
+  r.n0 = (t - gm * n_tiles_n) * bn;
   return r;
 }
 
@@ -113,20 +128,25 @@ __device__ __forceinline__ void gemm_abort(const GemmArgs& g, volatile int* s_ab
   set_device_error(g.err, MOE_ERR_TIMEOUT);
 }
 
-template <int BN, int STAGES, bool MX, int EPI>
+// B operand maps with box heights 256, 128 and 64 rows (one per tile width).
+struct BMaps {
+  CUtensorMap b256, b128, b64;
+};
+
+template <bool MX, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BMaps tmB,
                            const GemmArgs g) {
-  using C = GemmCfg<BN, STAGES, MX>;
+  using C = GemmSmem<MX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::MAX_STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::MAX_STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::MAX_STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::MAX_STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* s_off = reinterpret_cast<int*>(smem + C::OFF_TAB);
@@ -134,7 +154,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::MAX_STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
@@ -146,10 +166,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     *s_abort = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmA);
-    ptx::prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish();
   }
   if (warp == 2) build_mtile_prefix(g.offsets, g.E_loc, kBM, s_off, s_mtp);
@@ -158,42 +177,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   ptx::tc_fence_after();
 
   const uint32_t tmem_base = *tmem_slot;
+  const int m_tiles = s_mtp[g.E_loc];
+  const int BN = choose_bn(m_tiles, g.n_out, gridDim.x, MX);
+  const CUtensorMap* tmb = BN == 256 ? &tmB.b256 : BN == 128 ? &tmB.b128 : &tmB.b64;
+  const int stage_bytes = C::A_BYTES + BN * kRowBytes;  // multiple of 1024
+  const int stages = min(C::MAX_STAGES, C::PIPE_BYTES / stage_bytes);
+  const int sf_cols = MX ? (BN / 128 + 1) * 4 : 0;       // SFA 4 columns + SFB 4 per 128 rows
+  const int num_acc = (2 * BN + 2 * sf_cols <= 512) ? 2 : 1;
+  const uint32_t sf_base_col = static_cast<uint32_t>(num_acc * BN);
   const int n_tiles_n = (g.n_out + BN - 1) / BN;
-  const int total = s_mtp[g.E_loc] * n_tiles_n;
+  const int total = m_tiles * n_tiles_n;
   const int num_kb = (g.K + C::BK - 1) / C::BK;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ TMA producer
+      ptx::prefetch_tmap(tmb);
       int s = 0;
       uint32_t ph = 0;
       int64_t issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<BN>(t, n_tiles_n, s_off, s_mtp, g.E_loc);
+        const Tile tl = decode_tile(t, n_tiles_n, BN, s_off, s_mtp, g.E_loc);
         const int sfb_bytes = MX ? min(BN, g.n_out - tl.n0) / 128 * 512 : 0;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (*s_abort) { ok = false; break; }
           if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
           const uint32_t fb = full_bar(s);
-          ptx::mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + C::SFA_BYTES + sfb_bytes);
-          ptx::tma_load_3d(sbase + C::OFF_A + s * C::A_BYTES, &tmA, fb, kb * C::BK, tl.row0, 0);
-          ptx::tma_load_3d(sbase + C::OFF_B + s * C::B_BYTES, &tmB, fb, kb * C::BK, tl.n0, tl.e);
+          const uint32_t st_addr = sbase + C::OFF_PIPE + s * stage_bytes;
+          ptx::mbar_arrive_expect_tx(fb, stage_bytes + (MX ? 512 + sfb_bytes : 0));
+          ptx::tma_load_3d(st_addr, &tmA, fb, kb * C::BK, tl.row0, 0);
+          ptx::tma_load_3d(st_addr + C::A_BYTES, tmb, fb, kb * C::BK, tl.n0, tl.e);
           if constexpr (MX) {
             const int kg = g.K / 128;
-            ptx::bulk_load(sbase + C::OFF_SFA + s * C::SFA_BYTES,
-                           g.a_sf + (static_cast<int64_t>(tl.mt) * kg + kb) * 512, 512, fb);
-            ptx::bulk_load(sbase + C::OFF_SFB + s * C::SFB_BYTES,
+            const uint32_t sf_addr = sbase + C::OFF_SF + s * C::SF_STAGE_BYTES;
+            ptx::bulk_load(sf_addr, g.a_sf + (static_cast<int64_t>(tl.mt) * kg + kb) * 512, 512, fb);
+            ptx::bulk_load(sf_addr + 512,
                            g.b_sf + ((static_cast<int64_t>(tl.e) * kg + kb) * (g.n_out / 128) + tl.n0 / 128) * 512,
                            sfb_bytes, fb);
           }
           ++issued;
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+          if (++s == stages) { s = 0; ph ^= 1u; }
         }
       }
       if (!ok) {  // let the copies already issued land before the CTA exits
-        for (int64_t i = issued - 1; i >= 0 && i >= issued - STAGES; --i)
-          ptx::mbar_wait(full_bar(static_cast<int>(i % STAGES)), static_cast<uint32_t>((i / STAGES) & 1),
+        for (int64_t i = issued - 1; i >= 0 && i >= issued - stages; --i)
+          ptx::mbar_wait(full_bar(static_cast<int>(i % stages)), static_cast<uint32_t>((i / stages) & 1),
                          g.timeout_ns);
       }
     }
@@ -206,23 +235,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        const int acc = C::NUM_ACC == 2 ? (it & 1) : 0;
-        const uint32_t acc_ph = C::NUM_ACC == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
+        const int acc = num_acc == 2 ? (it & 1) : 0;
+        const uint32_t acc_ph = num_acc == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
         if (!ptx::mbar_wait(tempty_bar(acc), acc_ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); break; }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!ptx::mbar_wait(full_bar(s), ph, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t a_addr = sbase + C::OFF_A + s * C::A_BYTES;
-          const uint32_t b_addr = sbase + C::OFF_B + s * C::B_BYTES;
+          const uint32_t a_addr = sbase + C::OFF_PIPE + s * stage_bytes;
+          const uint32_t b_addr = a_addr + C::A_BYTES;
           if constexpr (MX) {
-            const uint32_t sf_col = tmem_base + C::ACC_COLS + (kbg & 1u) * C::SF_REGION;
-            ptx::tmem_cp_32x128b_x4(sf_col, ptx::sdesc_sf(sbase + C::OFF_SFA + s * C::SFA_BYTES));
-#pragma unroll
+            const uint32_t sf_addr = sbase + C::OFF_SF + s * C::SF_STAGE_BYTES;
+            const uint32_t sf_col = tmem_base + sf_base_col + (kbg & 1u) * static_cast<uint32_t>(sf_cols);
+            ptx::tmem_cp_32x128b_x4(sf_col, ptx::sdesc_sf(sf_addr));
             for (int i = 0; i < BN / 128; ++i)
-              ptx::tmem_cp_32x128b_x4(sf_col + 4 + 4 * i,
-                                      ptx::sdesc_sf(sbase + C::OFF_SFB + s * C::SFB_BYTES + i * 512));
+              ptx::tmem_cp_32x128b_x4(sf_col + 4 + 4 * i, ptx::sdesc_sf(sf_addr + 512 + i * 512));
 #pragma unroll
             for (int k = 0; k < C::BK / C::UMMA_K; ++k)
               ptx::mma_mxf8(d_tmem, ptx::sdesc_sw128(a_addr + k * 32), ptx::sdesc_sw128(b_addr + k * 32),
@@ -235,7 +263,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             (kb | k) != 0);
           }
           ptx::mma_commit(empty_bar(s));  // frees the stage once these MMAs have read it
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+          if (++s == stages) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
         ptx::mma_commit(tfull_bar(acc));  // accumulator ready for the epilogue
@@ -249,9 +277,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       if (*s_abort) break;
-      const Tile tl = decode_tile<BN>(t, n_tiles_n, s_off, s_mtp, g.E_loc);
-      const int acc = C::NUM_ACC == 2 ? (it & 1) : 0;
-      const uint32_t acc_ph = C::NUM_ACC == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
+      const Tile tl = decode_tile(t, n_tiles_n, BN, s_off, s_mtp, g.E_loc);
+      const int acc = num_acc == 2 ? (it & 1) : 0;
+      const uint32_t acc_ph = num_acc == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
       int okw = 0;
       if (lane == 0) okw = ptx::mbar_wait(tfull_bar(acc), acc_ph, g.timeout_ns) ? 1 : 0;
       okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -333,7 +361,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    ptx::tmem_dealloc(tmem_base, 512);
   }
 }
 
@@ -370,16 +398,28 @@ static bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_
 
 int num_sms();
 
-template <int BN, int STAGES, bool MX, int EPI>
+template <bool MX, int EPI>
 static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
                                     cudaStream_t st) {
-  using C = GemmCfg<BN, STAGES, MX>;
-  CUtensorMap ta, tb;
+  using C = GemmSmem<MX>;
+  CUtensorMap ta;
+  BMaps tb;
   if (!make_operand_map(&ta, A, MX, g.K, a_rows, 1, kBM)) return cudaErrorInvalidValue;
-  if (!make_operand_map(&tb, B, MX, g.K, g.n_out, g.E_loc, BN)) return cudaErrorInvalidValue;
-  auto kern = tc_grouped_gemm_kernel<BN, STAGES, MX, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (!make_operand_map(&tb.b256, B, MX, g.K, g.n_out, g.E_loc, 256)) return cudaErrorInvalidValue;
+  if (!make_operand_map(&tb.b128, B, MX, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
+  if (!make_operand_map(&tb.b64, B, MX, g.K, g.n_out, g.E_loc, 64)) return cudaErrorInvalidValue;
+  auto kern = tc_grouped_gemm_kernel<MX, EPI>;
+  // opt in to > 48 KB of dynamic shared memory once per device (keeps later launches,
+  // including ones recorded into a CUDA graph, free of non-launch API calls)
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
   kern<<<num_sms(), kGemmThreads, C::SMEM_BYTES, st>>>(ta, tb, g);
   return cudaGetLastError();
 }
@@ -408,8 +448,8 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
   g.row_prob = row_prob;
   g.a_sf = perm_sf;
   g.b_sf = Wgu_sf;
-  if (mx) return launch_gemm_inst<256, 4, true, EPI_SWIGLU_MX>(perm_x, N_cap, Wgu, g, st);
-  return launch_gemm_inst<256, 4, false, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
+  if (mx) return launch_gemm_inst<true, EPI_SWIGLU_MX>(perm_x, N_cap, Wgu, g, st);
+  return launch_gemm_inst<false, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
 }
 
 // GEMM2 on the tensor cores: h [N_cap, f] (bf16, or E4M3 + SF) -> Y2 bf16 [N_cap, d].
@@ -423,8 +463,8 @@ cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* o
   g.ld_out = d;
   g.a_sf = h_sf;
   g.b_sf = Wd_sf;
-  if (mx) return launch_gemm_inst<256, 4, true, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
-  return launch_gemm_inst<256, 4, false, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
+  if (mx) return launch_gemm_inst<true, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
+  return launch_gemm_inst<false, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
 }
 
 }  // namespace moe
