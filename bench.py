@@ -300,6 +300,8 @@ def run_ours(args, w):
     names = ["route_topk", "permute", "gemm1_swiglu", "gemm2", "combine"]
     n_ev = len(names) + 1
 
+    hint = moe.moe_rows_hint(T, k, w.E)
+
     def step(evs):
         evs[0].record()
         moe.moe_route_topk(lgd, k, ids, probs)
@@ -307,9 +309,9 @@ def run_ours(args, w):
         moe.moe_permute(xd, ids, probs, e0, E_loc, w.dtype, ws=ws_perm, out=P)
         evs[2].record()
         moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, h=h,
-                                    h_scale=hs, ws=ws_g)
+                                    h_scale=hs, ws=ws_g, rows_hint=hint)
         evs[3].record()
-        moe.moe_expert_gemm2(h, hs, P["offsets"], pw, Y2=Y2, ws=ws_g)
+        moe.moe_expert_gemm2(h, hs, P["offsets"], pw, Y2=Y2, ws=ws_g, rows_hint=hint)
         evs[4].record()
         moe.moe_unpermute_combine(Y2, P["pair_to_row"], w.dtype, y=y)
         evs[5].record()
@@ -402,7 +404,8 @@ def run_ours(args, w):
     else:
         roof = {"bound": "hbm", "achieved": by / t_s / 1e9, "peak": hbm, "unit": "GB/s",
                 "frac": by / t_s / 1e9 / hbm}
-    kname = "tc_grouped_gemm_kernel" if w.dtype != "f32" else "simt_grouped_gemm_kernel"
+    kname = ("simt_grouped_gemm_kernel" if w.dtype == "f32" else
+             "tc_grouped_gemm_pair_kernel" if (w.dtype == "bf16" and hint >= 384) else "tc_grouped_gemm_kernel")
     roof.update({"kernel": f"{kname} ({dom})", "traffic": recorded_traffic(dom, w.name),
                  "peak_kind": pk_kind + (" (bf16 x2 nominal fp8 ratio)" if w.dtype == "mxfp8" else "")})
     t_roof = max(bf["layer_flops"] / (tpeak * 1e12), bf["layer_bytes"] / (hbm * 1e9))

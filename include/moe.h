@@ -181,12 +181,18 @@ size_t moe_mx_weight_scale_bytes(int E_loc, int rows, int K);
  *   Wgu_packed, Wgu_scale, Wd_packed, Wd_scale   packed weights (scales NULL unless MXFP8)
  *   Y2      device [N_cap, d]: fp32 for MOE_F32, bf16 otherwise
  *   workspace device >= moe_grouped_mlp_workspace_size(...) bytes, 256-byte aligned
+ *   rows_hint  expected rows per local expert (e.g. moe_rows_hint(T, k, E)); it only picks
+ *              the kernel shape (bf16 runs on CTA pairs with 256-row tiles from 384 expected
+ *              rows up), never the result's meaning; <= 0 uses N_cap / E_loc.
  * Requires d % 8 == 0 and f % 32 == 0 (bf16); d % 128 == 0 and f % 128 == 0 (MXFP8). */
 moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                            const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
                            const void* Wgu_packed, const uint8_t* Wgu_scale, const void* Wd_packed,
-                           const uint8_t* Wd_scale, void* Y2, void* workspace, size_t workspace_bytes,
+                           const uint8_t* Wd_scale, void* Y2, int rows_hint, void* workspace, size_t workspace_bytes,
                            moe_stream_t stream);
+/* Expected rows per local expert under uniform routing, T * k / E (the hint
+ * moe_layer_forward uses). */
+int moe_rows_hint(int T, int k, int E);
 size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype);
 
 /* The two halves of moe_grouped_mlp, for callers that keep h themselves (same
@@ -197,14 +203,15 @@ size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, mo
  *       GroupedLinear + ScaledSwiGLU (+ quantisation) in one kernel].
  *   moe_expert_gemm2: h (+ h_scale) -> Y2 [N_cap, d] (fp32 for MOE_F32, else bf16)
  *       [BIO: the second GroupedLinear].
+ *   rows_hint: as for moe_grouped_mlp.
  *   workspace: >= moe_expert_gemm_workspace_size() bytes, 256-byte aligned (error word). */
 moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                                    const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
                                    const void* Wgu_packed, const uint8_t* Wgu_scale, void* h, uint8_t* h_scale,
-                                   void* workspace, size_t workspace_bytes, moe_stream_t stream);
+                                   int rows_hint, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t* offsets, int64_t N_cap, int E_loc,
                             int d, int f, moe_dtype dtype, const void* Wd_packed, const uint8_t* Wd_scale, void* Y2,
-                            void* workspace, size_t workspace_bytes, moe_stream_t stream);
+                            int rows_hint, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 size_t moe_expert_gemm_workspace_size(void);
 
 /* Unpermute + combine (step 5) [WEP "MoE basics": results of the chosen experts are

@@ -55,10 +55,11 @@ _SIGS = {
     "moe_mx_act_scale_bytes": (_SZ, [_I64, _I, _I]),
     "moe_pack_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_mx_weight_scale_bytes": (_SZ, [_I, _I, _I]),
-    "moe_grouped_mlp": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_grouped_mlp": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
+    "moe_rows_hint": (_I, [_I, _I, _I]),
     "moe_grouped_mlp_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
-    "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
+    "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm_workspace_size": (_SZ, []),
     "moe_unpermute_combine": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_layer_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -204,7 +205,11 @@ def moe_pack_weights(W_gate: torch.Tensor, W_up: torch.Tensor, W_down: torch.Ten
     return PackedWeights(dst, E_loc, d, f, Wgu, Wd, sg, sd)
 
 
-def moe_grouped_mlp(perm_x, perm_x_scale, offsets, row_prob, pw: PackedWeights, Y2=None, ws=None):
+def moe_rows_hint(T: int, k: int, E: int) -> int:
+    return int(_lib.moe_rows_hint(T, k, E))
+
+
+def moe_grouped_mlp(perm_x, perm_x_scale, offsets, row_prob, pw: PackedWeights, Y2=None, ws=None, rows_hint=0):
     cap = perm_x.shape[0]
     dev = perm_x.device
     Y2 = Y2 if Y2 is not None else torch.empty(cap, pw.d, dtype=torch_dtype(pw.dtype), device=dev)
@@ -212,7 +217,8 @@ def moe_grouped_mlp(perm_x, perm_x_scale, offsets, row_prob, pw: PackedWeights, 
     ws = ws if ws is not None else workspace(nb, dev)
     _check("moe_grouped_mlp", _lib.moe_grouped_mlp(
         _ptr(perm_x), _ptr(perm_x_scale), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f, pw.dtype,
-        _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(pw.Wd), _ptr(pw.Wd_scale), _ptr(Y2), _ptr(ws), ws.numel(), _stream()))
+        _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(pw.Wd), _ptr(pw.Wd_scale), _ptr(Y2), int(rows_hint), _ptr(ws), ws.numel(),
+        _stream()))
     return Y2, ws
 
 
@@ -226,24 +232,24 @@ def alloc_h(N_cap: int, pw: PackedWeights, device="cuda"):
 
 
 def moe_expert_gemm1_swiglu(perm_x, perm_x_scale, offsets, row_prob, pw: PackedWeights, h=None, h_scale=None,
-                            ws=None):
+                            ws=None, rows_hint=0):
     cap = perm_x.shape[0]
     if h is None:
         h, h_scale = alloc_h(cap, pw, perm_x.device)
     ws = ws if ws is not None else workspace(_lib.moe_expert_gemm_workspace_size(), perm_x.device)
     _check("moe_expert_gemm1_swiglu", _lib.moe_expert_gemm1_swiglu(
         _ptr(perm_x), _ptr(perm_x_scale), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f, pw.dtype,
-        _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(h), _ptr(h_scale), _ptr(ws), ws.numel(), _stream()))
+        _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(h), _ptr(h_scale), int(rows_hint), _ptr(ws), ws.numel(), _stream()))
     return h, h_scale, ws
 
 
-def moe_expert_gemm2(h, h_scale, offsets, pw: PackedWeights, Y2=None, ws=None):
+def moe_expert_gemm2(h, h_scale, offsets, pw: PackedWeights, Y2=None, ws=None, rows_hint=0):
     cap = h.shape[0]
     Y2 = Y2 if Y2 is not None else torch.empty(cap, pw.d, dtype=torch_dtype(pw.dtype), device=h.device)
     ws = ws if ws is not None else workspace(_lib.moe_expert_gemm_workspace_size(), h.device)
     _check("moe_expert_gemm2", _lib.moe_expert_gemm2(
         _ptr(h), _ptr(h_scale), _ptr(offsets), cap, pw.E_loc, pw.d, pw.f, pw.dtype, _ptr(pw.Wd), _ptr(pw.Wd_scale),
-        _ptr(Y2), _ptr(ws), ws.numel(), _stream()))
+        _ptr(Y2), int(rows_hint), _ptr(ws), ws.numel(), _stream()))
     return Y2, ws
 
 

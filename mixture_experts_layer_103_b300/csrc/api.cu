@@ -20,10 +20,11 @@ cudaError_t launch_simt_gemm1(const float* perm_x, const int32_t* offsets, const
 cudaError_t launch_simt_gemm2(const float* h, const int32_t* offsets, int64_t N_cap, int E_loc, int d, int f,
                               const float* Wd, float* Y2, cudaStream_t st);
 cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
-                            int64_t N_cap, int E_loc, int d, int f, bool mx, const void* Wgu, const uint8_t* Wgu_sf,
-                            void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns, cudaStream_t st);
+                            int64_t N_cap, int E_loc, int d, int f, bool mx, bool pair, const void* Wgu,
+                            const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns,
+                            cudaStream_t st);
 cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
-                            int f, bool mx, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
+                            int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
                             uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
@@ -81,36 +82,47 @@ static moe_status check_mlp_shape(int d, int f, int E_loc, moe_dtype dt) {
   return MOE_OK;
 }
 
+// Expected rows per local expert at or above which bf16 GEMMs run on CTA pairs (256-row
+// tiles); below it the 1-CTA kernel with its device-chosen tile width serves better.
+constexpr int kPairRowsThreshold = 384;
+
+static bool use_pair(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint) {
+  const int64_t rows = rows_hint > 0 ? rows_hint : n_cap / (E_loc > 0 ? E_loc : 1);
+  return dt == MOE_BF16 && rows >= kPairRowsThreshold;
+}
+
 static cudaError_t run_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets,
                              const float* row_prob, int64_t n_cap, int E_loc, int d, int f, moe_dtype dt,
                              const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
-                             cudaStream_t st) {
+                             int rows_hint, cudaStream_t st) {
   if (n_cap == 0) return cudaSuccess;
   if (dt == MOE_F32)
     return launch_simt_gemm1(static_cast<const float*>(perm_x), offsets, row_prob, n_cap, E_loc, d, f,
                              static_cast<const float*>(Wgu), static_cast<float*>(h), st);
-  return launch_tc_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt == MOE_MXFP8, Wgu, Wgu_sf, h, h_sf,
-                         err, kTimeoutNs, st);
+  return launch_tc_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt == MOE_MXFP8,
+                         use_pair(dt, n_cap, E_loc, rows_hint), Wgu, Wgu_sf, h, h_sf, err, kTimeoutNs, st);
 }
 
 static cudaError_t run_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t n_cap, int E_loc,
                              int d, int f, moe_dtype dt, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
-                             cudaStream_t st) {
+                             int rows_hint, cudaStream_t st) {
   if (n_cap == 0) return cudaSuccess;
   if (dt == MOE_F32)
     return launch_simt_gemm2(static_cast<const float*>(h), offsets, n_cap, E_loc, d, f, static_cast<const float*>(Wd),
                              static_cast<float*>(Y2), st);
-  return launch_tc_gemm2(h, h_sf, offsets, n_cap, E_loc, d, f, dt == MOE_MXFP8, Wd, Wd_sf, Y2, err, kTimeoutNs, st);
+  return launch_tc_gemm2(h, h_sf, offsets, n_cap, E_loc, d, f, dt == MOE_MXFP8, use_pair(dt, n_cap, E_loc, rows_hint),
+                         Wd, Wd_sf, Y2, err, kTimeoutNs, st);
 }
 
 static cudaError_t run_mlp(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
                            int64_t n_cap, int E_loc, int d, int f, moe_dtype dt, const void* Wgu, const uint8_t* Wgu_sf,
                            const void* Wd, const uint8_t* Wd_sf, void* Y2, uint8_t* scratch, int32_t* err,
-                           cudaStream_t st) {
+                           int rows_hint, cudaStream_t st) {
   MlpScratch s = carve_mlp(scratch, n_cap, f, dt);
-  cudaError_t e = run_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt, Wgu, Wgu_sf, s.h, s.h_sf, err, st);
+  cudaError_t e = run_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt, Wgu, Wgu_sf, s.h, s.h_sf, err,
+                            rows_hint, st);
   if (e != cudaSuccess) return e;
-  return run_gemm2(s.h, s.h_sf, offsets, n_cap, E_loc, d, f, dt, Wd, Wd_sf, Y2, err, st);
+  return run_gemm2(s.h, s.h_sf, offsets, n_cap, E_loc, d, f, dt, Wd, Wd_sf, Y2, err, rows_hint, st);
 }
 
 // ---- whole-layer workspace -------------------------------------------------------------
@@ -266,7 +278,7 @@ size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, mo
 moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                            const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
                            const void* Wgu_packed, const uint8_t* Wgu_scale, const void* Wd_packed,
-                           const uint8_t* Wd_scale, void* Y2, void* workspace, size_t workspace_bytes,
+                           const uint8_t* Wd_scale, void* Y2, int rows_hint, void* workspace, size_t workspace_bytes,
                            moe_stream_t stream) {
   moe_status s = check_mlp_shape(d, f, E_loc, dtype);
   if (s != MOE_OK) return s;
@@ -283,10 +295,16 @@ moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, cons
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(run_mlp(perm_x, perm_x_scale, offsets, row_prob, N_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale,
-                             Wd_packed, Wd_scale, Y2, ws + sizeof(WsHeader), reinterpret_cast<int32_t*>(ws), stream));
+                             Wd_packed, Wd_scale, Y2, ws + sizeof(WsHeader), reinterpret_cast<int32_t*>(ws), rows_hint,
+                             stream));
 }
 
 size_t moe_expert_gemm_workspace_size(void) { return sizeof(WsHeader); }
+
+int moe_rows_hint(int T, int k, int E) {
+  if (T <= 0 || k <= 0 || E <= 0) return 0;
+  return static_cast<int>(static_cast<int64_t>(T) * k / E);
+}
 
 static moe_status check_gemm_common(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype, const void* offsets,
                                     const void* a, const void* a_sf, const void* w, const void* w_sf, const void* out,
@@ -304,7 +322,7 @@ static moe_status check_gemm_common(int64_t N_cap, int E_loc, int d, int f, moe_
 moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                                    const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
                                    const void* Wgu_packed, const uint8_t* Wgu_scale, void* h, uint8_t* h_scale,
-                                   void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+                                   int rows_hint, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   moe_status s = check_gemm_common(N_cap, E_loc, d, f, dtype, offsets, perm_x, perm_x_scale, Wgu_packed, Wgu_scale, h,
                                    h_scale);
   if (s != MOE_OK) return s;
@@ -313,18 +331,19 @@ moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_sca
   int32_t* err = static_cast<int32_t*>(workspace);
   if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(run_gemm1(perm_x, perm_x_scale, offsets, row_prob, N_cap, E_loc, d, f, dtype, Wgu_packed,
-                               Wgu_scale, h, h_scale, err, stream));
+                               Wgu_scale, h, h_scale, err, rows_hint, stream));
 }
 
 moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t* offsets, int64_t N_cap, int E_loc,
                             int d, int f, moe_dtype dtype, const void* Wd_packed, const uint8_t* Wd_scale, void* Y2,
-                            void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+                            int rows_hint, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   moe_status s = check_gemm_common(N_cap, E_loc, d, f, dtype, offsets, h, h_scale, Wd_packed, Wd_scale, Y2, nullptr);
   if (s != MOE_OK) return s;
   if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
   int32_t* err = static_cast<int32_t*>(workspace);
   if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(run_gemm2(h, h_scale, offsets, N_cap, E_loc, d, f, dtype, Wd_packed, Wd_scale, Y2, err, stream));
+  return cuda_status(
+      run_gemm2(h, h_scale, offsets, N_cap, E_loc, d, f, dtype, Wd_packed, Wd_scale, Y2, err, rows_hint, stream));
 }
 
 moe_status moe_unpermute_combine(const void* Y2, const int32_t* pair_to_row, int T, int k, int d, moe_dtype dtype,
@@ -367,7 +386,7 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
                        w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
   if (e == cudaSuccess)
     e = run_mlp(w.perm_x, w.perm_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale,
-                Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, stream);
+                Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, moe_rows_hint(T, k, E), stream);
   if (e == cudaSuccess) e = launch_combine(w.Y2, w.pair_to_row, T, k, d, dtype, y, stream);
   return cuda_status(e);
 }

@@ -30,32 +30,9 @@
 
 #include <mutex>
 
-#include "moe_common.cuh"
-#include "tc_ptx.cuh"
+#include "gemm_tc.cuh"
 
 namespace moe {
-
-constexpr int kBM = 128;
-constexpr int kRowBytes = 128;  // bytes of one operand row per pipeline stage
-constexpr int kGemmThreads = 192;
-constexpr int kMaxEloc = 1024;
-
-enum { EPI_STORE_BF16 = 0, EPI_SWIGLU_BF16 = 1, EPI_SWIGLU_MX = 2 };
-
-struct GemmArgs {
-  const int32_t* offsets;  // [E_loc + 1]
-  int E_loc;
-  int n_out;               // output columns (GEMM1: packed 2f; GEMM2: d)
-  int K;                   // contraction length in elements
-  void* out;               // bf16 [rows, ld_out] or E4M3 bytes [rows, ld_out]
-  int64_t ld_out;          // elements per output row
-  uint8_t* out_sf;         // EPI_SWIGLU_MX: scales of h (activation SF tile layout, K = n_out / 2)
-  const float* row_prob;   // GEMM1: routing probability per permuted row
-  const uint8_t* a_sf;     // MXFP8: scales of A (activation SF tile layout)
-  const uint8_t* b_sf;     // MXFP8: scales of B (weight SF tile layout)
-  int32_t* err;            // device error word
-  uint64_t timeout_ns;
-};
 
 // Shared-memory plan.  The A/B pipeline is a ring of variable-size stages inside a fixed
 // byte budget: a stage holds one 128-row A tile and one BN-row B tile (128 bytes per
@@ -99,33 +76,6 @@ __device__ __forceinline__ int choose_bn(int m_tiles, int n_out, int ctas, bool 
     }
   }
   return best;
-}
-
-struct Tile {
-  int e, mt, row0, rows, n0;
-};
-
-__device__ __forceinline__ Tile decode_tile(int t, int n_tiles_n, int bn, const int* s_off, const int* s_mtp,
-                                            int E_loc) {
-  const int gm = t / n_tiles_n;
-  int lo = 0, hi = E_loc - 1;  // last expert whose first m-tile is <= gm (skips empty experts)
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_mtp[mid] <= gm) lo = mid;
-    else hi = mid - 1;
-  }
-  Tile r;
-  r.e = lo;
-  r.mt = gm;
-  r.row0 = s_off[lo] + (gm - s_mtp[lo]) * kBM;
-  r.rows = min(kBM, s_off[lo + 1] - r.row0);
-  r.n0 = (t - gm * n_tiles_n) * bn;
-  return r;
-}
-
-__device__ __forceinline__ void gemm_abort(const GemmArgs& g, volatile int* s_abort) {
-  *s_abort = 1;
-  set_device_error(g.err, MOE_ERR_TIMEOUT);
 }
 
 // B operand maps with box heights 256, 128 and 64 rows (one per tile width).
@@ -290,67 +240,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool valid = r < tl.rows;
       const int64_t grow = static_cast<int64_t>(tl.row0) + r;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if constexpr (EPI == EPI_STORE_BF16) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld32(tbase + c, v);
-          ptx::tmem_ld_wait();
-          const int n = tl.n0 + c;
-          if (valid && n < g.n_out) {
-            uint4* dst = reinterpret_cast<uint4*>(out + grow * g.ld_out + n);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (n + 8 * j < g.n_out)
-                dst[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-                                    pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                                    pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                                    pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
-          }
-        }
-      } else {
-        const float p = valid ? __ldg(g.row_prob + grow) : 0.0f;
-        const int fdim = g.n_out / 2;
-#pragma unroll 1
-        for (int sb = 0; sb < BN / 64; ++sb) {
-          uint32_t gv[32], uv[32];
-          ptx::tmem_ld32(tbase + sb * 64, gv);       // 32 gate columns
-          ptx::tmem_ld32(tbase + sb * 64 + 32, uv);  // the matching 32 up columns
-          ptx::tmem_ld_wait();
-          const int fc = tl.n0 / 2 + sb * 32;  // first h column of this block
-          float h[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float gg = __uint_as_float(gv[i]);
-            h[i] = p * (gg / (1.0f + __expf(-gg))) * __uint_as_float(uv[i]);
-          }
-          if (valid && fc < fdim) {
-            if constexpr (EPI == EPI_SWIGLU_BF16) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g.out) + grow * g.ld_out + fc);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                dst[j] = make_uint4(pack_bf16x2(h[8 * j + 0], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
-                                    pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
-            } else {
-              float amax = 0.0f;
-#pragma unroll
-              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
-              const int X = mx_exponent(amax);
-              const float inv = mx_inv_scale(X);
-              uint32_t w[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                w[j] = static_cast<uint32_t>(e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv)) |
-                       (static_cast<uint32_t>(e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv)) << 16);
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(g.out) + grow * g.ld_out + fc);
-              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-              g.out_sf[sf_act_offset(tl.mt, r, fc, fdim)] = static_cast<uint8_t>(X + 127);
-            }
-          }
-        }
-      }
+      epilogue_row<EPI>(g, tl, tbase, BN, r, valid, grow);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
@@ -380,7 +270,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 3-D K-major operand [outer, rows, K] (outer = 1 for a plain matrix), box [1, box_rows, 128 bytes].
-static bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, uint64_t rows, uint64_t outer,
+bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, uint64_t rows, uint64_t outer,
                              uint32_t box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
@@ -395,8 +285,6 @@ static bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
-
-int num_sms();
 
 template <bool MX, int EPI>
 static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
@@ -436,9 +324,14 @@ static GemmArgs base_args(const int32_t* offsets, int E_loc, int32_t* err, uint6
 // GEMM1 + fused scaled SwiGLU on the tensor cores.
 //   bf16:  perm_x bf16 [N_cap, d] -> h bf16 [N_cap, f]
 //   mxfp8: perm_x E4M3 [N_cap, d] + SF -> h E4M3 [N_cap, f] + SF
+cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu,
+                             cudaStream_t st);
+
+// pair: bf16 only -- run the CTA-pair kernel (large M per expert) instead of the 1-CTA one.
 cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
-                            int64_t N_cap, int E_loc, int d, int f, bool mx, const void* Wgu, const uint8_t* Wgu_sf,
-                            void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
+                            int64_t N_cap, int E_loc, int d, int f, bool mx, bool pair, const void* Wgu,
+                            const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns,
+                            cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
   g.n_out = 2 * f;
   g.K = d;
@@ -449,12 +342,13 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
   g.a_sf = perm_sf;
   g.b_sf = Wgu_sf;
   if (mx) return launch_gemm_inst<true, EPI_SWIGLU_MX>(perm_x, N_cap, Wgu, g, st);
+  if (pair) return launch_pair_gemm(perm_x, N_cap, Wgu, g, true, st);
   return launch_gemm_inst<false, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
 }
 
 // GEMM2 on the tensor cores: h [N_cap, f] (bf16, or E4M3 + SF) -> Y2 bf16 [N_cap, d].
 cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
-                            int f, bool mx, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
+                            int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
                             uint64_t timeout_ns, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
   g.n_out = d;
@@ -464,6 +358,7 @@ cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* o
   g.a_sf = h_sf;
   g.b_sf = Wd_sf;
   if (mx) return launch_gemm_inst<true, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
+  if (pair) return launch_pair_gemm(h, N_cap, Wd, g, false, st);
   return launch_gemm_inst<false, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
 }
 

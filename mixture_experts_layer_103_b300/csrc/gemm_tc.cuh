@@ -1,0 +1,139 @@
+// Shared pieces of the tcgen05 grouped GEMM kernels (1-CTA and 2-CTA variants): launch
+// arguments, tile decoding over the ragged per-expert segments, the fused epilogue and
+// the TMA tensor-map helper.
+#pragma once
+
+#include <cuda.h>
+
+#include "moe_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+constexpr int kBM = 128;
+constexpr int kRowBytes = 128;  // bytes of one operand row per pipeline stage
+constexpr int kGemmThreads = 192;
+constexpr int kMaxEloc = 1024;
+
+enum { EPI_STORE_BF16 = 0, EPI_SWIGLU_BF16 = 1, EPI_SWIGLU_MX = 2 };
+
+struct GemmArgs {
+  const int32_t* offsets;  // [E_loc + 1]
+  int E_loc;
+  int n_out;               // output columns (GEMM1: packed 2f; GEMM2: d)
+  int K;                   // contraction length in elements
+  void* out;               // bf16 [rows, ld_out] or E4M3 bytes [rows, ld_out]
+  int64_t ld_out;          // elements per output row
+  uint8_t* out_sf;         // EPI_SWIGLU_MX: scales of h (activation SF tile layout, K = n_out / 2)
+  const float* row_prob;   // GEMM1: routing probability per permuted row
+  const uint8_t* a_sf;     // MXFP8: scales of A (activation SF tile layout)
+  const uint8_t* b_sf;     // MXFP8: scales of B (weight SF tile layout)
+  int32_t* err;            // device error word
+  uint64_t timeout_ns;
+};
+
+struct Tile {
+  int e, mt, row0, rows, n0;
+};
+
+// Tile t of a launch whose m-tiles are `bm`-row slices of each expert segment, numbered
+// in expert order (s_mtp = prefix of ceil(count / bm)), and n-tiles are `bn` columns.
+__device__ __forceinline__ Tile decode_tile(int t, int n_tiles_n, int bn, const int* s_off, const int* s_mtp,
+                                            int E_loc, int bm = kBM) {
+  const int gm = t / n_tiles_n;
+  int lo = 0, hi = E_loc - 1;  // last expert whose first m-tile is <= gm (skips empty experts)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_mtp[mid] <= gm) lo = mid;
+    else hi = mid - 1;
+  }
+  Tile r;
+  r.e = lo;
+  r.mt = gm;
+  r.row0 = s_off[lo] + (gm - s_mtp[lo]) * bm;
+  r.rows = min(bm, s_off[lo + 1] - r.row0);
+  r.n0 = (t - gm * n_tiles_n) * bn;
+  return r;
+}
+
+__device__ __forceinline__ void gemm_abort(const GemmArgs& g, volatile int* s_abort) {
+  *s_abort = 1;
+  set_device_error(g.err, MOE_ERR_TIMEOUT);
+}
+
+// Epilogue of one accumulator row (one thread = one TMEM lane = one output row r of a
+// 128-row tile): bf16 store of BN columns (GEMM2), or the fused scaled SwiGLU on BN/64
+// blocks of 32 gate + 32 up columns with bf16 or MXFP8 (one 32-value block per thread)
+// output (GEMM1).  tbase = TMEM address of this warp's lane quarter and accumulator.
+template <int EPI>
+__device__ __forceinline__ void epilogue_row(const GemmArgs& g, const Tile& tl, uint32_t tbase, int BN, int r,
+                                             bool valid, int64_t grow) {
+  if constexpr (EPI == EPI_STORE_BF16) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tbase + c, v);
+      ptx::tmem_ld_wait();
+      const int n = tl.n0 + c;
+      if (valid && n < g.n_out) {
+        uint4* dst = reinterpret_cast<uint4*>(out + grow * g.ld_out + n);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (n + 8 * j < g.n_out)
+            dst[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+      }
+    }
+  } else {
+    const float p = valid ? __ldg(g.row_prob + grow) : 0.0f;
+    const int fdim = g.n_out / 2;
+#pragma unroll 1
+    for (int sb = 0; sb < BN / 64; ++sb) {
+      uint32_t gv[32], uv[32];
+      ptx::tmem_ld32(tbase + sb * 64, gv);       // 32 gate columns
+      ptx::tmem_ld32(tbase + sb * 64 + 32, uv);  // the matching 32 up columns
+      ptx::tmem_ld_wait();
+      const int fc = tl.n0 / 2 + sb * 32;  // first h column of this block
+      float h[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float gg = __uint_as_float(gv[i]);
+        h[i] = p * (gg / (1.0f + __expf(-gg))) * __uint_as_float(uv[i]);
+      }
+      if (valid && fc < fdim) {
+        if constexpr (EPI == EPI_SWIGLU_BF16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g.out) + grow * g.ld_out + fc);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(pack_bf16x2(h[8 * j + 0], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
+                                pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
+        } else {
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+          const int X = mx_exponent(amax);
+          const float inv = mx_inv_scale(X);
+          uint32_t w[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            w[j] = static_cast<uint32_t>(e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv)) |
+                   (static_cast<uint32_t>(e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv)) << 16);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(g.out) + grow * g.ld_out + fc);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          g.out_sf[sf_act_offset(tl.mt, r, fc, fdim)] = static_cast<uint8_t>(X + 127);
+        }
+      }
+    }
+  }
+}
+
+// 3-D K-major operand map [outer, rows, K], box [1, box_rows, 128 bytes], 128-byte swizzle.
+bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, uint64_t rows, uint64_t outer,
+                      uint32_t box_rows);
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,212 @@
+// Grouped GEMM on CTA pairs (tcgen05 cta_group::2), bf16, for the large-M regime.
+//
+// Same computation as the 1-CTA kernel in gemm_tc.cu ("Efficient MoE training for
+// biological foundation models", section "GroupedLinear Optimizes Expert Computation":
+// grouped per-expert GEMMs with ScaledSwiGLU fused after the first), but a cluster of two
+// CTAs on one TPC computes a 256 x 256 tile with one MMA stream:
+//   * CTA r of the pair stages rows [128 r, 128 r + 128) of the tile's A (token rows of
+//     one expert) and rows [128 r, 128 r + 128) of the 256-row B tile (packed weights);
+//     both TMA loads count on the leader's (rank 0) full barrier;
+//   * the leader's single MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
+//     K = 16); the accumulator rows of each CTA land in that CTA's own TMEM;
+//   * the leader's commits arrive on the empty / accumulator-full barriers of both CTAs
+//     (multicast); both CTAs' epilogue warps drain their own TMEM rows and arrive on the
+//     leader's accumulator-empty barrier.
+// Per SM and 64-wide K step this moves 32 KB into shared memory and reads 32 KB of
+// operands into the tensor core, half the shared-memory traffic of a 1-CTA 128 x 256
+// tile, which is what bounds the 1-CTA kernel.
+#include "gemm_tc.cuh"
+
+namespace moe {
+
+struct PairSmem {
+  static constexpr int STAGES = 6;
+  static constexpr int A_BYTES = 128 * kRowBytes;  // this CTA's 128 rows of A
+  static constexpr int B_BYTES = 128 * kRowBytes;  // this CTA's half of the 256 B rows
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BK = 64;                    // bf16 K elements per stage
+  static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_TAB = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = OFF_TAB + 2 * (kMaxEloc + 1) * 4 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+constexpr int kPairBM = 256;  // rows of a pair tile (128 per CTA)
+constexpr int kPairBN = 256;  // columns of a pair tile
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    tc_grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                                const GemmArgs g) {
+  using C = PairSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* s_off = reinterpret_cast<int*>(smem + C::OFF_TAB);
+  int* s_mtp = s_off + g.E_loc + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull_bar(a), 1);
+      ptx::mbar_init(tempty_bar(a), 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {  // one warp in each CTA of the pair allocates the pair's TMEM
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish_pair();
+  }
+  if (warp == 2) build_mtile_prefix(g.offsets, g.E_loc, kPairBM, s_off, s_mtp);
+  __syncwarp();
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // barrier inits of both CTAs visible before any cross-CTA signal
+  ptx::tc_fence_after();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int n_tiles_n = (g.n_out + kPairBN - 1) / kPairBN;
+  const int total = s_mtp[g.E_loc] * n_tiles_n;
+  const int num_kb = (g.K + C::BK - 1) / C::BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------------ TMA producer (both CTAs)
+      int s = 0;
+      uint32_t ph = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs) {
+        const Tile tl = decode_tile(t, n_tiles_n, kPairBN, s_off, s_mtp, g.E_loc, kPairBM);
+        const int a_row = tl.row0 + 128 * static_cast<int>(rank);
+        const int b_row = tl.n0 + 128 * static_cast<int>(rank);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (*s_abort) { ok = false; break; }
+          if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
+          const uint32_t fb_leader = ptx::mapa_shared(full_bar(s), 0);
+          if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * C::STAGE_BYTES);
+          const uint32_t st_addr = sbase + s * C::STAGE_BYTES;
+          ptx::tma_load_3d_pair(st_addr, &tmA, fb_leader, kb * C::BK, a_row, 0);
+          ptx::tma_load_3d_pair(st_addr + C::A_BYTES, &tmB, fb_leader, kb * C::BK, b_row, tl.e);
+          ++issued;
+          if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok && leader) {  // let the copies already issued land before the pair exits
+        for (int64_t i = issued - 1; i >= 0 && i >= issued - C::STAGES; --i)
+          ptx::mbar_wait(full_bar(static_cast<int>(i % C::STAGES)), static_cast<uint32_t>((i / C::STAGES) & 1),
+                         g.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------------ MMA issuer (leader)
+      const uint32_t idesc = ptx::idesc_bf16(kPairBM, kPairBN);
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_ph = static_cast<uint32_t>((it >> 1) & 1);
+        if (!ptx::mbar_wait(tempty_bar(acc), acc_ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); break; }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kPairBN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait(full_bar(s), ph, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = sbase + s * C::STAGE_BYTES;
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < C::BK / 16; ++k)
+            ptx::mma_bf16_pair(d_tmem, ptx::sdesc_sw128(a_addr + k * 32), ptx::sdesc_sw128(b_addr + k * 32), idesc,
+                               (kb | k) != 0);
+          ptx::mma_commit_pair(empty_bar(s), 0x3);  // frees the stage in both CTAs
+          if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair(tfull_bar(acc), 0x3);  // accumulator rows ready in both CTAs
+      }
+      ptx::mma_commit_pair(drain_bar, 0x1);  // every MMA issued by the pair has completed
+      ptx::mbar_wait(drain_bar, 0, g.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    int it = 0;
+    for (int t = pair; t < total; t += npairs, ++it) {
+      if (*s_abort) break;
+      Tile tl = decode_tile(t, n_tiles_n, kPairBN, s_off, s_mtp, g.E_loc, kPairBM);
+      tl.row0 += 128 * static_cast<int>(rank);             // this CTA's rows of the tile
+      tl.rows = max(0, min(128, tl.rows - 128 * static_cast<int>(rank)));
+      const int acc = it & 1;
+      const uint32_t acc_ph = static_cast<uint32_t>((it >> 1) & 1);
+      int okw = 0;
+      if (lane == 0) okw = ptx::mbar_wait(tfull_bar(acc), acc_ph, g.timeout_ns) ? 1 : 0;
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      if (!okw) { if (lane == 0) gemm_abort(g, s_abort); break; }
+      (void)ptx::mbar_try_wait(tfull_bar(acc), acc_ph);  // completed phase: acquire for every lane
+      ptx::tc_fence_after();
+      const int r = q * 32 + lane;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kPairBN);
+      epilogue_row<EPI>(g, tl, tbase, kPairBN, r, r < tl.rows, static_cast<int64_t>(tl.row0) + r);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+    }
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // neither CTA leaves while its peer may still signal or read it
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+template <int EPI>
+static cudaError_t launch_pair_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, A, false, g.K, a_rows, 1, 128)) return cudaErrorInvalidValue;
+  if (!make_operand_map(&tb, B, false, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
+  auto kern = tc_grouped_gemm_pair_kernel<EPI>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmem::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int grid = num_sms() & ~1;  // whole pairs
+  kern<<<grid, kGemmThreads, PairSmem::SMEM_BYTES, st>>>(ta, tb, g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu,
+                             cudaStream_t st) {
+  return swiglu ? launch_pair_inst<EPI_SWIGLU_BF16>(A, a_rows, B, g, st)
+                : launch_pair_inst<EPI_STORE_BF16>(A, a_rows, B, g, st);
+}
+
+}  // namespace moe

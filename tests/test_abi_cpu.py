@@ -86,11 +86,11 @@ def test_validation_before_any_launch(lib):
     assert L.moe_permute(P, 1, 1, 16, 60, P, P, 2, 0, 8, P, None, P, P, P, P, P, P, 1 << 20, s) == 2
     assert L.moe_permute(P, 1, 2, 16, 64, P, P, 2, 0, 8, P, None, P, P, P, P, P, P, 1 << 20, s) == 1
     # grouped MLP: E_loc out of range, unsupported dtype, workspace too small
-    assert L.moe_grouped_mlp(P, None, P, P, 64, 0, 64, 64, 1, P, None, P, None, P, P, 1 << 20, s) == 1
-    assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 64, 64, 7, P, None, P, None, P, P, 1 << 20, s) == 2
-    assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 64, 64, 1, P, None, P, None, P, P, 16, s) == 3
+    assert L.moe_grouped_mlp(P, None, P, P, 64, 0, 64, 64, 1, P, None, P, None, P, 0, P, 1 << 20, s) == 1
+    assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 64, 64, 7, P, None, P, None, P, 0, P, 1 << 20, s) == 2
+    assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 64, 64, 1, P, None, P, None, P, 0, P, 16, s) == 3
     # MXFP8 without scales
-    assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 128, 128, 2, P, None, P, None, P, P, 1 << 20, s) == 1
+    assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 128, 128, 2, P, None, P, None, P, 0, P, 1 << 20, s) == 1
     # combine: k > 32, bf16 d not a multiple of 8
     assert L.moe_unpermute_combine(P, P, 4, 33, 64, 1, P, s) == 1
     assert L.moe_unpermute_combine(P, P, 4, 2, 60, 1, P, s) == 2
@@ -98,6 +98,7 @@ def test_validation_before_any_launch(lib):
     assert L.moe_layer_forward(P, P, 8, 64, 64, 8, 2, 4, 8, 1, P, None, P, None, P, P, 1 << 30, s) == 1
     assert L.moe_layer_forward(P, P, 8, 64, 64, 8, 2, 0, 8, 1, P, None, P, None, P, P, 64, s) == 3
     # expert GEMMs: workspace missing
-    assert L.moe_expert_gemm2(P, None, P, 64, 4, 64, 64, 1, P, None, P, _null(), 256, s) == 3
+    assert L.moe_expert_gemm2(P, None, P, 64, 4, 64, 64, 1, P, None, P, 0, _null(), 256, s) == 3
+    assert L.moe_rows_hint(4096, 8, 64) == 512 and L.moe_rows_hint(0, 8, 64) == 0
     # device error read: null output
     assert L.moe_get_device_error(P, s, None) == 1

@@ -170,6 +170,7 @@ SMALL = [
     Workload("bf16_e64", 1024, 512, 512, 64, 8, 0, 64, "bf16", ("normal", 0.5)),
     Workload("bf16_ep64", 4096, 384, 256, 256, 8, 0, 4, "bf16"),
     Workload("bf16_zipf", 512, 256, 128, 256, 8, 0, 32, "bf16", ("zipf", 1.1)),
+    Workload("bf16_pair_layer", 2048, 256, 256, 8, 2, 0, 8, "bf16"),   # T*k/E = 512: CTA-pair GEMMs
     Workload("mx_a", 256, 256, 256, 8, 2, 0, 8, "mxfp8"),
     Workload("mx_ragged", 300, 384, 384, 16, 4, 4, 8, "mxfp8"),
     Workload("mx_zipf", 1024, 512, 256, 256, 8, 0, 32, "mxfp8", ("zipf", 1.1)),
@@ -240,10 +241,12 @@ def test_split_calls_equal_fused_call(moe):
     y_fused, _ = moe.moe_layer_forward(xd, lgd, w.E, w.k, w.e0, pw)
     ids, probs = moe.moe_route_topk(lgd, w.k)
     P = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, "bf16")
-    h, hs, _ = moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw)
-    Y2, _ = moe.moe_expert_gemm2(h, hs, P["offsets"], pw)
+    hint = moe.moe_rows_hint(w.T, w.k, w.E)
+    h, hs, _ = moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw,
+                                           rows_hint=hint)
+    Y2, _ = moe.moe_expert_gemm2(h, hs, P["offsets"], pw, rows_hint=hint)
     y = moe.moe_unpermute_combine(Y2, P["pair_to_row"], "bf16")
-    Y2b, _ = moe.moe_grouped_mlp(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw)
+    Y2b, _ = moe.moe_grouped_mlp(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, rows_hint=hint)
     torch.cuda.synchronize()
     assert torch.equal(y, y_fused)
     N = int(P["offsets"][-1])
@@ -314,3 +317,36 @@ def test_full_size_sampled(moe, name):
     yo = oracle_layer(w, x, lg, Wg, Wu, Wd, tokens=tok)
     err = rel_l2(to_np(y)[tok], yo)
     assert err <= TOL[w.dtype], f"{name}: rel L2 {err:.3e}"
+
+
+# ----------------------------------------------------------------------------- CTA-pair kernel
+PAIR_CASES = [
+    # name, counts per expert (k = 1), d, f
+    ("pair_edges", [1, 127, 128, 129, 255, 256, 257, 600], 256, 256),
+    ("pair_tails", [300, 0, 513, 77], 200, 96),      # K and N tails: d % 64 != 0, 2f < 256
+    ("pair_one_expert", [0, 0, 1100, 0], 384, 128),
+]
+
+
+@pytest.mark.parametrize("name,counts,d,f", PAIR_CASES, ids=[c[0] for c in PAIR_CASES])
+def test_pair_kernel_matches_oracle(moe, name, counts, d, f):
+    """bf16 GEMMs on CTA pairs (forced by a large rows_hint) vs the oracle and vs the 1-CTA kernel."""
+    E = len(counts)
+    lg = _forced_logits(counts, E, seed=len(name))
+    T = lg.shape[0]
+    w = Workload(name, T, d, f, E, 1, 0, E, "bf16")
+    x = gen_x(w)
+    Wg, Wu, Wd = gen_weights(w)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), "bf16")
+    ids, probs = moe.moe_route_topk(to_dev(lg), 1)
+    P = moe.moe_permute(to_dev(x), ids, probs, 0, E, "bf16")
+    ys = {}
+    for hint in (1, 4096):  # 1-CTA kernel, CTA-pair kernel
+        Y2, ws = moe.moe_grouped_mlp(P["perm_x"], None, P["offsets"], P["row_prob"], pw, rows_hint=hint)
+        ys[hint] = moe.moe_unpermute_combine(Y2, P["pair_to_row"], "bf16")
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_error(ws) == 0
+    yo = oracle_layer(w, x, lg, Wg, Wu, Wd)
+    for hint, y in ys.items():
+        assert rel_l2(to_np(y), yo) <= TOL["bf16"], hint
+    assert rel_l2(to_np(ys[4096]), to_np(ys[1])) <= 1e-2
