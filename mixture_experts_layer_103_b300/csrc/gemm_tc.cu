@@ -147,26 +147,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t ph = 0;
       int64_t issued = 0;
       bool ok = true;
-      // L2 prefetch cursor: (tile, k-block) kPrefetchKb k-blocks ahead of the loads
-      int pf_t = blockIdx.x, pf_kb = 0;
-      Tile pf_tl = pf_t < total ? decode_tile(pf_t, n_tiles_n, BN, s_off, s_mtp, g.E_loc) : Tile{};
-      auto prefetch_next = [&]() {
-        if (pf_t >= total) return;
-        ptx::tma_prefetch_3d(&tmA, pf_kb * C::BK, pf_tl.row0, 0);
-        ptx::tma_prefetch_3d(tmb, pf_kb * C::BK, pf_tl.n0, pf_tl.e);
-        if (++pf_kb == num_kb) {
-          pf_kb = 0;
-          pf_t += gridDim.x;
-          if (pf_t < total) pf_tl = decode_tile(pf_t, n_tiles_n, BN, s_off, s_mtp, g.E_loc);
-        }
-      };
-      for (int i = 0; i < kPrefetchKb; ++i) prefetch_next();
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile tl = decode_tile(t, n_tiles_n, BN, s_off, s_mtp, g.E_loc);
         const int sfb_bytes = MX ? min(BN, g.n_out - tl.n0) / 128 * 512 : 0;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (*s_abort) { ok = false; break; }
-          prefetch_next();
           if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
           const uint32_t fb = full_bar(s);
           const uint32_t st_addr = sbase + C::OFF_PIPE + s * stage_bytes;

@@ -56,11 +56,6 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles_n, int bn, const 
   return r;
 }
 
-// k-blocks the producer prefetches into L2 ahead of its TMA loads (continuing into its
-// next tile), so that first-touch weight reads from DRAM are hidden behind L2 latency
-// rather than stalling the shared-memory ring.
-constexpr int kPrefetchKb = 8;
-
 __device__ __forceinline__ void gemm_abort(const GemmArgs& g, volatile int* s_abort) {
   *s_abort = 1;
   set_device_error(g.err, MOE_ERR_TIMEOUT);

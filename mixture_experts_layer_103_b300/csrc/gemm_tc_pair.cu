@@ -12,11 +12,9 @@
 //   * the leader's commits arrive on the empty / accumulator-full barriers of both CTAs
 //     (multicast); both CTAs' epilogue warps drain their own TMEM rows and arrive on the
 //     leader's accumulator-empty barrier.
-// Per SM and 64-wide K step this stages 32 KB instead of the 48 KB of a 1-CTA 128 x 256
-// tile, so the same shared memory holds a 6-deep ring (more bytes in flight per FLOP)
-// and each weight byte fetched from L2 feeds two SMs.  Rows of a 256-row tile past the
-// expert's segment are computed and discarded, so the pair pays more padding on small
-// segments; the host picks it only when experts hold many rows.
+// Per SM and 64-wide K step this moves 32 KB into shared memory and reads 32 KB of
+// operands into the tensor core, half the shared-memory traffic of a 1-CTA 128 x 256
+// tile, which is what bounds the 1-CTA kernel.
 #include "gemm_tc.cuh"
 
 namespace moe {
@@ -97,27 +95,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t ph = 0;
       int64_t issued = 0;
       bool ok = true;
-      // L2 prefetch cursor over this CTA's halves, kPrefetchKb k-blocks ahead of the loads
-      int pf_t = pair, pf_kb = 0;
-      Tile pf_tl = pf_t < total ? decode_tile(pf_t, n_tiles_n, kPairBN, s_off, s_mtp, g.E_loc, kPairBM) : Tile{};
-      auto prefetch_next = [&]() {
-        if (pf_t >= total) return;
-        ptx::tma_prefetch_3d(&tmA, pf_kb * C::BK, pf_tl.row0 + 128 * static_cast<int>(rank), 0);
-        ptx::tma_prefetch_3d(&tmB, pf_kb * C::BK, pf_tl.n0 + 128 * static_cast<int>(rank), pf_tl.e);
-        if (++pf_kb == num_kb) {
-          pf_kb = 0;
-          pf_t += npairs;
-          if (pf_t < total) pf_tl = decode_tile(pf_t, n_tiles_n, kPairBN, s_off, s_mtp, g.E_loc, kPairBM);
-        }
-      };
-      for (int i = 0; i < kPrefetchKb; ++i) prefetch_next();
       for (int t = pair; t < total && ok; t += npairs) {
         const Tile tl = decode_tile(t, n_tiles_n, kPairBN, s_off, s_mtp, g.E_loc, kPairBM);
         const int a_row = tl.row0 + 128 * static_cast<int>(rank);
         const int b_row = tl.n0 + 128 * static_cast<int>(rank);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (*s_abort) { ok = false; break; }
-          prefetch_next();
           if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
           const uint32_t fb_leader = ptx::mapa_shared(full_bar(s), 0);
           if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * C::STAGE_BYTES);
