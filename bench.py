@@ -405,7 +405,7 @@ def run_ours(args, w):
         roof = {"bound": "hbm", "achieved": by / t_s / 1e9, "peak": hbm, "unit": "GB/s",
                 "frac": by / t_s / 1e9 / hbm}
     kname = ("simt_grouped_gemm_kernel" if w.dtype == "f32" else
-             "tc_grouped_gemm_pair_kernel" if (w.dtype == "bf16" and hint >= 384) else "tc_grouped_gemm_kernel")
+             "tc_grouped_gemm_pair_kernel" if (w.dtype == "bf16" and hint >= 2048) else "tc_grouped_gemm_kernel")
     roof.update({"kernel": f"{kname} ({dom})", "traffic": recorded_traffic(dom, w.name),
                  "peak_kind": pk_kind + (" (bf16 x2 nominal fp8 ratio)" if w.dtype == "mxfp8" else "")})
     t_roof = max(bf["layer_flops"] / (tpeak * 1e12), bf["layer_bytes"] / (hbm * 1e9))

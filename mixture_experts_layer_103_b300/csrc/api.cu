@@ -83,8 +83,10 @@ static moe_status check_mlp_shape(int d, int f, int E_loc, moe_dtype dt) {
 }
 
 // Expected rows per local expert at or above which bf16 GEMMs run on CTA pairs (256-row
-// tiles); below it the 1-CTA kernel with its device-chosen tile width serves better.
-constexpr int kPairRowsThreshold = 384;
+// tiles).  Measured on B300 the pair kernel did not beat the 1-CTA kernel at 512 or 1024
+// rows per expert (its 256-row tiles pad ragged segments twice as much), so it is only
+// chosen for very tall segments; callers can force either with rows_hint.
+constexpr int kPairRowsThreshold = 2048;
 
 static bool use_pair(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint) {
   const int64_t rows = rows_hint > 0 ? rows_hint : n_cap / (E_loc > 0 ? E_loc : 1);
