@@ -50,6 +50,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
+    p.add_argument("--rows-hint", type=int, default=None,
+                   help="expected rows per local expert passed to the grouped GEMMs (default T*k/E); "
+                        "it selects the GEMM kernel shape (>= 2048: CTA pairs, bf16)")
     return p.parse_args()
 
 
@@ -300,7 +303,7 @@ def run_ours(args, w):
     names = ["route_topk", "permute", "gemm1_swiglu", "gemm2", "combine"]
     n_ev = len(names) + 1
 
-    hint = moe.moe_rows_hint(T, k, w.E)
+    hint = args.rows_hint if args.rows_hint is not None else moe.moe_rows_hint(T, k, w.E)
 
     def step(evs):
         evs[0].record()

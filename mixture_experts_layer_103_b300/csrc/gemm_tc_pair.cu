@@ -12,9 +12,11 @@
 //   * the leader's commits arrive on the empty / accumulator-full barriers of both CTAs
 //     (multicast); both CTAs' epilogue warps drain their own TMEM rows and arrive on the
 //     leader's accumulator-empty barrier.
-// Per SM and 64-wide K step this moves 32 KB into shared memory and reads 32 KB of
-// operands into the tensor core, half the shared-memory traffic of a 1-CTA 128 x 256
-// tile, which is what bounds the 1-CTA kernel.
+// Per SM and 64-wide K step this stages 32 KB instead of the 48 KB of a 1-CTA 128 x 256
+// tile, so the same shared memory holds a 6-deep ring (more bytes in flight per FLOP)
+// and each weight byte fetched from L2 feeds two SMs.  Rows of a 256-row tile past the
+// expert's segment are computed and discarded, so the pair pays more padding on small
+// segments; the host picks it only when experts hold many rows.
 #include "gemm_tc.cuh"
 
 namespace moe {
