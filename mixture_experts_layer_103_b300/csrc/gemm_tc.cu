@@ -48,7 +48,8 @@ struct GemmSmem {
   static constexpr int UMMA_K = MX ? 32 : 16;               // K elements per MMA
   static constexpr int OFF_PIPE = 0;
   static constexpr int OFF_SF = OFF_PIPE + PIPE_BYTES;
-  static constexpr int OFF_BAR = OFF_SF + MAX_STAGES * SF_STAGE_BYTES;
+  static constexpr int OFF_EPI = OFF_SF + MAX_STAGES * SF_STAGE_BYTES;  // epilogue staging
+  static constexpr int OFF_BAR = OFF_EPI + kEpiBytes;
   static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TAB = OFF_MISC + 16;
@@ -236,11 +237,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!okw) { if (lane == 0) gemm_abort(g, s_abort); break; }
       (void)ptx::mbar_try_wait(tfull_bar(acc), acc_ph);  // completed phase: acquire for every lane
       ptx::tc_fence_after();
-      const int r = q * 32 + lane;
-      const bool valid = r < tl.rows;
-      const int64_t grow = static_cast<int64_t>(tl.row0) + r;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_row<EPI>(g, tl, tbase, BN, r, valid, grow);
+      epilogue_warp<EPI>(g, tl, tbase, BN, q, lane, smem + C::OFF_EPI + (warp - 2) * kEpiWarpBytes);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));

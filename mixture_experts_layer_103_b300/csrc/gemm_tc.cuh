@@ -61,34 +61,68 @@ __device__ __forceinline__ void gemm_abort(const GemmArgs& g, volatile int* s_ab
   set_device_error(g.err, MOE_ERR_TIMEOUT);
 }
 
-// Epilogue of one accumulator row (one thread = one TMEM lane = one output row r of a
-// 128-row tile): bf16 store of BN columns (GEMM2), or the fused scaled SwiGLU on BN/64
-// blocks of 32 gate + 32 up columns with bf16 or MXFP8 (one 32-value block per thread)
-// output (GEMM1).  tbase = TMEM address of this warp's lane quarter and accumulator.
+// Epilogue staging: each epilogue warp owns 32 rows x 80 bytes of shared memory (64 data
+// bytes per row + 16 bytes of padding to spread the banks).  A warp's 32 threads each hold
+// one output row of a 32-column block in registers; they write it to the staging rows and
+// read it back column-chunk-major, so each global store instruction covers whole 64-byte
+// (or 32-byte) row segments of 8 (or 16) rows instead of 32 scattered 16-byte pieces.
+constexpr int kEpiRowBytes = 80;
+constexpr int kEpiWarpBytes = 32 * kEpiRowBytes;
+constexpr int kEpiBytes = 4 * kEpiWarpBytes;  // 4 epilogue warps
+
+// v: this lane's row, CHUNKS x 16 bytes.  g0: global address of the warp's first row at
+// the block's first column; ld: bytes between rows.  Rows >= rows_valid and 16-byte
+// chunks >= chunks_valid are not written.
+template <int CHUNKS>
+__device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint4 (&v)[CHUNKS], int lane, uint8_t* g0,
+                                                int64_t ld, int rows_valid, int chunks_valid) {
+  uint4* mine = reinterpret_cast<uint4*>(stage + lane * kEpiRowBytes);
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) mine[c] = v[c];
+  __syncwarp();
+  constexpr int kRowsPerStore = 32 / CHUNKS;
+#pragma unroll
+  for (int j = 0; j < CHUNKS; ++j) {
+    const int r = j * kRowsPerStore + lane / CHUNKS;
+    const int c = lane % CHUNKS;
+    const uint4 val = *reinterpret_cast<const uint4*>(stage + r * kEpiRowBytes + c * 16);
+    if (r < rows_valid && c < chunks_valid) *reinterpret_cast<uint4*>(g0 + r * ld + c * 16) = val;
+  }
+  __syncwarp();
+}
+
+// Epilogue of one 32-row slab of an accumulator tile (one warp, one TMEM lane per thread):
+// bf16 store of BN columns (GEMM2), or the fused scaled SwiGLU on BN/64 blocks of 32 gate
+// + 32 up columns with bf16 or MXFP8 (one 32-value block per thread) output (GEMM1).
+// tbase = TMEM address of this warp's lane quarter and accumulator; q = lane quarter;
+// tl.row0/tl.rows describe the 128-row tile the slab belongs to.
 template <int EPI>
-__device__ __forceinline__ void epilogue_row(const GemmArgs& g, const Tile& tl, uint32_t tbase, int BN, int r,
-                                             bool valid, int64_t grow) {
+__device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl, uint32_t tbase, int BN, int q,
+                                              int lane, uint8_t* stage) {
+  const int r = q * 32 + lane;                         // row within the tile
+  const int rows_valid = max(0, min(32, tl.rows - q * 32));
+  const int64_t row_first = static_cast<int64_t>(tl.row0) + q * 32;
   if constexpr (EPI == EPI_STORE_BF16) {
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
+    uint8_t* out = static_cast<uint8_t*>(g.out);
+    const int64_t ld = g.ld_out * 2;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t v[32];
       ptx::tmem_ld32(tbase + c, v);
       ptx::tmem_ld_wait();
       const int n = tl.n0 + c;
-      if (valid && n < g.n_out) {
-        uint4* dst = reinterpret_cast<uint4*>(out + grow * g.ld_out + n);
+      uint4 pk[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (n + 8 * j < g.n_out)
-            dst[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-                                pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                                pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                                pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
-      }
+      for (int j = 0; j < 4; ++j)
+        pk[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+      const int chunks = max(0, min(4, (g.n_out - n) / 8));
+      warp_store_rows<4>(stage, pk, lane, out + row_first * ld + static_cast<int64_t>(n) * 2, ld, rows_valid, chunks);
     }
   } else {
-    const float p = valid ? __ldg(g.row_prob + grow) : 0.0f;
+    const float p = r < tl.rows ? __ldg(g.row_prob + row_first + lane) : 0.0f;
     const int fdim = g.n_out / 2;
 #pragma unroll 1
     for (int sb = 0; sb < BN / 64; ++sb) {
@@ -103,29 +137,31 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& g, const Tile& tl, 
         const float gg = __uint_as_float(gv[i]);
         h[i] = p * (gg / (1.0f + __expf(-gg))) * __uint_as_float(uv[i]);
       }
-      if (valid && fc < fdim) {
-        if constexpr (EPI == EPI_SWIGLU_BF16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(g.out) + grow * g.ld_out + fc);
+      if constexpr (EPI == EPI_SWIGLU_BF16) {
+        uint4 pk[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pack_bf16x2(h[8 * j + 0], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
-                                pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
-        } else {
-          float amax = 0.0f;
+        for (int j = 0; j < 4; ++j)
+          pk[j] = make_uint4(pack_bf16x2(h[8 * j + 0], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
+                             pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
+        const int64_t ld = g.ld_out * 2;
+        warp_store_rows<4>(stage, pk, lane,
+                           static_cast<uint8_t*>(g.out) + row_first * ld + static_cast<int64_t>(fc) * 2, ld,
+                           rows_valid, fc < fdim ? 4 : 0);
+      } else {
+        float amax = 0.0f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
-          const int X = mx_exponent(amax);
-          const float inv = mx_inv_scale(X);
-          uint32_t w[8];
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+        const int X = mx_exponent(amax);
+        const float inv = mx_inv_scale(X);
+        uint32_t w[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            w[j] = static_cast<uint32_t>(e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv)) |
-                   (static_cast<uint32_t>(e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv)) << 16);
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(g.out) + grow * g.ld_out + fc);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          g.out_sf[sf_act_offset(tl.mt, r, fc, fdim)] = static_cast<uint8_t>(X + 127);
-        }
+        for (int j = 0; j < 8; ++j)
+          w[j] = static_cast<uint32_t>(e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv)) |
+                 (static_cast<uint32_t>(e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv)) << 16);
+        const uint4 pk[2] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7])};
+        warp_store_rows<2>(stage, pk, lane, static_cast<uint8_t*>(g.out) + row_first * g.ld_out + fc, g.ld_out,
+                           rows_valid, fc < fdim ? 2 : 0);
+        if (r < tl.rows && fc < fdim) g.out_sf[sf_act_offset(tl.mt, r, fc, fdim)] = static_cast<uint8_t>(X + 127);
       }
     }
   }

@@ -27,7 +27,8 @@ struct PairSmem {
   static constexpr int B_BYTES = 128 * kRowBytes;  // this CTA's half of the 256 B rows
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BK = 64;                    // bf16 K elements per stage
-  static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
+  static constexpr int OFF_EPI = STAGES * STAGE_BYTES;  // epilogue staging
+  static constexpr int OFF_BAR = OFF_EPI + kEpiBytes;
   static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TAB = OFF_MISC + 16;
@@ -168,9 +169,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (!okw) { if (lane == 0) gemm_abort(g, s_abort); break; }
       (void)ptx::mbar_try_wait(tfull_bar(acc), acc_ph);  // completed phase: acquire for every lane
       ptx::tc_fence_after();
-      const int r = q * 32 + lane;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kPairBN);
-      epilogue_row<EPI>(g, tl, tbase, kPairBN, r, r < tl.rows, static_cast<int64_t>(tl.row0) + r);
+      epilogue_warp<EPI>(g, tl, tbase, kPairBN, q, lane, smem + C::OFF_EPI + (warp - 2) * kEpiWarpBytes);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
