@@ -1,16 +1,19 @@
 // Step 1: top-k routing over fp32 router logits ("Wide-EP ... NVIDIA" explainer, section
 // "MoE basics": the router chooses, per token, the experts it uses; DeepSeek-R1 picks 8 of
-// 256).  One warp per token: each lane holds E/32 logits as 64-bit keys
-// (order-preserving fp32 bits << 32 | ~expert_id), k rounds of a warp max-reduction pick
-// the winners in descending order with ties going to the lower id, then the softmax over
-// the k chosen logits gives the probabilities.  The logits are read once, coalesced.
+// 256).  One warp per token; each lane holds E/32 logits as 32-bit order-preserving keys
+// and keeps its local maximum.  Each of the k rounds takes the warp maximum of the lanes'
+// maxima with one redux instruction, then the lowest expert id holding that value with a
+// second one (ties go to the lower id); only the winning lane drops the entry and rescans
+// its few keys.  The softmax over the k chosen logits gives the probabilities.  The
+// logits are read once, coalesced.
 #include "moe_common.cuh"
 
 namespace moe {
 
 constexpr int kRouteWarps = 8;
 
-// Order-preserving map of a non-NaN fp32 to uint32 (-0.0 folded onto +0.0).
+// Order-preserving map of a non-NaN fp32 to a non-zero uint32 (-0.0 folded onto +0.0);
+// 0 marks an empty or already chosen slot.
 __device__ __forceinline__ uint32_t ordered_bits(float v) {
   uint32_t u = __float_as_uint(v);
   if ((u << 1) == 0) u = 0;  // +-0.0 -> +0.0
@@ -25,37 +28,36 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const floa
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + (threadIdx.x >> 5);
   if (t >= T) return;
   const float* row = logits + t * E;
-  unsigned long long key[VPL];
+  uint32_t key[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
-    key[i] = 0ull;  // below every real key (real keys have a non-zero high word or id bits)
-    if (e < E) {
-      const float v = __ldg(row + e);
-      key[i] = (static_cast<unsigned long long>(ordered_bits(v)) << 32) | static_cast<uint32_t>(~e);
-    }
+    key[i] = e < E ? ordered_bits(__ldg(row + e)) : 0u;
   }
+  uint32_t lmax = key[0];
+#pragma unroll
+  for (int i = 1; i < VPL; ++i) lmax = max(lmax, key[i]);
   int my_id = 0;
-  float my_val = 0.0f;
   for (int j = 0; j < k; ++j) {
-    unsigned long long best = key[0];
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, lmax);
+    uint32_t cand = 0xffffffffu;  // lowest id in this lane holding mx
 #pragma unroll
-    for (int i = 1; i < VPL; ++i) best = key[i] > best ? key[i] : best;
+    for (int i = VPL - 1; i >= 0; --i)
+      if (key[i] == mx) cand = static_cast<uint32_t>(lane + 32 * i);
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    if (cand == win) {  // the winning lane drops the entry and rescans
+      lmax = 0u;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-      best = o > best ? o : best;
+      for (int i = 0; i < VPL; ++i) {
+        if (lane + 32 * i == static_cast<int>(win)) key[i] = 0u;
+        lmax = max(lmax, key[i]);
+      }
     }
-    const int win = static_cast<int>(~static_cast<uint32_t>(best));
-#pragma unroll
-    for (int i = 0; i < VPL; ++i)  // remove the winner
-      if (lane + 32 * i == win) key[i] = 0ull;
-    if (lane == j) {
-      my_id = win;
-      my_val = __ldg(row + win);
-    }
+    // win < E for every non-NaN row; the clamp keeps NaN rows (unspecified result) in bounds
+    if (lane == j) my_id = min(static_cast<int>(win), E - 1);
   }
   // softmax over the k chosen logits; lane 0 holds the largest one
+  const float my_val = lane < k ? __ldg(row + my_id) : 0.0f;
   const float l0 = __shfl_sync(0xffffffffu, my_val, 0);
   const float w = (lane < k) ? expf(my_val - l0) : 0.0f;
   float s = w;
