@@ -291,11 +291,7 @@ def run_ours(args, w):
     T, d, k, E_loc, e0 = w.T, w.d, w.k, w.E_loc, w.e0
     ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
     probs = torch.empty(T, k, dtype=torch.float32, device="cuda")
-    hint = args.rows_hint if args.rows_hint is not None else moe.moe_rows_hint(T, k, w.E)
-    # bf16 on the 1-CTA GEMM: GEMM1 gathers its rows from x (as moe_layer_forward does),
-    # the permute builds the maps only
-    gathered = w.dtype == "bf16" and hint < 2048
-    P = moe.alloc_permute(T, d, k, E_loc, xd.dtype, w.dtype, rows=not gathered)
+    P = moe.alloc_permute(T, d, k, E_loc, xd.dtype, w.dtype)
     ws_perm = moe.workspace(moe.moe_permute_workspace_size(T, k, E_loc))
     h, hs = moe.alloc_h(moe.n_cap(T, k, E_loc), pw)
     Y2 = torch.empty(moe.n_cap(T, k, E_loc), d, dtype=moe.torch_dtype(w.dtype), device="cuda")
@@ -307,18 +303,16 @@ def run_ours(args, w):
     names = ["route_topk", "permute", "gemm1_swiglu", "gemm2", "combine"]
     n_ev = len(names) + 1
 
+    hint = args.rows_hint if args.rows_hint is not None else moe.moe_rows_hint(T, k, w.E)
+
     def step(evs):
         evs[0].record()
         moe.moe_route_topk(lgd, k, ids, probs)
         evs[1].record()
         moe.moe_permute(xd, ids, probs, e0, E_loc, w.dtype, ws=ws_perm, out=P)
         evs[2].record()
-        if gathered:
-            moe.moe_expert_gemm1_swiglu_gather(xd, P["row_src_token"], P["offsets"], P["row_prob"], pw, h=h, ws=ws_g,
-                                               rows_hint=hint)
-        else:
-            moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, h=h,
-                                        h_scale=hs, ws=ws_g, rows_hint=hint)
+        moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, h=h,
+                                    h_scale=hs, ws=ws_g, rows_hint=hint)
         evs[3].record()
         moe.moe_expert_gemm2(h, hs, P["offsets"], pw, Y2=Y2, ws=ws_g, rows_hint=hint)
         evs[4].record()

@@ -114,9 +114,7 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* top
  *   x            device [T, d]  x_dtype MOE_F32 or MOE_BF16
  *   perm_dtype   element type of perm_x: MOE_F32 (x fp32), MOE_BF16 (x bf16) or MOE_MXFP8
  *                (x bf16; rows quantised while copied, scales to perm_x_scale)
- *   perm_x       device [N_cap, d], N_cap = T * min(k, E_loc); rows >= N untouched.  May be
- *                NULL: then only the maps are built and no row is copied (for a GEMM1
- *                that gathers its rows from x, moe_expert_gemm1_swiglu_gather)
+ *   perm_x       device [N_cap, d], N_cap = T * min(k, E_loc); rows >= N untouched
  *   perm_x_scale device, MOE_MXFP8 only (else NULL): SF tile layout, K = d,
  *                moe_mx_act_scale_bytes(N_cap, d, E_loc) bytes
  *   counts [E_loc], offsets [E_loc+1], row_src_token [N_cap], row_prob [N_cap] (fp32),
@@ -215,17 +213,6 @@ moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t
                             int d, int f, moe_dtype dtype, const void* Wd_packed, const uint8_t* Wd_scale, void* Y2,
                             int rows_hint, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 size_t moe_expert_gemm_workspace_size(void);
-
-/* GEMM1 + scaled SwiGLU reading its A rows straight from x instead of a permuted copy:
- * permuted row i is x[row_src_token[i]] (the single-GPU analogue of dispatching each
- * token to its experts [WEP "Prerequisite ..."], folded into the expert GEMM).  Same
- * result as moe_permute + moe_expert_gemm1_swiglu, without writing or re-reading perm_x.
- *   x [T, d] bf16, row_src_token [N_cap] (from moe_permute), other arguments as for
- *   moe_expert_gemm1_swiglu.  MOE_BF16 only (MXFP8 needs the quantised permuted rows). */
-moe_status moe_expert_gemm1_swiglu_gather(const void* x, int T, const int32_t* row_src_token, const int32_t* offsets,
-                                          const float* row_prob, int64_t N_cap, int E_loc, int d, int f,
-                                          moe_dtype dtype, const void* Wgu_packed, void* h, int rows_hint,
-                                          void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* Unpermute + combine (step 5) [WEP "MoE basics": results of the chosen experts are
  * summed; "Prerequisite ...": combine].

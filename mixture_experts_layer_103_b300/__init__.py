@@ -60,7 +60,6 @@ _SIGS = {
     "moe_grouped_mlp_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),
-    "moe_expert_gemm1_swiglu_gather": (_I, [_P, _I, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm_workspace_size": (_SZ, []),
     "moe_unpermute_combine": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_layer_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -123,13 +122,10 @@ def moe_route_topk(logits: torch.Tensor, k: int, topk_ids=None, topk_probs=None)
     return ids, probs
 
 
-def alloc_permute(T: int, d: int, k: int, E_loc: int, x_dtype: torch.dtype, perm_dtype="bf16", device="cuda",
-                  rows: bool = True) -> dict:
-    """Output buffers of moe_permute (rows=False: maps only, no perm_x)."""
+def alloc_permute(T: int, d: int, k: int, E_loc: int, x_dtype: torch.dtype, perm_dtype="bf16", device="cuda") -> dict:
+    """Output buffers of moe_permute."""
     cap = n_cap(T, k, E_loc)
-    if not rows:
-        perm_x, perm_sf = None, None
-    elif _dt(perm_dtype) == MOE_MXFP8:
+    if _dt(perm_dtype) == MOE_MXFP8:
         perm_x = torch.empty(cap, d, dtype=torch.uint8, device=device)
         perm_sf = torch.empty(max(1, _lib.moe_mx_act_scale_bytes(cap, d, E_loc)), dtype=torch.uint8, device=device)
     else:
@@ -245,20 +241,6 @@ def moe_expert_gemm1_swiglu(perm_x, perm_x_scale, offsets, row_prob, pw: PackedW
         _ptr(perm_x), _ptr(perm_x_scale), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f, pw.dtype,
         _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(h), _ptr(h_scale), int(rows_hint), _ptr(ws), ws.numel(), _stream()))
     return h, h_scale, ws
-
-
-def moe_expert_gemm1_swiglu_gather(x, row_src_token, offsets, row_prob, pw: PackedWeights, h=None, ws=None,
-                                   rows_hint=0):
-    """GEMM1 + scaled SwiGLU with A rows gathered from x by row_src_token (bf16)."""
-    T = x.shape[0]
-    cap = row_src_token.shape[0]
-    if h is None:
-        h, _ = alloc_h(cap, pw, x.device)
-    ws = ws if ws is not None else workspace(_lib.moe_expert_gemm_workspace_size(), x.device)
-    _check("moe_expert_gemm1_swiglu_gather", _lib.moe_expert_gemm1_swiglu_gather(
-        _ptr(x), T, _ptr(row_src_token), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f, pw.dtype,
-        _ptr(pw.Wgu), _ptr(h), int(rows_hint), _ptr(ws), ws.numel(), _stream()))
-    return h, ws
 
 
 def moe_expert_gemm2(h, h_scale, offsets, pw: PackedWeights, Y2=None, ws=None, rows_hint=0):

@@ -26,9 +26,6 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
 cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
                             int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
                             uint64_t timeout_ns, cudaStream_t st);
-cudaError_t launch_tc_gemm1_gather(const void* x, int T, const int32_t* row_src_token, const int32_t* offsets,
-                                   const float* row_prob, int E_loc, int d, int f, const void* Wgu, void* h,
-                                   int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
 
@@ -231,14 +228,14 @@ static moe_status check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm
   if (T < 0 || d <= 0 || k < 1 || k > 32 || e0 < 0 || E_loc < 1 || E_loc > 1024 || e0 > (1 << 30))
     return MOE_ERR_INVALID_ARG;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!x || !ids || !probs || !rst || !rp || !p2r)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !ids || !probs || !perm_x || !rst || !rp || !p2r)) return MOE_ERR_INVALID_ARG;
   const bool ok_types = (x_dtype == MOE_F32 && perm_dtype == MOE_F32) || (x_dtype == MOE_BF16 && perm_dtype == MOE_BF16) ||
                         ((x_dtype == MOE_BF16 || x_dtype == MOE_F32) && perm_dtype == MOE_MXFP8);
   if (!ok_types) return MOE_ERR_UNSUPPORTED;
   if ((x_dtype == MOE_BF16 && d % 8 != 0) || (x_dtype == MOE_F32 && d % 4 != 0)) return MOE_ERR_UNSUPPORTED;
-  if (perm_dtype == MOE_MXFP8 && d % 128 != 0) return MOE_ERR_UNSUPPORTED;
-  if (perm_dtype == MOE_MXFP8 && T > 0 && perm_x && !perm_sf) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!aligned16(x) || (perm_x && !aligned16(perm_x)))) return MOE_ERR_INVALID_ARG;
+  if (perm_dtype == MOE_MXFP8 && (d % 128 != 0 || (T > 0 && !perm_sf))) return perm_sf ? MOE_ERR_UNSUPPORTED
+                                                                                          : MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(x) || !aligned16(perm_x))) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -339,27 +336,6 @@ moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_sca
                                Wgu_scale, h, h_scale, err, rows_hint, stream));
 }
 
-moe_status moe_expert_gemm1_swiglu_gather(const void* x, int T, const int32_t* row_src_token, const int32_t* offsets,
-                                          const float* row_prob, int64_t N_cap, int E_loc, int d, int f,
-                                          moe_dtype dtype, const void* Wgu_packed, void* h, int rows_hint,
-                                          void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-  (void)rows_hint;
-  moe_status s = check_mlp_shape(d, f, E_loc, dtype);
-  if (s != MOE_OK) return s;
-  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-  if (T < 0 || N_cap < 0 || N_cap > (int64_t(1) << 31) - 1 || !offsets) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && N_cap > 0 &&
-      (!x || !row_src_token || !row_prob || !Wgu_packed || !h || !aligned16(x) || !aligned16(Wgu_packed) ||
-       !aligned16(h)))
-    return MOE_ERR_INVALID_ARG;
-  if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
-  int32_t* err = static_cast<int32_t*>(workspace);
-  if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (T == 0 || N_cap == 0) return MOE_OK;
-  return cuda_status(launch_tc_gemm1_gather(x, T, row_src_token, offsets, row_prob, E_loc, d, f, Wgu_packed, h, err,
-                                            kTimeoutNs, stream));
-}
-
 moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t* offsets, int64_t N_cap, int E_loc,
                             int d, int f, moe_dtype dtype, const void* Wd_packed, const uint8_t* Wd_scale, void* Y2,
                             int rows_hint, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
@@ -407,23 +383,12 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
   const moe_dtype x_dtype = dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
   cudaError_t e = cudaMemsetAsync(w.err, 0, 4, stream);
   if (e == cudaSuccess) e = launch_route_topk(logits, T, E, k, w.topk_ids, w.topk_probs, stream);
-  const int hint = moe_rows_hint(T, k, E);
-  // bf16 on the 1-CTA kernel: GEMM1 gathers its A rows from x, so the permute only
-  // builds the maps and the permuted copy of x is never written
-  const bool gathered = dtype == MOE_BF16 && !use_pair(dtype, n_cap, E_loc, hint);
   if (e == cudaSuccess)
-    e = launch_permute(x, x_dtype, dtype, T, d, w.topk_ids, w.topk_probs, k, e0, E_loc, gathered ? nullptr : w.perm_x,
-                       w.perm_sf, w.counts, w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
-  if (e == cudaSuccess && gathered && n_cap > 0) {
-    MlpScratch sc = carve_mlp(w.mlp, n_cap, f, dtype);
-    e = launch_tc_gemm1_gather(x, T, w.row_src_token, w.offsets, w.row_prob, E_loc, d, f, Wgu_packed, sc.h, w.err,
-                               kTimeoutNs, stream);
-    if (e == cudaSuccess)
-      e = run_gemm2(sc.h, sc.h_sf, w.offsets, n_cap, E_loc, d, f, dtype, Wd_packed, Wd_scale, w.Y2, w.err, hint, stream);
-  } else if (e == cudaSuccess) {
+    e = launch_permute(x, x_dtype, dtype, T, d, w.topk_ids, w.topk_probs, k, e0, E_loc, w.perm_x, w.perm_sf, w.counts,
+                       w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
+  if (e == cudaSuccess)
     e = run_mlp(w.perm_x, w.perm_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale,
-                Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, hint, stream);
-  }
+                Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, moe_rows_hint(T, k, E), stream);
   if (e == cudaSuccess) e = launch_combine(w.Y2, w.pair_to_row, T, k, d, dtype, y, stream);
   return cuda_status(e);
 }

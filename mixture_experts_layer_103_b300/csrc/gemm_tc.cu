@@ -49,8 +49,7 @@ struct GemmSmem {
   static constexpr int OFF_PIPE = 0;
   static constexpr int OFF_SF = OFF_PIPE + PIPE_BYTES;
   static constexpr int OFF_EPI = OFF_SF + MAX_STAGES * SF_STAGE_BYTES;  // epilogue staging
-  static constexpr int OFF_IDX = OFF_EPI + kEpiBytes;  // gathered A: 2 x 128 source rows
-  static constexpr int OFF_BAR = OFF_IDX + 2 * 128 * 4;
+  static constexpr int OFF_BAR = OFF_EPI + kEpiBytes;
   static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TAB = OFF_MISC + 16;
@@ -85,10 +84,7 @@ struct BMaps {
   CUtensorMap b256, b128, b64;
 };
 
-// GATHER: A rows are read straight from x [T, d] through a one-row-box 2-D map with
-// tile::gather4 copies, indexed by the permutation's source-token list, so the permuted
-// copy of x is never materialised (bf16 only).
-template <bool MX, int EPI, bool GATHER>
+template <bool MX, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BMaps tmB,
                            const GemmArgs g) {
@@ -144,58 +140,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int total = m_tiles * n_tiles_n;
   const int num_kb = (g.K + C::BK - 1) / C::BK;
 
-  if (warp == 0 && GATHER) {
-    // ------------------------------------------------------------------ TMA producer (gathered A)
-    // The whole warp walks the tiles: all lanes stage the next tile's 128 source rows in
-    // shared memory while lane 0 issues the copies of the current one.
-    int* s_idx = reinterpret_cast<int*>(smem + C::OFF_IDX);
-    auto stage_rows = [&](int tt, int buf) {
-      if (tt >= total) return;
-      const Tile t2 = decode_tile(tt, n_tiles_n, BN, s_off, s_mtp, g.E_loc);
-      for (int i = lane; i < kBM; i += 32) s_idx[buf * kBM + i] = i < t2.rows ? __ldg(g.a_rows + t2.row0 + i) : 0;
-    };
-    int s = 0;
-    uint32_t ph = 0;
-    int64_t issued = 0;
-    bool ok = true;
-    int it = 0;
-    stage_rows(blockIdx.x, 0);
-    __syncwarp();
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-      const Tile tl = decode_tile(t, n_tiles_n, BN, s_off, s_mtp, g.E_loc);
-      const int* idx = s_idx + (it & 1) * kBM;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        int okl = 1;
-        if (lane == 0) {
-          if (*s_abort) {
-            okl = 0;
-          } else if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) {
-            gemm_abort(g, s_abort);
-            okl = 0;
-          } else {
-            const uint32_t fb = full_bar(s);
-            const uint32_t st_addr = sbase + C::OFF_PIPE + s * stage_bytes;
-            ptx::mbar_arrive_expect_tx(fb, stage_bytes);
-#pragma unroll 4
-            for (int q4 = 0; q4 < kBM / 4; ++q4)
-              ptx::tma_gather4(st_addr + q4 * 4 * kRowBytes, &tmA, fb, kb * C::BK, idx[4 * q4], idx[4 * q4 + 1],
-                               idx[4 * q4 + 2], idx[4 * q4 + 3]);
-            ptx::tma_load_3d(st_addr + C::A_BYTES, tmb, fb, kb * C::BK, tl.n0, tl.e);
-          }
-        }
-        okl = __shfl_sync(0xffffffffu, okl, 0);
-        if (!okl) { ok = false; break; }
-        ++issued;
-        if (++s == stages) { s = 0; ph ^= 1u; }
-        if (kb == 0) stage_rows(t + gridDim.x, (it + 1) & 1);  // next tile's rows, other buffer
-      }
-      __syncwarp();
-    }
-    if (!ok && lane == 0) {  // let the copies already issued land before the CTA exits
-      for (int64_t i = issued - 1; i >= 0 && i >= issued - stages; --i)
-        ptx::mbar_wait(full_bar(static_cast<int>(i % stages)), static_cast<uint32_t>((i / stages) & 1), g.timeout_ns);
-    }
-  } else if (warp == 0) {
+  if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ TMA producer
       ptx::prefetch_tmap(tmb);
@@ -339,31 +284,17 @@ bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, ui
   return r == CUDA_SUCCESS;
 }
 
-// 2-D map over x [rows, K] bf16 with a one-row box (128 bytes) for tile::gather4 loads.
-static bool make_gather_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {K, rows};
-  const cuuint64_t strides[1] = {K * 2};
-  const cuuint32_t box[2] = {kRowBytes / 2, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <bool MX, int EPI, bool GATHER = false>
+template <bool MX, int EPI>
 static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
                                     cudaStream_t st) {
   using C = GemmSmem<MX>;
   CUtensorMap ta;
   BMaps tb;
-  if (GATHER ? !make_gather_map(&ta, A, g.K, a_rows) : !make_operand_map(&ta, A, MX, g.K, a_rows, 1, kBM))
-    return cudaErrorInvalidValue;
+  if (!make_operand_map(&ta, A, MX, g.K, a_rows, 1, kBM)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b256, B, MX, g.K, g.n_out, g.E_loc, 256)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b128, B, MX, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b64, B, MX, g.K, g.n_out, g.E_loc, 64)) return cudaErrorInvalidValue;
-  auto kern = tc_grouped_gemm_kernel<MX, EPI, GATHER>;
+  auto kern = tc_grouped_gemm_kernel<MX, EPI>;
   // opt in to > 48 KB of dynamic shared memory once per device (keeps later launches,
   // including ones recorded into a CUDA graph, free of non-launch API calls)
   static bool attr_set[64] = {false};
@@ -411,20 +342,6 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
   if (mx) return launch_gemm_inst<true, EPI_SWIGLU_MX>(perm_x, N_cap, Wgu, g, st);
   if (pair) return launch_pair_gemm(perm_x, N_cap, Wgu, g, true, st);
   return launch_gemm_inst<false, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
-}
-
-// GEMM1 + fused scaled SwiGLU with A gathered from x [T, d] by row_src_token (bf16).
-cudaError_t launch_tc_gemm1_gather(const void* x, int T, const int32_t* row_src_token, const int32_t* offsets,
-                                   const float* row_prob, int E_loc, int d, int f, const void* Wgu, void* h,
-                                   int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
-  GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
-  g.n_out = 2 * f;
-  g.K = d;
-  g.out = h;
-  g.ld_out = f;
-  g.row_prob = row_prob;
-  g.a_rows = row_src_token;
-  return launch_gemm_inst<false, EPI_SWIGLU_BF16, true>(x, T, Wgu, g, st);
 }
 
 // GEMM2 on the tensor cores: h [N_cap, f] (bf16, or E4M3 + SF) -> Y2 bf16 [N_cap, d].

@@ -30,7 +30,6 @@ struct GemmArgs {
   const uint8_t* b_sf;     // MXFP8: scales of B (weight SF tile layout)
   int32_t* err;            // device error word
   uint64_t timeout_ns;
-  const int32_t* a_rows;   // gathered A: source row (token) of every permuted row, else NULL
 };
 
 struct Tile {

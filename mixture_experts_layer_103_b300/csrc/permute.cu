@@ -271,9 +271,7 @@ cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtyp
     perm_scatter_kernel<<<n_tiles, kPermTile, E_loc * (kPermTile / 32) * 4, st>>>(
         ids, probs, T, k, e0, E_loc, n_tiles, w.tile_counts, pair_to_row, row_src_token, row_prob);
     const int grid = gather_grid(st);
-    if (perm_x == nullptr) {
-      // maps only: the rows are gathered later by the consumer (GEMM1 with gathered A)
-    } else if (perm_dtype == MOE_MXFP8) {
+    if (perm_dtype == MOE_MXFP8) {
       const size_t sm = static_cast<size_t>(2 * (E_loc + 1)) * 4;
       if (x_dtype == MOE_BF16)
         perm_gather_mx_kernel<1><<<grid, 256, sm, st>>>(static_cast<const uint4*>(x), d, offsets, E_loc, w.mtile_base,

@@ -350,33 +350,3 @@ def test_pair_kernel_matches_oracle(moe, name, counts, d, f):
     for hint, y in ys.items():
         assert rel_l2(to_np(y), yo) <= TOL["bf16"], hint
     assert rel_l2(to_np(ys[4096]), to_np(ys[1])) <= 1e-2
-
-
-# ----------------------------------------------------------------------------- gathered GEMM1
-GATHER_CASES = [
-    Workload("g_e64", 1024, 512, 512, 64, 8, 0, 64, "bf16", ("normal", 0.5)),
-    Workload("g_tails", 300, 200, 96, 16, 4, 4, 8, "bf16"),          # K tail, N tail, local slice
-    Workload("g_zipf", 700, 256, 128, 256, 8, 0, 32, "bf16", ("zipf", 1.1)),
-]
-
-
-@pytest.mark.parametrize("w", GATHER_CASES, ids=[w.name for w in GATHER_CASES])
-def test_gemm1_gather_equals_permuted_copy(moe, w):
-    """GEMM1 reading its rows from x through the permutation gives bitwise the h of
-    GEMM1 on the materialised permuted copy; the maps-only permute writes no rows."""
-    x, lg = gen_x(w), gen_logits(w)
-    Wg, Wu, Wd = gen_weights(w)
-    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), "bf16")
-    xd = to_dev(x)
-    ids, probs = moe.moe_route_topk(to_dev(lg), w.k)
-    P = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, "bf16")
-    Pm = moe.alloc_permute(w.T, w.d, w.k, w.E_loc, xd.dtype, "bf16", rows=False)
-    moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, "bf16", out=Pm)
-    h_ref, _, _ = moe.moe_expert_gemm1_swiglu(P["perm_x"], None, P["offsets"], P["row_prob"], pw)
-    h_g, ws = moe.moe_expert_gemm1_swiglu_gather(xd, Pm["row_src_token"], Pm["offsets"], Pm["row_prob"], pw)
-    torch.cuda.synchronize()
-    assert moe.moe_get_device_error(ws) == 0
-    N = int(P["offsets"][-1])
-    for key in ("offsets", "pair_to_row"):
-        assert torch.equal(Pm[key], P[key])
-    assert torch.equal(h_g[:N], h_ref[:N])
