@@ -68,6 +68,22 @@ def peaks():
         return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Max of a per-rank number over all ranks (the job time is the slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own batch of tokens per step."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 def host_cores() -> int:
     return len(os.sched_getaffinity(0))
 
@@ -383,12 +399,9 @@ def run_ours(args, w):
                for j, nm in enumerate(names)}
     total_ms = sum(step_ms)
     region_ms = region0.elapsed_time(region1)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, "cuda")
     ms_per_step = total_ms / args.steps
-    value = T * world / (ms_per_step / 1e3)
+    value = job_tokens_per_s(T, world, ms_per_step)
 
     # ---- roofline of the dominant kernel and of the whole layer
     bf = layer_bytes_flops(w, N, nonempty, n_tok_local)

@@ -241,6 +241,14 @@ size_t moe_layer_workspace_size(int T, int d, int f, int E, int k, int E_loc, mo
  * *device_error.  Returns MOE_ERR_CUDA if the synchronisation fails. */
 moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* device_error);
 
+/* Self-test of the bounded device waits every pipelined kernel uses (failure detection):
+ * launches one thread that waits on an mbarrier nothing arrives on, for timeout_ns
+ * (1 ms .. 2 s); the wait gives up, MOE_ERR_TIMEOUT is stored in the error word at the
+ * start of `workspace` (>= 256 bytes, 256-byte aligned) and the kernel returns, leaving
+ * the context usable.  Read the result with moe_get_device_error(). */
+moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, void* workspace, size_t workspace_bytes,
+                                     moe_stream_t stream);
+
 /* 1 if the current CUDA device is compute capability 10.3 (sm_103a), else 0. */
 int moe_supported(void);
 

@@ -65,6 +65,7 @@ _SIGS = {
     "moe_layer_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_layer_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_get_device_error": (_I, [_P, _P, _P]),
+    "moe_selftest_wait_timeout": (_I, [ctypes.c_uint64, _P, _SZ, _P]),
     "moe_supported": (_I, []),
     "moe_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -281,6 +282,14 @@ def moe_get_device_error(ws: torch.Tensor) -> int:
     code = ctypes.c_int32(0)
     _check("moe_get_device_error", _lib.moe_get_device_error(_ptr(ws), _stream(), ctypes.byref(code)))
     return code.value
+
+
+def moe_selftest_wait_timeout(timeout_ns: int, ws=None):
+    """Run the bounded-wait self-test; returns the device error code it recorded."""
+    ws = ws if ws is not None else workspace(256)
+    _check("moe_selftest_wait_timeout", _lib.moe_selftest_wait_timeout(int(timeout_ns), _ptr(ws), ws.numel(),
+                                                                       _stream()))
+    return moe_get_device_error(ws)
 
 
 class MoELayer:

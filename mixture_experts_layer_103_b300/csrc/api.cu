@@ -26,6 +26,7 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
 cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
                             int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
                             uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
 
@@ -391,6 +392,15 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
                 Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, moe_rows_hint(T, k, E), stream);
   if (e == cudaSuccess) e = launch_combine(w.Y2, w.pair_to_row, T, k, d, dtype, y, stream);
   return cuda_status(e);
+}
+
+moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, void* workspace, size_t workspace_bytes,
+                                     moe_stream_t stream) {
+  if (timeout_ns < 1000000ull || timeout_ns > 2000000000ull) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+  int32_t* err = static_cast<int32_t*>(workspace);
+  if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_wait_timeout(err, timeout_ns, stream));
 }
 
 moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* device_error) {

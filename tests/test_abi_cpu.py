@@ -100,5 +100,9 @@ def test_validation_before_any_launch(lib):
     # expert GEMMs: workspace missing
     assert L.moe_expert_gemm2(P, None, P, 64, 4, 64, 64, 1, P, None, P, 0, _null(), 256, s) == 3
     assert L.moe_rows_hint(4096, 8, 64) == 512 and L.moe_rows_hint(0, 8, 64) == 0
+    # bounded-wait self-test: timeout outside [1 ms, 2 s], missing workspace
+    assert L.moe_selftest_wait_timeout(10, P, 256, s) == 1
+    assert L.moe_selftest_wait_timeout(5_000_000_000, P, 256, s) == 1
+    assert L.moe_selftest_wait_timeout(10_000_000, _null(), 256, s) == 3
     # device error read: null output
     assert L.moe_get_device_error(P, s, None) == 1

@@ -1,0 +1,50 @@
+"""The multi-rank logic of bench.py on CPU: two gloo ranks, each with its own timing; the
+job time is the slowest rank's and the job throughput counts every rank's tokens."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    slowest = bench.max_over_ranks(10.0 + 3.5 * rank, "cpu")
+    q.put((rank, slowest, bench.job_tokens_per_s(4096, world, 2.0)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_throughput_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in results] == [13.5, 13.5]
+    assert all(abs(r[2] - 4096 * 2 / 0.002) < 1e-6 for r in results)
+
+
+def test_single_process_passthrough():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(7.0, "cpu") == 7.0
+    assert bench.job_tokens_per_s(100, 1, 1.0) == 1e5
