@@ -33,7 +33,14 @@
  *     launch returns MOE_ERR_CUDA.
  *   - Matrices are dense, row-major and contiguous.  "bf16" means IEEE bfloat16 bits.
  *   - Device-detected errors (a bounded wait in a kernel that gave up) are written to
- *     the first 4 bytes of the workspace; read them with moe_get_device_error().
+ *     the first 4 bytes of the workspace (the "error word").  The word is sticky: kernels
+ *     only move it from 0 to an error code, moe_get_device_error() reads and clears it,
+ *     and calls never reset it (so a call adds no memset to the stream).  Initialise a
+ *     new workspace once with moe_workspace_init().
+ *   - Kernels are launched with programmatic dependent launch: each one lets the next
+ *     kernel on the stream start its set-up early and waits for the previous kernel's
+ *     results before touching them, so back-to-back calls (and CUDA graphs of them)
+ *     overlap kernel boundaries.
  *   - Only compute capability 10.3 (B300, sm_103a) is supported; there is no CPU path.
  */
 #ifndef MOE_B300_MOE_H_
@@ -236,6 +243,10 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
                              size_t workspace_bytes, moe_stream_t stream);
 size_t moe_layer_workspace_size(int T, int d, int f, int E, int k, int E_loc, moe_dtype dtype);
 
+/* Zeroes the 256-byte header of a new workspace (the device error word), asynchronously on
+ * `stream`.  Call once before a workspace's first use. */
+moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device error word at the start of
  * `workspace`.  Writes MOE_OK or the error code a kernel stored (MOE_ERR_TIMEOUT) to
  * *device_error.  Returns MOE_ERR_CUDA if the synchronisation fails. */
@@ -243,9 +254,9 @@ moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* d
 
 /* Self-test of the bounded device waits every pipelined kernel uses (failure detection):
  * launches one thread that waits on an mbarrier nothing arrives on, for timeout_ns
- * (1 ms .. 2 s); the wait gives up, MOE_ERR_TIMEOUT is stored in the error word at the
- * start of `workspace` (>= 256 bytes, 256-byte aligned) and the kernel returns, leaving
- * the context usable.  Read the result with moe_get_device_error(). */
+ * (1 ms .. 2 s); the wait gives up, MOE_ERR_TIMEOUT is stored in the (initialised) error
+ * word at the start of `workspace` (>= 256 bytes, 256-byte aligned) and the kernel
+ * returns, leaving the context usable.  Read the result with moe_get_device_error(). */
 moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, void* workspace, size_t workspace_bytes,
                                      moe_stream_t stream);
 

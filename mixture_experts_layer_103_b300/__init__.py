@@ -65,6 +65,7 @@ _SIGS = {
     "moe_layer_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_layer_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_get_device_error": (_I, [_P, _P, _P]),
+    "moe_workspace_init": (_I, [_P, _SZ, _P]),
     "moe_selftest_wait_timeout": (_I, [ctypes.c_uint64, _P, _SZ, _P]),
     "moe_supported": (_I, []),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -102,8 +103,11 @@ def torch_dtype(dtype) -> torch.dtype:
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
-    """A caller-owned device workspace (torch allocations are 256-byte aligned)."""
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    """A caller-owned device workspace (torch allocations are 256-byte aligned), its error
+    word initialised by moe_workspace_init on the current stream."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    _check("moe_workspace_init", _lib.moe_workspace_init(_ptr(ws), ws.numel(), _stream()))
+    return ws
 
 
 def n_cap(T: int, k: int, E_loc: int) -> int:

@@ -250,7 +250,6 @@ moe_status moe_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, i
   if (!workspace || !aligned256(workspace) || workspace_bytes < moe_permute_workspace_size(T, k, E_loc))
     return MOE_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(launch_permute(x, x_dtype, perm_dtype, T, d, topk_ids, topk_probs, k, e0, E_loc, perm_x,
                                     perm_x_scale, counts, offsets, row_src_token, row_prob, pair_to_row,
                                     ws + sizeof(WsHeader), stream));
@@ -296,7 +295,6 @@ moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, cons
   if (!workspace || !aligned256(workspace) || workspace_bytes < moe_grouped_mlp_workspace_size(N_cap, E_loc, d, f, dtype))
     return MOE_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(run_mlp(perm_x, perm_x_scale, offsets, row_prob, N_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale,
                              Wd_packed, Wd_scale, Y2, ws + sizeof(WsHeader), reinterpret_cast<int32_t*>(ws), rows_hint,
                              stream));
@@ -332,7 +330,6 @@ moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_sca
   if (N_cap > 0 && (!row_prob || (dtype == MOE_MXFP8 && !h_scale))) return MOE_ERR_INVALID_ARG;
   if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
   int32_t* err = static_cast<int32_t*>(workspace);
-  if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(run_gemm1(perm_x, perm_x_scale, offsets, row_prob, N_cap, E_loc, d, f, dtype, Wgu_packed,
                                Wgu_scale, h, h_scale, err, rows_hint, stream));
 }
@@ -344,7 +341,6 @@ moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t
   if (s != MOE_OK) return s;
   if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
   int32_t* err = static_cast<int32_t*>(workspace);
-  if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(
       run_gemm2(h, h_scale, offsets, N_cap, E_loc, d, f, dtype, Wd_packed, Wd_scale, Y2, err, rows_hint, stream));
 }
@@ -382,8 +378,7 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
   LayerWs w = layer_layout(static_cast<uint8_t*>(workspace), T, d, f, k, E_loc, dtype);
   const int64_t n_cap = n_cap_of(T, k, E_loc);
   const moe_dtype x_dtype = dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
-  cudaError_t e = cudaMemsetAsync(w.err, 0, 4, stream);
-  if (e == cudaSuccess) e = launch_route_topk(logits, T, E, k, w.topk_ids, w.topk_probs, stream);
+  cudaError_t e = launch_route_topk(logits, T, E, k, w.topk_ids, w.topk_probs, stream);
   if (e == cudaSuccess)
     e = launch_permute(x, x_dtype, dtype, T, d, w.topk_ids, w.topk_probs, k, e0, E_loc, w.perm_x, w.perm_sf, w.counts,
                        w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
@@ -398,9 +393,12 @@ moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, void* workspace, size_
                                      moe_stream_t stream) {
   if (timeout_ns < 1000000ull || timeout_ns > 2000000000ull) return MOE_ERR_INVALID_ARG;
   if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
-  int32_t* err = static_cast<int32_t*>(workspace);
-  if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_wait_timeout(err, timeout_ns, stream));
+  return cuda_status(launch_wait_timeout(static_cast<int32_t*>(workspace), timeout_ns, stream));
+}
+
+moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+  return cudaMemsetAsync(workspace, 0, sizeof(WsHeader), stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* device_error) {

@@ -13,6 +13,8 @@ constexpr int kCombineGroup = 8;  // slots whose loads are in flight together
 template <bool F32>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ p2r,
                                                       int T, int k, int64_t row_vecs, uint4* __restrict__ y) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int V = F32 ? 4 : 8;  // values per 16-byte vector
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -74,11 +76,11 @@ cudaError_t launch_combine(const void* Y2, const int32_t* p2r, int T, int k, int
   const int64_t row_vecs = static_cast<int64_t>(d) * (f32 ? 4 : 2) / 16;
   const dim3 grid(static_cast<unsigned>(ceil_div(T, 8))), block(256);
   if (f32)
-    combine_kernel<true><<<grid, block, 0, st>>>(static_cast<const uint4*>(Y2), p2r, T, k, row_vecs,
-                                                 static_cast<uint4*>(y));
+    return launch_pdl(combine_kernel<true>, grid, block, 0, st, static_cast<const uint4*>(Y2), p2r, T, k, row_vecs,
+                      static_cast<uint4*>(y));
   else
-    combine_kernel<false><<<grid, block, 0, st>>>(static_cast<const uint4*>(Y2), p2r, T, k, row_vecs,
-                                                  static_cast<uint4*>(y));
+    return launch_pdl(combine_kernel<false>, grid, block, 0, st, static_cast<const uint4*>(Y2), p2r, T, k, row_vecs,
+                      static_cast<uint4*>(y));
   return cudaGetLastError();
 }
 

@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BMaps tmB,
                            const GemmArgs g) {
   using C = GemmSmem<MX>;
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish();
   }
+  pdl_wait();  // offsets, row data and scales come from the previous kernels
   if (warp == 2) build_mtile_prefix(g.offsets, g.E_loc, kBM, s_off, s_mtp);
   ptx::tc_fence_before();
   __syncthreads();
@@ -306,8 +308,7 @@ static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kern<<<num_sms(), kGemmThreads, C::SMEM_BYTES, st>>>(ta, tb, g);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(num_sms()), dim3(kGemmThreads), C::SMEM_BYTES, st, ta, tb, g);
 }
 
 static GemmArgs base_args(const int32_t* offsets, int E_loc, int32_t* err, uint64_t timeout_ns) {

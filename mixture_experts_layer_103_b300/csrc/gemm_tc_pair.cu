@@ -43,6 +43,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tc_grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                 const GemmArgs g) {
   using C = PairSmem;
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -79,6 +80,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish_pair();
   }
+  pdl_wait();  // offsets, row data and scales come from the previous kernels
   if (warp == 2) build_mtile_prefix(g.offsets, g.E_loc, kPairBM, s_off, s_mtp);
   __syncwarp();
   ptx::tc_fence_before();
@@ -201,8 +203,7 @@ static cudaError_t launch_pair_inst(const void* A, int64_t a_rows, const void* B
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int grid = num_sms() & ~1;  // whole pairs
-  kern<<<grid, kGemmThreads, PairSmem::SMEM_BYTES, st>>>(ta, tb, g);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), PairSmem::SMEM_BYTES, st, ta, tb, g);
 }
 
 cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu,

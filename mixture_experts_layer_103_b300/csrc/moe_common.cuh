@@ -36,8 +36,35 @@ __host__ __device__ inline int gu_block_of(int f) {
 // Number of 128-row m-tiles of the activation SF layout, upper bound.
 __host__ __device__ inline int64_t mx_tiles_cap(int64_t n_cap, int E_loc) { return ceil_div(n_cap, 128) + E_loc; }
 
+// The device error word is sticky: kernels only ever move it from 0 to an error code;
+// moe_get_device_error() reads and clears it.
 __device__ __forceinline__ void set_device_error(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
+}
+
+// Programmatic dependent launch.  Every kernel of the layer lets the next kernel on the
+// stream be scheduled early (launch_dependents) and waits for the previous kernel to
+// finish and flush (wait) before it touches any data the pipeline produces; only
+// kernel-local set-up (shared memory, barriers, TMEM) may come before the wait.  On a
+// launch without the attribute both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kern` with programmatic stream serialization allowed (see pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // ---- bf16 / fp32 helpers --------------------------------------------------------------

@@ -20,6 +20,8 @@ constexpr int kPermTile = 256;  // tokens per tile (count / scatter)
 
 __global__ void __launch_bounds__(kPermTile) perm_count_kernel(const int32_t* __restrict__ ids, int T, int k, int e0,
                                                                int E_loc, int n_tiles, int32_t* __restrict__ tile_counts) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ int s_cnt[];
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
@@ -64,6 +66,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& tot
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ tile_counts, int n_tiles, int E_loc,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ mtile_base) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ int s_warp[32];
   __shared__ int s_off[1025];
   const int n = E_loc * n_tiles;
@@ -105,6 +109,8 @@ __global__ void __launch_bounds__(kPermTile) perm_scatter_kernel(const int32_t* 
                                                                  int32_t* __restrict__ pair_to_row,
                                                                  int32_t* __restrict__ row_src_token,
                                                                  float* __restrict__ row_prob) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ uint32_t s_mask[];  // [E_loc][kPermTile / 32] token bitmasks
   constexpr int W = kPermTile / 32;
   for (int i = threadIdx.x; i < E_loc * W; i += blockDim.x) s_mask[i] = 0u;
@@ -138,6 +144,8 @@ __global__ void __launch_bounds__(256) perm_gather_copy_kernel(const uint4* __re
                                                                const int32_t* __restrict__ offsets, int E_loc,
                                                                const int32_t* __restrict__ row_src_token,
                                                                uint4* __restrict__ perm_x) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int N = __ldg(offsets + E_loc);
@@ -165,6 +173,8 @@ __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __rest
                                                              const int32_t* __restrict__ mtile_base,
                                                              const int32_t* __restrict__ row_src_token,
                                                              uint8_t* __restrict__ perm_x, uint8_t* __restrict__ perm_sf) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int VPV = IN_BF16 ? 8 : 4;  // values per 16-byte vector
   constexpr int LPB = 32 / VPV;         // lanes per 32-value block
   extern __shared__ int32_t s_tab[];    // offsets [E_loc+1], mtile_base [E_loc+1]
@@ -262,30 +272,35 @@ cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtyp
   const int n_tiles = static_cast<int>(ceil_div(T > 0 ? T : 1, kPermTile));
   PermuteWs w = carve_permute_ws(ws, T, E_loc);
   if (T > 0) {
-    perm_count_kernel<<<n_tiles, kPermTile, E_loc * 4, st>>>(ids, T, k, e0, E_loc, n_tiles, w.tile_counts);
+    cudaError_t e = launch_pdl(perm_count_kernel, dim3(n_tiles), dim3(kPermTile), E_loc * 4, st, ids, T, k, e0, E_loc,
+                               n_tiles, w.tile_counts);
+    if (e != cudaSuccess) return e;
   } else {
     cudaMemsetAsync(w.tile_counts, 0, static_cast<size_t>(n_tiles) * E_loc * 4, st);
   }
-  perm_scan_kernel<<<1, 1024, 0, st>>>(w.tile_counts, n_tiles, E_loc, counts, offsets, w.mtile_base);
+  cudaError_t e = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, st, w.tile_counts, n_tiles, E_loc, counts,
+                             offsets, w.mtile_base);
+  if (e != cudaSuccess) return e;
   if (T > 0) {
-    perm_scatter_kernel<<<n_tiles, kPermTile, E_loc * (kPermTile / 32) * 4, st>>>(
-        ids, probs, T, k, e0, E_loc, n_tiles, w.tile_counts, pair_to_row, row_src_token, row_prob);
+    e = launch_pdl(perm_scatter_kernel, dim3(n_tiles), dim3(kPermTile), E_loc * (kPermTile / 32) * 4, st, ids, probs,
+                   T, k, e0, E_loc, n_tiles, static_cast<const int32_t*>(w.tile_counts), pair_to_row, row_src_token,
+                   row_prob);
+    if (e != cudaSuccess) return e;
     const int grid = gather_grid(st);
     if (perm_dtype == MOE_MXFP8) {
       const size_t sm = static_cast<size_t>(2 * (E_loc + 1)) * 4;
-      if (x_dtype == MOE_BF16)
-        perm_gather_mx_kernel<1><<<grid, 256, sm, st>>>(static_cast<const uint4*>(x), d, offsets, E_loc, w.mtile_base,
-                                                        row_src_token, static_cast<uint8_t*>(perm_x), perm_sf);
-      else
-        perm_gather_mx_kernel<0><<<grid, 256, sm, st>>>(static_cast<const uint4*>(x), d, offsets, E_loc, w.mtile_base,
-                                                        row_src_token, static_cast<uint8_t*>(perm_x), perm_sf);
+      e = launch_pdl(x_dtype == MOE_BF16 ? perm_gather_mx_kernel<1> : perm_gather_mx_kernel<0>, dim3(grid), dim3(256),
+                     sm, st, static_cast<const uint4*>(x), d, static_cast<const int32_t*>(offsets), E_loc,
+                     static_cast<const int32_t*>(w.mtile_base), static_cast<const int32_t*>(row_src_token),
+                     static_cast<uint8_t*>(perm_x), perm_sf);
     } else {
       const int64_t row_vecs = static_cast<int64_t>(d) * (x_dtype == MOE_F32 ? 4 : 2) / 16;
-      perm_gather_copy_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(x), row_vecs, offsets, E_loc,
-                                                    row_src_token, static_cast<uint4*>(perm_x));
+      e = launch_pdl(perm_gather_copy_kernel, dim3(grid), dim3(256), 0, st, static_cast<const uint4*>(x), row_vecs,
+                     static_cast<const int32_t*>(offsets), E_loc, static_cast<const int32_t*>(row_src_token),
+                     static_cast<uint4*>(perm_x));
     }
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace moe

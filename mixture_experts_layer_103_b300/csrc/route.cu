@@ -24,6 +24,8 @@ template <int VPL>  // values per lane = ceil(E / 32)
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const float* __restrict__ logits, int T, int E,
                                                                        int k, int32_t* __restrict__ ids,
                                                                        float* __restrict__ probs) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -74,8 +76,9 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
   if (T == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(ceil_div(T, kRouteWarps))), block(kRouteWarps * 32);
   const int vpl = static_cast<int>(ceil_div(E, 32));
+  cudaError_t e = cudaSuccess;
 #define MOE_ROUTE_CASE(V) \
-  case V: route_topk_kernel<V><<<grid, block, 0, st>>>(logits, T, E, k, ids, probs); break;
+  case V: e = launch_pdl(route_topk_kernel<V>, grid, block, 0, st, logits, T, E, k, ids, probs); break;
   switch (vpl <= 2 ? 2 : vpl <= 4 ? 4 : vpl <= 8 ? 8 : vpl <= 16 ? 16 : 32) {
     MOE_ROUTE_CASE(2)
     MOE_ROUTE_CASE(4)
@@ -84,7 +87,7 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
     MOE_ROUTE_CASE(32)
   }
 #undef MOE_ROUTE_CASE
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace moe

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) simt_grouped_gemm_kernel(const float* __r
                                                                 const float* __restrict__ B, int n_out,
                                                                 const float* __restrict__ row_prob,
                                                                 float* __restrict__ out, int64_t ld_out) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ int s_tab[];  // s_off [E_loc+1], s_mtp [E_loc+1]
   __shared__ float As[kSimtBK][kSimtBM + 4];
   __shared__ float Bs[kSimtBK][kSimtBN + 4];
@@ -97,9 +99,8 @@ cudaError_t launch_simt_gemm1(const float* perm_x, const int32_t* offsets, const
                               int E_loc, int d, int f, const float* Wgu, float* h, cudaStream_t st) {
   const unsigned mt = static_cast<unsigned>(ceil_div(N_cap, kSimtBM) + E_loc);
   const size_t sm = static_cast<size_t>(2 * (E_loc + 1)) * 4;
-  simt_grouped_gemm_kernel<true><<<dim3(mt, static_cast<unsigned>(ceil_div(2 * f, kSimtBN))), 256, sm, st>>>(
-      perm_x, d, offsets, E_loc, Wgu, 2 * f, row_prob, h, f);
-  return cudaGetLastError();
+  return launch_pdl(simt_grouped_gemm_kernel<true>, dim3(mt, static_cast<unsigned>(ceil_div(2 * f, kSimtBN))),
+                    dim3(256), sm, st, perm_x, d, offsets, E_loc, Wgu, 2 * f, row_prob, h, static_cast<int64_t>(f));
 }
 
 // GEMM2, fp32: h [N_cap, f] -> Y2 [N_cap, d].
@@ -107,9 +108,9 @@ cudaError_t launch_simt_gemm2(const float* h, const int32_t* offsets, int64_t N_
                               const float* Wd, float* Y2, cudaStream_t st) {
   const unsigned mt = static_cast<unsigned>(ceil_div(N_cap, kSimtBM) + E_loc);
   const size_t sm = static_cast<size_t>(2 * (E_loc + 1)) * 4;
-  simt_grouped_gemm_kernel<false><<<dim3(mt, static_cast<unsigned>(ceil_div(d, kSimtBN))), 256, sm, st>>>(
-      h, f, offsets, E_loc, Wd, d, nullptr, Y2, d);
-  return cudaGetLastError();
+  return launch_pdl(simt_grouped_gemm_kernel<false>, dim3(mt, static_cast<unsigned>(ceil_div(d, kSimtBN))), dim3(256),
+                    sm, st, h, f, offsets, E_loc, Wd, d, static_cast<const float*>(nullptr), Y2,
+                    static_cast<int64_t>(d));
 }
 
 }  // namespace moe

@@ -104,5 +104,9 @@ def test_validation_before_any_launch(lib):
     assert L.moe_selftest_wait_timeout(10, P, 256, s) == 1
     assert L.moe_selftest_wait_timeout(5_000_000_000, P, 256, s) == 1
     assert L.moe_selftest_wait_timeout(10_000_000, _null(), 256, s) == 3
+    # workspace init: null / misaligned / too small
+    assert L.moe_workspace_init(_null(), 256, s) == 3
+    assert L.moe_workspace_init(ctypes.c_void_p(272), 256, s) == 3
+    assert L.moe_workspace_init(P, 16, s) == 3
     # device error read: null output
     assert L.moe_get_device_error(P, s, None) == 1
