@@ -58,13 +58,13 @@ struct GemmSmem {
 };
 
 // Tile width of a launch, identical in every CTA: the candidate with the fewest
-// "weighted waves", waves(BN) * c(BN), where c is the relative time of one tile (a
-// 128x128 tile costs ~0.6 of a 128x256 one: same A traffic, half the MMA work; a 128x64
-// tile ~0.4: its MMAs are shared-memory bound).  Many tiles -> 256 (best reuse); few
-// tiles (decode-like slices) -> narrower tiles so that more SMs stream the weights.
+// "weighted waves", waves(BN) * c(BN), where c is the relative time of one tile measured
+// on B300 across the workloads (a 128x128 tile takes ~0.72 of a 128x256 one, a 128x64
+// tile ~0.5: narrower tiles re-read A and feed the tensor core less efficiently).  Many
+// tiles -> 256; a single partial wave -> narrower tiles so that more SMs stream weights.
 __device__ __forceinline__ int choose_bn(int m_tiles, int n_out, int ctas, bool mx) {
   const int cand[3] = {256, 128, 64};
-  const float cost[3] = {1.0f, 0.6f, 0.4f};
+  const float cost[3] = {1.0f, 0.72f, 0.5f};
   int best = 256;
   float best_cost = 3.0e38f;
   for (int i = 0; i < (mx ? 2 : 3); ++i) {
