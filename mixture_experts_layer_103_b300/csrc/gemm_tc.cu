@@ -20,14 +20,22 @@
 //               thread), then either bf16 store (GEMM2) or the fused scaled SwiGLU
 //               h = p * silu(gate) * up with bf16 or MXFP8 (32 values = one block per
 //               thread) output (GEMM1)
-// The tile scheduler is static: tile t -> (global m-tile t / n_tiles, n-tile t % n_tiles);
-// m-tiles are 128-row slices of each expert's segment [offsets[e], offsets[e+1]),
-// numbered in expert order, so experts with no tokens cost nothing and their weights are
-// never read.  Rows of a tile past its expert's segment are computed and discarded.
+// CTAs run in clusters of two.  The static scheduler hands out units of two tiles, one
+// per CTA of a cluster: while an expert has two m-tiles left, a unit is the pair of
+// m-tiles (m, m + 1) against one n-tile, and each CTA loads half of the shared weight
+// tile and multicasts it to both (half the L2 reads of B, the operand whose feed limits
+// the mainloop); an expert's odd last m-tile forms units of two n-tiles, each CTA loading
+// its own B.  m-tiles are 128-row slices of each expert's segment
+// [offsets[e], offsets[e+1]), numbered in expert order, so experts with no tokens cost
+// nothing and their weights are never read.  Rows of a tile past its expert's segment are
+// computed and discarded.  Both CTAs of a cluster consume the same sequence of pipeline
+// stages, and a stage is refilled only when both have finished with it (the MMA issuers
+// commit to the empty barriers of both CTAs).
 // Every wait is bounded; on a timeout the kernel records MOE_ERR_TIMEOUT in the device
 // error word, drains its own copies and MMAs and exits.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gemm_tc.cuh"
@@ -40,7 +48,7 @@ namespace moe {
 // scale atoms of each stage live in a separate ring.
 template <bool MX>
 struct GemmSmem {
-  static constexpr int MAX_STAGES = 8;
+  static constexpr int MAX_STAGES = MX ? 6 : 8;            // MXFP8 tiles are 256 or 128 wide
   static constexpr int A_BYTES = kBM * kRowBytes;           // 16 KB
   static constexpr int PIPE_BYTES = 192 * 1024;             // A + B ring
   static constexpr int SF_STAGE_BYTES = MX ? 512 + 1024 : 0; // SFA atom + up to two SFB atoms
@@ -53,23 +61,30 @@ struct GemmSmem {
   static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TAB = OFF_MISC + 16;
-  static constexpr int SMEM_BYTES = OFF_TAB + 2 * (kMaxEloc + 1) * 4 + 1024;  // + alignment slack
+  static constexpr int SMEM_BYTES = OFF_TAB + 3 * (kMaxEloc + 1) * 4 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
+// Units (tile pairs) of a launch with n-tile count nt: an expert with M m-tiles gives
+// (M / 2) * nt multicast units plus ceil(nt / 2) units for an odd last m-tile.
+// mt_total = total m-tiles, odd = experts with an odd m-tile count.
+__device__ __forceinline__ long unit_count(int mt_total, int odd, int nt) {
+  return static_cast<long>((mt_total - odd) / 2) * nt + static_cast<long>(odd) * ((nt + 1) / 2);
+}
+
 // Tile width of a launch, identical in every CTA: the candidate with the fewest
-// "weighted waves", waves(BN) * c(BN), where c is the relative time of one tile measured
-// on B300 across the workloads (a 128x128 tile takes ~0.72 of a 128x256 one, a 128x64
-// tile ~0.5: narrower tiles re-read A and feed the tensor core less efficiently).  Many
-// tiles -> 256; a single partial wave -> narrower tiles so that more SMs stream weights.
-__device__ __forceinline__ int choose_bn(int m_tiles, int n_out, int ctas, bool mx) {
+// cost-weighted waves of units over the clusters.  The relative costs of a 128 x BN tile
+// (1.0 / 0.72 / 0.5 for BN = 256 / 128 / 64) are measured per-wave times on B300 at
+// these shapes; a narrower tile does less work but feeds the tensor core less
+// efficiently.  MXFP8 uses 256 or 128 (its scale-factor atoms cover 128 rows of B).
+__device__ __forceinline__ int choose_bn(int mt_total, int odd, int n_out, int clusters, bool mx) {
   const int cand[3] = {256, 128, 64};
   const float cost[3] = {1.0f, 0.72f, 0.5f};
   int best = 256;
   float best_cost = 3.0e38f;
   for (int i = 0; i < (mx ? 2 : 3); ++i) {
-    const long tiles = static_cast<long>(m_tiles) * ((n_out + cand[i] - 1) / cand[i]);
-    const long waves = (tiles + ctas - 1) / ctas;
+    const long units = unit_count(mt_total, odd, (n_out + cand[i] - 1) / cand[i]);
+    const long waves = (units + clusters - 1) / clusters;
     const float c = static_cast<float>(waves) * cost[i];
     if (c < best_cost) {
       best_cost = c;
@@ -79,13 +94,102 @@ __device__ __forceinline__ int choose_bn(int m_tiles, int n_out, int ctas, bool 
   return best;
 }
 
-// B operand maps with box heights 256, 128 and 64 rows (one per tile width).
+// Per-expert tables in shared memory (one warp): s_off[e] = offsets[e], s_mtp[e] = m-tiles
+// of the experts before e, s_odd[e] = experts before e with an odd m-tile count; entry
+// E_loc holds the totals.
+__device__ __forceinline__ void build_unit_tables(const int32_t* __restrict__ offsets, int E_loc, int* s_off,
+                                                  int* s_mtp, int* s_odd) {
+  const int lane = threadIdx.x & 31;
+  const int per = (E_loc + 31) / 32;
+  const int e_begin = lane * per, e_end = min(E_loc, e_begin + per);
+  int sum = 0, odd = 0;
+  for (int e = e_begin; e < e_end; ++e) {
+    const int o0 = __ldg(offsets + e), o1 = __ldg(offsets + e + 1);
+    const int m = (o1 - o0 + kBM - 1) / kBM;
+    s_off[e] = o0;
+    sum += m;
+    odd += m & 1;
+  }
+  int incl = sum, incl_odd = odd;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    const int z = __shfl_up_sync(0xffffffffu, incl_odd, off);
+    if (lane >= off) {
+      incl += y;
+      incl_odd += z;
+    }
+  }
+  int run = incl - sum, run_odd = incl_odd - odd;
+  for (int e = e_begin; e < e_end; ++e) {
+    s_mtp[e] = run;
+    s_odd[e] = run_odd;
+    const int m = (__ldg(offsets + e + 1) - __ldg(offsets + e) + kBM - 1) / kBM;
+    run += m;
+    run_odd += m & 1;
+  }
+  if (lane == 31) {
+    s_mtp[E_loc] = incl;
+    s_odd[E_loc] = incl_odd;
+    s_off[E_loc] = __ldg(offsets + E_loc);
+  }
+}
+
+// The tile CTA `rank` of a cluster computes in unit u.  shared_b: both CTAs use the same
+// weight tile (multicast halves); valid = false only for the idle half of a unit whose
+// expert has an odd m-tile and an odd n-tile count: that CTA recomputes its partner's tile
+// and stores nothing.
+struct UnitTile {
+  Tile t;
+  bool shared_b, valid;
+};
+
+__device__ __forceinline__ UnitTile decode_unit(int u, int rank, int nt, int bn, const int* s_off, const int* s_mtp,
+                                                const int* s_odd, int E_loc) {
+  const int hnt = (nt + 1) / 2;
+  auto first_unit = [&](int e) { return nt * ((s_mtp[e] - s_odd[e]) >> 1) + hnt * s_odd[e]; };
+  int lo = 0, hi = E_loc - 1;  // last expert whose first unit is <= u (skips empty experts)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (first_unit(mid) <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const int e = lo, i = u - first_unit(e);
+  const int m_e = s_mtp[e + 1] - s_mtp[e];
+  const int pairs = m_e >> 1;
+  int mloc, n;
+  UnitTile r;
+  r.valid = true;
+  if (i < pairs * nt) {
+    mloc = 2 * (i / nt) + rank;
+    n = i % nt;
+    r.shared_b = true;
+  } else {
+    const int j = i - pairs * nt;
+    mloc = m_e - 1;
+    n = 2 * j + rank;
+    r.shared_b = false;
+    if (n >= nt) {
+      n = 2 * j;
+      r.valid = false;
+    }
+  }
+  r.t.e = e;
+  r.t.mt = s_mtp[e] + mloc;
+  r.t.row0 = s_off[e] + mloc * kBM;
+  r.t.rows = min(kBM, s_off[e + 1] - r.t.row0);
+  r.t.n0 = n * bn;
+  return r;
+}
+
+// B operand maps with box heights 256, 128, 64 and 32 rows: a full tile of each width,
+// and the half tiles a CTA loads for multicast.
 struct BMaps {
-  CUtensorMap b256, b128, b64;
+  CUtensorMap b256, b128, b64, b32;
 };
 
 template <bool MX, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BMaps tmB,
                            const GemmArgs g) {
   using C = GemmSmem<MX>;
@@ -103,12 +207,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* s_off = reinterpret_cast<int*>(smem + C::OFF_TAB);
   int* s_mtp = s_off + g.E_loc + 1;
+  int* s_odd = s_mtp + g.E_loc + 1;
+  const int rank = static_cast<int>(ptx::cluster_ctarank());
+  const int cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+  const uint16_t both = 0x3;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::MAX_STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 2);  // the MMA issuers of both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
@@ -124,34 +232,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ptx::tmem_relinquish();
   }
   pdl_wait();  // offsets, row data and scales come from the previous kernels
-  if (warp == 2) build_mtile_prefix(g.offsets, g.E_loc, kBM, s_off, s_mtp);
+  if (warp == 2) build_unit_tables(g.offsets, g.E_loc, s_off, s_mtp, s_odd);
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // the peer's barriers exist before any multicast or remote commit
   ptx::tc_fence_after();
 
   const uint32_t tmem_base = *tmem_slot;
-  const int m_tiles = s_mtp[g.E_loc];
-  const int BN = choose_bn(m_tiles, g.n_out, gridDim.x, MX);
+  const int BN = choose_bn(s_mtp[g.E_loc], s_odd[g.E_loc], g.n_out, clusters, MX);
   const CUtensorMap* tmb = BN == 256 ? &tmB.b256 : BN == 128 ? &tmB.b128 : &tmB.b64;
+  const CUtensorMap* tmb_half = BN == 256 ? &tmB.b128 : BN == 128 ? &tmB.b64 : &tmB.b32;
   const int stage_bytes = C::A_BYTES + BN * kRowBytes;  // multiple of 1024
   const int stages = min(C::MAX_STAGES, C::PIPE_BYTES / stage_bytes);
   const int sf_cols = MX ? (BN / 128 + 1) * 4 : 0;       // SFA 4 columns + SFB 4 per 128 rows
   const int num_acc = (2 * BN + 2 * sf_cols <= 512) ? 2 : 1;
   const uint32_t sf_base_col = static_cast<uint32_t>(num_acc * BN);
   const int n_tiles_n = (g.n_out + BN - 1) / BN;
-  const int total = m_tiles * n_tiles_n;
+  const int units = static_cast<int>(unit_count(s_mtp[g.E_loc], s_odd[g.E_loc], n_tiles_n));
   const int num_kb = (g.K + C::BK - 1) / C::BK;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------------ TMA producer
       ptx::prefetch_tmap(tmb);
+      ptx::prefetch_tmap(tmb_half);
       int s = 0;
       uint32_t ph = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(t, n_tiles_n, BN, s_off, s_mtp, g.E_loc);
+      for (int u = cluster; u < units && ok; u += clusters) {
+        const UnitTile ut = decode_unit(u, rank, n_tiles_n, BN, s_off, s_mtp, s_odd, g.E_loc);
+        const Tile& tl = ut.t;
         const int sfb_bytes = MX ? min(BN, g.n_out - tl.n0) / 128 * 512 : 0;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (*s_abort) { ok = false; break; }
@@ -160,7 +271,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t st_addr = sbase + C::OFF_PIPE + s * stage_bytes;
           ptx::mbar_arrive_expect_tx(fb, stage_bytes + (MX ? 512 + sfb_bytes : 0));
           ptx::tma_load_3d(st_addr, &tmA, fb, kb * C::BK, tl.row0, 0);
-          ptx::tma_load_3d(st_addr + C::A_BYTES, tmb, fb, kb * C::BK, tl.n0, tl.e);
+          if (ut.shared_b)  // this CTA's half of the weight tile, to both CTAs
+            ptx::tma_load_3d_mc(st_addr + C::A_BYTES + rank * (BN / 2) * kRowBytes, tmb_half, fb, kb * C::BK,
+                                tl.n0 + rank * (BN / 2), tl.e, both);
+          else
+            ptx::tma_load_3d(st_addr + C::A_BYTES, tmb, fb, kb * C::BK, tl.n0, tl.e);
           if constexpr (MX) {
             const int kg = g.K / 128;
             const uint32_t sf_addr = sbase + C::OFF_SF + s * C::SF_STAGE_BYTES;
@@ -187,7 +302,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t ph = 0, kbg = 0;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+      for (int u = cluster; u < units && ok; u += clusters, ++it) {
         const int acc = num_acc == 2 ? (it & 1) : 0;
         const uint32_t acc_ph = num_acc == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
         if (!ptx::mbar_wait(tempty_bar(acc), acc_ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); break; }
@@ -215,7 +330,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               ptx::mma_bf16(d_tmem, ptx::sdesc_sw128(a_addr + k * 32), ptx::sdesc_sw128(b_addr + k * 32), idesc,
                             (kb | k) != 0);
           }
-          ptx::mma_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+          ptx::mma_commit_mc(empty_bar(s), both);  // frees the stage (in both CTAs) once read
           if (++s == stages) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
@@ -228,9 +343,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+    for (int u = cluster; u < units; u += clusters, ++it) {
       if (*s_abort) break;
-      const Tile tl = decode_tile(t, n_tiles_n, BN, s_off, s_mtp, g.E_loc);
+      const UnitTile ut = decode_unit(u, rank, n_tiles_n, BN, s_off, s_mtp, s_odd, g.E_loc);
+      const Tile& tl = ut.t;
       const int acc = num_acc == 2 ? (it & 1) : 0;
       const uint32_t acc_ph = num_acc == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
       int okw = 0;
@@ -240,7 +356,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       (void)ptx::mbar_try_wait(tfull_bar(acc), acc_ph);  // completed phase: acquire for every lane
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_warp<EPI>(g, tl, tbase, BN, q, lane, smem + C::OFF_EPI + (warp - 2) * kEpiWarpBytes);
+      if (ut.valid) epilogue_warp<EPI>(g, tl, tbase, BN, q, lane, smem + C::OFF_EPI + (warp - 2) * kEpiWarpBytes);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
@@ -248,6 +364,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // no CTA leaves while its peer may still write or arrive into it
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
@@ -296,19 +413,32 @@ static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B
   if (!make_operand_map(&tb.b256, B, MX, g.K, g.n_out, g.E_loc, 256)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b128, B, MX, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b64, B, MX, g.K, g.n_out, g.E_loc, 64)) return cudaErrorInvalidValue;
+  if (!make_operand_map(&tb.b32, B, MX, g.K, g.n_out, g.E_loc, 32)) return cudaErrorInvalidValue;
   auto kern = tc_grouped_gemm_kernel<MX, EPI>;
-  // opt in to > 48 KB of dynamic shared memory once per device (keeps later launches,
-  // including ones recorded into a CUDA graph, free of non-launch API calls)
-  static bool attr_set[64] = {false};
+  // Once per device: opt in to > 48 KB of dynamic shared memory and size the grid to the
+  // clusters of two that can be resident at once (keeps later launches, including ones
+  // recorded into a CUDA graph, free of non-launch API calls).
+  static int grid_of[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  int grid = (dev >= 0 && dev < 64) ? grid_of[dev] : 0;
+  if (grid == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms()));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) {
+      (void)cudaGetLastError();
+      clusters = num_sms() / 2;
+    }
+    grid = 2 * std::min(clusters, num_sms() / 2);
+    if (dev >= 0 && dev < 64) grid_of[dev] = grid;
   }
-  return launch_pdl(kern, dim3(num_sms()), dim3(kGemmThreads), C::SMEM_BYTES, st, ta, tb, g);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kGemmThreads), C::SMEM_BYTES, st, ta, tb, g);
 }
 
 static GemmArgs base_args(const int32_t* offsets, int E_loc, int32_t* err, uint64_t timeout_ns) {

@@ -172,6 +172,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 
+// ---------------------------------------------------------------------------- multicast
+// TMA load delivered to the same shared-memory offset in every CTA of `cta_mask` (a
+// cluster); each destination CTA's mbarrier at offset `bar` counts the bytes it receives.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
+      : "memory");
+}
+// Arrive on the barrier at offset `bar` in every CTA of `cta_mask` once this thread's
+// previously issued (single-CTA) tcgen05 operations have completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                   "r"(bar),
+               "h"(cta_mask)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------- CTA pairs
 // A cluster of two CTAs on one TPC runs one tcgen05 MMA over both SMs (cta_group::2):
 // each CTA stages its own 128 rows of A and half of the B rows; the leader (rank 0)

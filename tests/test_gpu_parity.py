@@ -325,6 +325,8 @@ PAIR_CASES = [
     ("pair_edges", [1, 127, 128, 129, 255, 256, 257, 600], 256, 256),
     ("pair_tails", [300, 0, 513, 77], 200, 96),      # K and N tails: d % 64 != 0, 2f < 256
     ("pair_one_expert", [0, 0, 1100, 0], 384, 128),
+    # 1-CTA cluster units: experts with 1..5 m-tiles (odd and even), odd n-tile counts
+    ("odd_units", [1, 129, 300, 640, 0, 385, 128, 257], 192, 160),
 ]
 
 
