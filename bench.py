@@ -53,6 +53,8 @@ def parse_args():
     p.add_argument("--rows-hint", type=int, default=None,
                    help="expected rows per local expert passed to the grouped GEMMs (default T*k/E); "
                         "it selects the GEMM kernel shape (>= 2048: CTA pairs, bf16)")
+    p.add_argument("--no-gather", action="store_true",
+                   help="feed GEMM1 from a permuted copy of x instead of reading the token rows (row gather)")
     return p.parse_args()
 
 
@@ -308,7 +310,13 @@ def run_ours(args, w):
     T, d, k, E_loc, e0 = w.T, w.d, w.k, w.E_loc, w.e0
     ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
     probs = torch.empty(T, k, dtype=torch.float32, device="cuda")
-    P = moe.alloc_permute(T, d, k, E_loc, xd.dtype, w.dtype)
+    hint = args.rows_hint if args.rows_hint is not None else moe.moe_rows_hint(T, k, w.E)
+    # the library's own choice in moe_layer_forward: row gather for bf16 unless CTA-pair GEMMs
+    gather = not args.no_gather and w.dtype == "bf16" and hint < 2048
+    mx = w.dtype == "mxfp8"
+    P = moe.alloc_permute(T, d, k, E_loc, xd.dtype, w.dtype, maps_only=gather)
+    xq, xs = (torch.empty(T, d, dtype=torch.uint8, device="cuda"),
+              torch.empty(T, d // 32, dtype=torch.uint8, device="cuda")) if gather and mx else (None, None)
     ws_perm = moe.workspace(moe.moe_permute_workspace_size(T, k, E_loc))
     h, hs = moe.alloc_h(moe.n_cap(T, k, E_loc), pw)
     Y2 = torch.empty(moe.n_cap(T, k, E_loc), d, dtype=moe.torch_dtype(w.dtype), device="cuda")
@@ -317,7 +325,6 @@ def run_ours(args, w):
     wbytes = 3 * w.d * w.f * w.E_loc * (4 if w.dtype == "f32" else 2 if w.dtype == "bf16" else 1)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if wbytes <= L2_BYTES else None
 
-    hint = args.rows_hint if args.rows_hint is not None else moe.moe_rows_hint(T, k, w.E)
     names = ["route_topk", "permute", "gemm1_swiglu", "gemm2", "combine"]
 
     def call(i):
@@ -325,9 +332,15 @@ def run_ours(args, w):
             moe.moe_route_topk(lgd, k, ids, probs)
         elif i == 1:
             moe.moe_permute(xd, ids, probs, e0, E_loc, w.dtype, ws=ws_perm, out=P)
+            if gather and mx:
+                moe.moe_quantize_mx_rows(xd, xq, xs, pair_to_row=P["pair_to_row"])
         elif i == 2:
-            moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, h=h,
-                                        h_scale=hs, ws=ws_g, rows_hint=hint)
+            if gather:
+                moe.moe_expert_gemm1_swiglu_gather(xq if mx else xd, xs, P["row_src_token"], P["offsets"],
+                                                   P["row_prob"], pw, h=h, h_scale=hs, ws=ws_g)
+            else:
+                moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, h=h,
+                                            h_scale=hs, ws=ws_g, rows_hint=hint)
         elif i == 3:
             moe.moe_expert_gemm2(h, hs, P["offsets"], pw, Y2=Y2, ws=ws_g, rows_hint=hint)
         else:
@@ -500,7 +513,8 @@ def run_ours(args, w):
     if rank != 0:
         dist.destroy_process_group()
         return
-    launches_per_step = 8
+    # route 1, permute 3 (+1 copy or MXFP8 per-token quantisation), GEMM1, GEMM2, combine
+    launches_per_step = 1 + 3 + (0 if gather and not mx else 1) + 3
     cpu = None if args.no_cpu_baseline else cpu_baseline(w, args.cpu_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -509,6 +523,7 @@ def run_ours(args, w):
         "data": "synthetic (seeded; shapes of the pages' workloads)", "config": workload_config(w),
         "roofline": roof, "layer": layer, "kernels_us": {n: 1e3 * v for n, v in kern_ms.items()},
         "timed_region_ms": region_ms,
+        "gemm1_operand": "token rows gathered in the kernel" if gather else "permuted copy of x",
         "timing": ("one CUDA-graph replay of the K steps (region events; with an L2 flush, the sum of the steps' "
                    "own event intervals); GEMM1 bracketed by event nodes in the timed graph; kernels_us from a "
                    "separate graph with events between all kernels"),

@@ -121,8 +121,11 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* top
  *   x            device [T, d]  x_dtype MOE_F32 or MOE_BF16
  *   perm_dtype   element type of perm_x: MOE_F32 (x fp32), MOE_BF16 (x bf16) or MOE_MXFP8
  *                (x bf16; rows quantised while copied, scales to perm_x_scale)
- *   perm_x       device [N_cap, d], N_cap = T * min(k, E_loc); rows >= N untouched
- *   perm_x_scale device, MOE_MXFP8 only (else NULL): SF tile layout, K = d,
+ *   perm_x       device [N_cap, d], N_cap = T * min(k, E_loc); rows >= N untouched.
+ *                NULL: maps only -- counts, offsets, row_src_token, row_prob and
+ *                pair_to_row are written, no rows are copied (the input of
+ *                moe_expert_gemm1_swiglu_gather); perm_x_scale is then ignored
+ *   perm_x_scale device, MOE_MXFP8 with perm_x only (else NULL): SF tile layout, K = d,
  *                moe_mx_act_scale_bytes(N_cap, d, E_loc) bytes
  *   counts [E_loc], offsets [E_loc+1], row_src_token [N_cap], row_prob [N_cap] (fp32),
  *   pair_to_row [T, k]: device int32 outputs
@@ -221,6 +224,36 @@ moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t
                             int rows_hint, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 size_t moe_expert_gemm_workspace_size(void);
 
+/* GEMM1 + scaled SwiGLU reading the token rows directly ("row gather") [BIO "GroupedLinear
+ * ...": the grouped op consumes the routed tokens; here no permuted copy of x exists].
+ * Computes exactly what moe_expert_gemm1_swiglu computes on moe_permute's perm_x, with
+ * perm_x[row] = x[row_src_token[row]]: the kernel copies each 128-row x 128-byte operand
+ * tile from the token rows into shared memory itself.
+ *   x        MOE_BF16: device bf16 [T, d].  MOE_MXFP8: device E4M3 bytes [T, d] with
+ *            x_scale device E8M0 [T, d / 32] row-major (from moe_quantize_mx_rows).
+ *            (MOE_F32 is not supported: MOE_ERR_UNSUPPORTED.)
+ *   row_src_token [N_cap], offsets [E_loc+1], row_prob [N_cap]: device, from moe_permute
+ *            (which may be called with perm_x == NULL)
+ *   h, h_scale, Wgu_*, workspace: as for moe_expert_gemm1_swiglu.  16-byte aligned x, h
+ *   and packed weights; d % 8 == 0 (bf16), d % 128 == 0 and f % 128 == 0 (MXFP8). */
+moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale, const int32_t* row_src_token,
+                                          const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc,
+                                          int d, int f, moe_dtype dtype, const void* Wgu_packed,
+                                          const uint8_t* Wgu_scale, void* h, uint8_t* h_scale, void* workspace,
+                                          size_t workspace_bytes, moe_stream_t stream);
+
+/* MXFP8 quantisation of token rows [BIO "MXFP8 Precision ..."]: the quantisation rule
+ * above, per 32 consecutive values of a row -- the same rule moe_permute applies while
+ * copying.
+ *   x  device [T, d], x_dtype MOE_BF16 or MOE_F32, 16-byte aligned
+ *   pair_to_row  device int32 [T, k] from moe_permute, or NULL: when given, only rows of
+ *      tokens with at least one local expert (some pair_to_row[t, j] >= 0) are written --
+ *      the only rows the row-gather GEMM1 reads; requires 1 <= k <= 32
+ *   xq device E4M3 [T, d] out (16-byte aligned); x_scale device E8M0 [T, d / 32] out.
+ * Requires d % 32 == 0. */
+moe_status moe_quantize_mx_rows(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
+                                uint8_t* xq, uint8_t* x_scale, moe_stream_t stream);
+
 /* Unpermute + combine (step 5) [WEP "MoE basics": results of the chosen experts are
  * summed; "Prerequisite ...": combine].
  * y[t] = sum over j = 0..k-1 with pair_to_row[t, j] >= 0 of Y2[pair_to_row[t, j]], summed
@@ -236,7 +269,10 @@ moe_status moe_unpermute_combine(const void* Y2, const int32_t* pair_to_row, int
  *   x [T, d] (fp32 for MOE_F32, else bf16), logits [T, E] fp32, packed weights as above,
  *   y [T, d] (fp32 for MOE_F32, else bf16): device pointers.
  *   workspace device >= moe_layer_workspace_size(...) bytes, 256-byte aligned; it holds
- *   the routing table, the permutation, the permuted rows, h and Y2. */
+ *   the routing table, the permutation maps, h and Y2, plus the permuted rows where a
+ *   copy is made: bf16 layers feed GEMM1 by row gather, except when T * k / E >= 2048
+ *   selects the CTA-pair GEMMs, which read a permuted copy; fp32 and MXFP8 layers copy
+ *   (MXFP8 quantises while copying). */
 moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0,
                              int E_loc, moe_dtype dtype, const void* Wgu_packed, const uint8_t* Wgu_scale,
                              const void* Wd_packed, const uint8_t* Wd_scale, void* y, void* workspace,

@@ -59,6 +59,8 @@ _SIGS = {
     "moe_rows_hint": (_I, [_I, _I, _I]),
     "moe_grouped_mlp_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
+    "moe_expert_gemm1_swiglu_gather": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_quantize_mx_rows": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm_workspace_size": (_SZ, []),
     "moe_unpermute_combine": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
@@ -127,10 +129,13 @@ def moe_route_topk(logits: torch.Tensor, k: int, topk_ids=None, topk_probs=None)
     return ids, probs
 
 
-def alloc_permute(T: int, d: int, k: int, E_loc: int, x_dtype: torch.dtype, perm_dtype="bf16", device="cuda") -> dict:
-    """Output buffers of moe_permute."""
+def alloc_permute(T: int, d: int, k: int, E_loc: int, x_dtype: torch.dtype, perm_dtype="bf16", device="cuda",
+                  maps_only=False) -> dict:
+    """Output buffers of moe_permute (maps_only: no permuted copy of x)."""
     cap = n_cap(T, k, E_loc)
-    if _dt(perm_dtype) == MOE_MXFP8:
+    if maps_only:
+        perm_x = perm_sf = None
+    elif _dt(perm_dtype) == MOE_MXFP8:
         perm_x = torch.empty(cap, d, dtype=torch.uint8, device=device)
         perm_sf = torch.empty(max(1, _lib.moe_mx_act_scale_bytes(cap, d, E_loc)), dtype=torch.uint8, device=device)
     else:
@@ -145,11 +150,11 @@ def alloc_permute(T: int, d: int, k: int, E_loc: int, x_dtype: torch.dtype, perm
 
 
 def moe_permute(x: torch.Tensor, topk_ids: torch.Tensor, topk_probs: torch.Tensor, e0: int, E_loc: int,
-                perm_dtype="bf16", ws=None, out=None) -> dict:
+                perm_dtype="bf16", ws=None, out=None, maps_only=False) -> dict:
     T, d = x.shape
     k = topk_ids.shape[1]
     x_dt = MOE_F32 if x.dtype == torch.float32 else MOE_BF16
-    out = out if out is not None else alloc_permute(T, d, k, E_loc, x.dtype, perm_dtype, x.device)
+    out = out if out is not None else alloc_permute(T, d, k, E_loc, x.dtype, perm_dtype, x.device, maps_only)
     nb = _lib.moe_permute_workspace_size(T, k, E_loc)
     ws = ws if ws is not None else workspace(nb, x.device)
     _check("moe_permute", _lib.moe_permute(
@@ -246,6 +251,33 @@ def moe_expert_gemm1_swiglu(perm_x, perm_x_scale, offsets, row_prob, pw: PackedW
         _ptr(perm_x), _ptr(perm_x_scale), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f, pw.dtype,
         _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(h), _ptr(h_scale), int(rows_hint), _ptr(ws), ws.numel(), _stream()))
     return h, h_scale, ws
+
+
+def moe_expert_gemm1_swiglu_gather(x, x_scale, row_src_token, offsets, row_prob, pw: PackedWeights, h=None,
+                                   h_scale=None, ws=None):
+    """GEMM1 + scaled SwiGLU reading the token rows x (bf16, or E4M3 + row scales from
+    moe_quantize_mx_rows) through row_src_token."""
+    cap = row_src_token.shape[0]
+    if h is None:
+        h, h_scale = alloc_h(cap, pw, x.device)
+    ws = ws if ws is not None else workspace(_lib.moe_expert_gemm_workspace_size(), x.device)
+    _check("moe_expert_gemm1_swiglu_gather", _lib.moe_expert_gemm1_swiglu_gather(
+        _ptr(x), _ptr(x_scale), _ptr(row_src_token), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f,
+        pw.dtype, _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(h), _ptr(h_scale), _ptr(ws), ws.numel(), _stream()))
+    return h, h_scale, ws
+
+
+def moe_quantize_mx_rows(x: torch.Tensor, xq=None, x_scale=None, pair_to_row=None):
+    """E4M3 codes [T, d] and row-major E8M0 scales [T, d / 32] of the rows of x (with
+    pair_to_row: only the rows of tokens that have a local expert)."""
+    T, d = x.shape
+    x_dt = MOE_F32 if x.dtype == torch.float32 else MOE_BF16
+    xq = xq if xq is not None else torch.empty(T, d, dtype=torch.uint8, device=x.device)
+    x_scale = x_scale if x_scale is not None else torch.empty(T, d // 32, dtype=torch.uint8, device=x.device)
+    k = pair_to_row.shape[1] if pair_to_row is not None else 0
+    _check("moe_quantize_mx_rows", _lib.moe_quantize_mx_rows(_ptr(x), x_dt, T, d, _ptr(pair_to_row), k, _ptr(xq),
+                                                             _ptr(x_scale), _stream()))
+    return xq, x_scale
 
 
 def moe_expert_gemm2(h, h_scale, offsets, pw: PackedWeights, Y2=None, ws=None, rows_hint=0):

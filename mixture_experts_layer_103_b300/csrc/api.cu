@@ -26,6 +26,12 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
 cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
                             int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
                             uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
+                                   const int32_t* offsets, const float* row_prob, int E_loc, int d, int f, bool mx,
+                                   const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
+                                   uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_quant_rows_mx(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
+                                 uint8_t* xq, uint8_t* x_sf, cudaStream_t st);
 cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
@@ -128,6 +134,17 @@ static cudaError_t run_mlp(const void* perm_x, const uint8_t* perm_sf, const int
   return run_gemm2(s.h, s.h_sf, offsets, n_cap, E_loc, d, f, dt, Wd, Wd_sf, Y2, err, rows_hint, st);
 }
 
+// The bf16 layer reads x rows straight into GEMM1 (row gather) unless the CTA-pair GEMMs
+// are chosen; fp32 (SIMT) and MXFP8 take a permuted copy.  Measured on B300, the MXFP8
+// row-gather GEMM1 was 7-10 % slower than the TMA-fed one and quantising per token saved
+// nothing over quantising while copying, while bf16 gains: the permuted copy costs 27 us
+// at T = 4096, d = 2048, k = 8 and the gather adds less than that to GEMM1.
+static bool layer_gathers(moe_dtype dt, int T, int k, int E, int E_loc) {
+  const int64_t n_cap = n_cap_of(T, k, E_loc);
+  const int64_t rows = T > 0 && k > 0 && E > 0 ? static_cast<int64_t>(T) * k / E : 0;
+  return dt == MOE_BF16 && !use_pair(dt, n_cap, E_loc, static_cast<int>(rows));
+}
+
 // ---- whole-layer workspace -------------------------------------------------------------
 struct LayerWs {
   int32_t* err;
@@ -139,14 +156,15 @@ struct LayerWs {
   float* row_prob;
   int32_t* pair_to_row;
   uint8_t* perm_ws;
-  void* perm_x;
-  uint8_t* perm_sf;
+  void* perm_x;      // permuted copy (no row gather) or, MXFP8 row gather, E4M3 x [T, d]
+  uint8_t* perm_sf;  // its scales (SF tile layout, or row-major [T, d / 32] for the row gather)
   uint8_t* mlp;
   void* Y2;
   size_t total;
 };
-static LayerWs layer_layout(uint8_t* base, int T, int d, int f, int k, int E_loc, moe_dtype dt) {
+static LayerWs layer_layout(uint8_t* base, int T, int d, int f, int E, int k, int E_loc, moe_dtype dt) {
   const int64_t n_cap = n_cap_of(T, k, E_loc);
+  const bool gather = layer_gathers(dt, T, k, E, E_loc);
   LayerWs w{};
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -163,8 +181,13 @@ static LayerWs layer_layout(uint8_t* base, int T, int d, int f, int k, int E_loc
   w.row_prob = reinterpret_cast<float*>(take(static_cast<size_t>(n_cap) * 4));
   w.pair_to_row = reinterpret_cast<int32_t*>(take(static_cast<size_t>(T) * k * 4));
   w.perm_ws = take(permute_ws_bytes(T, E_loc));
-  w.perm_x = take(static_cast<size_t>(n_cap) * d * elt_bytes(dt));
-  w.perm_sf = dt == MOE_MXFP8 ? take(mx_act_sf_bytes(n_cap, d, E_loc)) : nullptr;
+  if (!gather) {
+    w.perm_x = take(static_cast<size_t>(n_cap) * d * elt_bytes(dt));
+    w.perm_sf = dt == MOE_MXFP8 ? take(mx_act_sf_bytes(n_cap, d, E_loc)) : nullptr;
+  } else if (dt == MOE_MXFP8) {
+    w.perm_x = take(static_cast<size_t>(T) * d);
+    w.perm_sf = take(static_cast<size_t>(T) * (d / 32));
+  }
   w.mlp = take(mlp_scratch_bytes(n_cap, E_loc, f, dt));
   w.Y2 = take(static_cast<size_t>(n_cap) * d * (dt == MOE_F32 ? 4 : 2));
   w.total = o;
@@ -229,14 +252,15 @@ static moe_status check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm
   if (T < 0 || d <= 0 || k < 1 || k > 32 || e0 < 0 || E_loc < 1 || E_loc > 1024 || e0 > (1 << 30))
     return MOE_ERR_INVALID_ARG;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!x || !ids || !probs || !perm_x || !rst || !rp || !p2r)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !ids || !probs || !rst || !rp || !p2r)) return MOE_ERR_INVALID_ARG;
   const bool ok_types = (x_dtype == MOE_F32 && perm_dtype == MOE_F32) || (x_dtype == MOE_BF16 && perm_dtype == MOE_BF16) ||
                         ((x_dtype == MOE_BF16 || x_dtype == MOE_F32) && perm_dtype == MOE_MXFP8);
   if (!ok_types) return MOE_ERR_UNSUPPORTED;
   if ((x_dtype == MOE_BF16 && d % 8 != 0) || (x_dtype == MOE_F32 && d % 4 != 0)) return MOE_ERR_UNSUPPORTED;
-  if (perm_dtype == MOE_MXFP8 && (d % 128 != 0 || (T > 0 && !perm_sf))) return perm_sf ? MOE_ERR_UNSUPPORTED
-                                                                                          : MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!aligned16(x) || !aligned16(perm_x))) return MOE_ERR_INVALID_ARG;
+  // perm_x == NULL: maps only (no permuted copy, so no scales either)
+  if (perm_dtype == MOE_MXFP8 && (d % 128 != 0 || (T > 0 && perm_x && !perm_sf)))
+    return (T > 0 && perm_x && !perm_sf) ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+  if (T > 0 && (!aligned16(x) || (perm_x && !aligned16(perm_x)))) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -334,6 +358,30 @@ moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_sca
                                Wgu_scale, h, h_scale, err, rows_hint, stream));
 }
 
+moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale, const int32_t* row_src_token,
+                                          const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc,
+                                          int d, int f, moe_dtype dtype, const void* Wgu_packed,
+                                          const uint8_t* Wgu_scale, void* h, uint8_t* h_scale, void* workspace,
+                                          size_t workspace_bytes, moe_stream_t stream) {
+  if (dtype == MOE_F32) return MOE_ERR_UNSUPPORTED;
+  moe_status s = check_gemm_common(N_cap, E_loc, d, f, dtype, offsets, x, x_scale, Wgu_packed, Wgu_scale, h, h_scale);
+  if (s != MOE_OK) return s;
+  if (N_cap > 0 && (!row_src_token || !row_prob || (dtype == MOE_MXFP8 && !h_scale))) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+  if (N_cap == 0) return MOE_OK;
+  return cuda_status(launch_tc_gemm1_gather(x, x_scale, row_src_token, offsets, row_prob, E_loc, d, f,
+                                            dtype == MOE_MXFP8, Wgu_packed, Wgu_scale, h, h_scale,
+                                            static_cast<int32_t*>(workspace), kTimeoutNs, stream));
+}
+
+moe_status moe_quantize_mx_rows(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
+                                uint8_t* xq, uint8_t* x_scale, moe_stream_t stream) {
+  if (T < 0 || d <= 0 || (pair_to_row && (k < 1 || k > 32))) return MOE_ERR_INVALID_ARG;
+  if ((x_dtype != MOE_BF16 && x_dtype != MOE_F32) || d % 32 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && (!x || !xq || !x_scale || !aligned16(x) || !aligned16(xq))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quant_rows_mx(x, x_dtype, T, d, pair_to_row, k, xq, x_scale, stream));
+}
+
 moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t* offsets, int64_t N_cap, int E_loc,
                             int d, int f, moe_dtype dtype, const void* Wd_packed, const uint8_t* Wd_scale, void* Y2,
                             int rows_hint, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
@@ -357,7 +405,7 @@ moe_status moe_unpermute_combine(const void* Y2, const int32_t* pair_to_row, int
 size_t moe_layer_workspace_size(int T, int d, int f, int E, int k, int E_loc, moe_dtype dtype) {
   if (T < 0 || d <= 0 || f <= 0 || E < 1 || k < 1 || E_loc < 1) return 0;
   (void)E;
-  return layer_layout(nullptr, T, d, f, k, E_loc, dtype).total;
+  return layer_layout(nullptr, T, d, f, E, k, E_loc, dtype).total;
 }
 
 moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0, int E_loc,
@@ -375,16 +423,33 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
   if (dtype == MOE_F32 && d % 4 != 0) return MOE_ERR_UNSUPPORTED;
   const size_t need = moe_layer_workspace_size(T, d, f, E, k, E_loc, dtype);
   if (!workspace || !aligned256(workspace) || workspace_bytes < need) return MOE_ERR_WORKSPACE;
-  LayerWs w = layer_layout(static_cast<uint8_t*>(workspace), T, d, f, k, E_loc, dtype);
+  LayerWs w = layer_layout(static_cast<uint8_t*>(workspace), T, d, f, E, k, E_loc, dtype);
   const int64_t n_cap = n_cap_of(T, k, E_loc);
   const moe_dtype x_dtype = dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
+  const int hint = moe_rows_hint(T, k, E);
   cudaError_t e = launch_route_topk(logits, T, E, k, w.topk_ids, w.topk_probs, stream);
-  if (e == cudaSuccess)
-    e = launch_permute(x, x_dtype, dtype, T, d, w.topk_ids, w.topk_probs, k, e0, E_loc, w.perm_x, w.perm_sf, w.counts,
-                       w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
-  if (e == cudaSuccess)
-    e = run_mlp(w.perm_x, w.perm_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale,
-                Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, moe_rows_hint(T, k, E), stream);
+  if (layer_gathers(dtype, T, k, E, E_loc)) {
+    // maps only, then GEMM1 reads the token rows (quantised once per token for MXFP8)
+    if (e == cudaSuccess)
+      e = launch_permute(x, x_dtype, dtype, T, d, w.topk_ids, w.topk_probs, k, e0, E_loc, nullptr, nullptr,
+                         w.counts, w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
+    const bool mx = dtype == MOE_MXFP8;
+    if (e == cudaSuccess && mx)
+      e = launch_quant_rows_mx(x, x_dtype, T, d, w.pair_to_row, k, static_cast<uint8_t*>(w.perm_x), w.perm_sf, stream);
+    MlpScratch s = carve_mlp(w.mlp, n_cap, f, dtype);
+    if (e == cudaSuccess && n_cap > 0)
+      e = launch_tc_gemm1_gather(mx ? w.perm_x : x, w.perm_sf, w.row_src_token, w.offsets, w.row_prob, E_loc, d, f,
+                                 mx, Wgu_packed, Wgu_scale, s.h, s.h_sf, w.err, kTimeoutNs, stream);
+    if (e == cudaSuccess)
+      e = run_gemm2(s.h, s.h_sf, w.offsets, n_cap, E_loc, d, f, dtype, Wd_packed, Wd_scale, w.Y2, w.err, hint, stream);
+  } else {
+    if (e == cudaSuccess)
+      e = launch_permute(x, x_dtype, dtype, T, d, w.topk_ids, w.topk_probs, k, e0, E_loc, w.perm_x, w.perm_sf,
+                         w.counts, w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
+    if (e == cudaSuccess)
+      e = run_mlp(w.perm_x, w.perm_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale,
+                  Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, hint, stream);
+  }
   if (e == cudaSuccess) e = launch_combine(w.Y2, w.pair_to_row, T, k, d, dtype, y, stream);
   return cuda_status(e);
 }

@@ -188,8 +188,8 @@ struct BMaps {
   CUtensorMap b256, b128, b64, b32;
 };
 
-template <bool MX, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+template <bool MX, int EPI, bool GATHER>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATHER ? kGatherThreads : 0), 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BMaps tmB,
                            const GemmArgs g) {
   using C = GemmSmem<MX>;
@@ -215,7 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::MAX_STAGES; ++s) {
-      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(full_bar(s), GATHER ? 1 + kGatherThreads : 1);  // + every gather thread
       ptx::mbar_init(empty_bar(s), 2);  // the MMA issuers of both CTAs
     }
     for (int a = 0; a < 2; ++a) {
@@ -225,7 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     ptx::mbar_init(drain_bar, 1);
     *s_abort = 0;
     ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&tmA);
+    if (!GATHER) ptx::prefetch_tmap(&tmA);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
@@ -269,8 +269,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
           const uint32_t fb = full_bar(s);
           const uint32_t st_addr = sbase + C::OFF_PIPE + s * stage_bytes;
-          ptx::mbar_arrive_expect_tx(fb, stage_bytes + (MX ? 512 + sfb_bytes : 0));
-          ptx::tma_load_3d(st_addr, &tmA, fb, kb * C::BK, tl.row0, 0);
+          // in row-gather mode the gather warps fill A (and its scales) themselves
+          ptx::mbar_arrive_expect_tx(fb, (GATHER ? BN * kRowBytes : stage_bytes) + (MX ? (GATHER ? 0 : 512) + sfb_bytes : 0));
+          if (!GATHER) ptx::tma_load_3d(st_addr, &tmA, fb, kb * C::BK, tl.row0, 0);
           if (ut.shared_b)  // this CTA's half of the weight tile, to both CTAs
             ptx::tma_load_3d_mc(st_addr + C::A_BYTES + rank * (BN / 2) * kRowBytes, tmb_half, fb, kb * C::BK,
                                 tl.n0 + rank * (BN / 2), tl.e, both);
@@ -279,7 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if constexpr (MX) {
             const int kg = g.K / 128;
             const uint32_t sf_addr = sbase + C::OFF_SF + s * C::SF_STAGE_BYTES;
-            ptx::bulk_load(sf_addr, g.a_sf + (static_cast<int64_t>(tl.mt) * kg + kb) * 512, 512, fb);
+            if (!GATHER) ptx::bulk_load(sf_addr, g.a_sf + (static_cast<int64_t>(tl.mt) * kg + kb) * 512, 512, fb);
             ptx::bulk_load(sf_addr + 512,
                            g.b_sf + ((static_cast<int64_t>(tl.e) * kg + kb) * (g.n_out / 128) + tl.n0 / 128) * 512,
                            sfb_bytes, fb);
@@ -310,6 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!ptx::mbar_wait(full_bar(s), ph, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
+          if (GATHER) ptx::fence_proxy_async_smem();  // gathered rows were written by cp.async
           ptx::tc_fence_after();
           const uint32_t a_addr = sbase + C::OFF_PIPE + s * stage_bytes;
           const uint32_t b_addr = a_addr + C::A_BYTES;
@@ -339,7 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       ptx::mma_commit(drain_bar);  // every MMA issued by this thread has completed
       ptx::mbar_wait(drain_bar, 0, g.timeout_ns);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int it = 0;
@@ -361,6 +363,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
     }
+  } else if constexpr (GATHER) {
+    // ------------------------------------------------------------------ A gather
+    // Thread gt copies 16-byte chunk (gt % 8) of the rows gt / 8 + 16 i (i < 8) of each
+    // stage's 128 x 128-byte A tile straight from the source rows (cp.async), into the
+    // 128-byte swizzled layout a TMA load would produce (chunk c of row r at
+    // r * 128 + (c ^ r % 8) * 16), and in MXFP8 mode the 4 scale bytes of row gt into the
+    // stage's SF atom.  Each thread's copies of a stage arrive on the stage's full barrier
+    // when they land (cp.async.mbarrier.arrive), so the gather runs as far ahead as the
+    // ring allows; the MMA issuer fences to the async proxy after its full-barrier wait.
+    constexpr int elt = MX ? 1 : 2;
+    const int gt = threadIdx.x - kGemmThreads;
+    const int chunk = gt & 7, rbase = gt >> 3;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int u = cluster; u < units && ok; u += clusters) {
+      const UnitTile ut = decode_unit(u, rank, n_tiles_n, BN, s_off, s_mtp, s_odd, g.E_loc);
+      const Tile& tl = ut.t;
+      const uint8_t* src[8];
+      uint32_t live = 0;  // bit i: row rbase + 16 i lies in the tile
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rbase + 16 * i;
+        const bool v = r < tl.rows;
+        const int64_t tok = v ? __ldg(g.row_token + tl.row0 + r) : 0;
+        src[i] = g.gx + tok * g.gx_ld + chunk * 16;
+        live |= static_cast<uint32_t>(v) << i;
+      }
+      const uint8_t* sf_src = nullptr;
+      if constexpr (MX) {
+        const int64_t tok = gt < tl.rows ? __ldg(g.row_token + tl.row0 + gt) : 0;
+        sf_src = g.gx_sf + tok * g.gx_sf_ld;
+      }
+      for (int kb = 0; kb < num_kb; ++kb) {
+        int okw = 0;
+        if (lane == 0) okw = *s_abort ? 0 : (ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns) ? 1 : 2);
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (okw != 1) {
+          if (okw == 2 && lane == 0) gemm_abort(g, s_abort);
+          ok = false;
+          break;
+        }
+        (void)ptx::mbar_try_wait(empty_bar(s), ph ^ 1u);  // completed phase: acquire for every lane
+        const uint32_t a_addr = sbase + C::OFF_PIPE + s * stage_bytes;
+        const int64_t kbyte = static_cast<int64_t>(kb) * C::BK * elt + chunk * 16;
+        const bool kin = kbyte < static_cast<int64_t>(g.K) * elt;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = rbase + 16 * i;
+          const bool v = kin && ((live >> i) & 1u);
+          ptx::cp_async_16(a_addr + r * kRowBytes + ((chunk ^ (r & 7)) << 4), v ? src[i] + kb * C::BK * elt : g.gx,
+                           v ? 16u : 0u);
+        }
+        if constexpr (MX) {
+          const uint32_t sf_addr = sbase + C::OFF_SF + s * C::SF_STAGE_BYTES + (gt & 31) * 16 + (gt >> 5) * 4;
+          const bool v = gt < tl.rows;
+          ptx::cp_async_4(sf_addr, v ? sf_src + kb * 4 : g.gx_sf, v ? 4u : 0u);
+        }
+        ptx::cp_async_arrive_noinc(full_bar(s));
+        if (++s == stages) { s = 0; ph ^= 1u; }
+      }
+    }
+    ptx::cp_async_wait_all();  // nothing of ours may still be landing when the CTA exits
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -403,18 +468,20 @@ bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, ui
   return r == CUDA_SUCCESS;
 }
 
-template <bool MX, int EPI>
+// A: the permuted rows [a_rows, K] (TMA), or unused (nullptr) in row-gather mode.
+template <bool MX, int EPI, bool GATHER = false>
 static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
                                     cudaStream_t st) {
   using C = GemmSmem<MX>;
-  CUtensorMap ta;
+  constexpr int threads = kGemmThreads + (GATHER ? kGatherThreads : 0);
+  CUtensorMap ta = {};
   BMaps tb;
-  if (!make_operand_map(&ta, A, MX, g.K, a_rows, 1, kBM)) return cudaErrorInvalidValue;
+  if (!GATHER && !make_operand_map(&ta, A, MX, g.K, a_rows, 1, kBM)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b256, B, MX, g.K, g.n_out, g.E_loc, 256)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b128, B, MX, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b64, B, MX, g.K, g.n_out, g.E_loc, 64)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b32, B, MX, g.K, g.n_out, g.E_loc, 32)) return cudaErrorInvalidValue;
-  auto kern = tc_grouped_gemm_kernel<MX, EPI>;
+  auto kern = tc_grouped_gemm_kernel<MX, EPI, GATHER>;
   // Once per device: opt in to > 48 KB of dynamic shared memory and size the grid to the
   // clusters of two that can be resident at once (keeps later launches, including ones
   // recorded into a CUDA graph, free of non-launch API calls).
@@ -428,7 +495,7 @@ static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms()));
-    cfg.blockDim = dim3(kGemmThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) {
@@ -438,7 +505,7 @@ static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B
     grid = 2 * std::min(clusters, num_sms() / 2);
     if (dev >= 0 && dev < 64) grid_of[dev] = grid;
   }
-  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kGemmThreads), C::SMEM_BYTES, st, ta, tb, g);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(threads), C::SMEM_BYTES, st, ta, tb, g);
 }
 
 static GemmArgs base_args(const int32_t* offsets, int E_loc, int32_t* err, uint64_t timeout_ns) {
@@ -473,6 +540,30 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
   if (mx) return launch_gemm_inst<true, EPI_SWIGLU_MX>(perm_x, N_cap, Wgu, g, st);
   if (pair) return launch_pair_gemm(perm_x, N_cap, Wgu, g, true, st);
   return launch_gemm_inst<false, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
+}
+
+// GEMM1 + fused scaled SwiGLU with A gathered from the token rows: row r of the
+// expert-ordered operand is x row row_src_token[r] (bf16 [T, d]; MXFP8: E4M3 [T, d] with
+// E8M0 scales x_sf [T, d / 32]), so no permuted copy of x is ever written.
+cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
+                                   const int32_t* offsets, const float* row_prob, int E_loc, int d, int f, bool mx,
+                                   const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
+                                   uint64_t timeout_ns, cudaStream_t st) {
+  GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
+  g.n_out = 2 * f;
+  g.K = d;
+  g.out = h;
+  g.ld_out = f;
+  g.out_sf = h_sf;
+  g.row_prob = row_prob;
+  g.b_sf = Wgu_sf;
+  g.gx = static_cast<const uint8_t*>(x);
+  g.gx_ld = static_cast<int64_t>(d) * (mx ? 1 : 2);
+  g.row_token = row_src_token;
+  g.gx_sf = x_sf;
+  g.gx_sf_ld = d / 32;
+  if (mx) return launch_gemm_inst<true, EPI_SWIGLU_MX, true>(nullptr, 0, Wgu, g, st);
+  return launch_gemm_inst<false, EPI_SWIGLU_BF16, true>(nullptr, 0, Wgu, g, st);
 }
 
 // GEMM2 on the tensor cores: h [N_cap, f] (bf16, or E4M3 + SF) -> Y2 bf16 [N_cap, d].

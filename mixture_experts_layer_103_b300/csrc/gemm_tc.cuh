@@ -12,7 +12,8 @@ namespace moe {
 
 constexpr int kBM = 128;
 constexpr int kRowBytes = 128;  // bytes of one operand row per pipeline stage
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 192;        // producer, MMA, 4 epilogue warps
+constexpr int kGatherThreads = 128;      // + 4 A-gather warps in row-gather mode
 constexpr int kMaxEloc = 1024;
 
 enum { EPI_STORE_BF16 = 0, EPI_SWIGLU_BF16 = 1, EPI_SWIGLU_MX = 2 };
@@ -30,6 +31,14 @@ struct GemmArgs {
   const uint8_t* b_sf;     // MXFP8: scales of B (weight SF tile layout)
   int32_t* err;            // device error word
   uint64_t timeout_ns;
+  // Row-gather mode (GEMM1 only): A row r of the tile is row row_token[r] of gx
+  // (gx_ld bytes per row) instead of row r of a permuted copy; MXFP8 takes its scales
+  // from gx_sf (gx_sf_ld bytes per row, one E8M0 byte per 32 values).
+  const uint8_t* gx;
+  int64_t gx_ld;
+  const int32_t* row_token;
+  const uint8_t* gx_sf;
+  int64_t gx_sf_ld;
 };
 
 struct Tile {

@@ -12,9 +12,15 @@
 //   gather  one warp per permuted row copies x[t] with 16-byte vector loads/stores (HBM
 //           bound); in MXFP8 mode it quantises each 32-value block while copying ("MXFP8
 //           Precision Reduces Memory Footprint": one scale per 32 consecutive values).
+//           Skipped when no permuted copy is asked for (the row-gather GEMM1 reads x
+//           through row_src_token instead); MXFP8 then quantises x once per token.
+#include <algorithm>
+
 #include "moe_common.cuh"
 
 namespace moe {
+
+int num_sms();
 
 constexpr int kPermTile = 256;  // tokens per tile (count / scatter)
 
@@ -165,8 +171,60 @@ __global__ void __launch_bounds__(256) perm_gather_copy_kernel(const uint4* __re
   }
 }
 
-// Row copy with MXFP8 quantisation (blocks of 32 along d).  IN = 1: bf16 input (8 values
-// per 16-byte vector, 4 lanes per block); IN = 0: fp32 input (4 per vector, 8 lanes).
+// MXFP8 quantisation of one row by one warp (blocks of 32 along d).  IN_BF16 = 1: bf16
+// input (8 values per 16-byte vector, 4 lanes per block); 0: fp32 input (4 per vector, 8
+// lanes).  E4M3 codes go to dst; the E8M0 byte of the block holding column col is passed
+// to put_sf(col, byte) by the first lane of the block.
+template <int IN_BF16, typename PutSf>
+__device__ __forceinline__ void quantize_row_mx(const uint4* __restrict__ src, int d, int lane, uint8_t* __restrict__ dst,
+                                                PutSf put_sf) {
+  constexpr int VPV = IN_BF16 ? 8 : 4;  // values per 16-byte vector
+  constexpr int LPB = 32 / VPV;         // lanes per 32-value block
+  const int row_vecs = d / VPV;
+  for (int base = 0; base < row_vecs; base += 32) {
+    const int c = base + lane;
+    const bool act = c < row_vecs;
+    float v[VPV];
+    if (act) {
+      const uint4 q = __ldg(src + c);
+      if (IN_BF16) {
+        v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+        v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
+      } else {
+        v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+        v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < VPV; ++u) v[u] = 0.0f;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int u = 0; u < VPV; ++u) amax = fmaxf(amax, fabsf(v[u]));
+#pragma unroll
+    for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const int X = mx_exponent(amax);
+    const float inv = mx_inv_scale(X);
+    if (act) {
+      if (IN_BF16) {
+        uint2 o;
+        o.x = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
+              (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
+        o.y = static_cast<uint32_t>(e4m3x2(v[4] * inv, v[5] * inv)) |
+              (static_cast<uint32_t>(e4m3x2(v[6] * inv, v[7] * inv)) << 16);
+        *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(c) * 8) = o;
+      } else {
+        const uint32_t o = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
+                           (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
+        *reinterpret_cast<uint32_t*>(dst + static_cast<int64_t>(c) * 4) = o;
+      }
+      if ((lane % LPB) == 0) put_sf(c * VPV, static_cast<uint8_t>(X + 127));
+    }
+  }
+}
+
+// Row copy with MXFP8 quantisation into the permuted order (scales in the activation SF
+// tile layout of the expert m-tiles).
 template <int IN_BF16>
 __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __restrict__ x, int d,
                                                              const int32_t* __restrict__ offsets, int E_loc,
@@ -175,8 +233,7 @@ __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __rest
                                                              uint8_t* __restrict__ perm_x, uint8_t* __restrict__ perm_sf) {
   pdl_launch_dependents();
   pdl_wait();
-  constexpr int VPV = IN_BF16 ? 8 : 4;  // values per 16-byte vector
-  constexpr int LPB = 32 / VPV;         // lanes per 32-value block
+  constexpr int VPV = IN_BF16 ? 8 : 4;
   extern __shared__ int32_t s_tab[];    // offsets [E_loc+1], mtile_base [E_loc+1]
   for (int i = threadIdx.x; i <= E_loc; i += blockDim.x) {
     s_tab[i] = offsets[i];
@@ -199,49 +256,41 @@ __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __rest
     const int64_t tile = s_tab[E_loc + 1 + lo] + il / 128;
     const int i = il % 128;
     const int64_t t = __ldg(row_src_token + r);
-    const uint4* src = x + t * row_vecs;
-    uint8_t* dst = perm_x + r * d;
-    for (int base = 0; base < row_vecs; base += 32) {
-      const int c = base + lane;
-      const bool act = c < row_vecs;
-      float v[VPV];
-      if (act) {
-        const uint4 q = __ldg(src + c);
-        if (IN_BF16) {
-          v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
-          v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
-        } else {
-          v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
-          v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < VPV; ++u) v[u] = 0.0f;
-      }
-      float amax = 0.0f;
-#pragma unroll
-      for (int u = 0; u < VPV; ++u) amax = fmaxf(amax, fabsf(v[u]));
-#pragma unroll
-      for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const int X = mx_exponent(amax);
-      const float inv = mx_inv_scale(X);
-      if (act) {
-        if (IN_BF16) {
-          uint2 o;
-          o.x = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
-                (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
-          o.y = static_cast<uint32_t>(e4m3x2(v[4] * inv, v[5] * inv)) |
-                (static_cast<uint32_t>(e4m3x2(v[6] * inv, v[7] * inv)) << 16);
-          *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(c) * 8) = o;
-        } else {
-          const uint32_t o = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
-                             (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
-          *reinterpret_cast<uint32_t*>(dst + static_cast<int64_t>(c) * 4) = o;
-        }
-        if ((lane % LPB) == 0) perm_sf[sf_act_offset(tile, i, c * VPV, d)] = static_cast<uint8_t>(X + 127);
-      }
-    }
+    quantize_row_mx<IN_BF16>(x + t * row_vecs, d, lane, perm_x + r * d,
+                             [&](int col, uint8_t b) { perm_sf[sf_act_offset(tile, i, col, d)] = b; });
   }
+}
+
+// MXFP8 quantisation of token rows in place order: xq [T, d] E4M3 and row-major scales
+// x_sf [T, d / 32] (the source of the row-gather GEMM1).  With pair_to_row [T, k], only
+// tokens routed to at least one local expert are quantised (the others are never read).
+template <int IN_BF16>
+__global__ void __launch_bounds__(256) quant_rows_mx_kernel(const uint4* __restrict__ x, int T, int d,
+                                                            const int32_t* __restrict__ pair_to_row, int k,
+                                                            uint8_t* __restrict__ xq, uint8_t* __restrict__ x_sf) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int VPV = IN_BF16 ? 8 : 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int row_vecs = d / VPV;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+    if (pair_to_row) {
+      const bool local = lane < k && __ldg(pair_to_row + t * k + lane) >= 0;
+      if (!__any_sync(0xffffffffu, local)) continue;
+    }
+    uint8_t* sf_row = x_sf + t * (d / 32);
+    quantize_row_mx<IN_BF16>(x + t * row_vecs, d, lane, xq + t * d, [&](int col, uint8_t b) { sf_row[col / 32] = b; });
+  }
+}
+
+cudaError_t launch_quant_rows_mx(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
+                                 uint8_t* xq, uint8_t* x_sf, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ceil_div(T, 8), static_cast<int64_t>(num_sms()) * 8));
+  cudaError_t e = launch_pdl(x_dtype == MOE_BF16 ? quant_rows_mx_kernel<1> : quant_rows_mx_kernel<0>, dim3(grid),
+                             dim3(256), 0, st, static_cast<const uint4*>(x), T, d, pair_to_row, k, xq, x_sf);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 struct PermuteWs {
@@ -287,7 +336,9 @@ cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtyp
                    row_prob);
     if (e != cudaSuccess) return e;
     const int grid = gather_grid(st);
-    if (perm_dtype == MOE_MXFP8) {
+    if (perm_x == nullptr) {
+      // maps only: the row-gather GEMM reads x through row_src_token
+    } else if (perm_dtype == MOE_MXFP8) {
       const size_t sm = static_cast<size_t>(2 * (E_loc + 1)) * 4;
       e = launch_pdl(x_dtype == MOE_BF16 ? perm_gather_mx_kernel<1> : perm_gather_mx_kernel<0>, dim3(grid), dim3(256),
                      sm, st, static_cast<const uint4*>(x), d, static_cast<const int32_t*>(offsets), E_loc,

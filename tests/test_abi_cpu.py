@@ -56,8 +56,18 @@ def test_sizes(lib):
     assert L.moe_mx_act_scale_bytes(1000, 256, 8) == (8 + 8) * 2 * 512
     assert L.moe_permute_workspace_size(4096, 8, 64) > 256
     big = L.moe_layer_workspace_size(4096, 2048, 1024, 64, 8, 64, 1)
-    # perm_x + Y2 (bf16) + h dominate: N_cap = 32768
-    assert big >= 32768 * 2048 * 2 * 2 + 32768 * 1024 * 2
+    # bf16 rows are gathered into GEMM1, so Y2 (bf16) + h dominate (N_cap = 32768) and no
+    # permuted copy of x is held
+    assert 32768 * 2048 * 2 + 32768 * 1024 * 2 <= big < 2 * 32768 * 2048 * 2 + 32768 * 1024 * 2
+    # fp32 copies the rows: perm_x + Y2 + h
+    f32 = L.moe_layer_workspace_size(4096, 2048, 1024, 64, 8, 64, 0)
+    assert f32 >= 32768 * 2048 * 4 * 2 + 32768 * 1024 * 4
+    # tall segments (T * k / E >= 2048) pick the CTA-pair GEMMs, which read a permuted copy
+    tall = L.moe_layer_workspace_size(2048, 256, 256, 8, 8, 8, 1)
+    assert tall >= 16384 * 256 * 2 * 2 + 16384 * 256 * 2
+    # MXFP8 copies while quantising: E4M3 perm_x + Y2 (bf16) + E4M3 h
+    mx = L.moe_layer_workspace_size(4096, 2048, 1024, 64, 8, 64, 2)
+    assert mx >= 32768 * 2048 + 32768 * 2048 * 2 + 32768 * 1024
     assert L.moe_expert_gemm_workspace_size() == 256
 
 
@@ -108,5 +118,16 @@ def test_validation_before_any_launch(lib):
     assert L.moe_workspace_init(_null(), 256, s) == 3
     assert L.moe_workspace_init(ctypes.c_void_p(272), 256, s) == 3
     assert L.moe_workspace_init(P, 16, s) == 3
+    # row-gather GEMM1: fp32 unsupported, null row map, bf16 d % 8
+    assert L.moe_expert_gemm1_swiglu_gather(P, None, P, P, P, 64, 4, 64, 64, 0, P, None, P, None, P, 256, s) == 2
+    assert L.moe_expert_gemm1_swiglu_gather(P, None, None, P, P, 64, 4, 64, 64, 1, P, None, P, None, P, 256, s) == 1
+    assert L.moe_expert_gemm1_swiglu_gather(P, None, P, P, P, 64, 4, 60, 64, 1, P, None, P, None, P, 256, s) == 2
+    assert L.moe_expert_gemm1_swiglu_gather(P, None, P, P, P, 64, 4, 64, 64, 1, P, None, P, None, _null(), 256,
+                                            s) == 3
+    # MXFP8 row quantiser: d % 32, negative T, wrong source type
+    assert L.moe_quantize_mx_rows(P, 1, 4, 48, None, 0, P, P, s) == 2
+    assert L.moe_quantize_mx_rows(P, 1, -1, 64, None, 0, P, P, s) == 1
+    assert L.moe_quantize_mx_rows(P, 2, 4, 64, None, 0, P, P, s) == 2
+    assert L.moe_quantize_mx_rows(P, 1, 4, 64, P, 33, P, P, s) == 1
     # device error read: null output
     assert L.moe_get_device_error(P, s, None) == 1

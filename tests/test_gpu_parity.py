@@ -352,3 +352,71 @@ def test_pair_kernel_matches_oracle(moe, name, counts, d, f):
     for hint, y in ys.items():
         assert rel_l2(to_np(y), yo) <= TOL["bf16"], hint
     assert rel_l2(to_np(ys[4096]), to_np(ys[1])) <= 1e-2
+
+
+# ----------------------------------------------------------------------------- row-gather GEMM1
+def _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd):
+    """GEMM1 reading x through row_src_token must equal GEMM1 on the permuted copy, bit for
+    bit (same operand values, same MMA order); MXFP8 compares through GEMM2 (h scales live
+    in the SF tile layout, whose pad bytes are unspecified)."""
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), w.dtype)
+    xd = to_dev(x)
+    ids, probs = moe.moe_route_topk(to_dev(lg), w.k)
+    P = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, w.dtype)
+    M = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, w.dtype, maps_only=True)
+    torch.cuda.synchronize()
+    N = int(P["offsets"][-1])
+    for key in ("counts", "offsets", "pair_to_row"):
+        assert torch.equal(P[key], M[key]), key
+    assert torch.equal(P["row_src_token"][:N], M["row_src_token"][:N])
+    assert torch.equal(P["row_prob"][:N], M["row_prob"][:N])
+    h1, hs1, _ = moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw,
+                                             rows_hint=1)
+    if w.dtype == "mxfp8":
+        xq, xs = moe.moe_quantize_mx_rows(xd, pair_to_row=M["pair_to_row"])
+        torch.cuda.synchronize()
+        rst = M["row_src_token"][:N].long()
+        assert torch.equal(P["perm_x"][:N], xq[rst])  # one quantisation rule, per row or per token
+        h2, hs2, ws = moe.moe_expert_gemm1_swiglu_gather(xq, xs, M["row_src_token"], M["offsets"], M["row_prob"], pw)
+    else:
+        h2, hs2, ws = moe.moe_expert_gemm1_swiglu_gather(xd, None, M["row_src_token"], M["offsets"], M["row_prob"], pw)
+    Y1, _ = moe.moe_expert_gemm2(h1, hs1, P["offsets"], pw, rows_hint=1)
+    Y2, _ = moe.moe_expert_gemm2(h2, hs2, M["offsets"], pw, rows_hint=1)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    assert torch.equal(h1[:N], h2[:N])
+    assert torch.equal(Y1[:N], Y2[:N])
+    return N
+
+
+GATHER_SMALL = ["bf16_a", "bf16_ragged", "bf16_e64", "bf16_ep64", "bf16_zipf", "mx_a", "mx_ragged", "mx_zipf"]
+
+
+@pytest.mark.parametrize("name", GATHER_SMALL)
+def test_gather_gemm1_matches_permuted_copy(moe, name):
+    w = {c.name: c for c in SMALL}[name]
+    Wg, Wu, Wd = gen_weights(w)
+    assert _gather_vs_copy(moe, w, gen_x(w), gen_logits(w), Wg, Wu, Wd) > 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
+def test_gather_gemm1_odd_units(moe, dtype):
+    """Forced segments of 1..5 m-tiles (odd and even) with odd n-tile counts."""
+    counts = [1, 129, 300, 640, 0, 385, 128, 257]
+    d, f = (256, 256) if dtype == "mxfp8" else (192, 160)
+    lg = _forced_logits(counts, len(counts), seed=5)
+    w = Workload("gather_odd", lg.shape[0], d, f, len(counts), 1, 0, len(counts), dtype)
+    Wg, Wu, Wd = gen_weights(w)
+    assert _gather_vs_copy(moe, w, gen_x(w), lg, Wg, Wu, Wd) == sum(counts)
+
+
+def test_quantize_rows_matches_oracle(moe):
+    """moe_quantize_mx_rows against the oracle's quantiser (codes and scale bytes)."""
+    w = Workload("q", 37, 256, 128, 8, 2, 0, 8, "mxfp8")
+    x = gen_x(w)
+    xq, xs = moe.moe_quantize_mx_rows(to_dev(x))
+    torch.cuda.synchronize()
+    assert x.dtype == np.uint16  # bf16 storage
+    codes, scales = oracle.mx_quantize(x, "bf16", (w.T, w.d, 1))
+    np.testing.assert_array_equal(xq.cpu().numpy(), codes)
+    np.testing.assert_array_equal(xs.cpu().numpy(), scales.reshape(w.T, w.d // 32))
