@@ -4,7 +4,8 @@
 //
 // Row offsets[e] + r holds the r-th token (ascending token id) routed to local expert e.
 // Positions are fixed without atomics so the result is deterministic:
-//   count   per 256-token tile, per-expert counts (shared-memory counters; order-free)
+//   count   per tile of 64 or 256 tokens, per-expert counts (shared-memory counters;
+//           order-free)
 //   scan    one CTA: exclusive scan over (expert, tile) in expert-major order gives each
 //           (expert, tile) its first row; offsets and the MXFP8 m-tile bases fall out
 //   scatter per tile, the rank of token t among the tile's tokens routed to e is the
@@ -22,16 +23,26 @@ namespace moe {
 
 int num_sms();
 
-constexpr int kPermTile = 256;  // tokens per tile (count / scatter)
+// Tokens per tile of the count and scatter kernels: 64 while the (expert, tile) count
+// table stays small (more CTAs for these latency-bound kernels), else 256 (a shorter
+// one-CTA scan).
+constexpr int kPermTileSmall = 64, kPermTileLarge = 256;
+constexpr int64_t kSmallTileTable = 16384;  // max E_loc * tiles for the 64-token tiles
 
-__global__ void __launch_bounds__(kPermTile) perm_count_kernel(const int32_t* __restrict__ ids, int T, int k, int e0,
+static int perm_tile(int T, int E_loc) {
+  const int64_t n = ceil_div(T > 0 ? T : 1, kPermTileSmall) * static_cast<int64_t>(E_loc);
+  return n <= kSmallTileTable ? kPermTileSmall : kPermTileLarge;
+}
+
+template <int TILE>
+__global__ void __launch_bounds__(TILE) perm_count_kernel(const int32_t* __restrict__ ids, int T, int k, int e0,
                                                                int E_loc, int n_tiles, int32_t* __restrict__ tile_counts) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ int s_cnt[];
   for (int e = threadIdx.x; e < E_loc; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kPermTile + threadIdx.x;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * TILE + threadIdx.x;
   if (t < T)
     for (int j = 0; j < k; ++j) {
       const int e = __ldg(ids + t * k + j) - e0;
@@ -78,14 +89,22 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ t
   __shared__ int s_off[1025];
   const int n = E_loc * n_tiles;
   int carry = 0;
-  for (int base = 0; base < n; base += blockDim.x) {
-    const int i = base + threadIdx.x;
-    const int v = i < n ? tile_counts[i] : 0;
+  // 4 consecutive entries per thread: 4096 entries per pass
+  for (int base = 0; base < n; base += 4 * blockDim.x) {
+    const int i0 = base + 4 * threadIdx.x;
+    int v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = i0 + q < n ? tile_counts[i0 + q] : 0;
     int total;
-    const int ex = block_exclusive_scan(v, s_warp, total);
-    if (i < n) {
-      tile_counts[i] = carry + ex;  // first row of (expert i / n_tiles, tile i % n_tiles)
-      if (i % n_tiles == 0) s_off[i / n_tiles] = carry + ex;
+    int run = carry + block_exclusive_scan(v[0] + v[1] + v[2] + v[3], s_warp, total);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q;
+      if (i < n) {
+        tile_counts[i] = run;  // first row of (expert i / n_tiles, tile i % n_tiles)
+        if (i % n_tiles == 0) s_off[i / n_tiles] = run;
+      }
+      run += v[q];
     }
     carry += total;
   }
@@ -108,7 +127,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ t
   }
 }
 
-__global__ void __launch_bounds__(kPermTile) perm_scatter_kernel(const int32_t* __restrict__ ids,
+template <int TILE>
+__global__ void __launch_bounds__(TILE) perm_scatter_kernel(const int32_t* __restrict__ ids,
                                                                  const float* __restrict__ probs, int T, int k, int e0,
                                                                  int E_loc, int n_tiles,
                                                                  const int32_t* __restrict__ tile_base,
@@ -117,12 +137,12 @@ __global__ void __launch_bounds__(kPermTile) perm_scatter_kernel(const int32_t* 
                                                                  float* __restrict__ row_prob) {
   pdl_launch_dependents();
   pdl_wait();
-  extern __shared__ uint32_t s_mask[];  // [E_loc][kPermTile / 32] token bitmasks
-  constexpr int W = kPermTile / 32;
+  extern __shared__ uint32_t s_mask[];  // [E_loc][TILE / 32] token bitmasks
+  constexpr int W = TILE / 32;
   for (int i = threadIdx.x; i < E_loc * W; i += blockDim.x) s_mask[i] = 0u;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kPermTile + threadIdx.x;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * TILE + threadIdx.x;
   if (t < T)
     for (int j = 0; j < k; ++j) {
       const int e = __ldg(ids + t * k + j) - e0;
@@ -299,12 +319,12 @@ struct PermuteWs {
 };
 
 size_t permute_ws_bytes(int T, int E_loc) {
-  const int64_t n_tiles = ceil_div(T > 0 ? T : 1, kPermTile);
+  const int64_t n_tiles = ceil_div(T > 0 ? T : 1, perm_tile(T, E_loc));
   return align_up(static_cast<size_t>(n_tiles) * E_loc * 4, kAlign) + align_up((E_loc + 1) * 4, kAlign);
 }
 
 static PermuteWs carve_permute_ws(uint8_t* base, int T, int E_loc) {
-  const int64_t n_tiles = ceil_div(T > 0 ? T : 1, kPermTile);
+  const int64_t n_tiles = ceil_div(T > 0 ? T : 1, perm_tile(T, E_loc));
   PermuteWs w;
   w.tile_counts = reinterpret_cast<int32_t*>(base);
   w.mtile_base = reinterpret_cast<int32_t*>(base + align_up(static_cast<size_t>(n_tiles) * E_loc * 4, kAlign));
@@ -318,11 +338,13 @@ cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtyp
                            const int32_t* ids, const float* probs, int k, int e0, int E_loc, void* perm_x,
                            uint8_t* perm_sf, int32_t* counts, int32_t* offsets, int32_t* row_src_token,
                            float* row_prob, int32_t* pair_to_row, uint8_t* ws, cudaStream_t st) {
-  const int n_tiles = static_cast<int>(ceil_div(T > 0 ? T : 1, kPermTile));
+  const int tile = perm_tile(T, E_loc);
+  const int n_tiles = static_cast<int>(ceil_div(T > 0 ? T : 1, tile));
   PermuteWs w = carve_permute_ws(ws, T, E_loc);
   if (T > 0) {
-    cudaError_t e = launch_pdl(perm_count_kernel, dim3(n_tiles), dim3(kPermTile), E_loc * 4, st, ids, T, k, e0, E_loc,
-                               n_tiles, w.tile_counts);
+    cudaError_t e = launch_pdl(tile == kPermTileSmall ? perm_count_kernel<kPermTileSmall>
+                                                      : perm_count_kernel<kPermTileLarge>,
+                               dim3(n_tiles), dim3(tile), E_loc * 4, st, ids, T, k, e0, E_loc, n_tiles, w.tile_counts);
     if (e != cudaSuccess) return e;
   } else {
     cudaMemsetAsync(w.tile_counts, 0, static_cast<size_t>(n_tiles) * E_loc * 4, st);
@@ -331,7 +353,8 @@ cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtyp
                              offsets, w.mtile_base);
   if (e != cudaSuccess) return e;
   if (T > 0) {
-    e = launch_pdl(perm_scatter_kernel, dim3(n_tiles), dim3(kPermTile), E_loc * (kPermTile / 32) * 4, st, ids, probs,
+    e = launch_pdl(tile == kPermTileSmall ? perm_scatter_kernel<kPermTileSmall> : perm_scatter_kernel<kPermTileLarge>,
+                   dim3(n_tiles), dim3(tile), E_loc * (tile / 32) * 4, st, ids, probs,
                    T, k, e0, E_loc, n_tiles, static_cast<const int32_t*>(w.tile_counts), pair_to_row, row_src_token,
                    row_prob);
     if (e != cudaSuccess) return e;
