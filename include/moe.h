@@ -288,6 +288,26 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_strea
  * *device_error.  Returns MOE_ERR_CUDA if the synchronisation fails. */
 moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* device_error);
 
+/* Expert placement and replication plan (host function, no GPU) ["Wide-EP ... MoE ...
+ * NVIDIA" explainer, "Load imbalance: EPLB": per-expert load decides placement, and the
+ * most loaded experts get copies on several GPUs].  The page gives no algorithm; this is
+ * the plain greedy reading:
+ *   1. every expert gets one copy; while free slots remain, one more copy goes to the
+ *      expert with the largest load per copy (ties: lower id), at most G copies each;
+ *   2. copies (load / copies each) in descending load (ties: lower expert id, then
+ *      copy index) go to the least loaded GPU with a free slot that holds no copy of
+ *      that expert (ties: lower GPU id); an extra copy no GPU can take is dropped.
+ *   load         host int64 [E]: tokens routed to each expert (e.g. summed counts from
+ *                moe_permute over recent steps), >= 0
+ *   E, G, S      experts, GPUs, slots per GPU; requires E <= G * S <= 2^24
+ *   slot_expert  host int32 [G * S] out: expert held by slot s of GPU g at g * S + s,
+ *                filled from s = 0 up, -1 for an empty slot
+ *   replicas     host int32 [E] out: copies placed per expert (>= 1)
+ *   gpu_load     host double [G] out: sum over the GPU's copies of load / replicas
+ * Deterministic; MOE_ERR_INVALID_ARG on a bad size or negative load. */
+moe_status moe_eplb_plan(const int64_t* load, int E, int G, int S, int32_t* slot_expert, int32_t* replicas,
+                         double* gpu_load);
+
 /* Self-test of the bounded device waits every pipelined kernel uses (failure detection):
  * launches one thread that waits on an mbarrier nothing arrives on, for timeout_ns
  * (1 ms .. 2 s); the wait gives up, MOE_ERR_TIMEOUT is stored in the (initialised) error

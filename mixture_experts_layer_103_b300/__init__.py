@@ -19,6 +19,7 @@ import ctypes
 import dataclasses
 import os
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -61,6 +62,7 @@ _SIGS = {
     "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm1_swiglu_gather": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_quantize_mx_rows": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "moe_eplb_plan": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm_workspace_size": (_SZ, []),
     "moe_unpermute_combine": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
@@ -312,6 +314,21 @@ def moe_layer_forward(x, logits, E: int, k: int, e0: int, pw: PackedWeights, y=N
         _ptr(x), _ptr(logits), T, d, pw.f, E, k, e0, pw.E_loc, pw.dtype, _ptr(pw.Wgu), _ptr(pw.Wgu_scale),
         _ptr(pw.Wd), _ptr(pw.Wd_scale), _ptr(y), _ptr(ws), ws.numel(), _stream()))
     return y, ws
+
+
+def moe_eplb_plan(load, G: int, S: int):
+    """Placement of E experts (load[e] tokens each) on G GPUs with S slots each, with
+    copies of the most loaded experts: (slot_expert [G, S], replicas [E], gpu_load [G])."""
+    ld = np.ascontiguousarray(np.asarray(load, dtype=np.int64))
+    E = ld.size
+    slot = np.empty((G, S), np.int32)
+    rep = np.empty(E, np.int32)
+    gl = np.empty(G, np.float64)
+    _check("moe_eplb_plan", _lib.moe_eplb_plan(ld.ctypes.data_as(ctypes.c_void_p), E, G, S,
+                                               slot.ctypes.data_as(ctypes.c_void_p),
+                                               rep.ctypes.data_as(ctypes.c_void_p),
+                                               gl.ctypes.data_as(ctypes.c_void_p)))
+    return slot, rep, gl
 
 
 def moe_get_device_error(ws: torch.Tensor) -> int:

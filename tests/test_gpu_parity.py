@@ -420,3 +420,25 @@ def test_quantize_rows_matches_oracle(moe):
     codes, scales = oracle.mx_quantize(x, "bf16", (w.T, w.d, 1))
     np.testing.assert_array_equal(xq.cpu().numpy(), codes)
     np.testing.assert_array_equal(xs.cpu().numpy(), scales.reshape(w.T, w.d // 32))
+
+
+# ----------------------------------------------------------------------------- placement plan
+def test_eplb_plan_from_device_counts(moe):
+    """The placement planner fed by the permute's per-expert counts of the Zipf-skewed
+    256-expert routing (all experts local): a valid plan, the oracle's plan, and a lower
+    peak GPU load than the contiguous 32-experts-per-GPU placement."""
+    from oracle.eplb import eplb_plan
+    w = WORKLOADS["ep8_zipf_T512"]
+    lg = gen_logits(w)
+    ids, probs = moe.moe_route_topk(to_dev(lg), w.k)
+    x = torch.zeros(w.T, 64, dtype=torch.bfloat16, device="cuda")
+    P = moe.moe_permute(x, ids, probs, 0, w.E, "bf16", maps_only=True)
+    counts = P["counts"].cpu().numpy().astype(np.int64)
+    oids, _ = oracle.route_topk(lg, w.k)
+    np.testing.assert_array_equal(counts, np.bincount(oids.ravel(), minlength=w.E))
+    G, S = 8, 40
+    slot, rep, gl = moe.moe_eplb_plan(counts, G, S)
+    oslot, orep, _ = eplb_plan(counts.tolist(), G, S)
+    assert slot.tolist() == oslot and rep.tolist() == orep
+    assert abs(gl.sum() - counts.sum()) <= 1e-9 * counts.sum()
+    assert gl.max() < counts.reshape(G, -1).sum(1).max()
