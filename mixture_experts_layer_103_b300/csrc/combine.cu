@@ -4,28 +4,43 @@
 // and broadcast, the rows of Y2 are summed in slot order in fp32 with 16-byte vector
 // loads, and the row of y is written once (zeros when no slot is local).  The routing
 // probability was applied inside the SwiGLU, so this is an unweighted sum.
+//
+// Work item = (token, slice of kCombineSlice 16-byte vectors of its row), grid-strided
+// over a persistent grid: a wide row (d = 7168) is spread over several warps, so the
+// serial chain of load latencies per warp stays short.
+#include <algorithm>
+
 #include "moe_common.cuh"
 
 namespace moe {
 
-constexpr int kCombineGroup = 8;  // slots whose loads are in flight together
+int num_sms();
+
+constexpr int kCombineGroup = 8;    // slots whose loads are in flight together
+constexpr int kCombineSlice = 128;  // 16-byte vectors per work item (4 per lane)
 
 template <bool F32>
-__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ p2r,
-                                                      int T, int k, int64_t row_vecs, uint4* __restrict__ y) {
+__global__ void __launch_bounds__(256, 2) combine_kernel(const uint4* __restrict__ Y2, const int32_t* __restrict__ p2r,
+                                                      int T, int k, int64_t row_vecs, int slices,
+                                                      uint4* __restrict__ y) {
   pdl_launch_dependents();
   pdl_wait();
   constexpr int V = F32 ? 4 : 8;  // values per 16-byte vector
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t items = static_cast<int64_t>(T) * slices;
+  for (int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
+       item += warps) {
+  const int64_t t = item / slices;
+  const int64_t c_begin = (item - t * slices) * kCombineSlice;
+  const int64_t c_end = std::min<int64_t>(row_vecs, c_begin + kCombineSlice);
   const int32_t my_row = lane < k ? __ldg(p2r + t * k + lane) : -1;
   const uint32_t valid = __ballot_sync(0xffffffffu, my_row >= 0);  // local slots, ascending j
   const int nv = __popc(valid);
   uint4* dst = y + t * row_vecs;
-  for (int64_t base = 0; base < row_vecs; base += 32) {  // warp-uniform trip count
+  for (int64_t base = c_begin; base < c_end; base += 32) {  // warp-uniform trip count
     const int64_t c = base + lane;
-    const bool act = c < row_vecs;
+    const bool act = c < c_end;
     float acc[V];
 #pragma unroll
     for (int u = 0; u < V; ++u) acc[u] = 0.0f;
@@ -67,6 +82,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     }
     if (act) dst[c] = o;
   }
+  }
 }
 
 cudaError_t launch_combine(const void* Y2, const int32_t* p2r, int T, int k, int d, moe_dtype dtype, void* y,
@@ -74,13 +90,16 @@ cudaError_t launch_combine(const void* Y2, const int32_t* p2r, int T, int k, int
   if (T == 0) return cudaSuccess;
   const bool f32 = dtype == MOE_F32;
   const int64_t row_vecs = static_cast<int64_t>(d) * (f32 ? 4 : 2) / 16;
-  const dim3 grid(static_cast<unsigned>(ceil_div(T, 8))), block(256);
+  const int slices = static_cast<int>(ceil_div(row_vecs, kCombineSlice));
+  const int64_t items = static_cast<int64_t>(T) * slices;
+  const dim3 grid(static_cast<unsigned>(std::min<int64_t>(ceil_div(items, 8), static_cast<int64_t>(num_sms()) * 4))),
+      block(256);
   if (f32)
     return launch_pdl(combine_kernel<true>, grid, block, 0, st, static_cast<const uint4*>(Y2), p2r, T, k, row_vecs,
-                      static_cast<uint4*>(y));
+                      slices, static_cast<uint4*>(y));
   else
     return launch_pdl(combine_kernel<false>, grid, block, 0, st, static_cast<const uint4*>(Y2), p2r, T, k, row_vecs,
-                      static_cast<uint4*>(y));
+                      slices, static_cast<uint4*>(y));
   return cudaGetLastError();
 }
 
