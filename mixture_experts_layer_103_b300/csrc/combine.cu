@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint4* __restrict
       o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                      pack_bf16x2(acc[6], acc[7]));
     }
-    if (act) dst[c] = o;
+    if (act) __stcs(dst + c, o);  // y is written once and not re-read: streaming store
   }
   }
 }
