@@ -59,6 +59,9 @@ def _load():
         lib.oracle_moe_forward.restype = i32
         lib.oracle_down_proj_mx.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, P, P, i32]
         lib.oracle_down_proj_mx.restype = i32
+        lib.oracle_moe_backward.argtypes = [P, i32, P, i64, i32, i32, i32, i32, i32, i32, i32, P, P, P, P, i32,
+                                            P, i64, P, P, P, i32, P, P, P, i32]
+        lib.oracle_moe_backward.restype = i32
         _lib = lib
     return _lib
 
@@ -141,7 +144,7 @@ def moe_forward(x, x_dtype: str, logits, d: int, f: int, E: int, k: int, e0: int
     (W_gate/W_up [E_loc, d, f], W_down [E_loc, f, d]) as f32, bf16 bits, or E4M3 codes
     with E8M0 scales ``w_scales`` ([E_loc, d/32, f], [E_loc, d/32, f], [E_loc, f/32, d]).
     """
-    npdt = {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8}
+    npdt = {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8, "f64": np.float64}
     x = _c(x, npdt[x_dtype])
     lg = _c(logits, np.float32)
     T = x.shape[0]
@@ -171,4 +174,34 @@ def down_proj_mx(h_codes, h_scales, row_expert, d: int, f: int, E_loc: int, W_do
                                      _p(out), threads())
     if st != 0:
         raise ValueError(f"oracle_down_proj_mx status {st}")
+    return out
+
+
+def moe_backward(x, x_dtype: str, logits, dy, dy_dtype: str, k: int, e0: int, E_loc: int, w_dtype: str,
+                 W_gate, W_up, W_down, tokens=None, experts=None, want_dx=True, want_dlogits=True,
+                 want_dw=True) -> dict:
+    """fp64 gradients of L = sum(dy * y): dx [n_tokens, d], dlogits [n_tokens, E] for
+    ``tokens`` (default all), dW_gate/dW_up [n_experts, d, f] and dW_down [n_experts, f, d]
+    for the local ``experts`` (default all)."""
+    sd = {"f32": np.float32, "bf16": np.uint16, "f64": np.float64}
+    xa, dya = _c(x, sd[x_dtype]), _c(dy, sd[dy_dtype])
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    d = xa.shape[1]
+    f = W_gate.shape[2]
+    wg, wu, wd = (_c(w, sd[w_dtype]) for w in (W_gate, W_up, W_down))
+    tok = np.arange(T, dtype=np.int64) if tokens is None else _c(tokens, np.int64)
+    exps = np.arange(E_loc, dtype=np.int32) if experts is None else _c(experts, np.int32)
+    out = {}
+    dx = np.empty((tok.size, d)) if want_dx else None
+    dl = np.empty((tok.size, E)) if want_dlogits else None
+    dwg = np.empty((exps.size, d, f)) if want_dw else None
+    dwu = np.empty((exps.size, d, f)) if want_dw else None
+    dwd = np.empty((exps.size, f, d)) if want_dw else None
+    st = _load().oracle_moe_backward(_p(xa), DT[x_dtype], _p(lg), T, d, f, E, k, e0, E_loc, DT[w_dtype], _p(wg),
+                                     _p(wu), _p(wd), _p(dya), DT[dy_dtype], _p(tok), tok.size, _p(dx), _p(dl),
+                                     _p(exps), exps.size, _p(dwg), _p(dwu), _p(dwd), threads())
+    if st != 0:
+        raise ValueError(f"oracle_moe_backward status {st}")
+    out.update(dx=dx, dlogits=dl, dW_gate=dwg, dW_up=dwu, dW_down=dwd)
     return out

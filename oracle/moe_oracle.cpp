@@ -32,6 +32,9 @@
 //  * MXFP8 blocks run along the contraction (K) dimension: x rows along d, W_gate/W_up
 //    columns along d, W_down columns along f, h rows along f (after the probability).
 //
+// The backward (oracle_moe_backward) is pinned by central finite differences of the
+// forward in fp64 (tests/test_backward_oracle.py).
+//
 // Parity pins: every function here is pinned by tests that do not call it back with
 // its own formula (hand-worked example, numpy brute force with an independent top-k and
 // an independent nearest-code quantiser, dense-MLP reductions, linearity and EP-slice
@@ -332,6 +335,133 @@ int oracle_down_proj_mx(const uint8_t* h_codes, const uint8_t* h_scales, const i
     }
   }
   return 0;
+}
+
+
+// Layer backward (bf16/fp32/fp64 inputs, no MXFP8), fp64.  With L = sum_t dy_t . y_t, for
+// each token t and local slot j (expert e, probability p_j, from route_one):
+//   g = x W_gate_e, u = x W_up_e, s = sigmoid(g), a = g s (= silu(g)), h = p_j a u
+//   dh = W_down_e dy_t                    (dh_n = sum_m W_down_e[n, m] dy_t[m])
+//   dW_down_e[n, m] += h_n dy_t[m]
+//   dp_j = sum_n dh_n a_n u_n
+//   du = p_j dh a,  dg = p_j dh u s (1 + g (1 - s))      (d silu / dg = s (1 + g (1 - s)))
+//   dx_t += W_gate_e dg + W_up_e du;  dW_gate_e[c, n] += x_c dg_n;  dW_up_e[c, n] += x_c du_n
+// and for the token's k selected logits (softmax over them, dp = 0 for non-local slots):
+//   dlogit_{id_j} = p_j (dp_j - sum_i p_i dp_i); the other E - k logits get 0.
+//   tokens [n_tokens]: dx [n_tokens, d] and dlogits [n_tokens, E] are written for these.
+//   experts [n_experts] (local indices): dWg, dWu [n_experts, d, f], dWd [n_experts, f, d]
+//   summed over all T tokens.  Null outputs are skipped.
+int oracle_moe_backward(const void* x, int x_dtype, const float* logits, int64_t T, int d, int f, int E, int k,
+                        int e0, int E_loc, int w_dtype, const void* W_gate, const void* W_up, const void* W_down,
+                        const void* dy, int dy_dtype, const int64_t* tokens, int64_t n_tokens, double* dx,
+                        double* dlogits, const int32_t* experts, int n_experts, double* dWg, double* dWu,
+                        double* dWd, int nthreads) {
+  if (k < 1 || k > E || e0 < 0 || e0 + E_loc > E || d <= 0 || f <= 0 || w_dtype == DT_E4M3) return -1;
+  for (int64_t i = 0; i < n_tokens; ++i)
+    if (tokens[i] < 0 || tokens[i] >= T) return -1;
+  for (int i = 0; i < n_experts; ++i)
+    if (experts[i] < 0 || experts[i] >= E_loc) return -1;
+  const WeightView Wg{W_gate, nullptr, w_dtype, d, f};
+  const WeightView Wu{W_up, nullptr, w_dtype, d, f};
+  const WeightView Wd{W_down, nullptr, w_dtype, f, d};
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+  int status = 0;
+  // per-slot quantities of one (token, expert) pair
+  auto pair_grads = [&](int64_t t, int e, double p, std::vector<double>& xt, std::vector<double>& dyt,
+                        std::vector<double>& g, std::vector<double>& u, std::vector<double>& h,
+                        std::vector<double>& dg, std::vector<double>& du) -> double {
+    for (int c = 0; c < d; ++c) xt[c] = load_value(x, x_dtype, t * d + c);
+    for (int m = 0; m < d; ++m) dyt[m] = load_value(dy, dy_dtype, t * d + m);
+    for (int n = 0; n < f; ++n) { g[n] = 0.0; u[n] = 0.0; }
+    for (int c = 0; c < d; ++c)
+      for (int n = 0; n < f; ++n) {
+        g[n] += xt[c] * Wg.at(e, c, n);
+        u[n] += xt[c] * Wu.at(e, c, n);
+      }
+    double dp = 0.0;
+    for (int n = 0; n < f; ++n) {
+      const double sg = 1.0 / (1.0 + std::exp(-g[n]));
+      const double a = g[n] * sg;
+      h[n] = p * a * u[n];
+      double dh = 0.0;
+      for (int m = 0; m < d; ++m) dh += Wd.at(e, n, m) * dyt[m];
+      dp += dh * a * u[n];
+      du[n] = p * dh * a;
+      dg[n] = p * dh * u[n] * sg * (1.0 + g[n] * (1.0 - sg));
+    }
+    return dp;
+  };
+  if (dx || dlogits) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t i = 0; i < n_tokens; ++i) {
+      const int64_t t = tokens[i];
+      std::vector<int32_t> ids(k);
+      std::vector<double> probs(k), dps(k, 0.0), xt(d), dyt(d), g(f), u(f), h(f), dg(f), du(f);
+      if (!route_one(logits + t * E, E, k, ids.data(), probs.data())) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+        status = -2;
+        continue;
+      }
+      if (dx)
+        for (int c = 0; c < d; ++c) dx[i * d + c] = 0.0;
+      for (int j = 0; j < k; ++j) {
+        const int e = ids[j] - e0;
+        if (e < 0 || e >= E_loc) continue;
+        dps[j] = pair_grads(t, e, probs[j], xt, dyt, g, u, h, dg, du);
+        if (dx)
+          for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int n = 0; n < f; ++n) acc += Wg.at(e, c, n) * dg[n] + Wu.at(e, c, n) * du[n];
+            dx[i * d + c] += acc;
+          }
+      }
+      if (dlogits) {
+        for (int q = 0; q < E; ++q) dlogits[i * E + q] = 0.0;
+        double pdp = 0.0;
+        for (int j = 0; j < k; ++j) pdp += probs[j] * dps[j];
+        for (int j = 0; j < k; ++j) dlogits[i * E + ids[j]] = probs[j] * (dps[j] - pdp);
+      }
+    }
+  }
+  if (dWg || dWu || dWd) {
+    // one expert per task; every token routed to it contributes
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int q = 0; q < n_experts; ++q) {
+      const int e = experts[q];
+      std::vector<int32_t> ids(k);
+      std::vector<double> probs(k), xt(d), dyt(d), g(f), u(f), h(f), dg(f), du(f);
+      double* gw = dWg ? dWg + static_cast<int64_t>(q) * d * f : nullptr;
+      double* uw = dWu ? dWu + static_cast<int64_t>(q) * d * f : nullptr;
+      double* dw = dWd ? dWd + static_cast<int64_t>(q) * f * d : nullptr;
+      if (gw) std::fill(gw, gw + static_cast<int64_t>(d) * f, 0.0);
+      if (uw) std::fill(uw, uw + static_cast<int64_t>(d) * f, 0.0);
+      if (dw) std::fill(dw, dw + static_cast<int64_t>(f) * d, 0.0);
+      for (int64_t t = 0; t < T; ++t) {
+        if (!route_one(logits + t * E, E, k, ids.data(), probs.data())) continue;
+        for (int j = 0; j < k; ++j) {
+          if (ids[j] - e0 != e) continue;
+          pair_grads(t, e, probs[j], xt, dyt, g, u, h, dg, du);
+          for (int c = 0; c < d; ++c)
+            for (int n = 0; n < f; ++n) {
+              if (gw) gw[static_cast<int64_t>(c) * f + n] += xt[c] * dg[n];
+              if (uw) uw[static_cast<int64_t>(c) * f + n] += xt[c] * du[n];
+            }
+          if (dw)
+            for (int n = 0; n < f; ++n)
+              for (int m = 0; m < d; ++m) dw[static_cast<int64_t>(n) * d + m] += h[n] * dyt[m];
+        }
+      }
+    }
+  }
+  return status;
 }
 
 }  // extern "C"

@@ -1,0 +1,78 @@
+"""Pins of the oracle's layer backward (CPU): central finite differences of the forward
+oracle in fp64 (itself pinned by test_oracle_pins.py), for x, all three weight tensors and
+the router logits, on a slice of local experts (some slots not local) and on all experts.
+A dropped term, a wrong sign or a transposed operand in the backward fails here."""
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _problem(seed, T, d, f, E, k, E_loc):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((E_loc, d, f)) / np.sqrt(d)
+    Wu = rng.standard_normal((E_loc, d, f)) / np.sqrt(d)
+    Wd = rng.standard_normal((E_loc, f, d)) / np.sqrt(f)
+    # logits on a 2^-8 grid with distinct values per token: the top-k stays fixed under
+    # the +-2^-12 perturbations below, and every perturbed value is exact in fp32
+    lg = np.stack([rng.permutation(np.arange(E)) * 0.25 + rng.integers(-64, 64) / 256.0 for _ in range(T)])
+    lg = lg.astype(np.float32)
+    dy = rng.standard_normal((T, d))
+    return x, lg, Wg, Wu, Wd, dy
+
+
+def _loss(x, lg, Wg, Wu, Wd, dy, k, e0, E_loc):
+    d, f, E = x.shape[1], Wg.shape[2], lg.shape[1]
+    y = oracle.moe_forward(x, "f64", lg, d, f, E, k, e0, E_loc, Wg, Wu, Wd, "f64")
+    return float((y * dy).sum())
+
+
+@pytest.mark.parametrize("e0,E_loc", [(1, 2), (0, 4)])
+def test_backward_matches_finite_differences(e0, E_loc):
+    T, d, f, E, k = 5, 6, 4, 4, 2
+    x, lg, Wg, Wu, Wd, dy = _problem(7 + e0, T, d, f, E, k, E_loc)
+    g = oracle.moe_backward(x, "f64", lg, dy, "f64", k, e0, E_loc, "f64", Wg, Wu, Wd)
+    L = lambda **kw: _loss(kw.get("x", x), kw.get("lg", lg), kw.get("Wg", Wg), kw.get("Wu", Wu),
+                           kw.get("Wd", Wd), dy, k, e0, E_loc)
+    eps = 1e-5
+
+    def fd(name, arr):
+        out = np.empty(arr.shape)
+        for idx in np.ndindex(arr.shape):
+            a, b = arr.copy(), arr.copy()
+            a[idx] += eps
+            b[idx] -= eps
+            out[idx] = (L(**{name: a}) - L(**{name: b})) / (2 * eps)
+        return out
+
+    for name, arr, key in [("x", x, "dx"), ("Wg", Wg, "dW_gate"), ("Wu", Wu, "dW_up"), ("Wd", Wd, "dW_down")]:
+        num = fd(name, arr)
+        np.testing.assert_allclose(g[key], num, rtol=1e-6, atol=1e-8, err_msg=key)
+    # router logits (fp32): perturb by 2^-12, exact on the 2^-8 grid
+    h = 2.0 ** -12
+    num = np.empty(lg.shape)
+    for idx in np.ndindex(lg.shape):
+        a, b = lg.copy(), lg.copy()
+        a[idx] += np.float32(h)
+        b[idx] -= np.float32(h)
+        num[idx] = (L(lg=a) - L(lg=b)) / (2 * h)
+    np.testing.assert_allclose(g["dlogits"], num, rtol=1e-5, atol=1e-7)
+
+
+def test_backward_structure():
+    """Linear in dy; logit gradients only on the k selected logits and summing to zero
+    (softmax Jacobian); a token with no local expert gets zero dx."""
+    T, d, f, E, k, e0, E_loc = 6, 5, 3, 4, 2, 2, 2
+    x, lg, Wg, Wu, Wd, dy = _problem(3, T, d, f, E, k, E_loc)
+    g1 = oracle.moe_backward(x, "f64", lg, dy, "f64", k, e0, E_loc, "f64", Wg, Wu, Wd)
+    g2 = oracle.moe_backward(x, "f64", lg, 2.5 * dy, "f64", k, e0, E_loc, "f64", Wg, Wu, Wd)
+    for key in ("dx", "dlogits", "dW_gate", "dW_up", "dW_down"):
+        np.testing.assert_allclose(g2[key], 2.5 * g1[key], rtol=1e-12, atol=1e-14)
+    ids, _ = oracle.route_topk(lg, k)
+    for t in range(T):
+        sel = set(ids[t].tolist())
+        assert all(g1["dlogits"][t, q] == 0.0 for q in range(E) if q not in sel)
+        assert abs(g1["dlogits"][t].sum()) < 1e-12
+        if not any(e0 <= i < e0 + E_loc for i in ids[t]):
+            assert (g1["dx"][t] == 0.0).all()
