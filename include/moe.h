@@ -288,6 +288,44 @@ moe_status moe_workspace_init(void* workspace, size_t workspace_bytes, moe_strea
  * *device_error.  Returns MOE_ERR_CUDA if the synchronisation fails. */
 moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* device_error);
 
+/* Layer backward (bf16) ["Efficient MoE training for biological foundation models",
+ * "GroupedLinear Optimizes Expert Computation": the fused GroupedMLP has a matching
+ * backward whose ScaledSwiGLU part also yields the gradient of the routing scales].
+ * Gradients of L = sum_t dy_t . y_t for the layer of moe_layer_forward (same x, routing and
+ * weights).  Per routed row (token t, local expert e, probability p), with s = sigmoid(g):
+ *   g, u = x W_gate_e, x W_up_e (recomputed);  h = p silu(g) u;  dh = W_down_e dy_t
+ *   du = p dh silu(g);  dg = p dh u s (1 + g (1 - s));  dp = sum_n dh_n silu(g_n) u_n
+ *   dx_t = sum over the token's local slots of W_gate_e dg + W_up_e du
+ *   dW_down_e = sum_rows h^T dy_t;  dW_gate_e = sum_rows x_t^T dg;  dW_up_e = sum_rows x_t^T du
+ *   dlogits[t, id_j] = p_j (dp_j - sum_i p_i dp_i) over the k selected logits (softmax over
+ *   the top k), dp = 0 for slots whose expert is not local; other logits 0.  With experts
+ *   split over GPUs, summing every GPU's dx and dlogits gives the full gradients.
+ *   x, dy              device bf16 [T, d]
+ *   topk_ids/probs     device [T, k] from moe_route_topk on the forward's logits
+ *   Wgu_packed         the forward's packed gate/up weights (moe_pack_weights, bf16)
+ *   W_down             device bf16 [E_loc, f, d], the user layout
+ *   WguT_packed        device bf16 [E_loc, d, 2f] from moe_pack_weights_backward
+ *   dx                 device bf16 [T, d] out (zero rows for tokens with no local expert)
+ *   dlogits            device fp32 [T, E] out
+ *   dW_gate, dW_up     device fp32 [E_loc, d, f] out;  dW_down device fp32 [E_loc, f, d] out
+ *                      (zero for experts that received no token)
+ *   workspace          device >= moe_layer_backward_workspace_size(T, d, f, k, E_loc) bytes,
+ *                      256-byte aligned, error word initialised (moe_workspace_init)
+ * Requires d % 8 == 0, f % 32 == 0; 16-byte aligned x, dy, dx and weights.  bf16 only. */
+moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
+                              int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
+                              const void* W_down, const void* WguT_packed, void* dx, float* dlogits, float* dW_gate,
+                              float* dW_up, float* dW_down, void* workspace, size_t workspace_bytes,
+                              moe_stream_t stream);
+size_t moe_layer_backward_workspace_size(int T, int d, int f, int k, int E_loc);
+
+/* Backward weight pack (one-off): WguT [E_loc, d, 2f] bf16, row c = rows c of W_gate and W_up
+ * ([E_loc, d, f], src_dtype MOE_BF16 or MOE_F32) interleaved in 32-column blocks (packed
+ * column 64b + i = gate column 32b + i, 64b + 32 + i = up column 32b + i) -- the order
+ * the backward stores dg/du in.  Requires f % 32 == 0, d % 8 == 0. */
+moe_status moe_pack_weights_backward(const void* W_gate, const void* W_up, moe_dtype src_dtype, int E_loc, int d,
+                                     int f, void* WguT_packed, moe_stream_t stream);
+
 /* Expert placement and replication plan (host function, no GPU) ["Wide-EP ... MoE ...
  * NVIDIA" explainer, "Load imbalance: EPLB": per-expert load decides placement, and the
  * most loaded experts get copies on several GPUs].  The page gives no algorithm; this is

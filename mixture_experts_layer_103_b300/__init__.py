@@ -63,6 +63,10 @@ _SIGS = {
     "moe_expert_gemm1_swiglu_gather": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_quantize_mx_rows": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "moe_eplb_plan": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_layer_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                _SZ, _P]),
+    "moe_layer_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_pack_weights_backward": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm_workspace_size": (_SZ, []),
     "moe_unpermute_combine": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
@@ -314,6 +318,38 @@ def moe_layer_forward(x, logits, E: int, k: int, e0: int, pw: PackedWeights, y=N
         _ptr(x), _ptr(logits), T, d, pw.f, E, k, e0, pw.E_loc, pw.dtype, _ptr(pw.Wgu), _ptr(pw.Wgu_scale),
         _ptr(pw.Wd), _ptr(pw.Wd_scale), _ptr(y), _ptr(ws), ws.numel(), _stream()))
     return y, ws
+
+
+def moe_pack_weights_backward(W_gate: torch.Tensor, W_up: torch.Tensor) -> torch.Tensor:
+    """WguT [E_loc, d, 2f] bf16 for moe_layer_backward."""
+    E_loc, d, f = W_gate.shape
+    src = MOE_F32 if W_gate.dtype == torch.float32 else MOE_BF16
+    out = torch.empty(E_loc, d, 2 * f, dtype=torch.bfloat16, device=W_gate.device)
+    _check("moe_pack_weights_backward", _lib.moe_pack_weights_backward(_ptr(W_gate), _ptr(W_up), src, E_loc, d, f,
+                                                                       _ptr(out), _stream()))
+    return out
+
+
+def moe_layer_backward(x, dy, topk_ids, topk_probs, E: int, e0: int, pw: PackedWeights, W_down: torch.Tensor,
+                       WguT: torch.Tensor, ws=None, out=None):
+    """Gradients of sum(dy * y) of the bf16 layer: dict(dx, dlogits, dW_gate, dW_up, dW_down)."""
+    T, d = x.shape
+    k = topk_ids.shape[1]
+    f, E_loc = pw.f, pw.E_loc
+    dev = x.device
+    if out is None:
+        out = dict(dx=torch.empty(T, d, dtype=torch.bfloat16, device=dev),
+                   dlogits=torch.empty(T, E, dtype=torch.float32, device=dev),
+                   dW_gate=torch.empty(E_loc, d, f, dtype=torch.float32, device=dev),
+                   dW_up=torch.empty(E_loc, d, f, dtype=torch.float32, device=dev),
+                   dW_down=torch.empty(E_loc, f, d, dtype=torch.float32, device=dev))
+    nb = _lib.moe_layer_backward_workspace_size(T, d, f, k, E_loc)
+    ws = ws if ws is not None else workspace(nb, dev)
+    _check("moe_layer_backward", _lib.moe_layer_backward(
+        _ptr(x), _ptr(dy), _ptr(topk_ids), _ptr(topk_probs), T, d, f, E, k, e0, E_loc, _ptr(pw.Wgu), _ptr(W_down),
+        _ptr(WguT), _ptr(out["dx"]), _ptr(out["dlogits"]), _ptr(out["dW_gate"]), _ptr(out["dW_up"]),
+        _ptr(out["dW_down"]), _ptr(ws), ws.numel(), _stream()))
+    return out, ws
 
 
 def moe_eplb_plan(load, G: int, S: int):

@@ -32,6 +32,23 @@ cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int
                                    uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_quant_rows_mx(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
                                  uint8_t* xq, uint8_t* x_sf, cudaStream_t st);
+cudaError_t launch_tc_gemm_gather_store(const void* x, const int32_t* row_src_token, const int32_t* offsets,
+                                        int E_loc, int K, int n_out, const void* B, void* out, int32_t* err,
+                                        uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_tc_dswiglu(const void* dy, const int32_t* row_src_token, const int32_t* offsets,
+                              const float* row_prob, int E_loc, int d, int f, const void* W_down, const void* gu,
+                              void* dgu, void* h, float* dp_part, int32_t* err, uint64_t timeout_ns,
+                              cudaStream_t st);
+cudaError_t launch_tc_gemm_store(const void* A, int64_t a_rows, const int32_t* offsets, int E_loc, int K, int n_out,
+                                 const void* B, void* out, int32_t* err, uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_pack_gu_t(const void* Wg, const void* Wu, moe_dtype src, int E_loc, int d, int f, void* WguT,
+                             cudaStream_t st);
+cudaError_t launch_dlogits(const int32_t* ids, const float* probs, const int32_t* p2r, const float* dp_part,
+                           int nparts, int T, int E, int k, float* dlogits, cudaStream_t st);
+cudaError_t launch_wgrad_down(const void* h, const void* dy, const int32_t* row_token, const int32_t* offsets,
+                              int E_loc, int d, int f, float* dWd, cudaStream_t st);
+cudaError_t launch_wgrad_gate_up(const void* x, const void* dgu, const int32_t* row_token, const int32_t* offsets,
+                                 int E_loc, int d, int f, float* dWg, float* dWu, cudaStream_t st);
 cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
@@ -190,6 +207,47 @@ static LayerWs layer_layout(uint8_t* base, int T, int d, int f, int E, int k, in
   }
   w.mlp = take(mlp_scratch_bytes(n_cap, E_loc, f, dt));
   w.Y2 = take(static_cast<size_t>(n_cap) * d * (dt == MOE_F32 ? 4 : 2));
+  w.total = o;
+  return w;
+}
+
+// ---- backward workspace ------------------------------------------------------------------
+struct BackwardWs {
+  int32_t* err;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_src_token;
+  float* row_prob;
+  int32_t* pair_to_row;
+  uint8_t* perm_ws;
+  void* gu;        // [N_cap, 2f] bf16, packed order
+  void* dgu;       // [N_cap, 2f] bf16, packed order
+  void* h;         // [N_cap, f] bf16
+  float* dp_part;  // [N_cap, f / 32]
+  void* dxp;       // [N_cap, d] bf16
+  size_t total;
+};
+static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int E_loc) {
+  const int64_t n_cap = n_cap_of(T, k, E_loc);
+  BackwardWs w{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? base + o : nullptr;
+    o += align_up(bytes, kAlign);
+    return p;
+  };
+  w.err = reinterpret_cast<int32_t*>(take(sizeof(WsHeader)));
+  w.counts = reinterpret_cast<int32_t*>(take(static_cast<size_t>(E_loc) * 4));
+  w.offsets = reinterpret_cast<int32_t*>(take(static_cast<size_t>(E_loc + 1) * 4));
+  w.row_src_token = reinterpret_cast<int32_t*>(take(static_cast<size_t>(n_cap) * 4));
+  w.row_prob = reinterpret_cast<float*>(take(static_cast<size_t>(n_cap) * 4));
+  w.pair_to_row = reinterpret_cast<int32_t*>(take(static_cast<size_t>(T) * k * 4));
+  w.perm_ws = take(permute_ws_bytes(T, E_loc));
+  w.gu = take(static_cast<size_t>(n_cap) * 2 * f * 2);
+  w.dgu = take(static_cast<size_t>(n_cap) * 2 * f * 2);
+  w.h = take(static_cast<size_t>(n_cap) * f * 2);
+  w.dp_part = reinterpret_cast<float*>(take(static_cast<size_t>(n_cap) * (f / 32) * 4));
+  w.dxp = take(static_cast<size_t>(n_cap) * d * 2);
   w.total = o;
   return w;
 }
@@ -451,6 +509,60 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
                   Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, hint, stream);
   }
   if (e == cudaSuccess) e = launch_combine(w.Y2, w.pair_to_row, T, k, d, dtype, y, stream);
+  return cuda_status(e);
+}
+
+moe_status moe_pack_weights_backward(const void* W_gate, const void* W_up, moe_dtype src_dtype, int E_loc, int d,
+                                     int f, void* WguT_packed, moe_stream_t stream) {
+  if (!W_gate || !W_up || !WguT_packed || E_loc < 1 || E_loc > 1024 || d <= 0 || f <= 0) return MOE_ERR_INVALID_ARG;
+  if ((src_dtype != MOE_BF16 && src_dtype != MOE_F32) || f % 32 != 0 || d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_pack_gu_t(W_gate, W_up, src_dtype, E_loc, d, f, WguT_packed, stream));
+}
+
+size_t moe_layer_backward_workspace_size(int T, int d, int f, int k, int E_loc) {
+  if (T < 0 || d <= 0 || f <= 0 || k < 1 || E_loc < 1) return 0;
+  return backward_layout(nullptr, T, d, f, k, E_loc).total;
+}
+
+moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
+                              int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
+                              const void* W_down, const void* WguT_packed, void* dx, float* dlogits, float* dW_gate,
+                              float* dW_up, float* dW_down, void* workspace, size_t workspace_bytes,
+                              moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32 || e0 < 0 || E_loc < 1 || e0 + E_loc > E)
+    return MOE_ERR_INVALID_ARG;
+  moe_status s = check_mlp_shape(d, f, E_loc, MOE_BF16);
+  if (s != MOE_OK) return s;
+  if (!Wgu_packed || !W_down || !WguT_packed || !dW_gate || !dW_up || !dW_down) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !dy || !topk_ids || !topk_probs || !dx || !dlogits)) return MOE_ERR_INVALID_ARG;
+  if ((T > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))) || !aligned16(Wgu_packed) ||
+      !aligned16(W_down) || !aligned16(WguT_packed))
+    return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < moe_layer_backward_workspace_size(T, d, f, k, E_loc))
+    return MOE_ERR_WORKSPACE;
+  BackwardWs w = backward_layout(static_cast<uint8_t*>(workspace), T, d, f, k, E_loc);
+  const int64_t n_cap = n_cap_of(T, k, E_loc);
+  cudaError_t e = cudaSuccess;
+  if (T > 0)
+    e = launch_permute(x, MOE_BF16, MOE_BF16, T, d, topk_ids, topk_probs, k, e0, E_loc, nullptr, nullptr, w.counts,
+                       w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
+  else
+    e = cudaMemsetAsync(w.offsets, 0, static_cast<size_t>(E_loc + 1) * 4, stream);
+  if (e == cudaSuccess && n_cap > 0)
+    e = launch_tc_gemm_gather_store(x, w.row_src_token, w.offsets, E_loc, d, 2 * f, Wgu_packed, w.gu, w.err,
+                                    kTimeoutNs, stream);
+  if (e == cudaSuccess && n_cap > 0)
+    e = launch_tc_dswiglu(dy, w.row_src_token, w.offsets, w.row_prob, E_loc, d, f, W_down, w.gu, w.dgu, w.h,
+                          w.dp_part, w.err, kTimeoutNs, stream);
+  if (e == cudaSuccess && n_cap > 0)
+    e = launch_tc_gemm_store(w.dgu, n_cap, w.offsets, E_loc, 2 * f, d, WguT_packed, w.dxp, w.err, kTimeoutNs,
+                             stream);
+  if (e == cudaSuccess) e = launch_combine(w.dxp, w.pair_to_row, T, k, d, MOE_BF16, dx, stream);
+  if (e == cudaSuccess)
+    e = launch_dlogits(topk_ids, topk_probs, w.pair_to_row, w.dp_part, f / 32, T, E, k, dlogits, stream);
+  if (e == cudaSuccess) e = launch_wgrad_down(w.h, dy, w.row_src_token, w.offsets, E_loc, d, f, dW_down, stream);
+  if (e == cudaSuccess)
+    e = launch_wgrad_gate_up(x, w.dgu, w.row_src_token, w.offsets, E_loc, d, f, dW_gate, dW_up, stream);
   return cuda_status(e);
 }
 

@@ -16,7 +16,7 @@ constexpr int kGemmThreads = 192;        // producer, MMA, 4 epilogue warps
 constexpr int kGatherThreads = 128;      // + 4 A-gather warps in row-gather mode
 constexpr int kMaxEloc = 1024;
 
-enum { EPI_STORE_BF16 = 0, EPI_SWIGLU_BF16 = 1, EPI_SWIGLU_MX = 2 };
+enum { EPI_STORE_BF16 = 0, EPI_SWIGLU_BF16 = 1, EPI_SWIGLU_MX = 2, EPI_DSWIGLU = 3 };
 
 struct GemmArgs {
   const int32_t* offsets;  // [E_loc + 1]
@@ -39,6 +39,13 @@ struct GemmArgs {
   const int32_t* row_token;
   const uint8_t* gx_sf;
   int64_t gx_sf_ld;
+  // EPI_DSWIGLU (backward, bf16): the accumulator is dh [rows, f]; aux = the forward
+  // pre-activations g/u [N_cap, 2f] bf16 in the packed column order; out = dg/du in the
+  // same order (ld_out = 2f); out2 = h [N_cap, f] bf16; dp_part [N_cap, f / 32] fp32 =
+  // per-32-column partial sums of dh * silu(g) * u.
+  const uint16_t* aux;
+  void* out2;
+  float* dp_part;
 };
 
 struct Tile {
@@ -129,6 +136,70 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl,
                            pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
       const int chunks = max(0, min(4, (g.n_out - n) / 8));
       warp_store_rows<4>(stage, pk, lane, out + row_first * ld + static_cast<int64_t>(n) * 2, ld, rows_valid, chunks);
+    }
+  } else if constexpr (EPI == EPI_DSWIGLU) {
+    // ScaledSwiGLU backward for h = p * silu(g) * u, from dh and the saved g, u:
+    //   du = p dh silu(g),  dg = p dh u s (1 + g (1 - s)) with s = sigmoid(g),
+    //   dp = sum over the row of dh silu(g) u (partial sums per 32 columns)
+    const float p = r < tl.rows ? __ldg(g.row_prob + row_first + lane) : 0.0f;
+    const int fdim = g.n_out;
+    const int64_t row = row_first + lane;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tbase + c, v);
+      ptx::tmem_ld_wait();
+      const int fc = tl.n0 + c;  // first f column of this block (a multiple of 32)
+      if (fc >= fdim) break;
+      float gg[32], uu[32];
+      if (r < tl.rows) {
+        const uint4* src = reinterpret_cast<const uint4*>(g.aux + row * 2 * fdim + 2 * fc);  // 64 packed columns
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 a = __ldg(src + j), b = __ldg(src + 4 + j);
+          gg[8 * j + 0] = bf16_lo(a.x); gg[8 * j + 1] = bf16_hi(a.x); gg[8 * j + 2] = bf16_lo(a.y);
+          gg[8 * j + 3] = bf16_hi(a.y); gg[8 * j + 4] = bf16_lo(a.z); gg[8 * j + 5] = bf16_hi(a.z);
+          gg[8 * j + 6] = bf16_lo(a.w); gg[8 * j + 7] = bf16_hi(a.w);
+          uu[8 * j + 0] = bf16_lo(b.x); uu[8 * j + 1] = bf16_hi(b.x); uu[8 * j + 2] = bf16_lo(b.y);
+          uu[8 * j + 3] = bf16_hi(b.y); uu[8 * j + 4] = bf16_lo(b.z); uu[8 * j + 5] = bf16_hi(b.z);
+          uu[8 * j + 6] = bf16_lo(b.w); uu[8 * j + 7] = bf16_hi(b.w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) gg[i] = uu[i] = 0.0f;
+      }
+      float dg[32], du[32], hh[32], dp = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float dh = __uint_as_float(v[i]);
+        const float sg = __fdividef(1.0f, 1.0f + __expf(-gg[i]));
+        const float a = gg[i] * sg;
+        hh[i] = p * a * uu[i];
+        dp += dh * a * uu[i];
+        du[i] = p * dh * a;
+        dg[i] = p * dh * uu[i] * sg * (1.0f + gg[i] * (1.0f - sg));
+      }
+      uint4 pk[4];
+      const int64_t ld2 = static_cast<int64_t>(2 * fdim) * 2;
+      uint8_t* gbase = static_cast<uint8_t*>(g.out) + row_first * ld2 + static_cast<int64_t>(2 * fc) * 2;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        pk[j] = make_uint4(pack_bf16x2(dg[8 * j + 0], dg[8 * j + 1]), pack_bf16x2(dg[8 * j + 2], dg[8 * j + 3]),
+                           pack_bf16x2(dg[8 * j + 4], dg[8 * j + 5]), pack_bf16x2(dg[8 * j + 6], dg[8 * j + 7]));
+      warp_store_rows<4>(stage, pk, lane, gbase, ld2, rows_valid, 4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        pk[j] = make_uint4(pack_bf16x2(du[8 * j + 0], du[8 * j + 1]), pack_bf16x2(du[8 * j + 2], du[8 * j + 3]),
+                           pack_bf16x2(du[8 * j + 4], du[8 * j + 5]), pack_bf16x2(du[8 * j + 6], du[8 * j + 7]));
+      warp_store_rows<4>(stage, pk, lane, gbase + 64, ld2, rows_valid, 4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        pk[j] = make_uint4(pack_bf16x2(hh[8 * j + 0], hh[8 * j + 1]), pack_bf16x2(hh[8 * j + 2], hh[8 * j + 3]),
+                           pack_bf16x2(hh[8 * j + 4], hh[8 * j + 5]), pack_bf16x2(hh[8 * j + 6], hh[8 * j + 7]));
+      const int64_t ldh = static_cast<int64_t>(fdim) * 2;
+      warp_store_rows<4>(stage, pk, lane, static_cast<uint8_t*>(g.out2) + row_first * ldh + static_cast<int64_t>(fc) * 2,
+                         ldh, rows_valid, 4);
+      if (r < tl.rows) g.dp_part[row * (fdim / 32) + fc / 32] = dp;
     }
   } else {
     const float p = r < tl.rows ? __ldg(g.row_prob + row_first + lane) : 0.0f;

@@ -36,6 +36,7 @@ TAG_X = 1
 TAG_LOGITS = 2
 TAG_BIAS = 3
 TAG_ZIPF_PERM = 4
+TAG_DY = 5
 TAG_W_GATE = 10
 TAG_W_UP = 11
 TAG_W_DOWN = 12
@@ -120,6 +121,12 @@ def gen_x(w: Workload, T: int | None = None) -> np.ndarray:
     """x [T, d] in storage dtype (fp32 or bf16 bits)."""
     T = w.T if T is None else T
     return as_storage(_normal(_rng(w.seed, TAG_X), (T, w.d), 1.0), w.act_dtype)
+
+
+def gen_dy(w: Workload, T: int | None = None) -> np.ndarray:
+    """Output gradient dy [T, d] for the backward, N(0, 1), in storage dtype."""
+    T = w.T if T is None else T
+    return as_storage(_normal(_rng(w.seed, TAG_DY), (T, w.d), 1.0), w.act_dtype)
 
 
 def gen_bias(w: Workload) -> np.ndarray:
