@@ -53,6 +53,8 @@ def parse_args():
     p.add_argument("--rows-hint", type=int, default=None,
                    help="expected rows per local expert passed to the grouped GEMMs (default T*k/E); "
                         "it selects the GEMM kernel shape (>= 2048: CTA pairs, bf16)")
+    p.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
+                   help="backward: time moe_layer_backward (bf16 workloads) instead of the forward step")
     p.add_argument("--no-gather", action="store_true",
                    help="feed GEMM1 from a permuted copy of x instead of reading the token rows (row gather)")
     return p.parse_args()
@@ -535,11 +537,86 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def run_backward(args, w):
+    """One step = moe_layer_backward (maps, recomputed gate/up, dh + ScaledSwiGLU backward,
+    dx, router-logit and weight gradients) on inputs resident in HBM; K steps captured as
+    one CUDA graph and replayed inside the timed region."""
+    import torch
+    import torch.distributed as dist
+
+    if w.dtype != "bf16":
+        raise SystemExit("the backward is bf16 only")
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import mixture_experts_layer_103_b300 as moe
+    from synthetic import gen_dy
+
+    pk, pk_kind = peaks()
+    wr = w.replace(seed=w.seed + rank)
+    xd, lgd, dyd = to_dev(gen_x(wr)), to_dev(gen_logits(wr)), to_dev(gen_dy(wr))
+    Wg, Wu, Wd = (to_dev(a) for a in gen_weights(w))
+    pw = moe.moe_pack_weights(Wg, Wu, Wd, "bf16")
+    WguT = moe.moe_pack_weights_backward(Wg, Wu)
+    del Wg, Wu
+    ids, probs = moe.moe_route_topk(lgd, w.k)
+    out, ws = moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT)
+    for _ in range(args.warmup):
+        moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, ws=ws, out=out)
+    torch.cuda.synchronize()
+    if moe.moe_get_device_error(ws) != 0:
+        raise RuntimeError("device error during warm-up")
+    P = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, "bf16", maps_only=True)
+    N = int(P["offsets"][-1].item())
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=cs):
+        for _ in range(args.steps):
+            moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, ws=ws, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    e0_, e1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]))
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark("t_begin")
+    e0_.record()
+    g.replay()
+    e1_.record()
+    torch.cuda.synchronize()
+    clocks.mark("t_end")
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = max_over_ranks(e0_.elapsed_time(e1_) / args.steps, torch.device("cuda", local))
+    value = job_tokens_per_s(w.T, world, ms)
+    # the backward's GEMM work: recomputed gate/up 4NDF, dh 2NDF, dx 4NDF, weight gradients 6NDF
+    flops = 16.0 * N * w.d * w.f
+    line = {
+        "metric": "MoE-layer backward tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": workload_config(w), "pass": "backward",
+        "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                     "kernel": "whole backward (16 N d f FLOP)", "traffic": None, "peak_kind": pk_kind},
+        "N_pairs": N, "gpu_launches": 10 * args.steps, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.which == "backward":
+        run_backward(args, w)
     else:
         run_ours(args, w)
 

@@ -106,6 +106,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
          (static_cast<uint64_t>(2) << 61);
 }
+// Descriptor of an MN-major operand with 128-byte swizzle: each K index is one 128-byte row
+// of 64 MN-contiguous bf16 values, 8 such rows form a 1024-byte swizzle atom; atoms follow
+// each other along K every 1024 bytes (stride byte offset) and along MN every mn_stride
+// bytes (leading byte offset).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr, uint32_t mn_stride) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
 // Descriptor of an unswizzled matrix of 16-byte rows (core matrices of 8 rows x 16 B
 // stored contiguously, 128 bytes apart): the scale-factor source of tcgen05.cp.
 __device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
@@ -118,6 +127,10 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+// Same with both operands MN-major (bits 15 and 16 set: A and B transposed).
+__host__ __device__ constexpr uint32_t idesc_bf16_mn(int M, int N) {
+  return idesc_bf16(M, N) | (1u << 15) | (1u << 16);
 }
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: A, B E4M3 (format 0), scale type
 // UE8M0 (bit 23 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28; the scale-factor byte
