@@ -220,27 +220,29 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const WgradArgs 
         }
         (void)ptx::mbar_try_wait(empty_bar(s), ph ^ 1u);
         const uint32_t a_addr = sbase + s * kWStage, b_addr = a_addr + kWA;
-        const int r0 = r_begin + kb * kWBK;
-        // A: 64 rows x 16 chunks (two 64-column atoms); B: 64 rows x 32 chunks (four atoms)
+        // thread -> K row kr = gt / 4 of the stage: 4 of its 16 A chunks (two 64-column
+        // atoms) and 8 of its 32 B chunks (four atoms); one row lookup per stage
+        const int kr = gt >> 2, sub = gt & 3;
+        const int r = r_begin + kb * kWBK + kr;
+        const bool rv = r < r_end;
+        const int64_t tok = rv ? __ldg(g.row_token + r) : 0;
+        const int64_t ra = MODE == 1 ? tok : r, rb = MODE == 0 ? tok : r;
+        const uint32_t swz = static_cast<uint32_t>(kr & 7);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int qd = gt + kWGather * i;
-          const int kr = qd >> 4, atom = (qd >> 3) & 1, c = qd & 7;
-          const int r = r0 + kr, m = m0 + atom * 64 + c * 8;
-          const bool v = r < r_end && m < g.M;
-          const int64_t src_row = v ? (MODE == 1 ? __ldg(g.row_token + r) : r) : 0;
-          ptx::cp_async_16(a_addr + atom * 8192 + kr * 128 + ((c ^ (kr & 7)) << 4),
-                           v ? static_cast<const void*>(g.A + src_row * g.lda + m) : g.A, v ? 16u : 0u);
+        for (int j = 0; j < 4; ++j) {
+          const int cc = sub + 4 * j, atom = cc >> 3, c = cc & 7;
+          const int m = m0 + atom * 64 + c * 8;
+          const bool v = rv && m < g.M;
+          ptx::cp_async_16(a_addr + atom * 8192 + kr * 128 + ((c ^ swz) << 4),
+                           v ? static_cast<const void*>(g.A + ra * g.lda + m) : g.A, v ? 16u : 0u);
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int qd = gt + kWGather * i;
-          const int kr = qd >> 5, atom = (qd >> 3) & 3, c = qd & 7;
-          const int r = r0 + kr, n = n0 + atom * 64 + c * 8;
-          const bool v = r < r_end && n < g.N;
-          const int64_t src_row = v ? (MODE == 0 ? __ldg(g.row_token + r) : r) : 0;
-          ptx::cp_async_16(b_addr + atom * 8192 + kr * 128 + ((c ^ (kr & 7)) << 4),
-                           v ? static_cast<const void*>(g.B + src_row * g.ldb + n) : g.B, v ? 16u : 0u);
+        for (int j = 0; j < 8; ++j) {
+          const int cc = sub + 4 * j, atom = cc >> 3, c = cc & 7;
+          const int n = n0 + atom * 64 + c * 8;
+          const bool v = rv && n < g.N;
+          ptx::cp_async_16(b_addr + atom * 8192 + kr * 128 + ((c ^ swz) << 4),
+                           v ? static_cast<const void*>(g.B + rb * g.ldb + n) : g.B, v ? 16u : 0u);
         }
         ptx::cp_async_arrive_noinc(full_bar(s));
         if (++s == kWStages) { s = 0; ph ^= 1u; }
