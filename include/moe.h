@@ -192,8 +192,9 @@ size_t moe_mx_weight_scale_bytes(int E_loc, int rows, int K);
  *   Y2      device [N_cap, d]: fp32 for MOE_F32, bf16 otherwise
  *   workspace device >= moe_grouped_mlp_workspace_size(...) bytes, 256-byte aligned
  *   rows_hint  expected rows per local expert (e.g. moe_rows_hint(T, k, E)); it only picks
- *              the kernel shape (bf16 runs on CTA pairs with 256-row tiles from 2048 expected
- *              rows up), never the result's meaning; <= 0 uses N_cap / E_loc.
+ *              the kernel shape (bf16 GEMM1 runs on CTA pairs with 256-row tiles from 2048
+ *              expected rows up, bf16 GEMM2 from 128), never the result's meaning; <= 0 uses
+ *              N_cap / E_loc.
  * Requires d % 8 == 0 and f % 32 == 0 (bf16); d % 128 == 0 and f % 128 == 0 (MXFP8). */
 moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                            const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,

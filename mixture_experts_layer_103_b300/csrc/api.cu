@@ -119,6 +119,18 @@ static bool use_pair(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint) {
   return dt == MOE_BF16 && rows >= kPairRowsThreshold;
 }
 
+// GEMM2 (K = f, output d) on CTA pairs from 128 expected rows per expert: measured on B300
+// inside the layer step the pair kernel's halved per-SM weight traffic outweighs its
+// coarser row padding there (bf16_e64 at 512 rows: 127.3 -> 119.9 us; EP64 slice at 256
+// rows: 49.3 -> 45.0; at 1024 rows: even) but not for short segments (EP64 slice at 64
+// rows: 30.9 -> 34.9; Zipf EP8 slice at 16 rows: 49.6 -> 55.7 in isolation).
+constexpr int kPairRowsThresholdGemm2 = 128;
+
+static bool use_pair_gemm2(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint) {
+  const int64_t rows = rows_hint > 0 ? rows_hint : n_cap / (E_loc > 0 ? E_loc : 1);
+  return dt == MOE_BF16 && rows >= kPairRowsThresholdGemm2;
+}
+
 static cudaError_t run_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets,
                              const float* row_prob, int64_t n_cap, int E_loc, int d, int f, moe_dtype dt,
                              const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
@@ -138,8 +150,8 @@ static cudaError_t run_gemm2(const void* h, const uint8_t* h_sf, const int32_t* 
   if (dt == MOE_F32)
     return launch_simt_gemm2(static_cast<const float*>(h), offsets, n_cap, E_loc, d, f, static_cast<const float*>(Wd),
                              static_cast<float*>(Y2), st);
-  return launch_tc_gemm2(h, h_sf, offsets, n_cap, E_loc, d, f, dt == MOE_MXFP8, use_pair(dt, n_cap, E_loc, rows_hint),
-                         Wd, Wd_sf, Y2, err, kTimeoutNs, st);
+  return launch_tc_gemm2(h, h_sf, offsets, n_cap, E_loc, d, f, dt == MOE_MXFP8,
+                         use_pair_gemm2(dt, n_cap, E_loc, rows_hint), Wd, Wd_sf, Y2, err, kTimeoutNs, st);
 }
 
 static cudaError_t run_mlp(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
