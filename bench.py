@@ -477,7 +477,7 @@ def run_ours(args, w):
     # ---- end to end through moe_layer_forward with host buffers
     e2e = None
     if not args.no_e2e:
-        # Steps are pipelined over three streams with double-buffered device inputs and
+        # Steps are pipelined over three streams with triple-buffered device inputs and
         # outputs: step i's host->device copy and step i-1's device->host read overlap
         # step i-1's / i's compute.  Every step still copies its own inputs in and its
         # result out inside the timed region.
@@ -485,29 +485,30 @@ def run_ours(args, w):
         x_pin.copy_(xd.cpu())
         lg_pin = torch.empty(lgd.shape, dtype=lgd.dtype).pin_memory()
         lg_pin.copy_(lgd.cpu())
-        y_pin = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
-        xb = [torch.empty_like(xd) for _ in range(2)]
-        lgb = [torch.empty_like(lgd) for _ in range(2)]
-        yb = [torch.empty_like(y) for _ in range(2)]
+        nbuf = 3
+        y_pin = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(nbuf)]
+        xb = [torch.empty_like(xd) for _ in range(nbuf)]
+        lgb = [torch.empty_like(lgd) for _ in range(nbuf)]
+        yb = [torch.empty_like(y) for _ in range(nbuf)]
         ws_layer = moe.workspace(moe.moe_layer_workspace_size(T, d, w.f, w.E, k, E_loc, w.dtype))
         s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_comp = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
-        for b_ in range(2):  # start with every buffer free
+        ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_comp = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+        for b_ in range(nbuf):  # start with every buffer free
             ev_comp[b_].record(s_comp)
             ev_out[b_].record(s_out)
 
         def e2e_step(i):
-            b_ = i % 2
+            b_ = i % nbuf
             with torch.cuda.stream(s_in):
-                s_in.wait_event(ev_comp[b_])   # step i-2 has finished reading this input buffer
+                s_in.wait_event(ev_comp[b_])   # step i-nbuf has finished reading this input buffer
                 xb[b_].copy_(x_pin, non_blocking=True)
                 lgb[b_].copy_(lg_pin, non_blocking=True)
                 ev_in[b_].record(s_in)
             with torch.cuda.stream(s_comp):
                 s_comp.wait_event(ev_in[b_])
-                s_comp.wait_event(ev_out[b_])  # step i-2's result has left this output buffer
+                s_comp.wait_event(ev_out[b_])  # step i-nbuf's result has left this output buffer
                 if flush is not None:
                     flush.zero_()
                 moe.moe_layer_forward(xb[b_], lgb[b_], w.E, k, e0, pw, y=yb[b_], ws=ws_layer)
@@ -529,7 +530,7 @@ def run_ours(args, w):
         with torch.cuda.graph(ge, stream=cap):
             for st_ in (s_in, s_comp, s_out):
                 st_.wait_stream(cap)
-            for b_ in range(2):
+            for b_ in range(nbuf):
                 ev_comp[b_].record(s_comp)
                 ev_out[b_].record(s_out)
             for i in range(n2):
@@ -550,7 +551,7 @@ def run_ours(args, w):
                "h2d_bytes_per_step": int(x_pin_bytes + lg_pin.numel() * 4),
                "d2h_bytes_per_step": int(y_pin[0].numel() * y_pin[0].element_size()), "steps": n2,
                "entry_point": "moe_layer_forward",
-               "pipelining": "copies of neighbouring steps overlap compute (3 streams, 2 buffers), "
+               "pipelining": "copies of neighbouring steps overlap compute (3 streams, 3 buffers), "
                              "the steps replayed as one CUDA graph"}
 
     if world > 1:
