@@ -604,10 +604,11 @@ def run_backward(args, w):
     pw = moe.moe_pack_weights(Wg, Wu, Wd, "bf16")
     WguT = moe.moe_pack_weights_backward(Wg, Wu)
     del Wg, Wu
-    ids, probs = moe.moe_route_topk(lgd, w.k)
-    out, ws = moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT)
+    # the training forward keeps the routing and the gate/up pre-activations for the backward
+    _, ids, probs, gu, _ = moe.moe_layer_forward_train(xd, lgd, w.E, w.k, w.e0, pw)
+    out, ws = moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, gu_saved=gu)
     for _ in range(args.warmup):
-        moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, ws=ws, out=out)
+        moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, ws=ws, out=out, gu_saved=gu)
     torch.cuda.synchronize()
     if moe.moe_get_device_error(ws) != 0:
         raise RuntimeError("device error during warm-up")
@@ -618,7 +619,7 @@ def run_backward(args, w):
     cs.wait_stream(torch.cuda.current_stream())
     with torch.cuda.graph(g, stream=cs):
         for _ in range(args.steps):
-            moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, ws=ws, out=out)
+            moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, ws=ws, out=out, gu_saved=gu)
     g.replay()
     torch.cuda.synchronize()
     e0_, e1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -638,8 +639,9 @@ def run_backward(args, w):
     clk = clocks.stop()
     ms = max_over_ranks(e0_.elapsed_time(e1_) / args.steps, torch.device("cuda", local))
     value = job_tokens_per_s(w.T, world, ms)
-    # the backward's GEMM work: recomputed gate/up 4NDF, dh 2NDF, dx 4NDF, weight gradients 6NDF
-    flops = 16.0 * N * w.d * w.f
+    # the backward's GEMM work (g, u saved by the training forward): dh 2NDF, dx 4NDF,
+    # weight gradients 6NDF
+    flops = 12.0 * N * w.d * w.f
     line = {
         "metric": "MoE-layer backward tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -647,8 +649,9 @@ def run_backward(args, w):
         "config": workload_config(w), "pass": "backward",
         "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
-                     "kernel": "whole backward (16 N d f FLOP)", "traffic": None, "peak_kind": pk_kind},
-        "N_pairs": N, "gpu_launches": 10 * args.steps, "clocks": clk,
+                     "kernel": "whole backward (12 N d f FLOP)", "traffic": None, "peak_kind": pk_kind},
+        "N_pairs": N, "gpu_launches": 9 * args.steps, "clocks": clk,
+        "saved_preactivations": "from moe_layer_forward_train (no recompute)",
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

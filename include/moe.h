@@ -306,6 +306,8 @@ moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* d
  *   Wgu_packed         the forward's packed gate/up weights (moe_pack_weights, bf16)
  *   W_down             device bf16 [E_loc, f, d], the user layout
  *   WguT_packed        device bf16 [E_loc, d, 2f] from moe_pack_weights_backward
+ *   gu_saved           device bf16 [N_cap, 2f] from moe_layer_forward_train on the same
+ *                      inputs (the gate/up pre-activations), or NULL to recompute them
  *   dx                 device bf16 [T, d] out (zero rows for tokens with no local expert)
  *   dlogits            device fp32 [T, E] out
  *   dW_gate, dW_up     device fp32 [E_loc, d, f] out;  dW_down device fp32 [E_loc, f, d] out
@@ -315,10 +317,23 @@ moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* d
  * Requires d % 8 == 0, f % 32 == 0; 16-byte aligned x, dy, dx and weights.  bf16 only. */
 moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
                               int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
-                              const void* W_down, const void* WguT_packed, void* dx, float* dlogits, float* dW_gate,
-                              float* dW_up, float* dW_down, void* workspace, size_t workspace_bytes,
-                              moe_stream_t stream);
+                              const void* W_down, const void* WguT_packed, const void* gu_saved, void* dx,
+                              float* dlogits, float* dW_gate, float* dW_up, float* dW_down, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream);
 size_t moe_layer_backward_workspace_size(int T, int d, int f, int k, int E_loc);
+
+/* Training forward: moe_layer_forward (bf16) that also returns what the backward needs.
+ *   topk_ids, topk_probs  device [T, k] out: the routing (as moe_route_topk)
+ *   gu_saved              device bf16 [N_cap, 2f] out, N_cap = T * min(k, E_loc): row r holds
+ *                         g = x W_gate and u = x W_up of permuted row r (moe_permute's order)
+ *                         in the packed column order (columns 64b..64b+31 gate, the next 32
+ *                         up, of h columns 32b..32b+31), rounded to bf16; rows >= N unused
+ * The other arguments and the workspace are those of moe_layer_forward with dtype bf16;
+ * y is bit-identical to moe_layer_forward's. */
+moe_status moe_layer_forward_train(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0,
+                                   int E_loc, const void* Wgu_packed, const void* Wd_packed, void* y,
+                                   int32_t* topk_ids, float* topk_probs, void* gu_saved, void* workspace,
+                                   size_t workspace_bytes, moe_stream_t stream);
 
 /* Backward weight pack (one-off): WguT [E_loc, d, 2f] bf16, row c = rows c of W_gate and W_up
  * ([E_loc, d, f], src_dtype MOE_BF16 or MOE_F32) interleaved in 32-column blocks (packed

@@ -64,7 +64,8 @@ _SIGS = {
     "moe_quantize_mx_rows": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "moe_eplb_plan": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_layer_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                _SZ, _P]),
+                                _P, _SZ, _P]),
+    "moe_layer_forward_train": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_layer_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_pack_weights_backward": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),
@@ -330,9 +331,27 @@ def moe_pack_weights_backward(W_gate: torch.Tensor, W_up: torch.Tensor) -> torch
     return out
 
 
+def moe_layer_forward_train(x, logits, E: int, k: int, e0: int, pw: PackedWeights, y=None, ws=None):
+    """bf16 forward that also returns the routing and the gate/up pre-activations for the
+    backward: (y, topk_ids, topk_probs, gu_saved, ws)."""
+    T, d = x.shape
+    dev = x.device
+    y = y if y is not None else torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    probs = torch.empty(T, k, dtype=torch.float32, device=dev)
+    gu = torch.empty(n_cap(T, k, pw.E_loc), 2 * pw.f, dtype=torch.bfloat16, device=dev)
+    nb = moe_layer_workspace_size(T, d, pw.f, E, k, pw.E_loc, "bf16")
+    ws = ws if ws is not None else workspace(nb, dev)
+    _check("moe_layer_forward_train", _lib.moe_layer_forward_train(
+        _ptr(x), _ptr(logits), T, d, pw.f, E, k, e0, pw.E_loc, _ptr(pw.Wgu), _ptr(pw.Wd), _ptr(y), _ptr(ids),
+        _ptr(probs), _ptr(gu), _ptr(ws), ws.numel(), _stream()))
+    return y, ids, probs, gu, ws
+
+
 def moe_layer_backward(x, dy, topk_ids, topk_probs, E: int, e0: int, pw: PackedWeights, W_down: torch.Tensor,
-                       WguT: torch.Tensor, ws=None, out=None):
-    """Gradients of sum(dy * y) of the bf16 layer: dict(dx, dlogits, dW_gate, dW_up, dW_down)."""
+                       WguT: torch.Tensor, ws=None, out=None, gu_saved=None):
+    """Gradients of sum(dy * y) of the bf16 layer: dict(dx, dlogits, dW_gate, dW_up, dW_down).
+    gu_saved: the pre-activations from moe_layer_forward_train (else recomputed)."""
     T, d = x.shape
     k = topk_ids.shape[1]
     f, E_loc = pw.f, pw.E_loc
@@ -347,7 +366,7 @@ def moe_layer_backward(x, dy, topk_ids, topk_probs, E: int, e0: int, pw: PackedW
     ws = ws if ws is not None else workspace(nb, dev)
     _check("moe_layer_backward", _lib.moe_layer_backward(
         _ptr(x), _ptr(dy), _ptr(topk_ids), _ptr(topk_probs), T, d, f, E, k, e0, E_loc, _ptr(pw.Wgu), _ptr(W_down),
-        _ptr(WguT), _ptr(out["dx"]), _ptr(out["dlogits"]), _ptr(out["dW_gate"]), _ptr(out["dW_up"]),
+        _ptr(WguT), _ptr(gu_saved), _ptr(out["dx"]), _ptr(out["dlogits"]), _ptr(out["dW_gate"]), _ptr(out["dW_up"]),
         _ptr(out["dW_down"]), _ptr(ws), ws.numel(), _stream()))
     return out, ws
 

@@ -22,14 +22,14 @@ cudaError_t launch_simt_gemm2(const float* h, const int32_t* offsets, int64_t N_
 cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
                             int64_t N_cap, int E_loc, int d, int f, bool mx, bool pair, const void* Wgu,
                             const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns,
-                            cudaStream_t st);
+                            void* gu_save, cudaStream_t st);
 cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
                             int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
                             uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
                                    const int32_t* offsets, const float* row_prob, int E_loc, int d, int f, bool mx,
                                    const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
-                                   uint64_t timeout_ns, cudaStream_t st);
+                                   uint64_t timeout_ns, void* gu_save, cudaStream_t st);
 cudaError_t launch_quant_rows_mx(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
                                  uint8_t* xq, uint8_t* x_sf, cudaStream_t st);
 cudaError_t launch_tc_gemm_gather_store(const void* x, const int32_t* row_src_token, const int32_t* offsets,
@@ -134,13 +134,14 @@ static bool use_pair_gemm2(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint
 static cudaError_t run_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets,
                              const float* row_prob, int64_t n_cap, int E_loc, int d, int f, moe_dtype dt,
                              const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
-                             int rows_hint, cudaStream_t st) {
+                             int rows_hint, cudaStream_t st, void* gu_save = nullptr) {
   if (n_cap == 0) return cudaSuccess;
   if (dt == MOE_F32)
     return launch_simt_gemm1(static_cast<const float*>(perm_x), offsets, row_prob, n_cap, E_loc, d, f,
                              static_cast<const float*>(Wgu), static_cast<float*>(h), st);
   return launch_tc_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt == MOE_MXFP8,
-                         use_pair(dt, n_cap, E_loc, rows_hint), Wgu, Wgu_sf, h, h_sf, err, kTimeoutNs, st);
+                         use_pair(dt, n_cap, E_loc, rows_hint), Wgu, Wgu_sf, h, h_sf, err, kTimeoutNs, gu_save,
+                         st);
 }
 
 static cudaError_t run_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t n_cap, int E_loc,
@@ -157,10 +158,10 @@ static cudaError_t run_gemm2(const void* h, const uint8_t* h_sf, const int32_t* 
 static cudaError_t run_mlp(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
                            int64_t n_cap, int E_loc, int d, int f, moe_dtype dt, const void* Wgu, const uint8_t* Wgu_sf,
                            const void* Wd, const uint8_t* Wd_sf, void* Y2, uint8_t* scratch, int32_t* err,
-                           int rows_hint, cudaStream_t st) {
+                           int rows_hint, cudaStream_t st, void* gu_save = nullptr) {
   MlpScratch s = carve_mlp(scratch, n_cap, f, dt);
   cudaError_t e = run_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt, Wgu, Wgu_sf, s.h, s.h_sf, err,
-                            rows_hint, st);
+                            rows_hint, st, gu_save);
   if (e != cudaSuccess) return e;
   return run_gemm2(s.h, s.h_sf, offsets, n_cap, E_loc, d, f, dt, Wd, Wd_sf, Y2, err, rows_hint, st);
 }
@@ -443,7 +444,7 @@ moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale,
   if (N_cap == 0) return MOE_OK;
   return cuda_status(launch_tc_gemm1_gather(x, x_scale, row_src_token, offsets, row_prob, E_loc, d, f,
                                             dtype == MOE_MXFP8, Wgu_packed, Wgu_scale, h, h_scale,
-                                            static_cast<int32_t*>(workspace), kTimeoutNs, stream));
+                                            static_cast<int32_t*>(workspace), kTimeoutNs, nullptr, stream));
 }
 
 moe_status moe_quantize_mx_rows(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
@@ -480,10 +481,14 @@ size_t moe_layer_workspace_size(int T, int d, int f, int E, int k, int E_loc, mo
   return layer_layout(nullptr, T, d, f, E, k, E_loc, dtype).total;
 }
 
-moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0, int E_loc,
-                             moe_dtype dtype, const void* Wgu_packed, const uint8_t* Wgu_scale, const void* Wd_packed,
-                             const uint8_t* Wd_scale, void* y, void* workspace, size_t workspace_bytes,
-                             moe_stream_t stream) {
+// Layer forward behind moe_layer_forward and moe_layer_forward_train: ids/probs (when not
+// null) receive the routing instead of the workspace; gu_save (bf16 only) keeps the gate/up
+// pre-activations for the backward.
+static moe_status layer_forward_impl(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0,
+                                     int E_loc, moe_dtype dtype, const void* Wgu_packed, const uint8_t* Wgu_scale,
+                                     const void* Wd_packed, const uint8_t* Wd_scale, void* y, int32_t* ids,
+                                     float* probs, void* gu_save, void* workspace, size_t workspace_bytes,
+                                     moe_stream_t stream) {
   if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
   if (e0 < 0 || E_loc < 1 || e0 + E_loc > E) return MOE_ERR_INVALID_ARG;
   moe_status s = check_mlp_shape(d, f, E_loc, dtype);
@@ -496,6 +501,8 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
   const size_t need = moe_layer_workspace_size(T, d, f, E, k, E_loc, dtype);
   if (!workspace || !aligned256(workspace) || workspace_bytes < need) return MOE_ERR_WORKSPACE;
   LayerWs w = layer_layout(static_cast<uint8_t*>(workspace), T, d, f, E, k, E_loc, dtype);
+  if (ids) w.topk_ids = ids;
+  if (probs) w.topk_probs = probs;
   const int64_t n_cap = n_cap_of(T, k, E_loc);
   const moe_dtype x_dtype = dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
   const int hint = moe_rows_hint(T, k, E);
@@ -511,7 +518,7 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
     MlpScratch s = carve_mlp(w.mlp, n_cap, f, dtype);
     if (e == cudaSuccess && n_cap > 0)
       e = launch_tc_gemm1_gather(mx ? w.perm_x : x, w.perm_sf, w.row_src_token, w.offsets, w.row_prob, E_loc, d, f,
-                                 mx, Wgu_packed, Wgu_scale, s.h, s.h_sf, w.err, kTimeoutNs, stream);
+                                 mx, Wgu_packed, Wgu_scale, s.h, s.h_sf, w.err, kTimeoutNs, gu_save, stream);
     if (e == cudaSuccess)
       e = run_gemm2(s.h, s.h_sf, w.offsets, n_cap, E_loc, d, f, dtype, Wd_packed, Wd_scale, w.Y2, w.err, hint, stream);
   } else {
@@ -520,10 +527,27 @@ moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, i
                          w.counts, w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
     if (e == cudaSuccess)
       e = run_mlp(w.perm_x, w.perm_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale,
-                  Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, hint, stream);
+                  Wd_packed, Wd_scale, w.Y2, w.mlp, w.err, hint, stream, gu_save);
   }
   if (e == cudaSuccess) e = launch_combine(w.Y2, w.pair_to_row, T, k, d, dtype, y, stream);
   return cuda_status(e);
+}
+
+moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0, int E_loc,
+                             moe_dtype dtype, const void* Wgu_packed, const uint8_t* Wgu_scale, const void* Wd_packed,
+                             const uint8_t* Wd_scale, void* y, void* workspace, size_t workspace_bytes,
+                             moe_stream_t stream) {
+  return layer_forward_impl(x, logits, T, d, f, E, k, e0, E_loc, dtype, Wgu_packed, Wgu_scale, Wd_packed, Wd_scale, y,
+                            nullptr, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_layer_forward_train(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0,
+                                   int E_loc, const void* Wgu_packed, const void* Wd_packed, void* y,
+                                   int32_t* topk_ids, float* topk_probs, void* gu_saved, void* workspace,
+                                   size_t workspace_bytes, moe_stream_t stream) {
+  if (T > 0 && (!topk_ids || !topk_probs || !gu_saved || !aligned16(gu_saved))) return MOE_ERR_INVALID_ARG;
+  return layer_forward_impl(x, logits, T, d, f, E, k, e0, E_loc, MOE_BF16, Wgu_packed, nullptr, Wd_packed, nullptr, y,
+                            topk_ids, topk_probs, gu_saved, workspace, workspace_bytes, stream);
 }
 
 moe_status moe_pack_weights_backward(const void* W_gate, const void* W_up, moe_dtype src_dtype, int E_loc, int d,
@@ -540,15 +564,16 @@ size_t moe_layer_backward_workspace_size(int T, int d, int f, int k, int E_loc) 
 
 moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
                               int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
-                              const void* W_down, const void* WguT_packed, void* dx, float* dlogits, float* dW_gate,
-                              float* dW_up, float* dW_down, void* workspace, size_t workspace_bytes,
-                              moe_stream_t stream) {
+                              const void* W_down, const void* WguT_packed, const void* gu_saved, void* dx,
+                              float* dlogits, float* dW_gate, float* dW_up, float* dW_down, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream) {
   if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32 || e0 < 0 || E_loc < 1 || e0 + E_loc > E)
     return MOE_ERR_INVALID_ARG;
   moe_status s = check_mlp_shape(d, f, E_loc, MOE_BF16);
   if (s != MOE_OK) return s;
   if (!Wgu_packed || !W_down || !WguT_packed || !dW_gate || !dW_up || !dW_down) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !dy || !topk_ids || !topk_probs || !dx || !dlogits)) return MOE_ERR_INVALID_ARG;
+  if (gu_saved && !aligned16(gu_saved)) return MOE_ERR_INVALID_ARG;
   if ((T > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))) || !aligned16(Wgu_packed) ||
       !aligned16(W_down) || !aligned16(WguT_packed))
     return MOE_ERR_INVALID_ARG;
@@ -562,12 +587,12 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
                        w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
   else
     e = cudaMemsetAsync(w.offsets, 0, static_cast<size_t>(E_loc + 1) * 4, stream);
-  if (e == cudaSuccess && n_cap > 0)
+  if (e == cudaSuccess && n_cap > 0 && !gu_saved)  // recompute g, u unless the forward kept them
     e = launch_tc_gemm_gather_store(x, w.row_src_token, w.offsets, E_loc, d, 2 * f, Wgu_packed, w.gu, w.err,
                                     kTimeoutNs, stream);
   if (e == cudaSuccess && n_cap > 0)
-    e = launch_tc_dswiglu(dy, w.row_src_token, w.offsets, w.row_prob, E_loc, d, f, W_down, w.gu, w.dgu, w.h,
-                          w.dp_part, w.err, kTimeoutNs, stream);
+    e = launch_tc_dswiglu(dy, w.row_src_token, w.offsets, w.row_prob, E_loc, d, f, W_down,
+                          gu_saved ? gu_saved : w.gu, w.dgu, w.h, w.dp_part, w.err, kTimeoutNs, stream);
   if (e == cudaSuccess && n_cap > 0)
     e = launch_tc_gemm_store(w.dgu, n_cap, w.offsets, E_loc, 2 * f, d, WguT_packed, w.dxp, w.err, kTimeoutNs,
                              stream);

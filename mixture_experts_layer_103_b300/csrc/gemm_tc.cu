@@ -527,8 +527,9 @@ cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const
 cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
                             int64_t N_cap, int E_loc, int d, int f, bool mx, bool pair, const void* Wgu,
                             const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns,
-                            cudaStream_t st) {
+                            void* gu_save, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
+  g.out2 = mx ? nullptr : gu_save;
   g.n_out = 2 * f;
   g.K = d;
   g.out = h;
@@ -548,8 +549,9 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
 cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
                                    const int32_t* offsets, const float* row_prob, int E_loc, int d, int f, bool mx,
                                    const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
-                                   uint64_t timeout_ns, cudaStream_t st) {
+                                   uint64_t timeout_ns, void* gu_save, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
+  g.out2 = mx ? nullptr : gu_save;
   g.n_out = 2 * f;
   g.K = d;
   g.out = h;

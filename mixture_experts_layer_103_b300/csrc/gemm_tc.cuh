@@ -43,6 +43,8 @@ struct GemmArgs {
   // pre-activations g/u [N_cap, 2f] bf16 in the packed column order; out = dg/du in the
   // same order (ld_out = 2f); out2 = h [N_cap, f] bf16; dp_part [N_cap, f / 32] fp32 =
   // per-32-column partial sums of dh * silu(g) * u.
+  // EPI_SWIGLU_BF16 with out2 set (training forward): out2 receives g/u [N_cap, 2f] bf16 in
+  // the packed column order, as the backward's aux.
   const uint16_t* aux;
   void* out2;
   float* dp_part;
@@ -229,6 +231,24 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl,
         warp_store_rows<4>(stage, pk, lane,
                            static_cast<uint8_t*>(g.out) + row_first * ld + static_cast<int64_t>(fc) * 2, ld,
                            rows_valid, fc < fdim ? 4 : 0);
+        if (g.out2 && fc < fdim) {  // training forward: keep g and u (bf16, packed order) for the backward
+          const int64_t ld2 = static_cast<int64_t>(g.n_out) * 2;
+          uint8_t* gbase = static_cast<uint8_t*>(g.out2) + row_first * ld2 + static_cast<int64_t>(2 * fc) * 2;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            pk[j] = make_uint4(pack_bf16x2(__uint_as_float(gv[8 * j + 0]), __uint_as_float(gv[8 * j + 1])),
+                               pack_bf16x2(__uint_as_float(gv[8 * j + 2]), __uint_as_float(gv[8 * j + 3])),
+                               pack_bf16x2(__uint_as_float(gv[8 * j + 4]), __uint_as_float(gv[8 * j + 5])),
+                               pack_bf16x2(__uint_as_float(gv[8 * j + 6]), __uint_as_float(gv[8 * j + 7])));
+          warp_store_rows<4>(stage, pk, lane, gbase, ld2, rows_valid, 4);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            pk[j] = make_uint4(pack_bf16x2(__uint_as_float(uv[8 * j + 0]), __uint_as_float(uv[8 * j + 1])),
+                               pack_bf16x2(__uint_as_float(uv[8 * j + 2]), __uint_as_float(uv[8 * j + 3])),
+                               pack_bf16x2(__uint_as_float(uv[8 * j + 4]), __uint_as_float(uv[8 * j + 5])),
+                               pack_bf16x2(__uint_as_float(uv[8 * j + 6]), __uint_as_float(uv[8 * j + 7])));
+          warp_store_rows<4>(stage, pk, lane, gbase + 64, ld2, rows_valid, 4);
+        }
       } else {
         float amax = 0.0f;
 #pragma unroll

@@ -129,5 +129,11 @@ def test_validation_before_any_launch(lib):
     assert L.moe_quantize_mx_rows(P, 1, -1, 64, None, 0, P, P, s) == 1
     assert L.moe_quantize_mx_rows(P, 2, 4, 64, None, 0, P, P, s) == 2
     assert L.moe_quantize_mx_rows(P, 1, 4, 64, P, 33, P, P, s) == 1
+    # training forward: missing routing / pre-activation outputs
+    assert L.moe_layer_forward_train(P, P, 8, 64, 64, 8, 2, 0, 8, P, P, P, None, P, P, P, 1 << 30, s) == 1
+    assert L.moe_layer_forward_train(P, P, 8, 64, 64, 8, 2, 0, 8, P, P, P, P, P, None, P, 1 << 30, s) == 1
+    # backward: misaligned saved pre-activations
+    assert L.moe_layer_backward(P, P, P, P, 8, 64, 64, 8, 2, 0, 8, P, P, P, ctypes.c_void_p(264), P, P, P, P, P, P,
+                                1 << 30, s) == 1
     # device error read: null output
     assert L.moe_get_device_error(P, s, None) == 1

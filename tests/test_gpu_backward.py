@@ -114,3 +114,28 @@ def test_backward_full_size_sampled(moe):
     ref = oracle.moe_backward(x, "bf16", lg, dy, "bf16", w.k, w.e0, w.E_loc, "bf16", Wg, Wu, Wd, tokens=tok,
                               experts=experts)
     _check(g, ref, tokens=tok, experts=experts)
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[2]], ids=["b_slice", "b_e64"])
+def test_training_forward_saves_preactivations(moe, w):
+    """moe_layer_forward_train: y bit-identical to moe_layer_forward, routing equal to
+    moe_route_topk, and the backward on its saved g/u bit-identical to the backward that
+    recomputes them."""
+    x, lg, dy = gen_x(w), gen_logits(w), gen_dy(w)
+    Wg, Wu, Wd = gen_weights(w)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), "bf16")
+    WguT = moe.moe_pack_weights_backward(to_dev(Wg), to_dev(Wu))
+    xd, lgd, dyd = to_dev(x), to_dev(lg), to_dev(dy)
+    y_t, ids, probs, gu, ws = moe.moe_layer_forward_train(xd, lgd, w.E, w.k, w.e0, pw)
+    y, _ = moe.moe_layer_forward(xd, lgd, w.E, w.k, w.e0, pw)
+    ids2, probs2 = moe.moe_route_topk(lgd, w.k)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    assert torch.equal(y_t, y) and torch.equal(ids, ids2) and torch.equal(probs, probs2)
+    g_saved, ws1 = moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, to_dev(Wd), WguT, gu_saved=gu)
+    g_saved = {k: v.clone() for k, v in g_saved.items()}
+    g_recomp, ws2 = moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, to_dev(Wd), WguT)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws1) == 0 and moe.moe_get_device_error(ws2) == 0
+    for key in g_saved:
+        assert torch.equal(g_saved[key], g_recomp[key]), key
