@@ -1,5 +1,6 @@
 // C ABI of the MoE expert-layer library: argument validation, workspace layout and the
 // launch sequence of each entry point (declared and documented in include/moe.h).
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -46,11 +47,11 @@ cudaError_t launch_pack_gu_t(const void* Wg, const void* Wu, moe_dtype src, int 
 cudaError_t launch_dlogits(const int32_t* ids, const float* probs, const int32_t* p2r, const float* dp_part,
                            int nparts, int T, int E, int k, float* dlogits, cudaStream_t st);
 cudaError_t launch_wgrad_down_tc(const void* h, const void* dy, const int32_t* row_token, const int32_t* offsets,
-                                 int E_loc, int d, int f, float* dWd, int32_t* err, uint64_t timeout_ns,
-                                 cudaStream_t st);
+                                 int64_t n_rows, int E_loc, int d, int f, float* dWd, int32_t* err,
+                                 uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_wgrad_gate_up_tc(const void* x, const void* dgu, const int32_t* row_token,
-                                    const int32_t* offsets, int E_loc, int d, int f, float* dWg, float* dWu,
-                                    int32_t* err, uint64_t timeout_ns, cudaStream_t st);
+                                    const int32_t* offsets, int64_t n_rows, int E_loc, int d, int f, float* dWg,
+                                    float* dWu, int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
@@ -600,10 +601,11 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
   if (e == cudaSuccess)
     e = launch_dlogits(topk_ids, topk_probs, w.pair_to_row, w.dp_part, f / 32, T, E, k, dlogits, stream);
   if (e == cudaSuccess)
-    e = launch_wgrad_down_tc(w.h, dy, w.row_src_token, w.offsets, E_loc, d, f, dW_down, w.err, kTimeoutNs, stream);
+    e = launch_wgrad_down_tc(w.h, dy, w.row_src_token, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_down,
+                             w.err, kTimeoutNs, stream);
   if (e == cudaSuccess)
-    e = launch_wgrad_gate_up_tc(x, w.dgu, w.row_src_token, w.offsets, E_loc, d, f, dW_gate, dW_up, w.err,
-                                kTimeoutNs, stream);
+    e = launch_wgrad_gate_up_tc(x, w.dgu, w.row_src_token, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f,
+                                dW_gate, dW_up, w.err, kTimeoutNs, stream);
   return cuda_status(e);
 }
 

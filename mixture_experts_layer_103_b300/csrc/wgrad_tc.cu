@@ -4,10 +4,13 @@
 // The contraction runs over the expert's routed rows, so K is ragged per expert while
 // M and N are the same for every expert.  Both operands are row-major [rows, M or N]:
 // each routed row is one K index holding M (or N) contiguous values, i.e. MN-major tiles.
-// Eight gather warps copy every stage with cp.async straight from the rows (through
-// row_token where the operand is indexed by token), zero-filling rows past the segment
-// end and columns past M / N, into the 128-byte-swizzled MN-major layout; a stage's full
-// barrier counts each thread's copies as they land (cp.async.mbarrier.arrive).  One
+// The operand indexed by token is gathered by eight warps with cp.async straight from the
+// rows (through row_token), zero-filling rows past the segment end and columns past M / N,
+// into the 128-byte-swizzled MN-major layout; a stage's full barrier counts each thread's
+// copies as they land (cp.async.mbarrier.arrive).  The other operand (rows in routed
+// order) is loaded by TMA, 64 x 64 boxes, for every full 64-row block of a segment, and by
+// the gather warps for a segment's last, partial block (TMA cannot stop at the segment
+// end).  One
 // thread issues tcgen05.mma (both operands MN-major) into a double-buffered TMEM
 // accumulator; four warps store the fp32 tiles.  Persistent: one CTA per SM, tiles
 // (expert, m-tile, n-tile) round-robin.  Experts without rows get zero tiles.
@@ -28,7 +31,7 @@ constexpr int kWA = kWBM * kWBK * 2;                   // 16 KB
 constexpr int kWB = kWBN * kWBK * 2;                   // 32 KB
 constexpr int kWStage = kWA + kWB;
 constexpr int kWGather = 256;                          // gather threads (8 warps)
-constexpr int kWThreads = 32 + 128 + kWGather;         // MMA warp, 4 epilogue warps, gather warps
+constexpr int kWThreads = 32 + 128 + kWGather + 32;    // MMA warp, 4 epilogue, 8 gather, TMA warp
 constexpr int kWEpiPitch = 144;                        // 128 data bytes + 16 pad per staged row
 constexpr int kWOffEpi = kWStages * kWStage;
 constexpr int kWOffBar = kWOffEpi + 4 * 32 * kWEpiPitch;
@@ -50,7 +53,8 @@ struct WgradArgs {
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const WgradArgs g) {
+__global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmD,
+                                                                const WgradArgs g) {
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -66,7 +70,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const WgradArgs 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
-      ptx::mbar_init(full_bar(s), kWGather);
+      ptx::mbar_init(full_bar(s), kWGather + 1);  // gather threads + the TMA thread
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -198,6 +202,45 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const WgradArgs 
         if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
       }
     }
+  } else if (warp == 13) {
+    // ------------------------------------------------------------------ TMA (direct operand)
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmD);
+      int s = 0;
+      uint32_t ph = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      constexpr int kDirectBytes = MODE == 0 ? kWA : kWB;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int e = t / per_e, rem = t - e * per_e;
+        const int m0 = (rem / nt_n) * kWBM, n0 = (rem % nt_n) * kWBN;
+        const int r_begin = __ldg(g.offsets + e), r_end = __ldg(g.offsets + e + 1);
+        const int nkb = (r_end - r_begin + kWBK - 1) / kWBK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (*s_abort) { ok = false; break; }
+          if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) { gemm_abort(abort_args, s_abort); ok = false; break; }
+          const int r0 = r_begin + kb * kWBK;
+          if (r0 + kWBK <= r_end) {
+            const uint32_t a_addr = sbase + s * kWStage;
+            ptx::mbar_arrive_expect_tx(full_bar(s), kDirectBytes);
+            if (MODE == 0) {
+              for (int a = 0; a < kWBM / 64; ++a) ptx::tma_load_3d(a_addr + a * 8192, &tmD, full_bar(s), m0 + 64 * a, r0, 0);
+            } else {
+              for (int a = 0; a < kWBN / 64; ++a)
+                ptx::tma_load_3d(a_addr + kWA + a * 8192, &tmD, full_bar(s), n0 + 64 * a, r0, 0);
+            }
+            ++issued;
+          } else {
+            ptx::mbar_arrive(full_bar(s));  // the gather warps load this partial block
+          }
+          if (++s == kWStages) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {  // let the issued copies land before the CTA exits
+        for (int i = 0; i < kWStages; ++i) ptx::mbar_wait(full_bar(i), 0, 1000000ull);
+      }
+      (void)issued;
+    }
   } else {
     // ------------------------------------------------------------------ gather
     const int gt = threadIdx.x - 160;
@@ -225,11 +268,13 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const WgradArgs 
         const int kr = gt >> 2, sub = gt & 3;
         const int r = r_begin + kb * kWBK + kr;
         const bool rv = r < r_end;
+        const bool partial = r_begin + (kb + 1) * kWBK > r_end;  // else TMA loads the direct operand
         const int64_t tok = rv ? __ldg(g.row_token + r) : 0;
         const int64_t ra = MODE == 1 ? tok : r, rb = MODE == 0 ? tok : r;
         const uint32_t swz = static_cast<uint32_t>(kr & 7);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
+          if (MODE == 0 && !partial) break;
           const int cc = sub + 4 * j, atom = cc >> 3, c = cc & 7;
           const int m = m0 + atom * 64 + c * 8;
           const bool v = rv && m < g.M;
@@ -238,6 +283,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const WgradArgs 
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
+          if (MODE == 1 && !partial) break;
           const int cc = sub + 4 * j, atom = cc >> 3, c = cc & 7;
           const int n = n0 + atom * 64 + c * 8;
           const bool v = rv && n < g.N;
@@ -259,8 +305,13 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const WgradArgs 
   }
 }
 
+// D: the operand in routed-row order (MODE 0: h [n_rows, f]; MODE 1: dg/du [n_rows, 2f]),
+// cols values per row; its TMA map has 64 x 64 boxes.
 template <int MODE>
-static cudaError_t launch_wgrad_tc(const WgradArgs& g, cudaStream_t st) {
+static cudaError_t launch_wgrad_tc(const WgradArgs& g, const void* D, int cols, int64_t n_rows, cudaStream_t st) {
+  CUtensorMap tmD;
+  if (!make_operand_map(&tmD, D, false, static_cast<uint64_t>(cols), static_cast<uint64_t>(n_rows), 1, 64))
+    return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -270,23 +321,24 @@ static cudaError_t launch_wgrad_tc(const WgradArgs& g, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  return launch_pdl(wgrad_tc_kernel<MODE>, dim3(static_cast<unsigned>(num_sms())), dim3(kWThreads), kWSmem, st, g);
+  return launch_pdl(wgrad_tc_kernel<MODE>, dim3(static_cast<unsigned>(num_sms())), dim3(kWThreads), kWSmem, st, tmD,
+                    g);
 }
 
 cudaError_t launch_wgrad_down_tc(const void* h, const void* dy, const int32_t* row_token, const int32_t* offsets,
-                                 int E_loc, int d, int f, float* dWd, int32_t* err, uint64_t timeout_ns,
-                                 cudaStream_t st) {
+                                 int64_t n_rows, int E_loc, int d, int f, float* dWd, int32_t* err,
+                                 uint64_t timeout_ns, cudaStream_t st) {
   WgradArgs g{static_cast<const uint16_t*>(h), f, static_cast<const uint16_t*>(dy), d, row_token, offsets,
               E_loc, f, d, dWd, nullptr, err, timeout_ns};
-  return launch_wgrad_tc<0>(g, st);
+  return launch_wgrad_tc<0>(g, h, f, n_rows, st);
 }
 
 cudaError_t launch_wgrad_gate_up_tc(const void* x, const void* dgu, const int32_t* row_token,
-                                    const int32_t* offsets, int E_loc, int d, int f, float* dWg, float* dWu,
-                                    int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
+                                    const int32_t* offsets, int64_t n_rows, int E_loc, int d, int f, float* dWg,
+                                    float* dWu, int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
   WgradArgs g{static_cast<const uint16_t*>(x), d, static_cast<const uint16_t*>(dgu), 2 * f, row_token, offsets,
               E_loc, d, 2 * f, dWg, dWu, err, timeout_ns};
-  return launch_wgrad_tc<1>(g, st);
+  return launch_wgrad_tc<1>(g, dgu, 2 * f, n_rows, st);
 }
 
 }  // namespace moe
