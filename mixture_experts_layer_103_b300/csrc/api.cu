@@ -46,12 +46,14 @@ cudaError_t launch_pack_gu_t(const void* Wg, const void* Wu, moe_dtype src, int 
                              cudaStream_t st);
 cudaError_t launch_dlogits(const int32_t* ids, const float* probs, const int32_t* p2r, const float* dp_part,
                            int nparts, int T, int E, int k, float* dlogits, cudaStream_t st);
-cudaError_t launch_wgrad_down_tc(const void* h, const void* dy, const int32_t* row_token, const int32_t* offsets,
-                                 int64_t n_rows, int E_loc, int d, int f, float* dWd, int32_t* err,
-                                 uint64_t timeout_ns, cudaStream_t st);
-cudaError_t launch_wgrad_gate_up_tc(const void* x, const void* dgu, const int32_t* row_token,
-                                    const int32_t* offsets, int64_t n_rows, int E_loc, int d, int f, float* dWg,
-                                    float* dWu, int32_t* err, uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_wgrad_down_tc(const void* h, const void* dy_rows, const int32_t* offsets, int64_t n_rows,
+                                 int E_loc, int d, int f, float* dWd, int32_t* err, uint64_t timeout_ns,
+                                 cudaStream_t st);
+cudaError_t launch_wgrad_gate_up_tc(const void* x_rows, const void* dgu, const int32_t* offsets, int64_t n_rows,
+                                    int E_loc, int d, int f, float* dWg, float* dWu, int32_t* err,
+                                    uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_gather_rows(const void* src, int64_t row_bytes, const int32_t* offsets, int E_loc,
+                               const int32_t* row_src_token, void* dst, cudaStream_t st);
 cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
@@ -241,6 +243,8 @@ struct BackwardWs {
   void* h;         // [N_cap, f] bf16
   float* dp_part;  // [N_cap, f / 32]
   void* dxp;       // [N_cap, d] bf16
+  void* x_rows;    // [N_cap, d] bf16: x and dy in routed-row order, the weight-gradient
+  void* dy_rows;   //   operands (TMA-loadable, unlike token-indexed rows)
   size_t total;
 };
 static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int E_loc) {
@@ -264,6 +268,8 @@ static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int
   w.h = take(static_cast<size_t>(n_cap) * f * 2);
   w.dp_part = reinterpret_cast<float*>(take(static_cast<size_t>(n_cap) * (f / 32) * 4));
   w.dxp = take(static_cast<size_t>(n_cap) * d * 2);
+  w.x_rows = take(static_cast<size_t>(n_cap) * d * 2);
+  w.dy_rows = take(static_cast<size_t>(n_cap) * d * 2);
   w.total = o;
   return w;
 }
@@ -601,11 +607,15 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
   if (e == cudaSuccess)
     e = launch_dlogits(topk_ids, topk_probs, w.pair_to_row, w.dp_part, f / 32, T, E, k, dlogits, stream);
   if (e == cudaSuccess)
-    e = launch_wgrad_down_tc(w.h, dy, w.row_src_token, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_down,
-                             w.err, kTimeoutNs, stream);
+    e = launch_gather_rows(dy, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.dy_rows, stream);
   if (e == cudaSuccess)
-    e = launch_wgrad_gate_up_tc(x, w.dgu, w.row_src_token, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f,
-                                dW_gate, dW_up, w.err, kTimeoutNs, stream);
+    e = launch_gather_rows(x, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.x_rows, stream);
+  if (e == cudaSuccess)
+    e = launch_wgrad_down_tc(w.h, w.dy_rows, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_down, w.err,
+                             kTimeoutNs, stream);
+  if (e == cudaSuccess)
+    e = launch_wgrad_gate_up_tc(w.x_rows, w.dgu, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_gate, dW_up,
+                                w.err, kTimeoutNs, stream);
   return cuda_status(e);
 }
 

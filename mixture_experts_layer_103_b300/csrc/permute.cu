@@ -332,6 +332,13 @@ static PermuteWs carve_permute_ws(uint8_t* base, int T, int E_loc) {
 }
 
 int gather_grid(cudaStream_t st);
+// Rows of src (row_bytes each, a multiple of 16) into routed order: dst row r = src row
+// row_src_token[r] for r < offsets[E_loc] (the permute's gather on its own).
+cudaError_t launch_gather_rows(const void* src, int64_t row_bytes, const int32_t* offsets, int E_loc,
+                               const int32_t* row_src_token, void* dst, cudaStream_t st) {
+  return launch_pdl(perm_gather_copy_kernel, dim3(gather_grid(st)), dim3(256), 0, st, static_cast<const uint4*>(src),
+                    row_bytes / 16, offsets, E_loc, row_src_token, static_cast<uint4*>(dst));
+}
 
 // perm_dtype: MOE_F32 / MOE_BF16 (copy in x's type) or MOE_MXFP8 (quantise).
 cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d,

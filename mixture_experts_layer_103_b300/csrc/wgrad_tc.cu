@@ -1,22 +1,20 @@
 // Weight gradients of the expert layer on the 5th-generation tensor cores:
 //   C_e[M, N] = sum over the rows r of expert e's segment [offsets[e], offsets[e+1]) of
-//               A[ra(r), 0:M]^T B[rb(r), 0:N]            (fp32 accumulate, fp32 out)
+//               A[r, 0:M]^T B[r, 0:N]                     (fp32 accumulate, fp32 out)
 // The contraction runs over the expert's routed rows, so K is ragged per expert while
-// M and N are the same for every expert.  Both operands are row-major [rows, M or N]:
-// each routed row is one K index holding M (or N) contiguous values, i.e. MN-major tiles.
-// The operand indexed by token is gathered by eight warps with cp.async straight from the
-// rows (through row_token), zero-filling rows past the segment end and columns past M / N,
-// into the 128-byte-swizzled MN-major layout; a stage's full barrier counts each thread's
-// copies as they land (cp.async.mbarrier.arrive).  The other operand (rows in routed
-// order) is loaded by TMA, 64 x 64 boxes, for every full 64-row block of a segment, and by
-// the gather warps for a segment's last, partial block (TMA cannot stop at the segment
-// end).  One
+// M and N are the same for every expert.  Both operands are row-major [rows, M or N] in
+// routed-row order (the token-indexed operand is first copied into that order): each row
+// is one K index holding M (or N) contiguous values, i.e. MN-major tiles.  One thread
+// loads every full 64-row block of a segment by TMA (64 x 64 boxes, 128-byte swizzle);
+// a segment's last, partial block is loaded by eight warps with cp.async, zero-filling
+// the rows past the segment end (TMA cannot stop there) and the columns past M / N, and
+// counted on the stage's full barrier as it lands (cp.async.mbarrier.arrive).  One
 // thread issues tcgen05.mma (both operands MN-major) into a double-buffered TMEM
 // accumulator; four warps store the fp32 tiles.  Persistent: one CTA per SM, tiles
 // (expert, m-tile, n-tile) round-robin.  Experts without rows get zero tiles.
-//   MODE 0: dW_down_e [f, d] = h^T dy (A = h rows direct, B = dy rows by token)
-//   MODE 1: dW_gate_e, dW_up_e [d, f] = x^T dg, x^T du (A = x rows by token, B = dg/du rows
-//           in the packed order, stored back to the gate and up matrices)
+//   MODE 0: dW_down_e [f, d] = h^T dy   (A = h, B = dy in routed order)
+//   MODE 1: dW_gate_e, dW_up_e [d, f] = x^T dg, x^T du (A = x in routed order, B = dg/du in
+//           the packed order, stored back to the gate and up matrices)
 // ("Efficient MoE training for biological foundation models", section "GroupedLinear
 // Optimizes Expert Computation": the GroupedMLP backward's weight-gradient GEMMs.)
 #include <algorithm>
@@ -30,8 +28,8 @@ constexpr int kWStages = 4;
 constexpr int kWA = kWBM * kWBK * 2;                   // 16 KB
 constexpr int kWB = kWBN * kWBK * 2;                   // 32 KB
 constexpr int kWStage = kWA + kWB;
-constexpr int kWGather = 256;                          // gather threads (8 warps)
-constexpr int kWThreads = 32 + 128 + kWGather + 32;    // MMA warp, 4 epilogue, 8 gather, TMA warp
+constexpr int kWGather = 256;                          // partial-block copy threads (8 warps)
+constexpr int kWThreads = 32 + 128 + kWGather + 32;    // MMA warp, 4 epilogue, 8 copy, TMA warp
 constexpr int kWEpiPitch = 144;                        // 128 data bytes + 16 pad per staged row
 constexpr int kWOffEpi = kWStages * kWStage;
 constexpr int kWOffBar = kWOffEpi + 4 * 32 * kWEpiPitch;
@@ -39,11 +37,10 @@ constexpr int kWSmem = kWOffBar + 16 * 8 + 16 + 1024;
 static_assert(kWSmem <= 232448, "shared memory per CTA");
 
 struct WgradArgs {
-  const uint16_t* A;
+  const uint16_t* A;  // [rows, M] routed-row order
   int64_t lda;
-  const uint16_t* B;
+  const uint16_t* B;  // [rows, N] routed-row order
   int64_t ldb;
-  const int32_t* row_token;
   const int32_t* offsets;
   int E_loc, M, N;
   float* out0;
@@ -53,7 +50,8 @@ struct WgradArgs {
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmD,
+__global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                                const __grid_constant__ CUtensorMap tmB,
                                                                 const WgradArgs g) {
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -70,7 +68,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
-      ptx::mbar_init(full_bar(s), kWGather + 1);  // gather threads + the TMA thread
+      ptx::mbar_init(full_bar(s), kWGather + 1);  // copy threads + the TMA thread
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -203,14 +201,15 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
       }
     }
   } else if (warp == 13) {
-    // ------------------------------------------------------------------ TMA (direct operand)
+    // ------------------------------------------------------------------ TMA (full blocks)
     if (lane == 0) {
-      ptx::prefetch_tmap(&tmD);
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB);
       int s = 0;
       uint32_t ph = 0;
       int64_t issued = 0;
       bool ok = true;
-      constexpr int kDirectBytes = MODE == 0 ? kWA : kWB;
+      constexpr int kStageBytes = kWA + kWB;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const int e = t / per_e, rem = t - e * per_e;
         const int m0 = (rem / nt_n) * kWBM, n0 = (rem % nt_n) * kWBN;
@@ -222,16 +221,13 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
           const int r0 = r_begin + kb * kWBK;
           if (r0 + kWBK <= r_end) {
             const uint32_t a_addr = sbase + s * kWStage;
-            ptx::mbar_arrive_expect_tx(full_bar(s), kDirectBytes);
-            if (MODE == 0) {
-              for (int a = 0; a < kWBM / 64; ++a) ptx::tma_load_3d(a_addr + a * 8192, &tmD, full_bar(s), m0 + 64 * a, r0, 0);
-            } else {
-              for (int a = 0; a < kWBN / 64; ++a)
-                ptx::tma_load_3d(a_addr + kWA + a * 8192, &tmD, full_bar(s), n0 + 64 * a, r0, 0);
-            }
+            ptx::mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+            for (int a = 0; a < kWBM / 64; ++a) ptx::tma_load_3d(a_addr + a * 8192, &tmA, full_bar(s), m0 + 64 * a, r0, 0);
+            for (int a = 0; a < kWBN / 64; ++a)
+              ptx::tma_load_3d(a_addr + kWA + a * 8192, &tmB, full_bar(s), n0 + 64 * a, r0, 0);
             ++issued;
           } else {
-            ptx::mbar_arrive(full_bar(s));  // the gather warps load this partial block
+            ptx::mbar_arrive(full_bar(s));  // the copy warps load this partial block
           }
           if (++s == kWStages) { s = 0; ph ^= 1u; }
         }
@@ -242,7 +238,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
       (void)issued;
     }
   } else {
-    // ------------------------------------------------------------------ gather
+    // ------------------------------------------------------------------ partial blocks
     const int gt = threadIdx.x - 160;
     int s = 0;
     uint32_t ph = 0;
@@ -262,35 +258,32 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
           break;
         }
         (void)ptx::mbar_try_wait(empty_bar(s), ph ^ 1u);
-        const uint32_t a_addr = sbase + s * kWStage, b_addr = a_addr + kWA;
-        // thread -> K row kr = gt / 4 of the stage: 4 of its 16 A chunks (two 64-column
-        // atoms) and 8 of its 32 B chunks (four atoms); one row lookup per stage
-        const int kr = gt >> 2, sub = gt & 3;
-        const int r = r_begin + kb * kWBK + kr;
-        const bool rv = r < r_end;
-        const bool partial = r_begin + (kb + 1) * kWBK > r_end;  // else TMA loads the direct operand
-        const int64_t tok = rv ? __ldg(g.row_token + r) : 0;
-        const int64_t ra = MODE == 1 ? tok : r, rb = MODE == 0 ? tok : r;
-        const uint32_t swz = static_cast<uint32_t>(kr & 7);
+        if (r_begin + (kb + 1) * kWBK > r_end) {  // the segment's last, partial block
+          const uint32_t a_addr = sbase + s * kWStage, b_addr = a_addr + kWA;
+          // thread -> K row kr = gt / 4: 4 of its 16 A chunks (two 64-column atoms) and 8 of
+          // its 32 B chunks (four atoms), in the swizzled layout TMA would produce
+          const int kr = gt >> 2, sub = gt & 3;
+          const int64_t r = r_begin + kb * kWBK + kr;
+          const bool rv = r < r_end;
+          const uint32_t swz = static_cast<uint32_t>(kr & 7);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (MODE == 0 && !partial) break;
-          const int cc = sub + 4 * j, atom = cc >> 3, c = cc & 7;
-          const int m = m0 + atom * 64 + c * 8;
-          const bool v = rv && m < g.M;
-          ptx::cp_async_16(a_addr + atom * 8192 + kr * 128 + ((c ^ swz) << 4),
-                           v ? static_cast<const void*>(g.A + ra * g.lda + m) : g.A, v ? 16u : 0u);
-        }
+          for (int j = 0; j < 4; ++j) {
+            const int cc = sub + 4 * j, atom = cc >> 3, c = cc & 7;
+            const int m = m0 + atom * 64 + c * 8;
+            const bool v = rv && m < g.M;
+            ptx::cp_async_16(a_addr + atom * 8192 + kr * 128 + ((c ^ swz) << 4),
+                             v ? static_cast<const void*>(g.A + r * g.lda + m) : g.A, v ? 16u : 0u);
+          }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (MODE == 1 && !partial) break;
-          const int cc = sub + 4 * j, atom = cc >> 3, c = cc & 7;
-          const int n = n0 + atom * 64 + c * 8;
-          const bool v = rv && n < g.N;
-          ptx::cp_async_16(b_addr + atom * 8192 + kr * 128 + ((c ^ swz) << 4),
-                           v ? static_cast<const void*>(g.B + rb * g.ldb + n) : g.B, v ? 16u : 0u);
+          for (int j = 0; j < 8; ++j) {
+            const int cc = sub + 4 * j, atom = cc >> 3, c = cc & 7;
+            const int n = n0 + atom * 64 + c * 8;
+            const bool v = rv && n < g.N;
+            ptx::cp_async_16(b_addr + atom * 8192 + kr * 128 + ((c ^ swz) << 4),
+                             v ? static_cast<const void*>(g.B + r * g.ldb + n) : g.B, v ? 16u : 0u);
+          }
         }
-        ptx::cp_async_arrive_noinc(full_bar(s));
+        ptx::cp_async_arrive_noinc(full_bar(s));  // every stage: the barrier counts all copy threads
         if (++s == kWStages) { s = 0; ph ^= 1u; }
       }
     }
@@ -305,12 +298,11 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
   }
 }
 
-// D: the operand in routed-row order (MODE 0: h [n_rows, f]; MODE 1: dg/du [n_rows, 2f]),
-// cols values per row; its TMA map has 64 x 64 boxes.
 template <int MODE>
-static cudaError_t launch_wgrad_tc(const WgradArgs& g, const void* D, int cols, int64_t n_rows, cudaStream_t st) {
-  CUtensorMap tmD;
-  if (!make_operand_map(&tmD, D, false, static_cast<uint64_t>(cols), static_cast<uint64_t>(n_rows), 1, 64))
+static cudaError_t launch_wgrad_tc(const WgradArgs& g, int64_t n_rows, cudaStream_t st) {
+  CUtensorMap tmA, tmB;  // 64 x 64 boxes over [n_rows, M] and [n_rows, N]
+  if (!make_operand_map(&tmA, g.A, false, static_cast<uint64_t>(g.M), static_cast<uint64_t>(n_rows), 1, 64) ||
+      !make_operand_map(&tmB, g.B, false, static_cast<uint64_t>(g.N), static_cast<uint64_t>(n_rows), 1, 64))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -321,24 +313,26 @@ static cudaError_t launch_wgrad_tc(const WgradArgs& g, const void* D, int cols, 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  return launch_pdl(wgrad_tc_kernel<MODE>, dim3(static_cast<unsigned>(num_sms())), dim3(kWThreads), kWSmem, st, tmD,
-                    g);
+  return launch_pdl(wgrad_tc_kernel<MODE>, dim3(static_cast<unsigned>(num_sms())), dim3(kWThreads), kWSmem, st, tmA,
+                    tmB, g);
 }
 
-cudaError_t launch_wgrad_down_tc(const void* h, const void* dy, const int32_t* row_token, const int32_t* offsets,
-                                 int64_t n_rows, int E_loc, int d, int f, float* dWd, int32_t* err,
-                                 uint64_t timeout_ns, cudaStream_t st) {
-  WgradArgs g{static_cast<const uint16_t*>(h), f, static_cast<const uint16_t*>(dy), d, row_token, offsets,
+// dW_down [E_loc, f, d] from h [n_rows, f] and dy_rows [n_rows, d] (routed order).
+cudaError_t launch_wgrad_down_tc(const void* h, const void* dy_rows, const int32_t* offsets, int64_t n_rows,
+                                 int E_loc, int d, int f, float* dWd, int32_t* err, uint64_t timeout_ns,
+                                 cudaStream_t st) {
+  WgradArgs g{static_cast<const uint16_t*>(h), f, static_cast<const uint16_t*>(dy_rows), d, offsets,
               E_loc, f, d, dWd, nullptr, err, timeout_ns};
-  return launch_wgrad_tc<0>(g, h, f, n_rows, st);
+  return launch_wgrad_tc<0>(g, n_rows, st);
 }
 
-cudaError_t launch_wgrad_gate_up_tc(const void* x, const void* dgu, const int32_t* row_token,
-                                    const int32_t* offsets, int64_t n_rows, int E_loc, int d, int f, float* dWg,
-                                    float* dWu, int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
-  WgradArgs g{static_cast<const uint16_t*>(x), d, static_cast<const uint16_t*>(dgu), 2 * f, row_token, offsets,
+// dW_gate, dW_up [E_loc, d, f] from x_rows [n_rows, d] (routed order) and dg/du [n_rows, 2f].
+cudaError_t launch_wgrad_gate_up_tc(const void* x_rows, const void* dgu, const int32_t* offsets, int64_t n_rows,
+                                    int E_loc, int d, int f, float* dWg, float* dWu, int32_t* err,
+                                    uint64_t timeout_ns, cudaStream_t st) {
+  WgradArgs g{static_cast<const uint16_t*>(x_rows), d, static_cast<const uint16_t*>(dgu), 2 * f, offsets,
               E_loc, d, 2 * f, dWg, dWu, err, timeout_ns};
-  return launch_wgrad_tc<1>(g, dgu, 2 * f, n_rows, st);
+  return launch_wgrad_tc<1>(g, n_rows, st);
 }
 
 }  // namespace moe
