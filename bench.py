@@ -650,7 +650,7 @@ def run_backward(args, w):
         "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
                      "kernel": "whole backward (12 N d f FLOP)", "traffic": None, "peak_kind": pk_kind},
-        "N_pairs": N, "gpu_launches": 9 * args.steps, "clocks": clk,
+        "N_pairs": N, "gpu_launches": 11 * args.steps, "clocks": clk,
         "saved_preactivations": "from moe_layer_forward_train (no recompute)",
     }
     if rank == 0:

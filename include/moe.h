@@ -314,7 +314,7 @@ moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* d
  *                      (zero for experts that received no token)
  *   workspace          device >= moe_layer_backward_workspace_size(T, d, f, k, E_loc) bytes,
  *                      256-byte aligned, error word initialised (moe_workspace_init)
- * Requires d % 8 == 0, f % 32 == 0; 16-byte aligned x, dy, dx and weights.  bf16 only. */
+ * Requires d % 8 == 0, f % 32 == 0; 16-byte aligned x, dy, dx, weights and gradients.  bf16 only. */
 moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
                               int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
                               const void* W_down, const void* WguT_packed, const void* gu_saved, void* dx,

@@ -582,7 +582,8 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
   if (T > 0 && (!x || !dy || !topk_ids || !topk_probs || !dx || !dlogits)) return MOE_ERR_INVALID_ARG;
   if (gu_saved && !aligned16(gu_saved)) return MOE_ERR_INVALID_ARG;
   if ((T > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))) || !aligned16(Wgu_packed) ||
-      !aligned16(W_down) || !aligned16(WguT_packed))
+      !aligned16(W_down) || !aligned16(WguT_packed) || !aligned16(dW_gate) || !aligned16(dW_up) ||
+      !aligned16(dW_down))
     return MOE_ERR_INVALID_ARG;
   if (!workspace || !aligned256(workspace) || workspace_bytes < moe_layer_backward_workspace_size(T, d, f, k, E_loc))
     return MOE_ERR_WORKSPACE;

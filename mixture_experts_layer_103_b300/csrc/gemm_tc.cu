@@ -468,6 +468,26 @@ bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, ui
   return r == CUDA_SUCCESS;
 }
 
+bool make_store_map(CUtensorMap* m, void* base, int elt, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                    uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc || (elt != 2 && elt != 4)) return false;
+  const uint32_t box_bytes = box_cols * static_cast<uint32_t>(elt);
+  const CUtensorMapSwizzle sw = box_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : box_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                  : CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (sw == CU_TENSOR_MAP_SWIZZLE_NONE) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * static_cast<uint64_t>(elt)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, elt == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // A: the permuted rows [a_rows, K] (TMA), or unused (nullptr) in row-gather mode.
 template <bool MX, int EPI, bool GATHER = false>
 static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,

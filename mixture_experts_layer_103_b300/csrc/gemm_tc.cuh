@@ -272,6 +272,11 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl,
 // 3-D K-major operand map [outer, rows, K], box [1, box_rows, 128 bytes], 128-byte swizzle.
 bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, uint64_t rows, uint64_t outer,
                       uint32_t box_rows);
+// 2-D row-major output map [rows, cols] of elt-byte elements (2 = bf16, 4 = fp32) for TMA
+// stores of box_rows x box_cols boxes; box_cols * elt must be 32, 64 or 128 bytes and
+// selects the matching swizzle (a row's 16-byte chunk c sits at c ^ ((row >> s) & m)).
+bool make_store_map(CUtensorMap* m, void* base, int elt, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                    uint32_t box_rows);
 int num_sms();
 
 }  // namespace moe

@@ -10,8 +10,9 @@
 // the rows past the segment end (TMA cannot stop there) and the columns past M / N, and
 // counted on the stage's full barrier as it lands (cp.async.mbarrier.arrive).  One
 // thread issues tcgen05.mma (both operands MN-major) into a double-buffered TMEM
-// accumulator; four warps store the fp32 tiles.  Persistent: one CTA per SM, tiles
-// (expert, m-tile, n-tile) round-robin.  Experts without rows get zero tiles.
+// accumulator; four warps move the fp32 tiles out through shared memory, one TMA store per
+// 32 x 32 block (plain stores for blocks cut by the matrix edge).  Persistent: one CTA per
+// SM, tiles (expert, m-tile, n-tile) round-robin.  Experts without rows get zero tiles.
 //   MODE 0: dW_down_e [f, d] = h^T dy   (A = h, B = dy in routed order)
 //   MODE 1: dW_gate_e, dW_up_e [d, f] = x^T dg, x^T du (A = x in routed order, B = dg/du in
 //           the packed order, stored back to the gate and up matrices)
@@ -30,9 +31,9 @@ constexpr int kWB = kWBN * kWBK * 2;                   // 32 KB
 constexpr int kWStage = kWA + kWB;
 constexpr int kWGather = 256;                          // partial-block copy threads (8 warps)
 constexpr int kWThreads = 32 + 128 + kWGather + 32;    // MMA warp, 4 epilogue, 8 copy, TMA warp
-constexpr int kWEpiPitch = 144;                        // 128 data bytes + 16 pad per staged row
-constexpr int kWOffEpi = kWStages * kWStage;
-constexpr int kWOffBar = kWOffEpi + 4 * 32 * kWEpiPitch;
+constexpr int kWEpiBuf = 32 * 128;                     // one staged 32 x 32 fp32 block (128-byte swizzle)
+constexpr int kWOffEpi = kWStages * kWStage;           // 2 staging buffers per epilogue warp
+constexpr int kWOffBar = kWOffEpi + 4 * 2 * kWEpiBuf;
 constexpr int kWSmem = kWOffBar + 16 * 8 + 16 + 1024;
 static_assert(kWSmem <= 232448, "shared memory per CTA");
 
@@ -52,6 +53,8 @@ struct WgradArgs {
 template <int MODE>
 __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                 const __grid_constant__ CUtensorMap tmB,
+                                                                const __grid_constant__ CUtensorMap tmO0,
+                                                                const __grid_constant__ CUtensorMap tmO1,
                                                                 const WgradArgs g) {
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -135,9 +138,14 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
     }
   } else if (warp < 5) {
     // ------------------------------------------------------------------ epilogue
+    // Each 32-column block of the warp's 32 rows is written to a staging buffer (thread =
+    // row, 16-byte chunk c of row r at c ^ (r & 7): the 128-byte swizzle of the store map)
+    // and leaves by one TMA store; two buffers alternate, a buffer is rewritten once the
+    // store that read it is done reading.
     const int q = warp & 3;  // TMEM lane quarter
-    uint8_t* stage = smem + kWOffEpi + (warp - 1) * 32 * kWEpiPitch;
-    int it = 0;
+    uint8_t* stage = smem + kWOffEpi + (warp - 1) * 2 * kWEpiBuf;
+    const uint32_t stage_s = sbase + static_cast<uint32_t>(kWOffEpi + (warp - 1) * 2 * kWEpiBuf);
+    int it = 0, sb = 0, last_sb = -1;  // last_sb: buffer of the most recent TMA store
     const int ncols_out = MODE == 0 ? g.N : g.N / 2;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       if (*s_abort) break;
@@ -156,6 +164,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
         ptx::tc_fence_after();
       }
       const int rows_valid = max(0, min(32, g.M - (m0 + q * 32)));
+      const int row_g = e * g.M + m0 + q * 32;  // first output row of the warp's slab
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kWBN);
 #pragma unroll 1
       for (int c = 0; c < kWBN; c += 32) {
@@ -169,30 +178,43 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        // destination of this 32-column block: dW_down row, or the gate / up matrix
-        float* dst;
-        int col;
-        if (MODE == 0) {
-          dst = g.out0;
-          col = n;
-        } else {
-          dst = ((n / 32) % 2 == 0) ? g.out0 : g.out1;
-          col = (n / 64) * 32;
-        }
-        uint4* mine = reinterpret_cast<uint4*>(stage + lane * kWEpiPitch);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) mine[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        __syncwarp();
+        // destination of this 32-column block: dW_down, or the gate / up matrix
+        const bool to_up = MODE == 1 && ((n / 32) % 2 == 1);
+        const int col = MODE == 0 ? n : (n / 64) * 32;
         const int chunks_valid = max(0, min(8, (g.N - n) / 4));
-        uint8_t* g0 = reinterpret_cast<uint8_t*>(dst + (static_cast<int64_t>(e) * g.M + m0 + q * 32) * ncols_out + col);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {  // 4 rows x 128 bytes per store instruction
-          const int r = j * 4 + lane / 8, ch = lane % 8;
-          const uint4 val = *reinterpret_cast<const uint4*>(stage + r * kWEpiPitch + ch * 16);
-          if (r < rows_valid && ch < chunks_valid)
-            *reinterpret_cast<uint4*>(g0 + static_cast<int64_t>(r) * ncols_out * 4 + ch * 16) = val;
+        const bool whole = rows_valid == 32 && chunks_valid == 8;
+        if (lane == 0) {
+          if (last_sb == (sb ^ 1)) ptx::bulk_wait_read<1>();
+          else ptx::bulk_wait_read<0>();
         }
         __syncwarp();
+        uint8_t* buf = stage + sb * kWEpiBuf;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        if (whole) {
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(to_up ? &tmO1 : &tmO0, stage_s + sb * kWEpiBuf, col, row_g);
+            ptx::bulk_commit();
+          }
+          last_sb = sb;
+        } else {  // block cut by the matrix edge: plain stores of the valid part
+          __syncwarp();
+          float* dst = to_up ? g.out1 : g.out0;
+          uint8_t* g0 = reinterpret_cast<uint8_t*>(dst + static_cast<int64_t>(row_g) * ncols_out + col);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {  // 4 rows x 128 bytes per store instruction
+            const int r = j * 4 + lane / 8, ch = lane % 8;
+            const uint4 val = *reinterpret_cast<const uint4*>(buf + r * 128 + ((ch ^ (r & 7)) << 4));
+            if (r < rows_valid && ch < chunks_valid)
+              *reinterpret_cast<uint4*>(g0 + static_cast<int64_t>(r) * ncols_out * 4 + ch * 16) = val;
+          }
+          __syncwarp();
+        }
+        sb ^= 1;
       }
       if (nkb > 0) {
         ptx::tc_fence_before();
@@ -200,6 +222,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
         if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
       }
     }
+    if (lane == 0) ptx::bulk_wait_all();  // the stores have completed before the CTA exits
   } else if (warp == 13) {
     // ------------------------------------------------------------------ TMA (full blocks)
     if (lane == 0) {
@@ -300,9 +323,14 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_tc_kernel(const __grid_con
 
 template <int MODE>
 static cudaError_t launch_wgrad_tc(const WgradArgs& g, int64_t n_rows, cudaStream_t st) {
-  CUtensorMap tmA, tmB;  // 64 x 64 boxes over [n_rows, M] and [n_rows, N]
+  CUtensorMap tmA, tmB, tmO0, tmO1;  // 64 x 64 operand boxes over [n_rows, M] and [n_rows, N]
   if (!make_operand_map(&tmA, g.A, false, static_cast<uint64_t>(g.M), static_cast<uint64_t>(n_rows), 1, 64) ||
       !make_operand_map(&tmB, g.B, false, static_cast<uint64_t>(g.N), static_cast<uint64_t>(n_rows), 1, 64))
+    return cudaErrorInvalidValue;
+  // outputs [E_loc * M, N or N / 2] fp32, 32 x 32 store boxes
+  const uint64_t out_rows = static_cast<uint64_t>(g.E_loc) * g.M, out_cols = MODE == 0 ? g.N : g.N / 2;
+  if (!make_store_map(&tmO0, g.out0, 4, out_cols, out_rows, 32, 32) ||
+      !make_store_map(&tmO1, MODE == 0 ? g.out0 : g.out1, 4, out_cols, out_rows, 32, 32))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -314,7 +342,7 @@ static cudaError_t launch_wgrad_tc(const WgradArgs& g, int64_t n_rows, cudaStrea
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   return launch_pdl(wgrad_tc_kernel<MODE>, dim3(static_cast<unsigned>(num_sms())), dim3(kWThreads), kWSmem, st, tmA,
-                    tmB, g);
+                    tmB, tmO0, tmO1, g);
 }
 
 // dW_down [E_loc, f, d] from h [n_rows, f] and dy_rows [n_rows, d] (routed order).
