@@ -28,17 +28,17 @@ cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* o
                             int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
                             uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
-                                   const int32_t* offsets, const float* row_prob, int E_loc, int d, int f, bool mx,
-                                   const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
-                                   uint64_t timeout_ns, void* gu_save, cudaStream_t st);
+                                   const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc, int d,
+                                   int f, bool mx, const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf,
+                                   int32_t* err, uint64_t timeout_ns, void* gu_save, cudaStream_t st);
 cudaError_t launch_quant_rows_mx(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
                                  uint8_t* xq, uint8_t* x_sf, cudaStream_t st);
 cudaError_t launch_tc_gemm_gather_store(const void* x, const int32_t* row_src_token, const int32_t* offsets,
-                                        int E_loc, int K, int n_out, const void* B, void* out, int32_t* err,
-                                        uint64_t timeout_ns, cudaStream_t st);
+                                        int64_t N_cap, int E_loc, int K, int n_out, const void* B, void* out,
+                                        int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_tc_dswiglu(const void* dy, const int32_t* row_src_token, const int32_t* offsets,
-                              const float* row_prob, int E_loc, int d, int f, const void* W_down, const void* gu,
-                              void* dgu, void* h, float* dp_part, int32_t* err, uint64_t timeout_ns,
+                              const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* W_down,
+                              const void* gu, void* dgu, void* h, float* dp_part, int32_t* err, uint64_t timeout_ns,
                               cudaStream_t st);
 cudaError_t launch_tc_gemm_store(const void* A, int64_t a_rows, const int32_t* offsets, int E_loc, int K, int n_out,
                                  const void* B, void* out, int32_t* err, uint64_t timeout_ns, cudaStream_t st);
@@ -449,7 +449,7 @@ moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale,
   if (N_cap > 0 && (!row_src_token || !row_prob || (dtype == MOE_MXFP8 && !h_scale))) return MOE_ERR_INVALID_ARG;
   if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
   if (N_cap == 0) return MOE_OK;
-  return cuda_status(launch_tc_gemm1_gather(x, x_scale, row_src_token, offsets, row_prob, E_loc, d, f,
+  return cuda_status(launch_tc_gemm1_gather(x, x_scale, row_src_token, offsets, row_prob, N_cap, E_loc, d, f,
                                             dtype == MOE_MXFP8, Wgu_packed, Wgu_scale, h, h_scale,
                                             static_cast<int32_t*>(workspace), kTimeoutNs, nullptr, stream));
 }
@@ -524,8 +524,8 @@ static moe_status layer_forward_impl(const void* x, const float* logits, int T, 
       e = launch_quant_rows_mx(x, x_dtype, T, d, w.pair_to_row, k, static_cast<uint8_t*>(w.perm_x), w.perm_sf, stream);
     MlpScratch s = carve_mlp(w.mlp, n_cap, f, dtype);
     if (e == cudaSuccess && n_cap > 0)
-      e = launch_tc_gemm1_gather(mx ? w.perm_x : x, w.perm_sf, w.row_src_token, w.offsets, w.row_prob, E_loc, d, f,
-                                 mx, Wgu_packed, Wgu_scale, s.h, s.h_sf, w.err, kTimeoutNs, gu_save, stream);
+      e = launch_tc_gemm1_gather(mx ? w.perm_x : x, w.perm_sf, w.row_src_token, w.offsets, w.row_prob, n_cap, E_loc,
+                                 d, f, mx, Wgu_packed, Wgu_scale, s.h, s.h_sf, w.err, kTimeoutNs, gu_save, stream);
     if (e == cudaSuccess)
       e = run_gemm2(s.h, s.h_sf, w.offsets, n_cap, E_loc, d, f, dtype, Wd_packed, Wd_scale, w.Y2, w.err, hint, stream);
   } else {
@@ -596,10 +596,10 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
   else
     e = cudaMemsetAsync(w.offsets, 0, static_cast<size_t>(E_loc + 1) * 4, stream);
   if (e == cudaSuccess && n_cap > 0 && !gu_saved)  // recompute g, u unless the forward kept them
-    e = launch_tc_gemm_gather_store(x, w.row_src_token, w.offsets, E_loc, d, 2 * f, Wgu_packed, w.gu, w.err,
+    e = launch_tc_gemm_gather_store(x, w.row_src_token, w.offsets, n_cap, E_loc, d, 2 * f, Wgu_packed, w.gu, w.err,
                                     kTimeoutNs, stream);
   if (e == cudaSuccess && n_cap > 0)
-    e = launch_tc_dswiglu(dy, w.row_src_token, w.offsets, w.row_prob, E_loc, d, f, W_down,
+    e = launch_tc_dswiglu(dy, w.row_src_token, w.offsets, w.row_prob, n_cap, E_loc, d, f, W_down,
                           gu_saved ? gu_saved : w.gu, w.dgu, w.h, w.dp_part, w.err, kTimeoutNs, stream);
   if (e == cudaSuccess && n_cap > 0)
     e = launch_tc_gemm_store(w.dgu, n_cap, w.offsets, E_loc, 2 * f, d, WguT_packed, w.dxp, w.err, kTimeoutNs,

@@ -57,7 +57,10 @@ struct GemmSmem {
   static constexpr int OFF_PIPE = 0;
   static constexpr int OFF_SF = OFF_PIPE + PIPE_BYTES;
   static constexpr int OFF_EPI = OFF_SF + MAX_STAGES * SF_STAGE_BYTES;  // epilogue staging
-  static constexpr int OFF_BAR = OFF_EPI + kEpiBytes;
+  // bf16 outputs leave by TMA stores (two swizzled buffers per warp); MXFP8 kernels keep
+  // the padded staging of plain stores (their scale rings leave no room for more)
+  static constexpr int EPI_WARP_BYTES = MX ? kEpiWarpBytes : kEpiTmaWarpBytes;
+  static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_WARP_BYTES;
   static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;       // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TAB = OFF_MISC + 16;
@@ -191,7 +194,7 @@ struct BMaps {
 template <bool MX, int EPI, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATHER ? kGatherThreads : 0), 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BMaps tmB,
-                           const GemmArgs g) {
+                           const __grid_constant__ OutMaps tmO, const GemmArgs g) {
   using C = GemmSmem<MX>;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -344,6 +347,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATH
   } else if (warp < 6) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    EpiStage est{smem + C::OFF_EPI + (warp - 2) * C::EPI_WARP_BYTES,
+                 sbase + static_cast<uint32_t>(C::OFF_EPI + (warp - 2) * C::EPI_WARP_BYTES), 0, -1};
     int it = 0;
     for (int u = cluster; u < units; u += clusters, ++it) {
       if (*s_abort) break;
@@ -358,11 +363,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATH
       (void)ptx::mbar_try_wait(tfull_bar(acc), acc_ph);  // completed phase: acquire for every lane
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if (ut.valid) epilogue_warp<EPI>(g, tl, tbase, BN, q, lane, smem + C::OFF_EPI + (warp - 2) * kEpiWarpBytes);
+      // TMA stores for the bf16 outputs except the ScaledSwiGLU backward's three per block,
+      // which measured faster with plain stores (two staging buffers serialise them)
+      if (ut.valid) epilogue_warp<EPI, !MX && EPI != EPI_DSWIGLU>(g, tmO, tl, tbase, BN, q, lane, est);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
     }
+    if (lane == 0) ptx::bulk_wait_all();  // this warp's TMA stores have completed
   } else if constexpr (GATHER) {
     // ------------------------------------------------------------------ A gather
     // Thread gt copies 16-byte chunk (gt % 8) of the rows gt / 8 + 16 i (i < 8) of each
@@ -488,6 +496,13 @@ bool make_store_map(CUtensorMap* m, void* base, int elt, uint64_t cols, uint64_t
   return r == CUDA_SUCCESS;
 }
 
+bool make_out_maps(OutMaps* m, const GemmArgs& g) {
+  const uint64_t rows = static_cast<uint64_t>(std::max<int64_t>(g.out_rows, 1));
+  if (g.out && !make_store_map(&m->out, g.out, 2, static_cast<uint64_t>(g.ld_out), rows, 32, 32)) return false;
+  if (g.out2 && !make_store_map(&m->out2, g.out2, 2, static_cast<uint64_t>(g.n_out), rows, 32, 32)) return false;
+  return true;
+}
+
 // A: the permuted rows [a_rows, K] (TMA), or unused (nullptr) in row-gather mode.
 template <bool MX, int EPI, bool GATHER = false>
 static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
@@ -501,6 +516,9 @@ static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B
   if (!make_operand_map(&tb.b128, B, MX, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b64, B, MX, g.K, g.n_out, g.E_loc, 64)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b32, B, MX, g.K, g.n_out, g.E_loc, 32)) return cudaErrorInvalidValue;
+  OutMaps tmo;
+  memset(&tmo, 0, sizeof(tmo));
+  if (!MX && !make_out_maps(&tmo, g)) return cudaErrorInvalidValue;
   auto kern = tc_grouped_gemm_kernel<MX, EPI, GATHER>;
   // Once per device: opt in to > 48 KB of dynamic shared memory and size the grid to the
   // clusters of two that can be resident at once (keeps later launches, including ones
@@ -525,7 +543,7 @@ static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B
     grid = 2 * std::min(clusters, num_sms() / 2);
     if (dev >= 0 && dev < 64) grid_of[dev] = grid;
   }
-  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(threads), C::SMEM_BYTES, st, ta, tb, g);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(threads), C::SMEM_BYTES, st, ta, tb, tmo, g);
 }
 
 static GemmArgs base_args(const int32_t* offsets, int E_loc, int32_t* err, uint64_t timeout_ns) {
@@ -554,6 +572,7 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
   g.K = d;
   g.out = h;
   g.ld_out = f;
+  g.out_rows = N_cap;
   g.out_sf = h_sf;
   g.row_prob = row_prob;
   g.a_sf = perm_sf;
@@ -567,15 +586,16 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
 // expert-ordered operand is x row row_src_token[r] (bf16 [T, d]; MXFP8: E4M3 [T, d] with
 // E8M0 scales x_sf [T, d / 32]), so no permuted copy of x is ever written.
 cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
-                                   const int32_t* offsets, const float* row_prob, int E_loc, int d, int f, bool mx,
-                                   const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
-                                   uint64_t timeout_ns, void* gu_save, cudaStream_t st) {
+                                   const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc, int d,
+                                   int f, bool mx, const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf,
+                                   int32_t* err, uint64_t timeout_ns, void* gu_save, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
   g.out2 = mx ? nullptr : gu_save;
   g.n_out = 2 * f;
   g.K = d;
   g.out = h;
   g.ld_out = f;
+  g.out_rows = N_cap;
   g.out_sf = h_sf;
   g.row_prob = row_prob;
   g.b_sf = Wgu_sf;
@@ -591,13 +611,14 @@ cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int
 // Backward, bf16.  Pre-activations g/u [N_cap, 2f] (packed column order) recomputed
 // from the token rows: the row-gather GEMM1 with a plain bf16 store epilogue.
 cudaError_t launch_tc_gemm_gather_store(const void* x, const int32_t* row_src_token, const int32_t* offsets,
-                                        int E_loc, int K, int n_out, const void* B, void* out, int32_t* err,
-                                        uint64_t timeout_ns, cudaStream_t st) {
+                                        int64_t N_cap, int E_loc, int K, int n_out, const void* B, void* out,
+                                        int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
   g.n_out = n_out;
   g.K = K;
   g.out = out;
   g.ld_out = n_out;
+  g.out_rows = N_cap;
   g.gx = static_cast<const uint8_t*>(x);
   g.gx_ld = static_cast<int64_t>(K) * 2;
   g.row_token = row_src_token;
@@ -608,14 +629,15 @@ cudaError_t launch_tc_gemm_gather_store(const void* x, const int32_t* row_src_to
 // row_src_token; B = W_down in the user layout [E_loc, f, d], K-major over d) with the
 // ScaledSwiGLU backward fused into the epilogue (dg/du, h and partial dp).
 cudaError_t launch_tc_dswiglu(const void* dy, const int32_t* row_src_token, const int32_t* offsets,
-                              const float* row_prob, int E_loc, int d, int f, const void* W_down, const void* gu,
-                              void* dgu, void* h, float* dp_part, int32_t* err, uint64_t timeout_ns,
+                              const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* W_down,
+                              const void* gu, void* dgu, void* h, float* dp_part, int32_t* err, uint64_t timeout_ns,
                               cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
   g.n_out = f;
   g.K = d;
   g.out = dgu;
   g.ld_out = 2 * f;
+  g.out_rows = N_cap;
   g.out2 = h;
   g.dp_part = dp_part;
   g.aux = static_cast<const uint16_t*>(gu);
@@ -635,6 +657,7 @@ cudaError_t launch_tc_gemm_store(const void* A, int64_t a_rows, const int32_t* o
   g.K = K;
   g.out = out;
   g.ld_out = n_out;
+  g.out_rows = a_rows;
   return launch_gemm_inst<false, EPI_STORE_BF16>(A, a_rows, B, g, st);
 }
 
@@ -647,6 +670,7 @@ cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* o
   g.K = f;
   g.out = Y2;
   g.ld_out = d;
+  g.out_rows = N_cap;
   g.a_sf = h_sf;
   g.b_sf = Wd_sf;
   if (mx) return launch_gemm_inst<true, EPI_STORE_BF16>(h, N_cap, Wd, g, st);

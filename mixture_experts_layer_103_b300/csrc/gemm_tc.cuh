@@ -48,6 +48,13 @@ struct GemmArgs {
   const uint16_t* aux;
   void* out2;
   float* dp_part;
+  int64_t out_rows;        // rows of out / out2 (the extent of their TMA store maps)
+};
+
+// TMA store maps of the bf16 outputs: 32 x 32 boxes over out [out_rows, ld_out] and out2
+// [out_rows, n_out] (64-byte swizzle); unused ones are left zero.
+struct OutMaps {
+  CUtensorMap out, out2;
 };
 
 struct Tile {
@@ -109,14 +116,75 @@ __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint4 (&v)
   __syncwarp();
 }
 
+// TMA-store staging of the bf16 epilogues: each epilogue warp owns two 2 KB buffers, each
+// one 32-row x 64-byte block in the 64-byte swizzle of the store maps (16-byte chunk c of
+// row r at c ^ ((r >> 1) & 3)).  The two alternate; a buffer is refilled once the TMA store
+// that read it has finished reading.
+constexpr int kEpiTmaBuf = 32 * 64;
+constexpr int kEpiTmaWarpBytes = 2 * kEpiTmaBuf;
+constexpr int kEpiTmaBytes = 4 * kEpiTmaWarpBytes;
+static_assert(kEpiTmaWarpBytes >= kEpiWarpBytes, "a TMA staging area also serves the padded staging");
+
+struct EpiStage {
+  uint8_t* buf;    // this warp's staging (generic address)
+  uint32_t buf_s;  // the same in the shared window
+  int next, last;  // buffer to fill next; buffer of the most recent TMA store (-1: none)
+};
+
+// One 32 x 32 bf16 block of the warp's rows (v = this lane's row, 4 x 16 bytes).  TMA: a
+// whole block (32 valid rows, 4 valid chunks) leaves by one TMA store at (col, row) of
+// `map`; a block cut by a segment or matrix edge is written from the staging buffer with
+// plain stores (g0 = global address of the warp's first row at the block's first column,
+// ld = bytes between rows).  Without TMA the padded staging of warp_store_rows is used
+// (st.buf then holds at least kEpiWarpBytes).
+template <bool TMA>
+__device__ __forceinline__ void warp_store_block(EpiStage& st, const uint4 (&v)[4], int lane, const CUtensorMap* map,
+                                                 int col, int64_t row, uint8_t* g0, int64_t ld, int rows_valid,
+                                                 int chunks_valid) {
+  if constexpr (!TMA) {
+    (void)map; (void)col; (void)row;
+    warp_store_rows<4>(st.buf, v, lane, g0, ld, rows_valid, chunks_valid);
+  } else {
+    const int b = st.next;
+    if (lane == 0) {
+      if (st.last == (b ^ 1)) ptx::bulk_wait_read<1>();
+      else ptx::bulk_wait_read<0>();
+    }
+    __syncwarp();
+    uint8_t* buf = st.buf + b * kEpiTmaBuf;
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ sw) << 4)) = v[c];
+    if (rows_valid == 32 && chunks_valid == 4) {
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(map, st.buf_s + b * kEpiTmaBuf, col, static_cast<int>(row));
+        ptx::bulk_commit();
+      }
+      st.last = b;
+    } else {
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // 8 rows x 64 bytes per store instruction
+        const int r = j * 8 + lane / 4, c = lane % 4;
+        const uint4 val = *reinterpret_cast<const uint4*>(buf + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+        if (r < rows_valid && c < chunks_valid) *reinterpret_cast<uint4*>(g0 + r * ld + c * 16) = val;
+      }
+      __syncwarp();
+    }
+    st.next = b ^ 1;
+  }
+}
+
 // Epilogue of one 32-row slab of an accumulator tile (one warp, one TMEM lane per thread):
 // bf16 store of BN columns (GEMM2), or the fused scaled SwiGLU on BN/64 blocks of 32 gate
 // + 32 up columns with bf16 or MXFP8 (one 32-value block per thread) output (GEMM1).
 // tbase = TMEM address of this warp's lane quarter and accumulator; q = lane quarter;
 // tl.row0/tl.rows describe the 128-row tile the slab belongs to.
-template <int EPI>
-__device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl, uint32_t tbase, int BN, int q,
-                                              int lane, uint8_t* stage) {
+template <int EPI, bool TMA>
+__device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const OutMaps& om, const Tile& tl, uint32_t tbase,
+                                              int BN, int q, int lane, EpiStage& st) {
   const int r = q * 32 + lane;                         // row within the tile
   const int rows_valid = max(0, min(32, tl.rows - q * 32));
   const int64_t row_first = static_cast<int64_t>(tl.row0) + q * 32;
@@ -137,7 +205,8 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl,
                            pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
                            pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
       const int chunks = max(0, min(4, (g.n_out - n) / 8));
-      warp_store_rows<4>(stage, pk, lane, out + row_first * ld + static_cast<int64_t>(n) * 2, ld, rows_valid, chunks);
+      warp_store_block<TMA>(st, pk, lane, &om.out, n, row_first, out + row_first * ld + static_cast<int64_t>(n) * 2, ld,
+                            rows_valid, chunks);
     }
   } else if constexpr (EPI == EPI_DSWIGLU) {
     // ScaledSwiGLU backward for h = p * silu(g) * u, from dh and the saved g, u:
@@ -188,19 +257,20 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl,
       for (int j = 0; j < 4; ++j)
         pk[j] = make_uint4(pack_bf16x2(dg[8 * j + 0], dg[8 * j + 1]), pack_bf16x2(dg[8 * j + 2], dg[8 * j + 3]),
                            pack_bf16x2(dg[8 * j + 4], dg[8 * j + 5]), pack_bf16x2(dg[8 * j + 6], dg[8 * j + 7]));
-      warp_store_rows<4>(stage, pk, lane, gbase, ld2, rows_valid, 4);
+      warp_store_block<TMA>(st, pk, lane, &om.out, 2 * fc, row_first, gbase, ld2, rows_valid, 4);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         pk[j] = make_uint4(pack_bf16x2(du[8 * j + 0], du[8 * j + 1]), pack_bf16x2(du[8 * j + 2], du[8 * j + 3]),
                            pack_bf16x2(du[8 * j + 4], du[8 * j + 5]), pack_bf16x2(du[8 * j + 6], du[8 * j + 7]));
-      warp_store_rows<4>(stage, pk, lane, gbase + 64, ld2, rows_valid, 4);
+      warp_store_block<TMA>(st, pk, lane, &om.out, 2 * fc + 32, row_first, gbase + 64, ld2, rows_valid, 4);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         pk[j] = make_uint4(pack_bf16x2(hh[8 * j + 0], hh[8 * j + 1]), pack_bf16x2(hh[8 * j + 2], hh[8 * j + 3]),
                            pack_bf16x2(hh[8 * j + 4], hh[8 * j + 5]), pack_bf16x2(hh[8 * j + 6], hh[8 * j + 7]));
       const int64_t ldh = static_cast<int64_t>(fdim) * 2;
-      warp_store_rows<4>(stage, pk, lane, static_cast<uint8_t*>(g.out2) + row_first * ldh + static_cast<int64_t>(fc) * 2,
-                         ldh, rows_valid, 4);
+      warp_store_block<TMA>(st, pk, lane, &om.out2, fc, row_first,
+                            static_cast<uint8_t*>(g.out2) + row_first * ldh + static_cast<int64_t>(fc) * 2, ldh,
+                            rows_valid, 4);
       if (r < tl.rows) g.dp_part[row * (fdim / 32) + fc / 32] = dp;
     }
   } else {
@@ -228,9 +298,10 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl,
           pk[j] = make_uint4(pack_bf16x2(h[8 * j + 0], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
                              pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
         const int64_t ld = g.ld_out * 2;
-        warp_store_rows<4>(stage, pk, lane,
-                           static_cast<uint8_t*>(g.out) + row_first * ld + static_cast<int64_t>(fc) * 2, ld,
-                           rows_valid, fc < fdim ? 4 : 0);
+        if (fc < fdim)
+          warp_store_block<TMA>(st, pk, lane, &om.out, fc, row_first,
+                                static_cast<uint8_t*>(g.out) + row_first * ld + static_cast<int64_t>(fc) * 2, ld,
+                                rows_valid, 4);
         if (g.out2 && fc < fdim) {  // training forward: keep g and u (bf16, packed order) for the backward
           const int64_t ld2 = static_cast<int64_t>(g.n_out) * 2;
           uint8_t* gbase = static_cast<uint8_t*>(g.out2) + row_first * ld2 + static_cast<int64_t>(2 * fc) * 2;
@@ -240,14 +311,14 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl,
                                pack_bf16x2(__uint_as_float(gv[8 * j + 2]), __uint_as_float(gv[8 * j + 3])),
                                pack_bf16x2(__uint_as_float(gv[8 * j + 4]), __uint_as_float(gv[8 * j + 5])),
                                pack_bf16x2(__uint_as_float(gv[8 * j + 6]), __uint_as_float(gv[8 * j + 7])));
-          warp_store_rows<4>(stage, pk, lane, gbase, ld2, rows_valid, 4);
+          warp_store_block<TMA>(st, pk, lane, &om.out2, 2 * fc, row_first, gbase, ld2, rows_valid, 4);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             pk[j] = make_uint4(pack_bf16x2(__uint_as_float(uv[8 * j + 0]), __uint_as_float(uv[8 * j + 1])),
                                pack_bf16x2(__uint_as_float(uv[8 * j + 2]), __uint_as_float(uv[8 * j + 3])),
                                pack_bf16x2(__uint_as_float(uv[8 * j + 4]), __uint_as_float(uv[8 * j + 5])),
                                pack_bf16x2(__uint_as_float(uv[8 * j + 6]), __uint_as_float(uv[8 * j + 7])));
-          warp_store_rows<4>(stage, pk, lane, gbase + 64, ld2, rows_valid, 4);
+          warp_store_block<TMA>(st, pk, lane, &om.out2, 2 * fc + 32, row_first, gbase + 64, ld2, rows_valid, 4);
         }
       } else {
         float amax = 0.0f;
@@ -261,7 +332,7 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const Tile& tl,
           w[j] = static_cast<uint32_t>(e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv)) |
                  (static_cast<uint32_t>(e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv)) << 16);
         const uint4 pk[2] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7])};
-        warp_store_rows<2>(stage, pk, lane, static_cast<uint8_t*>(g.out) + row_first * g.ld_out + fc, g.ld_out,
+        warp_store_rows<2>(st.buf, pk, lane, static_cast<uint8_t*>(g.out) + row_first * g.ld_out + fc, g.ld_out,
                            rows_valid, fc < fdim ? 2 : 0);
         if (r < tl.rows && fc < fdim) g.out_sf[sf_act_offset(tl.mt, r, fc, fdim)] = static_cast<uint8_t>(X + 127);
       }
@@ -278,5 +349,7 @@ bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, ui
 bool make_store_map(CUtensorMap* m, void* base, int elt, uint64_t cols, uint64_t rows, uint32_t box_cols,
                     uint32_t box_rows);
 int num_sms();
+// Store maps of g.out (bf16 [out_rows, ld_out]) and g.out2 (bf16 [out_rows, n_out]) where set.
+bool make_out_maps(OutMaps* m, const GemmArgs& g);
 
 }  // namespace moe

@@ -27,8 +27,8 @@ struct PairSmem {
   static constexpr int B_BYTES = 128 * kRowBytes;  // this CTA's half of the 256 B rows
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BK = 64;                    // bf16 K elements per stage
-  static constexpr int OFF_EPI = STAGES * STAGE_BYTES;  // epilogue staging
-  static constexpr int OFF_BAR = OFF_EPI + kEpiBytes;
+  static constexpr int OFF_EPI = STAGES * STAGE_BYTES;  // epilogue staging (TMA stores)
+  static constexpr int OFF_BAR = OFF_EPI + kEpiTmaBytes;
   static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TAB = OFF_MISC + 16;
@@ -41,7 +41,7 @@ constexpr int kPairBN = 256;  // columns of a pair tile
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tc_grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                                const GemmArgs g) {
+                                const __grid_constant__ OutMaps tmO, const GemmArgs g) {
   using C = PairSmem;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -157,6 +157,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
+    EpiStage est{smem + C::OFF_EPI + (warp - 2) * kEpiTmaWarpBytes,
+                 sbase + static_cast<uint32_t>(C::OFF_EPI + (warp - 2) * kEpiTmaWarpBytes), 0, -1};
     int it = 0;
     for (int t = pair; t < total; t += npairs, ++it) {
       if (*s_abort) break;
@@ -172,11 +174,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       (void)ptx::mbar_try_wait(tfull_bar(acc), acc_ph);  // completed phase: acquire for every lane
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kPairBN);
-      epilogue_warp<EPI>(g, tl, tbase, kPairBN, q, lane, smem + C::OFF_EPI + (warp - 2) * kEpiWarpBytes);
+      epilogue_warp<EPI, true>(g, tmO, tl, tbase, kPairBN, q, lane, est);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
     }
+    if (lane == 0) ptx::bulk_wait_all();  // this warp's TMA stores have completed
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -192,6 +195,9 @@ static cudaError_t launch_pair_inst(const void* A, int64_t a_rows, const void* B
   CUtensorMap ta, tb;
   if (!make_operand_map(&ta, A, false, g.K, a_rows, 1, 128)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb, B, false, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
+  OutMaps tmo;
+  memset(&tmo, 0, sizeof(tmo));
+  if (!make_out_maps(&tmo, g)) return cudaErrorInvalidValue;
   auto kern = tc_grouped_gemm_pair_kernel<EPI>;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -203,7 +209,7 @@ static cudaError_t launch_pair_inst(const void* A, int64_t a_rows, const void* B
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int grid = num_sms() & ~1;  // whole pairs
-  return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), PairSmem::SMEM_BYTES, st, ta, tb, g);
+  return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), PairSmem::SMEM_BYTES, st, ta, tb, tmo, g);
 }
 
 cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu,
