@@ -294,7 +294,7 @@ moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* d
  * backward whose ScaledSwiGLU part also yields the gradient of the routing scales].
  * Gradients of L = sum_t dy_t . y_t for the layer of moe_layer_forward (same x, routing and
  * weights).  Per routed row (token t, local expert e, probability p), with s = sigmoid(g):
- *   g, u = x W_gate_e, x W_up_e (recomputed);  h = p silu(g) u;  dh = W_down_e dy_t
+ *   g, u = x W_gate_e, x W_up_e (saved or recomputed);  h = p silu(g) u;  dh = W_down_e dy_t
  *   du = p dh silu(g);  dg = p dh u s (1 + g (1 - s));  dp = sum_n dh_n silu(g_n) u_n
  *   dx_t = sum over the token's local slots of W_gate_e dg + W_up_e du
  *   dW_down_e = sum_rows h^T dy_t;  dW_gate_e = sum_rows x_t^T dg;  dW_up_e = sum_rows x_t^T du

@@ -33,13 +33,9 @@ cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int
                                    int32_t* err, uint64_t timeout_ns, void* gu_save, cudaStream_t st);
 cudaError_t launch_quant_rows_mx(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
                                  uint8_t* xq, uint8_t* x_sf, cudaStream_t st);
-cudaError_t launch_tc_gemm_gather_store(const void* x, const int32_t* row_src_token, const int32_t* offsets,
-                                        int64_t N_cap, int E_loc, int K, int n_out, const void* B, void* out,
-                                        int32_t* err, uint64_t timeout_ns, cudaStream_t st);
-cudaError_t launch_tc_dswiglu(const void* dy, const int32_t* row_src_token, const int32_t* offsets,
-                              const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* W_down,
-                              const void* gu, void* dgu, void* h, float* dp_part, int32_t* err, uint64_t timeout_ns,
-                              cudaStream_t st);
+cudaError_t launch_tc_dswiglu(const void* dy_rows, const int32_t* offsets, const float* row_prob, int64_t N_cap,
+                              int E_loc, int d, int f, const void* W_down, const void* gu, void* dgu, void* h,
+                              float* dp_part, int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_tc_gemm_store(const void* A, int64_t a_rows, const int32_t* offsets, int E_loc, int K, int n_out,
                                  const void* B, void* out, int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack_gu_t(const void* Wg, const void* Wu, moe_dtype src, int E_loc, int d, int f, void* WguT,
@@ -243,8 +239,8 @@ struct BackwardWs {
   void* h;         // [N_cap, f] bf16
   float* dp_part;  // [N_cap, f / 32]
   void* dxp;       // [N_cap, d] bf16
-  void* x_rows;    // [N_cap, d] bf16: x and dy in routed-row order, the weight-gradient
-  void* dy_rows;   //   operands (TMA-loadable, unlike token-indexed rows)
+  void* x_rows;    // [N_cap, d] bf16: x and dy in routed-row order, the GEMM operands
+  void* dy_rows;   //   (TMA-loadable, unlike token-indexed rows)
   size_t total;
 };
 static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int E_loc) {
@@ -595,22 +591,23 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
                        w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
   else
     e = cudaMemsetAsync(w.offsets, 0, static_cast<size_t>(E_loc + 1) * 4, stream);
+  // dy and x rows in routed order: the A operands of the recompute and dh GEMMs and of
+  // the weight gradients, all loaded by TMA
+  if (e == cudaSuccess)
+    e = launch_gather_rows(dy, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.dy_rows, stream);
+  if (e == cudaSuccess)
+    e = launch_gather_rows(x, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.x_rows, stream);
   if (e == cudaSuccess && n_cap > 0 && !gu_saved)  // recompute g, u unless the forward kept them
-    e = launch_tc_gemm_gather_store(x, w.row_src_token, w.offsets, n_cap, E_loc, d, 2 * f, Wgu_packed, w.gu, w.err,
-                                    kTimeoutNs, stream);
+    e = launch_tc_gemm_store(w.x_rows, n_cap, w.offsets, E_loc, d, 2 * f, Wgu_packed, w.gu, w.err, kTimeoutNs, stream);
   if (e == cudaSuccess && n_cap > 0)
-    e = launch_tc_dswiglu(dy, w.row_src_token, w.offsets, w.row_prob, n_cap, E_loc, d, f, W_down,
-                          gu_saved ? gu_saved : w.gu, w.dgu, w.h, w.dp_part, w.err, kTimeoutNs, stream);
+    e = launch_tc_dswiglu(w.dy_rows, w.offsets, w.row_prob, n_cap, E_loc, d, f, W_down, gu_saved ? gu_saved : w.gu,
+                          w.dgu, w.h, w.dp_part, w.err, kTimeoutNs, stream);
   if (e == cudaSuccess && n_cap > 0)
     e = launch_tc_gemm_store(w.dgu, n_cap, w.offsets, E_loc, 2 * f, d, WguT_packed, w.dxp, w.err, kTimeoutNs,
                              stream);
   if (e == cudaSuccess) e = launch_combine(w.dxp, w.pair_to_row, T, k, d, MOE_BF16, dx, stream);
   if (e == cudaSuccess)
     e = launch_dlogits(topk_ids, topk_probs, w.pair_to_row, w.dp_part, f / 32, T, E, k, dlogits, stream);
-  if (e == cudaSuccess)
-    e = launch_gather_rows(dy, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.dy_rows, stream);
-  if (e == cudaSuccess)
-    e = launch_gather_rows(x, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.x_rows, stream);
   if (e == cudaSuccess)
     e = launch_wgrad_down_tc(w.h, w.dy_rows, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_down, w.err,
                              kTimeoutNs, stream);

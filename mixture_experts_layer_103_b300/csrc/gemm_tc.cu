@@ -608,30 +608,12 @@ cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int
   return launch_gemm_inst<false, EPI_SWIGLU_BF16, true>(nullptr, 0, Wgu, g, st);
 }
 
-// Backward, bf16.  Pre-activations g/u [N_cap, 2f] (packed column order) recomputed
-// from the token rows: the row-gather GEMM1 with a plain bf16 store epilogue.
-cudaError_t launch_tc_gemm_gather_store(const void* x, const int32_t* row_src_token, const int32_t* offsets,
-                                        int64_t N_cap, int E_loc, int K, int n_out, const void* B, void* out,
-                                        int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
-  GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
-  g.n_out = n_out;
-  g.K = K;
-  g.out = out;
-  g.ld_out = n_out;
-  g.out_rows = N_cap;
-  g.gx = static_cast<const uint8_t*>(x);
-  g.gx_ld = static_cast<int64_t>(K) * 2;
-  g.row_token = row_src_token;
-  return launch_gemm_inst<false, EPI_STORE_BF16, true>(nullptr, 0, B, g, st);
-}
-
-// Backward, bf16: dh = dy_row W_down^T for every routed row (dy gathered through
-// row_src_token; B = W_down in the user layout [E_loc, f, d], K-major over d) with the
-// ScaledSwiGLU backward fused into the epilogue (dg/du, h and partial dp).
-cudaError_t launch_tc_dswiglu(const void* dy, const int32_t* row_src_token, const int32_t* offsets,
-                              const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* W_down,
-                              const void* gu, void* dgu, void* h, float* dp_part, int32_t* err, uint64_t timeout_ns,
-                              cudaStream_t st) {
+// Backward, bf16: dh = dy_row W_down^T for every routed row (dy_rows = dy in routed-row
+// order [N_cap, d], loaded by TMA; B = W_down in the user layout [E_loc, f, d], K-major
+// over d) with the ScaledSwiGLU backward fused into the epilogue (dg/du, h and partial dp).
+cudaError_t launch_tc_dswiglu(const void* dy_rows, const int32_t* offsets, const float* row_prob, int64_t N_cap,
+                              int E_loc, int d, int f, const void* W_down, const void* gu, void* dgu, void* h,
+                              float* dp_part, int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
   g.n_out = f;
   g.K = d;
@@ -642,10 +624,7 @@ cudaError_t launch_tc_dswiglu(const void* dy, const int32_t* row_src_token, cons
   g.dp_part = dp_part;
   g.aux = static_cast<const uint16_t*>(gu);
   g.row_prob = row_prob;
-  g.gx = static_cast<const uint8_t*>(dy);
-  g.gx_ld = static_cast<int64_t>(d) * 2;
-  g.row_token = row_src_token;
-  return launch_gemm_inst<false, EPI_DSWIGLU, true>(nullptr, 0, W_down, g, st);
+  return launch_gemm_inst<false, EPI_DSWIGLU>(dy_rows, N_cap, W_down, g, st);
 }
 
 // Backward, bf16: dx rows = dg/du [N_cap, 2f] (packed order) times the transposed gate/up

@@ -212,66 +212,70 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const OutMaps& 
     // ScaledSwiGLU backward for h = p * silu(g) * u, from dh and the saved g, u:
     //   du = p dh silu(g),  dg = p dh u s (1 + g (1 - s)) with s = sigmoid(g),
     //   dp = sum over the row of dh silu(g) u (partial sums per 32 columns)
+    // Eight columns at a time, packed to bf16 at once (the kernel's register budget is
+    // 168 per thread); the next block's g/u loads are in flight during this block's stores.
     const float p = r < tl.rows ? __ldg(g.row_prob + row_first + lane) : 0.0f;
     const int fdim = g.n_out;
     const int64_t row = row_first + lane;
+    const int64_t ld2 = static_cast<int64_t>(2 * fdim) * 2, ldh = static_cast<int64_t>(fdim) * 2;
+    const bool live = r < tl.rows;
+    auto load_gu = [&](int fc, uint4 (&a)[4], uint4 (&b)[4]) {  // 32 gate + 32 up values of block fc
+      if (live && fc < fdim) {
+        const uint4* src = reinterpret_cast<const uint4*>(g.aux + row * 2 * fdim + 2 * fc);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { a[j] = __ldg(src + j); b[j] = __ldg(src + 4 + j); }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[j] = b[j] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    uint4 ga[4], ub[4];
+    load_gu(tl.n0, ga, ub);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
+      const int fc = tl.n0 + c;  // first f column of this block (a multiple of 32)
+      if (fc >= fdim) break;
       uint32_t v[32];
       ptx::tmem_ld32(tbase + c, v);
       ptx::tmem_ld_wait();
-      const int fc = tl.n0 + c;  // first f column of this block (a multiple of 32)
-      if (fc >= fdim) break;
-      float gg[32], uu[32];
-      if (r < tl.rows) {
-        const uint4* src = reinterpret_cast<const uint4*>(g.aux + row * 2 * fdim + 2 * fc);  // 64 packed columns
+      uint4 pdg[4], pdu[4], ph[4];
+      float dp = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 a = __ldg(src + j), b = __ldg(src + 4 + j);
-          gg[8 * j + 0] = bf16_lo(a.x); gg[8 * j + 1] = bf16_hi(a.x); gg[8 * j + 2] = bf16_lo(a.y);
-          gg[8 * j + 3] = bf16_hi(a.y); gg[8 * j + 4] = bf16_lo(a.z); gg[8 * j + 5] = bf16_hi(a.z);
-          gg[8 * j + 6] = bf16_lo(a.w); gg[8 * j + 7] = bf16_hi(a.w);
-          uu[8 * j + 0] = bf16_lo(b.x); uu[8 * j + 1] = bf16_hi(b.x); uu[8 * j + 2] = bf16_lo(b.y);
-          uu[8 * j + 3] = bf16_hi(b.y); uu[8 * j + 4] = bf16_lo(b.z); uu[8 * j + 5] = bf16_hi(b.z);
-          uu[8 * j + 6] = bf16_lo(b.w); uu[8 * j + 7] = bf16_hi(b.w);
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t gw[4] = {ga[j].x, ga[j].y, ga[j].z, ga[j].w};
+        const uint32_t uw[4] = {ub[j].x, ub[j].y, ub[j].z, ub[j].w};
+        uint32_t odg[4], odu[4], oh[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float rdg[2], rdu[2], rh[2];
+#pragma unroll
+          for (int hl = 0; hl < 2; ++hl) {
+            const float gg = hl ? bf16_hi(gw[e]) : bf16_lo(gw[e]);
+            const float uu = hl ? bf16_hi(uw[e]) : bf16_lo(uw[e]);
+            const float dh = __uint_as_float(v[8 * j + 2 * e + hl]);
+            const float sg = __fdividef(1.0f, 1.0f + __expf(-gg));
+            const float a = gg * sg;
+            rh[hl] = p * a * uu;
+            dp += dh * a * uu;
+            rdu[hl] = p * dh * a;
+            rdg[hl] = p * dh * uu * sg * (1.0f + gg * (1.0f - sg));
+          }
+          odg[e] = pack_bf16x2(rdg[0], rdg[1]);
+          odu[e] = pack_bf16x2(rdu[0], rdu[1]);
+          oh[e] = pack_bf16x2(rh[0], rh[1]);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) gg[i] = uu[i] = 0.0f;
+        pdg[j] = make_uint4(odg[0], odg[1], odg[2], odg[3]);
+        pdu[j] = make_uint4(odu[0], odu[1], odu[2], odu[3]);
+        ph[j] = make_uint4(oh[0], oh[1], oh[2], oh[3]);
       }
-      float dg[32], du[32], hh[32], dp = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float dh = __uint_as_float(v[i]);
-        const float sg = __fdividef(1.0f, 1.0f + __expf(-gg[i]));
-        const float a = gg[i] * sg;
-        hh[i] = p * a * uu[i];
-        dp += dh * a * uu[i];
-        du[i] = p * dh * a;
-        dg[i] = p * dh * uu[i] * sg * (1.0f + gg[i] * (1.0f - sg));
-      }
-      uint4 pk[4];
-      const int64_t ld2 = static_cast<int64_t>(2 * fdim) * 2;
+      load_gu(c + 32 < BN ? fc + 32 : fdim, ga, ub);
       uint8_t* gbase = static_cast<uint8_t*>(g.out) + row_first * ld2 + static_cast<int64_t>(2 * fc) * 2;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        pk[j] = make_uint4(pack_bf16x2(dg[8 * j + 0], dg[8 * j + 1]), pack_bf16x2(dg[8 * j + 2], dg[8 * j + 3]),
-                           pack_bf16x2(dg[8 * j + 4], dg[8 * j + 5]), pack_bf16x2(dg[8 * j + 6], dg[8 * j + 7]));
-      warp_store_block<TMA>(st, pk, lane, &om.out, 2 * fc, row_first, gbase, ld2, rows_valid, 4);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        pk[j] = make_uint4(pack_bf16x2(du[8 * j + 0], du[8 * j + 1]), pack_bf16x2(du[8 * j + 2], du[8 * j + 3]),
-                           pack_bf16x2(du[8 * j + 4], du[8 * j + 5]), pack_bf16x2(du[8 * j + 6], du[8 * j + 7]));
-      warp_store_block<TMA>(st, pk, lane, &om.out, 2 * fc + 32, row_first, gbase + 64, ld2, rows_valid, 4);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        pk[j] = make_uint4(pack_bf16x2(hh[8 * j + 0], hh[8 * j + 1]), pack_bf16x2(hh[8 * j + 2], hh[8 * j + 3]),
-                           pack_bf16x2(hh[8 * j + 4], hh[8 * j + 5]), pack_bf16x2(hh[8 * j + 6], hh[8 * j + 7]));
-      const int64_t ldh = static_cast<int64_t>(fdim) * 2;
-      warp_store_block<TMA>(st, pk, lane, &om.out2, fc, row_first,
+      warp_store_block<TMA>(st, pdg, lane, &om.out, 2 * fc, row_first, gbase, ld2, rows_valid, 4);
+      warp_store_block<TMA>(st, pdu, lane, &om.out, 2 * fc + 32, row_first, gbase + 64, ld2, rows_valid, 4);
+      warp_store_block<TMA>(st, ph, lane, &om.out2, fc, row_first,
                             static_cast<uint8_t*>(g.out2) + row_first * ldh + static_cast<int64_t>(fc) * 2, ldh,
                             rows_valid, 4);
-      if (r < tl.rows) g.dp_part[row * (fdim / 32) + fc / 32] = dp;
+      if (live) g.dp_part[row * (fdim / 32) + fc / 32] = dp;
     }
   } else {
     const float p = r < tl.rows ? __ldg(g.row_prob + row_first + lane) : 0.0f;
