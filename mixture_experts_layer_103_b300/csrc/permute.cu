@@ -200,45 +200,49 @@ __device__ __forceinline__ void quantize_row_mx(const uint4* __restrict__ src, i
                                                 PutSf put_sf) {
   constexpr int VPV = IN_BF16 ? 8 : 4;  // values per 16-byte vector
   constexpr int LPB = 32 / VPV;         // lanes per 32-value block
+  constexpr int U = IN_BF16 ? 4 : 8;    // 16-byte loads in flight per lane
   const int row_vecs = d / VPV;
-  for (int base = 0; base < row_vecs; base += 32) {
-    const int c = base + lane;
-    const bool act = c < row_vecs;
-    float v[VPV];
-    if (act) {
-      const uint4 q = __ldg(src + c);
-      if (IN_BF16) {
-        v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
-        v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
-      } else {
-        v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
-        v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
-      }
-    } else {
+  for (int base = 0; base < row_vecs; base += 32 * U) {
+    uint4 q[U];
 #pragma unroll
-      for (int u = 0; u < VPV; ++u) v[u] = 0.0f;
+    for (int u = 0; u < U; ++u) {
+      const int c = base + 32 * u + lane;
+      q[u] = c < row_vecs ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
     }
-    float amax = 0.0f;
 #pragma unroll
-    for (int u = 0; u < VPV; ++u) amax = fmaxf(amax, fabsf(v[u]));
-#pragma unroll
-    for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const int X = mx_exponent(amax);
-    const float inv = mx_inv_scale(X);
-    if (act) {
+    for (int u = 0; u < U; ++u) {
+      const int c = base + 32 * u + lane;
+      const bool act = c < row_vecs;       // whole blocks: row_vecs is a multiple of LPB
+      float v[VPV];
       if (IN_BF16) {
-        uint2 o;
-        o.x = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
-              (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
-        o.y = static_cast<uint32_t>(e4m3x2(v[4] * inv, v[5] * inv)) |
-              (static_cast<uint32_t>(e4m3x2(v[6] * inv, v[7] * inv)) << 16);
-        *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(c) * 8) = o;
+        v[0] = bf16_lo(q[u].x); v[1] = bf16_hi(q[u].x); v[2] = bf16_lo(q[u].y); v[3] = bf16_hi(q[u].y);
+        v[4] = bf16_lo(q[u].z); v[5] = bf16_hi(q[u].z); v[6] = bf16_lo(q[u].w); v[7] = bf16_hi(q[u].w);
       } else {
-        const uint32_t o = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
-                           (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
-        *reinterpret_cast<uint32_t*>(dst + static_cast<int64_t>(c) * 4) = o;
+        v[0] = __uint_as_float(q[u].x); v[1] = __uint_as_float(q[u].y);
+        v[2] = __uint_as_float(q[u].z); v[3] = __uint_as_float(q[u].w);
       }
-      if ((lane % LPB) == 0) put_sf(c * VPV, static_cast<uint8_t>(X + 127));
+      float amax = 0.0f;
+#pragma unroll
+      for (int e = 0; e < VPV; ++e) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+      for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const int X = mx_exponent(amax);
+      const float inv = mx_inv_scale(X);
+      if (act) {
+        if (IN_BF16) {
+          uint2 o;
+          o.x = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
+                (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
+          o.y = static_cast<uint32_t>(e4m3x2(v[4] * inv, v[5] * inv)) |
+                (static_cast<uint32_t>(e4m3x2(v[6] * inv, v[7] * inv)) << 16);
+          *reinterpret_cast<uint2*>(dst + static_cast<int64_t>(c) * 8) = o;
+        } else {
+          const uint32_t o = static_cast<uint32_t>(e4m3x2(v[0] * inv, v[1] * inv)) |
+                             (static_cast<uint32_t>(e4m3x2(v[2] * inv, v[3] * inv)) << 16);
+          *reinterpret_cast<uint32_t*>(dst + static_cast<int64_t>(c) * 4) = o;
+        }
+        if ((lane % LPB) == 0) put_sf(c * VPV, static_cast<uint8_t>(X + 127));
+      }
     }
   }
 }
