@@ -191,18 +191,25 @@ __global__ void __launch_bounds__(256) perm_gather_copy_kernel(const uint4* __re
   }
 }
 
-// MXFP8 quantisation of one row by one warp (blocks of 32 along d).  IN_BF16 = 1: bf16
-// input (8 values per 16-byte vector, 4 lanes per block); 0: fp32 input (4 per vector, 8
-// lanes).  E4M3 codes go to dst; the E8M0 byte of the block holding column col is passed
-// to put_sf(col, byte) by the first lane of the block.
+// MXFP8 quantisation of 16-byte vectors [v0, v1) of one row by one warp (blocks of 32
+// along d; v0 and v1 on block boundaries).  IN_BF16 = 1: bf16 input (8 values per 16-byte
+// vector, 4 lanes per block); 0: fp32 input (4 per vector, 8 lanes).  E4M3 codes go to
+// dst (the row's start); the E8M0 byte of the block holding column col is passed to
+// put_sf(col, byte) by the first lane of the block.
+template <int IN_BF16>
+struct MxRow {
+  static constexpr int VPV = IN_BF16 ? 8 : 4;  // values per 16-byte vector
+  static constexpr int U = IN_BF16 ? 4 : 8;    // 16-byte loads in flight per lane
+  static constexpr int SLICE = 32 * U;         // vectors one warp pass covers
+};
 template <int IN_BF16, typename PutSf>
-__device__ __forceinline__ void quantize_row_mx(const uint4* __restrict__ src, int d, int lane, uint8_t* __restrict__ dst,
-                                                PutSf put_sf) {
-  constexpr int VPV = IN_BF16 ? 8 : 4;  // values per 16-byte vector
-  constexpr int LPB = 32 / VPV;         // lanes per 32-value block
-  constexpr int U = IN_BF16 ? 4 : 8;    // 16-byte loads in flight per lane
-  const int row_vecs = d / VPV;
-  for (int base = 0; base < row_vecs; base += 32 * U) {
+__device__ __forceinline__ void quantize_row_mx(const uint4* __restrict__ src, int v0, int v1, int lane,
+                                                uint8_t* __restrict__ dst, PutSf put_sf) {
+  constexpr int VPV = MxRow<IN_BF16>::VPV;
+  constexpr int LPB = 32 / VPV;  // lanes per 32-value block
+  constexpr int U = MxRow<IN_BF16>::U;
+  const int row_vecs = v1;
+  for (int base = v0; base < row_vecs; base += 32 * U) {
     uint4 q[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -248,7 +255,8 @@ __device__ __forceinline__ void quantize_row_mx(const uint4* __restrict__ src, i
 }
 
 // Row copy with MXFP8 quantisation into the permuted order (scales in the activation SF
-// tile layout of the expert m-tiles).
+// tile layout of the expert m-tiles).  Work items are (row, slice of MxRow::SLICE vectors),
+// so short permutations still spread over every SM.
 template <int IN_BF16>
 __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __restrict__ x, int d,
                                                              const int32_t* __restrict__ offsets, int E_loc,
@@ -268,7 +276,13 @@ __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __rest
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int N = s_tab[E_loc];
   const int row_vecs = d / VPV;
-  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < N; r += warps) {
+  constexpr int SL = MxRow<IN_BF16>::SLICE;
+  const int slices = (row_vecs + SL - 1) / SL;
+  const int64_t items = static_cast<int64_t>(N) * slices;
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
+       it += warps) {
+    const int64_t r = it / slices;
+    const int sl = static_cast<int>(it - r * slices);
     // expert of row r: the last e with offsets[e] <= r
     int lo = 0, hi = E_loc - 1;
     while (lo < hi) {
@@ -280,7 +294,7 @@ __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __rest
     const int64_t tile = s_tab[E_loc + 1 + lo] + il / 128;
     const int i = il % 128;
     const int64_t t = __ldg(row_src_token + r);
-    quantize_row_mx<IN_BF16>(x + t * row_vecs, d, lane, perm_x + r * d,
+    quantize_row_mx<IN_BF16>(x + t * row_vecs, sl * SL, min(row_vecs, (sl + 1) * SL), lane, perm_x + r * d,
                              [&](int col, uint8_t b) { perm_sf[sf_act_offset(tile, i, col, d)] = b; });
   }
 }
@@ -304,7 +318,8 @@ __global__ void __launch_bounds__(256) quant_rows_mx_kernel(const uint4* __restr
       if (!__any_sync(0xffffffffu, local)) continue;
     }
     uint8_t* sf_row = x_sf + t * (d / 32);
-    quantize_row_mx<IN_BF16>(x + t * row_vecs, d, lane, xq + t * d, [&](int col, uint8_t b) { sf_row[col / 32] = b; });
+    quantize_row_mx<IN_BF16>(x + t * row_vecs, 0, row_vecs, lane, xq + t * d,
+                             [&](int col, uint8_t b) { sf_row[col / 32] = b; });
   }
 }
 
