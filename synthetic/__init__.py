@@ -80,6 +80,10 @@ WORKLOADS = {
     "mxfp8_ep8_zipf_T8192": Workload("mxfp8_ep8_zipf_T8192", 8192, 7168, 2048, 256, 8, 0, 32, "mxfp8", ("zipf", 1.1)),
     # MXFP8 variant of the EP64 slice at T=8192.
     "mxfp8_ep64_T8192": Workload("mxfp8_ep64_T8192", 8192, 7168, 2048, 256, 8, 0, 4, "mxfp8"),
+    # One expert holding every token (E = 1, top-1) at the slices' d and f: the grouped GEMMs
+    # without ragged segments, i.e. the dense tensor-core rate of the same kernels.
+    "dense_bf16_T16384": Workload("dense_bf16_T16384", 16384, 7168, 2048, 1, 1, 0, 1, "bf16"),
+    "dense_mxfp8_T16384": Workload("dense_mxfp8_T16384", 16384, 7168, 2048, 1, 1, 0, 1, "mxfp8"),
 }
 
 

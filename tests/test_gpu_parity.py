@@ -292,7 +292,7 @@ def test_canaries_untouched(moe, dtype):
 
 # ----------------------------------------------------------------------------- full size
 FULL = ["tiny_fp32", "bf16_e64", "ep8_zipf_T512", "ep64_T2048", "ep64_T8192", "ep64_T32768",
-        "mxfp8_ep8_zipf_T8192", "mxfp8_ep64_T8192"]
+        "mxfp8_ep8_zipf_T8192", "mxfp8_ep64_T8192", "dense_bf16_T16384", "dense_mxfp8_T16384"]
 
 
 @pytest.mark.parametrize("name", FULL)
