@@ -6,8 +6,9 @@
 // probability was applied inside the SwiGLU, so this is an unweighted sum.
 //
 // Work item = (token, slice of kCombineSlice 16-byte vectors of its row), grid-strided
-// over a persistent grid: a wide row (d = 7168) is spread over several warps, so the
-// serial chain of load latencies per warp stays short.
+// over a persistent grid: a wide row (d = 7168) is spread over several warps, and each
+// lane issues the loads of its 4 vectors for up to 4 slots at once, so even a token with
+// one local slot keeps several loads in flight.
 #include <algorithm>
 
 #include "moe_common.cuh"
@@ -16,7 +17,7 @@ namespace moe {
 
 int num_sms();
 
-constexpr int kCombineGroup = 8;    // slots whose loads are in flight together
+constexpr int kCombineGroup = 4;    // slots whose loads are in flight together
 constexpr int kCombineSlice = 128;  // 16-byte vectors per work item (4 per lane)
 
 template <bool F32>
@@ -25,63 +26,75 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const uint4* __restrict
                                                       uint4* __restrict__ y) {
   pdl_launch_dependents();
   pdl_wait();
-  constexpr int V = F32 ? 4 : 8;  // values per 16-byte vector
+  constexpr int V = F32 ? 4 : 8;                // values per 16-byte vector
+  constexpr int S = kCombineSlice / 32;         // vectors per lane per item
+  constexpr int G = kCombineGroup;
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t items = static_cast<int64_t>(T) * slices;
   for (int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
        item += warps) {
-  const int64_t t = item / slices;
-  const int64_t c_begin = (item - t * slices) * kCombineSlice;
-  const int64_t c_end = std::min<int64_t>(row_vecs, c_begin + kCombineSlice);
-  const int32_t my_row = lane < k ? __ldg(p2r + t * k + lane) : -1;
-  const uint32_t valid = __ballot_sync(0xffffffffu, my_row >= 0);  // local slots, ascending j
-  const int nv = __popc(valid);
-  uint4* dst = y + t * row_vecs;
-  for (int64_t base = c_begin; base < c_end; base += 32) {  // warp-uniform trip count
-    const int64_t c = base + lane;
-    const bool act = c < c_end;
-    float acc[V];
+    const int64_t t = item / slices;
+    const int64_t c_begin = (item - t * slices) * kCombineSlice;
+    const int64_t c_end = std::min<int64_t>(row_vecs, c_begin + kCombineSlice);
+    const int32_t my_row = lane < k ? __ldg(p2r + t * k + lane) : -1;
+    const uint32_t valid = __ballot_sync(0xffffffffu, my_row >= 0);  // local slots, ascending j
+    const int nv = __popc(valid);
+    float acc[S][V];
 #pragma unroll
-    for (int u = 0; u < V; ++u) acc[u] = 0.0f;
+    for (int s = 0; s < S; ++s)
+#pragma unroll
+      for (int u = 0; u < V; ++u) acc[s][u] = 0.0f;
     uint32_t m = valid;
-    for (int g = 0; g < nv; g += kCombineGroup) {
-      // issue the loads of up to 8 slots, then add them in slot order
-      uint4 q[kCombineGroup];
+    for (int g = 0; g < nv; g += G) {
+      // the loads of up to G slots x S vectors are issued together, then added in slot order
+      uint4 q[G][S];
 #pragma unroll
-      for (int j = 0; j < kCombineGroup; ++j) {
-        q[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (g + j < nv) {
+      for (int j = 0; j < G; ++j) {
+        int64_t row = 0;
+        if (g + j < nv) {  // warp-uniform
           const int src = __ffs(m) - 1;
           m &= m - 1;
-          const int64_t row = __shfl_sync(0xffffffffu, my_row, src);
-          if (act) q[j] = __ldg(Y2 + row * row_vecs + c);
+          row = __shfl_sync(0xffffffffu, my_row, src);
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+          const int64_t c = c_begin + lane + 32 * s;
+          q[j][s] = (g + j < nv && c < c_end) ? __ldg(Y2 + row * row_vecs + c) : make_uint4(0u, 0u, 0u, 0u);
         }
       }
 #pragma unroll
-      for (int j = 0; j < kCombineGroup; ++j) {
+      for (int j = 0; j < G; ++j) {
         if (g + j < nv) {
-          if (F32) {
-            acc[0] += __uint_as_float(q[j].x); acc[1] += __uint_as_float(q[j].y);
-            acc[2] += __uint_as_float(q[j].z); acc[3] += __uint_as_float(q[j].w);
-          } else {
-            acc[0] += bf16_lo(q[j].x); acc[1] += bf16_hi(q[j].x); acc[2] += bf16_lo(q[j].y);
-            acc[3] += bf16_hi(q[j].y); acc[4] += bf16_lo(q[j].z); acc[5] += bf16_hi(q[j].z);
-            acc[6] += bf16_lo(q[j].w); acc[7] += bf16_hi(q[j].w);
+#pragma unroll
+          for (int s = 0; s < S; ++s) {
+            if (F32) {
+              acc[s][0] += __uint_as_float(q[j][s].x); acc[s][1] += __uint_as_float(q[j][s].y);
+              acc[s][2] += __uint_as_float(q[j][s].z); acc[s][3] += __uint_as_float(q[j][s].w);
+            } else {
+              acc[s][0] += bf16_lo(q[j][s].x); acc[s][1] += bf16_hi(q[j][s].x);
+              acc[s][2] += bf16_lo(q[j][s].y); acc[s][3] += bf16_hi(q[j][s].y);
+              acc[s][4] += bf16_lo(q[j][s].z); acc[s][5] += bf16_hi(q[j][s].z);
+              acc[s][6] += bf16_lo(q[j][s].w); acc[s][7] += bf16_hi(q[j][s].w);
+            }
           }
         }
       }
     }
-    uint4 o;
-    if (F32) {
-      o = make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
-                     __float_as_uint(acc[3]));
-    } else {
-      o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                     pack_bf16x2(acc[6], acc[7]));
+    uint4* dst = y + t * row_vecs;
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      const int64_t c = c_begin + lane + 32 * s;
+      uint4 o;
+      if (F32) {
+        o = make_uint4(__float_as_uint(acc[s][0]), __float_as_uint(acc[s][1]), __float_as_uint(acc[s][2]),
+                       __float_as_uint(acc[s][3]));
+      } else {
+        o = make_uint4(pack_bf16x2(acc[s][0], acc[s][1]), pack_bf16x2(acc[s][2], acc[s][3]),
+                       pack_bf16x2(acc[s][4], acc[s][5]), pack_bf16x2(acc[s][6], acc[s][7]));
+      }
+      if (c < c_end) __stcs(dst + c, o);  // y is written once and not re-read: streaming store
     }
-    if (act) __stcs(dst + c, o);  // y is written once and not re-read: streaming store
-  }
   }
 }
 
