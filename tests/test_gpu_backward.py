@@ -91,6 +91,17 @@ def test_backward_forced_segments(moe):
         assert (g["dW_gate"][e] == 0).all() and (g["dW_up"][e] == 0).all() and (g["dW_down"][e] == 0).all()
 
 
+def test_backward_empty_batch(moe):
+    """T = 0: no routed rows, so every weight gradient is exactly zero."""
+    w = Workload("b_empty", 0, 128, 96, 8, 2, 0, 8, "bf16")
+    x, lg, dy = gen_x(w), gen_logits(w), gen_dy(w)
+    Wg, Wu, Wd = gen_weights(w)
+    g = _run(moe, w, x, lg, dy, Wg, Wu, Wd)
+    assert tuple(g["dx"].shape) == (0, w.d) and tuple(g["dlogits"].shape) == (0, w.E)
+    for key in ("dW_gate", "dW_up", "dW_down"):
+        assert (g[key] == 0).all(), key
+
+
 def test_backward_deterministic(moe):
     w = SMALL[2]
     x, lg, dy = gen_x(w), gen_logits(w), gen_dy(w)

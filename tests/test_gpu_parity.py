@@ -230,6 +230,16 @@ def test_no_local_expert_gives_zeros(moe, dtype):
     assert (to_np(y) == 0).all()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "mxfp8"])
+def test_layer_empty_batch(moe, dtype):
+    """T = 0: the fused forward launches nothing that touches rows and reports no error."""
+    w = Workload("empty", 0, 256, 128, 8, 2, 0, 8, dtype)
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    y = gpu_layer(moe, w, x, lg, Wg, Wu, Wd)
+    assert tuple(y.shape) == (0, w.d)
+
+
 def test_split_calls_equal_fused_call(moe):
     """route -> permute -> gemm1 -> gemm2 -> combine through the separate entry points
     gives exactly the fused moe_layer_forward result (same kernels, same order)."""
