@@ -582,9 +582,10 @@ def run_ours(args, w):
 
 
 def run_backward(args, w):
-    """One step = moe_layer_backward (maps, recomputed gate/up, dh + ScaledSwiGLU backward,
-    dx, router-logit and weight gradients) on inputs resident in HBM; K steps captured as
-    one CUDA graph and replayed inside the timed region."""
+    """One step = moe_layer_backward (maps, dy and x rows copied into routed order, dh +
+    ScaledSwiGLU backward, dx, router-logit and weight gradients; the gate/up
+    pre-activations come from moe_layer_forward_train) on inputs resident in HBM; K steps
+    captured as one CUDA graph and replayed inside the timed region."""
     import torch
     import torch.distributed as dist
 
