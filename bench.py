@@ -288,6 +288,23 @@ def layer_bytes_flops(w, N, nonempty, n_tok_local):
     return out
 
 
+def backward_floor(w, N, nonempty, pk):
+    """Per-kernel roofline of the bf16 backward: sum over its kernels of max(FLOPs / tensor
+    peak, algorithmic bytes / HBM bandwidth), in seconds, with the per-kernel terms."""
+    d, f, T, E = w.d, w.f, w.T, nonempty
+    tf, bw = pk["bf16_tflops"] * 1e12, pk["hbm_gbs"] * 1e9
+    parts = {  # name: (FLOPs, bytes)
+        "row_copies": (0.0, 2 * (N * d * 2 + T * d * 2)),
+        "dh_dswiglu": (2.0 * N * d * f, E * d * f * 2 + N * d * 2 + N * 2 * f * 2 + N * 2 * f * 2 + N * f * 2),
+        "dx_gemm": (4.0 * N * d * f, N * 2 * f * 2 + E * d * 2 * f * 2 + N * d * 2),
+        "slot_sum": (0.0, N * d * 2 + T * d * 2),
+        "wgrad_down": (2.0 * N * d * f, N * f * 2 + N * d * 2 + w.E_loc * f * d * 4),
+        "wgrad_gate_up": (4.0 * N * d * f, N * d * 2 + N * 2 * f * 2 + w.E_loc * d * 2 * f * 4),
+    }
+    terms = {k: max(fl / tf, by / bw) for k, (fl, by) in parts.items()}
+    return sum(terms.values()), terms
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -615,6 +632,7 @@ def run_backward(args, w):
         raise RuntimeError("device error during warm-up")
     P = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, "bf16", maps_only=True)
     N = int(P["offsets"][-1].item())
+    nonempty = int((P["counts"] > 0).sum().item())
     g = torch.cuda.CUDAGraph()
     cs = torch.cuda.Stream()
     cs.wait_stream(torch.cuda.current_stream())
@@ -643,6 +661,7 @@ def run_backward(args, w):
     # the backward's GEMM work (g, u saved by the training forward): dh 2NDF, dx 4NDF,
     # weight gradients 6NDF
     flops = 12.0 * N * w.d * w.f
+    floor_s, floor_terms = backward_floor(w, N, nonempty, pk)
     line = {
         "metric": "MoE-layer backward tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -652,6 +671,9 @@ def run_backward(args, w):
                      "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
                      "kernel": "whole backward (12 N d f FLOP)", "traffic": None, "peak_kind": pk_kind},
         "N_pairs": N, "gpu_launches": 11 * args.steps, "clocks": clk,
+        "per_kernel_floor": {"roofline_us": floor_s * 1e6, "measured_us": ms * 1e3, "frac": floor_s / (ms * 1e-3),
+                             "terms_us": {k: v * 1e6 for k, v in floor_terms.items()},
+                             "note": "sum over the backward's kernels of max(FLOPs / bf16 peak, bytes / HBM)"},
         "saved_preactivations": "from moe_layer_forward_train (no recompute)",
     }
     if rank == 0:
