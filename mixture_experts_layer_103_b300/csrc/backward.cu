@@ -2,10 +2,13 @@
 // x, the three expert weight tensors and the router logits ("Efficient MoE training for
 // biological foundation models", section "GroupedLinear Optimizes Expert Computation":
 // the fused GroupedMLP has a matching backward, with the ScaledSwiGLU backward producing
-// the scale (routing-probability) gradient).  Per routed row (token t, expert e, prob p):
-//   g, u = x W_gate_e, x W_up_e        recomputed (row-gather GEMM, bf16 store)
-//   dh = dy_t W_down_e^T                row-gather GEMM on dy with the ScaledSwiGLU backward in
-//                                       its epilogue: dg, du (packed order), h, partial dp
+// the scale (routing-probability) gradient).  Per routed row (token t, expert e, prob p),
+// with x and dy first copied into routed-row order (TMA-loadable operands):
+//   g, u = x W_gate_e, x W_up_e        kept by the training forward, else recomputed (bf16
+//                                       store GEMM on the x rows)
+//   dh = dy_t W_down_e^T                grouped GEMM on the dy rows with the ScaledSwiGLU
+//                                       backward in its epilogue: dg, du (packed order), h,
+//                                       partial dp
 //   dx_row = [dg du] [W_gate W_up]^T    grouped GEMM on the packed transposed weights
 //   dx_t = sum over the token's slots   (the forward's combine kernel)
 //   dlogits: softmax-over-top-k backward of the local dp (non-local slots count as 0)
