@@ -240,6 +240,22 @@ def test_layer_empty_batch(moe, dtype):
     assert tuple(y.shape) == (0, w.d)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
+def test_ep_slices_sum_to_full_layer(moe, dtype):
+    """Expert parallelism on one GPU: the partial outputs of the disjoint expert slices
+    e0 = 0, 32, ..., 224 of a 256-expert top-8 layer (what each GPU of an EP8 group
+    computes) sum to the full layer -- the sum-reduce that replaces the exchange step."""
+    w = Workload("ep_sum", 256, 256, 128, 256, 8, 0, 256, dtype, ("zipf", 1.1))
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    acc = np.zeros((w.T, w.d))
+    for e0 in range(0, 256, 32):
+        sl = slice(e0, e0 + 32)
+        acc += to_np(gpu_layer(moe, w.replace(e0=e0, E_loc=32), x, lg, Wg[sl], Wu[sl], Wd[sl]))
+    yo = oracle_layer(w, x, lg, Wg, Wu, Wd)
+    assert rel_l2(acc, yo) <= TOL[dtype]
+
+
 def test_split_calls_equal_fused_call(moe):
     """route -> permute -> gemm1 -> gemm2 -> combine through the separate entry points
     gives exactly the fused moe_layer_forward result (same kernels, same order)."""
