@@ -193,8 +193,8 @@ size_t moe_mx_weight_scale_bytes(int E_loc, int rows, int K);
  *   workspace device >= moe_grouped_mlp_workspace_size(...) bytes, 256-byte aligned
  *   rows_hint  expected rows per local expert (e.g. moe_rows_hint(T, k, E)); it only picks
  *              the kernel shape (bf16 GEMM1 runs on CTA pairs with 256-row tiles from 2048
- *              expected rows up, bf16 GEMM2 from 128), never the result's meaning; <= 0 uses
- *              N_cap / E_loc.
+ *              expected rows up, and from 256 to 1023 when d >= 4096; bf16 GEMM2 from 128),
+ *              never the result's meaning; <= 0 uses N_cap / E_loc.
  * Requires d % 8 == 0 and f % 32 == 0 (bf16); d % 128 == 0 and f % 128 == 0 (MXFP8). */
 moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                            const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
@@ -204,6 +204,11 @@ moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, cons
 /* Expected rows per local expert under uniform routing, T * k / E (the hint
  * moe_layer_forward uses). */
 int moe_rows_hint(int T, int k, int E);
+/* The GEMM1 kernel moe_layer_forward picks for this problem (host only, no launch): 1 if
+ * GEMM1 runs on CTA pairs (256-row tiles, A from a permuted copy of x), 0 if on the 1-CTA
+ * kernel (bf16: A read from the token rows inside the kernel; fp32 / MXFP8: from a
+ * permuted copy).  Returns -1 for invalid sizes. */
+int moe_layer_gemm1_pairs(int T, int d, int k, int E, int E_loc, moe_dtype dtype);
 size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype);
 
 /* The two halves of moe_grouped_mlp, for callers that keep h themselves (same

@@ -58,6 +58,7 @@ _SIGS = {
     "moe_mx_weight_scale_bytes": (_SZ, [_I, _I, _I]),
     "moe_grouped_mlp": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_rows_hint": (_I, [_I, _I, _I]),
+    "moe_layer_gemm1_pairs": (_I, [_I, _I, _I, _I, _I, _I]),
     "moe_grouped_mlp_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm1_swiglu_gather": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -224,6 +225,14 @@ def moe_pack_weights(W_gate: torch.Tensor, W_up: torch.Tensor, W_down: torch.Ten
 
 def moe_rows_hint(T: int, k: int, E: int) -> int:
     return int(_lib.moe_rows_hint(T, k, E))
+
+
+def moe_layer_gemm1_pairs(T: int, d: int, k: int, E: int, E_loc: int, dtype: str) -> bool:
+    """True if moe_layer_forward runs GEMM1 on CTA pairs (A from a permuted copy of x)."""
+    r = int(_lib.moe_layer_gemm1_pairs(T, d, k, E, E_loc, _dt(dtype)))
+    if r < 0:
+        raise ValueError("invalid sizes")
+    return bool(r)
 
 
 def moe_grouped_mlp(perm_x, perm_x_scale, offsets, row_prob, pw: PackedWeights, Y2=None, ws=None, rows_hint=0):

@@ -107,15 +107,20 @@ static moe_status check_mlp_shape(int d, int f, int E_loc, moe_dtype dt) {
   return MOE_OK;
 }
 
-// Expected rows per local expert at or above which bf16 GEMMs run on CTA pairs (256-row
-// tiles).  Measured on B300 the pair kernel did not beat the 1-CTA kernel at 512 or 1024
-// rows per expert (its 256-row tiles pad ragged segments twice as much), so it is only
-// chosen for very tall segments; callers can force either with rows_hint.
+// When bf16 GEMM1 runs on CTA pairs (256-row tiles), from the expected rows per local
+// expert and K = d.  Measured on B300 (each against the 1-CTA kernel):
+//   * from 2048 rows: the pairs win (dense segments, little padding);
+//   * 256-1023 rows with K >= 4096 (weight-streaming slices, tiles mostly full): the
+//     pairs' lower per-SM shared-memory fill wins (layer step at T = 8192 / 16384, d = 7168,
+//     4 of 256 experts: 192 -> 184 / 278 -> 263 us);
+//   * otherwise the 1-CTA kernel: at 512 rows with K = 2048 and skewed segments, or a
+//     Zipf-skewed 128-row average, the 256-row tiles pad too much (+20 / +28 us).
+// Callers of the single GEMMs can force either with rows_hint.
 constexpr int kPairRowsThreshold = 2048;
 
-static bool use_pair(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint) {
+static bool use_pair(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint, int K) {
   const int64_t rows = rows_hint > 0 ? rows_hint : n_cap / (E_loc > 0 ? E_loc : 1);
-  return dt == MOE_BF16 && rows >= kPairRowsThreshold;
+  return dt == MOE_BF16 && (rows >= kPairRowsThreshold || (rows >= 256 && rows < 1024 && K >= 4096));
 }
 
 // GEMM2 (K = f, output d) on CTA pairs from 128 expected rows per expert: measured on B300
@@ -139,7 +144,7 @@ static cudaError_t run_gemm1(const void* perm_x, const uint8_t* perm_sf, const i
     return launch_simt_gemm1(static_cast<const float*>(perm_x), offsets, row_prob, n_cap, E_loc, d, f,
                              static_cast<const float*>(Wgu), static_cast<float*>(h), st);
   return launch_tc_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt == MOE_MXFP8,
-                         use_pair(dt, n_cap, E_loc, rows_hint), Wgu, Wgu_sf, h, h_sf, err, kTimeoutNs, gu_save,
+                         use_pair(dt, n_cap, E_loc, rows_hint, d), Wgu, Wgu_sf, h, h_sf, err, kTimeoutNs, gu_save,
                          st);
 }
 
@@ -170,10 +175,10 @@ static cudaError_t run_mlp(const void* perm_x, const uint8_t* perm_sf, const int
 // row-gather GEMM1 was 7-10 % slower than the TMA-fed one and quantising per token saved
 // nothing over quantising while copying, while bf16 gains: the permuted copy costs 27 us
 // at T = 4096, d = 2048, k = 8 and the gather adds less than that to GEMM1.
-static bool layer_gathers(moe_dtype dt, int T, int k, int E, int E_loc) {
+static bool layer_gathers(moe_dtype dt, int T, int d, int k, int E, int E_loc) {
   const int64_t n_cap = n_cap_of(T, k, E_loc);
   const int64_t rows = T > 0 && k > 0 && E > 0 ? static_cast<int64_t>(T) * k / E : 0;
-  return dt == MOE_BF16 && !use_pair(dt, n_cap, E_loc, static_cast<int>(rows));
+  return dt == MOE_BF16 && !use_pair(dt, n_cap, E_loc, static_cast<int>(rows), d);
 }
 
 // ---- whole-layer workspace -------------------------------------------------------------
@@ -195,7 +200,7 @@ struct LayerWs {
 };
 static LayerWs layer_layout(uint8_t* base, int T, int d, int f, int E, int k, int E_loc, moe_dtype dt) {
   const int64_t n_cap = n_cap_of(T, k, E_loc);
-  const bool gather = layer_gathers(dt, T, k, E, E_loc);
+  const bool gather = layer_gathers(dt, T, d, k, E, E_loc);
   LayerWs w{};
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -407,6 +412,11 @@ int moe_rows_hint(int T, int k, int E) {
   return static_cast<int>(static_cast<int64_t>(T) * k / E);
 }
 
+int moe_layer_gemm1_pairs(int T, int d, int k, int E, int E_loc, moe_dtype dtype) {
+  if (T < 0 || d <= 0 || k <= 0 || E <= 0 || E_loc <= 0 || E_loc > E) return -1;
+  return use_pair(dtype, n_cap_of(T, k, E_loc), E_loc, moe_rows_hint(T, k, E), d) ? 1 : 0;
+}
+
 static moe_status check_gemm_common(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype, const void* offsets,
                                     const void* a, const void* a_sf, const void* w, const void* w_sf, const void* out,
                                     const void* out_sf) {
@@ -510,7 +520,7 @@ static moe_status layer_forward_impl(const void* x, const float* logits, int T, 
   const moe_dtype x_dtype = dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
   const int hint = moe_rows_hint(T, k, E);
   cudaError_t e = launch_route_topk(logits, T, E, k, w.topk_ids, w.topk_probs, stream);
-  if (layer_gathers(dtype, T, k, E, E_loc)) {
+  if (layer_gathers(dtype, T, d, k, E, E_loc)) {
     // maps only, then GEMM1 reads the token rows (quantised once per token for MXFP8)
     if (e == cudaSuccess)
       e = launch_permute(x, x_dtype, dtype, T, d, w.topk_ids, w.topk_probs, k, e0, E_loc, nullptr, nullptr,

@@ -127,7 +127,8 @@ def test_backward_full_size_sampled(moe):
     _check(g, ref, tokens=tok, experts=experts)
 
 
-@pytest.mark.parametrize("w", [SMALL[1], SMALL[2]], ids=["b_slice", "b_e64"])
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[2], Workload("b_pair", 512, 4096, 128, 4, 2, 0, 4, "bf16")],
+                         ids=["b_slice", "b_e64", "b_pair_longk"])
 def test_training_forward_saves_preactivations(moe, w):
     """moe_layer_forward_train: y bit-identical to moe_layer_forward, routing equal to
     moe_route_topk, and the backward on its saved g/u bit-identical to the backward that

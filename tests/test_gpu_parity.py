@@ -171,6 +171,7 @@ SMALL = [
     Workload("bf16_ep64", 4096, 384, 256, 256, 8, 0, 4, "bf16"),
     Workload("bf16_zipf", 512, 256, 128, 256, 8, 0, 32, "bf16", ("zipf", 1.1)),
     Workload("bf16_pair_layer", 2048, 256, 256, 8, 2, 0, 8, "bf16"),   # T*k/E = 512: CTA-pair GEMMs
+    Workload("bf16_pair_longk", 512, 4096, 128, 4, 2, 0, 4, "bf16"),   # 256 rows, d >= 4096: pair GEMM1
     Workload("mx_a", 256, 256, 256, 8, 2, 0, 8, "mxfp8"),
     Workload("mx_ragged", 300, 384, 384, 16, 4, 4, 8, "mxfp8"),
     Workload("mx_zipf", 1024, 512, 256, 256, 8, 0, 32, "mxfp8", ("zipf", 1.1)),
