@@ -137,3 +137,22 @@ def test_validation_before_any_launch(lib):
                                 1 << 30, s) == 1
     # device error read: null output
     assert L.moe_get_device_error(P, s, None) == 1
+
+
+def test_gemm1_kernel_choice(lib):
+    """The host-side rule behind moe_layer_forward's GEMM1 kernel: CTA pairs from 2048
+    expected rows per expert, or 256-1023 rows when d >= 4096 (bf16 only); the 1-CTA
+    kernel otherwise (measured per shape on B300)."""
+    pairs = lib.moe_layer_gemm1_pairs
+    assert not pairs(4096, 2048, 8, 64, 64, "bf16")      # 512 rows, d = 2048
+    assert pairs(8192, 7168, 8, 256, 4, "bf16")          # 256 rows, d = 7168
+    assert pairs(16384, 7168, 8, 256, 4, "bf16")         # 512 rows
+    assert not pairs(32768, 7168, 8, 256, 4, "bf16")     # 1024 rows
+    assert not pairs(2048, 7168, 8, 256, 4, "bf16")      # 64 rows
+    assert not pairs(8192, 2048, 8, 256, 4, "bf16")      # 256 rows but d < 4096
+    assert pairs(16384, 7168, 1, 1, 1, "bf16")           # dense: 16384 rows
+    assert pairs(4096, 1024, 8, 16, 16, "bf16")          # 2048 rows
+    assert not pairs(8192, 7168, 8, 256, 4, "mxfp8")     # no MXFP8 pair kernel
+    assert not pairs(8192, 7168, 8, 256, 4, "f32")
+    with pytest.raises(ValueError):
+        pairs(8192, 7168, 8, 256, 512, "bf16")            # E_loc > E
