@@ -55,6 +55,7 @@ cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dty
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;  // routed rows are int32 indices
 constexpr int kMaxDevices = 64;
 
 int num_sms() {
@@ -332,6 +333,7 @@ static moe_status check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm
                                 const void* p2r) {
   if (T < 0 || d <= 0 || k < 1 || k > 32 || e0 < 0 || E_loc < 1 || E_loc > 1024 || e0 > (1 << 30))
     return MOE_ERR_INVALID_ARG;
+  if (n_cap_of(T, k, E_loc) > kMaxRows) return MOE_ERR_INVALID_ARG;  // int32 rows and offsets
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !ids || !probs || !rst || !rp || !p2r)) return MOE_ERR_INVALID_ARG;
   const bool ok_types = (x_dtype == MOE_F32 && perm_dtype == MOE_F32) || (x_dtype == MOE_BF16 && perm_dtype == MOE_BF16) ||
@@ -504,6 +506,7 @@ static moe_status layer_forward_impl(const void* x, const float* logits, int T, 
                                      moe_stream_t stream) {
   if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32) return MOE_ERR_INVALID_ARG;
   if (e0 < 0 || E_loc < 1 || e0 + E_loc > E) return MOE_ERR_INVALID_ARG;
+  if (n_cap_of(T, k, E_loc) > kMaxRows) return MOE_ERR_INVALID_ARG;  // int32 rows and offsets
   moe_status s = check_mlp_shape(d, f, E_loc, dtype);
   if (s != MOE_OK) return s;
   if (!Wgu_packed || !Wd_packed) return MOE_ERR_INVALID_ARG;
@@ -582,6 +585,7 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
                               size_t workspace_bytes, moe_stream_t stream) {
   if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32 || e0 < 0 || E_loc < 1 || e0 + E_loc > E)
     return MOE_ERR_INVALID_ARG;
+  if (n_cap_of(T, k, E_loc) > kMaxRows) return MOE_ERR_INVALID_ARG;  // int32 rows and offsets
   moe_status s = check_mlp_shape(d, f, E_loc, MOE_BF16);
   if (s != MOE_OK) return s;
   if (!Wgu_packed || !W_down || !WguT_packed || !dW_gate || !dW_up || !dW_down) return MOE_ERR_INVALID_ARG;

@@ -106,6 +106,10 @@ def test_validation_before_any_launch(lib):
     assert L.moe_unpermute_combine(P, P, 4, 2, 60, 1, P, s) == 2
     # layer: e0 + E_loc > E, workspace too small
     assert L.moe_layer_forward(P, P, 8, 64, 64, 8, 2, 4, 8, 1, P, None, P, None, P, P, 1 << 30, s) == 1
+    # more routed rows than int32 indices hold (T * min(k, E_loc) > 2^31 - 1)
+    big_T = (1 << 28) + 1
+    assert L.moe_layer_forward(P, P, big_T, 64, 64, 8, 8, 0, 8, 1, P, None, P, None, P, P, 1 << 30, s) == 1
+    assert L.moe_permute(P, 1, 1, big_T, 64, P, P, 8, 0, 8, P, None, P, P, P, P, P, P, 1 << 20, s) == 1
     assert L.moe_layer_forward(P, P, 8, 64, 64, 8, 2, 0, 8, 1, P, None, P, None, P, P, 64, s) == 3
     # expert GEMMs: workspace missing
     assert L.moe_expert_gemm2(P, None, P, 64, 4, 64, 64, 1, P, None, P, 0, _null(), 256, s) == 3
