@@ -131,7 +131,8 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* top
  *   pair_to_row [T, k]: device int32 outputs
  *   workspace    device, >= moe_permute_workspace_size(T, k, E_loc) bytes, 256-aligned
  * Requires 0 <= e0, 1 <= E_loc, e0 + E_loc <= 65536, 1 <= k <= 32; d % 8 == 0 (bf16),
- * d % 4 == 0 (fp32), d % 128 == 0 (MXFP8). */
+ * d % 4 == 0 (fp32), d % 128 == 0 (MXFP8); N_cap = T * min(k, E_loc) <= 2^31 - 1 (int32
+ * row indices), else MOE_ERR_INVALID_ARG. */
 moe_status moe_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d,
                        const int32_t* topk_ids, const float* topk_probs, int k, int e0, int E_loc,
                        void* perm_x, uint8_t* perm_x_scale, int32_t* counts, int32_t* offsets,
@@ -276,9 +277,10 @@ moe_status moe_unpermute_combine(const void* Y2, const int32_t* pair_to_row, int
  *   y [T, d] (fp32 for MOE_F32, else bf16): device pointers.
  *   workspace device >= moe_layer_workspace_size(...) bytes, 256-byte aligned; it holds
  *   the routing table, the permutation maps, h and Y2, plus the permuted rows where a
- *   copy is made: bf16 layers feed GEMM1 by row gather, except when T * k / E >= 2048
- *   selects the CTA-pair GEMMs, which read a permuted copy; fp32 and MXFP8 layers copy
- *   (MXFP8 quantises while copying). */
+ *   copy is made: bf16 layers feed GEMM1 by row gather, except when the CTA-pair GEMM1
+ *   is chosen (moe_layer_gemm1_pairs), which reads a permuted copy; fp32 and MXFP8
+ *   layers copy (MXFP8 quantises while copying).
+ * Requires T * min(k, E_loc) <= 2^31 - 1 (int32 row indices), else MOE_ERR_INVALID_ARG. */
 moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0,
                              int E_loc, moe_dtype dtype, const void* Wgu_packed, const uint8_t* Wgu_scale,
                              const void* Wd_packed, const uint8_t* Wd_scale, void* y, void* workspace,
@@ -319,7 +321,8 @@ moe_status moe_get_device_error(void* workspace, moe_stream_t stream, int32_t* d
  *                      (zero for experts that received no token)
  *   workspace          device >= moe_layer_backward_workspace_size(T, d, f, k, E_loc) bytes,
  *                      256-byte aligned, error word initialised (moe_workspace_init)
- * Requires d % 8 == 0, f % 32 == 0; 16-byte aligned x, dy, dx, weights and gradients.  bf16 only. */
+ * Requires d % 8 == 0, f % 32 == 0; 16-byte aligned x, dy, dx, weights and gradients;
+ * T * min(k, E_loc) <= 2^31 - 1.  bf16 only. */
 moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
                               int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
                               const void* W_down, const void* WguT_packed, const void* gu_saved, void* dx,
