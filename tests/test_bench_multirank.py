@@ -48,3 +48,23 @@ def test_single_process_passthrough():
     import bench
     assert bench.max_over_ranks(7.0, "cpu") == 7.0
     assert bench.job_tokens_per_s(100, 1, 1.0) == 1e5
+
+
+def test_reference_arm_json_line_on_cpu():
+    """`bench.py --impl reference` runs the oracle on the host cores (no GPU) and prints
+    one JSON line with the contract's keys, its cpu_baseline and e2e equal to its value."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tiny_fp32", "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=300,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in j, key
+    assert j["impl"] == "reference" and j["config"]["workload"] == "tiny_fp32" and j["value"] > 0
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["value"] == j["value"]
+    assert j["e2e"]["value"] == j["value"] and j["e2e"]["h2d_bytes_per_step"] == 0
