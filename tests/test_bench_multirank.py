@@ -68,3 +68,21 @@ def test_reference_arm_json_line_on_cpu():
     assert j["impl"] == "reference" and j["config"]["workload"] == "tiny_fp32" and j["value"] > 0
     assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["value"] == j["value"]
     assert j["e2e"]["value"] == j["value"] and j["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_backward_floor_terms():
+    """The backward's per-kernel roofline terms for the bf16_e64 shape, by hand: the
+    weight-gradient kernels are HBM-bound by their fp32 outputs, the dx GEMM tensor-bound."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from synthetic import WORKLOADS
+    w = WORKLOADS["bf16_e64"]
+    pk = {"bf16_tflops": 1797.5, "hbm_gbs": 6484.3}
+    N, d, f = 32768, 2048, 1024
+    total, terms = bench.backward_floor(w, N, 64, pk)
+    bw, tf = 6484.3e9, 1797.5e12
+    assert abs(terms["wgrad_gate_up"] - (N * d * 2 + N * 2 * f * 2 + 64 * d * 2 * f * 4) / bw) < 1e-12
+    assert abs(terms["wgrad_down"] - (N * f * 2 + N * d * 2 + 64 * f * d * 4) / bw) < 1e-12
+    assert abs(terms["dx_gemm"] - 4.0 * N * d * f / tf) < 1e-12
+    assert abs(total - sum(terms.values())) < 1e-15
+    assert 650e-6 < total < 665e-6
