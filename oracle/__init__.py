@@ -205,3 +205,87 @@ def moe_backward(x, x_dtype: str, logits, dy, dy_dtype: str, k: int, e0: int, E_
         raise ValueError(f"oracle_moe_backward status {st}")
     out.update(dx=dx, dlogits=dl, dW_gate=dwg, dW_up=dwu, dW_down=dwd)
     return out
+
+
+# ----------------------------------------------------------------------------- MXFP8 backward
+def mx_dequantized(a, axis: int) -> np.ndarray:
+    """Values of ``a`` (fp64) after MXFP8 quantisation in 32-blocks along ``axis`` (the
+    rule of ``mx_quantize``); a length that is not a multiple of 32 is padded with zeros
+    (zeros never raise a block's amax) and the padding is dropped again."""
+    a = np.moveaxis(np.asarray(a, np.float64), axis, -1)
+    n = a.shape[-1]
+    pad = (-n) % 32
+    if pad:
+        a = np.concatenate([a, np.zeros(a.shape[:-1] + (pad,))], axis=-1)
+    K = a.shape[-1]
+    lead = int(np.prod(a.shape[:-1])) if a.ndim > 1 else 1
+    if lead == 0 or K == 0:
+        return np.moveaxis(a[..., :n], -1, axis)
+    codes, scales = mx_quantize(np.ascontiguousarray(a.reshape(lead, K)), "f64", (lead, K, 1))
+    vals = e4m3_decode(codes).reshape(lead, K // 32, 32) * np.exp2(scales.astype(np.float64) - 127.0)
+    return np.moveaxis(vals.reshape(a.shape)[..., :n], -1, axis)
+
+
+def _bf16_values(bits) -> np.ndarray:
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def moe_backward_mx(x, logits, dy, k: int, e0: int, E_loc: int, W_gate, W_up, W_down) -> dict:
+    """fp64 gradients of L = sum(dy * y) for the MXFP8 layer (bf16 bits in: x, dy [T, d];
+    W_gate, W_up [E_loc, d, f]; W_down [E_loc, f, d]; logits [T, E] fp32).
+
+    The forward is the MXFP8 layer's (x rows and the gate/up weights quantised along d).
+    Every backward GEMM reads its two operands MXFP8-quantised in 32-blocks along that
+    GEMM's own contraction axis ("Efficient MoE training for biological foundation
+    models", section "MXFP8 Precision Reduces Memory Footprint": 8-bit values with one
+    scale per 32 consecutive values, on Blackwell's MXFP8 GEMMs):
+      dh = dy W_down^T              dy rows and W_down along d
+      dx_row = dg W_gate^T + du W_up^T   dg, du rows and W_gate, W_up along f
+      dW_down = h^T dy_rows         h and the expert's dy rows along the expert's rows
+      dW_gate, dW_up = x_rows^T dg, du   x rows and dg / du along the expert's rows
+    (the weight gradients contract over tokens, so their operands are quantised
+    column-wise, each expert segment padded with zero rows to a multiple of 32).  The
+    ScaledSwiGLU backward and the router gradient are exact fp64 arithmetic:
+      du = p dh silu(g), dg = p dh u s (1 + g (1 - s)), dp = sum dh silu(g) u,
+      dlogit_j = p_j (dp_j - sum_i p_i dp_i) over the token's k slots (dp = 0 off-slice).
+    Returns dict(dx [T, d], dlogits [T, E], dW_gate, dW_up [E_loc, d, f], dW_down [E_loc, f, d]).
+    """
+    xv, dyv = _bf16_values(x), _bf16_values(dy)
+    Wg, Wu, Wd = (_bf16_values(w) for w in (W_gate, W_up, W_down))
+    lg = np.asarray(logits, np.float32)
+    T, d = xv.shape
+    E = lg.shape[1]
+    f = Wg.shape[2]
+    ids, probs = route_topk(lg, k)
+    P = permute(ids, e0, E_loc)
+    off, rst, slot = P["offsets"], P["row_src_token"], P["row_slot"]
+    # forward operands (GEMM1 contracts over d) and backward operands of the row-wise GEMMs
+    xq, Wgq, Wuq = mx_dequantized(xv, 1), mx_dequantized(Wg, 1), mx_dequantized(Wu, 1)
+    dyq, Wd_d = mx_dequantized(dyv, 1), mx_dequantized(Wd, 2)
+    Wg_f, Wu_f = mx_dequantized(Wg, 2), mx_dequantized(Wu, 2)
+    dx = np.zeros((T, d))
+    dp = np.zeros((T, k))
+    dWg, dWu, dWd = np.zeros((E_loc, d, f)), np.zeros((E_loc, d, f)), np.zeros((E_loc, f, d))
+    for e in range(E_loc):
+        rows = slice(int(off[e]), int(off[e + 1]))
+        t, j = rst[rows].astype(np.int64), slot[rows].astype(np.int64)
+        if t.size == 0:
+            continue
+        p = probs[t, j][:, None]
+        g, u = xq[t] @ Wgq[e], xq[t] @ Wuq[e]
+        s = 1.0 / (1.0 + np.exp(-g))
+        a = g * s
+        h = p * a * u
+        dh = dyq[t] @ Wd_d[e].T
+        du = p * dh * a
+        dg = p * dh * u * s * (1.0 + g * (1.0 - s))
+        dp[t, j] = (dh * a * u).sum(axis=1)
+        np.add.at(dx, t, mx_dequantized(dg, 1) @ Wg_f[e].T + mx_dequantized(du, 1) @ Wu_f[e].T)
+        dWd[e] = mx_dequantized(h, 0).T @ mx_dequantized(dyv[t], 0)
+        xr = mx_dequantized(xv[t], 0)
+        dWg[e] = xr.T @ mx_dequantized(dg, 0)
+        dWu[e] = xr.T @ mx_dequantized(du, 0)
+    dl = np.zeros((T, E))
+    mix = (probs * dp).sum(axis=1, keepdims=True)
+    np.add.at(dl, (np.arange(T)[:, None].repeat(k, 1), ids), probs * (dp - mix))
+    return dict(dx=dx, dlogits=dl, dW_gate=dWg, dW_up=dWu, dW_down=dWd)

@@ -113,3 +113,65 @@ def forward(x, logits, Wg, Wu, Wd, k: int, e0: int, mx: bool = False) -> np.ndar
                     h = mx_quantize_rows(p[j] * act[e])[2]
                     y[t] += h @ Wd[e]
     return y
+
+
+def _q(v: np.ndarray, axis: int) -> np.ndarray:
+    """Dequantised MXFP8 values of v in 32-blocks along ``axis`` (zero-padded to 32)."""
+    v = np.moveaxis(np.asarray(v, np.float64), axis, -1)
+    n = v.shape[-1]
+    pad = (-n) % 32
+    if pad:
+        v = np.concatenate([v, np.zeros(v.shape[:-1] + (pad,))], axis=-1)
+    return np.moveaxis(mx_quantize_rows(v)[2][..., :n], -1, axis)
+
+
+def backward_mx(x, logits, dy, Wg, Wu, Wd, k: int, e0: int):
+    """Gradients of sum(dy * y) for the MXFP8 layer, token by token (fp64 values in).
+
+    Same definition as the oracle's MXFP8 backward, reached another way: experts are
+    visited in id order and their tokens collected by a scan in ascending token order (no
+    permutation tables), the per-row backward is evaluated one token at a time, and the
+    weight gradients are accumulated as sums of per-token outer products of the
+    column-wise quantised operands.
+    """
+    x, dy = np.asarray(x, np.float64), np.asarray(dy, np.float64)
+    T, d = x.shape
+    E_loc, _, f = Wg.shape
+    E = logits.shape[1]
+    sel = [topk(logits[t], k) for t in range(T)]
+    xq, dyq = _q(x, 1), _q(dy, 1)
+    Wgq, Wuq, Wd_d, Wg_f, Wu_f = _q(Wg, 1), _q(Wu, 1), _q(Wd, 2), _q(Wg, 2), _q(Wu, 2)
+    dx, dlog = np.zeros((T, d)), np.zeros((T, E))
+    dp = np.zeros((T, k))
+    dWg, dWu, dWd = np.zeros((E_loc, d, f)), np.zeros((E_loc, d, f)), np.zeros((E_loc, f, d))
+    for e in range(E_loc):
+        members = [(t, list(sel[t][0]).index(e0 + e)) for t in range(T) if e0 + e in sel[t][0]]
+        if not members:
+            continue
+        H, DG, DU = [], [], []
+        for t, j in members:
+            p = sel[t][1][j]
+            g = np.array([xq[t] @ Wgq[e][:, n] for n in range(f)])
+            u = np.array([xq[t] @ Wuq[e][:, n] for n in range(f)])
+            s = 1.0 / (1.0 + np.exp(-g))
+            dh = np.array([dyq[t] @ Wd_d[e][n, :] for n in range(f)])
+            dg = p * dh * u * s * (1.0 + g * (1.0 - s))
+            du = p * dh * g * s
+            dp[t, j] = float(np.sum(dh * g * s * u))
+            dx[t] += _q(dg[None, :], 1)[0] @ Wg_f[e].T + _q(du[None, :], 1)[0] @ Wu_f[e].T
+            H.append(p * g * s * u)
+            DG.append(dg)
+            DU.append(du)
+        ts = [t for t, _ in members]
+        Hq, DYq = _q(np.array(H), 0), _q(dy[ts], 0)
+        Xq, DGq, DUq = _q(x[ts], 0), _q(np.array(DG), 0), _q(np.array(DU), 0)
+        for r in range(len(ts)):
+            dWd[e] += np.outer(Hq[r], DYq[r])
+            dWg[e] += np.outer(Xq[r], DGq[r])
+            dWu[e] += np.outer(Xq[r], DUq[r])
+    for t in range(T):
+        ids, p = sel[t]
+        mix = float(np.sum(p * dp[t]))
+        for j in range(k):
+            dlog[t, ids[j]] += p[j] * (dp[t, j] - mix)
+    return dict(dx=dx, dlogits=dlog, dW_gate=dWg, dW_up=dWu, dW_down=dWd)

@@ -76,3 +76,42 @@ def test_backward_structure():
         assert abs(g1["dlogits"][t].sum()) < 1e-12
         if not any(e0 <= i < e0 + E_loc for i in ids[t]):
             assert (g1["dx"][t] == 0.0).all()
+
+
+# ----------------------------------------------------------------------------- MXFP8 backward
+# The MXFP8 backward is not differentiable through its quantisers, so it is pinned by an
+# independent brute force of the same definition (oracle/brute.py: nearest-code quantiser,
+# experts collected by a token scan, per-token rows, per-token outer products for the
+# weight gradients) and by its distance to the unquantised backward.
+from synthetic import Workload, bf16_to_f32, gen_dy, gen_logits, gen_weights, gen_x  # noqa: E402
+from oracle import brute  # noqa: E402
+
+MX_BWD = [
+    Workload("mx_bwd_slice", 40, 64, 32, 8, 2, 2, 4, "mxfp8"),                    # non-local slots
+    Workload("mx_bwd_skew", 70, 96, 64, 6, 3, 0, 6, "mxfp8", ("normal", 0.5)),    # ragged segments
+]
+
+
+@pytest.mark.parametrize("w", MX_BWD, ids=[w.name for w in MX_BWD])
+def test_mx_backward_matches_brute_force(w):
+    x, lg, dy = gen_x(w), gen_logits(w), gen_dy(w)
+    Wg, Wu, Wd = gen_weights(w)
+    got = oracle.moe_backward_mx(x, lg, dy, w.k, w.e0, w.E_loc, Wg, Wu, Wd)
+    v = lambda a: bf16_to_f32(a).astype(np.float64)
+    ref = brute.backward_mx(v(x), lg, v(dy), v(Wg), v(Wu), v(Wd), w.k, w.e0)
+    for key in ref:
+        err = np.linalg.norm(got[key] - ref[key]) / np.linalg.norm(ref[key])
+        assert err <= 1e-12, (key, err)
+
+
+@pytest.mark.parametrize("w", MX_BWD, ids=[w.name for w in MX_BWD])
+def test_mx_backward_near_unquantised(w):
+    """Same gradients as the bf16 backward up to the E4M3 rounding of the GEMM operands:
+    relative L2 between 1 % and 15 % (quantisation happened, nothing larger broke)."""
+    x, lg, dy = gen_x(w), gen_logits(w), gen_dy(w)
+    Wg, Wu, Wd = gen_weights(w)
+    got = oracle.moe_backward_mx(x, lg, dy, w.k, w.e0, w.E_loc, Wg, Wu, Wd)
+    ref = oracle.moe_backward(x, "bf16", lg, dy, "bf16", w.k, w.e0, w.E_loc, "bf16", Wg, Wu, Wd)
+    for key in ("dx", "dlogits", "dW_gate", "dW_up", "dW_down"):
+        err = np.linalg.norm(got[key] - ref[key]) / np.linalg.norm(ref[key])
+        assert 0.01 <= err <= 0.15, (key, err)
