@@ -8,7 +8,9 @@ imports the CUDA library.
   (routing, permutation, scaled-SwiGLU expert FFN, combine, MXFP8 codec).
 * ``brute.py``: a second, independent numpy brute force (all experts evaluated densely,
   top-k by a full stable sort, quantiser by nearest-code search) used to pin the C++
-  oracle on tiny inputs.
+  oracle on tiny inputs, and the MXFP8 backward token by token.
+* ``moe_backward_mx`` (numpy over the C++ codec): the MXFP8 layer backward, every backward
+  GEMM operand quantised along that GEMM's contraction axis.
 
 Functions of this module are thin ctypes marshalling around the C++ oracle.
 """
