@@ -130,7 +130,7 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* top
  *   counts [E_loc], offsets [E_loc+1], row_src_token [N_cap], row_prob [N_cap] (fp32),
  *   pair_to_row [T, k]: device int32 outputs
  *   workspace    device, >= moe_permute_workspace_size(T, k, E_loc) bytes, 256-aligned
- * Requires 0 <= e0, 1 <= E_loc, e0 + E_loc <= 65536, 1 <= k <= 32; d % 8 == 0 (bf16),
+ * Requires 0 <= e0, 1 <= E_loc <= 1024, e0 + E_loc <= 65536, 1 <= k <= 32; d % 8 == 0 (bf16),
  * d % 4 == 0 (fp32), d % 128 == 0 (MXFP8); N_cap = T * min(k, E_loc) <= 2^31 - 1 (int32
  * row indices), else MOE_ERR_INVALID_ARG. */
 moe_status moe_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d,
@@ -152,7 +152,8 @@ size_t moe_permute_workspace_size(int T, int k, int E_loc);
  * allocated or freed.
  *   Limit: moe_permute_workspace_size(T, k, E_loc) <= 1 MiB, i.e. ceil(T / 256) * E_loc
  *   <= about 260,000 (T <= 65,024 tokens at E_loc = 1024, T <= 260,864 at E_loc <= 256);
- *   larger inputs return MOE_ERR_WORKSPACE and launch nothing.
+ *   larger inputs return MOE_ERR_WORKSPACE and launch nothing.  Arguments are checked as
+ *   in moe_permute first (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED before the size).
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call before any
  *   stream capture.  Every call shares the one array: calls whose kernels may overlap on

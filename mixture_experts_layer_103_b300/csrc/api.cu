@@ -57,6 +57,7 @@ cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dty
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;  // routed rows are int32 indices
 constexpr int kMaxDevices = 64;
+constexpr int kMaxExpertId = 65535;  // e0 + E_loc <= 65536 (moe_permute's contract)
 
 int num_sms() {
   static int cache[kMaxDevices] = {0};
@@ -323,15 +324,18 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* top
 
 size_t moe_permute_workspace_size(int T, int k, int E_loc) {
   (void)k;
-  if (T < 0 || E_loc < 1) return 0;
+  if (T < 0 || E_loc < 1 || E_loc > 1024) return 0;
   return sizeof(WsHeader) + permute_ws_bytes(T, E_loc);
 }
 
-static moe_status check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d, const void* ids,
-                                const void* probs, int k, int e0, int E_loc, const void* perm_x, const void* perm_sf,
-                                const void* counts, const void* offsets, const void* rst, const void* rp,
-                                const void* p2r) {
-  if (T < 0 || d <= 0 || k < 1 || k > 32 || e0 < 0 || E_loc < 1 || E_loc > 1024 || e0 > (1 << 30))
+}  // extern "C"
+
+// Argument checks of moe_permute (also run first by moe_permute_noalloc).
+moe_status moe::check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d, const void* ids,
+                              const void* probs, int k, int e0, int E_loc, const void* perm_x, const void* perm_sf,
+                              const void* counts, const void* offsets, const void* rst, const void* rp,
+                              const void* p2r) {
+  if (T < 0 || d <= 0 || k < 1 || k > 32 || e0 < 0 || E_loc < 1 || E_loc > 1024 || e0 > kMaxExpertId + 1 - E_loc)
     return MOE_ERR_INVALID_ARG;
   if (n_cap_of(T, k, E_loc) > kMaxRows) return MOE_ERR_INVALID_ARG;  // int32 rows and offsets
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
@@ -346,6 +350,8 @@ static moe_status check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm
   if (T > 0 && (!aligned16(x) || (perm_x && !aligned16(perm_x)))) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
+
+extern "C" {
 
 moe_status moe_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d, const int32_t* topk_ids,
                        const float* topk_probs, int k, int e0, int E_loc, void* perm_x, uint8_t* perm_x_scale,

@@ -22,15 +22,17 @@
 //               thread) output (GEMM1)
 // CTAs run in clusters of two.  The static scheduler hands out units of two tiles, one
 // per CTA of a cluster: while an expert has two m-tiles left, a unit is the pair of
-// m-tiles (m, m + 1) against one n-tile, and each CTA loads half of the shared weight
-// tile and multicasts it to both (half the L2 reads of B, the operand whose feed limits
-// the mainloop); an expert's odd last m-tile forms units of two n-tiles, each CTA loading
-// its own B.  m-tiles are 128-row slices of each expert's segment
+// m-tiles (m, m + 1) against one n-tile, so both CTAs stream the same weight tile at the
+// same time (the second read of each weight box is an L2 hit); an expert's odd last
+// m-tile forms units of two n-tiles.  Every CTA loads all of its own operands with plain
+// TMA loads into its own shared memory (no cross-CTA copies, so the kernel is the same on
+// any number of GPUs).  m-tiles are 128-row slices of each expert's segment
 // [offsets[e], offsets[e+1]), numbered in expert order, so experts with no tokens cost
 // nothing and their weights are never read.  Rows of a tile past its expert's segment are
 // computed and discarded.  Both CTAs of a cluster consume the same sequence of pipeline
-// stages, and a stage is refilled only when both have finished with it (the MMA issuers
-// commit to the empty barriers of both CTAs).
+// stages in lockstep: a stage is refilled only when both have finished with it (each MMA
+// issuer's commit arrives on the empty barriers of both CTAs), which keeps the two weight
+// streams of a unit within a few k-blocks of each other.
 // Every wait is bounded; on a timeout the kernel records MOE_ERR_TIMEOUT in the device
 // error word, drains its own copies and MMAs and exits.
 #include <cudaTypedefs.h>
@@ -69,7 +71,7 @@ struct GemmSmem {
 };
 
 // Units (tile pairs) of a launch with n-tile count nt: an expert with M m-tiles gives
-// (M / 2) * nt multicast units plus ceil(nt / 2) units for an odd last m-tile.
+// (M / 2) * nt shared-weight units plus ceil(nt / 2) units for an odd last m-tile.
 // mt_total = total m-tiles, odd = experts with an odd m-tile count.
 __device__ __forceinline__ long unit_count(int mt_total, int odd, int nt) {
   return static_cast<long>((mt_total - odd) / 2) * nt + static_cast<long>(odd) * ((nt + 1) / 2);
@@ -139,7 +141,7 @@ __device__ __forceinline__ void build_unit_tables(const int32_t* __restrict__ of
 }
 
 // The tile CTA `rank` of a cluster computes in unit u.  shared_b: both CTAs use the same
-// weight tile (multicast halves); valid = false only for the idle half of a unit whose
+// weight tile; valid = false only for the idle half of a unit whose
 // expert has an odd m-tile and an odd n-tile count: that CTA recomputes its partner's tile
 // and stores nothing.
 struct UnitTile {
@@ -185,10 +187,9 @@ __device__ __forceinline__ UnitTile decode_unit(int u, int rank, int nt, int bn,
   return r;
 }
 
-// B operand maps with box heights 256, 128, 64 and 32 rows: a full tile of each width,
-// and the half tiles a CTA loads for multicast.
+// B operand maps with box heights 256, 128 and 64 rows: a full tile of each width.
 struct BMaps {
-  CUtensorMap b256, b128, b64, b32;
+  CUtensorMap b256, b128, b64;
 };
 
 template <bool MX, int EPI, bool GATHER>
@@ -238,13 +239,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATH
   if (warp == 2) build_unit_tables(g.offsets, g.E_loc, s_off, s_mtp, s_odd);
   ptx::tc_fence_before();
   __syncthreads();
-  ptx::cluster_sync();  // the peer's barriers exist before any multicast or remote commit
+  ptx::cluster_sync();  // the peer's barriers exist before any remote commit
   ptx::tc_fence_after();
 
   const uint32_t tmem_base = *tmem_slot;
   const int BN = choose_bn(s_mtp[g.E_loc], s_odd[g.E_loc], g.n_out, clusters, MX);
   const CUtensorMap* tmb = BN == 256 ? &tmB.b256 : BN == 128 ? &tmB.b128 : &tmB.b64;
-  const CUtensorMap* tmb_half = BN == 256 ? &tmB.b128 : BN == 128 ? &tmB.b64 : &tmB.b32;
   const int stage_bytes = C::A_BYTES + BN * kRowBytes;  // multiple of 1024
   const int stages = min(C::MAX_STAGES, C::PIPE_BYTES / stage_bytes);
   const int sf_cols = MX ? (BN / 128 + 1) * 4 : 0;       // SFA 4 columns + SFB 4 per 128 rows
@@ -258,7 +258,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATH
     if (lane == 0) {
       // ------------------------------------------------------------------ TMA producer
       ptx::prefetch_tmap(tmb);
-      ptx::prefetch_tmap(tmb_half);
       int s = 0;
       uint32_t ph = 0;
       int64_t issued = 0;
@@ -275,11 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATH
           // in row-gather mode the gather warps fill A (and its scales) themselves
           ptx::mbar_arrive_expect_tx(fb, (GATHER ? BN * kRowBytes : stage_bytes) + (MX ? (GATHER ? 0 : 512) + sfb_bytes : 0));
           if (!GATHER) ptx::tma_load_3d(st_addr, &tmA, fb, kb * C::BK, tl.row0, 0);
-          if (ut.shared_b)  // this CTA's half of the weight tile, to both CTAs
-            ptx::tma_load_3d_mc(st_addr + C::A_BYTES + rank * (BN / 2) * kRowBytes, tmb_half, fb, kb * C::BK,
-                                tl.n0 + rank * (BN / 2), tl.e, both);
-          else
-            ptx::tma_load_3d(st_addr + C::A_BYTES, tmb, fb, kb * C::BK, tl.n0, tl.e);
+          ptx::tma_load_3d(st_addr + C::A_BYTES, tmb, fb, kb * C::BK, tl.n0, tl.e);
           if constexpr (MX) {
             const int kg = g.K / 128;
             const uint32_t sf_addr = sbase + C::OFF_SF + s * C::SF_STAGE_BYTES;
@@ -335,7 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATH
               ptx::mma_bf16(d_tmem, ptx::sdesc_sw128(a_addr + k * 32), ptx::sdesc_sw128(b_addr + k * 32), idesc,
                             (kb | k) != 0);
           }
-          ptx::mma_commit_mc(empty_bar(s), both);  // frees the stage (in both CTAs) once read
+          ptx::mma_commit_mc(empty_bar(s), both);  // frees the stage in both CTAs (lockstep) once read
           if (++s == stages) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
@@ -515,7 +510,6 @@ static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B
   if (!make_operand_map(&tb.b256, B, MX, g.K, g.n_out, g.E_loc, 256)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b128, B, MX, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb.b64, B, MX, g.K, g.n_out, g.E_loc, 64)) return cudaErrorInvalidValue;
-  if (!make_operand_map(&tb.b32, B, MX, g.K, g.n_out, g.E_loc, 32)) return cudaErrorInvalidValue;
   OutMaps tmo;
   memset(&tmo, 0, sizeof(tmo));
   if (!MX && !make_out_maps(&tmo, g)) return cudaErrorInvalidValue;

@@ -67,6 +67,11 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Host-side argument checks of moe_permute, shared by its workspace-free variant.
+moe_status check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d, const void* ids,
+                         const void* probs, int k, int e0, int E_loc, const void* perm_x, const void* perm_sf,
+                         const void* counts, const void* offsets, const void* rst, const void* rp, const void* p2r);
+
 // ---- bf16 / fp32 helpers --------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }

@@ -51,6 +51,11 @@ extern "C" moe_status moe_permute_noalloc(const void* x, moe_dtype x_dtype, moe_
                                           void* perm_x, uint8_t* perm_x_scale, int32_t* counts, int32_t* offsets,
                                           int32_t* row_src_token, float* row_prob, int32_t* pair_to_row,
                                           moe_stream_t stream) {
+  // the arguments first, so an out-of-range size is reported as such and never reaches
+  // the workspace arithmetic
+  const moe_status s = moe::check_permute(x, x_dtype, perm_dtype, T, d, topk_ids, topk_probs, k, e0, E_loc, perm_x,
+                                          perm_x_scale, counts, offsets, row_src_token, row_prob, pair_to_row);
+  if (s != MOE_OK) return s;
   const size_t need = moe_permute_workspace_size(T, k, E_loc);
   if (need == 0) return MOE_ERR_INVALID_ARG;
   if (need > moe::kStaticPermuteScratchBytes) return MOE_ERR_WORKSPACE;  // beyond the static array

@@ -372,8 +372,9 @@ cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtyp
                                                       : perm_count_kernel<kPermTileLarge>,
                                dim3(n_tiles), dim3(tile), E_loc * 4, st, ids, T, k, e0, E_loc, n_tiles, w.tile_counts);
     if (e != cudaSuccess) return e;
-  } else {
-    cudaMemsetAsync(w.tile_counts, 0, static_cast<size_t>(n_tiles) * E_loc * 4, st);
+  } else {  // an empty batch: the scan still writes zero counts and offsets
+    cudaError_t e = cudaMemsetAsync(w.tile_counts, 0, static_cast<size_t>(n_tiles) * E_loc * 4, st);
+    if (e != cudaSuccess) return e;
   }
   cudaError_t e = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, st, w.tile_counts, n_tiles, E_loc, counts,
                              offsets, w.mtile_base);

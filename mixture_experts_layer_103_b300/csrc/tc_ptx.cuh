@@ -223,17 +223,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ---------------------------------------------------------------------------- multicast
-// TMA load delivered to the same shared-memory offset in every CTA of `cta_mask` (a
-// cluster); each destination CTA's mbarrier at offset `bar` counts the bytes it receives.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::
-          "r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
-      : "memory");
-}
+// ---------------------------------------------------------------------------- clusters
 // Arrive on the barrier at offset `bar` in every CTA of `cta_mask` once this thread's
 // previously issued (single-CTA) tcgen05 operations have completed.
 __device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {

@@ -95,6 +95,17 @@ def test_validation_before_any_launch(lib):
                          s) == 3
     assert L.moe_permute(P, 1, 1, 16, 60, P, P, 2, 0, 8, P, None, P, P, P, P, P, P, 1 << 20, s) == 2
     assert L.moe_permute(P, 1, 2, 16, 64, P, P, 2, 0, 8, P, None, P, P, P, P, P, P, 1 << 20, s) == 1
+    # permute: local expert ids beyond 65535 (e0 + E_loc > 65536), E_loc > 1024
+    assert L.moe_permute(P, 1, 1, 16, 64, P, P, 2, 65536 - 7, 8, P, None, P, P, P, P, P, P, 1 << 20, s) == 1
+    assert L.moe_permute(P, 1, 1, 16, 64, P, P, 2, 65536 - 8, 8, P, None, P, P, P, P, P, _null(), 0, s) == 3
+    assert L.moe_permute(P, 1, 1, 16, 64, P, P, 2, 0, 2048, P, None, P, P, P, P, P, P, 1 << 20, s) == 1
+    assert L.moe_permute_workspace_size(16, 2, 2048) == 0
+    # workspace-free permute: the arguments are checked before its scratch size, so an
+    # out-of-range E_loc or e0 is an invalid argument, not a workspace overflow
+    assert L.moe_permute_noalloc(P, 1, 1, 16, 64, P, P, 2, 0, 2048, P, None, P, P, P, P, P, s) == 1
+    assert L.moe_permute_noalloc(P, 1, 1, 16, 64, P, P, 2, 65530, 8, P, None, P, P, P, P, P, s) == 1
+    assert L.moe_permute_noalloc(P, 1, 1, 16, 64, P, P, 33, 0, 8, P, None, P, P, P, P, P, s) == 1
+    assert L.moe_permute_noalloc(P, 1, 1, 1 << 20, 64, P, P, 8, 0, 1024, P, None, P, P, P, P, P, s) == 3
     # grouped MLP: E_loc out of range, unsupported dtype, workspace too small
     assert L.moe_grouped_mlp(P, None, P, P, 64, 0, 64, 64, 1, P, None, P, None, P, 0, P, 1 << 20, s) == 1
     assert L.moe_grouped_mlp(P, None, P, P, 64, 4, 64, 64, 7, P, None, P, None, P, 0, P, 1 << 20, s) == 2
