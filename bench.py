@@ -57,6 +57,11 @@ def parse_args():
                    help="backward: time moe_layer_backward (bf16 workloads) instead of the forward step")
     p.add_argument("--no-gather", action="store_true",
                    help="feed GEMM1 from a permuted copy of x instead of reading the token rows (row gather)")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="time the headline workload only (default: also every other configuration, "
+                        "reported under 'workloads')")
+    p.add_argument("--sweep-cpu-seconds", type=float, default=3.0,
+                   help="budget of the CPU-oracle sample of each swept configuration")
     return p.parse_args()
 
 
@@ -305,25 +310,26 @@ def backward_floor(w, N, nonempty, pk):
     return sum(terms.values()), terms
 
 
-def run_ours(args, w):
+SWEEP = ["tiny_fp32", "ep8_zipf_T512", "ep64_T2048", "ep64_T8192", "ep64_T32768", "mxfp8_ep8_zipf_T8192",
+         "mxfp8_ep64_T8192"]
+
+
+def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
+    """Time K steps of one workload (one CUDA-graph replay) and compute its rooflines.
+
+    headline: also the eager and end-to-end legs.  Returns a dict of results."""
     import torch
-    import torch.distributed as dist
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    import mixture_experts_layer_103_b300 as moe
-
-    pk, pk_kind = peaks()
     wr = w.replace(seed=w.seed + rank)  # each rank its own token batch; same expert weights
     x, lg = gen_x(wr), gen_logits(wr)
     Wg, Wu, Wd = gen_weights(w)
     xd, lgd = to_dev(x), to_dev(lg)
+    del x, lg
     wg_d, wu_d, wd_d = to_dev(Wg), to_dev(Wu), to_dev(Wd)
+    del Wg, Wu, Wd
     pw = moe.moe_pack_weights(wg_d, wu_d, wd_d, w.dtype)
     torch.cuda.synchronize()
-    del wg_d, wu_d, wd_d, Wg, Wu, Wd
+    del wg_d, wu_d, wd_d
     torch.cuda.empty_cache()
 
     T, d, k, E_loc, e0 = w.T, w.d, w.k, w.E_loc, w.e0
@@ -384,7 +390,7 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     err = moe.moe_get_device_error(ws_g)
     if err != 0:
-        raise RuntimeError(f"device error {err} during warm-up")
+        raise RuntimeError(f"{w.name}: device error {err} during warm-up")
     offs = P["offsets"].cpu().numpy().astype(np.int64)
     N = int(offs[-1])
     nonempty = int((np.diff(offs) > 0).sum())
@@ -422,6 +428,7 @@ def run_ours(args, w):
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     if rank == 0:
@@ -437,7 +444,7 @@ def run_ours(args, w):
     clk = clocks.stop() if rank == 0 else None
     err = moe.moe_get_device_error(ws_g)
     if err != 0:
-        raise RuntimeError(f"device error {err} in the timed region")
+        raise RuntimeError(f"{w.name}: device error {err} in the timed region")
     del graph
     region_ms = region0.elapsed_time(region1)
     gemm1_ms = statistics.mean(marks[i][2].elapsed_time(marks[i][3]) for i in range(args.steps))
@@ -452,17 +459,18 @@ def run_ours(args, w):
                for j, nm in enumerate(names)}
     kern_ms["gemm1_swiglu_timed_region"] = gemm1_ms
     del bgraph
-    # eager (one Python call per step), for reference only: includes host launch overhead
-    n_eager = min(args.steps, 50)
-    ev_e = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_eager)]
-    for i in range(n_eager):
-        step(ev_e[i])
-    torch.cuda.synchronize()
-    eager_ms = statistics.mean(ev_e[i][0].elapsed_time(ev_e[i][-1]) for i in range(n_eager))
+    eager_ms = None
+    if headline:
+        # eager (one Python call per step), for reference only: includes host launch overhead
+        n_eager = min(args.steps, 50)
+        ev_e = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_eager)]
+        for i in range(n_eager):
+            step(ev_e[i])
+        torch.cuda.synchronize()
+        eager_ms = statistics.mean(ev_e[i][0].elapsed_time(ev_e[i][-1]) for i in range(n_eager))
 
     total_ms = max_over_ranks(total_ms, "cuda")
     ms_per_step = total_ms / args.steps
-    value = job_tokens_per_s(T, world, ms_per_step)
 
     # ---- roofline of the dominant kernel and of the whole layer
     bf = layer_bytes_flops(w, N, nonempty, n_tok_local)
@@ -496,105 +504,148 @@ def run_ours(args, w):
 
     # ---- end to end through moe_layer_forward with host buffers
     e2e = None
-    if not args.no_e2e:
-        # Steps are pipelined over three streams with triple-buffered device inputs and
-        # outputs: step i's host->device copy and step i-1's device->host read overlap
-        # step i-1's / i's compute.  Every step still copies its own inputs in and its
-        # result out inside the timed region.
-        x_pin = torch.empty(xd.shape, dtype=xd.dtype).pin_memory()
-        x_pin.copy_(xd.cpu())
-        lg_pin = torch.empty(lgd.shape, dtype=lgd.dtype).pin_memory()
-        lg_pin.copy_(lgd.cpu())
-        nbuf = 3
-        y_pin = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(nbuf)]
-        xb = [torch.empty_like(xd) for _ in range(nbuf)]
-        lgb = [torch.empty_like(lgd) for _ in range(nbuf)]
-        yb = [torch.empty_like(y) for _ in range(nbuf)]
-        ws_layer = moe.workspace(moe.moe_layer_workspace_size(T, d, w.f, w.E, k, E_loc, w.dtype))
-        s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        ev_in = [torch.cuda.Event() for _ in range(nbuf)]
-        ev_comp = [torch.cuda.Event() for _ in range(nbuf)]
-        ev_out = [torch.cuda.Event() for _ in range(nbuf)]
-        for b_ in range(nbuf):  # start with every buffer free
+    if headline and not args.no_e2e:
+        e2e = e2e_leg(moe, args, w, xd, lgd, y, pw, flush, world)
+    # route 1, permute 3 (+1 copy or MXFP8 per-token quantisation), GEMM1, GEMM2, combine
+    launches_per_step = 1 + 3 + (0 if gather and not mx else 1) + 3
+    return dict(value=job_tokens_per_s(T, world, ms_per_step), ms_per_step=ms_per_step, roof=roof, layer=layer,
+                kern_ms=kern_ms, region_ms=region_ms, gather=gather, eager_ms=eager_ms, e2e=e2e, clocks=clk,
+                launches_per_step=launches_per_step)
+
+
+def e2e_leg(moe, args, w, xd, lgd, y, pw, flush, world):
+    """The same metric end to end through moe_layer_forward with pinned host buffers."""
+    import torch
+    T, d, k, E_loc, e0 = w.T, w.d, w.k, w.E_loc, w.e0
+    # Steps are pipelined over three streams with triple-buffered device inputs and
+    # outputs: step i's host->device copy and step i-1's device->host read overlap
+    # step i-1's / i's compute.  Every step still copies its own inputs in and its
+    # result out inside the timed region.
+    x_pin = torch.empty(xd.shape, dtype=xd.dtype).pin_memory()
+    x_pin.copy_(xd.cpu())
+    lg_pin = torch.empty(lgd.shape, dtype=lgd.dtype).pin_memory()
+    lg_pin.copy_(lgd.cpu())
+    nbuf = 3
+    y_pin = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(nbuf)]
+    xb = [torch.empty_like(xd) for _ in range(nbuf)]
+    lgb = [torch.empty_like(lgd) for _ in range(nbuf)]
+    yb = [torch.empty_like(y) for _ in range(nbuf)]
+    ws_layer = moe.workspace(moe.moe_layer_workspace_size(T, d, w.f, w.E, k, E_loc, w.dtype))
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_comp = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+    for b_ in range(nbuf):  # start with every buffer free
+        ev_comp[b_].record(s_comp)
+        ev_out[b_].record(s_out)
+
+    def e2e_step(i):
+        b_ = i % nbuf
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_comp[b_])   # step i-nbuf has finished reading this input buffer
+            xb[b_].copy_(x_pin, non_blocking=True)
+            lgb[b_].copy_(lg_pin, non_blocking=True)
+            ev_in[b_].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev_in[b_])
+            s_comp.wait_event(ev_out[b_])  # step i-nbuf's result has left this output buffer
+            if flush is not None:
+                flush.zero_()
+            moe.moe_layer_forward(xb[b_], lgb[b_], w.E, k, e0, pw, y=yb[b_], ws=ws_layer)
             ev_comp[b_].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b_])
+            y_pin[b_].copy_(yb[b_], non_blocking=True)
             ev_out[b_].record(s_out)
 
-        def e2e_step(i):
-            b_ = i % nbuf
-            with torch.cuda.stream(s_in):
-                s_in.wait_event(ev_comp[b_])   # step i-nbuf has finished reading this input buffer
-                xb[b_].copy_(x_pin, non_blocking=True)
-                lgb[b_].copy_(lg_pin, non_blocking=True)
-                ev_in[b_].record(s_in)
-            with torch.cuda.stream(s_comp):
-                s_comp.wait_event(ev_in[b_])
-                s_comp.wait_event(ev_out[b_])  # step i-nbuf's result has left this output buffer
-                if flush is not None:
-                    flush.zero_()
-                moe.moe_layer_forward(xb[b_], lgb[b_], w.E, k, e0, pw, y=yb[b_], ws=ws_layer)
-                ev_comp[b_].record(s_comp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[b_])
-                y_pin[b_].copy_(yb[b_], non_blocking=True)
-                ev_out[b_].record(s_out)
-
-        for i in range(3):
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    n2 = args.e2e_steps or max(3, args.steps // 4)
+    # the n2 steps (copies, layer calls, event dependencies on three streams) are captured
+    # once as a CUDA graph and replayed inside the timed region, like the device-only steps
+    ge = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(ge, stream=cap):
+        for st_ in (s_in, s_comp, s_out):
+            st_.wait_stream(cap)
+        for b_ in range(nbuf):
+            ev_comp[b_].record(s_comp)
+            ev_out[b_].record(s_out)
+        for i in range(n2):
             e2e_step(i)
-        torch.cuda.synchronize()
-        n2 = args.e2e_steps or max(3, args.steps // 4)
-        # the n2 steps (copies, layer calls, event dependencies on three streams) are captured
-        # once as a CUDA graph and replayed inside the timed region, like the device-only steps
-        ge = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream()
-        cap.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.graph(ge, stream=cap):
-            for st_ in (s_in, s_comp, s_out):
-                st_.wait_stream(cap)
-            for b_ in range(nbuf):
-                ev_comp[b_].record(s_comp)
-                ev_out[b_].record(s_out)
-            for i in range(n2):
-                e2e_step(i)
-            for st_ in (s_in, s_comp, s_out):
-                cap.wait_stream(st_)
-        ge.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        ge.replay()
-        b.record()
-        torch.cuda.synchronize()
-        assert moe.moe_get_device_error(ws_layer) == 0
-        ms = a.elapsed_time(b) / n2
-        x_pin_bytes = x_pin.numel() * x_pin.element_size()
-        e2e = {"value": T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
-               "h2d_bytes_per_step": int(x_pin_bytes + lg_pin.numel() * 4),
-               "d2h_bytes_per_step": int(y_pin[0].numel() * y_pin[0].element_size()), "steps": n2,
-               "entry_point": "moe_layer_forward",
-               "pipelining": "copies of neighbouring steps overlap compute (3 streams, 3 buffers), "
-                             "the steps replayed as one CUDA graph"}
+        for st_ in (s_in, s_comp, s_out):
+            cap.wait_stream(st_)
+    ge.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    ge.replay()
+    b.record()
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws_layer) == 0
+    ms = a.elapsed_time(b) / n2
+    x_pin_bytes = x_pin.numel() * x_pin.element_size()
+    return {"value": T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(x_pin_bytes + lg_pin.numel() * 4),
+            "d2h_bytes_per_step": int(y_pin[0].numel() * y_pin[0].element_size()), "steps": n2,
+            "entry_point": "moe_layer_forward",
+            "pipelining": "copies of neighbouring steps overlap compute (3 streams, 3 buffers), "
+                          "the steps replayed as one CUDA graph"}
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import mixture_experts_layer_103_b300 as moe
+
+    pk, pk_kind = peaks()
+    R = measure(moe, args, w, pk, pk_kind, rank, world, local, headline=True)
+    torch.cuda.empty_cache()
+    # every other configuration of the pages' workloads, timed the same way in this process
+    # (one rank: the sweep documents per-config kernel quality, the headline line scales)
+    sweep = {}
+    if not args.no_sweep and world == 1:
+        for name in SWEEP:
+            if name == w.name:
+                continue
+            ws_ = WORKLOADS[name]
+            r = measure(moe, args, ws_, pk, pk_kind, rank, world, local, headline=False)
+            torch.cuda.empty_cache()
+            cpu_ws = None if args.no_cpu_baseline else cpu_baseline(ws_, args.sweep_cpu_seconds)
+            sweep[name] = {"value": r["value"], "unit": "tokens/s", "ms_per_step": r["ms_per_step"],
+                           "dtype": ws_.dtype, "config": workload_config(ws_), "roofline": r["roof"],
+                           "layer": r["layer"], "kernels_us": {n: 1e3 * v for n, v in r["kern_ms"].items()},
+                           "gemm1_operand": "token rows gathered in the kernel" if r["gather"]
+                           else "permuted copy of x", "gpu_launches": r["launches_per_step"] * args.steps,
+                           "clocks": r["clocks"], "cpu_baseline": cpu_ws}
 
     if world > 1:
         dist.barrier()
     if rank != 0:
         dist.destroy_process_group()
         return
-    # route 1, permute 3 (+1 copy or MXFP8 per-token quantisation), GEMM1, GEMM2, combine
-    launches_per_step = 1 + 3 + (0 if gather and not mx else 1) + 3
     cpu = None if args.no_cpu_baseline else cpu_baseline(w, args.cpu_seconds)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": R["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": R["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "mxfp8": "e4m3+e8m0 (mxfp8)"}[w.dtype],
         "data": "synthetic (seeded; shapes of the pages' workloads)", "config": workload_config(w),
-        "roofline": roof, "layer": layer, "kernels_us": {n: 1e3 * v for n, v in kern_ms.items()},
-        "timed_region_ms": region_ms,
-        "gemm1_operand": "token rows gathered in the kernel" if gather else "permuted copy of x",
+        "roofline": R["roof"], "layer": R["layer"], "kernels_us": {n: 1e3 * v for n, v in R["kern_ms"].items()},
+        "timed_region_ms": R["region_ms"],
+        "gemm1_operand": "token rows gathered in the kernel" if R["gather"] else "permuted copy of x",
         "timing": ("one CUDA-graph replay of the K steps (region events; with an L2 flush, the sum of the steps' "
                    "own event intervals); GEMM1 bracketed by event nodes in the timed graph; kernels_us from a "
                    "separate graph with events between all kernels"),
-        "eager_ms_per_step": eager_ms, "e2e": e2e, "cpu_baseline": cpu,
-        "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+        "eager_ms_per_step": R["eager_ms"], "e2e": R["e2e"], "cpu_baseline": cpu,
+        "gpu_launches": R["launches_per_step"] * args.steps, "clocks": R["clocks"],
+        "workloads": sweep,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -324,8 +324,9 @@ FULL = ["tiny_fp32", "bf16_e64", "ep8_zipf_T512", "ep64_T2048", "ep64_T8192", "e
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled(moe, name):
-    """Full workload through moe_layer_forward; routing/permutation checked for every token,
-    the output on a seeded sample of tokens against the oracle."""
+    """Full workload through moe_layer_forward; routing and the whole permutation (counts,
+    offsets, pair_to_row, row_src_token, row_prob) checked bit for bit for every token, the
+    output on a seeded sample of tokens against the oracle."""
     w = WORKLOADS[name]
     x, lg = gen_x(w), gen_logits(w)
     Wg, Wu, Wd = gen_weights(w)
@@ -337,6 +338,20 @@ def test_full_size_sampled(moe, name):
     assert moe.moe_get_device_error(ws) == 0
     oids, _ = oracle.route_topk(lg, w.k)
     np.testing.assert_array_equal(ids.cpu().numpy(), oids)
+    # the permutation maps of the layer's own kernels (moe_permute, maps only) at full size
+    probs_d = torch.empty(w.T, w.k, dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(lgd, w.k, topk_ids=ids, topk_probs=probs_d)
+    P = moe.moe_permute(xd, ids, probs_d, w.e0, w.E_loc, "f32" if w.dtype == "f32" else "bf16", maps_only=True)
+    torch.cuda.synchronize()
+    O = oracle.permute(oids, w.e0, w.E_loc)
+    N = O["N"]
+    np.testing.assert_array_equal(P["counts"].cpu().numpy(), O["counts"])
+    np.testing.assert_array_equal(P["offsets"].cpu().numpy(), O["offsets"])
+    np.testing.assert_array_equal(P["pair_to_row"].cpu().numpy(), O["pair_to_row"])
+    np.testing.assert_array_equal(P["row_src_token"].cpu().numpy()[:N], O["row_src_token"])
+    np.testing.assert_array_equal(P["row_prob"].cpu().numpy()[:N],
+                                  probs_d.cpu().numpy()[O["row_src_token"], O["row_slot"]])
+    del P
     tok = sample_tokens(w, 48 if w.T > 64 else w.T)
     # always include tokens with a local expert so the sample is not all zeros
     local = np.where(((oids >= w.e0) & (oids < w.e0 + w.E_loc)).any(1))[0]

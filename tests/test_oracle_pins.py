@@ -335,3 +335,36 @@ def test_mx_scale_rule():
     bc, bs, _ = brute.mx_quantize_rows(a)
     np.testing.assert_array_equal(bc, codes.reshape(a.shape))
     np.testing.assert_array_equal(bs[:, 0], scales)
+
+
+# ----------------------------------------------------------------------------- MXFP8 down projection
+@pytest.mark.parametrize("w_dtype", ["e4m3", "bf16"])
+def test_down_proj_mx_matches_brute(w_dtype):
+    """oracle.down_proj_mx (GEMM2 of given MXFP8 h rows) against numpy: the h codes decoded
+    from the E4M3 bit fields (brute force's table) times 2^(s - 127) per 32-block along f,
+    multiplied by W_down of the row's expert (E4M3 codes decoded the same way with their
+    per-column scales along f, or exact bf16 values); a row with an out-of-range expert is
+    zero.  A wrong block index, a transposed W_down or a dropped scale fails it."""
+    rng = np.random.default_rng(11)
+    E_loc, d, f, n = 3, 64, 96, 40
+    codes = rng.integers(0, 256, size=(n, f)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x11          # no NaN codes
+    scales = rng.integers(120, 135, size=(n, f // 32)).astype(np.uint8)
+    row_expert = rng.integers(0, E_loc, size=n).astype(np.int32)
+    row_expert[[3, 17]] = -1                       # not a local row: zero output
+    h = brute.e4m3_value(codes) * np.repeat(np.exp2(scales.astype(np.float64) - 127.0), 32, axis=1)
+    Wd32 = (rng.standard_normal((E_loc, f, d)) / np.sqrt(f)).astype(np.float32)
+    if w_dtype == "bf16":
+        Wd = bf16_bits(Wd32)
+        Wd_val = bf16_to_f32(Wd).astype(np.float64)
+        Wd_scale = None
+    else:
+        Wd, Wd_scale = oracle.mx_quantize(Wd32, "f32", (E_loc, f, d))   # blocks along f
+        Wd_val = brute.e4m3_value(Wd) * np.repeat(np.exp2(Wd_scale.astype(np.float64) - 127.0), 32, axis=1)
+    want = np.zeros((n, d))
+    for r in range(n):
+        if row_expert[r] >= 0:
+            want[r] = h[r] @ Wd_val[row_expert[r]]
+    got = oracle.down_proj_mx(codes, scales, row_expert, d, f, E_loc, Wd, w_dtype, Wd_scale)
+    assert (got[[3, 17]] == 0).all()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
