@@ -353,7 +353,14 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     wbytes = 3 * w.d * w.f * w.E_loc * (4 if w.dtype == "f32" else 2 if w.dtype == "bf16" else 1)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if wbytes <= L2_BYTES else None
 
-    names = ["route_topk", "permute", "gemm1_swiglu", "gemm2", "combine"]
+    # the layer's own choice: GEMM2 with the combine folded in on expert slices with under
+    # one local slot per token (the standalone entry adds a small per-token set-up kernel
+    # that moe_layer_forward folds into its permute), else GEMM2 and the combine kernel
+    fused = moe.moe_layer_fused_combine(k, w.E, E_loc, w.dtype)
+    names = ["route_topk", "permute", "gemm1_swiglu"] + (["gemm2_combine"] if fused else ["gemm2", "combine"])
+    nc = len(names)
+    ws_c = moe.workspace(moe.lib().moe_expert_gemm2_combine_workspace_size(moe.n_cap(T, k, E_loc), T, d)) \
+        if fused else None
 
     def call(i):
         if i == 0:
@@ -369,26 +376,29 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
             else:
                 moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, h=h,
                                             h_scale=hs, ws=ws_g, rows_hint=hint)
+        elif i == 3 and fused:
+            moe.moe_expert_gemm2_combine(h, hs, P["offsets"], P["row_src_token"], P["pair_to_row"], pw, y=y,
+                                         ws=ws_c, rows_hint=hint)
         elif i == 3:
             moe.moe_expert_gemm2(h, hs, P["offsets"], pw, Y2=Y2, ws=ws_g, rows_hint=hint)
         else:
             moe.moe_unpermute_combine(Y2, P["pair_to_row"], w.dtype, y=y)
 
     def step(marks):
-        """One step; marks[i] (an event or None) is recorded before call i, marks[5] after the last."""
-        for i in range(5):
+        """One step; marks[i] (an event or None) is recorded before call i, marks[nc] after the last."""
+        for i in range(nc):
             if marks[i] is not None:
                 marks[i].record()
             call(i)
-        if marks[5] is not None:
-            marks[5].record()
+        if marks[nc] is not None:
+            marks[nc].record()
 
     for _ in range(args.warmup):
         if flush is not None:
             flush.zero_()
-        step([None] * 6)
+        step([None] * (nc + 1))
     torch.cuda.synchronize()
-    err = moe.moe_get_device_error(ws_g)
+    err = moe.moe_get_device_error(ws_g) or (moe.moe_get_device_error(ws_c) if fused else 0)
     if err != 0:
         raise RuntimeError(f"{w.name}: device error {err} during warm-up")
     offs = P["offsets"].cpu().numpy().astype(np.int64)
@@ -406,8 +416,8 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
         dependent-launch overlap, so the timed graph keeps them to that one kernel."""
         # with an L2 flush between steps the step itself is bracketed too (the flush is
         # excluded from the step time)
-        keep = (0, 2, 3, 5) if flush is not None else (2, 3)
-        marks = [[ev() if (mark_all or j in keep) else None for j in range(6)] for _ in range(n_steps)]
+        keep = (0, 2, 3, nc) if flush is not None else (2, 3)
+        marks = [[ev() if (mark_all or j in keep) else None for j in range(nc + 1)] for _ in range(n_steps)]
         g = torch.cuda.CUDAGraph()
         cs = torch.cuda.Stream()
         cs.wait_stream(torch.cuda.current_stream())
@@ -442,13 +452,13 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if rank == 0 else None
-    err = moe.moe_get_device_error(ws_g)
+    err = moe.moe_get_device_error(ws_g) or (moe.moe_get_device_error(ws_c) if fused else 0)
     if err != 0:
         raise RuntimeError(f"{w.name}: device error {err} in the timed region")
     del graph
     region_ms = region0.elapsed_time(region1)
     gemm1_ms = statistics.mean(marks[i][2].elapsed_time(marks[i][3]) for i in range(args.steps))
-    total_ms = (sum(marks[i][0].elapsed_time(marks[i][5]) for i in range(args.steps)) if flush is not None
+    total_ms = (sum(marks[i][0].elapsed_time(marks[i][nc]) for i in range(args.steps)) if flush is not None
                 else region_ms)
     # per-kernel breakdown: a separate (untimed for `value`) graph with events between all kernels
     nb = min(args.steps, 50)
@@ -463,7 +473,7 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     if headline:
         # eager (one Python call per step), for reference only: includes host launch overhead
         n_eager = min(args.steps, 50)
-        ev_e = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_eager)]
+        ev_e = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(n_eager)]
         for i in range(n_eager):
             step(ev_e[i])
         torch.cuda.synchronize()
@@ -476,7 +486,8 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     bf = layer_bytes_flops(w, N, nonempty, n_tok_local)
     hbm = pk["hbm_gbs"]
     tpeak = pk["bf16_tflops"] * (2.0 if w.dtype == "mxfp8" else 1.0)
-    dom = max(("gemm1_swiglu", "gemm2"), key=lambda n: kern_ms[n])
+    g2name = "gemm2_combine" if fused else "gemm2"
+    dom = max(("gemm1_swiglu", g2name), key=lambda n: kern_ms[n])
     key = "gemm1" if dom == "gemm1_swiglu" else "gemm2"
     fl, by = bf[key + "_flops"], bf[key + "_bytes"]
     # the dominant kernel's duration: live, from the events around it in the timed region
@@ -495,7 +506,7 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     roof.update({"kernel": f"{kname} ({dom})", "traffic": recorded_traffic(dom, w.name),
                  "peak_kind": pk_kind + (" (bf16 x2 nominal fp8 ratio)" if w.dtype == "mxfp8" else "")})
     t_roof = max(bf["layer_flops"] / (tpeak * 1e12), bf["layer_bytes"] / (hbm * 1e9))
-    gemm_s = (gemm1_ms + kern_ms["gemm2"]) / 1e3
+    gemm_s = (gemm1_ms + kern_ms[g2name]) / 1e3
     layer = {"roofline_us": t_roof * 1e6, "measured_us": ms_per_step * 1e3, "frac": t_roof / (ms_per_step / 1e3),
              "algorithmic_bytes": bf["layer_bytes"], "flops": bf["layer_flops"], "N_pairs": N,
              "nonempty_experts": nonempty, "tokens_with_local_expert": n_tok_local,
@@ -506,7 +517,8 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     e2e = None
     if headline and not args.no_e2e:
         e2e = e2e_leg(moe, args, w, xd, lgd, y, pw, flush, world)
-    # route 1, permute 3 (+1 copy or MXFP8 per-token quantisation), GEMM1, GEMM2, combine
+    # route 1, permute 3 (+1 copy or MXFP8 per-token quantisation), GEMM1, then GEMM2 +
+    # combine (set-up kernel + fused GEMM2) or GEMM2 and the combine kernel
     launches_per_step = 1 + 3 + (0 if gather and not mx else 1) + 3
     return dict(value=job_tokens_per_s(T, world, ms_per_step), ms_per_step=ms_per_step, roof=roof, layer=layer,
                 kern_ms=kern_ms, region_ms=region_ms, gather=gather, eager_ms=eager_ms, e2e=e2e, clocks=clk,

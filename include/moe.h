@@ -211,6 +211,12 @@ int moe_rows_hint(int T, int k, int E);
  * kernel (bf16: A read from the token rows inside the kernel; fp32 / MXFP8: from a
  * permuted copy).  Returns -1 for invalid sizes. */
 int moe_layer_gemm1_pairs(int T, int d, int k, int E, int E_loc, moe_dtype dtype);
+
+/* Whether moe_layer_forward folds the combine into GEMM2 (moe_expert_gemm2_combine's
+ * path) for this routing shape: 1 when tokens average under one local slot (k * E_loc <
+ * E, bf16 or MXFP8), else 0 (GEMM2, then moe_unpermute_combine's kernel); -1 for invalid
+ * sizes.  The result is the same either way; only the kernels differ. */
+int moe_layer_fused_combine(int k, int E, int E_loc, moe_dtype dtype);
 size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype);
 
 /* The two halves of moe_grouped_mlp, for callers that keep h themselves (same
@@ -272,6 +278,32 @@ moe_status moe_quantize_mx_rows(const void* x, moe_dtype x_dtype, int T, int d, 
  * Requires d % 8 == 0 (bf16) / d % 4 == 0 (fp32). */
 moe_status moe_unpermute_combine(const void* Y2, const int32_t* pair_to_row, int T, int k, int d,
                                  moe_dtype dtype, void* y, moe_stream_t stream);
+
+/* GEMM2 with the unpermute + combine folded into it (steps 4-5) [BIO "GroupedLinear ...":
+ * the grouped down projection; WEP "MoE basics": the chosen experts' results are summed
+ * per token].  y equals, bit for bit, moe_expert_gemm2 followed by moe_unpermute_combine
+ * on the same inputs: each token's local rows (h W_down_e, rounded to bf16) are added in
+ * slot order in fp32 from zero and rounded once; tokens with no local expert get a zero
+ * row.  The GEMM2 kernel writes y itself for every token with at most one local slot (its
+ * row unchanged, which is that sum; or zeros, from extra warps running alongside the
+ * GEMM), and stores only the rows of tokens with several local slots to a scratch Y2,
+ * which a combine pass over those tokens alone then sums.  moe_layer_forward runs this path for MOE_BF16 and MOE_MXFP8.
+ *   h, h_scale, offsets, Wd_packed, Wd_scale   as for moe_expert_gemm2 (dtype MOE_BF16 or
+ *                                              MOE_MXFP8; MOE_F32 is MOE_ERR_UNSUPPORTED)
+ *   row_src_token [N_cap], pair_to_row [T, k]   device, from moe_permute
+ *   y         device bf16 [T, d], fully written (16-byte aligned)
+ *   rows_hint  as for moe_expert_gemm2; it also tells the expected local slots per token
+ *             (rows_hint * E_loc / T: under one picks the pass built for few multi-slot
+ *             tokens); <= 0 assumes min(k, E_loc).  It never changes the result.
+ *   workspace device, >= moe_expert_gemm2_combine_workspace_size(N_cap, T, d) bytes,
+ *             256-aligned (scratch Y2 and per-token slot counts, set by a small kernel)
+ * Requires 1 <= k <= 32 and the shape rules of moe_expert_gemm2. */
+moe_status moe_expert_gemm2_combine(const void* h, const uint8_t* h_scale, const int32_t* offsets,
+                                    const int32_t* row_src_token, const int32_t* pair_to_row, int T, int k,
+                                    int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype, const void* Wd_packed,
+                                    const uint8_t* Wd_scale, void* y, int rows_hint, void* workspace,
+                                    size_t workspace_bytes, moe_stream_t stream);
+size_t moe_expert_gemm2_combine_workspace_size(int64_t N_cap, int T, int d);
 
 /* Whole layer (steps 1-5 in one call) on the local experts [e0, e0 + E_loc).
  *   x [T, d] (fp32 for MOE_F32, else bf16), logits [T, E] fp32, packed weights as above,

@@ -59,6 +59,7 @@ _SIGS = {
     "moe_grouped_mlp": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_rows_hint": (_I, [_I, _I, _I]),
     "moe_layer_gemm1_pairs": (_I, [_I, _I, _I, _I, _I, _I]),
+    "moe_layer_fused_combine": (_I, [_I, _I, _I, _I]),
     "moe_grouped_mlp_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm1_swiglu_gather": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -72,6 +73,9 @@ _SIGS = {
     "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm_workspace_size": (_SZ, []),
     "moe_unpermute_combine": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_expert_gemm2_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I64, _I, _I, _I, _I, _P, _P, _P, _I, _P, _SZ,
+                                      _P]),
+    "moe_expert_gemm2_combine_workspace_size": (_SZ, [_I64, _I, _I]),
     "moe_layer_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_layer_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_get_device_error": (_I, [_P, _P, _P]),
@@ -235,6 +239,14 @@ def moe_layer_gemm1_pairs(T: int, d: int, k: int, E: int, E_loc: int, dtype: str
     return bool(r)
 
 
+def moe_layer_fused_combine(k: int, E: int, E_loc: int, dtype: str) -> bool:
+    """True if moe_layer_forward folds the combine into GEMM2 for this routing shape."""
+    r = int(_lib.moe_layer_fused_combine(k, E, E_loc, _dt(dtype)))
+    if r < 0:
+        raise ValueError("invalid sizes")
+    return bool(r)
+
+
 def moe_grouped_mlp(perm_x, perm_x_scale, offsets, row_prob, pw: PackedWeights, Y2=None, ws=None, rows_hint=0):
     cap = perm_x.shape[0]
     dev = perm_x.device
@@ -313,6 +325,19 @@ def moe_unpermute_combine(Y2, pair_to_row, dtype, y=None):
     _check("moe_unpermute_combine", _lib.moe_unpermute_combine(_ptr(Y2), _ptr(pair_to_row), T, k, d, _dt(dtype),
                                                                _ptr(y), _stream()))
     return y
+
+
+def moe_expert_gemm2_combine(h, h_scale, offsets, row_src_token, pair_to_row, pw: PackedWeights, y=None, ws=None,
+                             rows_hint=0):
+    """GEMM2 with the unpermute + combine in its epilogue: y [T, d] bf16 straight from h."""
+    cap = h.shape[0]
+    T, k = pair_to_row.shape
+    y = y if y is not None else torch.empty(T, pw.d, dtype=torch.bfloat16, device=h.device)
+    ws = ws if ws is not None else workspace(_lib.moe_expert_gemm2_combine_workspace_size(cap, T, pw.d), h.device)
+    _check("moe_expert_gemm2_combine", _lib.moe_expert_gemm2_combine(
+        _ptr(h), _ptr(h_scale), _ptr(offsets), _ptr(row_src_token), _ptr(pair_to_row), T, k, cap, pw.E_loc, pw.d,
+        pw.f, pw.dtype, _ptr(pw.Wd), _ptr(pw.Wd_scale), _ptr(y), int(rows_hint), _ptr(ws), ws.numel(), _stream()))
+    return y, ws
 
 
 def moe_layer_workspace_size(T, d, f, E, k, E_loc, dtype) -> int:

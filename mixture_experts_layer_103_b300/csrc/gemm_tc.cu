@@ -192,8 +192,14 @@ struct BMaps {
   CUtensorMap b256, b128, b64;
 };
 
+// Threads beyond the 6 GEMM warps: A-gather warps (row gather) or zero-row warps (combine).
+template <int EPI, bool GATHER>
+constexpr int extra_threads() {
+  return GATHER ? kGatherThreads : EPI == EPI_COMBINE ? kZeroThreads : 0;
+}
+
 template <bool MX, int EPI, bool GATHER>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATHER ? kGatherThreads : 0), 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + extra_threads<EPI, GATHER>(), 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ BMaps tmB,
                            const __grid_constant__ OutMaps tmO, const GemmArgs g) {
   using C = GemmSmem<MX>;
@@ -360,12 +366,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATH
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       // TMA stores for the bf16 outputs except the ScaledSwiGLU backward's three per block,
       // which measured faster with plain stores (two staging buffers serialise them)
-      if (ut.valid) epilogue_warp<EPI, !MX && EPI != EPI_DSWIGLU>(g, tmO, tl, tbase, BN, q, lane, est);
+      if (ut.valid)
+        epilogue_warp<EPI, !MX && EPI != EPI_DSWIGLU>(g, tmO, tl, tbase, BN, q, lane, est);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
     }
     if (lane == 0) ptx::bulk_wait_all();  // this warp's TMA stores have completed
+
   } else if constexpr (GATHER) {
     // ------------------------------------------------------------------ A gather
     // Thread gt copies 16-byte chunk (gt % 8) of the rows gt / 8 + 16 i (i < 8) of each
@@ -429,6 +437,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (GATH
       }
     }
     ptx::cp_async_wait_all();  // nothing of ours may still be landing when the CTA exits
+  } else if constexpr (EPI == EPI_COMBINE) {
+    // ------------------------------------------------------------------ combine + zero rows of y
+    zero_rows(g, blockIdx.x * 4 + (warp - 6), gridDim.x * 4, lane);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -503,7 +514,7 @@ template <bool MX, int EPI, bool GATHER = false>
 static cudaError_t launch_gemm_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
                                     cudaStream_t st) {
   using C = GemmSmem<MX>;
-  constexpr int threads = kGemmThreads + (GATHER ? kGatherThreads : 0);
+  constexpr int threads = kGemmThreads + extra_threads<EPI, GATHER>();
   CUtensorMap ta = {};
   BMaps tb;
   if (!GATHER && !make_operand_map(&ta, A, MX, g.K, a_rows, 1, kBM)) return cudaErrorInvalidValue;
@@ -554,6 +565,8 @@ static GemmArgs base_args(const int32_t* offsets, int E_loc, int32_t* err, uint6
 //   mxfp8: perm_x E4M3 [N_cap, d] + SF -> h E4M3 [N_cap, f] + SF
 cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu,
                              cudaStream_t st);
+cudaError_t launch_pair_gemm_combine(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
+                                     cudaStream_t st);
 
 // pair: bf16 only -- run the CTA-pair kernel (large M per expert) instead of the 1-CTA one.
 cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
@@ -632,6 +645,30 @@ cudaError_t launch_tc_gemm_store(const void* A, int64_t a_rows, const int32_t* o
   g.ld_out = n_out;
   g.out_rows = a_rows;
   return launch_gemm_inst<false, EPI_STORE_BF16>(A, a_rows, B, g, st);
+}
+
+// GEMM2 with the direct part of the unpermute + combine: h [N_cap, f] (bf16, or E4M3 +
+// SF) -> y rows of the tokens with at most one local slot (their row, or zeros), Y2
+// [N_cap, d] rows of the tokens with several (summed afterwards by the combine kernel).
+cudaError_t launch_tc_gemm2_combine(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap,
+                                    int E_loc, int d, int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf,
+                                    void* Y2, const int32_t* row_src_token, const int32_t* tok_nloc, int T, void* y,
+                                    int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
+  GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
+  g.n_out = d;
+  g.K = f;
+  g.out = Y2;
+  g.ld_out = d;
+  g.out_rows = N_cap;
+  g.a_sf = h_sf;
+  g.b_sf = Wd_sf;
+  g.row_token = row_src_token;
+  g.tok_nloc = tok_nloc;
+  g.y = y;
+  g.T = T;
+  if (mx) return launch_gemm_inst<true, EPI_COMBINE>(h, N_cap, Wd, g, st);
+  if (pair) return launch_pair_gemm_combine(h, N_cap, Wd, g, st);
+  return launch_gemm_inst<false, EPI_COMBINE>(h, N_cap, Wd, g, st);
 }
 
 // GEMM2 on the tensor cores: h [N_cap, f] (bf16, or E4M3 + SF) -> Y2 bf16 [N_cap, d].

@@ -14,9 +14,12 @@ constexpr int kBM = 128;
 constexpr int kRowBytes = 128;  // bytes of one operand row per pipeline stage
 constexpr int kGemmThreads = 192;        // producer, MMA, 4 epilogue warps
 constexpr int kGatherThreads = 128;      // + 4 A-gather warps in row-gather mode
+constexpr int kZeroThreads = 128;        // + 4 zero-row warps in combine mode (GEMM2)
 constexpr int kMaxEloc = 1024;
 
-enum { EPI_STORE_BF16 = 0, EPI_SWIGLU_BF16 = 1, EPI_SWIGLU_MX = 2, EPI_DSWIGLU = 3 };
+// EPI_COMBINE: GEMM2 with the unpermute + combine fused into its epilogue (bf16 y).
+enum { EPI_STORE_BF16 = 0, EPI_SWIGLU_BF16 = 1, EPI_SWIGLU_MX = 2, EPI_DSWIGLU = 3, EPI_COMBINE = 4 };
+
 
 struct GemmArgs {
   const int32_t* offsets;  // [E_loc + 1]
@@ -49,6 +52,13 @@ struct GemmArgs {
   void* out2;
   float* dp_part;
   int64_t out_rows;        // rows of out / out2 (the extent of their TMA store maps)
+  // EPI_COMBINE: y [T, n_out] bf16.  row_token [N_cap] = token of each routed row;
+  // tok_nloc [T] = local slots per token.  Rows of tokens with one local slot go straight
+  // to y, tokens without one get a zero row (zero-row warps), rows of tokens with several
+  // go to out (Y2) for the slot-ordered sum that follows.
+  void* y;
+  const int32_t* tok_nloc;
+  int T;
 };
 
 // TMA store maps of the bf16 outputs: 32 x 32 boxes over out [out_rows, ld_out] and out2
@@ -116,6 +126,26 @@ __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint4 (&v)
   __syncwarp();
 }
 
+// Same staging, but each lane's row goes to its own destination: dst = this lane's
+// row at the block's first column (nullptr: nothing stored for that row).  Each store
+// instruction covers whole 64-byte row segments (4 lanes per row).
+__device__ __forceinline__ void warp_store_rows_to(uint8_t* stage, const uint4 (&v)[4], int lane, uint8_t* dst,
+                                                   int chunks_valid) {
+  uint4* mine = reinterpret_cast<uint4*>(stage + lane * kEpiRowBytes);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) mine[c] = v[c];
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = j * 8 + lane / 4;
+    const int c = lane % 4;
+    uint8_t* row_dst = reinterpret_cast<uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(dst), r));
+    const uint4 val = *reinterpret_cast<const uint4*>(stage + r * kEpiRowBytes + c * 16);
+    if (row_dst != nullptr && c < chunks_valid) *reinterpret_cast<uint4*>(row_dst + c * 16) = val;
+  }
+  __syncwarp();
+}
+
 // TMA-store staging of the bf16 epilogues: each epilogue warp owns two 2 KB buffers, each
 // one 32-row x 64-byte block in the 64-byte swizzle of the store maps (16-byte chunk c of
 // row r at c ^ ((r >> 1) & 3)).  The two alternate; a buffer is refilled once the TMA store
@@ -177,6 +207,24 @@ __device__ __forceinline__ void warp_store_block(EpiStage& st, const uint4 (&v)[
   }
 }
 
+// ---- combine fused into GEMM2: zero rows of y, written by the zero-row warps
+
+// Zero row of token t (no local slot), streaming stores.
+__device__ __forceinline__ void zero_row(const GemmArgs& g, int t, int lane) {
+  const int64_t row_vecs = static_cast<int64_t>(g.n_out) * 2 / 16;
+  uint4* dst = static_cast<uint4*>(g.y) + static_cast<int64_t>(t) * row_vecs;
+  for (int64_t c = lane; c < row_vecs; c += 32) __stcs(dst + c, make_uint4(0u, 0u, 0u, 0u));
+}
+
+// Zero-row warp zw of nzw over the grid: the tokens t = zw, zw + nzw, ... without a local
+// slot get a zero row, written as early as possible, alongside the GEMM.  (Spreading the
+// writes over the GEMM's tiles instead measured slower on B300: the GEMM's operands are
+// mostly L2 hits, and the early writes overlap its start-up.)
+__device__ __forceinline__ void zero_rows(const GemmArgs& g, int zw, int nzw, int lane) {
+  for (int t = zw; t < g.T; t += nzw)
+    if (__ldg(g.tok_nloc + t) == 0) zero_row(g, t, lane);
+}
+
 // Epilogue of one 32-row slab of an accumulator tile (one warp, one TMEM lane per thread):
 // bf16 store of BN columns (GEMM2), or the fused scaled SwiGLU on BN/64 blocks of 32 gate
 // + 32 up columns with bf16 or MXFP8 (one 32-value block per thread) output (GEMM1).
@@ -207,6 +255,46 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const OutMaps& 
       const int chunks = max(0, min(4, (g.n_out - n) / 8));
       warp_store_block<TMA>(st, pk, lane, &om.out, n, row_first, out + row_first * ld + static_cast<int64_t>(n) * 2, ld,
                             rows_valid, chunks);
+    }
+  } else if constexpr (EPI == EPI_COMBINE) {
+    // GEMM2 + the direct part of the unpermute + combine ("Wide-EP ... NVIDIA" explainer,
+    // section "MoE basics": the chosen experts' results are summed per token).  A token
+    // with one local slot has y = its row (the slot sum of one bf16 value rounds to
+    // itself), so that row goes straight to y; rows of tokens with several local slots go
+    // to Y2 for the slot-ordered sum of the follow-up combine pass.  A slab whose rows all
+    // go to Y2 leaves by the ordinary (TMA) store path.
+    const bool live = r < tl.rows;
+    const int64_t row = row_first + lane;
+    const int t = live ? __ldg(g.row_token + row) : 0;
+    const int nloc = live ? __ldg(g.tok_nloc + t) : 0;
+    const bool direct = __any_sync(0xffffffffu, live && nloc == 1);
+    uint8_t* Y2 = static_cast<uint8_t*>(g.out);
+    const int64_t ld2 = g.ld_out * 2;
+    uint8_t* dst = !live ? nullptr
+                         : nloc == 1 ? static_cast<uint8_t*>(g.y) + t * (static_cast<int64_t>(g.n_out) * 2)
+                                     : Y2 + row * ld2;
+    if (TMA && direct && lane == 0) ptx::bulk_wait_read<0>();  // the padded staging reuses the TMA buffers
+    if (TMA && direct) st.last = -1;
+    __syncwarp();
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tbase + c, v);
+      ptx::tmem_ld_wait();
+      const int n = tl.n0 + c;
+      uint4 pk[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        pk[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+      const int chunks = max(0, min(4, (g.n_out - n) / 8));
+      if (direct)
+        warp_store_rows_to(st.buf, pk, lane, dst == nullptr ? nullptr : dst + static_cast<int64_t>(n) * 2, chunks);
+      else
+        warp_store_block<TMA>(st, pk, lane, &om.out, n, row_first, Y2 + row_first * ld2 + static_cast<int64_t>(n) * 2,
+                              ld2, rows_valid, chunks);
     }
   } else if constexpr (EPI == EPI_DSWIGLU) {
     // ScaledSwiGLU backward for h = p * silu(g) * u, from dh and the saved g, u:

@@ -39,7 +39,7 @@ constexpr int kPairBM = 256;  // rows of a pair tile (128 per CTA)
 constexpr int kPairBN = 256;  // columns of a pair tile
 
 template <int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI == EPI_COMBINE ? kZeroThreads : 0), 1)
     tc_grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                 const __grid_constant__ OutMaps tmO, const GemmArgs g) {
   using C = PairSmem;
@@ -154,7 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       ptx::mma_commit_pair(drain_bar, 0x1);  // every MMA issued by the pair has completed
       ptx::mbar_wait(drain_bar, 0, g.timeout_ns);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     EpiStage est{smem + C::OFF_EPI + (warp - 2) * kEpiTmaWarpBytes,
@@ -180,6 +180,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
     }
     if (lane == 0) ptx::bulk_wait_all();  // this warp's TMA stores have completed
+
+  } else if constexpr (EPI == EPI_COMBINE) {
+    // ------------------------------------------------------------------ combine + zero rows of y
+    zero_rows(g, blockIdx.x * 4 + (warp - 6), gridDim.x * 4, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -209,13 +213,19 @@ static cudaError_t launch_pair_inst(const void* A, int64_t a_rows, const void* B
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int grid = num_sms() & ~1;  // whole pairs
-  return launch_pdl(kern, dim3(grid), dim3(kGemmThreads), PairSmem::SMEM_BYTES, st, ta, tb, tmo, g);
+  const int threads = kGemmThreads + (EPI == EPI_COMBINE ? kZeroThreads : 0);
+  return launch_pdl(kern, dim3(grid), dim3(threads), PairSmem::SMEM_BYTES, st, ta, tb, tmo, g);
 }
 
 cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu,
                              cudaStream_t st) {
   return swiglu ? launch_pair_inst<EPI_SWIGLU_BF16>(A, a_rows, B, g, st)
                 : launch_pair_inst<EPI_STORE_BF16>(A, a_rows, B, g, st);
+}
+
+cudaError_t launch_pair_gemm_combine(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
+                                     cudaStream_t st) {
+  return launch_pair_inst<EPI_COMBINE>(A, a_rows, B, g, st);
 }
 
 }  // namespace moe

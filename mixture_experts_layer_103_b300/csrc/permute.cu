@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(TILE) perm_scatter_kernel(const int32_t* __res
                                                                  const int32_t* __restrict__ tile_base,
                                                                  int32_t* __restrict__ pair_to_row,
                                                                  int32_t* __restrict__ row_src_token,
-                                                                 float* __restrict__ row_prob) {
+                                                                 float* __restrict__ row_prob,
+                                                                 int32_t* __restrict__ tok_nloc) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ uint32_t s_mask[];  // [E_loc][TILE / 32] token bitmasks
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(TILE) perm_scatter_kernel(const int32_t* __res
     }
   __syncthreads();
   if (t >= T) return;
+  int nloc = 0;
   for (int j = 0; j < k; ++j) {
     const int e = __ldg(ids + t * k + j) - e0;
     int32_t row = -1;
@@ -159,9 +161,29 @@ __global__ void __launch_bounds__(TILE) perm_scatter_kernel(const int32_t* __res
       row = tile_base[static_cast<int64_t>(e) * n_tiles + blockIdx.x] + rank;
       row_src_token[row] = static_cast<int32_t>(t);
       row_prob[row] = __ldg(probs + t * k + j);
+      ++nloc;
     }
     pair_to_row[t * k + j] = row;
   }
+  if (tok_nloc) tok_nloc[t] = nloc;  // local slots per token, for the GEMM2 that combines
+}
+
+// The same per-token slot count for a GEMM2 + combine call on maps made elsewhere.
+__global__ void __launch_bounds__(256) combine_prep_kernel(const int32_t* __restrict__ pair_to_row, int T, int k,
+                                                           int32_t* __restrict__ tok_nloc) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  int nloc = 0;
+  for (int j = 0; j < k; ++j) nloc += __ldg(pair_to_row + t * k + j) >= 0;
+  tok_nloc[t] = nloc;
+}
+
+cudaError_t launch_combine_prep(const int32_t* pair_to_row, int T, int k, int32_t* tok_nloc, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  return launch_pdl(combine_prep_kernel, dim3(static_cast<unsigned>(ceil_div(T, 256))), dim3(256), 0, st, pair_to_row,
+                    T, k, tok_nloc);
 }
 
 // ------------------------------------------------------------------------------ gather
@@ -359,11 +381,13 @@ cudaError_t launch_gather_rows(const void* src, int64_t row_bytes, const int32_t
                     row_bytes / 16, offsets, E_loc, row_src_token, static_cast<uint4*>(dst));
 }
 
-// perm_dtype: MOE_F32 / MOE_BF16 (copy in x's type) or MOE_MXFP8 (quantise).
+// perm_dtype: MOE_F32 / MOE_BF16 (copy in x's type) or MOE_MXFP8 (quantise).  tok_nloc
+// (optional): per-token local slot counts, for the GEMM2 that combines in its epilogue.
 cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtype, int T, int d,
                            const int32_t* ids, const float* probs, int k, int e0, int E_loc, void* perm_x,
                            uint8_t* perm_sf, int32_t* counts, int32_t* offsets, int32_t* row_src_token,
-                           float* row_prob, int32_t* pair_to_row, uint8_t* ws, cudaStream_t st) {
+                           float* row_prob, int32_t* pair_to_row, uint8_t* ws, cudaStream_t st,
+                           int32_t* tok_nloc) {
   const int tile = perm_tile(T, E_loc);
   const int n_tiles = static_cast<int>(ceil_div(T > 0 ? T : 1, tile));
   PermuteWs w = carve_permute_ws(ws, T, E_loc);
@@ -383,7 +407,7 @@ cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtyp
     e = launch_pdl(tile == kPermTileSmall ? perm_scatter_kernel<kPermTileSmall> : perm_scatter_kernel<kPermTileLarge>,
                    dim3(n_tiles), dim3(tile), E_loc * (tile / 32) * 4, st, ids, probs,
                    T, k, e0, E_loc, n_tiles, static_cast<const int32_t*>(w.tile_counts), pair_to_row, row_src_token,
-                   row_prob);
+                   row_prob, tok_nloc);
     if (e != cudaSuccess) return e;
     const int grid = gather_grid(st);
     if (perm_x == nullptr) {

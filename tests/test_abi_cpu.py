@@ -171,3 +171,15 @@ def test_gemm1_kernel_choice(lib):
     assert not pairs(8192, 7168, 8, 256, 4, "f32")
     with pytest.raises(ValueError):
         pairs(8192, 7168, 8, 256, 512, "bf16")            # E_loc > E
+
+
+def test_combine_fusion_choice(lib):
+    """moe_layer_forward folds the combine into GEMM2 when tokens average under one local
+    slot (k * E_loc < E), for bf16 and MXFP8 (measured per shape on B300)."""
+    fused = lib.moe_layer_fused_combine
+    assert fused(8, 256, 4, "bf16") and fused(8, 256, 4, "mxfp8")   # EP64 slice: 0.125 slots
+    assert not fused(8, 256, 32, "bf16")                             # EP8 slice: 1 slot
+    assert not fused(8, 64, 64, "bf16")                              # all experts local
+    assert not fused(8, 256, 4, "f32")                               # fp32: SIMT GEMMs + combine
+    with pytest.raises(ValueError):
+        fused(8, 4, 8, "bf16")

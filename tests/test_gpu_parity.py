@@ -257,27 +257,83 @@ def test_ep_slices_sum_to_full_layer(moe, dtype):
     assert rel_l2(acc, yo) <= TOL[dtype]
 
 
-def test_split_calls_equal_fused_call(moe):
+SPLIT_CASES = [
+    Workload("split", 512, 256, 256, 32, 4, 8, 16, "bf16"),           # 2 local slots per token
+    Workload("split_slice", 3000, 256, 256, 256, 8, 8, 4, "bf16"),    # 1/8: combine folded into GEMM2
+    Workload("split_slice_mx", 3000, 256, 256, 256, 8, 8, 4, "mxfp8"),
+]
+
+
+@pytest.mark.parametrize("w", SPLIT_CASES, ids=[c.name for c in SPLIT_CASES])
+def test_split_calls_equal_fused_call(moe, w):
     """route -> permute -> gemm1 -> gemm2 -> combine through the separate entry points
-    gives exactly the fused moe_layer_forward result (same kernels, same order)."""
-    w = Workload("split", 512, 256, 256, 32, 4, 8, 16, "bf16")
+    gives exactly the fused moe_layer_forward result, whichever way the layer combines."""
     x, lg = gen_x(w), gen_logits(w)
     Wg, Wu, Wd = gen_weights(w)
-    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), "bf16")
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), w.dtype)
     xd, lgd = to_dev(x), to_dev(lg)
     y_fused, _ = moe.moe_layer_forward(xd, lgd, w.E, w.k, w.e0, pw)
+    assert moe.moe_layer_fused_combine(w.k, w.E, w.E_loc, w.dtype) == (w.k * w.E_loc < w.E)
     ids, probs = moe.moe_route_topk(lgd, w.k)
-    P = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, "bf16")
+    P = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, w.dtype)
     hint = moe.moe_rows_hint(w.T, w.k, w.E)
     h, hs, _ = moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw,
                                            rows_hint=hint)
     Y2, _ = moe.moe_expert_gemm2(h, hs, P["offsets"], pw, rows_hint=hint)
-    y = moe.moe_unpermute_combine(Y2, P["pair_to_row"], "bf16")
+    y = moe.moe_unpermute_combine(Y2, P["pair_to_row"], w.dtype)
     Y2b, _ = moe.moe_grouped_mlp(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, rows_hint=hint)
     torch.cuda.synchronize()
     assert torch.equal(y, y_fused)
     N = int(P["offsets"][-1])
     assert torch.equal(Y2[:N], Y2b[:N])
+
+
+COMBINE_CASES = [
+    # workload, rows_hint (1: 1-CTA GEMM2, 4096: CTA-pair GEMM2, 0: the layer's own choice)
+    (Workload("cmb_e64", 777, 256, 256, 64, 8, 0, 64, "bf16", ("normal", 0.5)), 1),
+    (Workload("cmb_e64_pair", 777, 256, 256, 64, 8, 0, 64, "bf16", ("normal", 0.5)), 4096),
+    (Workload("cmb_slice", 1000, 384, 128, 256, 8, 224, 32, "bf16"), 0),  # tokens with 0, 1 and many slots
+    (Workload("cmb_zipf", 1000, 384, 128, 256, 8, 32, 32, "bf16", ("zipf", 1.1)), 0),
+    (Workload("cmb_k32", 300, 128, 128, 64, 32, 0, 64, "bf16"), 0),
+    (Workload("cmb_tail", 513, 200, 96, 16, 4, 4, 8, "bf16"), 1),  # d % 64 != 0: a partial n-tile
+    (Workload("cmb_mx", 1024, 512, 256, 256, 8, 0, 32, "mxfp8", ("zipf", 1.1)), 0),
+    (Workload("cmb_mx_e8", 700, 256, 256, 8, 4, 0, 8, "mxfp8"), 0),
+    # rows_hint 1: the pass for few multi-slot tokens, here on a slice where many have several
+    (Workload("cmb_sparse_pass", 1000, 384, 128, 256, 8, 0, 64, "bf16", ("zipf", 1.1)), 1),
+]
+
+
+@pytest.mark.parametrize("w,hint", COMBINE_CASES, ids=[c[0].name for c in COMBINE_CASES])
+def test_gemm2_combine_equals_separate_kernels(moe, w, hint):
+    """GEMM2 with the combine folded in (direct rows for tokens with one local slot, zero
+    rows from the GEMM's extra warps, the slot sum for the rest) gives, bit for bit, GEMM2
+    followed by the combine kernel, on two calls in a row, and the layer's y matches the
+    oracle."""
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), w.dtype)
+    xd = to_dev(x)
+    ids, probs = moe.moe_route_topk(to_dev(lg), w.k)
+    P = moe.moe_permute(xd, ids, probs, w.e0, w.E_loc, w.dtype)
+    h, hs, _ = moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw,
+                                           rows_hint=hint)
+    Y2, _ = moe.moe_expert_gemm2(h, hs, P["offsets"], pw, rows_hint=hint)
+    y_sep = moe.moe_unpermute_combine(Y2, P["pair_to_row"], "bf16")
+    y1, ws = moe.moe_expert_gemm2_combine(h, hs, P["offsets"], P["row_src_token"], P["pair_to_row"], pw,
+                                          rows_hint=hint)
+    y1 = y1.clone()
+    y2, _ = moe.moe_expert_gemm2_combine(h, hs, P["offsets"], P["row_src_token"], P["pair_to_row"], pw, ws=ws,
+                                         rows_hint=hint)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    nloc = (P["pair_to_row"] >= 0).sum(1).cpu().numpy()
+    if w.name == "cmb_slice":
+        assert (nloc == 0).any() and (nloc == 1).any() and (nloc > 2).any()
+    assert torch.equal(y1, y_sep), int((y1 != y_sep).sum())
+    assert torch.equal(y2, y_sep)
+    assert (to_np(y1)[nloc == 0] == 0).all()
+    yl = gpu_layer(moe, w, x, lg, Wg, Wu, Wd)
+    assert rel_l2(to_np(yl), oracle_layer(w, x, lg, Wg, Wu, Wd)) <= TOL[w.dtype]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
