@@ -340,7 +340,7 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     # CTA pairs
     pairs1 = moe.moe_layer_gemm1_pairs(T, d, k, w.E, E_loc, w.dtype) if args.rows_hint is None else (
         w.dtype == "bf16" and (hint >= 2048 or (256 <= hint < 1024 and d >= 4096)))
-    gather = not args.no_gather and w.dtype == "bf16" and not pairs1
+    gather = not args.no_gather and w.dtype == "bf16"
     mx = w.dtype == "mxfp8"
     P = moe.alloc_permute(T, d, k, E_loc, xd.dtype, w.dtype, maps_only=gather)
     xq, xs = (torch.empty(T, d, dtype=torch.uint8, device="cuda"),
@@ -372,7 +372,7 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
         elif i == 2:
             if gather:
                 moe.moe_expert_gemm1_swiglu_gather(xq if mx else xd, xs, P["row_src_token"], P["offsets"],
-                                                   P["row_prob"], pw, h=h, h_scale=hs, ws=ws_g)
+                                                   P["row_prob"], pw, h=h, h_scale=hs, ws=ws_g, rows_hint=hint)
             else:
                 moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, h=h,
                                             h_scale=hs, ws=ws_g, rows_hint=hint)

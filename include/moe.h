@@ -248,12 +248,14 @@ size_t moe_expert_gemm_workspace_size(void);
  *            (MOE_F32 is not supported: MOE_ERR_UNSUPPORTED.)
  *   row_src_token [N_cap], offsets [E_loc+1], row_prob [N_cap]: device, from moe_permute
  *            (which may be called with perm_x == NULL)
- *   h, h_scale, Wgu_*, workspace: as for moe_expert_gemm1_swiglu.  16-byte aligned x, h
- *   and packed weights; d % 8 == 0 (bf16), d % 128 == 0 and f % 128 == 0 (MXFP8). */
+ *   h, h_scale, Wgu_*, rows_hint, workspace: as for moe_expert_gemm1_swiglu (bf16: the
+ *   CTA-pair kernel copies its 256-row tiles' rows the same way, each CTA its own 128).
+ *   16-byte aligned x, h and packed weights; d % 8 == 0 (bf16), d % 128 == 0 and f % 128 ==
+ *   0 (MXFP8). */
 moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale, const int32_t* row_src_token,
                                           const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc,
                                           int d, int f, moe_dtype dtype, const void* Wgu_packed,
-                                          const uint8_t* Wgu_scale, void* h, uint8_t* h_scale, void* workspace,
+                                          const uint8_t* Wgu_scale, void* h, uint8_t* h_scale, int rows_hint, void* workspace,
                                           size_t workspace_bytes, moe_stream_t stream);
 
 /* MXFP8 quantisation of token rows [BIO "MXFP8 Precision ..."]: the quantisation rule

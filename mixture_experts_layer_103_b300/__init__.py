@@ -62,7 +62,8 @@ _SIGS = {
     "moe_layer_fused_combine": (_I, [_I, _I, _I, _I]),
     "moe_grouped_mlp_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
-    "moe_expert_gemm1_swiglu_gather": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_gemm1_swiglu_gather": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ,
+                                            _P]),
     "moe_quantize_mx_rows": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P]),
     "moe_eplb_plan": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_layer_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -282,16 +283,18 @@ def moe_expert_gemm1_swiglu(perm_x, perm_x_scale, offsets, row_prob, pw: PackedW
 
 
 def moe_expert_gemm1_swiglu_gather(x, x_scale, row_src_token, offsets, row_prob, pw: PackedWeights, h=None,
-                                   h_scale=None, ws=None):
+                                   h_scale=None, ws=None, rows_hint=1):
     """GEMM1 + scaled SwiGLU reading the token rows x (bf16, or E4M3 + row scales from
-    moe_quantize_mx_rows) through row_src_token."""
+    moe_quantize_mx_rows) through row_src_token.  rows_hint picks the kernel shape as for
+    moe_expert_gemm1_swiglu (the default 1 keeps the 1-CTA kernel)."""
     cap = row_src_token.shape[0]
     if h is None:
         h, h_scale = alloc_h(cap, pw, x.device)
     ws = ws if ws is not None else workspace(_lib.moe_expert_gemm_workspace_size(), x.device)
     _check("moe_expert_gemm1_swiglu_gather", _lib.moe_expert_gemm1_swiglu_gather(
         _ptr(x), _ptr(x_scale), _ptr(row_src_token), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f,
-        pw.dtype, _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(h), _ptr(h_scale), _ptr(ws), ws.numel(), _stream()))
+        pw.dtype, _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(h), _ptr(h_scale), int(rows_hint), _ptr(ws), ws.numel(),
+        _stream()))
     return h, h_scale, ws
 
 

@@ -36,8 +36,8 @@ cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* o
                             uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
                                    const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc, int d,
-                                   int f, bool mx, const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf,
-                                   int32_t* err, uint64_t timeout_ns, void* gu_save, cudaStream_t st);
+                                   int f, bool mx, bool pair, const void* Wgu, const uint8_t* Wgu_sf, void* h,
+                                   uint8_t* h_sf, int32_t* err, uint64_t timeout_ns, void* gu_save, cudaStream_t st);
 cudaError_t launch_quant_rows_mx(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
                                  uint8_t* xq, uint8_t* x_sf, cudaStream_t st);
 cudaError_t launch_tc_dswiglu(const void* dy_rows, const int32_t* offsets, const float* row_prob, int64_t N_cap,
@@ -179,15 +179,14 @@ static cudaError_t run_mlp(const void* perm_x, const uint8_t* perm_sf, const int
   return run_gemm2(s.h, s.h_sf, offsets, n_cap, E_loc, d, f, dt, Wd, Wd_sf, Y2, err, rows_hint, st);
 }
 
-// The bf16 layer reads x rows straight into GEMM1 (row gather) unless the CTA-pair GEMMs
-// are chosen; fp32 (SIMT) and MXFP8 take a permuted copy.  Measured on B300, the MXFP8
+// The bf16 layer reads x rows straight into GEMM1 (row gather), on CTA pairs or the 1-CTA
+// kernel; fp32 (SIMT) and MXFP8 take a permuted copy.  Measured on B300, the MXFP8
 // row-gather GEMM1 was 7-10 % slower than the TMA-fed one and quantising per token saved
 // nothing over quantising while copying, while bf16 gains: the permuted copy costs 27 us
 // at T = 4096, d = 2048, k = 8 and the gather adds less than that to GEMM1.
 static bool layer_gathers(moe_dtype dt, int T, int d, int k, int E, int E_loc) {
-  const int64_t n_cap = n_cap_of(T, k, E_loc);
-  const int64_t rows = T > 0 && k > 0 && E > 0 ? static_cast<int64_t>(T) * k / E : 0;
-  return dt == MOE_BF16 && !use_pair(dt, n_cap, E_loc, static_cast<int>(rows), d);
+  (void)T; (void)d; (void)k; (void)E; (void)E_loc;
+  return dt == MOE_BF16;
 }
 
 // The layer folds the combine into GEMM2 (direct rows for tokens with one local slot, zero
@@ -480,8 +479,8 @@ moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_sca
 moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale, const int32_t* row_src_token,
                                           const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc,
                                           int d, int f, moe_dtype dtype, const void* Wgu_packed,
-                                          const uint8_t* Wgu_scale, void* h, uint8_t* h_scale, void* workspace,
-                                          size_t workspace_bytes, moe_stream_t stream) {
+                                          const uint8_t* Wgu_scale, void* h, uint8_t* h_scale, int rows_hint,
+                                          void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   if (dtype == MOE_F32) return MOE_ERR_UNSUPPORTED;
   moe_status s = check_gemm_common(N_cap, E_loc, d, f, dtype, offsets, x, x_scale, Wgu_packed, Wgu_scale, h, h_scale);
   if (s != MOE_OK) return s;
@@ -489,8 +488,9 @@ moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale,
   if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
   if (N_cap == 0) return MOE_OK;
   return cuda_status(launch_tc_gemm1_gather(x, x_scale, row_src_token, offsets, row_prob, N_cap, E_loc, d, f,
-                                            dtype == MOE_MXFP8, Wgu_packed, Wgu_scale, h, h_scale,
-                                            static_cast<int32_t*>(workspace), kTimeoutNs, nullptr, stream));
+                                            dtype == MOE_MXFP8, use_pair(dtype, N_cap, E_loc, rows_hint, d),
+                                            Wgu_packed, Wgu_scale, h, h_scale, static_cast<int32_t*>(workspace),
+                                            kTimeoutNs, nullptr, stream));
 }
 
 moe_status moe_quantize_mx_rows(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
@@ -627,7 +627,8 @@ static moe_status layer_forward_impl(const void* x, const float* logits, int T, 
       e = launch_quant_rows_mx(x, x_dtype, T, d, w.pair_to_row, k, static_cast<uint8_t*>(w.perm_x), w.perm_sf, stream);
     if (e == cudaSuccess)
       e = launch_tc_gemm1_gather(mx ? w.perm_x : x, w.perm_sf, w.row_src_token, w.offsets, w.row_prob, n_cap, E_loc,
-                                 d, f, mx, Wgu_packed, Wgu_scale, ms.h, ms.h_sf, w.err, kTimeoutNs, gu_save, stream);
+                                 d, f, mx, !mx && use_pair(dtype, n_cap, E_loc, hint, d), Wgu_packed, Wgu_scale,
+                                 ms.h, ms.h_sf, w.err, kTimeoutNs, gu_save, stream);
   } else if (e == cudaSuccess) {
     e = run_gemm1(w.perm_x, w.perm_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale, ms.h,
                   ms.h_sf, w.err, hint, stream, gu_save);

@@ -567,6 +567,7 @@ cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const
                              cudaStream_t st);
 cudaError_t launch_pair_gemm_combine(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
                                      cudaStream_t st);
+cudaError_t launch_pair_gemm1_gather(const void* B, const GemmArgs& g, cudaStream_t st);
 
 // pair: bf16 only -- run the CTA-pair kernel (large M per expert) instead of the 1-CTA one.
 cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
@@ -592,10 +593,11 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
 // GEMM1 + fused scaled SwiGLU with A gathered from the token rows: row r of the
 // expert-ordered operand is x row row_src_token[r] (bf16 [T, d]; MXFP8: E4M3 [T, d] with
 // E8M0 scales x_sf [T, d / 32]), so no permuted copy of x is ever written.
+// pair: bf16 only -- the CTA-pair kernel (256-row tiles) instead of the 1-CTA one.
 cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
                                    const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc, int d,
-                                   int f, bool mx, const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf,
-                                   int32_t* err, uint64_t timeout_ns, void* gu_save, cudaStream_t st) {
+                                   int f, bool mx, bool pair, const void* Wgu, const uint8_t* Wgu_sf, void* h,
+                                   uint8_t* h_sf, int32_t* err, uint64_t timeout_ns, void* gu_save, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
   g.out2 = mx ? nullptr : gu_save;
   g.n_out = 2 * f;
@@ -612,6 +614,7 @@ cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int
   g.gx_sf = x_sf;
   g.gx_sf_ld = d / 32;
   if (mx) return launch_gemm_inst<true, EPI_SWIGLU_MX, true>(nullptr, 0, Wgu, g, st);
+  if (pair) return launch_pair_gemm1_gather(Wgu, g, st);
   return launch_gemm_inst<false, EPI_SWIGLU_BF16, true>(nullptr, 0, Wgu, g, st);
 }
 

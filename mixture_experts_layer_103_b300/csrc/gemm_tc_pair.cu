@@ -17,6 +17,12 @@
 // and each weight byte fetched from L2 feeds two SMs.  Rows of a 256-row tile past the
 // expert's segment are computed and discarded, so the pair pays more padding on small
 // segments; the host picks it only when experts hold many rows.
+// Row-gather mode (GEMM1): A is not loaded by TMA from a permuted copy; 4 extra warps in
+// each CTA copy that CTA's 128 token rows of the stage straight from x (cp.async into the
+// 128-byte swizzled layout).  The leader's gather threads arrive on the leader's full
+// barrier when their copies land; the peer's arrive on a barrier of their own, and the
+// peer's MMA warp (idle otherwise) relays each completed stage to the leader's full barrier
+// after a proxy fence, so the leader's MMA sees both halves of A.
 #include "gemm_tc.cuh"
 
 namespace moe {
@@ -29,7 +35,8 @@ struct PairSmem {
   static constexpr int BK = 64;                    // bf16 K elements per stage
   static constexpr int OFF_EPI = STAGES * STAGE_BYTES;  // epilogue staging (TMA stores)
   static constexpr int OFF_BAR = OFF_EPI + kEpiTmaBytes;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+  // full, empty, tmem_full[2], tmem_empty[2], drain, gathered (row-gather mode, peer CTA)
+  static constexpr int NUM_BARS = 3 * STAGES + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TAB = OFF_MISC + 16;
   static constexpr int SMEM_BYTES = OFF_TAB + 2 * (kMaxEloc + 1) * 4 + 1024;
@@ -38,8 +45,14 @@ struct PairSmem {
 constexpr int kPairBM = 256;  // rows of a pair tile (128 per CTA)
 constexpr int kPairBN = 256;  // columns of a pair tile
 
-template <int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI == EPI_COMBINE ? kZeroThreads : 0), 1)
+// Threads beyond the 6 GEMM warps: A-gather warps (row gather) or zero-row warps (combine).
+template <int EPI, bool GATHER>
+constexpr int pair_extra_threads() {
+  return GATHER ? kGatherThreads : EPI == EPI_COMBINE ? kZeroThreads : 0;
+}
+
+template <int EPI, bool GATHER>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_extra_threads<EPI, GATHER>(), 1)
     tc_grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                                 const __grid_constant__ OutMaps tmO, const GemmArgs g) {
   using C = PairSmem;
@@ -53,6 +66,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI 
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  auto gath_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + 5 + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* s_off = reinterpret_cast<int*>(smem + C::OFF_TAB);
@@ -63,8 +77,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI 
   const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      ptx::mbar_init(full_bar(s), 1);
+      // row gather: the leader's expect-tx arrival, its own 128 gather threads and the
+      // peer's relay
+      ptx::mbar_init(full_bar(s), GATHER ? 1 + kGatherThreads + 1 : 1);
       ptx::mbar_init(empty_bar(s), 1);
+      if (GATHER) ptx::mbar_init(gath_bar(s), kGatherThreads);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
@@ -73,7 +90,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI 
     ptx::mbar_init(drain_bar, 1);
     *s_abort = 0;
     ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&tmA);
+    if (!GATHER) ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
   }
   if (warp == 1) {  // one warp in each CTA of the pair allocates the pair's TMEM
@@ -108,9 +125,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI 
           if (*s_abort) { ok = false; break; }
           if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
           const uint32_t fb_leader = ptx::mapa_shared(full_bar(s), 0);
-          if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * C::STAGE_BYTES);
+          // in row-gather mode the gather warps fill A themselves
+          if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), GATHER ? 2 * C::B_BYTES : 2 * C::STAGE_BYTES);
           const uint32_t st_addr = sbase + s * C::STAGE_BYTES;
-          ptx::tma_load_3d_pair(st_addr, &tmA, fb_leader, kb * C::BK, a_row, 0);
+          if (!GATHER) ptx::tma_load_3d_pair(st_addr, &tmA, fb_leader, kb * C::BK, a_row, 0);
           ptx::tma_load_3d_pair(st_addr + C::A_BYTES, &tmB, fb_leader, kb * C::BK, b_row, tl.e);
           ++issued;
           if (++s == C::STAGES) { s = 0; ph ^= 1u; }
@@ -137,7 +155,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI 
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kPairBN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!ptx::mbar_wait(full_bar(s), ph, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
+          // row gather: the peer's rows were released at cluster scope by its relay
+          const bool got = GATHER ? ptx::mbar_wait_cluster(full_bar(s), ph, g.timeout_ns)
+                                  : ptx::mbar_wait(full_bar(s), ph, g.timeout_ns);
+          if (!got) { gemm_abort(g, s_abort); ok = false; break; }
+          if (GATHER) ptx::fence_proxy_async_smem();  // the leader's gathered rows were written by cp.async
           ptx::tc_fence_after();
           const uint32_t a_addr = sbase + s * C::STAGE_BYTES;
           const uint32_t b_addr = a_addr + C::A_BYTES;
@@ -153,6 +175,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI 
       }
       ptx::mma_commit_pair(drain_bar, 0x1);  // every MMA issued by the pair has completed
       ptx::mbar_wait(drain_bar, 0, g.timeout_ns);
+    } else if (GATHER && lane == 0 && !leader) {
+      // ------------------------------------------------------------------ gather relay (peer)
+      // Each stage this CTA's gather threads completed: make their cp.async rows (already in
+      // this CTA's shared memory) visible to the async proxy that the pair MMA reads them
+      // through, then arrive on the leader's full barrier.  The arrival is a CTA-scope
+      // release: a cluster-scope one measured ~1 us per stage on B300 (GEMM1 241 vs 97 us at
+      // T = 8192, d = 7168, 4 experts).
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs) {
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (*s_abort) { ok = false; break; }
+          if (!ptx::mbar_wait(gath_bar(s), ph, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive_remote(ptx::mapa_shared(full_bar(s), 0));
+          if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
@@ -181,6 +222,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI 
     }
     if (lane == 0) ptx::bulk_wait_all();  // this warp's TMA stores have completed
 
+  } else if constexpr (GATHER) {
+    // ------------------------------------------------------------------ A gather (both CTAs)
+    // Thread gt copies 16-byte chunk (gt % 8) of rows gt / 8 + 16 i (i < 8) of this CTA's
+    // 128 rows of each stage's A straight from the token rows, into the 128-byte swizzled
+    // layout a TMA load would produce; its copies of a stage arrive (when they land) on the
+    // leader's full barrier in the leader, on the relayed barrier in the peer.
+    const int gt = threadIdx.x - kGemmThreads;
+    const int chunk = gt & 7, rbase = gt >> 3;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs) {
+      Tile tl = decode_tile(t, n_tiles_n, kPairBN, s_off, s_mtp, g.E_loc, kPairBM);
+      tl.row0 += 128 * static_cast<int>(rank);  // this CTA's rows of the tile
+      tl.rows = max(0, min(128, tl.rows - 128 * static_cast<int>(rank)));
+      const uint8_t* src[8];
+      uint32_t live = 0;  // bit i: row rbase + 16 i lies in the tile
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rbase + 16 * i;
+        const bool v = r < tl.rows;
+        const int64_t tok = v ? __ldg(g.row_token + tl.row0 + r) : 0;
+        src[i] = g.gx + tok * g.gx_ld + chunk * 16;
+        live |= static_cast<uint32_t>(v) << i;
+      }
+      for (int kb = 0; kb < num_kb; ++kb) {
+        int okw = 0;
+        if (lane == 0) okw = *s_abort ? 0 : (ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns) ? 1 : 2);
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (okw != 1) {
+          if (okw == 2 && lane == 0) gemm_abort(g, s_abort);
+          ok = false;
+          break;
+        }
+        (void)ptx::mbar_try_wait(empty_bar(s), ph ^ 1u);  // completed phase: acquire for every lane
+        const uint32_t a_addr = sbase + s * C::STAGE_BYTES;
+        const int64_t kbyte = static_cast<int64_t>(kb) * C::BK * 2 + chunk * 16;
+        const bool kin = kbyte < static_cast<int64_t>(g.K) * 2;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = rbase + 16 * i;
+          const bool v = kin && ((live >> i) & 1u);
+          ptx::cp_async_16(a_addr + r * kRowBytes + ((chunk ^ (r & 7)) << 4), v ? src[i] + kb * C::BK * 2 : g.gx,
+                           v ? 16u : 0u);
+        }
+        ptx::cp_async_arrive_noinc(leader ? full_bar(s) : gath_bar(s));
+        if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+      }
+    }
+    ptx::cp_async_wait_all();  // nothing of ours may still be landing when the CTA exits
   } else if constexpr (EPI == EPI_COMBINE) {
     // ------------------------------------------------------------------ combine + zero rows of y
     zero_rows(g, blockIdx.x * 4 + (warp - 6), gridDim.x * 4, lane);
@@ -194,15 +285,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + (EPI 
   }
 }
 
-template <int EPI>
+// A: the permuted rows [a_rows, K] (TMA), or unused (nullptr) in row-gather mode.
+template <int EPI, bool GATHER = false>
 static cudaError_t launch_pair_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, A, false, g.K, a_rows, 1, 128)) return cudaErrorInvalidValue;
+  CUtensorMap ta = {}, tb;
+  if (!GATHER && !make_operand_map(&ta, A, false, g.K, a_rows, 1, 128)) return cudaErrorInvalidValue;
   if (!make_operand_map(&tb, B, false, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
   OutMaps tmo;
   memset(&tmo, 0, sizeof(tmo));
   if (!make_out_maps(&tmo, g)) return cudaErrorInvalidValue;
-  auto kern = tc_grouped_gemm_pair_kernel<EPI>;
+  auto kern = tc_grouped_gemm_pair_kernel<EPI, GATHER>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -213,7 +305,7 @@ static cudaError_t launch_pair_inst(const void* A, int64_t a_rows, const void* B
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int grid = num_sms() & ~1;  // whole pairs
-  const int threads = kGemmThreads + (EPI == EPI_COMBINE ? kZeroThreads : 0);
+  const int threads = kGemmThreads + pair_extra_threads<EPI, GATHER>();
   return launch_pdl(kern, dim3(grid), dim3(threads), PairSmem::SMEM_BYTES, st, ta, tb, tmo, g);
 }
 
@@ -226,6 +318,11 @@ cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const
 cudaError_t launch_pair_gemm_combine(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
                                      cudaStream_t st) {
   return launch_pair_inst<EPI_COMBINE>(A, a_rows, B, g, st);
+}
+
+// GEMM1 + scaled SwiGLU on CTA pairs with A gathered from the token rows (g.gx, g.row_token).
+cudaError_t launch_pair_gemm1_gather(const void* B, const GemmArgs& g, cudaStream_t st) {
+  return launch_pair_inst<EPI_SWIGLU_BF16, true>(nullptr, 0, B, g, st);
 }
 
 }  // namespace moe

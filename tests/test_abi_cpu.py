@@ -62,9 +62,10 @@ def test_sizes(lib):
     # fp32 copies the rows: perm_x + Y2 + h
     f32 = L.moe_layer_workspace_size(4096, 2048, 1024, 64, 8, 64, 0)
     assert f32 >= 32768 * 2048 * 4 * 2 + 32768 * 1024 * 4
-    # tall segments (T * k / E >= 2048) pick the CTA-pair GEMMs, which read a permuted copy
+    # tall segments (T * k / E >= 2048) pick the CTA-pair GEMMs, which gather the token
+    # rows as well: Y2 + h, no permuted copy
     tall = L.moe_layer_workspace_size(2048, 256, 256, 8, 8, 8, 1)
-    assert tall >= 16384 * 256 * 2 * 2 + 16384 * 256 * 2
+    assert 16384 * 256 * 2 + 16384 * 256 * 2 <= tall < 2 * 16384 * 256 * 2 + 16384 * 256 * 2
     # MXFP8 copies while quantising: E4M3 perm_x + Y2 (bf16) + E4M3 h
     mx = L.moe_layer_workspace_size(4096, 2048, 1024, 64, 8, 64, 2)
     assert mx >= 32768 * 2048 + 32768 * 2048 * 2 + 32768 * 1024
@@ -134,10 +135,11 @@ def test_validation_before_any_launch(lib):
     assert L.moe_workspace_init(ctypes.c_void_p(272), 256, s) == 3
     assert L.moe_workspace_init(P, 16, s) == 3
     # row-gather GEMM1: fp32 unsupported, null row map, bf16 d % 8
-    assert L.moe_expert_gemm1_swiglu_gather(P, None, P, P, P, 64, 4, 64, 64, 0, P, None, P, None, P, 256, s) == 2
-    assert L.moe_expert_gemm1_swiglu_gather(P, None, None, P, P, 64, 4, 64, 64, 1, P, None, P, None, P, 256, s) == 1
-    assert L.moe_expert_gemm1_swiglu_gather(P, None, P, P, P, 64, 4, 60, 64, 1, P, None, P, None, P, 256, s) == 2
-    assert L.moe_expert_gemm1_swiglu_gather(P, None, P, P, P, 64, 4, 64, 64, 1, P, None, P, None, _null(), 256,
+    assert L.moe_expert_gemm1_swiglu_gather(P, None, P, P, P, 64, 4, 64, 64, 0, P, None, P, None, 0, P, 256, s) == 2
+    assert L.moe_expert_gemm1_swiglu_gather(P, None, None, P, P, 64, 4, 64, 64, 1, P, None, P, None, 0, P, 256,
+                                            s) == 1
+    assert L.moe_expert_gemm1_swiglu_gather(P, None, P, P, P, 64, 4, 60, 64, 1, P, None, P, None, 0, P, 256, s) == 2
+    assert L.moe_expert_gemm1_swiglu_gather(P, None, P, P, P, 64, 4, 64, 64, 1, P, None, P, None, 0, _null(), 256,
                                             s) == 3
     # MXFP8 row quantiser: d % 32, negative T, wrong source type
     assert L.moe_quantize_mx_rows(P, 1, 4, 48, None, 0, P, P, s) == 2

@@ -453,7 +453,7 @@ def test_pair_kernel_matches_oracle(moe, name, counts, d, f):
 
 
 # ----------------------------------------------------------------------------- row-gather GEMM1
-def _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd):
+def _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd, hint=1):
     """GEMM1 reading x through row_src_token must equal GEMM1 on the permuted copy, bit for
     bit (same operand values, same MMA order); MXFP8 compares through GEMM2 (h scales live
     in the SF tile layout, whose pad bytes are unspecified)."""
@@ -469,7 +469,7 @@ def _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd):
     assert torch.equal(P["row_src_token"][:N], M["row_src_token"][:N])
     assert torch.equal(P["row_prob"][:N], M["row_prob"][:N])
     h1, hs1, _ = moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw,
-                                             rows_hint=1)
+                                             rows_hint=hint)
     if w.dtype == "mxfp8":
         xq, xs = moe.moe_quantize_mx_rows(xd, pair_to_row=M["pair_to_row"])
         torch.cuda.synchronize()
@@ -477,7 +477,8 @@ def _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd):
         assert torch.equal(P["perm_x"][:N], xq[rst])  # one quantisation rule, per row or per token
         h2, hs2, ws = moe.moe_expert_gemm1_swiglu_gather(xq, xs, M["row_src_token"], M["offsets"], M["row_prob"], pw)
     else:
-        h2, hs2, ws = moe.moe_expert_gemm1_swiglu_gather(xd, None, M["row_src_token"], M["offsets"], M["row_prob"], pw)
+        h2, hs2, ws = moe.moe_expert_gemm1_swiglu_gather(xd, None, M["row_src_token"], M["offsets"], M["row_prob"], pw,
+                                                         rows_hint=hint)
     Y1, _ = moe.moe_expert_gemm2(h1, hs1, P["offsets"], pw, rows_hint=1)
     Y2, _ = moe.moe_expert_gemm2(h2, hs2, M["offsets"], pw, rows_hint=1)
     torch.cuda.synchronize()
@@ -506,6 +507,30 @@ def test_gather_gemm1_odd_units(moe, dtype):
     w = Workload("gather_odd", lg.shape[0], d, f, len(counts), 1, 0, len(counts), dtype)
     Wg, Wu, Wd = gen_weights(w)
     assert _gather_vs_copy(moe, w, gen_x(w), lg, Wg, Wu, Wd) == sum(counts)
+
+
+@pytest.mark.parametrize("name,counts,d,f", PAIR_CASES, ids=[c[0] for c in PAIR_CASES])
+def test_pair_gather_gemm1_matches_pair_copy(moe, name, counts, d, f):
+    """GEMM1 on CTA pairs with each CTA gathering its 128 token rows (the peer's stages
+    relayed to the leader) equals GEMM1 on CTA pairs fed by TMA from the permuted copy,
+    bit for bit: segment edges at 1/127/128/129/255/256/257 rows, K and N tails, one
+    expert holding every token, odd unit counts."""
+    E = len(counts)
+    lg = _forced_logits(counts, E, seed=len(name) + 1)
+    w = Workload(name, lg.shape[0], d, f, E, 1, 0, E, "bf16")
+    Wg, Wu, Wd = gen_weights(w)
+    assert _gather_vs_copy(moe, w, gen_x(w), lg, Wg, Wu, Wd, hint=4096) == sum(counts)
+
+
+def test_pair_gather_layer(moe):
+    """The bf16 layer at 2048 expected rows per expert runs GEMM1 on CTA pairs with the row
+    gather (no permuted copy) and matches the oracle."""
+    w = Workload("pair_gather_layer", 4096, 256, 256, 16, 8, 0, 16, "bf16", ("normal", 0.5))
+    assert moe.moe_layer_gemm1_pairs(w.T, w.d, w.k, w.E, w.E_loc, "bf16")
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    y = gpu_layer(moe, w, x, lg, Wg, Wu, Wd)
+    assert rel_l2(to_np(y), oracle_layer(w, x, lg, Wg, Wu, Wd)) <= TOL["bf16"]
 
 
 def test_quantize_rows_matches_oracle(moe):
