@@ -195,8 +195,10 @@ size_t moe_mx_weight_scale_bytes(int E_loc, int rows, int K);
  *   workspace device >= moe_grouped_mlp_workspace_size(...) bytes, 256-byte aligned
  *   rows_hint  expected rows per local expert (e.g. moe_rows_hint(T, k, E)); it only picks
  *              the kernel shape (bf16 GEMM1 runs on CTA pairs with 256-row tiles from 2048
- *              expected rows up, and from 256 to 1023 when d >= 4096; bf16 GEMM2 from 128),
- *              never the result's meaning; <= 0 uses N_cap / E_loc.
+ *              expected rows up, and from 256 to 1023 when d >= 4096; bf16 GEMM2 from 128;
+ *              MXFP8 GEMMs from 65536, as the block-scaled pair kernel measured slower than
+ *              the 1-CTA one on every shape tried), never the result's meaning; <= 0 uses
+ *              N_cap / E_loc.
  * Requires d % 8 == 0 and f % 32 == 0 (bf16); d % 128 == 0 and f % 128 == 0 (MXFP8). */
 moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                            const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,

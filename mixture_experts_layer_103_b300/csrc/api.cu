@@ -127,8 +127,17 @@ static moe_status check_mlp_shape(int d, int f, int E_loc, moe_dtype dt) {
 // Callers of the single GEMMs can force either with rows_hint.
 constexpr int kPairRowsThreshold = 2048;
 
+// MXFP8 on CTA pairs (block-scaled cta_group::2 MMAs): correct, but measured slower than
+// the 1-CTA kernel at every shape tried on B300 (dense 16384 rows, d = 7168: GEMM1 388 vs
+// 373 us, GEMM2 256 vs 237; EP64 slice GEMM2 70 vs 58; Zipf EP8 slice GEMM1 186 vs 158):
+// the per-stage scale copies into TMEM cost ~13 % of the main loop and two 256-column
+// accumulators do not fit beside the scales.  Taken only from this many expected rows per
+// expert (no workload here comes near it).
+constexpr int kPairRowsThresholdMx = 1 << 16;
+
 static bool use_pair(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint, int K) {
   const int64_t rows = rows_hint > 0 ? rows_hint : n_cap / (E_loc > 0 ? E_loc : 1);
+  if (dt == MOE_MXFP8) return rows >= kPairRowsThresholdMx;
   return dt == MOE_BF16 && (rows >= kPairRowsThreshold || (rows >= 256 && rows < 1024 && K >= 4096));
 }
 
@@ -141,6 +150,7 @@ constexpr int kPairRowsThresholdGemm2 = 128;
 
 static bool use_pair_gemm2(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint) {
   const int64_t rows = rows_hint > 0 ? rows_hint : n_cap / (E_loc > 0 ? E_loc : 1);
+  if (dt == MOE_MXFP8) return rows >= kPairRowsThresholdMx;
   return dt == MOE_BF16 && rows >= kPairRowsThresholdGemm2;
 }
 

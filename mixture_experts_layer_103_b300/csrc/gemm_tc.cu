@@ -366,11 +366,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + extra
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       // TMA stores for the bf16 outputs except the ScaledSwiGLU backward's three per block,
       // which measured faster with plain stores (two staging buffers serialise them)
+      auto release = [&]() {  // the accumulator may be overwritten by the next tile's MMAs
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+      };
       if (ut.valid)
-        epilogue_warp<EPI, !MX && EPI != EPI_DSWIGLU>(g, tmO, tl, tbase, BN, q, lane, est);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+        epilogue_warp<EPI, !MX && EPI != EPI_DSWIGLU>(g, tmO, tl, tbase, BN, q, lane, est, release);
+      else
+        release();
     }
     if (lane == 0) ptx::bulk_wait_all();  // this warp's TMA stores have completed
 
@@ -563,13 +567,13 @@ static GemmArgs base_args(const int32_t* offsets, int E_loc, int32_t* err, uint6
 // GEMM1 + fused scaled SwiGLU on the tensor cores.
 //   bf16:  perm_x bf16 [N_cap, d] -> h bf16 [N_cap, f]
 //   mxfp8: perm_x E4M3 [N_cap, d] + SF -> h E4M3 [N_cap, f] + SF
-cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu,
+cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu, bool mx,
                              cudaStream_t st);
-cudaError_t launch_pair_gemm_combine(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
+cudaError_t launch_pair_gemm_combine(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool mx,
                                      cudaStream_t st);
 cudaError_t launch_pair_gemm1_gather(const void* B, const GemmArgs& g, cudaStream_t st);
 
-// pair: bf16 only -- run the CTA-pair kernel (large M per expert) instead of the 1-CTA one.
+// pair: run the CTA-pair kernel (large M per expert) instead of the 1-CTA one.
 cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
                             int64_t N_cap, int E_loc, int d, int f, bool mx, bool pair, const void* Wgu,
                             const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns,
@@ -585,8 +589,8 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
   g.row_prob = row_prob;
   g.a_sf = perm_sf;
   g.b_sf = Wgu_sf;
+  if (pair) return launch_pair_gemm(perm_x, N_cap, Wgu, g, true, mx, st);
   if (mx) return launch_gemm_inst<true, EPI_SWIGLU_MX>(perm_x, N_cap, Wgu, g, st);
-  if (pair) return launch_pair_gemm(perm_x, N_cap, Wgu, g, true, st);
   return launch_gemm_inst<false, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
 }
 
@@ -669,8 +673,8 @@ cudaError_t launch_tc_gemm2_combine(const void* h, const uint8_t* h_sf, const in
   g.tok_nloc = tok_nloc;
   g.y = y;
   g.T = T;
+  if (pair) return launch_pair_gemm_combine(h, N_cap, Wd, g, mx, st);
   if (mx) return launch_gemm_inst<true, EPI_COMBINE>(h, N_cap, Wd, g, st);
-  if (pair) return launch_pair_gemm_combine(h, N_cap, Wd, g, st);
   return launch_gemm_inst<false, EPI_COMBINE>(h, N_cap, Wd, g, st);
 }
 
@@ -686,8 +690,8 @@ cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* o
   g.out_rows = N_cap;
   g.a_sf = h_sf;
   g.b_sf = Wd_sf;
+  if (pair) return launch_pair_gemm(h, N_cap, Wd, g, false, mx, st);
   if (mx) return launch_gemm_inst<true, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
-  if (pair) return launch_pair_gemm(h, N_cap, Wd, g, false, st);
   return launch_gemm_inst<false, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
 }
 

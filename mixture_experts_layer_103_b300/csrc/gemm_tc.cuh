@@ -230,9 +230,12 @@ __device__ __forceinline__ void zero_rows(const GemmArgs& g, int zw, int nzw, in
 // + 32 up columns with bf16 or MXFP8 (one 32-value block per thread) output (GEMM1).
 // tbase = TMEM address of this warp's lane quarter and accumulator; q = lane quarter;
 // tl.row0/tl.rows describe the 128-row tile the slab belongs to.
-template <int EPI, bool TMA>
+// release(): called by every lane once this warp's last TMEM read of the tile is done (it
+// frees the accumulator for the next tile's MMAs); the MXFP8 SwiGLU epilogue calls it
+// before its global stores, the others at the end.
+template <int EPI, bool TMA, typename Release>
 __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const OutMaps& om, const Tile& tl, uint32_t tbase,
-                                              int BN, int q, int lane, EpiStage& st) {
+                                              int BN, int q, int lane, EpiStage& st, Release&& release) {
   const int r = q * 32 + lane;                         // row within the tile
   const int rows_valid = max(0, min(32, tl.rows - q * 32));
   const int64_t row_first = static_cast<int64_t>(tl.row0) + q * 32;
@@ -365,6 +368,56 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const OutMaps& 
                             rows_valid, 4);
       if (live) g.dp_part[row * (fdim / 32) + fc / 32] = dp;
     }
+  } else if constexpr (EPI == EPI_SWIGLU_MX) {
+    // The whole tile's h is computed and quantised into registers first (4 blocks of 32
+    // values: 8 words of E4M3 codes and one E8M0 byte each), the accumulator is released,
+    // and only then are the codes and scales stored: with one accumulator in TMEM (256-wide
+    // MXFP8 tiles) the next tile's MMAs overlap these stores.
+    const float p = r < tl.rows ? __ldg(g.row_prob + row_first + lane) : 0.0f;
+    const int fdim = g.n_out / 2;
+    constexpr int MAXB = 4;  // BN / 64 <= 4
+    const int nb = BN / 64;
+    uint32_t W[MAXB][8];
+    int XS[MAXB];
+#pragma unroll
+    for (int sb = 0; sb < MAXB; ++sb) {
+      XS[sb] = 0;
+      if (sb < nb) {
+        uint32_t gv[32], uv[32];
+        ptx::tmem_ld32(tbase + sb * 64, gv);       // 32 gate columns
+        ptx::tmem_ld32(tbase + sb * 64 + 32, uv);  // the matching 32 up columns
+        ptx::tmem_ld_wait();
+        float h[32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float gg = __uint_as_float(gv[i]);
+          h[i] = p * __fdividef(gg, 1.0f + __expf(-gg)) * __uint_as_float(uv[i]);
+          amax = fmaxf(amax, fabsf(h[i]));
+        }
+        const int X = mx_exponent(amax);
+        const float inv = mx_inv_scale(X);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          W[sb][j] = static_cast<uint32_t>(e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv)) |
+                     (static_cast<uint32_t>(e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv)) << 16);
+        XS[sb] = X;
+      }
+    }
+    release();
+#pragma unroll
+    for (int sb = 0; sb < MAXB; ++sb) {
+      if (sb < nb) {
+        const int fc = tl.n0 / 2 + sb * 32;  // first h column of this block
+        const uint4 pk[2] = {make_uint4(W[sb][0], W[sb][1], W[sb][2], W[sb][3]),
+                             make_uint4(W[sb][4], W[sb][5], W[sb][6], W[sb][7])};
+        warp_store_rows<2>(st.buf, pk, lane, static_cast<uint8_t*>(g.out) + row_first * g.ld_out + fc, g.ld_out,
+                           rows_valid, fc < fdim ? 2 : 0);
+        if (r < tl.rows && fc < fdim)
+          g.out_sf[sf_act_offset(tl.mt, r, fc, fdim)] = static_cast<uint8_t>(XS[sb] + 127);
+      }
+    }
+    return;
   } else {
     const float p = r < tl.rows ? __ldg(g.row_prob + row_first + lane) : 0.0f;
     const int fdim = g.n_out / 2;
@@ -430,6 +483,7 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const OutMaps& 
       }
     }
   }
+  release();
 }
 
 // 3-D K-major operand map [outer, rows, K], box [1, box_rows, 128 bytes], 128-byte swizzle.

@@ -1,4 +1,4 @@
-// Grouped GEMM on CTA pairs (tcgen05 cta_group::2), bf16, for the large-M regime.
+// Grouped GEMM on CTA pairs (tcgen05 cta_group::2), bf16 and MXFP8, for the large-M regime.
 //
 // Same computation as the 1-CTA kernel in gemm_tc.cu ("Efficient MoE training for
 // biological foundation models", section "GroupedLinear Optimizes Expert Computation":
@@ -23,27 +23,54 @@
 // barrier when their copies land; the peer's arrive on a barrier of their own, and the
 // peer's MMA warp (idle otherwise) relays each completed stage to the leader's full barrier
 // after a proxy fence, so the leader's MMA sees both halves of A.
+// MXFP8 ("MXFP8 Precision Reduces Memory Footprint": E4M3 values with one E8M0 scale per 32
+// along K, Blackwell block-scaled MMAs): 128 K values (128 bytes) per stage, block-scaled
+// MMAs (M = 256, N = 256, K = 32).  Each CTA stages its own scale atoms by TMA (its 128 rows'
+// A scales; B's scales as the pair MMA reads them), the leader copies them into both CTAs'
+// TMEM (tcgen05.cp.cta_group::2) before the stage's MMAs.  TMEM holds one 256-column
+// accumulator and two sets of scale columns, so the epilogue of a tile does not overlap the
+// next tile's main loop (as in the 1-CTA MXFP8 kernel at 256-wide tiles).
+#include <cudaTypedefs.h>
+
 #include "gemm_tc.cuh"
 
 namespace moe {
 
-struct PairSmem {
+// B's scales in each CTA's TMEM: all 256 columns of the pair tile (true), or the CTA's own
+// 128 (false).
+constexpr bool kPairSfbFull = true;
+
+template <bool MX>
+struct PairSmemT {
   static constexpr int STAGES = 6;
   static constexpr int A_BYTES = 128 * kRowBytes;  // this CTA's 128 rows of A
   static constexpr int B_BYTES = 128 * kRowBytes;  // this CTA's half of the 256 B rows
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int BK = 64;                    // bf16 K elements per stage
-  static constexpr int OFF_EPI = STAGES * STAGE_BYTES;  // epilogue staging (TMA stores)
-  static constexpr int OFF_BAR = OFF_EPI + kEpiTmaBytes;
+  static constexpr int BK = MX ? 128 : 64;         // K elements per stage (128 bytes per row)
+  static constexpr int SFA_BYTES = MX ? 512 : 0;   // one scale atom (128 rows x 128 K)
+  static constexpr int SFB_BYTES = MX ? (kPairSfbFull ? 1024 : 512) : 0;
+  static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
+  static constexpr int OFF_SF = STAGES * STAGE_BYTES;
+  static constexpr int OFF_EPI = OFF_SF + STAGES * SF_STAGE;
+  // bf16 outputs leave by TMA stores; MXFP8 keeps the padded staging of plain stores
+  static constexpr int EPI_WARP_BYTES = MX ? kEpiWarpBytes : kEpiTmaWarpBytes;
+  static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_WARP_BYTES;
   // full, empty, tmem_full[2], tmem_empty[2], drain, gathered (row-gather mode, peer CTA)
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TAB = OFF_MISC + 16;
-  static constexpr int SMEM_BYTES = OFF_TAB + 2 * (kMaxEloc + 1) * 4 + 1024;
+  // s_off, s_mtp (256-row m-tiles), s_mtp128 (128-row m-tiles: the scale layout's)
+  static constexpr int SMEM_BYTES = OFF_TAB + 3 * (kMaxEloc + 1) * 4 + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 constexpr int kPairBM = 256;  // rows of a pair tile (128 per CTA)
 constexpr int kPairBN = 256;  // columns of a pair tile
+
+// Scale-factor maps (MXFP8): the 512-byte atoms of A's and B's SF tile layouts as rows of
+// 128 uint32 (box: one atom of A; one or two consecutive atoms of B).
+struct SfMaps {
+  CUtensorMap sfa, sfb;
+};
 
 // Threads beyond the 6 GEMM warps: A-gather warps (row gather) or zero-row warps (combine).
 template <int EPI, bool GATHER>
@@ -51,11 +78,14 @@ constexpr int pair_extra_threads() {
   return GATHER ? kGatherThreads : EPI == EPI_COMBINE ? kZeroThreads : 0;
 }
 
-template <int EPI, bool GATHER>
+template <bool MX, int EPI, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_extra_threads<EPI, GATHER>(), 1)
     tc_grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                                const __grid_constant__ OutMaps tmO, const GemmArgs g) {
-  using C = PairSmem;
+                                const __grid_constant__ SfMaps tmS, const __grid_constant__ OutMaps tmO,
+                                const GemmArgs g) {
+  static_assert(!(MX && GATHER), "the MXFP8 pair kernel reads A by TMA");
+  using C = PairSmemT<MX>;
+  constexpr int NUM_ACC = MX ? 1 : 2;  // accumulators in TMEM (MXFP8: + scale columns)
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -71,6 +101,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* s_off = reinterpret_cast<int*>(smem + C::OFF_TAB);
   int* s_mtp = s_off + g.E_loc + 1;
+  int* s_mtp128 = s_mtp + g.E_loc + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
@@ -92,13 +123,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
     ptx::fence_mbar_init();
     if (!GATHER) ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    if (MX) {
+      ptx::prefetch_tmap(&tmS.sfa);
+      ptx::prefetch_tmap(&tmS.sfb);
+    }
   }
   if (warp == 1) {  // one warp in each CTA of the pair allocates the pair's TMEM
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish_pair();
   }
   pdl_wait();  // offsets, row data and scales come from the previous kernels
-  if (warp == 2) build_mtile_prefix(g.offsets, g.E_loc, kPairBM, s_off, s_mtp);
+  if (warp == 2) {
+    build_mtile_prefix(g.offsets, g.E_loc, kPairBM, s_off, s_mtp);
+    if (MX) build_mtile_prefix(g.offsets, g.E_loc, 128, s_off, s_mtp128);
+  }
   __syncwarp();
   ptx::tc_fence_before();
   ptx::cluster_sync();  // barrier inits of both CTAs visible before any cross-CTA signal
@@ -109,6 +147,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
   const int n_tiles_n = (g.n_out + kPairBN - 1) / kPairBN;
   const int total = s_mtp[g.E_loc] * n_tiles_n;
   const int num_kb = (g.K + C::BK - 1) / C::BK;
+  // 128-row m-tile of the scale layout holding this CTA's rows of tile tl
+  auto mtile128 = [&](const Tile& tl) {
+    return s_mtp128[tl.e] + (tl.row0 + 128 * static_cast<int>(rank) - s_off[tl.e]) / 128;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -126,10 +168,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
           if (!ptx::mbar_wait(empty_bar(s), ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); ok = false; break; }
           const uint32_t fb_leader = ptx::mapa_shared(full_bar(s), 0);
           // in row-gather mode the gather warps fill A themselves
-          if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), GATHER ? 2 * C::B_BYTES : 2 * C::STAGE_BYTES);
+          if (leader)
+            ptx::mbar_arrive_expect_tx(full_bar(s), GATHER ? 2 * C::B_BYTES : 2 * (C::STAGE_BYTES + C::SF_STAGE));
           const uint32_t st_addr = sbase + s * C::STAGE_BYTES;
           if (!GATHER) ptx::tma_load_3d_pair(st_addr, &tmA, fb_leader, kb * C::BK, a_row, 0);
           ptx::tma_load_3d_pair(st_addr + C::A_BYTES, &tmB, fb_leader, kb * C::BK, b_row, tl.e);
+          if constexpr (MX) {
+            const int kg = g.K / 128;
+            const uint32_t sf_addr = sbase + C::OFF_SF + s * C::SF_STAGE;
+            ptx::tma_load_2d_pair(sf_addr, &tmS.sfa, fb_leader, 0, mtile128(tl) * kg + kb);
+            const int b_atom = (tl.e * kg + kb) * (g.n_out / 128) + tl.n0 / 128 + (kPairSfbFull ? 0 : static_cast<int>(rank));
+            ptx::tma_load_2d_pair(sf_addr + C::SFA_BYTES, &tmS.sfb, fb_leader, 0, b_atom);
+          }
           ++issued;
           if (++s == C::STAGES) { s = 0; ph ^= 1u; }
         }
@@ -143,14 +193,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ------------------------------------------------------------------ MMA issuer (leader)
-      const uint32_t idesc = ptx::idesc_bf16(kPairBM, kPairBN);
+      const uint32_t idesc = MX ? ptx::idesc_mxf8(kPairBM, kPairBN) : ptx::idesc_bf16(kPairBM, kPairBN);
+      constexpr int SF_COLS = 4 + (kPairSfbFull ? 8 : 4);  // A's scales + B's, per stage
       int s = 0;
-      uint32_t ph = 0;
+      uint32_t ph = 0, kbg = 0;
       int it = 0;
       bool ok = true;
       for (int t = pair; t < total && ok; t += npairs, ++it) {
-        const int acc = it & 1;
-        const uint32_t acc_ph = static_cast<uint32_t>((it >> 1) & 1);
+        const int acc = NUM_ACC == 2 ? (it & 1) : 0;
+        const uint32_t acc_ph = NUM_ACC == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
         if (!ptx::mbar_wait(tempty_bar(acc), acc_ph ^ 1u, g.timeout_ns)) { gemm_abort(g, s_abort); break; }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kPairBN);
@@ -163,10 +214,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
           ptx::tc_fence_after();
           const uint32_t a_addr = sbase + s * C::STAGE_BYTES;
           const uint32_t b_addr = a_addr + C::A_BYTES;
+          if constexpr (MX) {
+            const uint32_t sf_addr = sbase + C::OFF_SF + s * C::SF_STAGE;
+            const uint32_t sf_col = tmem_base + NUM_ACC * kPairBN + (kbg & 1u) * SF_COLS;
+            ptx::tmem_cp_32x128b_x4_pair(sf_col, ptx::sdesc_sf(sf_addr));
+            ptx::tmem_cp_32x128b_x4_pair(sf_col + 4, ptx::sdesc_sf(sf_addr + C::SFA_BYTES));
+            if (kPairSfbFull) ptx::tmem_cp_32x128b_x4_pair(sf_col + 8, ptx::sdesc_sf(sf_addr + C::SFA_BYTES + 512));
 #pragma unroll
-          for (int k = 0; k < C::BK / 16; ++k)
-            ptx::mma_bf16_pair(d_tmem, ptx::sdesc_sw128(a_addr + k * 32), ptx::sdesc_sw128(b_addr + k * 32), idesc,
-                               (kb | k) != 0);
+            for (int k = 0; k < C::BK / 32; ++k)
+              ptx::mma_mxf8_pair(d_tmem, ptx::sdesc_sw128(a_addr + k * 32), ptx::sdesc_sw128(b_addr + k * 32),
+                                 ptx::idesc_sf_id(idesc, k), sf_col, sf_col + 4, (kb | k) != 0);
+            ++kbg;
+          } else {
+#pragma unroll
+            for (int k = 0; k < C::BK / 16; ++k)
+              ptx::mma_bf16_pair(d_tmem, ptx::sdesc_sw128(a_addr + k * 32), ptx::sdesc_sw128(b_addr + k * 32), idesc,
+                                 (kb | k) != 0);
+          }
           ptx::mma_commit_pair(empty_bar(s), 0x3);  // frees the stage in both CTAs
           if (++s == C::STAGES) { s = 0; ph ^= 1u; }
         }
@@ -198,16 +262,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
   } else if (warp < 6) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
-    EpiStage est{smem + C::OFF_EPI + (warp - 2) * kEpiTmaWarpBytes,
-                 sbase + static_cast<uint32_t>(C::OFF_EPI + (warp - 2) * kEpiTmaWarpBytes), 0, -1};
+    EpiStage est{smem + C::OFF_EPI + (warp - 2) * C::EPI_WARP_BYTES,
+                 sbase + static_cast<uint32_t>(C::OFF_EPI + (warp - 2) * C::EPI_WARP_BYTES), 0, -1};
     int it = 0;
     for (int t = pair; t < total; t += npairs, ++it) {
       if (*s_abort) break;
       Tile tl = decode_tile(t, n_tiles_n, kPairBN, s_off, s_mtp, g.E_loc, kPairBM);
+      if (MX) tl.mt = mtile128(tl);                        // the scale layout's m-tile of this CTA's rows
       tl.row0 += 128 * static_cast<int>(rank);             // this CTA's rows of the tile
       tl.rows = max(0, min(128, tl.rows - 128 * static_cast<int>(rank)));
-      const int acc = it & 1;
-      const uint32_t acc_ph = static_cast<uint32_t>((it >> 1) & 1);
+      const int acc = NUM_ACC == 2 ? (it & 1) : 0;
+      const uint32_t acc_ph = NUM_ACC == 2 ? static_cast<uint32_t>((it >> 1) & 1) : static_cast<uint32_t>(it & 1);
       int okw = 0;
       if (lane == 0) okw = ptx::mbar_wait(tfull_bar(acc), acc_ph, g.timeout_ns) ? 1 : 0;
       okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -215,10 +280,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
       (void)ptx::mbar_try_wait(tfull_bar(acc), acc_ph);  // completed phase: acquire for every lane
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kPairBN);
-      epilogue_warp<EPI, true>(g, tmO, tl, tbase, kPairBN, q, lane, est);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+      auto release = [&]() {  // the accumulator may be overwritten by the next tile's MMAs
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+      };
+      epilogue_warp<EPI, !MX>(g, tmO, tl, tbase, kPairBN, q, lane, est, release);
     }
     if (lane == 0) ptx::bulk_wait_all();  // this warp's TMA stores have completed
 
@@ -285,44 +352,79 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
   }
 }
 
+// 2-D map over an SF tile layout buffer of n_atoms 512-byte atoms, box = atoms_per_box atoms.
+static bool make_sf_map(CUtensorMap* m, const void* base, uint64_t n_atoms, uint32_t atoms_per_box) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!enc) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  const cuuint64_t dims[2] = {128, n_atoms};
+  const cuuint64_t strides[1] = {512};
+  const cuuint32_t box[2] = {128, atoms_per_box};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A: the permuted rows [a_rows, K] (TMA), or unused (nullptr) in row-gather mode.
-template <int EPI, bool GATHER = false>
+template <bool MX, int EPI, bool GATHER = false>
 static cudaError_t launch_pair_inst(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, cudaStream_t st) {
+  using C = PairSmemT<MX>;
   CUtensorMap ta = {}, tb;
-  if (!GATHER && !make_operand_map(&ta, A, false, g.K, a_rows, 1, 128)) return cudaErrorInvalidValue;
-  if (!make_operand_map(&tb, B, false, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
+  if (!GATHER && !make_operand_map(&ta, A, MX, g.K, a_rows, 1, 128)) return cudaErrorInvalidValue;
+  if (!make_operand_map(&tb, B, MX, g.K, g.n_out, g.E_loc, 128)) return cudaErrorInvalidValue;
+  SfMaps ts;
+  memset(&ts, 0, sizeof(ts));
+  if (MX) {
+    const uint64_t kg = static_cast<uint64_t>(g.K / 128);
+    if (!make_sf_map(&ts.sfa, g.a_sf, static_cast<uint64_t>(mx_tiles_cap(a_rows, g.E_loc)) * kg, 1))
+      return cudaErrorInvalidValue;
+    if (!make_sf_map(&ts.sfb, g.b_sf, static_cast<uint64_t>(g.E_loc) * kg * (g.n_out / 128), kPairSfbFull ? 2 : 1))
+      return cudaErrorInvalidValue;
+  }
   OutMaps tmo;
   memset(&tmo, 0, sizeof(tmo));
-  if (!make_out_maps(&tmo, g)) return cudaErrorInvalidValue;
-  auto kern = tc_grouped_gemm_pair_kernel<EPI, GATHER>;
+  if (!MX && !make_out_maps(&tmo, g)) return cudaErrorInvalidValue;
+  auto kern = tc_grouped_gemm_pair_kernel<MX, EPI, GATHER>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmem::SMEM_BYTES);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int grid = num_sms() & ~1;  // whole pairs
   const int threads = kGemmThreads + pair_extra_threads<EPI, GATHER>();
-  return launch_pdl(kern, dim3(grid), dim3(threads), PairSmem::SMEM_BYTES, st, ta, tb, tmo, g);
+  return launch_pdl(kern, dim3(grid), dim3(threads), C::SMEM_BYTES, st, ta, tb, ts, tmo, g);
 }
 
-cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu,
+// swiglu: GEMM1 (+ scaled SwiGLU, MXFP8: + requantisation of h), else GEMM2 (bf16 store).
+cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu, bool mx,
                              cudaStream_t st) {
-  return swiglu ? launch_pair_inst<EPI_SWIGLU_BF16>(A, a_rows, B, g, st)
-                : launch_pair_inst<EPI_STORE_BF16>(A, a_rows, B, g, st);
+  if (mx)
+    return swiglu ? launch_pair_inst<true, EPI_SWIGLU_MX>(A, a_rows, B, g, st)
+                  : launch_pair_inst<true, EPI_STORE_BF16>(A, a_rows, B, g, st);
+  return swiglu ? launch_pair_inst<false, EPI_SWIGLU_BF16>(A, a_rows, B, g, st)
+                : launch_pair_inst<false, EPI_STORE_BF16>(A, a_rows, B, g, st);
 }
 
-cudaError_t launch_pair_gemm_combine(const void* A, int64_t a_rows, const void* B, const GemmArgs& g,
+cudaError_t launch_pair_gemm_combine(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool mx,
                                      cudaStream_t st) {
-  return launch_pair_inst<EPI_COMBINE>(A, a_rows, B, g, st);
+  return mx ? launch_pair_inst<true, EPI_COMBINE>(A, a_rows, B, g, st)
+            : launch_pair_inst<false, EPI_COMBINE>(A, a_rows, B, g, st);
 }
 
 // GEMM1 + scaled SwiGLU on CTA pairs with A gathered from the token rows (g.gx, g.row_token).
 cudaError_t launch_pair_gemm1_gather(const void* B, const GemmArgs& g, cudaStream_t st) {
-  return launch_pair_inst<EPI_SWIGLU_BF16, true>(nullptr, 0, B, g, st);
+  return launch_pair_inst<false, EPI_SWIGLU_BF16, true>(nullptr, 0, B, g, st);
 }
 
 }  // namespace moe

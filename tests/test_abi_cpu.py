@@ -169,7 +169,8 @@ def test_gemm1_kernel_choice(lib):
     assert not pairs(8192, 2048, 8, 256, 4, "bf16")      # 256 rows but d < 4096
     assert pairs(16384, 7168, 1, 1, 1, "bf16")           # dense: 16384 rows
     assert pairs(4096, 1024, 8, 16, 16, "bf16")          # 2048 rows
-    assert not pairs(8192, 7168, 8, 256, 4, "mxfp8")     # no MXFP8 pair kernel
+    assert not pairs(8192, 7168, 8, 256, 4, "mxfp8")     # MXFP8 pairs only from 65536 rows per expert
+    assert not pairs(16384, 7168, 1, 1, 1, "mxfp8")
     assert not pairs(8192, 7168, 8, 256, 4, "f32")
     with pytest.raises(ValueError):
         pairs(8192, 7168, 8, 256, 512, "bf16")            # E_loc > E

@@ -52,15 +52,16 @@ def _ulp_bf16(v):
     return np.exp2(e - 7)
 
 
-def _run(moe, w: Workload, rows_wanted: int | None):
-    """MXFP8 permute -> GEMM1 -> GEMM2 through the separate entry points; returns the
-    device results and the oracle-side operands for a set of permuted rows."""
+def _run(moe, w: Workload, rows_wanted: int | None, hint=None):
+    """MXFP8 permute -> GEMM1 -> GEMM2 through the separate entry points (rows_hint: the
+    layer's own, or a forced kernel shape); returns the device results and the oracle-side
+    operands for a set of permuted rows."""
     x, lg = gen_x(w), gen_logits(w)
     Wg, Wu, Wd = gen_weights(w)
     pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), "mxfp8")
     ids, probs = moe.moe_route_topk(to_dev(lg), w.k)
     P = moe.moe_permute(to_dev(x), ids, probs, w.e0, w.E_loc, "mxfp8")
-    hint = moe.moe_rows_hint(w.T, w.k, w.E)
+    hint = moe.moe_rows_hint(w.T, w.k, w.E) if hint is None else hint
     h, hs, ws1 = moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw,
                                              rows_hint=hint)
     Y2, ws2 = moe.moe_expert_gemm2(h, hs, P["offsets"], pw, rows_hint=hint)
@@ -95,15 +96,19 @@ CASES = [
     Workload("mx_zipf", 1024, 512, 256, 256, 8, 0, 32, "mxfp8", ("zipf", 1.1)),
 ]
 FULL = [("mxfp8_ep64_T8192", 96), ("mxfp8_ep8_zipf_T8192", 96)]
+MX_PAIR_HINT = 1 << 16  # expected rows per expert from which MXFP8 GEMMs run on CTA pairs
 
 
 def _cases():
-    return [(w, None) for w in CASES] + [(WORKLOADS[n], r) for n, r in FULL]
+    # hint 65536: both GEMMs on CTA pairs (block-scaled cta_group::2 MMAs); 1: the 1-CTA kernel
+    out = [(w, None, h) for w in CASES for h in (1, MX_PAIR_HINT)]
+    return out + [(WORKLOADS[n], r, h) for n, r in FULL for h in (None, MX_PAIR_HINT)]
 
 
-@pytest.mark.parametrize("w,rows_wanted", _cases(), ids=[w.name for w, _ in _cases()])
-def test_mx_h_quantisation_and_gemm2(moe, w, rows_wanted):
-    R = _run(moe, w, rows_wanted)
+@pytest.mark.parametrize("w,rows_wanted,hint", _cases(),
+                         ids=[f"{w.name}-{'auto' if h is None else h}" for w, _, h in _cases()])
+def test_mx_h_quantisation_and_gemm2(moe, w, rows_wanted, hint):
+    R = _run(moe, w, rows_wanted, hint)
     rows, re_, tok = R["rows"], R["row_expert"], R["tok"]
     d, f, E_loc = w.d, w.f, w.E_loc
     # ---- GEMM1 + ScaledSwiGLU: fp64 h of these rows from the MXFP8 operands

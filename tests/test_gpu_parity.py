@@ -452,6 +452,37 @@ def test_pair_kernel_matches_oracle(moe, name, counts, d, f):
     assert rel_l2(to_np(ys[4096]), to_np(ys[1])) <= 1e-2
 
 
+MX_PAIR_CASES = [
+    ("mx_pair_edges", [1, 127, 128, 129, 255, 256, 257, 600], 256, 256),
+    ("mx_pair_one_expert", [0, 0, 1100, 0], 384, 128),   # d % 256 == 128: a half-width last n-tile
+    ("mx_pair_tails", [300, 0, 513, 77], 512, 384),
+]
+
+
+@pytest.mark.parametrize("name,counts,d,f", MX_PAIR_CASES, ids=[c[0] for c in MX_PAIR_CASES])
+def test_mx_pair_kernel_matches_oracle(moe, name, counts, d, f):
+    """MXFP8 GEMMs on CTA pairs (block-scaled cta_group::2, forced by rows_hint = 65536) vs
+    the oracle and vs the 1-CTA MXFP8 kernel."""
+    E = len(counts)
+    lg = _forced_logits(counts, E, seed=len(name) + 3)
+    w = Workload(name, lg.shape[0], d, f, E, 1, 0, E, "mxfp8")
+    x = gen_x(w)
+    Wg, Wu, Wd = gen_weights(w)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), "mxfp8")
+    ids, probs = moe.moe_route_topk(to_dev(lg), 1)
+    P = moe.moe_permute(to_dev(x), ids, probs, 0, E, "mxfp8")
+    ys = {}
+    for hint in (1, 1 << 16):
+        Y2, ws = moe.moe_grouped_mlp(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, rows_hint=hint)
+        ys[hint] = moe.moe_unpermute_combine(Y2, P["pair_to_row"], "mxfp8")
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_error(ws) == 0
+    yo = oracle_layer(w, x, lg, Wg, Wu, Wd)
+    for hint, y in ys.items():
+        assert rel_l2(to_np(y), yo) <= TOL["mxfp8"], hint
+    assert rel_l2(to_np(ys[1 << 16]), to_np(ys[1])) <= 1e-2
+
+
 # ----------------------------------------------------------------------------- row-gather GEMM1
 def _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd, hint=1):
     """GEMM1 reading x through row_src_token must equal GEMM1 on the permuted copy, bit for
