@@ -672,8 +672,9 @@ def run_backward(args, w):
     import torch
     import torch.distributed as dist
 
-    if w.dtype != "bf16":
-        raise SystemExit("the backward is bf16 only")
+    if w.dtype not in ("bf16", "mxfp8"):
+        raise SystemExit("the backward is bf16 or MXFP8")
+    mx = w.dtype == "mxfp8"
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     if world > 1:
@@ -685,14 +686,27 @@ def run_backward(args, w):
     wr = w.replace(seed=w.seed + rank)
     xd, lgd, dyd = to_dev(gen_x(wr)), to_dev(gen_logits(wr)), to_dev(gen_dy(wr))
     Wg, Wu, Wd = (to_dev(a) for a in gen_weights(w))
-    pw = moe.moe_pack_weights(Wg, Wu, Wd, "bf16")
-    WguT = moe.moe_pack_weights_backward(Wg, Wu)
-    del Wg, Wu
-    # the training forward keeps the routing and the gate/up pre-activations for the backward
-    _, ids, probs, gu, _ = moe.moe_layer_forward_train(xd, lgd, w.E, w.k, w.e0, pw)
-    out, ws = moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, gu_saved=gu)
+    if mx:
+        # MXFP8: g, u recomputed on the block-scaled tensor cores inside the backward
+        pw = moe.moe_pack_weights(Wg, Wu, Wd, "mxfp8")
+        bw = moe.moe_pack_weights_backward_mx(Wg, Wu, Wd)
+        del Wg, Wu, Wd
+        ids, probs = moe.moe_route_topk(lgd, w.k)
+
+        def bwd(ws=None, out=None):
+            return moe.moe_layer_backward_mx(xd, dyd, ids, probs, w.E, w.e0, pw, bw, ws=ws, out=out)
+    else:
+        pw = moe.moe_pack_weights(Wg, Wu, Wd, "bf16")
+        WguT = moe.moe_pack_weights_backward(Wg, Wu)
+        del Wg, Wu
+        # the training forward keeps the routing and the gate/up pre-activations for the backward
+        _, ids, probs, gu, _ = moe.moe_layer_forward_train(xd, lgd, w.E, w.k, w.e0, pw)
+
+        def bwd(ws=None, out=None):
+            return moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, ws=ws, out=out, gu_saved=gu)
+    out, ws = bwd()
     for _ in range(args.warmup):
-        moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, ws=ws, out=out, gu_saved=gu)
+        bwd(ws=ws, out=out)
     torch.cuda.synchronize()
     if moe.moe_get_device_error(ws) != 0:
         raise RuntimeError("device error during warm-up")
@@ -704,7 +718,7 @@ def run_backward(args, w):
     cs.wait_stream(torch.cuda.current_stream())
     with torch.cuda.graph(g, stream=cs):
         for _ in range(args.steps):
-            moe.moe_layer_backward(xd, dyd, ids, probs, w.E, w.e0, pw, Wd, WguT, ws=ws, out=out, gu_saved=gu)
+            bwd(ws=ws, out=out)
     g.replay()
     torch.cuda.synchronize()
     e0_, e1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -725,22 +739,24 @@ def run_backward(args, w):
     ms = max_over_ranks(e0_.elapsed_time(e1_) / args.steps, torch.device("cuda", local))
     value = job_tokens_per_s(w.T, world, ms)
     # the backward's GEMM work (g, u saved by the training forward): dh 2NDF, dx 4NDF,
-    # weight gradients 6NDF
+    # weight gradients 6NDF (MXFP8: + the 4NDF recompute of g, u)
     flops = 12.0 * N * w.d * w.f
     floor_s, floor_terms = backward_floor(w, N, nonempty, pk)
     line = {
         "metric": "MoE-layer backward tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+e8m0 (mxfp8)" if mx else "bf16",
+        "data": "synthetic (seeded)",
         "config": workload_config(w), "pass": "backward",
         "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
                      "kernel": "whole backward (12 N d f FLOP)", "traffic": None, "peak_kind": pk_kind},
-        "N_pairs": N, "gpu_launches": 11 * args.steps, "clocks": clk,
+        "N_pairs": N, "gpu_launches": (19 if mx else 11) * args.steps, "clocks": clk,
         "per_kernel_floor": {"roofline_us": floor_s * 1e6, "measured_us": ms * 1e3, "frac": floor_s / (ms * 1e-3),
                              "terms_us": {k: v * 1e6 for k, v in floor_terms.items()},
                              "note": "sum over the backward's kernels of max(FLOPs / bf16 peak, bytes / HBM)"},
-        "saved_preactivations": "from moe_layer_forward_train (no recompute)",
+        "saved_preactivations": ("recomputed on the block-scaled tensor cores (4 N d f more FLOP, not counted "
+                                 "above)" if mx else "from moe_layer_forward_train (no recompute)"),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

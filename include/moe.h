@@ -387,6 +387,50 @@ moe_status moe_layer_forward_train(const void* x, const float* logits, int T, in
 moe_status moe_pack_weights_backward(const void* W_gate, const void* W_up, moe_dtype src_dtype, int E_loc, int d,
                                      int f, void* WguT_packed, moe_stream_t stream);
 
+/* Layer backward, MXFP8 [BIO "GroupedLinear ...": the fused GroupedMLP's backward; "MXFP8
+ * Precision Reduces Memory Footprint": 8-bit values with one E8M0 scale per 32 consecutive
+ * values, Blackwell MXFP8 GEMMs].  The gradients of L = sum_t dy_t . y_t for the MXFP8 layer
+ * of moe_layer_forward (x rows and W_gate, W_up quantised along d), every backward GEMM
+ * reading its two operands quantised in 32-blocks along that GEMM's own contraction axis
+ * (the rule of moe_pack_weights):
+ *   g, u = x W_gate, x W_up            recomputed on the block-scaled tensor cores
+ *   dh = dy W_down^T                   dy rows and W_down along d; block-scaled MMAs, the
+ *                                      ScaledSwiGLU backward (exact, fp32) in the epilogue
+ *   dx_row = dg W_gate^T + du W_up^T   dg, du rows and W_gate, W_up along f; block-scaled
+ *   dW_down_e = h^T dy, dW_gate_e = x^T dg, dW_up_e = x^T du
+ *                                      h, dy, x, dg, du quantised column-wise in 32-row
+ *                                      blocks of each expert's segment (the last block
+ *                                      padded with zeros); the dequantised values (code *
+ *                                      2^X, exact in bf16) feed the bf16 tensor-core
+ *                                      weight-gradient kernel, fp32 accumulate and output
+ *   dlogits as moe_layer_backward.
+ * g, u, dg, du and h are rounded to bf16 once before their quantisation.
+ *   x, dy              device bf16 [T, d]
+ *   topk_ids/probs     the forward's routing [T, k]
+ *   Wgu_packed, Wgu_scale   moe_pack_weights(..., MOE_MXFP8): the forward's gate/up codes
+ *   Wd_q, Wd_scale, WguT_q, WguT_scale   moe_pack_weights_backward_mx
+ *   dx (bf16 [T, d]), dlogits (fp32 [T, E]), dW_gate, dW_up (fp32 [E_loc, d, f]),
+ *   dW_down (fp32 [E_loc, f, d])   device outputs, fully written
+ *   workspace          device >= moe_layer_backward_mx_workspace_size(T, d, f, k, E_loc)
+ *                      bytes, 256-byte aligned
+ * Requires d % 128 == 0 and f % 128 == 0; other rules as moe_layer_backward. */
+moe_status moe_layer_backward_mx(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
+                                 int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
+                                 const uint8_t* Wgu_scale, const uint8_t* Wd_q, const uint8_t* Wd_scale,
+                                 const uint8_t* WguT_q, const uint8_t* WguT_scale, void* dx, float* dlogits,
+                                 float* dW_gate, float* dW_up, float* dW_down, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream);
+size_t moe_layer_backward_mx_workspace_size(int T, int d, int f, int k, int E_loc);
+
+/* Backward weight operands in MXFP8 (one-off): Wd_q [E_loc, f, d] = W_down quantised along d
+ * (scales Wd_scale in the weight SF tile layout, rows f, K = d: moe_mx_weight_scale_bytes(
+ * E_loc, f, d) bytes) and WguT_q [E_loc, d, 2f] = W_gate, W_up in the packed column order of
+ * moe_pack_weights_backward quantised along f (WguT_scale: rows d, K = 2f).  Sources in the
+ * user layouts (bf16 or fp32).  Requires d % 128 == 0 and f % 128 == 0. */
+moe_status moe_pack_weights_backward_mx(const void* W_gate, const void* W_up, const void* W_down, moe_dtype src_dtype,
+                                        int E_loc, int d, int f, uint8_t* WguT_q, uint8_t* WguT_scale, uint8_t* Wd_q,
+                                        uint8_t* Wd_scale, moe_stream_t stream);
+
 /* Expert placement and replication plan (host function, no GPU) ["Wide-EP ... MoE ...
  * NVIDIA" explainer, "Load imbalance: EPLB": per-expert load decides placement, and the
  * most loaded experts get copies on several GPUs].  The page gives no algorithm; this is

@@ -58,6 +58,21 @@ cudaError_t launch_wgrad_gate_up_tc(const void* x_rows, const void* dgu, const i
 cudaError_t launch_gather_rows(const void* src, int64_t row_bytes, const int32_t* offsets, int E_loc,
                                const int32_t* row_src_token, void* dst, cudaStream_t st);
 cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t st);
+int32_t* permute_mtile_base(uint8_t* ws, int T, int E_loc);
+cudaError_t launch_gather_rows_mx(const void* src, int K, const int32_t* offsets, int E_loc,
+                                  const int32_t* mtile_base, const int32_t* row_src_token, uint8_t* dst,
+                                  uint8_t* dst_sf, cudaStream_t st);
+cudaError_t launch_pack_backward_mx(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, int E_loc, int d,
+                                    int f, uint8_t* WguT_q, uint8_t* WguT_sf, uint8_t* Wd_q, uint8_t* Wd_sf,
+                                    cudaStream_t st);
+cudaError_t launch_colquant_mx(void* buf, int C, const int32_t* offsets, int E_loc, cudaStream_t st);
+cudaError_t launch_tc_dswiglu_mx(const void* dy_q, const uint8_t* dy_sf, const int32_t* offsets,
+                                 const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* Wd_q,
+                                 const uint8_t* Wd_sf, const void* gu, void* dgu, void* h, float* dp_part, int32_t* err,
+                                 uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_tc_gemm_store_mx(const void* A, const uint8_t* a_sf, int64_t a_rows, const int32_t* offsets,
+                                    int E_loc, int K, int n_out, const void* B, const uint8_t* b_sf, void* out,
+                                    int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
 
@@ -277,9 +292,12 @@ struct BackwardWs {
   void* dxp;       // [N_cap, d] bf16
   void* x_rows;    // [N_cap, d] bf16: x and dy in routed-row order, the GEMM operands
   void* dy_rows;   //   (TMA-loadable, unlike token-indexed rows)
+  // MXFP8 backward: x and dy rows quantised along d, dg/du rows along f (E4M3 + scales in
+  // the activation SF tile layout)
+  uint8_t *x_q, *x_sf, *dy_q, *dy_sf, *dgu_q, *dgu_sf;
   size_t total;
 };
-static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int E_loc) {
+static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int E_loc, bool mx = false) {
   const int64_t n_cap = n_cap_of(T, k, E_loc);
   BackwardWs w{};
   size_t o = 0;
@@ -302,6 +320,14 @@ static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int
   w.dxp = take(static_cast<size_t>(n_cap) * d * 2);
   w.x_rows = take(static_cast<size_t>(n_cap) * d * 2);
   w.dy_rows = take(static_cast<size_t>(n_cap) * d * 2);
+  if (mx) {  // MXFP8 operands of the row-wise GEMMs (recompute, dh, dx)
+    w.x_q = take(static_cast<size_t>(n_cap) * d);
+    w.x_sf = take(mx_act_sf_bytes(n_cap, d, E_loc));
+    w.dy_q = take(static_cast<size_t>(n_cap) * d);
+    w.dy_sf = take(mx_act_sf_bytes(n_cap, d, E_loc));
+    w.dgu_q = take(static_cast<size_t>(n_cap) * 2 * f);
+    w.dgu_sf = take(mx_act_sf_bytes(n_cap, 2 * f, E_loc));
+  }
   w.total = o;
   return w;
 }
@@ -732,6 +758,96 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
   if (e == cudaSuccess) e = launch_combine(w.dxp, w.pair_to_row, T, k, d, MOE_BF16, dx, stream);
   if (e == cudaSuccess)
     e = launch_dlogits(topk_ids, topk_probs, w.pair_to_row, w.dp_part, f / 32, T, E, k, dlogits, stream);
+  if (e == cudaSuccess)
+    e = launch_wgrad_down_tc(w.h, w.dy_rows, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_down, w.err,
+                             kTimeoutNs, stream);
+  if (e == cudaSuccess)
+    e = launch_wgrad_gate_up_tc(w.x_rows, w.dgu, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_gate, dW_up,
+                                w.err, kTimeoutNs, stream);
+  return cuda_status(e);
+}
+
+moe_status moe_pack_weights_backward_mx(const void* W_gate, const void* W_up, const void* W_down, moe_dtype src_dtype,
+                                        int E_loc, int d, int f, uint8_t* WguT_q, uint8_t* WguT_scale, uint8_t* Wd_q,
+                                        uint8_t* Wd_scale, moe_stream_t stream) {
+  if (!W_gate || !W_up || !W_down || !WguT_q || !WguT_scale || !Wd_q || !Wd_scale || E_loc < 1 || E_loc > 1024 ||
+      d <= 0 || f <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((src_dtype != MOE_BF16 && src_dtype != MOE_F32) || d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(WguT_q) || !aligned16(Wd_q)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_backward_mx(W_gate, W_up, W_down, src_dtype, E_loc, d, f, WguT_q, WguT_scale, Wd_q,
+                                             Wd_scale, stream));
+}
+
+size_t moe_layer_backward_mx_workspace_size(int T, int d, int f, int k, int E_loc) {
+  if (T < 0 || d <= 0 || f <= 0 || k < 1 || E_loc < 1) return 0;
+  return backward_layout(nullptr, T, d, f, k, E_loc, true).total;
+}
+
+moe_status moe_layer_backward_mx(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
+                                 int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
+                                 const uint8_t* Wgu_scale, const uint8_t* Wd_q, const uint8_t* Wd_scale,
+                                 const uint8_t* WguT_q, const uint8_t* WguT_scale, void* dx, float* dlogits,
+                                 float* dW_gate, float* dW_up, float* dW_down, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32 || e0 < 0 || E_loc < 1 || e0 + E_loc > E)
+    return MOE_ERR_INVALID_ARG;
+  if (n_cap_of(T, k, E_loc) > kMaxRows) return MOE_ERR_INVALID_ARG;  // int32 rows and offsets
+  moe_status s = check_mlp_shape(d, f, E_loc, MOE_MXFP8);
+  if (s != MOE_OK) return s;
+  if (!Wgu_packed || !Wgu_scale || !Wd_q || !Wd_scale || !WguT_q || !WguT_scale || !dW_gate || !dW_up || !dW_down)
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !dy || !topk_ids || !topk_probs || !dx || !dlogits)) return MOE_ERR_INVALID_ARG;
+  if ((T > 0 && (!aligned16(x) || !aligned16(dy) || !aligned16(dx))) || !aligned16(Wgu_packed) || !aligned16(Wd_q) ||
+      !aligned16(WguT_q) || !aligned16(Wgu_scale) || !aligned16(Wd_scale) || !aligned16(WguT_scale) ||
+      !aligned16(dW_gate) || !aligned16(dW_up) || !aligned16(dW_down))
+    return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) ||
+      workspace_bytes < moe_layer_backward_mx_workspace_size(T, d, f, k, E_loc))
+    return MOE_ERR_WORKSPACE;
+  BackwardWs w = backward_layout(static_cast<uint8_t*>(workspace), T, d, f, k, E_loc, true);
+  const int64_t n_cap = n_cap_of(T, k, E_loc);
+  cudaError_t e = cudaSuccess;
+  if (T > 0)
+    e = launch_permute(x, MOE_BF16, MOE_BF16, T, d, topk_ids, topk_probs, k, e0, E_loc, nullptr, nullptr, w.counts,
+                       w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
+  else
+    e = cudaMemsetAsync(w.offsets, 0, static_cast<size_t>(E_loc + 1) * 4, stream);
+  const int32_t* mtb = permute_mtile_base(w.perm_ws, T, E_loc);
+  if (e == cudaSuccess && n_cap > 0) {
+    // x and dy rows in routed order: MXFP8 along d (the row-wise GEMMs' A operands) and bf16
+    // (the weight gradients' operands, quantised column-wise below)
+    e = launch_gather_rows_mx(x, d, w.offsets, E_loc, mtb, w.row_src_token, w.x_q, w.x_sf, stream);
+    if (e == cudaSuccess)
+      e = launch_gather_rows_mx(dy, d, w.offsets, E_loc, mtb, w.row_src_token, w.dy_q, w.dy_sf, stream);
+    if (e == cudaSuccess)
+      e = launch_gather_rows(dy, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.dy_rows, stream);
+    if (e == cudaSuccess)
+      e = launch_gather_rows(x, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.x_rows, stream);
+    // g, u of the MXFP8 forward (x and the gate/up weights along d), kept in bf16
+    if (e == cudaSuccess)
+      e = launch_tc_gemm_store_mx(w.x_q, w.x_sf, n_cap, w.offsets, E_loc, d, 2 * f, Wgu_packed, Wgu_scale, w.gu,
+                                  w.err, kTimeoutNs, stream);
+    // dh = dy W_down^T (both along d) with the ScaledSwiGLU backward: dg/du, h, partial dp
+    if (e == cudaSuccess)
+      e = launch_tc_dswiglu_mx(w.dy_q, w.dy_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, Wd_q, Wd_scale, w.gu, w.dgu,
+                               w.h, w.dp_part, w.err, kTimeoutNs, stream);
+    // dx rows = [dg du] [W_gate W_up]^T, both along f
+    if (e == cudaSuccess)
+      e = launch_gather_rows_mx(w.dgu, 2 * f, w.offsets, E_loc, mtb, nullptr, w.dgu_q, w.dgu_sf, stream);
+    if (e == cudaSuccess)
+      e = launch_tc_gemm_store_mx(w.dgu_q, w.dgu_sf, n_cap, w.offsets, E_loc, 2 * f, d, WguT_q, WguT_scale, w.dxp,
+                                  w.err, kTimeoutNs, stream);
+  }
+  if (e == cudaSuccess) e = launch_combine(w.dxp, w.pair_to_row, T, k, d, MOE_BF16, dx, stream);
+  if (e == cudaSuccess)
+    e = launch_dlogits(topk_ids, topk_probs, w.pair_to_row, w.dp_part, f / 32, T, E, k, dlogits, stream);
+  // weight gradients: operands quantised column-wise (32-row blocks of each expert's
+  // segment), the dequantised values in place, then the tensor-core weight-gradient GEMMs
+  if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.x_rows, d, w.offsets, E_loc, stream);
+  if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.dy_rows, d, w.offsets, E_loc, stream);
+  if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.h, f, w.offsets, E_loc, stream);
+  if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.dgu, 2 * f, w.offsets, E_loc, stream);
   if (e == cudaSuccess)
     e = launch_wgrad_down_tc(w.h, w.dy_rows, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_down, w.err,
                              kTimeoutNs, stream);

@@ -57,6 +57,125 @@ cudaError_t launch_pack_gu_t(const void* Wg, const void* Wu, moe_dtype src, int 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------- MXFP8 backward
+// "MXFP8 Precision Reduces Memory Footprint" (8-bit values, one E8M0 scale per 32
+// consecutive values, Blackwell MXFP8 GEMMs): every backward GEMM reads its two operands
+// quantised in 32-blocks along that GEMM's own contraction axis.
+
+// Weight operands of the two row-wise backward GEMMs, quantised along their K:
+//   mode 0: Wd_q [E_loc, f, d] = W_down quantised along d  (B of dh = dy W_down^T, rows f)
+//   mode 1: WguT_q [E_loc, d, 2f] = [W_gate W_up] in the packed column order, quantised
+//           along f (B of dx = [dg du] [W_gate W_up]^T, rows d); a 32-block of the packed
+//           order is 32 consecutive gate (or up) columns of one row
+// One thread per (row, 32-block): 64 contiguous source bytes in, 32 codes and one scale
+// byte (weight SF tile layout) out.
+template <typename TIn>
+__global__ void __launch_bounds__(256) pack_rows_mx_kernel(const TIn* __restrict__ src0, const TIn* __restrict__ src1,
+                                                           int mode, int E_loc, int rows, int K, int f,
+                                                           uint8_t* __restrict__ dst, uint8_t* __restrict__ dst_sf) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int nkb = K / 32;
+  if (i >= static_cast<int64_t>(E_loc) * rows * nkb) return;
+  const int kb = static_cast<int>(i % nkb);
+  const int64_t er = i / nkb;  // e * rows + row
+  const TIn* s;
+  if (mode == 0) s = src0 + er * K + kb * 32;
+  else s = ((kb & 1) ? src1 : src0) + er * f + (kb >> 1) * 32;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if constexpr (sizeof(TIn) == 4) v[j] = __ldg(reinterpret_cast<const float*>(s) + j);
+    else v[j] = __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(s) + j)) << 16);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const int X = mx_exponent(amax);
+  const float inv = mx_inv_scale(X);
+  uint32_t w[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    w[q] = static_cast<uint32_t>(e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv)) |
+           (static_cast<uint32_t>(e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv)) << 16);
+  uint4* d = reinterpret_cast<uint4*>(dst + er * K + kb * 32);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  const int e = static_cast<int>(er / rows), row = static_cast<int>(er % rows);
+  dst_sf[sf_w_offset(e, rows, row, kb * 32, K)] = static_cast<uint8_t>(X + 127);
+}
+
+cudaError_t launch_pack_backward_mx(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, int E_loc, int d,
+                                    int f, uint8_t* WguT_q, uint8_t* WguT_sf, uint8_t* Wd_q, uint8_t* Wd_sf,
+                                    cudaStream_t st) {
+  const int64_t n_d = static_cast<int64_t>(E_loc) * f * (d / 32);
+  const int64_t n_gu = static_cast<int64_t>(E_loc) * d * (2 * f / 32);
+  const dim3 block(256);
+  if (src == MOE_F32) {
+    pack_rows_mx_kernel<float><<<dim3(static_cast<unsigned>(ceil_div(n_d, 256))), block, 0, st>>>(
+        static_cast<const float*>(Wdn), nullptr, 0, E_loc, f, d, f, Wd_q, Wd_sf);
+    pack_rows_mx_kernel<float><<<dim3(static_cast<unsigned>(ceil_div(n_gu, 256))), block, 0, st>>>(
+        static_cast<const float*>(Wg), static_cast<const float*>(Wu), 1, E_loc, d, 2 * f, f, WguT_q, WguT_sf);
+  } else {
+    pack_rows_mx_kernel<uint16_t><<<dim3(static_cast<unsigned>(ceil_div(n_d, 256))), block, 0, st>>>(
+        static_cast<const uint16_t*>(Wdn), nullptr, 0, E_loc, f, d, f, Wd_q, Wd_sf);
+    pack_rows_mx_kernel<uint16_t><<<dim3(static_cast<unsigned>(ceil_div(n_gu, 256))), block, 0, st>>>(
+        static_cast<const uint16_t*>(Wg), static_cast<const uint16_t*>(Wu), 1, E_loc, d, 2 * f, f, WguT_q, WguT_sf);
+  }
+  return cudaGetLastError();
+}
+
+// Column-wise MXFP8 quantisation for the weight-gradient GEMMs, which contract over an
+// expert's routed rows: each column of buf [rows, C] (bf16, routed order) is quantised in
+// blocks of 32 rows counted from the start of its expert's segment (a segment's last
+// block is padded with zeros, which never raise a block's amax), and replaced in place by
+// the dequantised values code * 2^X.  Those are exactly bf16 values (4 significant bits,
+// a power-of-two scale), so the bf16 tensor-core weight-gradient kernel reading them
+// forms exactly the products a block-scaled MMA of the E4M3 codes would.  Thread = (32-row
+// block, column pair); a CTA row of the grid per expert.
+__global__ void __launch_bounds__(128) colquant_mx_kernel(uint32_t* __restrict__ buf, int C,
+                                                          const int32_t* __restrict__ offsets) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int e = blockIdx.y;
+  const int r0 = __ldg(offsets + e), cnt = __ldg(offsets + e + 1) - r0;
+  const int cpairs = C / 2;
+  const int nrb = (cnt + 31) / 32;
+  const int ncc = (cpairs + blockDim.x - 1) / blockDim.x;
+  for (int item = blockIdx.x; item < nrb * ncc; item += gridDim.x) {
+    const int rb = item / ncc, cc = item - rb * ncc;
+    const int cp = cc * blockDim.x + threadIdx.x;
+    if (cp >= cpairs) continue;
+    const int rows = min(32, cnt - rb * 32);
+    uint32_t* base = buf + static_cast<int64_t>(r0 + rb * 32) * cpairs + cp;
+    float lo[32], hi[32];
+    float alo = 0.0f, ahi = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t w = i < rows ? base[static_cast<int64_t>(i) * cpairs] : 0u;
+      lo[i] = bf16_lo(w);
+      hi[i] = bf16_hi(w);
+      alo = fmaxf(alo, fabsf(lo[i]));
+      ahi = fmaxf(ahi, fabsf(hi[i]));
+    }
+    const int Xl = mx_exponent(alo), Xh = mx_exponent(ahi);
+    const float il = mx_inv_scale(Xl), ih = mx_inv_scale(Xh);
+    const float sl = ldexpf(1.0f, Xl), sh = ldexpf(1.0f, Xh);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < rows) {
+        const __nv_fp8x2_storage_t q = e4m3x2(lo[i] * il, hi[i] * ih);
+        const float2 dq = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(q, __NV_E4M3)));
+        base[static_cast<int64_t>(i) * cpairs] = pack_bf16x2(dq.x * sl, dq.y * sh);
+      }
+    }
+  }
+}
+
+cudaError_t launch_colquant_mx(void* buf, int C, const int32_t* offsets, int E_loc, cudaStream_t st) {
+  return launch_pdl(colquant_mx_kernel, dim3(32, static_cast<unsigned>(E_loc)), dim3(128), 0, st,
+                    static_cast<uint32_t*>(buf), C, offsets);
+}
+
 // ---------------------------------------------------------------------- router gradient
 // One warp per token.  Lane j < k: dp_j = sum over the f / 32 partial sums of its row (in
 // order) when slot j is local, else 0; then dlogit_{id_j} = p_j (dp_j - sum_i p_i dp_i), the

@@ -641,6 +641,44 @@ cudaError_t launch_tc_dswiglu(const void* dy_rows, const int32_t* offsets, const
   return launch_gemm_inst<false, EPI_DSWIGLU>(dy_rows, N_cap, W_down, g, st);
 }
 
+// Backward, MXFP8: dh = dy_row W_down^T on the block-scaled tensor cores (dy rows E4M3 [N_cap,
+// d] with scales in the activation SF tile layout, K = d; W_down E4M3 [E_loc, f, d] with its
+// weight SF tile layout), the ScaledSwiGLU backward fused into the epilogue as in bf16.
+cudaError_t launch_tc_dswiglu_mx(const void* dy_q, const uint8_t* dy_sf, const int32_t* offsets,
+                                 const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* Wd_q,
+                                 const uint8_t* Wd_sf, const void* gu, void* dgu, void* h, float* dp_part, int32_t* err,
+                                 uint64_t timeout_ns, cudaStream_t st) {
+  GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
+  g.n_out = f;
+  g.K = d;
+  g.out = dgu;
+  g.ld_out = 2 * f;
+  g.out_rows = N_cap;
+  g.out2 = h;
+  g.dp_part = dp_part;
+  g.aux = static_cast<const uint16_t*>(gu);
+  g.row_prob = row_prob;
+  g.a_sf = dy_sf;
+  g.b_sf = Wd_sf;
+  return launch_gemm_inst<true, EPI_DSWIGLU>(dy_q, N_cap, Wd_q, g, st);
+}
+
+// MXFP8 grouped GEMM with a bf16 store: out [a_rows, n_out] = A [rows, K] (E4M3, activation SF
+// tile layout) times B^T per expert (E4M3 [E_loc, n_out, K], weight SF tile layout).
+cudaError_t launch_tc_gemm_store_mx(const void* A, const uint8_t* a_sf, int64_t a_rows, const int32_t* offsets,
+                                    int E_loc, int K, int n_out, const void* B, const uint8_t* b_sf, void* out,
+                                    int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
+  GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
+  g.n_out = n_out;
+  g.K = K;
+  g.out = out;
+  g.ld_out = n_out;
+  g.out_rows = a_rows;
+  g.a_sf = a_sf;
+  g.b_sf = b_sf;
+  return launch_gemm_inst<true, EPI_STORE_BF16>(A, a_rows, B, g, st);
+}
+
 // Backward, bf16: dx rows = dg/du [N_cap, 2f] (packed order) times the transposed gate/up
 // weights WguT [E_loc, d, 2f] (same packed order along K) -> [N_cap, d].
 cudaError_t launch_tc_gemm_store(const void* A, int64_t a_rows, const int32_t* offsets, int E_loc, int K, int n_out,

@@ -278,7 +278,8 @@ __device__ __forceinline__ void quantize_row_mx(const uint4* __restrict__ src, i
 
 // Row copy with MXFP8 quantisation into the permuted order (scales in the activation SF
 // tile layout of the expert m-tiles).  Work items are (row, slice of MxRow::SLICE vectors),
-// so short permutations still spread over every SM.
+// so short permutations still spread over every SM.  row_src_token == nullptr: the source
+// rows are already in routed order (row r from source row r).
 template <int IN_BF16>
 __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __restrict__ x, int d,
                                                              const int32_t* __restrict__ offsets, int E_loc,
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __rest
     const int il = static_cast<int>(r - s_tab[lo]);
     const int64_t tile = s_tab[E_loc + 1 + lo] + il / 128;
     const int i = il % 128;
-    const int64_t t = __ldg(row_src_token + r);
+    const int64_t t = row_src_token ? __ldg(row_src_token + r) : r;
     quantize_row_mx<IN_BF16>(x + t * row_vecs, sl * SL, min(row_vecs, (sl + 1) * SL), lane, perm_x + r * d,
                              [&](int col, uint8_t b) { perm_sf[sf_act_offset(tile, i, col, d)] = b; });
   }
@@ -372,7 +373,23 @@ static PermuteWs carve_permute_ws(uint8_t* base, int T, int E_loc) {
   return w;
 }
 
+// m-tile bases [E_loc + 1] (128-row m-tiles of the expert segments, expert order) that the
+// permute's scan leaves in its scratch.
+int32_t* permute_mtile_base(uint8_t* ws, int T, int E_loc) { return carve_permute_ws(ws, T, E_loc).mtile_base; }
+
 int gather_grid(cudaStream_t st);
+// bf16 rows [*, K] into routed order with MXFP8 quantisation (32-blocks along K): dst row r
+// = src row row_src_token[r] (or src row r when row_src_token is null) for r <
+// offsets[E_loc], E4M3 codes [N_cap, K] and scales in the activation SF tile layout
+// (mtile_base from the permute).  K % 128 == 0.
+cudaError_t launch_gather_rows_mx(const void* src, int K, const int32_t* offsets, int E_loc,
+                                  const int32_t* mtile_base, const int32_t* row_src_token, uint8_t* dst,
+                                  uint8_t* dst_sf, cudaStream_t st) {
+  const size_t sm = static_cast<size_t>(2 * (E_loc + 1)) * 4;
+  return launch_pdl(perm_gather_mx_kernel<1>, dim3(gather_grid(st)), dim3(256), sm, st, static_cast<const uint4*>(src),
+                    K, offsets, E_loc, mtile_base, row_src_token, dst, dst_sf);
+}
+
 // Rows of src (row_bytes each, a multiple of 16) into routed order: dst row r = src row
 // row_src_token[r] for r < offsets[E_loc] (the permute's gather on its own).
 cudaError_t launch_gather_rows(const void* src, int64_t row_bytes, const int32_t* offsets, int E_loc,
