@@ -69,6 +69,17 @@ typedef int32_t moe_dtype;
 #define MOE_BF16 1  /* bf16 inputs/weights/outputs; tcgen05 bf16 MMA, fp32 accumulate   */
 #define MOE_MXFP8 2 /* E4M3 values + E8M0 scale per 32 along K; tcgen05 block-scaled MMA */
 
+/* Grouped-GEMM kernel shapes.  Passed as rows_hint (negative values), they force that
+ * kernel; moe_layer_gemm_kernel reports the one moe_layer_forward picks.
+ *   MOE_KERNEL_CTA   token-major 128-row tiles on one CTA
+ *   MOE_KERNEL_PAIR  token-major 256-row tiles on a CTA pair (cta_group::2); fp32: CTA
+ *   MOE_KERNEL_SWAP  swapped operands on a CTA pair: 256 packed weight rows on the MMA's M
+ *                    side, up to 384 of an expert's tokens (padded to 16) on N; fp32 and
+ *                    GEMM1 calls that keep g/u: CTA */
+#define MOE_KERNEL_CTA (-1)
+#define MOE_KERNEL_PAIR (-2)
+#define MOE_KERNEL_SWAP (-3)
+
 /* MXFP8 quantisation rule (both for x, the weights and the intermediate h): blocks of 32
  * consecutive values along the contraction dimension K; amax = max |v| over the block;
  * shared exponent X = floor(log2(amax)) - 8, clamped to [-127, 127] (X = 0 for an
@@ -194,11 +205,14 @@ size_t moe_mx_weight_scale_bytes(int E_loc, int rows, int K);
  *   Y2      device [N_cap, d]: fp32 for MOE_F32, bf16 otherwise
  *   workspace device >= moe_grouped_mlp_workspace_size(...) bytes, 256-byte aligned
  *   rows_hint  expected rows per local expert (e.g. moe_rows_hint(T, k, E)); it only picks
- *              the kernel shape (bf16 GEMM1 runs on CTA pairs with 256-row tiles from 2048
- *              expected rows up, and from 256 to 1023 when d >= 4096; bf16 GEMM2 from 128;
- *              MXFP8 GEMMs from 65536, as the block-scaled pair kernel measured slower than
- *              the 1-CTA one on every shape tried), never the result's meaning; <= 0 uses
- *              N_cap / E_loc.
+ *              the kernel shape, never the result's meaning: bf16 GEMM1 runs on the
+ *              swapped-operand kernel (MOE_KERNEL_SWAP, 1.2 x the expected rows per tile)
+ *              from 256 to 320 expected rows when d >= 4096 and E_loc <= 256, on
+ *              token-major CTA pairs from 2048 expected rows up and from 321 to 1023 when
+ *              d >= 4096; bf16 GEMM2 on token-major pairs from 128; MXFP8 GEMMs on pairs
+ *              only from 65536 (the block-scaled pair kernel measured slower than the 1-CTA
+ *              one on every shape tried); everything else on the 1-CTA kernel.  0 uses
+ *              N_cap / E_loc; MOE_KERNEL_* forces a kernel.
  * Requires d % 8 == 0 and f % 32 == 0 (bf16); d % 128 == 0 and f % 128 == 0 (MXFP8). */
 moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                            const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
@@ -209,10 +223,13 @@ moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, cons
  * moe_layer_forward uses). */
 int moe_rows_hint(int T, int k, int E);
 /* The GEMM1 kernel moe_layer_forward picks for this problem (host only, no launch): 1 if
- * GEMM1 runs on CTA pairs (256-row tiles, A from a permuted copy of x), 0 if on the 1-CTA
- * kernel (bf16: A read from the token rows inside the kernel; fp32 / MXFP8: from a
- * permuted copy).  Returns -1 for invalid sizes. */
+ * GEMM1 runs on token-major CTA pairs (256-row tiles), else 0 (the 1-CTA or the
+ * swapped-operand kernel; moe_layer_gemm_kernel tells which).  Returns -1 for invalid
+ * sizes. */
 int moe_layer_gemm1_pairs(int T, int d, int k, int E, int E_loc, moe_dtype dtype);
+/* The kernel moe_layer_forward runs for GEMM `gemm` (1 or 2) of this problem, as a
+ * MOE_KERNEL_* value (host only, no launch); 0 for invalid arguments. */
+int moe_layer_gemm_kernel(int T, int d, int f, int k, int E, int E_loc, moe_dtype dtype, int gemm);
 
 /* Whether moe_layer_forward folds the combine into GEMM2 (moe_expert_gemm2_combine's
  * path) for this routing shape: 1 when tokens average under one local slot (k * E_loc <

@@ -60,6 +60,7 @@ _SIGS = {
     "moe_rows_hint": (_I, [_I, _I, _I]),
     "moe_layer_gemm1_pairs": (_I, [_I, _I, _I, _I, _I, _I]),
     "moe_layer_fused_combine": (_I, [_I, _I, _I, _I]),
+    "moe_layer_gemm_kernel": (_I, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "moe_grouped_mlp_workspace_size": (_SZ, [_I64, _I, _I, _I, _I]),
     "moe_expert_gemm1_swiglu": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm1_swiglu_gather": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _I, _P, _SZ,
@@ -244,6 +245,19 @@ def moe_layer_gemm1_pairs(T: int, d: int, k: int, E: int, E_loc: int, dtype: str
     return bool(r)
 
 
+# rows_hint values that force a grouped-GEMM kernel (moe.h MOE_KERNEL_*)
+KERNEL_CTA, KERNEL_PAIR, KERNEL_SWAP = -1, -2, -3
+_KERNEL_NAMES = {KERNEL_CTA: "cta", KERNEL_PAIR: "pair", KERNEL_SWAP: "swap"}
+
+
+def moe_layer_gemm_kernel(T: int, d: int, f: int, k: int, E: int, E_loc: int, dtype: str, gemm: int) -> str:
+    """The kernel moe_layer_forward runs for GEMM 1 or 2: "cta", "pair" or "swap"."""
+    r = int(_lib.moe_layer_gemm_kernel(T, d, f, k, E, E_loc, _dt(dtype), gemm))
+    if r not in _KERNEL_NAMES:
+        raise ValueError("invalid sizes")
+    return _KERNEL_NAMES[r]
+
+
 def moe_layer_fused_combine(k: int, E: int, E_loc: int, dtype: str) -> bool:
     """True if moe_layer_forward folds the combine into GEMM2 for this routing shape."""
     r = int(_lib.moe_layer_fused_combine(k, E, E_loc, _dt(dtype)))
@@ -287,10 +301,10 @@ def moe_expert_gemm1_swiglu(perm_x, perm_x_scale, offsets, row_prob, pw: PackedW
 
 
 def moe_expert_gemm1_swiglu_gather(x, x_scale, row_src_token, offsets, row_prob, pw: PackedWeights, h=None,
-                                   h_scale=None, ws=None, rows_hint=1):
+                                   h_scale=None, ws=None, rows_hint=KERNEL_CTA):
     """GEMM1 + scaled SwiGLU reading the token rows x (bf16, or E4M3 + row scales from
     moe_quantize_mx_rows) through row_src_token.  rows_hint picks the kernel shape as for
-    moe_expert_gemm1_swiglu (the default 1 keeps the 1-CTA kernel)."""
+    moe_expert_gemm1_swiglu (the default keeps the 1-CTA kernel)."""
     cap = row_src_token.shape[0]
     if h is None:
         h, h_scale = alloc_h(cap, pw, x.device)

@@ -16,7 +16,7 @@ cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtyp
 size_t permute_ws_bytes(int T, int E_loc);
 cudaError_t launch_combine_prep(const int32_t* pair_to_row, int T, int k, int32_t* tok_nloc, cudaStream_t st);
 cudaError_t launch_tc_gemm2_combine(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap,
-                                    int E_loc, int d, int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf,
+                                    int E_loc, int d, int f, bool mx, int shape, const void* Wd, const uint8_t* Wd_sf,
                                     void* Y2, const int32_t* row_src_token, const int32_t* tok_nloc, int T, void* y,
                                     int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_combine(const void* Y2, const int32_t* p2r, int T, int k, int d, moe_dtype dtype, void* y,
@@ -28,15 +28,15 @@ cudaError_t launch_simt_gemm1(const float* perm_x, const int32_t* offsets, const
 cudaError_t launch_simt_gemm2(const float* h, const int32_t* offsets, int64_t N_cap, int E_loc, int d, int f,
                               const float* Wd, float* Y2, cudaStream_t st);
 cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
-                            int64_t N_cap, int E_loc, int d, int f, bool mx, bool pair, const void* Wgu,
+                            int64_t N_cap, int E_loc, int d, int f, bool mx, int shape, const void* Wgu,
                             const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns,
                             void* gu_save, cudaStream_t st);
 cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
-                            int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
+                            int f, bool mx, int shape, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
                             uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
                                    const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc, int d,
-                                   int f, bool mx, bool pair, const void* Wgu, const uint8_t* Wgu_sf, void* h,
+                                   int f, bool mx, int shape, const void* Wgu, const uint8_t* Wgu_sf, void* h,
                                    uint8_t* h_sf, int32_t* err, uint64_t timeout_ns, void* gu_save, cudaStream_t st);
 cudaError_t launch_quant_rows_mx(const void* x, moe_dtype x_dtype, int T, int d, const int32_t* pair_to_row, int k,
                                  uint8_t* xq, uint8_t* x_sf, cudaStream_t st);
@@ -77,6 +77,7 @@ cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dty
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
+constexpr int kShapeSwapMin = 64;  // GEMM kernel shapes >= this: swapped operands (gemm_tc.cu)
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;  // routed rows are int32 indices
 constexpr int kMaxDevices = 64;
 constexpr int kMaxExpertId = 65535;  // e0 + E_loc <= 65536 (moe_permute's contract)
@@ -150,8 +151,12 @@ constexpr int kPairRowsThreshold = 2048;
 // expert (no workload here comes near it).
 constexpr int kPairRowsThresholdMx = 1 << 16;
 
+static int64_t expected_rows(int64_t n_cap, int E_loc, int rows_hint) {
+  return rows_hint > 0 ? rows_hint : n_cap / (E_loc > 0 ? E_loc : 1);
+}
+
 static bool use_pair(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint, int K) {
-  const int64_t rows = rows_hint > 0 ? rows_hint : n_cap / (E_loc > 0 ? E_loc : 1);
+  const int64_t rows = expected_rows(n_cap, E_loc, rows_hint);
   if (dt == MOE_MXFP8) return rows >= kPairRowsThresholdMx;
   return dt == MOE_BF16 && (rows >= kPairRowsThreshold || (rows >= 256 && rows < 1024 && K >= 4096));
 }
@@ -164,9 +169,50 @@ static bool use_pair(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint, int 
 constexpr int kPairRowsThresholdGemm2 = 128;
 
 static bool use_pair_gemm2(moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint) {
-  const int64_t rows = rows_hint > 0 ? rows_hint : n_cap / (E_loc > 0 ? E_loc : 1);
+  const int64_t rows = expected_rows(n_cap, E_loc, rows_hint);
   if (dt == MOE_MXFP8) return rows >= kPairRowsThresholdMx;
   return dt == MOE_BF16 && rows >= kPairRowsThresholdGemm2;
+}
+
+// The swapped-operand kernel (gemm_tc_swap.cu: weight rows on the MMA's M side, an
+// expert's tokens on N, padded to 16).  Measured on B300 against the token-major kernels
+// (graph-replayed layer steps, 2032 MHz):
+//   * it wins for bf16 GEMM1 where one tile of up to 384 tokens covers an expert that the
+//     token-major tiles split into two 256-row or three 128-row m-tiles, each re-streaming
+//     the expert's weights: the EP64 slice at T = 8192 (269 rows per expert, d = 7168):
+//     GEMM1 96.6 -> 82-86 us;
+//   * it loses elsewhere: with a few dozen tokens per expert every tile still streams its
+//     256 weight rows and issues its K / 16 MMAs, now for 128 weight rows per SM instead of
+//     256 (EP64 slice at T = 2048: GEMM1 54 -> 62-75 us; Zipf EP8 slice: 95 -> 198), and an
+//     expert's short last chunk costs a full weight pass (T = 32768: GEMM1 189 -> 265); its
+//     GEMM2 (K = f) and its MXFP8 tiles lost at every shape tried (EP64 slice: GEMM2 67 ->
+//     89 us bf16, 57 -> 72 MXFP8; MXFP8 GEMM1 69 -> 74-86).
+// Tokens per tile: 1.2 x the expected rows, rounded up to 32 (MXFP8: to 128, the scale
+// layout's row tiles), within [64, 384] (MXFP8 [128, 384]); experts above it take more
+// tiles.  MOE_KERNEL_SWAP forces it for either GEMM and dtype.
+constexpr int kSwapRowsMin = 256;
+constexpr int kSwapRowsMax = 320;
+constexpr int kSwapElocMax = 256;
+
+static int swap_tokens(moe_dtype dt, int64_t rows) {
+  const int gran = dt == MOE_MXFP8 ? 128 : 32;
+  const int64_t nt = ((rows * 6 + 4) / 5 + gran - 1) / gran * gran;
+  return static_cast<int>(std::min<int64_t>(384, std::max<int64_t>(nt, dt == MOE_MXFP8 ? 128 : 64)));
+}
+
+// Kernel shape of a grouped GEMM (0 = 1-CTA, 1 = token-major CTA pairs, >= 64 = swapped
+// operands with that many tokens per tile).  rows_hint > 0: expected rows per expert; 0:
+// N_cap / E_loc; MOE_KERNEL_* (negative): that kernel.  keeps_gu: GEMM1 must also write
+// the gate/up pre-activations (the swapped kernel does not).
+static int gemm_shape(bool gemm1, moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint, int K, bool keeps_gu) {
+  const int64_t rows = expected_rows(n_cap, E_loc, rows_hint > 0 ? rows_hint : 0);
+  const bool swap_ok = dt != MOE_F32 && E_loc <= kSwapElocMax && !(gemm1 && keeps_gu);
+  if (rows_hint == MOE_KERNEL_CTA) return 0;
+  if (rows_hint == MOE_KERNEL_PAIR) return dt == MOE_F32 ? 0 : 1;
+  if (rows_hint == MOE_KERNEL_SWAP) return swap_ok ? swap_tokens(dt, std::max<int64_t>(rows, 1)) : 0;
+  if (swap_ok && gemm1 && dt == MOE_BF16 && K >= 4096 && rows >= kSwapRowsMin && rows <= kSwapRowsMax)
+    return swap_tokens(dt, rows);
+  return (gemm1 ? use_pair(dt, n_cap, E_loc, rows_hint, K) : use_pair_gemm2(dt, n_cap, E_loc, rows_hint)) ? 1 : 0;
 }
 
 static cudaError_t run_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets,
@@ -178,8 +224,8 @@ static cudaError_t run_gemm1(const void* perm_x, const uint8_t* perm_sf, const i
     return launch_simt_gemm1(static_cast<const float*>(perm_x), offsets, row_prob, n_cap, E_loc, d, f,
                              static_cast<const float*>(Wgu), static_cast<float*>(h), st);
   return launch_tc_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt == MOE_MXFP8,
-                         use_pair(dt, n_cap, E_loc, rows_hint, d), Wgu, Wgu_sf, h, h_sf, err, kTimeoutNs, gu_save,
-                         st);
+                         gemm_shape(true, dt, n_cap, E_loc, rows_hint, d, gu_save != nullptr), Wgu, Wgu_sf, h, h_sf,
+                         err, kTimeoutNs, gu_save, st);
 }
 
 static cudaError_t run_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t n_cap, int E_loc,
@@ -190,7 +236,7 @@ static cudaError_t run_gemm2(const void* h, const uint8_t* h_sf, const int32_t* 
     return launch_simt_gemm2(static_cast<const float*>(h), offsets, n_cap, E_loc, d, f, static_cast<const float*>(Wd),
                              static_cast<float*>(Y2), st);
   return launch_tc_gemm2(h, h_sf, offsets, n_cap, E_loc, d, f, dt == MOE_MXFP8,
-                         use_pair_gemm2(dt, n_cap, E_loc, rows_hint), Wd, Wd_sf, Y2, err, kTimeoutNs, st);
+                         gemm_shape(false, dt, n_cap, E_loc, rows_hint, f, false), Wd, Wd_sf, Y2, err, kTimeoutNs, st);
 }
 
 static cudaError_t run_mlp(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
@@ -482,7 +528,16 @@ int moe_layer_fused_combine(int k, int E, int E_loc, moe_dtype dtype) {
 
 int moe_layer_gemm1_pairs(int T, int d, int k, int E, int E_loc, moe_dtype dtype) {
   if (T < 0 || d <= 0 || k <= 0 || E <= 0 || E_loc <= 0 || E_loc > E) return -1;
-  return use_pair(dtype, n_cap_of(T, k, E_loc), E_loc, moe_rows_hint(T, k, E), d) ? 1 : 0;
+  return gemm_shape(true, dtype, n_cap_of(T, k, E_loc), E_loc, moe_rows_hint(T, k, E), d, false) == 1 ? 1 : 0;
+}
+
+int moe_layer_gemm_kernel(int T, int d, int f, int k, int E, int E_loc, moe_dtype dtype, int gemm) {
+  if (T < 0 || d <= 0 || f <= 0 || k <= 0 || E <= 0 || E_loc <= 0 || E_loc > E || (gemm != 1 && gemm != 2))
+    return 0;
+  if (dtype != MOE_F32 && dtype != MOE_BF16 && dtype != MOE_MXFP8) return 0;
+  const int s = gemm_shape(gemm == 1, dtype, n_cap_of(T, k, E_loc), E_loc, moe_rows_hint(T, k, E), gemm == 1 ? d : f,
+                           false);
+  return s >= kShapeSwapMin ? MOE_KERNEL_SWAP : s == 1 ? MOE_KERNEL_PAIR : MOE_KERNEL_CTA;
 }
 
 static moe_status check_gemm_common(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype, const void* offsets,
@@ -524,7 +579,8 @@ moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale,
   if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
   if (N_cap == 0) return MOE_OK;
   return cuda_status(launch_tc_gemm1_gather(x, x_scale, row_src_token, offsets, row_prob, N_cap, E_loc, d, f,
-                                            dtype == MOE_MXFP8, use_pair(dtype, N_cap, E_loc, rows_hint, d),
+                                            dtype == MOE_MXFP8,
+                                            dtype == MOE_MXFP8 ? 0 : gemm_shape(true, dtype, N_cap, E_loc, rows_hint, d, false),
                                             Wgu_packed, Wgu_scale, h, h_scale, static_cast<int32_t*>(workspace),
                                             kTimeoutNs, nullptr, stream));
 }
@@ -603,7 +659,7 @@ moe_status moe_expert_gemm2_combine(const void* h, const uint8_t* h_scale, const
   cudaError_t e = launch_combine_prep(pair_to_row, T, k, w.tok_nloc, stream);
   if (e == cudaSuccess)
     e = launch_tc_gemm2_combine(h, h_scale, offsets, N_cap, E_loc, d, f, dtype == MOE_MXFP8,
-                                use_pair_gemm2(dtype, N_cap, E_loc, rows_hint), Wd_packed, Wd_scale, w.Y2,
+                                gemm_shape(false, dtype, N_cap, E_loc, rows_hint, f, false), Wd_packed, Wd_scale, w.Y2,
                                 row_src_token, w.tok_nloc, T, y, static_cast<int32_t*>(workspace), kTimeoutNs, stream);
   // expected local slots per token (rows_hint rows per expert), which picks the sparse or
   // dense pass for the tokens with several local slots (same result either way)
@@ -663,8 +719,8 @@ static moe_status layer_forward_impl(const void* x, const float* logits, int T, 
       e = launch_quant_rows_mx(x, x_dtype, T, d, w.pair_to_row, k, static_cast<uint8_t*>(w.perm_x), w.perm_sf, stream);
     if (e == cudaSuccess)
       e = launch_tc_gemm1_gather(mx ? w.perm_x : x, w.perm_sf, w.row_src_token, w.offsets, w.row_prob, n_cap, E_loc,
-                                 d, f, mx, !mx && use_pair(dtype, n_cap, E_loc, hint, d), Wgu_packed, Wgu_scale,
-                                 ms.h, ms.h_sf, w.err, kTimeoutNs, gu_save, stream);
+                                 d, f, mx, mx ? 0 : gemm_shape(true, dtype, n_cap, E_loc, hint, d, gu_save != nullptr),
+                                 Wgu_packed, Wgu_scale, ms.h, ms.h_sf, w.err, kTimeoutNs, gu_save, stream);
   } else if (e == cudaSuccess) {
     e = run_gemm1(w.perm_x, w.perm_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale, ms.h,
                   ms.h_sf, w.err, hint, stream, gu_save);
@@ -672,7 +728,7 @@ static moe_status layer_forward_impl(const void* x, const float* logits, int T, 
   if (fused_combine) {
     if (e == cudaSuccess)
       e = launch_tc_gemm2_combine(ms.h, ms.h_sf, w.offsets, n_cap, E_loc, d, f, dtype == MOE_MXFP8,
-                                  use_pair_gemm2(dtype, n_cap, E_loc, hint), Wd_packed, Wd_scale, w.Y2,
+                                  gemm_shape(false, dtype, n_cap, E_loc, hint, f, false), Wd_packed, Wd_scale, w.Y2,
                                   w.row_src_token, w.tok_nloc, T, y, w.err, kTimeoutNs, stream);
     if (e == cudaSuccess)  // expected local slots per token: k E_loc / E
       e = launch_combine_multi(w.Y2, w.pair_to_row, w.tok_nloc, T, k, d, y,

@@ -564,18 +564,29 @@ static GemmArgs base_args(const int32_t* offsets, int E_loc, int32_t* err, uint6
   return g;
 }
 
-// GEMM1 + fused scaled SwiGLU on the tensor cores.
-//   bf16:  perm_x bf16 [N_cap, d] -> h bf16 [N_cap, f]
-//   mxfp8: perm_x E4M3 [N_cap, d] + SF -> h E4M3 [N_cap, f] + SF
 cudaError_t launch_pair_gemm(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool swiglu, bool mx,
                              cudaStream_t st);
 cudaError_t launch_pair_gemm_combine(const void* A, int64_t a_rows, const void* B, const GemmArgs& g, bool mx,
                                      cudaStream_t st);
 cudaError_t launch_pair_gemm1_gather(const void* B, const GemmArgs& g, cudaStream_t st);
+cudaError_t launch_swap_gemm1(const void* perm_x, int64_t rows, const void* Wgu, const GemmArgs& g, bool mx, int nt_max,
+                              cudaStream_t st);
+cudaError_t launch_swap_gemm1_gather(const void* Wgu, const GemmArgs& g, int nt_max, cudaStream_t st);
+cudaError_t launch_swap_gemm2(const void* h, int64_t rows, const void* Wd, const GemmArgs& g, bool mx, bool combine,
+                              int nt_max, cudaStream_t st);
 
-// pair: run the CTA-pair kernel (large M per expert) instead of the 1-CTA one.
+// Kernel shape of the grouped GEMM launchers below: 0 = 1-CTA kernel (gemm_tc.cu), 1 =
+// token-major CTA pairs (gemm_tc_pair.cu), kShapeSwapMin and above = the swapped-operand
+// pair kernel (gemm_tc_swap.cu) with that many tokens per tile.
+constexpr int kShapeSwapMin = 64;
+
+// GEMM1 + fused scaled SwiGLU on the tensor cores.
+//   bf16:  perm_x bf16 [N_cap, d] -> h bf16 [N_cap, f]
+//   mxfp8: perm_x E4M3 [N_cap, d] + SF -> h E4M3 [N_cap, f] + SF
+// The swapped-operand kernel does not write g/u (gu_save): with gu_save the token-major
+// kernels run.
 cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets, const float* row_prob,
-                            int64_t N_cap, int E_loc, int d, int f, bool mx, bool pair, const void* Wgu,
+                            int64_t N_cap, int E_loc, int d, int f, bool mx, int shape, const void* Wgu,
                             const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err, uint64_t timeout_ns,
                             void* gu_save, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
@@ -589,7 +600,8 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
   g.row_prob = row_prob;
   g.a_sf = perm_sf;
   g.b_sf = Wgu_sf;
-  if (pair) return launch_pair_gemm(perm_x, N_cap, Wgu, g, true, mx, st);
+  if (shape >= kShapeSwapMin && !g.out2) return launch_swap_gemm1(perm_x, N_cap, Wgu, g, mx, shape, st);
+  if (shape == 1) return launch_pair_gemm(perm_x, N_cap, Wgu, g, true, mx, st);
   if (mx) return launch_gemm_inst<true, EPI_SWIGLU_MX>(perm_x, N_cap, Wgu, g, st);
   return launch_gemm_inst<false, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
 }
@@ -597,10 +609,11 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
 // GEMM1 + fused scaled SwiGLU with A gathered from the token rows: row r of the
 // expert-ordered operand is x row row_src_token[r] (bf16 [T, d]; MXFP8: E4M3 [T, d] with
 // E8M0 scales x_sf [T, d / 32]), so no permuted copy of x is ever written.
-// pair: bf16 only -- the CTA-pair kernel (256-row tiles) instead of the 1-CTA one.
+// shape (bf16 only): the token-major CTA-pair kernel (1) or the swapped-operand one (>=
+// kShapeSwapMin) instead of the 1-CTA kernel (0).
 cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int32_t* row_src_token,
                                    const int32_t* offsets, const float* row_prob, int64_t N_cap, int E_loc, int d,
-                                   int f, bool mx, bool pair, const void* Wgu, const uint8_t* Wgu_sf, void* h,
+                                   int f, bool mx, int shape, const void* Wgu, const uint8_t* Wgu_sf, void* h,
                                    uint8_t* h_sf, int32_t* err, uint64_t timeout_ns, void* gu_save, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
   g.out2 = mx ? nullptr : gu_save;
@@ -618,7 +631,8 @@ cudaError_t launch_tc_gemm1_gather(const void* x, const uint8_t* x_sf, const int
   g.gx_sf = x_sf;
   g.gx_sf_ld = d / 32;
   if (mx) return launch_gemm_inst<true, EPI_SWIGLU_MX, true>(nullptr, 0, Wgu, g, st);
-  if (pair) return launch_pair_gemm1_gather(Wgu, g, st);
+  if (shape >= kShapeSwapMin && !g.out2) return launch_swap_gemm1_gather(Wgu, g, shape, st);
+  if (shape == 1) return launch_pair_gemm1_gather(Wgu, g, st);
   return launch_gemm_inst<false, EPI_SWIGLU_BF16, true>(nullptr, 0, Wgu, g, st);
 }
 
@@ -696,7 +710,7 @@ cudaError_t launch_tc_gemm_store(const void* A, int64_t a_rows, const int32_t* o
 // SF) -> y rows of the tokens with at most one local slot (their row, or zeros), Y2
 // [N_cap, d] rows of the tokens with several (summed afterwards by the combine kernel).
 cudaError_t launch_tc_gemm2_combine(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap,
-                                    int E_loc, int d, int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf,
+                                    int E_loc, int d, int f, bool mx, int shape, const void* Wd, const uint8_t* Wd_sf,
                                     void* Y2, const int32_t* row_src_token, const int32_t* tok_nloc, int T, void* y,
                                     int32_t* err, uint64_t timeout_ns, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
@@ -711,14 +725,15 @@ cudaError_t launch_tc_gemm2_combine(const void* h, const uint8_t* h_sf, const in
   g.tok_nloc = tok_nloc;
   g.y = y;
   g.T = T;
-  if (pair) return launch_pair_gemm_combine(h, N_cap, Wd, g, mx, st);
+  if (shape >= kShapeSwapMin) return launch_swap_gemm2(h, N_cap, Wd, g, mx, true, shape, st);
+  if (shape == 1) return launch_pair_gemm_combine(h, N_cap, Wd, g, mx, st);
   if (mx) return launch_gemm_inst<true, EPI_COMBINE>(h, N_cap, Wd, g, st);
   return launch_gemm_inst<false, EPI_COMBINE>(h, N_cap, Wd, g, st);
 }
 
 // GEMM2 on the tensor cores: h [N_cap, f] (bf16, or E4M3 + SF) -> Y2 bf16 [N_cap, d].
 cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* offsets, int64_t N_cap, int E_loc, int d,
-                            int f, bool mx, bool pair, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
+                            int f, bool mx, int shape, const void* Wd, const uint8_t* Wd_sf, void* Y2, int32_t* err,
                             uint64_t timeout_ns, cudaStream_t st) {
   GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
   g.n_out = d;
@@ -728,7 +743,8 @@ cudaError_t launch_tc_gemm2(const void* h, const uint8_t* h_sf, const int32_t* o
   g.out_rows = N_cap;
   g.a_sf = h_sf;
   g.b_sf = Wd_sf;
-  if (pair) return launch_pair_gemm(h, N_cap, Wd, g, false, mx, st);
+  if (shape >= kShapeSwapMin) return launch_swap_gemm2(h, N_cap, Wd, g, mx, false, shape, st);
+  if (shape == 1) return launch_pair_gemm(h, N_cap, Wd, g, false, mx, st);
   if (mx) return launch_gemm_inst<true, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
   return launch_gemm_inst<false, EPI_STORE_BF16>(h, N_cap, Wd, g, st);
 }

@@ -5,6 +5,9 @@
 
 #include <cuda.h>
 
+#include <algorithm>
+#include <cstring>
+
 #include "moe_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -59,6 +62,11 @@ struct GemmArgs {
   void* y;
   const int32_t* tok_nloc;
   int T;
+  // Swapped-operand kernel (gemm_tc_swap.cu): tokens per tile, pipeline depth and bytes
+  // per stage (set by its launcher).
+  int nt_max;
+  int sw_stages;
+  int sw_stage_bytes;
 };
 
 // TMA store maps of the bf16 outputs: 32 x 32 boxes over out [out_rows, ld_out] and out2
@@ -495,6 +503,9 @@ bool make_operand_map(CUtensorMap* m, const void* base, bool fp8, uint64_t K, ui
 bool make_store_map(CUtensorMap* m, void* base, int elt, uint64_t cols, uint64_t rows, uint32_t box_cols,
                     uint32_t box_rows);
 int num_sms();
+// 2-D map over an SF tile layout buffer of n_atoms 512-byte atoms (rows of 128 uint32),
+// box = atoms_per_box consecutive atoms.
+bool make_sf_map(CUtensorMap* m, const void* base, uint64_t n_atoms, uint32_t atoms_per_box);
 // Store maps of g.out (bf16 [out_rows, ld_out]) and g.out2 (bf16 [out_rows, n_out]) where set.
 bool make_out_maps(OutMaps* m, const GemmArgs& g);
 

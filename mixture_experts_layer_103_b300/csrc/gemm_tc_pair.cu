@@ -352,8 +352,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads + pair_
   }
 }
 
-// 2-D map over an SF tile layout buffer of n_atoms 512-byte atoms, box = atoms_per_box atoms.
-static bool make_sf_map(CUtensorMap* m, const void* base, uint64_t n_atoms, uint32_t atoms_per_box) {
+bool make_sf_map(CUtensorMap* m, const void* base, uint64_t n_atoms, uint32_t atoms_per_box) {
   static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if (!enc) {
     void* p = nullptr;

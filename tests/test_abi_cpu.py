@@ -162,7 +162,7 @@ def test_gemm1_kernel_choice(lib):
     kernel otherwise (measured per shape on B300)."""
     pairs = lib.moe_layer_gemm1_pairs
     assert not pairs(4096, 2048, 8, 64, 64, "bf16")      # 512 rows, d = 2048
-    assert pairs(8192, 7168, 8, 256, 4, "bf16")          # 256 rows, d = 7168
+    assert not pairs(8192, 7168, 8, 256, 4, "bf16")      # 256 rows, d = 7168: swapped operands
     assert pairs(16384, 7168, 8, 256, 4, "bf16")         # 512 rows
     assert not pairs(32768, 7168, 8, 256, 4, "bf16")     # 1024 rows
     assert not pairs(2048, 7168, 8, 256, 4, "bf16")      # 64 rows
@@ -174,6 +174,30 @@ def test_gemm1_kernel_choice(lib):
     assert not pairs(8192, 7168, 8, 256, 4, "f32")
     with pytest.raises(ValueError):
         pairs(8192, 7168, 8, 256, 512, "bf16")            # E_loc > E
+
+
+def test_gemm_kernel_choice(lib):
+    """Which grouped-GEMM kernel moe_layer_forward runs (each rule measured on B300): bf16
+    GEMM1 on the swapped-operand pair kernel from 256 to 320 expected rows per expert when
+    d >= 4096 (E_loc <= 256), on token-major pairs from 321 to 1023 rows (d >= 4096) or from
+    2048; bf16 GEMM2 on pairs from 128 rows; MXFP8 on the 1-CTA kernel; fp32 on its own."""
+    kern = lib.moe_layer_gemm_kernel
+    assert kern(8192, 7168, 2048, 8, 256, 4, "bf16", 1) == "swap"     # 256 rows (EP64, T = 8192)
+    assert kern(10240, 7168, 2048, 8, 256, 4, "bf16", 1) == "swap"    # 320 rows
+    assert kern(10272, 7168, 2048, 8, 256, 4, "bf16", 1) == "pair"    # 321 rows
+    assert kern(8160, 7168, 2048, 8, 256, 4, "bf16", 1) == "cta"      # 255 rows
+    assert kern(8192, 2048, 2048, 8, 256, 4, "bf16", 1) == "cta"      # 256 rows, d < 4096
+    assert kern(8192, 7168, 2048, 8, 256, 4, "bf16", 2) == "pair"     # GEMM2: token-major pairs
+    assert kern(2048, 7168, 2048, 8, 256, 4, "bf16", 1) == "cta"      # 64 rows
+    assert kern(2048, 7168, 2048, 8, 256, 4, "bf16", 2) == "cta"
+    assert kern(8192, 7168, 2048, 8, 256, 4, "mxfp8", 1) == "cta"
+    assert kern(8192, 7168, 2048, 8, 256, 4, "mxfp8", 2) == "cta"
+    assert kern(4096, 2048, 1024, 8, 64, 64, "bf16", 1) == "cta"      # bf16_e64: 512 rows
+    assert kern(4096, 2048, 1024, 8, 64, 64, "bf16", 2) == "pair"
+    assert kern(19200, 7168, 2048, 8, 512, 512, "bf16", 1) == "pair"  # 300 rows, but E_loc > 256
+    assert kern(64, 128, 256, 2, 8, 8, "f32", 1) == "cta"
+    with pytest.raises(ValueError):
+        kern(8192, 7168, 2048, 8, 256, 4, "bf16", 3)
 
 
 def test_combine_fusion_choice(lib):

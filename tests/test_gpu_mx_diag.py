@@ -99,10 +99,15 @@ FULL = [("mxfp8_ep64_T8192", 96), ("mxfp8_ep8_zipf_T8192", 96)]
 MX_PAIR_HINT = 1 << 16  # expected rows per expert from which MXFP8 GEMMs run on CTA pairs
 
 
+K_CTA, K_SWAP = -1, -3  # rows_hint values that force a kernel (moe.h MOE_KERNEL_*)
+
+
 def _cases():
-    # hint 65536: both GEMMs on CTA pairs (block-scaled cta_group::2 MMAs); 1: the 1-CTA kernel
-    out = [(w, None, h) for w in CASES for h in (1, MX_PAIR_HINT)]
-    return out + [(WORKLOADS[n], r, h) for n, r in FULL for h in (None, MX_PAIR_HINT)]
+    # hint 65536: both GEMMs on token-major CTA pairs (block-scaled cta_group::2 MMAs);
+    # K_CTA: the 1-CTA kernel; K_SWAP: the swapped-operand pair kernel; None: the layer's
+    # choice (the swapped kernel at both full-size slices)
+    out = [(w, None, h) for w in CASES for h in (K_CTA, MX_PAIR_HINT, K_SWAP)]
+    return out + [(WORKLOADS[n], r, h) for n, r in FULL for h in (None, K_CTA, MX_PAIR_HINT)]
 
 
 @pytest.mark.parametrize("w,rows_wanted,hint", _cases(),

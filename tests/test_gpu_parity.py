@@ -288,16 +288,23 @@ def test_split_calls_equal_fused_call(moe, w):
     assert torch.equal(Y2[:N], Y2b[:N])
 
 
+# rows_hint values that force a GEMM kernel (moe.h MOE_KERNEL_*)
+K_CTA, K_PAIR, K_SWAP = -1, -2, -3
+
 COMBINE_CASES = [
-    # workload, rows_hint (1: 1-CTA GEMM2, 4096: CTA-pair GEMM2, 0: the layer's own choice)
-    (Workload("cmb_e64", 777, 256, 256, 64, 8, 0, 64, "bf16", ("normal", 0.5)), 1),
+    # workload, rows_hint (K_CTA: 1-CTA GEMM2, 4096: CTA-pair GEMM2, K_SWAP: swapped
+    # operands, 0: N_cap / E_loc expected rows, i.e. mostly the swapped kernel here)
+    (Workload("cmb_e64", 777, 256, 256, 64, 8, 0, 64, "bf16", ("normal", 0.5)), K_CTA),
     (Workload("cmb_e64_pair", 777, 256, 256, 64, 8, 0, 64, "bf16", ("normal", 0.5)), 4096),
+    (Workload("cmb_e64_swap", 777, 256, 256, 64, 8, 0, 64, "bf16", ("normal", 0.5)), K_SWAP),
     (Workload("cmb_slice", 1000, 384, 128, 256, 8, 224, 32, "bf16"), 0),  # tokens with 0, 1 and many slots
     (Workload("cmb_zipf", 1000, 384, 128, 256, 8, 32, 32, "bf16", ("zipf", 1.1)), 0),
     (Workload("cmb_k32", 300, 128, 128, 64, 32, 0, 64, "bf16"), 0),
-    (Workload("cmb_tail", 513, 200, 96, 16, 4, 4, 8, "bf16"), 1),  # d % 64 != 0: a partial n-tile
+    (Workload("cmb_tail", 513, 200, 96, 16, 4, 4, 8, "bf16"), K_CTA),  # d % 64 != 0: a partial n-tile
+    (Workload("cmb_tail_swap", 513, 200, 96, 16, 4, 4, 8, "bf16"), K_SWAP),  # d % 256: a partial weight tile
     (Workload("cmb_mx", 1024, 512, 256, 256, 8, 0, 32, "mxfp8", ("zipf", 1.1)), 0),
     (Workload("cmb_mx_e8", 700, 256, 256, 8, 4, 0, 8, "mxfp8"), 0),
+    (Workload("cmb_mx_e8_swap", 700, 256, 256, 8, 4, 0, 8, "mxfp8"), K_SWAP),
     # rows_hint 1: the pass for few multi-slot tokens, here on a slice where many have several
     (Workload("cmb_sparse_pass", 1000, 384, 128, 256, 8, 0, 64, "bf16", ("zipf", 1.1)), 1),
 ]
@@ -430,7 +437,8 @@ PAIR_CASES = [
 
 @pytest.mark.parametrize("name,counts,d,f", PAIR_CASES, ids=[c[0] for c in PAIR_CASES])
 def test_pair_kernel_matches_oracle(moe, name, counts, d, f):
-    """bf16 GEMMs on CTA pairs (forced by a large rows_hint) vs the oracle and vs the 1-CTA kernel."""
+    """bf16 GEMMs on token-major CTA pairs (forced by a large rows_hint) and on the
+    swapped-operand kernel vs the oracle and vs the 1-CTA kernel."""
     E = len(counts)
     lg = _forced_logits(counts, E, seed=len(name))
     T = lg.shape[0]
@@ -441,7 +449,7 @@ def test_pair_kernel_matches_oracle(moe, name, counts, d, f):
     ids, probs = moe.moe_route_topk(to_dev(lg), 1)
     P = moe.moe_permute(to_dev(x), ids, probs, 0, E, "bf16")
     ys = {}
-    for hint in (1, 4096):  # 1-CTA kernel, CTA-pair kernel
+    for hint in (K_CTA, 4096, K_SWAP):  # 1-CTA kernel, token-major pairs, swapped operands
         Y2, ws = moe.moe_grouped_mlp(P["perm_x"], None, P["offsets"], P["row_prob"], pw, rows_hint=hint)
         ys[hint] = moe.moe_unpermute_combine(Y2, P["pair_to_row"], "bf16")
         torch.cuda.synchronize()
@@ -449,7 +457,8 @@ def test_pair_kernel_matches_oracle(moe, name, counts, d, f):
     yo = oracle_layer(w, x, lg, Wg, Wu, Wd)
     for hint, y in ys.items():
         assert rel_l2(to_np(y), yo) <= TOL["bf16"], hint
-    assert rel_l2(to_np(ys[4096]), to_np(ys[1])) <= 1e-2
+    for hint in (4096, K_SWAP):
+        assert rel_l2(to_np(ys[hint]), to_np(ys[K_CTA])) <= 1e-2, hint
 
 
 MX_PAIR_CASES = [
@@ -461,8 +470,8 @@ MX_PAIR_CASES = [
 
 @pytest.mark.parametrize("name,counts,d,f", MX_PAIR_CASES, ids=[c[0] for c in MX_PAIR_CASES])
 def test_mx_pair_kernel_matches_oracle(moe, name, counts, d, f):
-    """MXFP8 GEMMs on CTA pairs (block-scaled cta_group::2, forced by rows_hint = 65536) vs
-    the oracle and vs the 1-CTA MXFP8 kernel."""
+    """MXFP8 GEMMs on token-major CTA pairs (block-scaled cta_group::2, forced by rows_hint =
+    65536) and on the swapped-operand kernel vs the oracle and vs the 1-CTA MXFP8 kernel."""
     E = len(counts)
     lg = _forced_logits(counts, E, seed=len(name) + 3)
     w = Workload(name, lg.shape[0], d, f, E, 1, 0, E, "mxfp8")
@@ -472,7 +481,7 @@ def test_mx_pair_kernel_matches_oracle(moe, name, counts, d, f):
     ids, probs = moe.moe_route_topk(to_dev(lg), 1)
     P = moe.moe_permute(to_dev(x), ids, probs, 0, E, "mxfp8")
     ys = {}
-    for hint in (1, 1 << 16):
+    for hint in (K_CTA, 1 << 16, K_SWAP):
         Y2, ws = moe.moe_grouped_mlp(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, rows_hint=hint)
         ys[hint] = moe.moe_unpermute_combine(Y2, P["pair_to_row"], "mxfp8")
         torch.cuda.synchronize()
@@ -480,11 +489,12 @@ def test_mx_pair_kernel_matches_oracle(moe, name, counts, d, f):
     yo = oracle_layer(w, x, lg, Wg, Wu, Wd)
     for hint, y in ys.items():
         assert rel_l2(to_np(y), yo) <= TOL["mxfp8"], hint
-    assert rel_l2(to_np(ys[1 << 16]), to_np(ys[1])) <= 1e-2
+    for hint in (1 << 16, K_SWAP):
+        assert rel_l2(to_np(ys[hint]), to_np(ys[K_CTA])) <= 1e-2, hint
 
 
 # ----------------------------------------------------------------------------- row-gather GEMM1
-def _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd, hint=1):
+def _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd, hint=K_CTA):
     """GEMM1 reading x through row_src_token must equal GEMM1 on the permuted copy, bit for
     bit (same operand values, same MMA order); MXFP8 compares through GEMM2 (h scales live
     in the SF tile layout, whose pad bytes are unspecified)."""
@@ -510,8 +520,8 @@ def _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd, hint=1):
     else:
         h2, hs2, ws = moe.moe_expert_gemm1_swiglu_gather(xd, None, M["row_src_token"], M["offsets"], M["row_prob"], pw,
                                                          rows_hint=hint)
-    Y1, _ = moe.moe_expert_gemm2(h1, hs1, P["offsets"], pw, rows_hint=1)
-    Y2, _ = moe.moe_expert_gemm2(h2, hs2, M["offsets"], pw, rows_hint=1)
+    Y1, _ = moe.moe_expert_gemm2(h1, hs1, P["offsets"], pw, rows_hint=K_CTA)
+    Y2, _ = moe.moe_expert_gemm2(h2, hs2, M["offsets"], pw, rows_hint=K_CTA)
     torch.cuda.synchronize()
     assert moe.moe_get_device_error(ws) == 0
     assert torch.equal(h1[:N], h2[:N])
@@ -551,6 +561,63 @@ def test_pair_gather_gemm1_matches_pair_copy(moe, name, counts, d, f):
     w = Workload(name, lg.shape[0], d, f, E, 1, 0, E, "bf16")
     Wg, Wu, Wd = gen_weights(w)
     assert _gather_vs_copy(moe, w, gen_x(w), lg, Wg, Wu, Wd, hint=4096) == sum(counts)
+
+
+# ----------------------------------------------------------------------------- swapped operands
+SWAP_CASES = [
+    # name, counts per expert (k = 1), d, f: segments around the 16-token MMA granule, one and
+    # two MMAs per tile (up to 256 / more tokens), experts split over several tiles, K and
+    # weight-row tails (d % 64 != 0, 2f % 256 != 0)
+    ("swap_edges", [1, 15, 16, 17, 255, 256, 257, 383, 384, 385, 1000], 256, 256),
+    ("swap_tails", [300, 0, 513, 77], 200, 96),
+    ("swap_small", [3, 64, 0, 40, 9, 64, 1, 33], 512, 384),
+]
+
+
+@pytest.mark.parametrize("name,counts,d,f", SWAP_CASES, ids=[c[0] for c in SWAP_CASES])
+@pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
+def test_swap_kernel_matches_oracle(moe, name, counts, d, f, dtype):
+    """Both GEMMs on the swapped-operand kernel (weight rows on M, tokens on N) vs the
+    oracle and vs the 1-CTA kernel; the bf16 GEMM1 with the token rows gathered from x
+    equals the one fed by TMA from the permuted copy, bit for bit."""
+    if dtype == "mxfp8":
+        d, f = max(128, d // 128 * 128), max(128, f // 128 * 128)
+    E = len(counts)
+    lg = _forced_logits(counts, E, seed=len(name) + 11)
+    w = Workload(name, lg.shape[0], d, f, E, 1, 0, E, dtype)
+    x = gen_x(w)
+    Wg, Wu, Wd = gen_weights(w)
+    pw = moe.moe_pack_weights(to_dev(Wg), to_dev(Wu), to_dev(Wd), dtype)
+    ids, probs = moe.moe_route_topk(to_dev(lg), 1)
+    P = moe.moe_permute(to_dev(x), ids, probs, 0, E, dtype)
+    ys = {}
+    for hint in (K_CTA, K_SWAP):
+        Y2, ws = moe.moe_grouped_mlp(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, rows_hint=hint)
+        ys[hint] = moe.moe_unpermute_combine(Y2, P["pair_to_row"], dtype)
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_error(ws) == 0
+    yo = oracle_layer(w, x, lg, Wg, Wu, Wd)
+    for hint, y in ys.items():
+        assert rel_l2(to_np(y), yo) <= TOL[dtype], hint
+    assert rel_l2(to_np(ys[K_SWAP]), to_np(ys[K_CTA])) <= 1e-2
+    if dtype == "bf16":
+        assert _gather_vs_copy(moe, w, x, lg, Wg, Wu, Wd, hint=K_SWAP) == sum(counts)
+
+
+def test_swap_layer_choice(moe):
+    """moe_layer_forward runs the bf16 GEMM1 of the EP64 slice at T = 8192 on the
+    swapped-operand kernel (gather mode) and the layer matches the oracle on sampled tokens."""
+    w = WORKLOADS["ep64_T8192"]
+    assert moe.moe_layer_gemm_kernel(w.T, w.d, w.f, w.k, w.E, w.E_loc, w.dtype, 1) == "swap"
+    assert moe.moe_layer_gemm_kernel(w.T, w.d, w.f, w.k, w.E, w.E_loc, w.dtype, 2) == "pair"
+    x, lg = gen_x(w), gen_logits(w)
+    Wg, Wu, Wd = gen_weights(w)
+    y = to_np(gpu_layer(moe, w, x, lg, Wg, Wu, Wd))
+    oids, _ = oracle.route_topk(lg, w.k)
+    local = np.where(((oids >= w.e0) & (oids < w.e0 + w.E_loc)).any(1))[0]
+    tok = np.unique(np.concatenate([local[:: max(1, local.size // 40)][:40], sample_tokens(w, 8)]))
+    yo = oracle_layer(w, x, lg, Wg, Wu, Wd, tokens=tok)
+    assert rel_l2(y[tok], yo) <= TOL["bf16"]
 
 
 def test_pair_gather_layer(moe):
