@@ -11,6 +11,8 @@ imports the CUDA library.
   oracle on tiny inputs, and the MXFP8 backward token by token.
 * ``moe_backward_mx`` (numpy over the C++ codec): the MXFP8 layer backward, every backward
   GEMM operand quantised along that GEMM's contraction axis.
+* ``moe_forward_fp8`` (numpy over the C++ codec): the per-tensor FP8 layer (one
+  power-of-two scale per tensor).
 
 Functions of this module are thin ctypes marshalling around the C++ oracle.
 """
@@ -291,3 +293,76 @@ def moe_backward_mx(x, logits, dy, k: int, e0: int, E_loc: int, W_gate, W_up, W_
     mix = (probs * dp).sum(axis=1, keepdims=True)
     np.add.at(dl, (np.arange(T)[:, None].repeat(k, 1), ids), probs * (dp - mix))
     return dict(dx=dx, dlogits=dl, dW_gate=dWg, dW_up=dWu, dW_down=dWd)
+
+
+# ----------------------------------------------------------------------------- per-tensor FP8
+def fp8_tensor_exponent(amax: float) -> int:
+    """Scale exponent X of a per-tensor FP8 (E4M3) tensor whose largest magnitude is
+    ``amax``: the smallest integer with amax <= 448 * 2^X, so every value divided by 2^X
+    lies within E4M3's finite range (448 = 0.875 * 2^9; with amax = m * 2^e, m in
+    [0.5, 1): X = e - 9, or e - 8 when m > 0.875), clamped to [-127, 127]; 0 for an
+    all-zero tensor."""
+    a = float(amax)
+    if a == 0.0:
+        return 0
+    m, e = np.frexp(a)
+    X = int(e) - 9 + (1 if m > 0.875 else 0)
+    return max(-127, min(127, X))
+
+
+def fp8_tensor_quantize(a) -> tuple[np.ndarray, int]:
+    """Per-tensor FP8: E4M3 codes of a / 2^X (round to nearest even) and X for the whole of
+    ``a`` (fp64 values)."""
+    v = np.asarray(a, np.float64)
+    X = fp8_tensor_exponent(np.abs(v).max() if v.size else 0.0)
+    return e4m3_encode(v * np.exp2(-X)), X
+
+
+def fp8_tensor_dequantized(a) -> np.ndarray:
+    codes, X = fp8_tensor_quantize(a)
+    return e4m3_decode(codes) * np.exp2(X)
+
+
+def moe_forward_fp8(x, logits, k: int, e0: int, E_loc: int, W_gate, W_up, W_down, tokens=None) -> np.ndarray:
+    """fp64 layer output [n_tokens, d] of the per-tensor FP8 layer (bf16 bits in: x [T, d];
+    W_gate, W_up [E_loc, d, f]; W_down [E_loc, f, d]; logits [T, E] fp32).
+
+    "Efficient MoE training for biological foundation models", section "MXFP8 Precision
+    Reduces Memory Footprint" (the layer runs in FP8 as well as MXFP8): here every GEMM
+    operand is an E4M3 tensor with one power-of-two scale for the whole tensor
+    (``fp8_tensor_quantize``): x [T, d] as one tensor; each expert's W_gate, W_up and
+    W_down as one tensor each; h (all local routed rows, after the probability scaling)
+    as one tensor.  Accumulation, SwiGLU and the slot-ordered combine are exact fp64.
+    """
+    xv = _bf16_values(x)
+    Wg, Wu, Wd = (_bf16_values(w) for w in (W_gate, W_up, W_down))
+    lg = np.asarray(logits, np.float32)
+    T, d = xv.shape
+    f = Wg.shape[2]
+    ids, probs = route_topk(lg, k)
+    P = permute(ids, e0, E_loc)
+    off, rst, slot = P["offsets"], P["row_src_token"], P["row_slot"]
+    xq = fp8_tensor_dequantized(xv)
+    N = int(off[-1])
+    h = np.zeros((N, f))
+    for e in range(E_loc):
+        rows = slice(int(off[e]), int(off[e + 1]))
+        t, j = rst[rows].astype(np.int64), slot[rows].astype(np.int64)
+        if t.size == 0:
+            continue
+        g = xq[t] @ fp8_tensor_dequantized(Wg[e])
+        u = xq[t] @ fp8_tensor_dequantized(Wu[e])
+        h[rows] = probs[t, j][:, None] * (g / (1.0 + np.exp(-g))) * u
+    hq = fp8_tensor_dequantized(h)
+    Y2 = np.zeros((N, d))
+    for e in range(E_loc):
+        rows = slice(int(off[e]), int(off[e + 1]))
+        if off[e + 1] > off[e]:
+            Y2[rows] = hq[rows] @ fp8_tensor_dequantized(Wd[e])
+    y = np.zeros((T, d))
+    p2r = P["pair_to_row"]
+    for j in range(k):  # slot order
+        r = p2r[:, j]
+        m = r >= 0
+        y[m] += Y2[r[m]]
+    return y if tokens is None else y[np.asarray(tokens, np.int64)]

@@ -115,6 +115,49 @@ def forward(x, logits, Wg, Wu, Wd, k: int, e0: int, mx: bool = False) -> np.ndar
     return y
 
 
+def fp8_tensor_exponent(amax: float) -> int:
+    """The smallest integer X with amax <= 448 * 2^X, by search (0 for amax == 0)."""
+    if amax == 0:
+        return 0
+    X = -160
+    while not amax <= 448.0 * 2.0 ** X:
+        X += 1
+    return int(min(max(X, -127), 127))
+
+
+def fp8_tensor_quantize(v: np.ndarray):
+    """Per-tensor FP8 of the whole of v: (codes, X, dequantised values)."""
+    v = np.asarray(v, np.float64)
+    X = fp8_tensor_exponent(float(np.abs(v).max()) if v.size else 0.0)
+    codes = e4m3_nearest(v * 2.0 ** -X)
+    return codes, X, e4m3_value(codes) * 2.0 ** X
+
+
+def forward_fp8(x, logits, Wg, Wu, Wd, k: int, e0: int) -> np.ndarray:
+    """y [T, d] (fp64) of the per-tensor FP8 layer, token by token: x, each expert's three
+    matrices and h (every local routed row of the batch) are each one FP8 tensor."""
+    xq = fp8_tensor_quantize(x)[2]
+    E_loc = Wg.shape[0]
+    Wgq = np.stack([fp8_tensor_quantize(Wg[e])[2] for e in range(E_loc)])
+    Wuq = np.stack([fp8_tensor_quantize(Wu[e])[2] for e in range(E_loc)])
+    Wdq = np.stack([fp8_tensor_quantize(Wd[e])[2] for e in range(E_loc)])
+    T, d = xq.shape
+    pairs = []  # (token, expert, h row) of every local slot
+    for t in range(T):
+        ids, p = topk(logits[t], k)
+        for j in range(k):
+            e = ids[j] - e0
+            if 0 <= e < E_loc:
+                pairs.append((t, e, p[j] * silu(xq[t] @ Wgq[e]) * (xq[t] @ Wuq[e])))
+    y = np.zeros((T, d))
+    if not pairs:
+        return y
+    hq = fp8_tensor_quantize(np.stack([h for _, _, h in pairs]))[2]
+    for (t, e, _), h in zip(pairs, hq):
+        y[t] += h @ Wdq[e]
+    return y
+
+
 def _q(v: np.ndarray, axis: int) -> np.ndarray:
     """Dequantised MXFP8 values of v in 32-blocks along ``axis`` (zero-padded to 32)."""
     v = np.moveaxis(np.asarray(v, np.float64), axis, -1)

@@ -368,3 +368,82 @@ def test_down_proj_mx_matches_brute(w_dtype):
     got = oracle.down_proj_mx(codes, scales, row_expert, d, f, E_loc, Wd, w_dtype, Wd_scale)
     assert (got[[3, 17]] == 0).all()
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
+# ----------------------------------------------------------------------------- per-tensor FP8
+def test_fp8_tensor_exponent_definition():
+    """oracle.fp8_tensor_exponent (from the fp64 bit fields) is the smallest integer X with
+    amax <= 448 * 2^X, found here by search: at 448 * 2^j exactly, just above and below it,
+    powers of two, the 0.875 mantissa edge, subnormals, huge values and 0."""
+    probe = [0.0, 448.0, 448.0 * (1 + 2 ** -40), 448.0 * (1 - 2 ** -40), 1.0, 0.5, 2.0 ** -130, 2.0 ** -149,
+             3.4e38, 0.875, 0.875 * (1 + 2 ** -30), 1.75, 7.0, 7.0 * (1 + 2 ** -20), 1e-3, 123.456]
+    probe += [448.0 * 2.0 ** j for j in range(-20, 21, 3)]
+    rng = np.random.default_rng(21)
+    probe += list(np.exp(rng.uniform(-60, 60, 200)))
+    for a in probe:
+        X = oracle.fp8_tensor_exponent(a)
+        assert X == brute.fp8_tensor_exponent(a), a
+        if a > 0 and -127 < X < 127:
+            assert a <= 448.0 * 2.0 ** X and not a <= 448.0 * 2.0 ** (X - 1), a
+
+
+def test_fp8_tensor_quantize_vs_nearest_search():
+    """Per-tensor quantisation: every code is the nearest E4M3 value of v / 2^X (ties to
+    even), X from the tensor's largest magnitude; the largest element never saturates; a
+    tensor of powers of two within range round-trips exactly; scaling a tensor by 2^s
+    shifts X by s and leaves the codes unchanged."""
+    rng = np.random.default_rng(22)
+    for scale in (1e-3, 1.0, 37.0, 1e4):
+        v = rng.standard_normal((17, 40)) * scale
+        codes, X = oracle.fp8_tensor_quantize(v)
+        bc, bX, bdeq = brute.fp8_tensor_quantize(v)
+        assert X == bX
+        np.testing.assert_array_equal(codes, bc)
+        deq = oracle.e4m3_decode(codes) * 2.0 ** X
+        np.testing.assert_array_equal(deq, bdeq)
+        assert np.abs(v / 2.0 ** X).max() <= 448.0
+        c2, X2 = oracle.fp8_tensor_quantize(v * 2.0 ** 5)
+        assert X2 == X + 5
+        np.testing.assert_array_equal(c2, codes)
+    p2 = 2.0 ** rng.integers(-6, 8, size=50) * rng.choice([-1.0, 1.0], size=50)
+    p2[0] = 2.0 ** 8                                 # amax 256 <= 448: X = 0
+    codes, X = oracle.fp8_tensor_quantize(p2)
+    assert X == 0
+    np.testing.assert_array_equal(oracle.e4m3_decode(codes), p2)
+
+
+@pytest.mark.parametrize("seed,T,E,d,f,k,e0,E_loc", [
+    (31, 8, 8, 32, 32, 2, 0, 8),
+    (32, 7, 8, 64, 32, 3, 2, 4),
+    (33, 5, 4, 32, 64, 1, 1, 2),
+])
+def test_oracle_fp8_matches_brute_force(seed, T, E, d, f, k, e0, E_loc):
+    """oracle.moe_forward_fp8 (vectorised over the permutation, C++ codec, exponent from the
+    bit fields) against brute.forward_fp8 (token by token, dense expert evaluation, nearest
+    search, exponent by search): a tensor quantised per row or per expert block instead of
+    as a whole, a dropped probability or a wrong slot order fails it."""
+    x, lg, Wg, Wu, Wd = _tiny(seed, T, E, d, f, k, e0, E_loc, "bf16")
+    y = oracle.moe_forward_fp8(x, lg, k, e0, E_loc, Wg, Wu, Wd)
+    yb = brute.forward_fp8(bf16_to_f32(x).astype(np.float64), lg, *(bf16_to_f32(w).astype(np.float64)
+                                                                    for w in (Wg, Wu, Wd)), k, e0)
+    assert rel_l2(y, yb) <= 1e-12
+
+
+def test_fp8_layer_near_exact_layer():
+    """The per-tensor FP8 layer stays near the exact bf16-input layer and is not equal to it:
+    E4M3 keeps 3 mantissa bits, so each operand carries ~2-4 % relative rounding and the
+    output lands at a few percent (measured 6.5-6.7 % at these sizes, against 7.7-7.9 %
+    for the MXFP8 layer, whose power-of-two block scales put amax in [256, 512) and round
+    the largest values more coarsely); a per-tensor scale off by a binade, a dropped
+    dequantisation factor or unquantised h moves it out of that band."""
+    x, lg, Wg, Wu, Wd = _tiny(41, 64, 8, 256, 128, 2, 0, 8, "bf16")
+    d, f = 256, 128
+    y8 = oracle.moe_forward_fp8(x, lg, 2, 0, 8, Wg, Wu, Wd)
+    y = oracle.moe_forward(x, "bf16", lg, d, f, 8, 2, 0, 8, Wg, Wu, Wd, "bf16")
+    cg, sg = oracle.mx_quantize(Wg, "bf16", (8, d, f))
+    cu, su = oracle.mx_quantize(Wu, "bf16", (8, d, f))
+    cd, sd = oracle.mx_quantize(Wd, "bf16", (8, f, d))
+    ym = oracle.moe_forward(x, "bf16", lg, d, f, 8, 2, 0, 8, cg, cu, cd, "e4m3", (sg, su, sd), mx_act=True)
+    err8, errmx = rel_l2(y8, y), rel_l2(ym, y)
+    assert 0.03 < err8 <= 0.1
+    assert 0.5 * errmx <= err8 <= errmx
