@@ -116,6 +116,9 @@ def oracle_time(w, x, lg, wts, tokens, threads):
     import oracle
     Wg, Wu, Wd, wdt, scales = wts
     t0 = time.perf_counter()
+    if w.dtype == "fp8":  # per-tensor FP8: h's one scale needs every local row, whatever the sample
+        oracle.moe_forward_fp8(x, lg, w.k, w.e0, w.E_loc, Wg, Wu, Wd, tokens=tokens)
+        return time.perf_counter() - t0
     oracle.moe_forward(x, w.act_dtype, lg, w.d, w.f, w.E, w.k, w.e0, w.E_loc, Wg, Wu, Wd, wdt, scales,
                        mx_act=(w.dtype == "mxfp8"), tokens=tokens, nthreads=threads)
     return time.perf_counter() - t0
@@ -126,6 +129,8 @@ def calibrate_sample(w, x, lg, wts, threads, budget_s):
     n = max(threads, 8)
     rng = np.random.default_rng(123)
     order = rng.permutation(w.T)
+    if w.dtype == "fp8":  # the oracle's cost does not depend on the sample: time all tokens
+        return np.arange(w.T)
     while True:
         dt = oracle_time(w, x, lg, wts, np.sort(order[:n]), threads)
         if dt > budget_s / 4 or n >= w.T:
@@ -141,8 +146,8 @@ def cpu_baseline(w, budget_s):
     tok = calibrate_sample(w, x, lg, wts, threads, budget_s)
     dt = oracle_time(w, x, lg, wts, tok, threads)
     return {"value": tok.size / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{tok.size} of {w.T} tokens of {w.name} (seeded uniform sample), fp64 C++ oracle, "
-                      f"{dt:.1f} s"}
+            "sample": f"{tok.size} of {w.T} tokens of {w.name} (seeded uniform sample), fp64 "
+                      f"{'numpy oracle (per-tensor FP8)' if w.dtype == 'fp8' else 'C++ oracle'}, {dt:.1f} s"}
 
 
 def run_reference(args, w):
@@ -311,7 +316,7 @@ def backward_floor(w, N, nonempty, pk):
 
 
 SWEEP = ["tiny_fp32", "ep8_zipf_T512", "ep64_T2048", "ep64_T8192", "ep64_T32768", "mxfp8_ep8_zipf_T8192",
-         "mxfp8_ep64_T8192"]
+         "mxfp8_ep64_T8192", "fp8_ep64_T8192"]
 
 
 def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
@@ -350,6 +355,8 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     Y2 = torch.empty(moe.n_cap(T, k, E_loc), d, dtype=moe.torch_dtype(w.dtype), device="cuda")
     y = torch.empty(T, d, dtype=moe.torch_dtype(w.dtype), device="cuda")
     ws_g = moe.workspace(256)
+    # GEMM1's own workspace (per-tensor FP8: + bf16 h and its amax)
+    ws_g1 = moe.workspace(moe.lib().moe_expert_gemm1_workspace_size(moe.n_cap(T, k, E_loc), w.f, moe._dt(w.dtype)))
     wbytes = 3 * w.d * w.f * w.E_loc * (4 if w.dtype == "f32" else 2 if w.dtype == "bf16" else 1)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if wbytes <= L2_BYTES else None
 
@@ -375,7 +382,7 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
                                                    P["row_prob"], pw, h=h, h_scale=hs, ws=ws_g, rows_hint=hint)
             else:
                 moe.moe_expert_gemm1_swiglu(P["perm_x"], P["perm_x_scale"], P["offsets"], P["row_prob"], pw, h=h,
-                                            h_scale=hs, ws=ws_g, rows_hint=hint)
+                                            h_scale=hs, ws=ws_g1, rows_hint=hint)
         elif i == 3 and fused:
             moe.moe_expert_gemm2_combine(h, hs, P["offsets"], P["row_src_token"], P["pair_to_row"], pw, y=y,
                                          ws=ws_c, rows_hint=hint)
@@ -485,7 +492,7 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     # ---- roofline of the dominant kernel and of the whole layer
     bf = layer_bytes_flops(w, N, nonempty, n_tok_local)
     hbm = pk["hbm_gbs"]
-    tpeak = pk["bf16_tflops"] * (2.0 if w.dtype == "mxfp8" else 1.0)
+    tpeak = pk["bf16_tflops"] * (2.0 if w.dtype in ("mxfp8", "fp8") else 1.0)
     g2name = "gemm2_combine" if fused else "gemm2"
     dom = max(("gemm1_swiglu", g2name), key=lambda n: kern_ms[n])
     key = "gemm1" if dom == "gemm1_swiglu" else "gemm2"
@@ -504,7 +511,7 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     kname = ("simt_grouped_gemm_kernel" if w.dtype == "f32" else
              "tc_grouped_gemm_pair_kernel" if pairs1 else "tc_grouped_gemm_kernel")
     roof.update({"kernel": f"{kname} ({dom})", "traffic": recorded_traffic(dom, w.name),
-                 "peak_kind": pk_kind + (" (bf16 x2 nominal fp8 ratio)" if w.dtype == "mxfp8" else "")})
+                 "peak_kind": pk_kind + (" (bf16 x2 nominal fp8 ratio)" if w.dtype in ("mxfp8", "fp8") else "")})
     t_roof = max(bf["layer_flops"] / (tpeak * 1e12), bf["layer_bytes"] / (hbm * 1e9))
     gemm_s = (gemm1_ms + kern_ms[g2name]) / 1e3
     layer = {"roofline_us": t_roof * 1e6, "measured_us": ms_per_step * 1e3, "frac": t_roof / (ms_per_step / 1e3),
@@ -647,7 +654,8 @@ def run_ours(args, w):
     line = {
         "metric": METRIC, "value": R["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": R["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "mxfp8": "e4m3+e8m0 (mxfp8)"}[w.dtype],
+        "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "mxfp8": "e4m3+e8m0 (mxfp8)",
+                                       "fp8": "e4m3, one power-of-two scale per tensor (fp8)"}[w.dtype],
         "data": "synthetic (seeded; shapes of the pages' workloads)", "config": workload_config(w),
         "roofline": R["roof"], "layer": R["layer"], "kernels_us": {n: 1e3 * v for n, v in R["kern_ms"].items()},
         "timed_region_ms": R["region_ms"],

@@ -68,6 +68,9 @@ typedef int32_t moe_dtype;
 #define MOE_F32 0   /* fp32 inputs and outputs; expert GEMMs in fp32 FMA                  */
 #define MOE_BF16 1  /* bf16 inputs/weights/outputs; tcgen05 bf16 MMA, fp32 accumulate   */
 #define MOE_MXFP8 2 /* E4M3 values + E8M0 scale per 32 along K; tcgen05 block-scaled MMA */
+#define MOE_FP8 3   /* per-tensor FP8: E4M3 values, one power-of-two scale per tensor (x, each */
+                    /* expert weight matrix, h); stored in the MXFP8 layouts with every block  */
+                    /* scale equal to the tensor's, run by the same block-scaled MMAs          */
 
 /* Grouped-GEMM kernel shapes.  Passed as rows_hint (negative values), they force that
  * kernel; moe_layer_gemm_kernel reports the one moe_layer_forward picks.
@@ -130,13 +133,15 @@ moe_status moe_route_topk(const float* logits, int T, int E, int k, int32_t* top
  * pair_to_row[t, j] = row (or -1 if not local), perm_x[row, :] = x[t, :].  The result is
  * deterministic (no atomics decide a position).
  *   x            device [T, d]  x_dtype MOE_F32 or MOE_BF16
- *   perm_dtype   element type of perm_x: MOE_F32 (x fp32), MOE_BF16 (x bf16) or MOE_MXFP8
- *                (x bf16; rows quantised while copied, scales to perm_x_scale)
+ *   perm_dtype   element type of perm_x: MOE_F32 (x fp32), MOE_BF16 (x bf16), MOE_MXFP8
+ *                (x bf16 or fp32; rows quantised while copied, scales to perm_x_scale) or
+ *                MOE_FP8 (the same layouts; x quantised as one tensor: an amax pass over
+ *                all of x [T, d] first, then every scale byte = its exponent + 127)
  *   perm_x       device [N_cap, d], N_cap = T * min(k, E_loc); rows >= N untouched.
  *                NULL: maps only -- counts, offsets, row_src_token, row_prob and
  *                pair_to_row are written, no rows are copied (the input of
  *                moe_expert_gemm1_swiglu_gather); perm_x_scale is then ignored
- *   perm_x_scale device, MOE_MXFP8 with perm_x only (else NULL): SF tile layout, K = d,
+ *   perm_x_scale device, MOE_MXFP8 / MOE_FP8 with perm_x only (else NULL): SF tile layout, K = d,
  *                moe_mx_act_scale_bytes(N_cap, d, E_loc) bytes
  *   counts [E_loc], offsets [E_loc+1], row_src_token [N_cap], row_prob [N_cap] (fp32),
  *   pair_to_row [T, k]: device int32 outputs
@@ -184,11 +189,24 @@ size_t moe_mx_act_scale_bytes(int64_t N_cap, int K, int E_loc);
  * MOE_F32 or MOE_BF16) to the packed layout above in dst_dtype: MOE_F32 (src fp32),
  * MOE_BF16 (src bf16) or MOE_MXFP8 (src bf16 or fp32; quantised per output column in
  * blocks of 32 along K, scales to Wgu_scale / Wd_scale, sizes moe_mx_weight_scale_bytes).
- * All pointers device.  MXFP8 requires d % 128 == 0 and f % 128 == 0. */
+ * All pointers device.  MXFP8 requires d % 128 == 0 and f % 128 == 0.  Per-tensor FP8
+ * (MOE_FP8) is packed by moe_pack_weights_fp8 (MOE_ERR_UNSUPPORTED here). */
 moe_status moe_pack_weights(const void* W_gate, const void* W_up, const void* W_down, moe_dtype src_dtype,
                             moe_dtype dst_dtype, int E_loc, int d, int f, void* Wgu_packed, void* Wd_packed,
                             uint8_t* Wgu_scale, uint8_t* Wd_scale, moe_stream_t stream);
 size_t moe_mx_weight_scale_bytes(int E_loc, int rows, int K);
+/* Per-tensor FP8 packing [BIO "MXFP8 Precision Reduces Memory Footprint": the layer runs
+ * in FP8 as well as MXFP8].  Each expert's W_gate, W_up and W_down is one E4M3 tensor
+ * with one power-of-two scale 2^X, X the smallest integer with amax <= 448 * 2^X (amax:
+ * the matrix's largest magnitude; X clamped to [-127, 127], 0 for an all-zero matrix), so
+ * the codes RNE(v / 2^X) never saturate.  Output: the MXFP8 packed layouts (codes as for
+ * moe_pack_weights, every scale byte of a matrix X + 127), and w_exp [3][E_loc] int32 =
+ * X of W_gate, W_up, W_down per expert.  src_dtype MOE_BF16 or MOE_FP32; d % 128 == 0,
+ * f % 128 == 0; all pointers device, 16-byte aligned matrices.  Four kernel passes: the
+ * three amax reductions (into w_exp), the quantisation, the exponents (in place). */
+moe_status moe_pack_weights_fp8(const void* W_gate, const void* W_up, const void* W_down, moe_dtype src_dtype,
+                                int E_loc, int d, int f, void* Wgu_packed, void* Wd_packed, uint8_t* Wgu_scale,
+                                uint8_t* Wd_scale, int32_t* w_exp, moe_stream_t stream);
 
 /* Grouped expert MLP (steps 3-4) [BIO "GroupedLinear ...", "MXFP8 Precision ..."].
  * For each local expert e and each row i of its segment [offsets[e], offsets[e+1]):
@@ -212,8 +230,10 @@ size_t moe_mx_weight_scale_bytes(int E_loc, int rows, int K);
  *              d >= 4096; bf16 GEMM2 on token-major pairs from 128; MXFP8 GEMMs on pairs
  *              only from 65536 (the block-scaled pair kernel measured slower than the 1-CTA
  *              one on every shape tried); everything else on the 1-CTA kernel.  0 uses
- *              N_cap / E_loc; MOE_KERNEL_* forces a kernel.
- * Requires d % 8 == 0 and f % 32 == 0 (bf16); d % 128 == 0 and f % 128 == 0 (MXFP8). */
+ *              N_cap / E_loc; MOE_KERNEL_* forces a kernel.  MOE_FP8 always runs on the
+ *              1-CTA kernel: GEMM1 writes bf16 h and its amax into the workspace, h is
+ *              quantised as one tensor, GEMM2 reads it like MXFP8.
+ * Requires d % 8 == 0 and f % 32 == 0 (bf16); d % 128 == 0 and f % 128 == 0 (MXFP8, FP8). */
 moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                            const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
                            const void* Wgu_packed, const uint8_t* Wgu_scale, const void* Wd_packed,
@@ -240,7 +260,9 @@ size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, mo
 
 /* The two halves of moe_grouped_mlp, for callers that keep h themselves (same
  * preconditions; N = offsets[E_loc] on the device).
- *   moe_expert_gemm1_swiglu: perm_x (+ scales) -> h [N_cap, f] (fp32 / bf16 / E4M3 bytes)
+ *   moe_expert_gemm1_swiglu: perm_x (+ scales) -> h [N_cap, f] (fp32 / bf16 / E4M3 bytes;
+ *       MOE_FP8: GEMM1 writes bf16 h and its amax into the workspace, then h is quantised
+ *       as one tensor into h / h_scale; workspace >= moe_expert_gemm1_workspace_size())
  *       and, for MOE_MXFP8, h_scale in the SF tile layout with K = f
  *       (moe_mx_act_scale_bytes(N_cap, f, E_loc) bytes) [BIO "GroupedLinear ...":
  *       GroupedLinear + ScaledSwiGLU (+ quantisation) in one kernel].
@@ -248,6 +270,9 @@ size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, mo
  *       [BIO: the second GroupedLinear].
  *   rows_hint: as for moe_grouped_mlp.
  *   workspace: >= moe_expert_gemm_workspace_size() bytes, 256-byte aligned (error word). */
+/* Workspace of moe_expert_gemm1_swiglu: the error word, plus for MOE_FP8 bf16 h [N_cap, f]
+ * and its amax. */
+size_t moe_expert_gemm1_workspace_size(int64_t N_cap, int f, moe_dtype dtype);
 moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_scale, const int32_t* offsets,
                                    const float* row_prob, int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype,
                                    const void* Wgu_packed, const uint8_t* Wgu_scale, void* h, uint8_t* h_scale,
@@ -264,7 +289,7 @@ size_t moe_expert_gemm_workspace_size(void);
  * tile from the token rows into shared memory itself.
  *   x        MOE_BF16: device bf16 [T, d].  MOE_MXFP8: device E4M3 bytes [T, d] with
  *            x_scale device E8M0 [T, d / 32] row-major (from moe_quantize_mx_rows).
- *            (MOE_F32 is not supported: MOE_ERR_UNSUPPORTED.)
+ *            (MOE_F32 and MOE_FP8 are not supported: MOE_ERR_UNSUPPORTED.)
  *   row_src_token [N_cap], offsets [E_loc+1], row_prob [N_cap]: device, from moe_permute
  *            (which may be called with perm_x == NULL)
  *   h, h_scale, Wgu_*, rows_hint, workspace: as for moe_expert_gemm1_swiglu (bf16: the
@@ -334,6 +359,11 @@ size_t moe_expert_gemm2_combine_workspace_size(int64_t N_cap, int T, int d);
  *   copy is made: bf16 layers feed GEMM1 by row gather, except when the CTA-pair GEMM1
  *   is chosen (moe_layer_gemm1_pairs), which reads a permuted copy; fp32 and MXFP8
  *   layers copy (MXFP8 quantises while copying).
+ *   MOE_FP8 (per-tensor FP8, weights from moe_pack_weights_fp8): x is one E4M3 tensor (its
+ *   amax over all T x d values gives X as for the weights), quantised while copying; GEMM1
+ *   writes bf16 h and its amax, h is then quantised as one tensor (all local rows), and
+ *   GEMM2 and the combine run as for MXFP8 (the block-scaled kernels with every scale of
+ *   a tensor equal).
  * Requires T * min(k, E_loc) <= 2^31 - 1 (int32 row indices), else MOE_ERR_INVALID_ARG. */
 moe_status moe_layer_forward(const void* x, const float* logits, int T, int d, int f, int E, int k, int e0,
                              int E_loc, moe_dtype dtype, const void* Wgu_packed, const uint8_t* Wgu_scale,

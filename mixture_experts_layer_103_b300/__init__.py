@@ -25,8 +25,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
-MOE_F32, MOE_BF16, MOE_MXFP8 = 0, 1, 2
-DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "mxfp8": MOE_MXFP8}
+MOE_F32, MOE_BF16, MOE_MXFP8, MOE_FP8 = 0, 1, 2, 3
+DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "mxfp8": MOE_MXFP8, "fp8": MOE_FP8}
+FP8_CODES = (MOE_MXFP8, MOE_FP8)  # E4M3 codes with scales in the SF tile layouts
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
 
@@ -54,6 +55,8 @@ _SIGS = {
     "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
     "moe_permute_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_mx_act_scale_bytes": (_SZ, [_I64, _I, _I]),
+    "moe_expert_gemm1_workspace_size": (_SZ, [_I64, _I, _I]),
+    "moe_pack_weights_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_pack_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_mx_weight_scale_bytes": (_SZ, [_I, _I, _I]),
     "moe_grouped_mlp": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
@@ -153,7 +156,7 @@ def alloc_permute(T: int, d: int, k: int, E_loc: int, x_dtype: torch.dtype, perm
     cap = n_cap(T, k, E_loc)
     if maps_only:
         perm_x = perm_sf = None
-    elif _dt(perm_dtype) == MOE_MXFP8:
+    elif _dt(perm_dtype) in FP8_CODES:
         perm_x = torch.empty(cap, d, dtype=torch.uint8, device=device)
         perm_sf = torch.empty(max(1, _lib.moe_mx_act_scale_bytes(cap, d, E_loc)), dtype=torch.uint8, device=device)
     else:
@@ -210,6 +213,7 @@ class PackedWeights:
     Wd: torch.Tensor
     Wgu_scale: torch.Tensor | None = None
     Wd_scale: torch.Tensor | None = None
+    w_exp: torch.Tensor | None = None  # per-tensor FP8: exponents [3, E_loc] of W_gate, W_up, W_down
 
 
 def moe_pack_weights(W_gate: torch.Tensor, W_up: torch.Tensor, W_down: torch.Tensor, dtype="bf16") -> PackedWeights:
@@ -217,7 +221,7 @@ def moe_pack_weights(W_gate: torch.Tensor, W_up: torch.Tensor, W_down: torch.Ten
     dev = W_gate.device
     src = MOE_F32 if W_gate.dtype == torch.float32 else MOE_BF16
     dst = _dt(dtype)
-    if dst == MOE_MXFP8:
+    if dst in FP8_CODES:
         Wgu = torch.empty(E_loc, 2 * f, d, dtype=torch.uint8, device=dev)
         Wd = torch.empty(E_loc, d, f, dtype=torch.uint8, device=dev)
         sg = torch.empty(_lib.moe_mx_weight_scale_bytes(E_loc, 2 * f, d), dtype=torch.uint8, device=dev)
@@ -227,6 +231,12 @@ def moe_pack_weights(W_gate: torch.Tensor, W_up: torch.Tensor, W_down: torch.Ten
         Wgu = torch.empty(E_loc, 2 * f, d, dtype=tdt, device=dev)
         Wd = torch.empty(E_loc, d, f, dtype=tdt, device=dev)
         sg = sd = None
+    if dst == MOE_FP8:
+        w_exp = torch.empty(3, E_loc, dtype=torch.int32, device=dev)
+        _check("moe_pack_weights_fp8", _lib.moe_pack_weights_fp8(
+            _ptr(W_gate), _ptr(W_up), _ptr(W_down), src, E_loc, d, f, _ptr(Wgu), _ptr(Wd), _ptr(sg), _ptr(sd),
+            _ptr(w_exp), _stream()))
+        return PackedWeights(dst, E_loc, d, f, Wgu, Wd, sg, sd, w_exp)
     _check("moe_pack_weights", _lib.moe_pack_weights(
         _ptr(W_gate), _ptr(W_up), _ptr(W_down), src, dst, E_loc, d, f, _ptr(Wgu), _ptr(Wd), _ptr(sg), _ptr(sd),
         _stream()))
@@ -281,7 +291,7 @@ def moe_grouped_mlp(perm_x, perm_x_scale, offsets, row_prob, pw: PackedWeights, 
 
 def alloc_h(N_cap: int, pw: PackedWeights, device="cuda"):
     """h buffer (+ its MXFP8 scales) for moe_expert_gemm1_swiglu."""
-    if pw.dtype == MOE_MXFP8:
+    if pw.dtype in FP8_CODES:
         return (torch.empty(N_cap, pw.f, dtype=torch.uint8, device=device),
                 torch.empty(max(1, _lib.moe_mx_act_scale_bytes(N_cap, pw.f, pw.E_loc)), dtype=torch.uint8,
                             device=device))
@@ -293,7 +303,7 @@ def moe_expert_gemm1_swiglu(perm_x, perm_x_scale, offsets, row_prob, pw: PackedW
     cap = perm_x.shape[0]
     if h is None:
         h, h_scale = alloc_h(cap, pw, perm_x.device)
-    ws = ws if ws is not None else workspace(_lib.moe_expert_gemm_workspace_size(), perm_x.device)
+    ws = ws if ws is not None else workspace(_lib.moe_expert_gemm1_workspace_size(cap, pw.f, pw.dtype), perm_x.device)
     _check("moe_expert_gemm1_swiglu", _lib.moe_expert_gemm1_swiglu(
         _ptr(perm_x), _ptr(perm_x_scale), _ptr(offsets), _ptr(row_prob), cap, pw.E_loc, pw.d, pw.f, pw.dtype,
         _ptr(pw.Wgu), _ptr(pw.Wgu_scale), _ptr(h), _ptr(h_scale), int(rows_hint), _ptr(ws), ws.numel(), _stream()))

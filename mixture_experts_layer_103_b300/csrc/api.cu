@@ -61,7 +61,14 @@ cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t 
 int32_t* permute_mtile_base(uint8_t* ws, int T, int E_loc);
 cudaError_t launch_gather_rows_mx(const void* src, int K, const int32_t* offsets, int E_loc,
                                   const int32_t* mtile_base, const int32_t* row_src_token, uint8_t* dst,
-                                  uint8_t* dst_sf, cudaStream_t st);
+                                  uint8_t* dst_sf, cudaStream_t st, const uint32_t* tensor_amax = nullptr);
+cudaError_t launch_tc_gemm1_fp8(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets,
+                                const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* Wgu,
+                                const uint8_t* Wgu_sf, void* h_bf16, uint32_t* h_amax, int32_t* err,
+                                uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_pack_fp8(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, int E_loc, int d, int f,
+                            void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, int32_t* w_exp,
+                            cudaStream_t st);
 cudaError_t launch_pack_backward_mx(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, int E_loc, int d,
                                     int f, uint8_t* WguT_q, uint8_t* WguT_sf, uint8_t* Wd_q, uint8_t* Wd_sf,
                                     cudaStream_t st);
@@ -98,6 +105,9 @@ int num_sms() {
 int gather_grid(cudaStream_t) { return num_sms() * 6; }
 
 static int elt_bytes(moe_dtype dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
+// E4M3 codes with scales in the SF tile layouts: MXFP8, and per-tensor FP8 (every scale of
+// a tensor equal), which runs on the same block-scaled kernels.
+static bool is_fp8(moe_dtype dt) { return dt == MOE_MXFP8 || dt == MOE_FP8; }
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 static moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -106,20 +116,29 @@ static size_t mx_act_sf_bytes(int64_t n_cap, int K, int E_loc) {
   return static_cast<size_t>(mx_tiles_cap(n_cap, E_loc)) * (K / 128) * 512;
 }
 
-// ---- grouped MLP scratch: h (+ its scales) -------------------------------------------
+// ---- grouped MLP scratch: h (+ its scales; per-tensor FP8: + bf16 h and its amax) ----
 struct MlpScratch {
   void* h;
   uint8_t* h_sf;
+  void* h16;          // per-tensor FP8: GEMM1's bf16 h, quantised once its amax is known
+  uint32_t* h_amax;   // per-tensor FP8: largest |h| (fp32 bits)
 };
 static size_t mlp_scratch_bytes(int64_t n_cap, int E_loc, int f, moe_dtype dt) {
   size_t b = align_up(static_cast<size_t>(n_cap) * f * elt_bytes(dt), kAlign);
-  if (dt == MOE_MXFP8) b += align_up(mx_act_sf_bytes(n_cap, f, E_loc), kAlign);
+  if (is_fp8(dt)) b += align_up(mx_act_sf_bytes(n_cap, f, E_loc), kAlign);
+  if (dt == MOE_FP8) b += align_up(static_cast<size_t>(n_cap) * f * 2, kAlign) + kAlign;
   return b;
 }
-static MlpScratch carve_mlp(uint8_t* p, int64_t n_cap, int f, moe_dtype dt) {
-  MlpScratch s;
+static MlpScratch carve_mlp(uint8_t* p, int64_t n_cap, int f, moe_dtype dt, int E_loc) {
+  MlpScratch s{};
   s.h = p;
-  s.h_sf = dt == MOE_MXFP8 ? p + align_up(static_cast<size_t>(n_cap) * f * elt_bytes(dt), kAlign) : nullptr;
+  const size_t hb = align_up(static_cast<size_t>(n_cap) * f * elt_bytes(dt), kAlign);
+  s.h_sf = is_fp8(dt) ? p + hb : nullptr;
+  if (dt == MOE_FP8) {
+    uint8_t* q = p + hb + align_up(mx_act_sf_bytes(n_cap, f, E_loc), kAlign);
+    s.h16 = q;
+    s.h_amax = reinterpret_cast<uint32_t*>(q + align_up(static_cast<size_t>(n_cap) * f * 2, kAlign));
+  }
   return s;
 }
 
@@ -127,8 +146,8 @@ static moe_status check_mlp_shape(int d, int f, int E_loc, moe_dtype dt) {
   if (d <= 0 || f <= 0 || E_loc < 1 || E_loc > 1024) return MOE_ERR_INVALID_ARG;
   if (f % 32 != 0) return MOE_ERR_UNSUPPORTED;
   if (dt == MOE_BF16 && d % 8 != 0) return MOE_ERR_UNSUPPORTED;
-  if (dt == MOE_MXFP8 && (d % 128 != 0 || f % 128 != 0)) return MOE_ERR_UNSUPPORTED;
-  if (dt != MOE_F32 && dt != MOE_BF16 && dt != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (is_fp8(dt) && (d % 128 != 0 || f % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (dt != MOE_F32 && dt != MOE_BF16 && !is_fp8(dt)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -205,6 +224,7 @@ static int swap_tokens(moe_dtype dt, int64_t rows) {
 // N_cap / E_loc; MOE_KERNEL_* (negative): that kernel.  keeps_gu: GEMM1 must also write
 // the gate/up pre-activations (the swapped kernel does not).
 static int gemm_shape(bool gemm1, moe_dtype dt, int64_t n_cap, int E_loc, int rows_hint, int K, bool keeps_gu) {
+  if (dt == MOE_FP8) return 0;  // per-tensor FP8: the 1-CTA block-scaled kernel, whatever the hint
   const int64_t rows = expected_rows(n_cap, E_loc, rows_hint > 0 ? rows_hint : 0);
   const bool swap_ok = dt != MOE_F32 && E_loc <= kSwapElocMax && !(gemm1 && keeps_gu);
   if (rows_hint == MOE_KERNEL_CTA) return 0;
@@ -218,12 +238,25 @@ static int gemm_shape(bool gemm1, moe_dtype dt, int64_t n_cap, int E_loc, int ro
 static cudaError_t run_gemm1(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets,
                              const float* row_prob, int64_t n_cap, int E_loc, int d, int f, moe_dtype dt,
                              const void* Wgu, const uint8_t* Wgu_sf, void* h, uint8_t* h_sf, int32_t* err,
-                             int rows_hint, cudaStream_t st, void* gu_save = nullptr) {
+                             int rows_hint, cudaStream_t st, void* gu_save = nullptr, void* h16 = nullptr,
+                             uint32_t* h_amax = nullptr) {
   if (n_cap == 0) return cudaSuccess;
+  if (dt == MOE_FP8) {
+    // per-tensor FP8: bf16 h and its largest magnitude first, then h as one E4M3 tensor
+    // (one exponent, rows in place order) for GEMM2
+    if (!h16 || !h_amax) return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(h_amax, 0, 4, st);
+    if (e == cudaSuccess)
+      e = launch_tc_gemm1_fp8(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, Wgu, Wgu_sf, h16, h_amax, err,
+                              kTimeoutNs, st);
+    if (e == cudaSuccess)
+      e = launch_gather_rows_mx(h16, f, offsets, E_loc, nullptr, nullptr, static_cast<uint8_t*>(h), h_sf, st, h_amax);
+    return e;
+  }
   if (dt == MOE_F32)
     return launch_simt_gemm1(static_cast<const float*>(perm_x), offsets, row_prob, n_cap, E_loc, d, f,
                              static_cast<const float*>(Wgu), static_cast<float*>(h), st);
-  return launch_tc_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt == MOE_MXFP8,
+  return launch_tc_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, is_fp8(dt),
                          gemm_shape(true, dt, n_cap, E_loc, rows_hint, d, gu_save != nullptr), Wgu, Wgu_sf, h, h_sf,
                          err, kTimeoutNs, gu_save, st);
 }
@@ -235,7 +268,7 @@ static cudaError_t run_gemm2(const void* h, const uint8_t* h_sf, const int32_t* 
   if (dt == MOE_F32)
     return launch_simt_gemm2(static_cast<const float*>(h), offsets, n_cap, E_loc, d, f, static_cast<const float*>(Wd),
                              static_cast<float*>(Y2), st);
-  return launch_tc_gemm2(h, h_sf, offsets, n_cap, E_loc, d, f, dt == MOE_MXFP8,
+  return launch_tc_gemm2(h, h_sf, offsets, n_cap, E_loc, d, f, is_fp8(dt),
                          gemm_shape(false, dt, n_cap, E_loc, rows_hint, f, false), Wd, Wd_sf, Y2, err, kTimeoutNs, st);
 }
 
@@ -243,9 +276,9 @@ static cudaError_t run_mlp(const void* perm_x, const uint8_t* perm_sf, const int
                            int64_t n_cap, int E_loc, int d, int f, moe_dtype dt, const void* Wgu, const uint8_t* Wgu_sf,
                            const void* Wd, const uint8_t* Wd_sf, void* Y2, uint8_t* scratch, int32_t* err,
                            int rows_hint, cudaStream_t st, void* gu_save = nullptr) {
-  MlpScratch s = carve_mlp(scratch, n_cap, f, dt);
+  MlpScratch s = carve_mlp(scratch, n_cap, f, dt, E_loc);
   cudaError_t e = run_gemm1(perm_x, perm_sf, offsets, row_prob, n_cap, E_loc, d, f, dt, Wgu, Wgu_sf, s.h, s.h_sf, err,
-                            rows_hint, st, gu_save);
+                            rows_hint, st, gu_save, s.h16, s.h_amax);
   if (e != cudaSuccess) return e;
   return run_gemm2(s.h, s.h_sf, offsets, n_cap, E_loc, d, f, dt, Wd, Wd_sf, Y2, err, rows_hint, st);
 }
@@ -310,7 +343,7 @@ static LayerWs layer_layout(uint8_t* base, int T, int d, int f, int E, int k, in
   w.perm_ws = take(permute_ws_bytes(T, E_loc));
   if (!gather) {
     w.perm_x = take(static_cast<size_t>(n_cap) * d * elt_bytes(dt));
-    w.perm_sf = dt == MOE_MXFP8 ? take(mx_act_sf_bytes(n_cap, d, E_loc)) : nullptr;
+    w.perm_sf = is_fp8(dt) ? take(mx_act_sf_bytes(n_cap, d, E_loc)) : nullptr;
   } else if (dt == MOE_MXFP8) {
     w.perm_x = take(static_cast<size_t>(T) * d);
     w.perm_sf = take(static_cast<size_t>(T) * (d / 32));
@@ -442,11 +475,11 @@ moe_status moe::check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_d
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !ids || !probs || !rst || !rp || !p2r)) return MOE_ERR_INVALID_ARG;
   const bool ok_types = (x_dtype == MOE_F32 && perm_dtype == MOE_F32) || (x_dtype == MOE_BF16 && perm_dtype == MOE_BF16) ||
-                        ((x_dtype == MOE_BF16 || x_dtype == MOE_F32) && perm_dtype == MOE_MXFP8);
+                        ((x_dtype == MOE_BF16 || x_dtype == MOE_F32) && is_fp8(perm_dtype));
   if (!ok_types) return MOE_ERR_UNSUPPORTED;
   if ((x_dtype == MOE_BF16 && d % 8 != 0) || (x_dtype == MOE_F32 && d % 4 != 0)) return MOE_ERR_UNSUPPORTED;
   // perm_x == NULL: maps only (no permuted copy, so no scales either)
-  if (perm_dtype == MOE_MXFP8 && (d % 128 != 0 || (T > 0 && perm_x && !perm_sf)))
+  if (is_fp8(perm_dtype) && (d % 128 != 0 || (T > 0 && perm_x && !perm_sf)))
     return (T > 0 && perm_x && !perm_sf) ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
   if (T > 0 && (!aligned16(x) || (perm_x && !aligned16(perm_x)))) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -485,6 +518,20 @@ moe_status moe_pack_weights(const void* W_gate, const void* W_up, const void* W_
                                  Wgu_scale, Wd_scale, stream));
 }
 
+moe_status moe_pack_weights_fp8(const void* W_gate, const void* W_up, const void* W_down, moe_dtype src_dtype,
+                                int E_loc, int d, int f, void* Wgu_packed, void* Wd_packed, uint8_t* Wgu_scale,
+                                uint8_t* Wd_scale, int32_t* w_exp, moe_stream_t stream) {
+  if (!W_gate || !W_up || !W_down || !Wgu_packed || !Wd_packed || !Wgu_scale || !Wd_scale || !w_exp)
+    return MOE_ERR_INVALID_ARG;
+  moe_status s = check_mlp_shape(d, f, E_loc, MOE_FP8);
+  if (s != MOE_OK) return s;
+  if (src_dtype != MOE_BF16 && src_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(W_gate) || !aligned16(W_up) || !aligned16(W_down) || !aligned16(Wgu_packed) || !aligned16(Wd_packed))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_fp8(W_gate, W_up, W_down, src_dtype, E_loc, d, f, Wgu_packed, Wd_packed, Wgu_scale,
+                                     Wd_scale, w_exp, stream));
+}
+
 size_t moe_grouped_mlp_workspace_size(int64_t N_cap, int E_loc, int d, int f, moe_dtype dtype) {
   (void)d;
   if (N_cap < 0 || E_loc < 1 || f <= 0) return 0;
@@ -501,7 +548,7 @@ moe_status moe_grouped_mlp(const void* perm_x, const uint8_t* perm_x_scale, cons
   if (N_cap < 0 || N_cap > (int64_t(1) << 31) - 1) return MOE_ERR_INVALID_ARG;
   if (!offsets) return MOE_ERR_INVALID_ARG;
   if (N_cap > 0 && (!perm_x || !row_prob || !Wgu_packed || !Wd_packed || !Y2)) return MOE_ERR_INVALID_ARG;
-  if (dtype == MOE_MXFP8 && N_cap > 0 && (!perm_x_scale || !Wgu_scale || !Wd_scale)) return MOE_ERR_INVALID_ARG;
+  if (is_fp8(dtype) && N_cap > 0 && (!perm_x_scale || !Wgu_scale || !Wd_scale)) return MOE_ERR_INVALID_ARG;
   if (N_cap > 0 && (!aligned16(perm_x) || !aligned16(Wgu_packed) || !aligned16(Wd_packed) || !aligned16(Y2) ||
                     (perm_x_scale && !aligned16(perm_x_scale)) || (Wgu_scale && !aligned16(Wgu_scale)) ||
                     (Wd_scale && !aligned16(Wd_scale))))
@@ -534,7 +581,7 @@ int moe_layer_gemm1_pairs(int T, int d, int k, int E, int E_loc, moe_dtype dtype
 int moe_layer_gemm_kernel(int T, int d, int f, int k, int E, int E_loc, moe_dtype dtype, int gemm) {
   if (T < 0 || d <= 0 || f <= 0 || k <= 0 || E <= 0 || E_loc <= 0 || E_loc > E || (gemm != 1 && gemm != 2))
     return 0;
-  if (dtype != MOE_F32 && dtype != MOE_BF16 && dtype != MOE_MXFP8) return 0;
+  if (dtype != MOE_F32 && dtype != MOE_BF16 && !is_fp8(dtype)) return 0;
   const int s = gemm_shape(gemm == 1, dtype, n_cap_of(T, k, E_loc), E_loc, moe_rows_hint(T, k, E), gemm == 1 ? d : f,
                            false);
   return s >= kShapeSwapMin ? MOE_KERNEL_SWAP : s == 1 ? MOE_KERNEL_PAIR : MOE_KERNEL_CTA;
@@ -548,7 +595,7 @@ static moe_status check_gemm_common(int64_t N_cap, int E_loc, int d, int f, moe_
   if (N_cap < 0 || N_cap > (int64_t(1) << 31) - 1 || !offsets) return MOE_ERR_INVALID_ARG;
   if (N_cap == 0) return MOE_OK;
   if (!a || !w || !out || !aligned16(a) || !aligned16(w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-  if (dtype == MOE_MXFP8 && (!a_sf || !w_sf || !aligned16(a_sf) || !aligned16(w_sf))) return MOE_ERR_INVALID_ARG;
+  if (is_fp8(dtype) && (!a_sf || !w_sf || !aligned16(a_sf) || !aligned16(w_sf))) return MOE_ERR_INVALID_ARG;
   (void)out_sf;
   return MOE_OK;
 }
@@ -560,11 +607,22 @@ moe_status moe_expert_gemm1_swiglu(const void* perm_x, const uint8_t* perm_x_sca
   moe_status s = check_gemm_common(N_cap, E_loc, d, f, dtype, offsets, perm_x, perm_x_scale, Wgu_packed, Wgu_scale, h,
                                    h_scale);
   if (s != MOE_OK) return s;
-  if (N_cap > 0 && (!row_prob || (dtype == MOE_MXFP8 && !h_scale))) return MOE_ERR_INVALID_ARG;
-  if (!workspace || !aligned256(workspace) || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+  if (N_cap > 0 && (!row_prob || (is_fp8(dtype) && !h_scale))) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned256(workspace) || workspace_bytes < moe_expert_gemm1_workspace_size(N_cap, f, dtype))
+    return MOE_ERR_WORKSPACE;
   int32_t* err = static_cast<int32_t*>(workspace);
+  // per-tensor FP8: GEMM1's bf16 h and its amax live in the workspace after the error word
+  uint8_t* h16 = static_cast<uint8_t*>(workspace) + sizeof(WsHeader);
+  uint32_t* h_amax = reinterpret_cast<uint32_t*>(h16 + align_up(static_cast<size_t>(N_cap) * f * 2, kAlign));
   return cuda_status(run_gemm1(perm_x, perm_x_scale, offsets, row_prob, N_cap, E_loc, d, f, dtype, Wgu_packed,
-                               Wgu_scale, h, h_scale, err, rows_hint, stream));
+                               Wgu_scale, h, h_scale, err, rows_hint, stream, nullptr,
+                               dtype == MOE_FP8 ? h16 : nullptr, dtype == MOE_FP8 ? h_amax : nullptr));
+}
+
+size_t moe_expert_gemm1_workspace_size(int64_t N_cap, int f, moe_dtype dtype) {
+  if (N_cap < 0 || f <= 0) return 0;
+  if (dtype != MOE_FP8) return sizeof(WsHeader);
+  return sizeof(WsHeader) + align_up(static_cast<size_t>(N_cap) * f * 2, kAlign) + kAlign;
 }
 
 moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale, const int32_t* row_src_token,
@@ -572,7 +630,7 @@ moe_status moe_expert_gemm1_swiglu_gather(const void* x, const uint8_t* x_scale,
                                           int d, int f, moe_dtype dtype, const void* Wgu_packed,
                                           const uint8_t* Wgu_scale, void* h, uint8_t* h_scale, int rows_hint,
                                           void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-  if (dtype == MOE_F32) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_F32 || dtype == MOE_FP8) return MOE_ERR_UNSUPPORTED;
   moe_status s = check_gemm_common(N_cap, E_loc, d, f, dtype, offsets, x, x_scale, Wgu_packed, Wgu_scale, h, h_scale);
   if (s != MOE_OK) return s;
   if (N_cap > 0 && (!row_src_token || !row_prob || (dtype == MOE_MXFP8 && !h_scale))) return MOE_ERR_INVALID_ARG;
@@ -607,7 +665,7 @@ moe_status moe_expert_gemm2(const void* h, const uint8_t* h_scale, const int32_t
 moe_status moe_unpermute_combine(const void* Y2, const int32_t* pair_to_row, int T, int k, int d, moe_dtype dtype,
                                  void* y, moe_stream_t stream) {
   if (T < 0 || k < 1 || k > 32 || d <= 0) return MOE_ERR_INVALID_ARG;
-  if (dtype != MOE_F32 && dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (dtype != MOE_F32 && dtype != MOE_BF16 && !is_fp8(dtype)) return MOE_ERR_UNSUPPORTED;
   if ((dtype == MOE_F32 && d % 4 != 0) || (dtype != MOE_F32 && d % 8 != 0)) return MOE_ERR_UNSUPPORTED;
   if (T > 0 && (!Y2 || !pair_to_row || !y || !aligned16(Y2) || !aligned16(y))) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_combine(Y2, pair_to_row, T, k, d, dtype, y, stream));
@@ -658,7 +716,7 @@ moe_status moe_expert_gemm2_combine(const void* h, const uint8_t* h_scale, const
   Gemm2CombineWs w = gemm2_combine_layout(static_cast<uint8_t*>(workspace), N_cap, T, d);
   cudaError_t e = launch_combine_prep(pair_to_row, T, k, w.tok_nloc, stream);
   if (e == cudaSuccess)
-    e = launch_tc_gemm2_combine(h, h_scale, offsets, N_cap, E_loc, d, f, dtype == MOE_MXFP8,
+    e = launch_tc_gemm2_combine(h, h_scale, offsets, N_cap, E_loc, d, f, is_fp8(dtype),
                                 gemm_shape(false, dtype, N_cap, E_loc, rows_hint, f, false), Wd_packed, Wd_scale, w.Y2,
                                 row_src_token, w.tok_nloc, T, y, static_cast<int32_t*>(workspace), kTimeoutNs, stream);
   // expected local slots per token (rows_hint rows per expert), which picks the sparse or
@@ -688,7 +746,7 @@ static moe_status layer_forward_impl(const void* x, const float* logits, int T, 
   moe_status s = check_mlp_shape(d, f, E_loc, dtype);
   if (s != MOE_OK) return s;
   if (!Wgu_packed || !Wd_packed) return MOE_ERR_INVALID_ARG;
-  if (dtype == MOE_MXFP8 && (!Wgu_scale || !Wd_scale)) return MOE_ERR_INVALID_ARG;
+  if (is_fp8(dtype) && (!Wgu_scale || !Wd_scale)) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !logits || !y || !aligned16(x) || !aligned16(y))) return MOE_ERR_INVALID_ARG;
   if (!aligned16(Wgu_packed) || !aligned16(Wd_packed)) return MOE_ERR_INVALID_ARG;
   if (dtype == MOE_F32 && d % 4 != 0) return MOE_ERR_UNSUPPORTED;
@@ -711,7 +769,7 @@ static moe_status layer_forward_impl(const void* x, const float* logits, int T, 
     e = launch_permute(x, x_dtype, dtype, T, d, w.topk_ids, w.topk_probs, k, e0, E_loc, gathers ? nullptr : w.perm_x,
                        gathers ? nullptr : w.perm_sf, w.counts, w.offsets, w.row_src_token, w.row_prob, w.pair_to_row,
                        w.perm_ws, stream, fused_combine ? w.tok_nloc : nullptr);
-  MlpScratch ms = carve_mlp(w.mlp, n_cap, f, dtype);
+  MlpScratch ms = carve_mlp(w.mlp, n_cap, f, dtype, E_loc);
   if (gathers) {
     // GEMM1 reads the token rows (quantised once per token for MXFP8)
     const bool mx = dtype == MOE_MXFP8;
@@ -723,11 +781,11 @@ static moe_status layer_forward_impl(const void* x, const float* logits, int T, 
                                  Wgu_packed, Wgu_scale, ms.h, ms.h_sf, w.err, kTimeoutNs, gu_save, stream);
   } else if (e == cudaSuccess) {
     e = run_gemm1(w.perm_x, w.perm_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, dtype, Wgu_packed, Wgu_scale, ms.h,
-                  ms.h_sf, w.err, hint, stream, gu_save);
+                  ms.h_sf, w.err, hint, stream, gu_save, ms.h16, ms.h_amax);
   }
   if (fused_combine) {
     if (e == cudaSuccess)
-      e = launch_tc_gemm2_combine(ms.h, ms.h_sf, w.offsets, n_cap, E_loc, d, f, dtype == MOE_MXFP8,
+      e = launch_tc_gemm2_combine(ms.h, ms.h_sf, w.offsets, n_cap, E_loc, d, f, is_fp8(dtype),
                                   gemm_shape(false, dtype, n_cap, E_loc, hint, f, false), Wd_packed, Wd_scale, w.Y2,
                                   w.row_src_token, w.tok_nloc, T, y, w.err, kTimeoutNs, stream);
     if (e == cudaSuccess)  // expected local slots per token: k E_loc / E

@@ -1,0 +1,77 @@
+// Per-tensor FP8 support: largest magnitude of a tensor (the scale of per-tensor current
+// scaling) and its conversion into the tensor's exponent.
+//
+// "Efficient MoE training for biological foundation models", section "MXFP8 Precision
+// Reduces Memory Footprint": the layer runs in FP8 as well as MXFP8.  Per-tensor FP8 gives
+// a whole tensor one scale; here it is a power of two, 2^X with X the smallest integer
+// such that amax <= 448 * 2^X (fp8_tensor_exponent), so the E4M3 codes of v / 2^X never
+// saturate and the block-scaled MMAs run the tensor with every block scale set to X.
+#include <algorithm>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+// amax of n_seg segments of n values each (segment s at src + s * n): blockIdx.y = segment,
+// grid-stride over 16-byte vectors, one atomicMax per block on the fp32 bits (non-negative
+// floats order like their bit patterns).  n is a multiple of 8 (bf16) or 4 (fp32).
+template <int IN_BF16>
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ src, int64_t nvec, uint32_t* amax_bits) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const uint4* s = src + static_cast<int64_t>(blockIdx.y) * nvec;
+  float m = 0.0f;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 q = __ldg(s + i);
+    if (IN_BF16) {
+      m = fmaxf(m, fmaxf(fabsf(bf16_lo(q.x)), fabsf(bf16_hi(q.x))));
+      m = fmaxf(m, fmaxf(fabsf(bf16_lo(q.y)), fabsf(bf16_hi(q.y))));
+      m = fmaxf(m, fmaxf(fabsf(bf16_lo(q.z)), fabsf(bf16_hi(q.z))));
+      m = fmaxf(m, fmaxf(fabsf(bf16_lo(q.w)), fabsf(bf16_hi(q.w))));
+    } else {
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(q.x)), fabsf(__uint_as_float(q.y))));
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(q.z)), fabsf(__uint_as_float(q.w))));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float s_m[8];
+  if ((threadIdx.x & 31) == 0) s_m[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, s_m[w]);
+    atomicMax(amax_bits + blockIdx.y, __float_as_uint(m));
+  }
+}
+
+// amax_bits[s] = largest |value| of segment s (fp32 bits), zeroed first.
+cudaError_t launch_amax(const void* src, moe_dtype dt, int64_t n_per_seg, int n_seg, uint32_t* amax_bits,
+                        cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(amax_bits, 0, static_cast<size_t>(n_seg) * 4, st);
+  if (e != cudaSuccess || n_per_seg == 0 || n_seg == 0) return e;
+  const int vpv = dt == MOE_BF16 ? 8 : 4;
+  const int64_t nvec = n_per_seg / vpv;
+  int sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = ceil_div(nvec, 256 * 8);  // ~8 vectors per thread
+  const int gx = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, std::max(1, 4 * sms / n_seg))));
+  return launch_pdl(dt == MOE_BF16 ? amax_kernel<1> : amax_kernel<0>, dim3(gx, n_seg), dim3(256), 0, st,
+                    static_cast<const uint4*>(src), nvec, amax_bits);
+}
+
+__global__ void fp8_exponents_kernel(int32_t* v, int n) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) v[i] = fp8_tensor_exponent(static_cast<uint32_t>(v[i]));
+}
+
+// In place: amax bits -> the tensors' exponents X.
+cudaError_t launch_fp8_exponents(int32_t* v, int n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(fp8_exponents_kernel, dim3(static_cast<unsigned>(ceil_div(n, 256))), dim3(256), 0, st, v, n);
+}
+
+}  // namespace moe

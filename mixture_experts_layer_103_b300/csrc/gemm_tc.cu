@@ -606,6 +606,27 @@ cudaError_t launch_tc_gemm1(const void* perm_x, const uint8_t* perm_sf, const in
   return launch_gemm_inst<false, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
 }
 
+// Per-tensor FP8 GEMM1: the block-scaled mainloop (x rows and weights in the MXFP8
+// layouts, every scale of a tensor equal) with the bf16 scaled-SwiGLU epilogue, which also
+// accumulates the largest |h| into *h_amax (fp32 bits; zeroed by the caller) for the
+// per-tensor quantisation of h that GEMM2 reads.
+cudaError_t launch_tc_gemm1_fp8(const void* perm_x, const uint8_t* perm_sf, const int32_t* offsets,
+                                const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* Wgu,
+                                const uint8_t* Wgu_sf, void* h_bf16, uint32_t* h_amax, int32_t* err,
+                                uint64_t timeout_ns, cudaStream_t st) {
+  GemmArgs g = base_args(offsets, E_loc, err, timeout_ns);
+  g.n_out = 2 * f;
+  g.K = d;
+  g.out = h_bf16;
+  g.ld_out = f;
+  g.out_rows = N_cap;
+  g.row_prob = row_prob;
+  g.a_sf = perm_sf;
+  g.b_sf = Wgu_sf;
+  g.amax = h_amax;
+  return launch_gemm_inst<true, EPI_SWIGLU_BF16>(perm_x, N_cap, Wgu, g, st);
+}
+
 // GEMM1 + fused scaled SwiGLU with A gathered from the token rows: row r of the
 // expert-ordered operand is x row row_src_token[r] (bf16 [T, d]; MXFP8: E4M3 [T, d] with
 // E8M0 scales x_sf [T, d / 32]), so no permuted copy of x is ever written.

@@ -67,6 +67,9 @@ struct GemmArgs {
   int nt_max;
   int sw_stages;
   int sw_stage_bytes;
+  // EPI_SWIGLU_BF16, per-tensor FP8 GEMM1: largest |h| of the bf16 h written (fp32 bits,
+  // atomicMax), the scale of h's quantisation for GEMM2; nullptr otherwise.
+  uint32_t* amax;
 };
 
 // TMA store maps of the bf16 outputs: 32 x 32 boxes over out [out_rows, ld_out] and out2
@@ -429,6 +432,7 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const OutMaps& 
   } else {
     const float p = r < tl.rows ? __ldg(g.row_prob + row_first + lane) : 0.0f;
     const int fdim = g.n_out / 2;
+    float hmax = 0.0f;  // largest |h| as stored (bf16), per-tensor FP8 only
 #pragma unroll 1
     for (int sb = 0; sb < BN / 64; ++sb) {
       uint32_t gv[32], uv[32];
@@ -451,6 +455,14 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const OutMaps& 
           pk[j] = make_uint4(pack_bf16x2(h[8 * j + 0], h[8 * j + 1]), pack_bf16x2(h[8 * j + 2], h[8 * j + 3]),
                              pack_bf16x2(h[8 * j + 4], h[8 * j + 5]), pack_bf16x2(h[8 * j + 6], h[8 * j + 7]));
         const int64_t ld = g.ld_out * 2;
+        if (g.amax && r < tl.rows && fc < fdim) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t w4[4] = {pk[j].x, pk[j].y, pk[j].z, pk[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) hmax = fmaxf(hmax, fmaxf(fabsf(bf16_lo(w4[e])), fabsf(bf16_hi(w4[e]))));
+          }
+        }
         if (fc < fdim)
           warp_store_block<TMA>(st, pk, lane, &om.out, fc, row_first,
                                 static_cast<uint8_t*>(g.out) + row_first * ld + static_cast<int64_t>(fc) * 2, ld,
@@ -488,6 +500,13 @@ __device__ __forceinline__ void epilogue_warp(const GemmArgs& g, const OutMaps& 
         warp_store_rows<2>(st.buf, pk, lane, static_cast<uint8_t*>(g.out) + row_first * g.ld_out + fc, g.ld_out,
                            rows_valid, fc < fdim ? 2 : 0);
         if (r < tl.rows && fc < fdim) g.out_sf[sf_act_offset(tl.mt, r, fc, fdim)] = static_cast<uint8_t>(X + 127);
+      }
+    }
+    if constexpr (EPI == EPI_SWIGLU_BF16) {
+      if (g.amax) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) hmax = fmaxf(hmax, __shfl_xor_sync(0xffffffffu, hmax, o));
+        if (lane == 0 && hmax > 0.0f) atomicMax(g.amax, __float_as_uint(hmax));
       }
     }
   }

@@ -99,6 +99,19 @@ __device__ __forceinline__ uint16_t e4m3x2(float a, float b) {
   return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
+// Per-tensor FP8 (E4M3 with one power-of-two scale per tensor): the smallest X with
+// amax <= 448 * 2^X, from the fp32 bit fields of amax (a non-negative float given as its
+// bits, the form atomicMax accumulates): amax = (1.m / 2) * 2^(b - 126) and 448 = 0.875 *
+// 2^9, so X = b - 135, plus 1 when the significand 1.m exceeds 1.75; clamped to [-127,
+// 127]; 0 for amax == 0, -127 for a subnormal amax.
+__device__ __forceinline__ int fp8_tensor_exponent(uint32_t amax_bits) {
+  if (amax_bits == 0) return 0;
+  const int b = static_cast<int>((amax_bits >> 23) & 0xFFu);
+  if (b == 0) return -127;
+  const int X = b - 135 + ((amax_bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
 // Byte offset of (row i of m-tile `tile`, K index k) in the activation SF tile layout.
 __host__ __device__ inline int64_t sf_act_offset(int64_t tile, int i, int k, int K) {
   return (tile * (K / 128) + k / 128) * 512 + (i % 32) * 16 + (i / 32) * 4 + (k % 128) / 32;

@@ -15,9 +15,12 @@
 
 namespace moe {
 
-template <typename TIn, int OUT>  // OUT: 0 = fp32, 1 = bf16, 2 = mxfp8
+// OUT: 0 = fp32, 1 = bf16, 2 = MXFP8, 3 = per-tensor FP8 (MXFP8 layout; every block of
+// expert e takes the exponent of tensor_amax[e], the amax of that expert's matrix)
+template <typename TIn, int OUT>
 __global__ void __launch_bounds__(256) pack_kernel(const TIn* __restrict__ src, int K, int ncols, int map_kind,
-                                                   int64_t rows_out, void* __restrict__ dst, uint8_t* __restrict__ dst_sf) {
+                                                   int64_t rows_out, void* __restrict__ dst, uint8_t* __restrict__ dst_sf,
+                                                   const uint32_t* __restrict__ tensor_amax) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = blockIdx.x * 32 + lane;
   const int e = blockIdx.z;
@@ -51,7 +54,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const TIn* __restrict__ src, 
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const int X = mx_exponent(amax);
+    const int X = OUT == 3 ? fp8_tensor_exponent(__ldg(tensor_amax + e)) : mx_exponent(amax);
     const float inv = mx_inv_scale(X);
     uint32_t w[8];
 #pragma unroll
@@ -67,9 +70,10 @@ __global__ void __launch_bounds__(256) pack_kernel(const TIn* __restrict__ src, 
 
 template <typename TIn, int OUT>
 static void pack_one(const void* src, int E_loc, int K, int ncols, int map_kind, int64_t rows_out, void* dst,
-                     uint8_t* sf, cudaStream_t st) {
+                     uint8_t* sf, cudaStream_t st, const uint32_t* tensor_amax = nullptr) {
   const dim3 grid(static_cast<unsigned>(ceil_div(ncols, 32)), static_cast<unsigned>(ceil_div(K, 256)), E_loc);
-  pack_kernel<TIn, OUT><<<grid, 256, 0, st>>>(static_cast<const TIn*>(src), K, ncols, map_kind, rows_out, dst, sf);
+  pack_kernel<TIn, OUT><<<grid, 256, 0, st>>>(static_cast<const TIn*>(src), K, ncols, map_kind, rows_out, dst, sf,
+                                              tensor_amax);
 }
 
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
@@ -87,6 +91,38 @@ cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dty
   else MOE_PACK3(float, 2);
 #undef MOE_PACK3
   return cudaGetLastError();
+}
+
+cudaError_t launch_amax(const void* src, moe_dtype dt, int64_t n_per_seg, int n_seg, uint32_t* amax_bits,
+                        cudaStream_t st);
+cudaError_t launch_fp8_exponents(int32_t* v, int n, cudaStream_t st);
+
+// Per-tensor FP8 packing: w_exp [3, E_loc] receives the amax of each expert's W_gate, W_up
+// and W_down (first pass), the matrices are quantised with their exponent into the MXFP8
+// packed layouts (every scale byte of a matrix the same), and w_exp is turned into the
+// exponents X in place.
+cudaError_t launch_pack_fp8(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, int E_loc, int d, int f,
+                            void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, int32_t* w_exp,
+                            cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(d) * f;
+  uint32_t* amax = reinterpret_cast<uint32_t*>(w_exp);
+  cudaError_t e = launch_amax(Wg, src, n, E_loc, amax, st);
+  if (e == cudaSuccess) e = launch_amax(Wu, src, n, E_loc, amax + E_loc, st);
+  if (e == cudaSuccess) e = launch_amax(Wdn, src, n, E_loc, amax + 2 * E_loc, st);
+  if (e != cudaSuccess) return e;
+  const int64_t gu_rows = 2LL * f;
+  if (src == MOE_BF16) {
+    pack_one<uint16_t, 3>(Wg, E_loc, d, f, 1, gu_rows, Wgu_p, Wgu_sf, st, amax);
+    pack_one<uint16_t, 3>(Wu, E_loc, d, f, 2, gu_rows, Wgu_p, Wgu_sf, st, amax + E_loc);
+    pack_one<uint16_t, 3>(Wdn, E_loc, f, d, 0, d, Wd_p, Wd_sf, st, amax + 2 * E_loc);
+  } else {
+    pack_one<float, 3>(Wg, E_loc, d, f, 1, gu_rows, Wgu_p, Wgu_sf, st, amax);
+    pack_one<float, 3>(Wu, E_loc, d, f, 2, gu_rows, Wgu_p, Wgu_sf, st, amax + E_loc);
+    pack_one<float, 3>(Wdn, E_loc, f, d, 0, d, Wd_p, Wd_sf, st, amax + 2 * E_loc);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_fp8_exponents(w_exp, 3 * E_loc, st);
 }
 
 }  // namespace moe

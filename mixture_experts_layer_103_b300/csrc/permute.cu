@@ -21,6 +21,9 @@
 
 namespace moe {
 
+cudaError_t launch_amax(const void* src, moe_dtype dt, int64_t n_per_seg, int n_seg, uint32_t* amax_bits,
+                        cudaStream_t st);
+
 int num_sms();
 
 // Tokens per tile of the count and scatter kernels: 64 while the (expert, tile) count
@@ -224,9 +227,13 @@ struct MxRow {
   static constexpr int U = IN_BF16 ? 4 : 8;    // 16-byte loads in flight per lane
   static constexpr int SLICE = 32 * U;         // vectors one warp pass covers
 };
+// tensor_amax (per-tensor FP8): when set, every block uses the one exponent of the whole
+// tensor (fp8_tensor_exponent of the tensor's amax) instead of its own.
 template <int IN_BF16, typename PutSf>
 __device__ __forceinline__ void quantize_row_mx(const uint4* __restrict__ src, int v0, int v1, int lane,
-                                                uint8_t* __restrict__ dst, PutSf put_sf) {
+                                                uint8_t* __restrict__ dst, PutSf put_sf,
+                                                const uint32_t* __restrict__ tensor_amax = nullptr) {
+  const int Xt = tensor_amax ? fp8_tensor_exponent(__ldg(tensor_amax)) : 0;
   constexpr int VPV = MxRow<IN_BF16>::VPV;
   constexpr int LPB = 32 / VPV;  // lanes per 32-value block
   constexpr int U = MxRow<IN_BF16>::U;
@@ -255,7 +262,7 @@ __device__ __forceinline__ void quantize_row_mx(const uint4* __restrict__ src, i
       for (int e = 0; e < VPV; ++e) amax = fmaxf(amax, fabsf(v[e]));
 #pragma unroll
       for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const int X = mx_exponent(amax);
+      const int X = tensor_amax ? Xt : mx_exponent(amax);
       const float inv = mx_inv_scale(X);
       if (act) {
         if (IN_BF16) {
@@ -279,20 +286,26 @@ __device__ __forceinline__ void quantize_row_mx(const uint4* __restrict__ src, i
 // Row copy with MXFP8 quantisation into the permuted order (scales in the activation SF
 // tile layout of the expert m-tiles).  Work items are (row, slice of MxRow::SLICE vectors),
 // so short permutations still spread over every SM.  row_src_token == nullptr: the source
-// rows are already in routed order (row r from source row r).
+// rows are already in routed order (row r from source row r).  mtile_base == nullptr: the
+// m-tile table is built from offsets.  tensor_amax: per-tensor FP8 (one exponent for all).
 template <int IN_BF16>
 __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __restrict__ x, int d,
                                                              const int32_t* __restrict__ offsets, int E_loc,
                                                              const int32_t* __restrict__ mtile_base,
                                                              const int32_t* __restrict__ row_src_token,
-                                                             uint8_t* __restrict__ perm_x, uint8_t* __restrict__ perm_sf) {
+                                                             uint8_t* __restrict__ perm_x, uint8_t* __restrict__ perm_sf,
+                                                             const uint32_t* __restrict__ tensor_amax) {
   pdl_launch_dependents();
   pdl_wait();
   constexpr int VPV = IN_BF16 ? 8 : 4;
   extern __shared__ int32_t s_tab[];    // offsets [E_loc+1], mtile_base [E_loc+1]
-  for (int i = threadIdx.x; i <= E_loc; i += blockDim.x) {
-    s_tab[i] = offsets[i];
-    s_tab[E_loc + 1 + i] = mtile_base[i];
+  if (mtile_base) {
+    for (int i = threadIdx.x; i <= E_loc; i += blockDim.x) {
+      s_tab[i] = offsets[i];
+      s_tab[E_loc + 1 + i] = mtile_base[i];
+    }
+  } else if (threadIdx.x < 32) {  // no table given: the 128-row m-tile prefix from offsets
+    build_mtile_prefix(offsets, E_loc, 128, s_tab, s_tab + E_loc + 1);
   }
   __syncthreads();
   const int lane = threadIdx.x & 31;
@@ -318,7 +331,7 @@ __global__ void __launch_bounds__(256) perm_gather_mx_kernel(const uint4* __rest
     const int i = il % 128;
     const int64_t t = row_src_token ? __ldg(row_src_token + r) : r;
     quantize_row_mx<IN_BF16>(x + t * row_vecs, sl * SL, min(row_vecs, (sl + 1) * SL), lane, perm_x + r * d,
-                             [&](int col, uint8_t b) { perm_sf[sf_act_offset(tile, i, col, d)] = b; });
+                             [&](int col, uint8_t b) { perm_sf[sf_act_offset(tile, i, col, d)] = b; }, tensor_amax);
   }
 }
 
@@ -358,11 +371,12 @@ cudaError_t launch_quant_rows_mx(const void* x, moe_dtype x_dtype, int T, int d,
 struct PermuteWs {
   int32_t* tile_counts;  // [E_loc][n_tiles]
   int32_t* mtile_base;   // [E_loc + 1]
+  uint32_t* x_amax;      // per-tensor FP8: largest |x| (fp32 bits)
 };
 
 size_t permute_ws_bytes(int T, int E_loc) {
   const int64_t n_tiles = ceil_div(T > 0 ? T : 1, perm_tile(T, E_loc));
-  return align_up(static_cast<size_t>(n_tiles) * E_loc * 4, kAlign) + align_up((E_loc + 1) * 4, kAlign);
+  return align_up(static_cast<size_t>(n_tiles) * E_loc * 4, kAlign) + align_up((E_loc + 1) * 4, kAlign) + kAlign;
 }
 
 static PermuteWs carve_permute_ws(uint8_t* base, int T, int E_loc) {
@@ -370,6 +384,8 @@ static PermuteWs carve_permute_ws(uint8_t* base, int T, int E_loc) {
   PermuteWs w;
   w.tile_counts = reinterpret_cast<int32_t*>(base);
   w.mtile_base = reinterpret_cast<int32_t*>(base + align_up(static_cast<size_t>(n_tiles) * E_loc * 4, kAlign));
+  w.x_amax = reinterpret_cast<uint32_t*>(base + align_up(static_cast<size_t>(n_tiles) * E_loc * 4, kAlign) +
+                                         align_up((E_loc + 1) * 4, kAlign));
   return w;
 }
 
@@ -384,10 +400,10 @@ int gather_grid(cudaStream_t st);
 // (mtile_base from the permute).  K % 128 == 0.
 cudaError_t launch_gather_rows_mx(const void* src, int K, const int32_t* offsets, int E_loc,
                                   const int32_t* mtile_base, const int32_t* row_src_token, uint8_t* dst,
-                                  uint8_t* dst_sf, cudaStream_t st) {
+                                  uint8_t* dst_sf, cudaStream_t st, const uint32_t* tensor_amax) {
   const size_t sm = static_cast<size_t>(2 * (E_loc + 1)) * 4;
   return launch_pdl(perm_gather_mx_kernel<1>, dim3(gather_grid(st)), dim3(256), sm, st, static_cast<const uint4*>(src),
-                    K, offsets, E_loc, mtile_base, row_src_token, dst, dst_sf);
+                    K, offsets, E_loc, mtile_base, row_src_token, dst, dst_sf, tensor_amax);
 }
 
 // Rows of src (row_bytes each, a multiple of 16) into routed order: dst row r = src row
@@ -429,12 +445,16 @@ cudaError_t launch_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_dtyp
     const int grid = gather_grid(st);
     if (perm_x == nullptr) {
       // maps only: the row-gather GEMM reads x through row_src_token
-    } else if (perm_dtype == MOE_MXFP8) {
+    } else if (perm_dtype == MOE_MXFP8 || perm_dtype == MOE_FP8) {
+      // per-tensor FP8: one exponent for the whole of x [T, d], from its largest magnitude
+      if (perm_dtype == MOE_FP8) e = launch_amax(x, x_dtype, static_cast<int64_t>(T) * d, 1, w.x_amax, st);
+      if (e != cudaSuccess) return e;
       const size_t sm = static_cast<size_t>(2 * (E_loc + 1)) * 4;
       e = launch_pdl(x_dtype == MOE_BF16 ? perm_gather_mx_kernel<1> : perm_gather_mx_kernel<0>, dim3(grid), dim3(256),
                      sm, st, static_cast<const uint4*>(x), d, static_cast<const int32_t*>(offsets), E_loc,
                      static_cast<const int32_t*>(w.mtile_base), static_cast<const int32_t*>(row_src_token),
-                     static_cast<uint8_t*>(perm_x), perm_sf);
+                     static_cast<uint8_t*>(perm_x), perm_sf,
+                     perm_dtype == MOE_FP8 ? static_cast<const uint32_t*>(w.x_amax) : nullptr);
     } else {
       const int64_t row_vecs = static_cast<int64_t>(d) * (x_dtype == MOE_F32 ? 4 : 2) / 16;
       e = launch_pdl(perm_gather_copy_kernel, dim3(grid), dim3(256), 0, st, static_cast<const uint4*>(x), row_vecs,

@@ -52,7 +52,7 @@ class Workload:
     k: int
     e0: int
     E_loc: int
-    dtype: str  # "f32" | "bf16" | "mxfp8"  (mxfp8: inputs drawn as bf16, quantised by the layer)
+    dtype: str  # "f32" | "bf16" | "mxfp8" | "fp8"  (mxfp8 / fp8: inputs drawn as bf16, quantised by the layer)
     bias: tuple = ()  # () | ("normal", var) | ("zipf", s)
     seed: int = 0
 
@@ -80,6 +80,8 @@ WORKLOADS = {
     "mxfp8_ep8_zipf_T8192": Workload("mxfp8_ep8_zipf_T8192", 8192, 7168, 2048, 256, 8, 0, 32, "mxfp8", ("zipf", 1.1)),
     # MXFP8 variant of the EP64 slice at T=8192.
     "mxfp8_ep64_T8192": Workload("mxfp8_ep64_T8192", 8192, 7168, 2048, 256, 8, 0, 4, "mxfp8"),
+    # the same slice with per-tensor FP8 (one power-of-two scale per tensor)
+    "fp8_ep64_T8192": Workload("fp8_ep64_T8192", 8192, 7168, 2048, 256, 8, 0, 4, "fp8"),
     # One expert holding every token (E = 1, top-1) at the slices' d and f: the grouped GEMMs
     # without ragged segments, i.e. the dense tensor-core rate of the same kernels.
     "dense_bf16_T16384": Workload("dense_bf16_T16384", 16384, 7168, 2048, 1, 1, 0, 1, "bf16"),

@@ -144,6 +144,8 @@ def test_pack_parity(moe, dtype, E_loc, d, f):
 
 # ----------------------------------------------------------------------------- layer
 def oracle_layer(w: Workload, x, lg, Wg, Wu, Wd, tokens=None):
+    if w.dtype == "fp8":
+        return oracle.moe_forward_fp8(x, lg, w.k, w.e0, w.E_loc, Wg, Wu, Wd, tokens=tokens)
     if w.dtype == "mxfp8":
         cg, sg = oracle.mx_quantize(Wg, "bf16", (w.E_loc, w.d, w.f))
         cu, su = oracle.mx_quantize(Wu, "bf16", (w.E_loc, w.d, w.f))
@@ -382,7 +384,7 @@ def test_canaries_untouched(moe, dtype):
 
 # ----------------------------------------------------------------------------- full size
 FULL = ["tiny_fp32", "bf16_e64", "ep8_zipf_T512", "ep64_T2048", "ep64_T8192", "ep64_T32768",
-        "mxfp8_ep8_zipf_T8192", "mxfp8_ep64_T8192", "dense_bf16_T16384", "dense_mxfp8_T16384"]
+        "mxfp8_ep8_zipf_T8192", "mxfp8_ep64_T8192", "fp8_ep64_T8192", "dense_bf16_T16384", "dense_mxfp8_T16384"]
 
 
 @pytest.mark.parametrize("name", FULL)
