@@ -580,7 +580,9 @@ def e2e_leg(moe, args, w, xd, lgd, y, pw, flush, world):
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
-    n2 = args.e2e_steps or max(3, args.steps // 4)
+    # as many steps as the device-timed region (at least 10): the pipeline's first copy in
+    # and last copy out are not overlapped, so few steps would mostly time its fill
+    n2 = args.e2e_steps or max(10, args.steps)
     # the n2 steps (copies, layer calls, event dependencies on three streams) are captured
     # once as a CUDA graph and replayed inside the timed region, like the device-only steps
     ge = torch.cuda.CUDAGraph()
