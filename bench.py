@@ -341,10 +341,10 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
     ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
     probs = torch.empty(T, k, dtype=torch.float32, device="cuda")
     hint = args.rows_hint if args.rows_hint is not None else moe.moe_rows_hint(T, k, w.E)
-    # the library's own choice in moe_layer_forward: row gather for bf16 unless GEMM1 runs on
-    # CTA pairs
-    pairs1 = moe.moe_layer_gemm1_pairs(T, d, k, w.E, E_loc, w.dtype) if args.rows_hint is None else (
-        w.dtype == "bf16" and (hint >= 2048 or (256 <= hint < 1024 and d >= 4096)))
+    # the library's own kernel choice per GEMM (a forced rows_hint names its kernel directly)
+    forced = {-1: "cta", -2: "pair", -3: "swap"}
+    kinds = {g: (forced.get(args.rows_hint, "cta") if args.rows_hint is not None and args.rows_hint < 0 else
+                 moe.moe_layer_gemm_kernel(T, d, w.f, k, w.E, E_loc, w.dtype, g)) for g in (1, 2)}
     gather = not args.no_gather and w.dtype == "bf16"
     mx = w.dtype == "mxfp8"
     P = moe.alloc_permute(T, d, k, E_loc, xd.dtype, w.dtype, maps_only=gather)
@@ -509,7 +509,8 @@ def measure(moe, args, w, pk, pk_kind, rank, world, local, headline: bool):
         roof = {"bound": "hbm", "achieved": by / t_s / 1e9, "peak": hbm, "unit": "GB/s",
                 "frac": by / t_s / 1e9 / hbm}
     kname = ("simt_grouped_gemm_kernel" if w.dtype == "f32" else
-             "tc_grouped_gemm_pair_kernel" if pairs1 else "tc_grouped_gemm_kernel")
+             {"cta": "tc_grouped_gemm_kernel", "pair": "tc_grouped_gemm_pair_kernel",
+              "swap": "tc_swap_gemm_kernel"}[kinds[1 if dom == "gemm1_swiglu" else 2]])
     roof.update({"kernel": f"{kname} ({dom})", "traffic": recorded_traffic(dom, w.name),
                  "peak_kind": pk_kind + (" (bf16 x2 nominal fp8 ratio)" if w.dtype in ("mxfp8", "fp8") else "")})
     t_roof = max(bf["layer_flops"] / (tpeak * 1e12), bf["layer_bytes"] / (hbm * 1e9))
