@@ -609,7 +609,27 @@ def e2e_leg(moe, args, w, xd, lgd, y, pw, flush, world):
     assert moe.moe_get_device_error(ws_layer) == 0
     ms = a.elapsed_time(b) / n2
     x_pin_bytes = x_pin.numel() * x_pin.element_size()
+
+    # the copies alone (same buffers, 5 each, after the timed region): the host link's
+    # rates, which bound the end-to-end step from below
+    def copy_ms(fn):
+        e0_, e1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize()
+        e0_.record()
+        for _ in range(5):
+            fn()
+        e1_.record()
+        torch.cuda.synchronize()
+        return e0_.elapsed_time(e1_) / 5
+
+    h2d_bytes = x_pin_bytes + lg_pin.numel() * 4
+    d2h_bytes = y_pin[0].numel() * y_pin[0].element_size()
+    h2d_ms = copy_ms(lambda: (xb[0].copy_(x_pin, non_blocking=True), lgb[0].copy_(lg_pin, non_blocking=True)))
+    d2h_ms = copy_ms(lambda: y_pin[0].copy_(yb[0], non_blocking=True))
     return {"value": T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_gbs": h2d_bytes / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h_bytes / (d2h_ms / 1e3) / 1e9,
+            "copy_bound_ms_per_step": max(h2d_ms, d2h_ms),
             "h2d_bytes_per_step": int(x_pin_bytes + lg_pin.numel() * 4),
             "d2h_bytes_per_step": int(y_pin[0].numel() * y_pin[0].element_size()), "steps": n2,
             "entry_point": "moe_layer_forward",
