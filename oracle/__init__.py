@@ -11,8 +11,8 @@ imports the CUDA library.
   oracle on tiny inputs, and the MXFP8 backward token by token.
 * ``moe_backward_mx`` (numpy over the C++ codec): the MXFP8 layer backward, every backward
   GEMM operand quantised along that GEMM's contraction axis.
-* ``moe_forward_fp8`` (numpy over the C++ codec): the per-tensor FP8 layer (one
-  power-of-two scale per tensor).
+* ``moe_forward_fp8``, ``moe_backward_fp8`` (numpy over the C++ codec): the per-tensor FP8
+  layer and its backward (one power-of-two scale per tensor).
 
 Functions of this module are thin ctypes marshalling around the C++ oracle.
 """
@@ -366,3 +366,69 @@ def moe_forward_fp8(x, logits, k: int, e0: int, E_loc: int, W_gate, W_up, W_down
         m = r >= 0
         y[m] += Y2[r[m]]
     return y if tokens is None else y[np.asarray(tokens, np.int64)]
+
+
+def moe_backward_fp8(x, logits, dy, k: int, e0: int, E_loc: int, W_gate, W_up, W_down) -> dict:
+    """fp64 gradients of L = sum(dy * y) for the per-tensor FP8 layer (bf16 bits in: x, dy
+    [T, d]; W_gate, W_up [E_loc, d, f]; W_down [E_loc, f, d]; logits [T, E] fp32).
+
+    Every GEMM operand is one per-tensor FP8 tensor (``fp8_tensor_quantize``), the same
+    whichever axis a GEMM contracts: x and dy as wholes; each expert's W_gate, W_up and
+    W_down; h over all local routed rows; and the gradient of the gate/up pre-activation
+    [dg du] over all local routed rows (one tensor, the input gradient of the first grouped
+    linear).  The forward g, u, h are recomputed from the quantised x and weights.  Then,
+    with Q the per-tensor quantisation:
+      dh = Q(dy) Q(W_down)^T,  du = p dh silu(g),  dg = p dh u s (1 + g (1 - s)),
+      dp = sum dh silu(g) u,   dx_row = Q(dg) Q(W_gate)^T + Q(du) Q(W_up)^T,
+      dW_down = Q(h)^T Q(dy),  dW_gate = Q(x)^T Q(dg),  dW_up = Q(x)^T Q(du)  (per expert)
+    and the router gradient as for the MXFP8 backward.
+    Returns dict(dx [T, d], dlogits [T, E], dW_gate, dW_up [E_loc, d, f], dW_down [E_loc, f, d]).
+    """
+    xv, dyv = _bf16_values(x), _bf16_values(dy)
+    Wg, Wu, Wd = (_bf16_values(w) for w in (W_gate, W_up, W_down))
+    lg = np.asarray(logits, np.float32)
+    T, d = xv.shape
+    E = lg.shape[1]
+    f = Wg.shape[2]
+    ids, probs = route_topk(lg, k)
+    P = permute(ids, e0, E_loc)
+    off, rst, slot = P["offsets"], P["row_src_token"], P["row_slot"]
+    N = int(off[-1])
+    xq, dyq = fp8_tensor_dequantized(xv), fp8_tensor_dequantized(dyv)
+    Wgq = [fp8_tensor_dequantized(Wg[e]) for e in range(E_loc)]
+    Wuq = [fp8_tensor_dequantized(Wu[e]) for e in range(E_loc)]
+    Wdq = [fp8_tensor_dequantized(Wd[e]) for e in range(E_loc)]
+    h, dg, du = np.zeros((N, f)), np.zeros((N, f)), np.zeros((N, f))
+    dp = np.zeros((T, k))
+    for e in range(E_loc):
+        rows = slice(int(off[e]), int(off[e + 1]))
+        t, j = rst[rows].astype(np.int64), slot[rows].astype(np.int64)
+        if t.size == 0:
+            continue
+        p = probs[t, j][:, None]
+        g, u = xq[t] @ Wgq[e], xq[t] @ Wuq[e]
+        s = 1.0 / (1.0 + np.exp(-g))
+        a = g * s
+        h[rows] = p * a * u
+        dh = dyq[t] @ Wdq[e].T
+        du[rows] = p * dh * a
+        dg[rows] = p * dh * u * s * (1.0 + g * (1.0 - s))
+        dp[t, j] = (dh * a * u).sum(axis=1)
+    hq = fp8_tensor_dequantized(h)
+    dgu = fp8_tensor_dequantized(np.concatenate([dg, du], axis=1)) if N else np.zeros((0, 2 * f))
+    dgq, duq = dgu[:, :f], dgu[:, f:]
+    dx = np.zeros((T, d))
+    dWg, dWu, dWd = np.zeros((E_loc, d, f)), np.zeros((E_loc, d, f)), np.zeros((E_loc, f, d))
+    for e in range(E_loc):
+        rows = slice(int(off[e]), int(off[e + 1]))
+        t = rst[rows].astype(np.int64)
+        if t.size == 0:
+            continue
+        np.add.at(dx, t, dgq[rows] @ Wgq[e].T + duq[rows] @ Wuq[e].T)
+        dWd[e] = hq[rows].T @ dyq[t]
+        dWg[e] = xq[t].T @ dgq[rows]
+        dWu[e] = xq[t].T @ duq[rows]
+    dl = np.zeros((T, E))
+    mix = (probs * dp).sum(axis=1, keepdims=True)
+    np.add.at(dl, (np.arange(T)[:, None].repeat(k, 1), ids), probs * (dp - mix))
+    return dict(dx=dx, dlogits=dl, dW_gate=dWg, dW_up=dWu, dW_down=dWd)

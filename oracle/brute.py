@@ -218,3 +218,50 @@ def backward_mx(x, logits, dy, Wg, Wu, Wd, k: int, e0: int):
         for j in range(k):
             dlog[t, ids[j]] += p[j] * (dp[t, j] - mix)
     return dict(dx=dx, dlogits=dlog, dW_gate=dWg, dW_up=dWu, dW_down=dWd)
+
+
+def backward_fp8(x, logits, dy, Wg, Wu, Wd, k: int, e0: int):
+    """Gradients of sum(dy * y) for the per-tensor FP8 layer, token by token (fp64 values
+    in): x, dy, each expert matrix, h and [dg du] (every local routed row of the batch) are
+    one FP8 tensor each; experts visited by a scan over tokens, no permutation tables."""
+    x, dy = np.asarray(x, np.float64), np.asarray(dy, np.float64)
+    T, d = x.shape
+    E_loc, _, f = Wg.shape
+    E = logits.shape[1]
+    xq, dyq = fp8_tensor_quantize(x)[2], fp8_tensor_quantize(dy)[2]
+    Wgq = [fp8_tensor_quantize(Wg[e])[2] for e in range(E_loc)]
+    Wuq = [fp8_tensor_quantize(Wu[e])[2] for e in range(E_loc)]
+    Wdq = [fp8_tensor_quantize(Wd[e])[2] for e in range(E_loc)]
+    route = [topk(logits[t], k) for t in range(T)]
+    rows = []  # (token, slot, expert, h, dg, du) in expert order, ascending tokens
+    dp = np.zeros((T, k))
+    for e in range(E_loc):
+        for t in range(T):
+            ids, p = route[t]
+            for j in range(k):
+                if ids[j] - e0 != e:
+                    continue
+                g, u = xq[t] @ Wgq[e], xq[t] @ Wuq[e]
+                s = 1.0 / (1.0 + np.exp(-g))
+                dh = Wdq[e] @ dyq[t]
+                dp[t, j] = np.sum(dh * g * s * u)
+                rows.append((t, j, e, p[j] * g * s * u, p[j] * dh * u * s * (1.0 + g * (1.0 - s)), p[j] * dh * g * s))
+    dx = np.zeros((T, d))
+    dWg, dWu, dWd = np.zeros((E_loc, d, f)), np.zeros((E_loc, d, f)), np.zeros((E_loc, f, d))
+    if rows:
+        hq = fp8_tensor_quantize(np.stack([r[3] for r in rows]))[2]
+        dgu = fp8_tensor_quantize(np.stack([np.concatenate([r[4], r[5]]) for r in rows]))[2]
+        for (t, j, e, _, _, _), hr, gr in zip(rows, hq, dgu):
+            dgq, duq = gr[:f], gr[f:]
+            dx[t] += Wgq[e] @ dgq + Wuq[e] @ duq
+            dWd[e] += np.outer(hr, dyq[t])
+            dWg[e] += np.outer(xq[t], dgq)
+            dWu[e] += np.outer(xq[t], duq)
+    dl = np.zeros((T, E))
+    for t in range(T):
+        ids, p = route[t]
+        mix = np.sum(p * dp[t])
+        for j in range(k):
+            dl[t, ids[j]] += p[j] * (dp[t, j] - mix)
+    return dict(dx=dx, dlogits=dl, dW_gate=dWg, dW_up=dWu, dW_down=dWd)
+

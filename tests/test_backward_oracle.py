@@ -115,3 +115,38 @@ def test_mx_backward_near_unquantised(w):
     for key in ("dx", "dlogits", "dW_gate", "dW_up", "dW_down"):
         err = np.linalg.norm(got[key] - ref[key]) / np.linalg.norm(ref[key])
         assert 0.01 <= err <= 0.15, (key, err)
+
+
+FP8_BWD = [
+    Workload("fp8_bwd_slice", 40, 64, 32, 8, 2, 2, 4, "fp8"),                     # non-local slots
+    Workload("fp8_bwd_skew", 70, 96, 64, 6, 3, 0, 6, "fp8", ("normal", 0.5)),     # ragged segments
+]
+
+
+@pytest.mark.parametrize("w", FP8_BWD, ids=[w.name for w in FP8_BWD])
+def test_fp8_backward_matches_brute_force(w):
+    """oracle.moe_backward_fp8 (vectorised over the permutation, C++ codec) against
+    brute.backward_fp8 (token by token, nearest-code quantiser, exponent by search): a
+    tensor quantised per expert or per row instead of as a whole, [dg du] split into two
+    tensors, or h left unquantised fails it."""
+    x, lg, dy = gen_x(w), gen_logits(w), gen_dy(w)
+    Wg, Wu, Wd = gen_weights(w)
+    got = oracle.moe_backward_fp8(x, lg, dy, w.k, w.e0, w.E_loc, Wg, Wu, Wd)
+    v = lambda a: bf16_to_f32(a).astype(np.float64)
+    ref = brute.backward_fp8(v(x), lg, v(dy), v(Wg), v(Wu), v(Wd), w.k, w.e0)
+    for key in ref:
+        err = np.linalg.norm(got[key] - ref[key]) / np.linalg.norm(ref[key])
+        assert err <= 1e-12, (key, err)
+
+
+@pytest.mark.parametrize("w", FP8_BWD, ids=[w.name for w in FP8_BWD])
+def test_fp8_backward_near_unquantised(w):
+    """Same gradients as the bf16 backward up to the E4M3 rounding of the GEMM operands:
+    relative L2 between 1 % and 15 %."""
+    x, lg, dy = gen_x(w), gen_logits(w), gen_dy(w)
+    Wg, Wu, Wd = gen_weights(w)
+    got = oracle.moe_backward_fp8(x, lg, dy, w.k, w.e0, w.E_loc, Wg, Wu, Wd)
+    ref = oracle.moe_backward(x, "bf16", lg, dy, "bf16", w.k, w.e0, w.E_loc, "bf16", Wg, Wu, Wd)
+    for key in ("dx", "dlogits", "dW_gate", "dW_up", "dW_down"):
+        err = np.linalg.norm(got[key] - ref[key]) / np.linalg.norm(ref[key])
+        assert 0.01 <= err <= 0.15, (key, err)
