@@ -703,9 +703,9 @@ def run_backward(args, w):
     import torch
     import torch.distributed as dist
 
-    if w.dtype not in ("bf16", "mxfp8"):
-        raise SystemExit("the backward is bf16 or MXFP8")
-    mx = w.dtype == "mxfp8"
+    if w.dtype not in ("bf16", "mxfp8", "fp8"):
+        raise SystemExit("the backward is bf16, MXFP8 or per-tensor FP8")
+    mx = w.dtype in ("mxfp8", "fp8")
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     if world > 1:
@@ -719,8 +719,8 @@ def run_backward(args, w):
     Wg, Wu, Wd = (to_dev(a) for a in gen_weights(w))
     if mx:
         # MXFP8: g, u recomputed on the block-scaled tensor cores inside the backward
-        pw = moe.moe_pack_weights(Wg, Wu, Wd, "mxfp8")
-        bw = moe.moe_pack_weights_backward_mx(Wg, Wu, Wd)
+        pw = moe.moe_pack_weights(Wg, Wu, Wd, w.dtype)
+        bw = moe.moe_pack_weights_backward_mx(Wg, Wu, Wd, w_exp=pw.w_exp)
         del Wg, Wu, Wd
         ids, probs = moe.moe_route_topk(lgd, w.k)
 
@@ -776,13 +776,14 @@ def run_backward(args, w):
     line = {
         "metric": "MoE-layer backward tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+e8m0 (mxfp8)" if mx else "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"mxfp8": "e4m3+e8m0 (mxfp8)", "fp8": "e4m3, one power-of-two scale per tensor (fp8)"}.get(w.dtype, "bf16"),
         "data": "synthetic (seeded)",
         "config": workload_config(w), "pass": "backward",
         "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
                      "kernel": "whole backward (12 N d f FLOP)", "traffic": None, "peak_kind": pk_kind},
-        "N_pairs": N, "gpu_launches": (19 if mx else 11) * args.steps, "clocks": clk,
+        "N_pairs": N, "gpu_launches": ({"mxfp8": 19, "fp8": 23}.get(w.dtype, 11)) * args.steps, "clocks": clk,
         "per_kernel_floor": {"roofline_us": floor_s * 1e6, "measured_us": ms * 1e3, "frac": floor_s / (ms * 1e-3),
                              "terms_us": {k: v * 1e6 for k, v in floor_terms.items()},
                              "note": "sum over the backward's kernels of max(FLOPs / bf16 peak, bytes / HBM)"},

@@ -478,6 +478,30 @@ moe_status moe_pack_weights_backward_mx(const void* W_gate, const void* W_up, co
                                         int E_loc, int d, int f, uint8_t* WguT_q, uint8_t* WguT_scale, uint8_t* Wd_q,
                                         uint8_t* Wd_scale, moe_stream_t stream);
 
+/* Per-tensor FP8 layer backward ["Efficient MoE training ...", "MXFP8 Precision Reduces
+ * Memory Footprint": the layer trains in FP8 as well as MXFP8].  Same arguments, outputs
+ * and workspace as moe_layer_backward_mx, with the weights packed by moe_pack_weights_fp8
+ * (forward) and moe_pack_weights_backward_fp8 (backward layouts).  Every GEMM operand is
+ * one E4M3 tensor with one power-of-two scale (the rule of moe_pack_weights_fp8): x and dy
+ * as wholes (an amax pass over each), each expert weight matrix, h and the gradient of the
+ * gate/up pre-activation [dg du] over the local routed rows; axis-independent, so the
+ * weight gradients read the same values as the row-wise GEMMs (quantised and dequantised
+ * in place, exact in bf16).  moe_layer_backward_fp8_workspace_size equals the MXFP8 one. */
+moe_status moe_layer_backward_fp8(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs,
+                                  int T, int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
+                                  const uint8_t* Wgu_scale, const uint8_t* Wd_q, const uint8_t* Wd_scale,
+                                  const uint8_t* WguT_q, const uint8_t* WguT_scale, void* dx, float* dlogits,
+                                  float* dW_gate, float* dW_up, float* dW_down, void* workspace,
+                                  size_t workspace_bytes, moe_stream_t stream);
+size_t moe_layer_backward_fp8_workspace_size(int T, int d, int f, int k, int E_loc);
+/* The backward weight layouts of moe_pack_weights_backward_mx for per-tensor FP8: each
+ * matrix quantised with its exponent from w_exp [3][E_loc] (moe_pack_weights_fp8's output:
+ * W_gate, W_up, W_down per expert), every scale byte of a matrix that exponent + 127. */
+moe_status moe_pack_weights_backward_fp8(const void* W_gate, const void* W_up, const void* W_down,
+                                         moe_dtype src_dtype, int E_loc, int d, int f, const int32_t* w_exp,
+                                         uint8_t* WguT_q, uint8_t* WguT_scale, uint8_t* Wd_q, uint8_t* Wd_scale,
+                                         moe_stream_t stream);
+
 /* Expert placement and replication plan (host function, no GPU) ["Wide-EP ... MoE ...
  * NVIDIA" explainer, "Load imbalance: EPLB": per-expert load decides placement, and the
  * most loaded experts get copies on several GPUs].  The page gives no algorithm; this is

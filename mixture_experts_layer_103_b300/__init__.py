@@ -76,9 +76,13 @@ _SIGS = {
     "moe_layer_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_pack_weights_backward": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_pack_weights_backward_mx": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_pack_weights_backward_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_layer_backward_mx": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _P, _P, _SZ, _P]),
+    "moe_layer_backward_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _P, _SZ, _P]),
     "moe_layer_backward_mx_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_layer_backward_fp8_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_expert_gemm2": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_gemm_workspace_size": (_SZ, []),
     "moe_unpermute_combine": (_I, [_P, _P, _I, _I, _I, _I, _P, _P]),
@@ -445,7 +449,10 @@ class BackwardWeightsMx:
     WguT_scale: torch.Tensor
 
 
-def moe_pack_weights_backward_mx(W_gate: torch.Tensor, W_up: torch.Tensor, W_down: torch.Tensor) -> BackwardWeightsMx:
+def moe_pack_weights_backward_mx(W_gate: torch.Tensor, W_up: torch.Tensor, W_down: torch.Tensor,
+                                 w_exp: torch.Tensor | None = None) -> BackwardWeightsMx:
+    """Backward weight layouts; with w_exp (PackedWeights.w_exp of a per-tensor FP8 pack)
+    the per-tensor FP8 ones (moe_pack_weights_backward_fp8)."""
     E_loc, d, f = W_gate.shape
     dev = W_gate.device
     src = MOE_F32 if W_gate.dtype == torch.float32 else MOE_BF16
@@ -454,6 +461,11 @@ def moe_pack_weights_backward_mx(W_gate: torch.Tensor, W_up: torch.Tensor, W_dow
         Wd_scale=torch.empty(_lib.moe_mx_weight_scale_bytes(E_loc, f, d), dtype=torch.uint8, device=dev),
         WguT_q=torch.empty(E_loc, d, 2 * f, dtype=torch.uint8, device=dev),
         WguT_scale=torch.empty(_lib.moe_mx_weight_scale_bytes(E_loc, d, 2 * f), dtype=torch.uint8, device=dev))
+    if w_exp is not None:
+        _check("moe_pack_weights_backward_fp8", _lib.moe_pack_weights_backward_fp8(
+            _ptr(W_gate), _ptr(W_up), _ptr(W_down), src, E_loc, d, f, _ptr(w_exp), _ptr(bw.WguT_q),
+            _ptr(bw.WguT_scale), _ptr(bw.Wd_q), _ptr(bw.Wd_scale), _stream()))
+        return bw
     _check("moe_pack_weights_backward_mx", _lib.moe_pack_weights_backward_mx(
         _ptr(W_gate), _ptr(W_up), _ptr(W_down), src, E_loc, d, f, _ptr(bw.WguT_q), _ptr(bw.WguT_scale), _ptr(bw.Wd_q),
         _ptr(bw.Wd_scale), _stream()))
@@ -462,7 +474,8 @@ def moe_pack_weights_backward_mx(W_gate: torch.Tensor, W_up: torch.Tensor, W_dow
 
 def moe_layer_backward_mx(x, dy, topk_ids, topk_probs, E: int, e0: int, pw: PackedWeights, bw: BackwardWeightsMx,
                           ws=None, out=None):
-    """Gradients of sum(dy * y) of the MXFP8 layer: dict(dx, dlogits, dW_gate, dW_up, dW_down)."""
+    """Gradients of sum(dy * y) of the MXFP8 layer, or of the per-tensor FP8 layer when pw
+    is a per-tensor FP8 pack: dict(dx, dlogits, dW_gate, dW_up, dW_down)."""
     T, d = x.shape
     k = topk_ids.shape[1]
     f, E_loc = pw.f, pw.E_loc
@@ -475,7 +488,8 @@ def moe_layer_backward_mx(x, dy, topk_ids, topk_probs, E: int, e0: int, pw: Pack
                    dW_down=torch.empty(E_loc, f, d, dtype=torch.float32, device=dev))
     nb = _lib.moe_layer_backward_mx_workspace_size(T, d, f, k, E_loc)
     ws = ws if ws is not None else workspace(nb, dev)
-    _check("moe_layer_backward_mx", _lib.moe_layer_backward_mx(
+    fn = "moe_layer_backward_fp8" if pw.dtype == MOE_FP8 else "moe_layer_backward_mx"
+    _check(fn, getattr(_lib, fn)(
         _ptr(x), _ptr(dy), _ptr(topk_ids), _ptr(topk_probs), T, d, f, E, k, e0, E_loc, _ptr(pw.Wgu), _ptr(pw.Wgu_scale),
         _ptr(bw.Wd_q), _ptr(bw.Wd_scale), _ptr(bw.WguT_q), _ptr(bw.WguT_scale), _ptr(out["dx"]), _ptr(out["dlogits"]),
         _ptr(out["dW_gate"]), _ptr(out["dW_up"]), _ptr(out["dW_down"]), _ptr(ws), ws.numel(), _stream()))

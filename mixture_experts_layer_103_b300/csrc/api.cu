@@ -71,7 +71,7 @@ cudaError_t launch_pack_fp8(const void* Wg, const void* Wu, const void* Wdn, moe
                             cudaStream_t st);
 cudaError_t launch_pack_backward_mx(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, int E_loc, int d,
                                     int f, uint8_t* WguT_q, uint8_t* WguT_sf, uint8_t* Wd_q, uint8_t* Wd_sf,
-                                    cudaStream_t st);
+                                    cudaStream_t st, const int32_t* tensor_exp = nullptr);
 cudaError_t launch_colquant_mx(void* buf, int C, const int32_t* offsets, int E_loc, cudaStream_t st);
 cudaError_t launch_tc_dswiglu_mx(const void* dy_q, const uint8_t* dy_sf, const int32_t* offsets,
                                  const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* Wd_q,
@@ -82,6 +82,13 @@ cudaError_t launch_tc_gemm_store_mx(const void* A, const uint8_t* a_sf, int64_t 
                                     int32_t* err, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_pack(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, moe_dtype dst, int E_loc, int d,
                         int f, void* Wgu_p, void* Wd_p, uint8_t* Wgu_sf, uint8_t* Wd_sf, cudaStream_t st);
+
+cudaError_t launch_amax(const void* src, moe_dtype dt, int64_t n_per_seg, int n_seg, uint32_t* amax_bits,
+                        cudaStream_t st);
+cudaError_t launch_amax_rows(const void* src, int row_elems, const int32_t* n_rows, int64_t max_rows,
+                             uint32_t* amax_bits, cudaStream_t st);
+cudaError_t launch_qdq_fp8_rows(void* buf, int row_elems, const int32_t* n_rows, int64_t max_rows,
+                                const uint32_t* amax_bits, cudaStream_t st);
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
 constexpr int kShapeSwapMin = 64;  // GEMM kernel shapes >= this: swapped operands (gemm_tc.cu)
@@ -374,6 +381,7 @@ struct BackwardWs {
   // MXFP8 backward: x and dy rows quantised along d, dg/du rows along f (E4M3 + scales in
   // the activation SF tile layout)
   uint8_t *x_q, *x_sf, *dy_q, *dy_sf, *dgu_q, *dgu_sf;
+  uint32_t* amax;  // per-tensor FP8: largest |x|, |dy|, |h|, |[dg du]| (fp32 bits)
   size_t total;
 };
 static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int E_loc, bool mx = false) {
@@ -406,6 +414,7 @@ static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int
     w.dy_sf = take(mx_act_sf_bytes(n_cap, d, E_loc));
     w.dgu_q = take(static_cast<size_t>(n_cap) * 2 * f);
     w.dgu_sf = take(mx_act_sf_bytes(n_cap, 2 * f, E_loc));
+    w.amax = reinterpret_cast<uint32_t*>(take(16));
   }
   w.total = o;
   return w;
@@ -893,17 +902,41 @@ moe_status moe_pack_weights_backward_mx(const void* W_gate, const void* W_up, co
                                              Wd_scale, stream));
 }
 
+moe_status moe_pack_weights_backward_fp8(const void* W_gate, const void* W_up, const void* W_down,
+                                         moe_dtype src_dtype, int E_loc, int d, int f, const int32_t* w_exp,
+                                         uint8_t* WguT_q, uint8_t* WguT_scale, uint8_t* Wd_q, uint8_t* Wd_scale,
+                                         moe_stream_t stream) {
+  if (!w_exp) return MOE_ERR_INVALID_ARG;
+  if (!W_gate || !W_up || !W_down || !WguT_q || !WguT_scale || !Wd_q || !Wd_scale || E_loc < 1 || E_loc > 1024 ||
+      d <= 0 || f <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((src_dtype != MOE_BF16 && src_dtype != MOE_F32) || d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(WguT_q) || !aligned16(Wd_q)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_backward_mx(W_gate, W_up, W_down, src_dtype, E_loc, d, f, WguT_q, WguT_scale, Wd_q,
+                                             Wd_scale, stream, w_exp));
+}
+
+size_t moe_layer_backward_fp8_workspace_size(int T, int d, int f, int k, int E_loc) {
+  return moe_layer_backward_mx_workspace_size(T, d, f, k, E_loc);
+}
+
 size_t moe_layer_backward_mx_workspace_size(int T, int d, int f, int k, int E_loc) {
   if (T < 0 || d <= 0 || f <= 0 || k < 1 || E_loc < 1) return 0;
   return backward_layout(nullptr, T, d, f, k, E_loc, true).total;
 }
 
-moe_status moe_layer_backward_mx(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
-                                 int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
-                                 const uint8_t* Wgu_scale, const uint8_t* Wd_q, const uint8_t* Wd_scale,
-                                 const uint8_t* WguT_q, const uint8_t* WguT_scale, void* dx, float* dlogits,
-                                 float* dW_gate, float* dW_up, float* dW_down, void* workspace, size_t workspace_bytes,
-                                 moe_stream_t stream) {
+}  // extern "C"
+
+// The 8-bit layer backward: MXFP8 (per_tensor = false: operands quantised in 32-blocks along
+// each GEMM's contraction axis) or per-tensor FP8 (every operand one tensor with one
+// power-of-two scale, axis-independent, on the same block-scaled kernels with uniform
+// scales; the weight-gradient operands quantised and dequantised in place).
+static moe_status layer_backward_8bit(bool per_tensor, const void* x, const void* dy, const int32_t* topk_ids,
+                                      const float* topk_probs, int T, int d, int f, int E, int k, int e0, int E_loc,
+                                      const void* Wgu_packed, const uint8_t* Wgu_scale, const uint8_t* Wd_q,
+                                      const uint8_t* Wd_scale, const uint8_t* WguT_q, const uint8_t* WguT_scale,
+                                      void* dx, float* dlogits, float* dW_gate, float* dW_up, float* dW_down,
+                                      void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32 || e0 < 0 || E_loc < 1 || e0 + E_loc > E)
     return MOE_ERR_INVALID_ARG;
   if (n_cap_of(T, k, E_loc) > kMaxRows) return MOE_ERR_INVALID_ARG;  // int32 rows and offsets
@@ -928,12 +961,19 @@ moe_status moe_layer_backward_mx(const void* x, const void* dy, const int32_t* t
   else
     e = cudaMemsetAsync(w.offsets, 0, static_cast<size_t>(E_loc + 1) * 4, stream);
   const int32_t* mtb = permute_mtile_base(w.perm_ws, T, E_loc);
+  uint32_t* ax = per_tensor ? w.amax : nullptr;  // x, dy, h, [dg du]
+  const int32_t* n_rows = w.offsets + E_loc;     // N on the device
+  if (e == cudaSuccess && n_cap > 0 && per_tensor) {
+    e = launch_amax(x, MOE_BF16, static_cast<int64_t>(T) * d, 1, ax, stream);
+    if (e == cudaSuccess) e = launch_amax(dy, MOE_BF16, static_cast<int64_t>(T) * d, 1, ax + 1, stream);
+  }
   if (e == cudaSuccess && n_cap > 0) {
-    // x and dy rows in routed order: MXFP8 along d (the row-wise GEMMs' A operands) and bf16
-    // (the weight gradients' operands, quantised column-wise below)
-    e = launch_gather_rows_mx(x, d, w.offsets, E_loc, mtb, w.row_src_token, w.x_q, w.x_sf, stream);
+    // x and dy rows in routed order: 8-bit along d (the row-wise GEMMs' A operands) and bf16
+    // (the weight gradients' operands, quantised below)
+    e = launch_gather_rows_mx(x, d, w.offsets, E_loc, mtb, w.row_src_token, w.x_q, w.x_sf, stream, ax);
     if (e == cudaSuccess)
-      e = launch_gather_rows_mx(dy, d, w.offsets, E_loc, mtb, w.row_src_token, w.dy_q, w.dy_sf, stream);
+      e = launch_gather_rows_mx(dy, d, w.offsets, E_loc, mtb, w.row_src_token, w.dy_q, w.dy_sf, stream,
+                                per_tensor ? ax + 1 : nullptr);
     if (e == cudaSuccess)
       e = launch_gather_rows(dy, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.dy_rows, stream);
     if (e == cudaSuccess)
@@ -946,9 +986,11 @@ moe_status moe_layer_backward_mx(const void* x, const void* dy, const int32_t* t
     if (e == cudaSuccess)
       e = launch_tc_dswiglu_mx(w.dy_q, w.dy_sf, w.offsets, w.row_prob, n_cap, E_loc, d, f, Wd_q, Wd_scale, w.gu, w.dgu,
                                w.h, w.dp_part, w.err, kTimeoutNs, stream);
-    // dx rows = [dg du] [W_gate W_up]^T, both along f
+    // dx rows = [dg du] [W_gate W_up]^T, both along f (per-tensor: [dg du] as one tensor)
+    if (e == cudaSuccess && per_tensor) e = launch_amax_rows(w.dgu, 2 * f, n_rows, n_cap, ax + 3, stream);
     if (e == cudaSuccess)
-      e = launch_gather_rows_mx(w.dgu, 2 * f, w.offsets, E_loc, mtb, nullptr, w.dgu_q, w.dgu_sf, stream);
+      e = launch_gather_rows_mx(w.dgu, 2 * f, w.offsets, E_loc, mtb, nullptr, w.dgu_q, w.dgu_sf, stream,
+                                per_tensor ? ax + 3 : nullptr);
     if (e == cudaSuccess)
       e = launch_tc_gemm_store_mx(w.dgu_q, w.dgu_sf, n_cap, w.offsets, E_loc, 2 * f, d, WguT_q, WguT_scale, w.dxp,
                                   w.err, kTimeoutNs, stream);
@@ -956,12 +998,21 @@ moe_status moe_layer_backward_mx(const void* x, const void* dy, const int32_t* t
   if (e == cudaSuccess) e = launch_combine(w.dxp, w.pair_to_row, T, k, d, MOE_BF16, dx, stream);
   if (e == cudaSuccess)
     e = launch_dlogits(topk_ids, topk_probs, w.pair_to_row, w.dp_part, f / 32, T, E, k, dlogits, stream);
-  // weight gradients: operands quantised column-wise (32-row blocks of each expert's
-  // segment), the dequantised values in place, then the tensor-core weight-gradient GEMMs
-  if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.x_rows, d, w.offsets, E_loc, stream);
-  if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.dy_rows, d, w.offsets, E_loc, stream);
-  if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.h, f, w.offsets, E_loc, stream);
-  if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.dgu, 2 * f, w.offsets, E_loc, stream);
+  // weight gradients: operands quantised (MXFP8: column-wise, 32-row blocks of each
+  // expert's segment; per-tensor FP8: with the tensor's one exponent), the dequantised
+  // values in place, then the tensor-core weight-gradient GEMMs
+  if (per_tensor) {
+    if (e == cudaSuccess && n_cap > 0) e = launch_amax_rows(w.h, f, n_rows, n_cap, ax + 2, stream);
+    if (e == cudaSuccess && n_cap > 0) e = launch_qdq_fp8_rows(w.x_rows, d, n_rows, n_cap, ax, stream);
+    if (e == cudaSuccess && n_cap > 0) e = launch_qdq_fp8_rows(w.dy_rows, d, n_rows, n_cap, ax + 1, stream);
+    if (e == cudaSuccess && n_cap > 0) e = launch_qdq_fp8_rows(w.h, f, n_rows, n_cap, ax + 2, stream);
+    if (e == cudaSuccess && n_cap > 0) e = launch_qdq_fp8_rows(w.dgu, 2 * f, n_rows, n_cap, ax + 3, stream);
+  } else {
+    if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.x_rows, d, w.offsets, E_loc, stream);
+    if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.dy_rows, d, w.offsets, E_loc, stream);
+    if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.h, f, w.offsets, E_loc, stream);
+    if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.dgu, 2 * f, w.offsets, E_loc, stream);
+  }
   if (e == cudaSuccess)
     e = launch_wgrad_down_tc(w.h, w.dy_rows, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_down, w.err,
                              kTimeoutNs, stream);
@@ -969,6 +1020,30 @@ moe_status moe_layer_backward_mx(const void* x, const void* dy, const int32_t* t
     e = launch_wgrad_gate_up_tc(w.x_rows, w.dgu, w.offsets, std::max<int64_t>(n_cap, 1), E_loc, d, f, dW_gate, dW_up,
                                 w.err, kTimeoutNs, stream);
   return cuda_status(e);
+}
+
+extern "C" {
+
+moe_status moe_layer_backward_mx(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs, int T,
+                                 int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
+                                 const uint8_t* Wgu_scale, const uint8_t* Wd_q, const uint8_t* Wd_scale,
+                                 const uint8_t* WguT_q, const uint8_t* WguT_scale, void* dx, float* dlogits,
+                                 float* dW_gate, float* dW_up, float* dW_down, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream) {
+  return layer_backward_8bit(false, x, dy, topk_ids, topk_probs, T, d, f, E, k, e0, E_loc, Wgu_packed, Wgu_scale, Wd_q,
+                             Wd_scale, WguT_q, WguT_scale, dx, dlogits, dW_gate, dW_up, dW_down, workspace,
+                             workspace_bytes, stream);
+}
+
+moe_status moe_layer_backward_fp8(const void* x, const void* dy, const int32_t* topk_ids, const float* topk_probs,
+                                  int T, int d, int f, int E, int k, int e0, int E_loc, const void* Wgu_packed,
+                                  const uint8_t* Wgu_scale, const uint8_t* Wd_q, const uint8_t* Wd_scale,
+                                  const uint8_t* WguT_q, const uint8_t* WguT_scale, void* dx, float* dlogits,
+                                  float* dW_gate, float* dW_up, float* dW_down, void* workspace,
+                                  size_t workspace_bytes, moe_stream_t stream) {
+  return layer_backward_8bit(true, x, dy, topk_ids, topk_probs, T, d, f, E, k, e0, E_loc, Wgu_packed, Wgu_scale, Wd_q,
+                             Wd_scale, WguT_q, WguT_scale, dx, dlogits, dW_gate, dW_up, dW_down, workspace,
+                             workspace_bytes, stream);
 }
 
 moe_status moe_selftest_wait_timeout(uint64_t timeout_ns, void* workspace, size_t workspace_bytes,

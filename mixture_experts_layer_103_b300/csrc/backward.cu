@@ -68,11 +68,13 @@ cudaError_t launch_pack_gu_t(const void* Wg, const void* Wu, moe_dtype src, int 
 //           along f (B of dx = [dg du] [W_gate W_up]^T, rows d); a 32-block of the packed
 //           order is 32 consecutive gate (or up) columns of one row
 // One thread per (row, 32-block): 64 contiguous source bytes in, 32 codes and one scale
-// byte (weight SF tile layout) out.
+// byte (weight SF tile layout) out.  tensor_exp [3][E_loc] (per-tensor FP8, optional): the
+// exponents of each expert's W_gate, W_up, W_down, used for every block of that matrix.
 template <typename TIn>
 __global__ void __launch_bounds__(256) pack_rows_mx_kernel(const TIn* __restrict__ src0, const TIn* __restrict__ src1,
                                                            int mode, int E_loc, int rows, int K, int f,
-                                                           uint8_t* __restrict__ dst, uint8_t* __restrict__ dst_sf) {
+                                                           uint8_t* __restrict__ dst, uint8_t* __restrict__ dst_sf,
+                                                           const int32_t* __restrict__ tensor_exp) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int nkb = K / 32;
   if (i >= static_cast<int64_t>(E_loc) * rows * nkb) return;
@@ -90,7 +92,8 @@ __global__ void __launch_bounds__(256) pack_rows_mx_kernel(const TIn* __restrict
   float amax = 0.0f;
 #pragma unroll
   for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
-  const int X = mx_exponent(amax);
+  const int e_ = static_cast<int>(er / rows);
+  const int X = tensor_exp ? __ldg(tensor_exp + (mode == 0 ? 2 : (kb & 1)) * E_loc + e_) : mx_exponent(amax);
   const float inv = mx_inv_scale(X);
   uint32_t w[8];
 #pragma unroll
@@ -104,22 +107,25 @@ __global__ void __launch_bounds__(256) pack_rows_mx_kernel(const TIn* __restrict
   dst_sf[sf_w_offset(e, rows, row, kb * 32, K)] = static_cast<uint8_t>(X + 127);
 }
 
+// tensor_exp: nullptr (MXFP8) or the per-tensor FP8 exponents [3][E_loc] of moe_pack_weights_fp8.
 cudaError_t launch_pack_backward_mx(const void* Wg, const void* Wu, const void* Wdn, moe_dtype src, int E_loc, int d,
                                     int f, uint8_t* WguT_q, uint8_t* WguT_sf, uint8_t* Wd_q, uint8_t* Wd_sf,
-                                    cudaStream_t st) {
+                                    cudaStream_t st, const int32_t* tensor_exp) {
   const int64_t n_d = static_cast<int64_t>(E_loc) * f * (d / 32);
   const int64_t n_gu = static_cast<int64_t>(E_loc) * d * (2 * f / 32);
   const dim3 block(256);
   if (src == MOE_F32) {
     pack_rows_mx_kernel<float><<<dim3(static_cast<unsigned>(ceil_div(n_d, 256))), block, 0, st>>>(
-        static_cast<const float*>(Wdn), nullptr, 0, E_loc, f, d, f, Wd_q, Wd_sf);
+        static_cast<const float*>(Wdn), nullptr, 0, E_loc, f, d, f, Wd_q, Wd_sf, tensor_exp);
     pack_rows_mx_kernel<float><<<dim3(static_cast<unsigned>(ceil_div(n_gu, 256))), block, 0, st>>>(
-        static_cast<const float*>(Wg), static_cast<const float*>(Wu), 1, E_loc, d, 2 * f, f, WguT_q, WguT_sf);
+        static_cast<const float*>(Wg), static_cast<const float*>(Wu), 1, E_loc, d, 2 * f, f, WguT_q, WguT_sf,
+        tensor_exp);
   } else {
     pack_rows_mx_kernel<uint16_t><<<dim3(static_cast<unsigned>(ceil_div(n_d, 256))), block, 0, st>>>(
-        static_cast<const uint16_t*>(Wdn), nullptr, 0, E_loc, f, d, f, Wd_q, Wd_sf);
+        static_cast<const uint16_t*>(Wdn), nullptr, 0, E_loc, f, d, f, Wd_q, Wd_sf, tensor_exp);
     pack_rows_mx_kernel<uint16_t><<<dim3(static_cast<unsigned>(ceil_div(n_gu, 256))), block, 0, st>>>(
-        static_cast<const uint16_t*>(Wg), static_cast<const uint16_t*>(Wu), 1, E_loc, d, 2 * f, f, WguT_q, WguT_sf);
+        static_cast<const uint16_t*>(Wg), static_cast<const uint16_t*>(Wu), 1, E_loc, d, 2 * f, f, WguT_q, WguT_sf,
+        tensor_exp);
   }
   return cudaGetLastError();
 }

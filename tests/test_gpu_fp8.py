@@ -155,3 +155,69 @@ def test_fp8_split_calls_equal_layer(moe):
     with pytest.raises(MoeError) as ei:
         moe.moe_expert_gemm1_swiglu_gather(xd, None, M["row_src_token"], M["offsets"], M["row_prob"], pw)
     assert ei.value.status == 2
+
+
+# ----------------------------------------------------------------------------- backward
+BWD = [
+    Workload("fp8b_slice", 300, 256, 128, 16, 4, 4, 8, "fp8"),                       # non-local slots
+    Workload("fp8b_skew", 500, 384, 256, 8, 2, 0, 8, "fp8", ("normal", 0.5)),        # ragged segments
+    Workload("fp8b_e64", 1024, 256, 256, 64, 8, 0, 64, "fp8", ("normal", 0.5)),      # every slot local
+]
+
+
+def _bwd(moe, w, x, lg, dy, Wg, Wu, Wd):
+    wg, wu, wd = to_dev(Wg), to_dev(Wu), to_dev(Wd)
+    pw = moe.moe_pack_weights(wg, wu, wd, "fp8")
+    bw = moe.moe_pack_weights_backward_mx(wg, wu, wd, w_exp=pw.w_exp)
+    ids, probs = moe.moe_route_topk(to_dev(lg), w.k)
+    g, ws = moe.moe_layer_backward_mx(to_dev(x), to_dev(dy), ids, probs, w.E, w.e0, pw, bw)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    return g, pw, bw
+
+
+@pytest.mark.parametrize("w", BWD, ids=[w.name for w in BWD])
+def test_fp8_backward_matches_oracle(moe, w):
+    """The per-tensor FP8 layer backward (C ABI) against oracle.moe_backward_fp8: dx, the
+    router-logit gradients and the three weight gradients within the FP8 tolerance."""
+    from synthetic import gen_dy
+    x, lg, dy = gen_x(w), gen_logits(w), gen_dy(w)
+    Wg, Wu, Wd = gen_weights(w)
+    g, _, _ = _bwd(moe, w, x, lg, dy, Wg, Wu, Wd)
+    ref = oracle.moe_backward_fp8(x, lg, dy, w.k, w.e0, w.E_loc, Wg, Wu, Wd)
+    errs = {key: rel_l2(to_np(g[key]), ref[key]) for key in ("dx", "dlogits", "dW_gate", "dW_up", "dW_down")}
+    print(w.name, {k: f"{v:.2e}" for k, v in errs.items()})
+    bad = {k: v for k, v in errs.items() if not v <= TOL["fp8"]}
+    assert not bad, f"relative L2 above {TOL['fp8']}: {bad}"
+
+
+def test_fp8_backward_weights_use_forward_exponents(moe):
+    """The backward weight layouts (each matrix transposed / re-blocked along the other
+    axis) carry the forward pack's exponents: every scale byte of a matrix equals its
+    exponent + 127, and the codes equal the oracle's per-tensor codes of that matrix."""
+    w = BWD[0]
+    Wg, Wu, Wd = gen_weights(w)
+    wg, wu, wd = to_dev(Wg), to_dev(Wu), to_dev(Wd)
+    pw = moe.moe_pack_weights(wg, wu, wd, "fp8")
+    bw = moe.moe_pack_weights_backward_mx(wg, wu, wd, w_exp=pw.w_exp)
+    torch.cuda.synchronize()
+    w_exp = pw.w_exp.cpu().numpy()
+    Wdq = bw.Wd_q.cpu().numpy()  # [E_loc, f, d]: W_down rows, blocks along d
+    for e in range(w.E_loc):
+        codes, X = oracle.fp8_tensor_quantize(_bf16_values(Wd[e]))
+        assert w_exp[2, e] == X
+        np.testing.assert_array_equal(Wdq[e], codes)
+    S = unpack_w_sf(bw.Wd_scale.cpu().numpy(), w.E_loc, w.f, w.d)
+    for e in range(w.E_loc):
+        assert (S[e] == w_exp[2, e] + 127).all()
+
+
+def test_fp8_backward_deterministic(moe):
+    from synthetic import gen_dy
+    w = BWD[1]
+    x, lg, dy = gen_x(w), gen_logits(w), gen_dy(w)
+    Wg, Wu, Wd = gen_weights(w)
+    a, _, _ = _bwd(moe, w, x, lg, dy, Wg, Wu, Wd)
+    b, _, _ = _bwd(moe, w, x, lg, dy, Wg, Wu, Wd)
+    for key in a:
+        assert torch.equal(a[key], b[key]), key
