@@ -41,6 +41,19 @@ def _logits(kind, T, E, seed=0):
         lg[:, ::3] = -0.0
         lg[:, 1::5] = 0.0
         return lg
+    # the router's lanes hold experts e = lane + 32 i: make one or two lanes hold all of a
+    # token's top choices (distinct, or tied within the lane)
+    if kind in ("one_lane", "one_lane_tied", "two_lanes"):
+        lg = (rng.integers(-3, 3, size=(T, E)) * 0.5).astype(np.float32) if kind == "one_lane_tied" else \
+            rng.standard_normal((T, E)).astype(np.float32)
+        for t in range(T):
+            lanes = rng.choice(32, 2 if kind == "two_lanes" else 1, replace=False)
+            for ln in lanes:
+                if kind == "one_lane_tied":
+                    lg[t, ln::32] = 5.0
+                else:
+                    lg[t, ln::32] += 10.0
+        return lg
     raise ValueError(kind)
 
 
@@ -49,6 +62,8 @@ def _logits(kind, T, E, seed=0):
     (512, 256, 8, "normal"), (300, 64, 8, "normal"), (64, 8, 2, "normal"), (100, 1024, 32, "normal"),
     (77, 37, 5, "normal"), (256, 256, 8, "quarter"), (33, 256, 8, "equal"), (40, 96, 7, "signed_zero"),
     (5, 1, 1, "normal"), (0, 8, 2, "normal"),
+    (300, 256, 8, "one_lane"), (300, 256, 8, "one_lane_tied"), (200, 512, 16, "two_lanes"),
+    (100, 1024, 32, "one_lane"), (150, 160, 9, "one_lane"), (120, 1024, 32, "quarter"),
 ])
 def test_route_parity(moe, T, E, k, kind):
     lg = _logits(kind, T, E, seed=T + E)
