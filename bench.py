@@ -627,9 +627,22 @@ def e2e_leg(moe, args, w, xd, lgd, y, pw, flush, world):
     d2h_bytes = y_pin[0].numel() * y_pin[0].element_size()
     h2d_ms = copy_ms(lambda: (xb[0].copy_(x_pin, non_blocking=True), lgb[0].copy_(lg_pin, non_blocking=True)))
     d2h_ms = copy_ms(lambda: y_pin[0].copy_(yb[0], non_blocking=True))
+
+    def both():  # a step's copies in both directions at once, as the pipeline runs them
+        s_in.wait_stream(torch.cuda.current_stream())
+        s_out.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s_in):
+            xb[0].copy_(x_pin, non_blocking=True)
+            lgb[0].copy_(lg_pin, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            y_pin[1].copy_(yb[1], non_blocking=True)
+        torch.cuda.current_stream().wait_stream(s_in)
+        torch.cuda.current_stream().wait_stream(s_out)
+    both_ms = copy_ms(both)
     return {"value": T * world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_gbs": h2d_bytes / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h_bytes / (d2h_ms / 1e3) / 1e9,
             "copy_bound_ms_per_step": max(h2d_ms, d2h_ms),
+            "copies_both_directions_ms_per_step": both_ms,
             "h2d_bytes_per_step": int(x_pin_bytes + lg_pin.numel() * 4),
             "d2h_bytes_per_step": int(y_pin[0].numel() * y_pin[0].element_size()), "steps": n2,
             "entry_point": "moe_layer_forward",
