@@ -12,10 +12,21 @@
 
 namespace moe {
 
+// Largest |value| of one 16-byte vector (8 bf16 or 4 fp32 values).
+template <int IN_BF16>
+__device__ __forceinline__ float vec_amax(const uint4 q) {
+  if (IN_BF16)
+    return fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(q.x)), fabsf(bf16_hi(q.x))), fmaxf(fabsf(bf16_lo(q.y)), fabsf(bf16_hi(q.y)))),
+                 fmaxf(fmaxf(fabsf(bf16_lo(q.z)), fabsf(bf16_hi(q.z))), fmaxf(fabsf(bf16_lo(q.w)), fabsf(bf16_hi(q.w)))));
+  return fmaxf(fmaxf(fabsf(__uint_as_float(q.x)), fabsf(__uint_as_float(q.y))),
+               fmaxf(fabsf(__uint_as_float(q.z)), fabsf(__uint_as_float(q.w))));
+}
+
 // amax of n_seg segments of n values each (segment s at src + s * n): blockIdx.y = segment,
-// grid-stride over 16-byte vectors, one atomicMax per block on the fp32 bits (non-negative
-// floats order like their bit patterns).  n is a multiple of 8 (bf16) or 4 (fp32).
-// n_rows (optional, device): the segment is its first *n_rows rows of row_vecs vectors.
+// grid-stride over 16-byte vectors with four independent loads in flight per thread, one
+// atomicMax per block on the fp32 bits (non-negative floats order like their bit
+// patterns).  n is a multiple of 8 (bf16) or 4 (fp32).  n_rows (optional, device): the
+// segment is its first *n_rows rows of row_vecs vectors.
 template <int IN_BF16>
 __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ src, int64_t nvec, uint32_t* amax_bits,
                                                    const int32_t* __restrict__ n_rows, int64_t row_vecs) {
@@ -23,20 +34,16 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ src
   pdl_wait();
   if (n_rows) nvec = min(nvec, static_cast<int64_t>(__ldg(n_rows)) * row_vecs);
   const uint4* s = src + static_cast<int64_t>(blockIdx.y) * nvec;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   float m = 0.0f;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint4 q = __ldg(s + i);
-    if (IN_BF16) {
-      m = fmaxf(m, fmaxf(fabsf(bf16_lo(q.x)), fabsf(bf16_hi(q.x))));
-      m = fmaxf(m, fmaxf(fabsf(bf16_lo(q.y)), fabsf(bf16_hi(q.y))));
-      m = fmaxf(m, fmaxf(fabsf(bf16_lo(q.z)), fabsf(bf16_hi(q.z))));
-      m = fmaxf(m, fmaxf(fabsf(bf16_lo(q.w)), fabsf(bf16_hi(q.w))));
-    } else {
-      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(q.x)), fabsf(__uint_as_float(q.y))));
-      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(q.z)), fabsf(__uint_as_float(q.w))));
-    }
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < nvec; i += 4 * stride) {
+    const uint4 q0 = __ldg(s + i), q1 = __ldg(s + i + stride), q2 = __ldg(s + i + 2 * stride),
+                q3 = __ldg(s + i + 3 * stride);
+    m = fmaxf(m, fmaxf(fmaxf(vec_amax<IN_BF16>(q0), vec_amax<IN_BF16>(q1)),
+                       fmaxf(vec_amax<IN_BF16>(q2), vec_amax<IN_BF16>(q3))));
   }
+  for (; i < nvec; i += stride) m = fmaxf(m, vec_amax<IN_BF16>(__ldg(s + i)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   __shared__ float s_m[8];
