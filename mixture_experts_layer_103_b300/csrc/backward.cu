@@ -178,8 +178,10 @@ __global__ void __launch_bounds__(128) colquant_mx_kernel(uint32_t* __restrict__
 }
 
 cudaError_t launch_colquant_mx(void* buf, int C, const int32_t* offsets, int E_loc, cudaStream_t st) {
-  return launch_pdl(colquant_mx_kernel, dim3(32, static_cast<unsigned>(E_loc)), dim3(128), 0, st,
-                    static_cast<uint32_t*>(buf), C, offsets);
+  // at least four CTAs per SM over all experts (few local experts: many CTAs per expert)
+  const int gx = std::max(32, 4 * num_sms() / E_loc);
+  return launch_pdl(colquant_mx_kernel, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(E_loc)), dim3(128), 0,
+                    st, static_cast<uint32_t*>(buf), C, offsets);
 }
 
 // ---------------------------------------------------------------------- router gradient

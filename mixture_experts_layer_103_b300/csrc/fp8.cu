@@ -100,9 +100,7 @@ __global__ void __launch_bounds__(256) qdq_fp8_kernel(uint4* __restrict__ buf, i
   nvec = min(nvec, static_cast<int64_t>(__ldg(n_rows)) * row_vecs);
   const int X = fp8_tensor_exponent(__ldg(amax_bits));
   const float inv = mx_inv_scale(X), sc = ldexpf(1.0f, X);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    uint4 q = buf[i];
+  auto qdq = [&](uint4& q) {
     uint32_t* w = reinterpret_cast<uint32_t*>(&q);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -110,6 +108,20 @@ __global__ void __launch_bounds__(256) qdq_fp8_kernel(uint4* __restrict__ buf, i
       const float2 dq = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3)));
       w[j] = pack_bf16x2(dq.x * sc, dq.y * sc);
     }
+  };
+  // two independent vectors in flight per thread
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + stride < nvec; i += 2 * stride) {
+    uint4 q0 = buf[i], q1 = buf[i + stride];
+    qdq(q0);
+    qdq(q1);
+    buf[i] = q0;
+    buf[i + stride] = q1;
+  }
+  if (i < nvec) {
+    uint4 q = buf[i];
+    qdq(q);
     buf[i] = q;
   }
 }
