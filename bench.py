@@ -181,7 +181,7 @@ class ClockSampler:
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_power_cap,clocks.mem,clocks.max.mem,pstate")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -217,7 +217,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons, power = [], [], set(), []
+        sm, smax, reasons, power, mem, mmax, pstates = [], [], set(), [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         t0, t1 = getattr(self, "t_begin", 0.0), getattr(self, "t_end", 1e30) + 0.05
         for ts, ln in self.lines:
@@ -238,8 +238,17 @@ class ClockSampler:
             for nm, v in zip(names, parts[4:8]):
                 if v.lower() == "active":
                     reasons.add(nm)
+            if len(parts) >= 11:
+                try:
+                    mem.append(float(parts[8]))
+                    mmax.append(float(parts[9]))
+                except ValueError:
+                    pass
+                pstates.add(parts[10])
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+                "mem_mhz": statistics.median(mem) if mem else None, "mem_max_mhz": max(mmax) if mmax else None,
+                "pstates": sorted(pstates), "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
 
 
 # ----------------------------------------------------------------------------- ours
