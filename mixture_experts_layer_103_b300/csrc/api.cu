@@ -382,6 +382,7 @@ struct BackwardWs {
   // the activation SF tile layout)
   uint8_t *x_q, *x_sf, *dy_q, *dy_sf, *dgu_q, *dgu_sf;
   uint32_t* amax;  // per-tensor FP8: largest |x|, |dy|, |h|, |[dg du]| (fp32 bits)
+  int32_t* tok_nloc;  // [T] local slots per token (the dx GEMM that combines)
   size_t total;
 };
 static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int E_loc, bool mx = false) {
@@ -407,6 +408,7 @@ static BackwardWs backward_layout(uint8_t* base, int T, int d, int f, int k, int
   w.dxp = take(static_cast<size_t>(n_cap) * d * 2);
   w.x_rows = take(static_cast<size_t>(n_cap) * d * 2);
   w.dy_rows = take(static_cast<size_t>(n_cap) * d * 2);
+  w.tok_nloc = reinterpret_cast<int32_t*>(take(static_cast<size_t>(T) * 4));
   if (mx) {  // MXFP8 operands of the row-wise GEMMs (recompute, dh, dx)
     w.x_q = take(static_cast<size_t>(n_cap) * d);
     w.x_sf = take(mx_act_sf_bytes(n_cap, d, E_loc));
@@ -492,6 +494,31 @@ moe_status moe::check_permute(const void* x, moe_dtype x_dtype, moe_dtype perm_d
     return (T > 0 && perm_x && !perm_sf) ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
   if (T > 0 && (!aligned16(x) || (perm_x && !aligned16(perm_x)))) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
+}
+
+// dx = the slot sum of the dx rows [N_cap, d] = [dg du] (K = 2f) x WguT per expert.  On
+// expert slices with under one local slot per token (k E_loc < E) the GEMM writes the dx
+// rows of single-slot tokens straight to dx and zero rows for tokens with none, and a
+// sparse pass sums the others (the forward GEMM2's combine mode); otherwise a store GEMM
+// and the combine kernel.  a / a_sf: the [dg du] rows (bf16, or E4M3 + SF when mx).
+static cudaError_t backward_dx(bool mx, const void* a, const uint8_t* a_sf, const BackwardWs& w, int64_t n_cap, int T,
+                               int E, int k, int E_loc, int d, int f, const void* B, const uint8_t* b_sf, void* dx,
+                               cudaStream_t st) {
+  const moe_dtype dt = mx ? MOE_MXFP8 : MOE_BF16;
+  if (n_cap > 0 && fuses_combine(dt, k, E_loc, E)) {
+    const int shape = gemm_shape(false, dt, n_cap, E_loc, moe_rows_hint(T, k, E), 2 * f, false);
+    cudaError_t e = launch_tc_gemm2_combine(a, a_sf, w.offsets, n_cap, E_loc, d, 2 * f, mx, shape, B, b_sf, w.dxp,
+                                            w.row_src_token, w.tok_nloc, T, dx, w.err, kTimeoutNs, st);
+    if (e == cudaSuccess)
+      e = launch_combine_multi(w.dxp, w.pair_to_row, w.tok_nloc, T, k, d, dx, static_cast<double>(k) * E_loc / E, st);
+    return e;
+  }
+  cudaError_t e = cudaSuccess;
+  if (n_cap > 0)
+    e = mx ? launch_tc_gemm_store_mx(a, a_sf, n_cap, w.offsets, E_loc, 2 * f, d, B, b_sf, w.dxp, w.err, kTimeoutNs, st)
+           : launch_tc_gemm_store(a, n_cap, w.offsets, E_loc, 2 * f, d, B, w.dxp, w.err, kTimeoutNs, st);
+  if (e == cudaSuccess) e = launch_combine(w.dxp, w.pair_to_row, T, k, d, MOE_BF16, dx, st);
+  return e;
 }
 
 extern "C" {
@@ -861,7 +888,8 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
   cudaError_t e = cudaSuccess;
   if (T > 0)
     e = launch_permute(x, MOE_BF16, MOE_BF16, T, d, topk_ids, topk_probs, k, e0, E_loc, nullptr, nullptr, w.counts,
-                       w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
+                       w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream,
+                       fuses_combine(MOE_BF16, k, E_loc, E) ? w.tok_nloc : nullptr);
   else
     e = cudaMemsetAsync(w.offsets, 0, static_cast<size_t>(E_loc + 1) * 4, stream);
   // dy and x rows in routed order: the A operands of the recompute and dh GEMMs and of
@@ -875,10 +903,8 @@ moe_status moe_layer_backward(const void* x, const void* dy, const int32_t* topk
   if (e == cudaSuccess && n_cap > 0)
     e = launch_tc_dswiglu(w.dy_rows, w.offsets, w.row_prob, n_cap, E_loc, d, f, W_down, gu_saved ? gu_saved : w.gu,
                           w.dgu, w.h, w.dp_part, w.err, kTimeoutNs, stream);
-  if (e == cudaSuccess && n_cap > 0)
-    e = launch_tc_gemm_store(w.dgu, n_cap, w.offsets, E_loc, 2 * f, d, WguT_packed, w.dxp, w.err, kTimeoutNs,
-                             stream);
-  if (e == cudaSuccess) e = launch_combine(w.dxp, w.pair_to_row, T, k, d, MOE_BF16, dx, stream);
+  if (e == cudaSuccess)
+    e = backward_dx(false, w.dgu, nullptr, w, n_cap, T, E, k, E_loc, d, f, WguT_packed, nullptr, dx, stream);
   if (e == cudaSuccess)
     e = launch_dlogits(topk_ids, topk_probs, w.pair_to_row, w.dp_part, f / 32, T, E, k, dlogits, stream);
   if (e == cudaSuccess)
@@ -957,7 +983,8 @@ static moe_status layer_backward_8bit(bool per_tensor, const void* x, const void
   cudaError_t e = cudaSuccess;
   if (T > 0)
     e = launch_permute(x, MOE_BF16, MOE_BF16, T, d, topk_ids, topk_probs, k, e0, E_loc, nullptr, nullptr, w.counts,
-                       w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream);
+                       w.offsets, w.row_src_token, w.row_prob, w.pair_to_row, w.perm_ws, stream,
+                       fuses_combine(MOE_MXFP8, k, E_loc, E) ? w.tok_nloc : nullptr);
   else
     e = cudaMemsetAsync(w.offsets, 0, static_cast<size_t>(E_loc + 1) * 4, stream);
   const int32_t* mtb = permute_mtile_base(w.perm_ws, T, E_loc);
@@ -991,11 +1018,9 @@ static moe_status layer_backward_8bit(bool per_tensor, const void* x, const void
     if (e == cudaSuccess)
       e = launch_gather_rows_mx(w.dgu, 2 * f, w.offsets, E_loc, mtb, nullptr, w.dgu_q, w.dgu_sf, stream,
                                 per_tensor ? ax + 3 : nullptr);
-    if (e == cudaSuccess)
-      e = launch_tc_gemm_store_mx(w.dgu_q, w.dgu_sf, n_cap, w.offsets, E_loc, 2 * f, d, WguT_q, WguT_scale, w.dxp,
-                                  w.err, kTimeoutNs, stream);
   }
-  if (e == cudaSuccess) e = launch_combine(w.dxp, w.pair_to_row, T, k, d, MOE_BF16, dx, stream);
+  if (e == cudaSuccess)
+    e = backward_dx(true, w.dgu_q, w.dgu_sf, w, n_cap, T, E, k, E_loc, d, f, WguT_q, WguT_scale, dx, stream);
   if (e == cudaSuccess)
     e = launch_dlogits(topk_ids, topk_probs, w.pair_to_row, w.dp_part, f / 32, T, E, k, dlogits, stream);
   // weight gradients: operands quantised (MXFP8: column-wise, 32-row blocks of each

@@ -55,6 +55,9 @@ SMALL = [
     Workload("b_slice", 200, 256, 128, 16, 4, 4, 8, "bf16"),
     Workload("b_e64", 1024, 512, 512, 64, 8, 0, 64, "bf16", ("normal", 0.5)),
     Workload("b_zipf", 512, 256, 128, 256, 8, 0, 32, "bf16", ("zipf", 1.1)),
+    # under one local slot per token (k E_loc < E): the dx GEMM writes single-slot tokens'
+    # rows and the zero rows itself, a sparse pass sums the rest
+    Workload("b_ep", 1000, 256, 128, 256, 8, 32, 16, "bf16"),
 ]
 
 

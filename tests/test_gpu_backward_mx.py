@@ -51,6 +51,7 @@ SMALL = [
     Workload("mxb_slice", 300, 256, 128, 16, 4, 4, 8, "mxfp8"),                        # non-local slots
     Workload("mxb_skew", 500, 384, 256, 8, 2, 0, 8, "mxfp8", ("normal", 0.5)),         # ragged segments
     Workload("mxb_e64", 1024, 256, 256, 64, 8, 0, 64, "mxfp8", ("normal", 0.5)),       # every slot local
+    Workload("mxb_ep", 1000, 256, 128, 256, 8, 32, 16, "mxfp8"),                       # dx combined in its GEMM
 ]
 
 

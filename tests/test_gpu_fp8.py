@@ -162,6 +162,7 @@ BWD = [
     Workload("fp8b_slice", 300, 256, 128, 16, 4, 4, 8, "fp8"),                       # non-local slots
     Workload("fp8b_skew", 500, 384, 256, 8, 2, 0, 8, "fp8", ("normal", 0.5)),        # ragged segments
     Workload("fp8b_e64", 1024, 256, 256, 64, 8, 0, 64, "fp8", ("normal", 0.5)),      # every slot local
+    Workload("fp8b_ep", 1000, 256, 128, 256, 8, 32, 16, "fp8"),                      # dx combined in its GEMM
 ]
 
 
