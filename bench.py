@@ -805,7 +805,7 @@ def run_backward(args, w):
         "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
                      "kernel": "whole backward (12 N d f FLOP)", "traffic": None, "peak_kind": pk_kind},
-        "N_pairs": N, "gpu_launches": ({"mxfp8": 19, "fp8": 23}.get(w.dtype, 11)) * args.steps, "clocks": clk,
+        "N_pairs": N, "gpu_launches": ({"mxfp8": 15, "fp8": 23}.get(w.dtype, 11)) * args.steps, "clocks": clk,
         "per_kernel_floor": {"roofline_us": floor_s * 1e6, "measured_us": ms * 1e3, "frac": floor_s / (ms * 1e-3),
                              "terms_us": {k: v * 1e6 for k, v in floor_terms.items()},
                              "note": "sum over the backward's kernels of max(FLOPs / bf16 peak, bytes / HBM)"},

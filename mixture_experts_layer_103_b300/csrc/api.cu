@@ -73,6 +73,8 @@ cudaError_t launch_pack_backward_mx(const void* Wg, const void* Wu, const void* 
                                     int f, uint8_t* WguT_q, uint8_t* WguT_sf, uint8_t* Wd_q, uint8_t* Wd_sf,
                                     cudaStream_t st, const int32_t* tensor_exp = nullptr);
 cudaError_t launch_colquant_mx(void* buf, int C, const int32_t* offsets, int E_loc, cudaStream_t st);
+cudaError_t launch_rows_mx_both(const void* src, int d, const int32_t* offsets, int E_loc, const int32_t* mtile_base,
+                                const int32_t* row_src_token, uint8_t* q, uint8_t* q_sf, void* deq, cudaStream_t st);
 cudaError_t launch_tc_dswiglu_mx(const void* dy_q, const uint8_t* dy_sf, const int32_t* offsets,
                                  const float* row_prob, int64_t N_cap, int E_loc, int d, int f, const void* Wd_q,
                                  const uint8_t* Wd_sf, const void* gu, void* dgu, void* h, float* dp_part, int32_t* err,
@@ -996,15 +998,22 @@ static moe_status layer_backward_8bit(bool per_tensor, const void* x, const void
   }
   if (e == cudaSuccess && n_cap > 0) {
     // x and dy rows in routed order: 8-bit along d (the row-wise GEMMs' A operands) and bf16
-    // (the weight gradients' operands, quantised below)
-    e = launch_gather_rows_mx(x, d, w.offsets, E_loc, mtb, w.row_src_token, w.x_q, w.x_sf, stream, ax);
-    if (e == cudaSuccess)
-      e = launch_gather_rows_mx(dy, d, w.offsets, E_loc, mtb, w.row_src_token, w.dy_q, w.dy_sf, stream,
-                                per_tensor ? ax + 1 : nullptr);
-    if (e == cudaSuccess)
-      e = launch_gather_rows(dy, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.dy_rows, stream);
-    if (e == cudaSuccess)
-      e = launch_gather_rows(x, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.x_rows, stream);
+    // (the weight gradients' operands; MXFP8: quantised column-wise in the same pass,
+    // per-tensor FP8: quantised below)
+    if (per_tensor) {
+      e = launch_gather_rows_mx(x, d, w.offsets, E_loc, mtb, w.row_src_token, w.x_q, w.x_sf, stream, ax);
+      if (e == cudaSuccess)
+        e = launch_gather_rows_mx(dy, d, w.offsets, E_loc, mtb, w.row_src_token, w.dy_q, w.dy_sf, stream, ax + 1);
+      if (e == cudaSuccess)
+        e = launch_gather_rows(dy, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.dy_rows,
+                               stream);
+      if (e == cudaSuccess)
+        e = launch_gather_rows(x, static_cast<int64_t>(d) * 2, w.offsets, E_loc, w.row_src_token, w.x_rows, stream);
+    } else {
+      e = launch_rows_mx_both(x, d, w.offsets, E_loc, mtb, w.row_src_token, w.x_q, w.x_sf, w.x_rows, stream);
+      if (e == cudaSuccess)
+        e = launch_rows_mx_both(dy, d, w.offsets, E_loc, mtb, w.row_src_token, w.dy_q, w.dy_sf, w.dy_rows, stream);
+    }
     // g, u of the MXFP8 forward (x and the gate/up weights along d), kept in bf16
     if (e == cudaSuccess)
       e = launch_tc_gemm_store_mx(w.x_q, w.x_sf, n_cap, w.offsets, E_loc, d, 2 * f, Wgu_packed, Wgu_scale, w.gu,
@@ -1032,9 +1041,7 @@ static moe_status layer_backward_8bit(bool per_tensor, const void* x, const void
     if (e == cudaSuccess && n_cap > 0) e = launch_qdq_fp8_rows(w.dy_rows, d, n_rows, n_cap, ax + 1, stream);
     if (e == cudaSuccess && n_cap > 0) e = launch_qdq_fp8_rows(w.h, f, n_rows, n_cap, ax + 2, stream);
     if (e == cudaSuccess && n_cap > 0) e = launch_qdq_fp8_rows(w.dgu, 2 * f, n_rows, n_cap, ax + 3, stream);
-  } else {
-    if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.x_rows, d, w.offsets, E_loc, stream);
-    if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.dy_rows, d, w.offsets, E_loc, stream);
+  } else {  // (x and dy rows: quantised column-wise while gathered)
     if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.h, f, w.offsets, E_loc, stream);
     if (e == cudaSuccess && n_cap > 0) e = launch_colquant_mx(w.dgu, 2 * f, w.offsets, E_loc, stream);
   }

@@ -177,6 +177,130 @@ __global__ void __launch_bounds__(128) colquant_mx_kernel(uint32_t* __restrict__
   }
 }
 
+// MXFP8 backward, the x or dy rows in one pass: each warp takes a 32-row block of an
+// expert's segment (rows in routed order, row r = source row row_src_token[r]) by 32
+// columns and writes, from one read, both forms the backward uses:
+//   q, q_sf  E4M3 codes with one E8M0 scale per 32 values along the row (the row-wise
+//            GEMMs' operand, scales in the activation SF tile layout): what
+//            launch_gather_rows_mx writes
+//   deq      the bf16 values quantised column-wise (one scale per 32 rows of a column
+//            within the segment) and dequantised: what launch_gather_rows followed by
+//            launch_colquant_mx leaves
+// Lane = row: a row block's scale comes from the lane's own 32 values, a column block's
+// from one warp max (redux) per column.  Same arithmetic as those kernels, so the same
+// bits.  d % 32 == 0.
+__global__ void __launch_bounds__(256) rows_mx_both_kernel(const uint16_t* __restrict__ src, int d,
+                                                           const int32_t* __restrict__ offsets, int E_loc,
+                                                           const int32_t* __restrict__ mtile_base,
+                                                           const int32_t* __restrict__ row_src_token,
+                                                           uint8_t* __restrict__ q, uint8_t* __restrict__ q_sf,
+                                                           uint16_t* __restrict__ deq) {
+  pdl_launch_dependents();
+  pdl_wait();
+  extern __shared__ int32_t s_tab[];
+  int32_t* s_off = s_tab;               // [E_loc + 1] segment starts
+  int32_t* s_rbp = s_off + E_loc + 1;   // [E_loc + 1] 32-row blocks before each expert
+  int32_t* s_mtb = s_rbp + E_loc + 1;   // [E_loc + 1] 128-row m-tiles before each expert
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    const int per = (E_loc + 31) / 32, e_begin = lane * per, e_end = min(E_loc, e_begin + per);
+    int sum = 0;
+    for (int e = e_begin; e < e_end; ++e) sum += (__ldg(offsets + e + 1) - __ldg(offsets + e) + 31) / 32;
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - sum;
+    for (int e = e_begin; e < e_end; ++e) {
+      s_off[e] = __ldg(offsets + e);
+      s_rbp[e] = run;
+      s_mtb[e] = __ldg(mtile_base + e);
+      run += (__ldg(offsets + e + 1) - __ldg(offsets + e) + 31) / 32;
+    }
+    if (lane == 31) {
+      s_off[E_loc] = __ldg(offsets + E_loc);
+      s_rbp[E_loc] = incl;
+    }
+  }
+  __syncthreads();
+  const int ncb = d / 32;
+  const int64_t items = static_cast<int64_t>(s_rbp[E_loc]) * ncb;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t it = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
+       it += nwarps) {
+    const int cb = static_cast<int>(it % ncb);
+    const int rbg = static_cast<int>(it / ncb);
+    int lo = 0, hi = E_loc - 1;  // expert: the last e with s_rbp[e] <= rbg
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_rbp[mid] <= rbg) lo = mid;
+      else hi = mid - 1;
+    }
+    const int e = lo;
+    const int il = (rbg - s_rbp[e]) * 32 + lane;  // row within the expert's segment
+    const bool valid = il < s_off[e + 1] - s_off[e];
+    const int64_t r = static_cast<int64_t>(s_off[e]) + il;
+    uint4 a[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                  make_uint4(0u, 0u, 0u, 0u)};
+    if (valid) {
+      const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<int64_t>(__ldg(row_src_token + r)) * d + cb * 32);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) a[j] = __ldg(p + j);
+    }
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * j + 0] = bf16_lo(a[j].x); v[8 * j + 1] = bf16_hi(a[j].x);
+      v[8 * j + 2] = bf16_lo(a[j].y); v[8 * j + 3] = bf16_hi(a[j].y);
+      v[8 * j + 4] = bf16_lo(a[j].z); v[8 * j + 5] = bf16_hi(a[j].z);
+      v[8 * j + 6] = bf16_lo(a[j].w); v[8 * j + 7] = bf16_hi(a[j].w);
+    }
+    // along the row: one block of 32 values
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(v[i]));
+    const int X = mx_exponent(am);
+    const float inv = mx_inv_scale(X);
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      w[j] = static_cast<uint32_t>(e4m3x2(v[4 * j] * inv, v[4 * j + 1] * inv)) |
+             (static_cast<uint32_t>(e4m3x2(v[4 * j + 2] * inv, v[4 * j + 3] * inv)) << 16);
+    if (valid) {
+      uint4* dq = reinterpret_cast<uint4*>(q + r * d + cb * 32);
+      dq[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dq[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      q_sf[sf_act_offset(s_mtb[e] + il / 128, il % 128, cb * 32, d)] = static_cast<uint8_t>(X + 127);
+    }
+    // down the columns: a block of the segment's 32 rows per column, from the warp's max
+    uint32_t o[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float m0 = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[2 * j]))));
+      const float m1 = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[2 * j + 1]))));
+      const int X0 = mx_exponent(m0), X1 = mx_exponent(m1);
+      const __nv_fp8x2_storage_t c = e4m3x2(v[2 * j] * mx_inv_scale(X0), v[2 * j + 1] * mx_inv_scale(X1));
+      const float2 f2 = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3)));
+      o[j] = pack_bf16x2(f2.x * ldexpf(1.0f, X0), f2.y * ldexpf(1.0f, X1));
+    }
+    if (valid) {
+      uint4* dd = reinterpret_cast<uint4*>(deq + r * d + cb * 32);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dd[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+    }
+  }
+}
+
+cudaError_t launch_rows_mx_both(const void* src, int d, const int32_t* offsets, int E_loc, const int32_t* mtile_base,
+                                const int32_t* row_src_token, uint8_t* q, uint8_t* q_sf, void* deq, cudaStream_t st) {
+  const size_t sm = static_cast<size_t>(3 * (E_loc + 1)) * 4;
+  return launch_pdl(rows_mx_both_kernel, dim3(static_cast<unsigned>(num_sms() * 8)), dim3(256), sm, st,
+                    static_cast<const uint16_t*>(src), d, offsets, E_loc, mtile_base, row_src_token, q, q_sf,
+                    static_cast<uint16_t*>(deq));
+}
+
 cudaError_t launch_colquant_mx(void* buf, int C, const int32_t* offsets, int E_loc, cudaStream_t st) {
   // at least four CTAs per SM over all experts (few local experts: many CTAs per expert)
   const int gx = std::max(32, 4 * num_sms() / E_loc);
