@@ -156,6 +156,40 @@ def test_validation_before_any_launch(lib):
     assert L.moe_get_device_error(P, s, None) == 1
 
 
+def test_8bit_entries_validate_before_any_launch(lib):
+    """Per-tensor FP8 and MXFP8 packing / backward entries: argument and shape checks on the
+    host, the workspace sizes they quote."""
+    L = lib.lib()
+    P = ctypes.c_void_p(256)  # never dereferenced
+    s = _null()
+    MX, FP8 = 2, 3
+    # per-tensor FP8 pack: no exponent output, d or f not a multiple of 128, 8-bit source
+    assert L.moe_pack_weights_fp8(P, P, P, 1, 4, 128, 128, P, P, P, P, None, s) == 1
+    assert L.moe_pack_weights_fp8(P, P, P, 1, 4, 96, 128, P, P, P, P, P, s) == 2
+    assert L.moe_pack_weights_fp8(P, P, P, 1, 4, 128, 96, P, P, P, P, P, s) == 2
+    assert L.moe_pack_weights_fp8(P, P, P, MX, 4, 128, 128, P, P, P, P, P, s) == 2
+    assert L.moe_pack_weights_fp8(P, P, P, 1, 2048, 128, 128, P, P, P, P, P, s) == 1  # E_loc > 1024
+    # backward weight layouts: no exponents (FP8), d % 128, misaligned output
+    assert L.moe_pack_weights_backward_fp8(P, P, P, 1, 4, 128, 128, None, P, P, P, P, s) == 1
+    assert L.moe_pack_weights_backward_fp8(P, P, P, 1, 4, 96, 128, P, P, P, P, P, s) == 2
+    assert L.moe_pack_weights_backward_mx(P, P, P, 1, 4, 128, 128, ctypes.c_void_p(264), P, P, P, s) == 1
+    # 8-bit layer backward: e0 + E_loc > E, d % 128, workspace too small (both entry points)
+    for fn in (L.moe_layer_backward_mx, L.moe_layer_backward_fp8):
+        assert fn(P, P, P, P, 8, 128, 128, 8, 2, 4, 8, P, P, P, P, P, P, P, P, P, P, P, P, 1 << 30, s) == 1
+        assert fn(P, P, P, P, 8, 96, 128, 8, 2, 0, 8, P, P, P, P, P, P, P, P, P, P, P, P, 1 << 30, s) == 2
+        assert fn(P, P, P, P, 8, 128, 128, 8, 2, 0, 8, P, P, P, P, P, P, P, P, P, P, P, P, 64, s) == 3
+    # the per-tensor FP8 backward uses the MXFP8 backward's workspace
+    for args in ((4096, 2048, 1024, 8, 64), (8192, 7168, 2048, 8, 4), (0, 128, 128, 2, 1)):
+        assert L.moe_layer_backward_fp8_workspace_size(*args) == L.moe_layer_backward_mx_workspace_size(*args) > 0
+    # GEMM1's own workspace: the error word, plus bf16 h and its amax for per-tensor FP8
+    assert L.moe_expert_gemm1_workspace_size(1000, 256, 1) == L.moe_expert_gemm1_workspace_size(1000, 256, MX) == 256
+    assert L.moe_expert_gemm1_workspace_size(1000, 256, FP8) >= 256 + 1000 * 256 * 2 + 4
+    # per-tensor FP8 GEMMs always run on the 1-CTA block-scaled kernel
+    for g in (1, 2):
+        assert lib.moe_layer_gemm_kernel(8192, 7168, 2048, 8, 256, 4, "fp8", g) == "cta"
+        assert lib.moe_layer_gemm_kernel(4096, 2048, 1024, 8, 64, 64, "fp8", g) == "cta"
+
+
 def test_gemm1_kernel_choice(lib):
     """The host-side rule behind moe_layer_forward's GEMM1 kernel: CTA pairs from 2048
     expected rows per expert, or 256-1023 rows when d >= 4096 (bf16 only); the 1-CTA
