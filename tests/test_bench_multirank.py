@@ -86,3 +86,33 @@ def test_backward_floor_terms():
     assert abs(terms["dx_gemm"] - 4.0 * N * d * f / tf) < 1e-12
     assert abs(total - sum(terms.values())) < 1e-15
     assert 650e-6 < total < 665e-6
+
+
+def test_layer_bytes_and_flops():
+    """The roofline numerators the bench reports, by hand: bf16_e64 (every expert local,
+    N = T k) is tensor-bound in GEMM1 (4 N d f FLOP against 2 d f 2 B of weights per
+    expert, the routed x rows and h); an EP64 MXFP8 slice counts E4M3 bytes plus one scale
+    byte per 32 values, and only the non-empty experts' weights."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from synthetic import WORKLOADS
+    w = WORKLOADS["bf16_e64"]
+    T, d, f, E = 4096, 2048, 1024, 64
+    N = T * 8
+    b = bench.layer_bytes_flops(w, N, E, T)
+    assert b["gemm1_flops"] == 4.0 * N * d * f and b["gemm2_flops"] == 2.0 * N * d * f
+    assert b["layer_flops"] == b["gemm1_flops"] + b["gemm2_flops"]
+    assert b["gemm1_bytes"] == 2 * d * f * 2 * E + N * d * 2 + N * f * 2
+    assert b["gemm2_bytes"] == d * f * 2 * E + N * f * 2 + N * d * 2
+    assert b["layer_bytes"] == 3 * d * f * 2 * E + T * d * 2 + T * d * 2 + T * E * 4
+    # GEMM1 at bf16_e64: 275 GFLOP and 738 MB, tensor-bound against 1768 TFLOP/s and 6486 GB/s
+    assert b["gemm1_flops"] / 1768.2e12 > b["gemm1_bytes"] / 6486.1e9
+    m = WORKLOADS["mxfp8_ep64_T8192"]
+    N, nonempty, tok = 1075, 4, 1000
+    d, f = m.d, m.f
+    b = bench.layer_bytes_flops(m, N, nonempty, tok)
+    wb = pb = 1 + 1 / 32
+    assert abs(b["gemm1_bytes"] - (2 * d * f * wb * nonempty + N * d * pb + N * f * pb)) < 1e-3
+    assert abs(b["layer_bytes"] - (3 * d * f * wb * nonempty + tok * d * 2 + m.T * d * 2 + m.T * m.E * 4)) < 1e-3
+    # the EP64 slice's GEMM1 is bound by its weight bytes
+    assert b["gemm1_flops"] / 3536.4e12 < b["gemm1_bytes"] / 6486.1e9
